@@ -1,0 +1,273 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, not against the oracle's own formula.
+
+Each test is chosen so that a plausible mistake in the oracle (dropped term,
+wrong sign or index, transposed operand, wrong mask side, missing GQA sum)
+fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import fa_workloads as W
+import oracle
+from oracle import numpy_oracle as npo
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed, s=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * s
+
+
+def qkv(B=2, N=13, Hq=4, Hkv=2, d=8, seed=0, s=1.0):
+    return rnd((B, N, Hq, d), seed, s), rnd((B, N, Hkv, d), seed + 1, s), rnd((B, N, Hkv, d), seed + 2, s)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_c_oracle_matches_numpy_oracle(causal):
+    q, k, v = qkv(B=2, N=37, Hq=4, Hkv=2, d=8, seed=3)
+    do = rnd(q.shape, 9)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.3)
+    o2, lse2 = npo.attn_fwd(q, k, v, causal, 0.3)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+    g = oracle.attn_bwd(q, k, v, do, causal, 0.3)
+    g2 = npo.attn_bwd(q, k, v, do, causal, 0.3)
+    for a, b in zip(g, g2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(causal):
+    # With V = [I_N | 0] the output's first N columns are P itself.
+    N, d = 9, 16
+    q = rnd((1, N, 1, d), 1)
+    k = rnd((1, N, 1, d), 2)
+    v = np.zeros((1, N, 1, d))
+    v[0, :, 0, :N] = np.eye(N)
+    o, _ = oracle.attn_fwd(q, k, v, causal, 0.7)
+    P = o[0, :, 0, :N]
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert (P >= 0).all()
+    np.testing.assert_allclose(o[0, :, 0, N:], 0.0, atol=0)
+    if causal:
+        assert np.all(P[np.triu_indices(N, 1)] == 0.0)
+        assert np.all(P[np.tril_indices(N)] > 0.0)
+    np.testing.assert_allclose(P, npo.attn_probs(q, k, causal, 0.7), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_constant_o(causal):
+    q, k, _ = qkv(seed=4)
+    c = rnd((1, 1, 2, 8), 5)
+    v = np.broadcast_to(c, (2, 13, 2, 8)).copy()
+    o, _ = oracle.attn_fwd(q, k, v, causal, 0.5)
+    for h in range(4):
+        np.testing.assert_allclose(o[:, :, h, :], np.broadcast_to(c[0, 0, h // 2], (2, 13, 8)),
+                                   rtol=0, atol=1e-12)
+
+
+def test_single_key_gives_o_equal_v():
+    q, k, v = qkv(N=1, seed=6)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, 0.25)
+        for h in range(4):
+            np.testing.assert_allclose(o[:, 0, h], v[:, 0, h // 2], rtol=0, atol=1e-14)
+            np.testing.assert_allclose(lse[:, h, 0],
+                                       0.25 * np.einsum("bc,bc->b", q[:, 0, h], k[:, 0, h // 2]),
+                                       rtol=0, atol=1e-13)
+
+
+def test_causal_first_row_is_first_value():
+    q, k, v = qkv(N=17, seed=7)
+    o, lse = oracle.attn_fwd(q, k, v, True, 0.5)
+    for h in range(4):
+        np.testing.assert_allclose(o[:, 0, h], v[:, 0, h // 2], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_is_mean_of_visible_values(causal):
+    N = 11
+    q, k, v = qkv(N=N, seed=8)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.0)
+    for h in range(4):
+        vh = v[:, :, h // 2]
+        if causal:
+            expect = np.cumsum(vh, axis=1) / np.arange(1, N + 1)[None, :, None]
+            lexp = np.log(np.arange(1, N + 1))[None, :]
+        else:
+            expect = np.broadcast_to(vh.mean(axis=1, keepdims=True), vh.shape)
+            lexp = np.full((1, N), math.log(N))
+        np.testing.assert_allclose(o[:, :, h], expect, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, h], np.broadcast_to(lexp, (2, N)), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("a,b", [(0.3, -1.7), (4.0, 2.5), (-6.0, 0.0)])
+def test_closed_form_two_keys(a, b):
+    # Q = [[a],[b]], K = [[1],[0]], V = [[1],[0]], scale 1: scores [q_i, 0],
+    # so O_i = sigmoid(q_i) and lse_i = ln(1 + e^{q_i}) without the mask;
+    # with it, row 0 sees key 0 only: O_0 = 1, lse_0 = a.
+    q = np.array([a, b]).reshape(1, 2, 1, 1)
+    k = np.array([1.0, 0.0]).reshape(1, 2, 1, 1)
+    v = np.array([1.0, 0.0]).reshape(1, 2, 1, 1)
+    sig = lambda x: 1.0 / (1.0 + math.exp(-x))
+    sp = lambda x: math.log1p(math.exp(x))
+    o, lse = oracle.attn_fwd(q, k, v, False, 1.0)
+    np.testing.assert_allclose(o.ravel(), [sig(a), sig(b)], rtol=1e-13)
+    np.testing.assert_allclose(lse.ravel(), [sp(a), sp(b)], rtol=1e-13)
+    o, lse = oracle.attn_fwd(q, k, v, True, 1.0)
+    np.testing.assert_allclose(o.ravel(), [1.0, sig(b)], rtol=1e-13)
+    np.testing.assert_allclose(lse.ravel(), [a, sp(b)], rtol=1e-13)
+
+
+def test_joint_key_value_permutation_invariance():
+    q, k, v = qkv(N=19, seed=10)
+    perm = np.random.default_rng(11).permutation(19)
+    o, lse = oracle.attn_fwd(q, k, v, False, 0.4)
+    o2, lse2 = oracle.attn_fwd(q, k[:, perm], v[:, perm], False, 0.4)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_common_key_offset_shifts_only_lse(causal):
+    # Adding one vector u to every key row adds scale*q_i.u to a whole row of
+    # scores: softmax is unchanged, lse_i moves by exactly that amount.
+    q, k, v = qkv(N=15, seed=12)
+    u = rnd((1, 1, 2, 8), 13)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.6)
+    o2, lse2 = oracle.attn_fwd(q, k + u, v, causal, 0.6)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    shift = np.stack([0.6 * np.einsum("bnc,c->bn", q[:, :, h], u[0, 0, h // 2]) for h in range(4)],
+                     axis=1)
+    np.testing.assert_allclose(lse2 - lse, shift, rtol=0, atol=1e-12)
+
+
+def test_two_block_merge_equals_full():
+    # The two-block update of the online softmax ("FlashAttention 1, 2, and 3
+    # Explained", section 2): l_new = e^{m1-m} l1 + e^{m2-m} l2 and
+    # O_new = diag(e^{m1-m}) O1 + (block-2 contribution), then normalised.
+    # Written here with lse = m + ln l of each half.
+    q, k, v = qkv(N=24, seed=14)
+    o, lse = oracle.attn_fwd(q, k, v, False, 0.5)
+    # query rows 0..11 against keys 0..11 and keys 12..23 separately
+    o1, l1 = oracle.attn_fwd(q[:, :12], k[:, :12], v[:, :12], False, 0.5)
+    o2, l2 = oracle.attn_fwd(q[:, :12], k[:, 12:], v[:, 12:], False, 0.5)
+    m = np.maximum(l1, l2)
+    a1, a2 = np.exp(l1 - m), np.exp(l2 - m)
+    lsum = a1 + a2
+    a1t = np.transpose(a1, (0, 2, 1))[..., None]
+    a2t = np.transpose(a2, (0, 2, 1))[..., None]
+    om = (a1t * o1 + a2t * o2) / np.transpose(lsum, (0, 2, 1))[..., None]
+    np.testing.assert_allclose(om, o[:, :12], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(m + np.log(lsum), lse[:, :, :12], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_mha_with_repeated_kv(causal):
+    B, N, Hq, Hkv, d = 2, 11, 6, 2, 5
+    q, k, v = qkv(B, N, Hq, Hkv, d, seed=15)
+    do = rnd(q.shape, 16)
+    g = Hq // Hkv
+    kr, vr = np.repeat(k, g, axis=2), np.repeat(v, g, axis=2)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.45)
+    o2, lse2 = oracle.attn_fwd(q, kr, vr, causal, 0.45)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-14)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.45)
+    dq2, dk2, dv2 = oracle.attn_bwd(q, kr, vr, do, causal, 0.45)
+    np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2.reshape(B, N, Hkv, g, d).sum(3), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv2.reshape(B, N, Hkv, g, d).sum(3), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_match_central_differences(causal):
+    B, N, Hq, Hkv, d = 1, 6, 2, 1, 3
+    q, k, v = qkv(B, N, Hq, Hkv, d, seed=17)
+    do = rnd(q.shape, 18)
+    scale = 0.8
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, scale)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attn_fwd(qq, kk, vv, causal, scale)
+        return float((o * do).sum())
+
+    h = 1e-6
+    base = {"q": q, "k": k, "v": v}
+    for name, g in (("q", dq), ("k", dk), ("v", dv)):
+        x = base[name]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            plus, minus = dict(base), dict(base)
+            plus[name], minus[name] = x.copy(), x.copy()
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            fd[idx] = (loss(plus["q"], plus["k"], plus["v"])
+                       - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_identities(causal):
+    B, N, Hq, Hkv, d = 2, 14, 4, 2, 6
+    q, k, v = qkv(B, N, Hq, Hkv, d, seed=19)
+    do = rnd(q.shape, 20)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.5)
+    # each row of dS sums to zero  =>  sum over keys of dK vanishes
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    # rows of P sum to one  =>  sum over keys of dV = sum over queries of dO (per group)
+    np.testing.assert_allclose(dv.sum(axis=1), do.reshape(B, N, Hkv, 2, d).sum(axis=(1, 3)),
+                               rtol=0, atol=1e-12)
+    # all keys equal  =>  dQ = scale * k * rowsum(dS) = 0
+    kc = np.broadcast_to(k[:, :1], k.shape).copy()
+    dq0, _, _ = oracle.attn_bwd(q, kc, v, do, causal, 0.5)
+    np.testing.assert_allclose(dq0, 0.0, atol=1e-13)
+
+
+def test_row_sampled_entry_points_match_full():
+    B, N, Hq, Hkv, d = 2, 21, 4, 2, 8
+    q, k, v = qkv(B, N, Hq, Hkv, d, seed=21)
+    do = rnd(q.shape, 22)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, 0.5)
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.5)
+        rows = np.array([[0, 0, 0], [1, 3, 20], [0, 2, 7], [1, 1, 13]])
+        orow, lrow = oracle.attn_fwd_rows(q, k, v, rows, causal, 0.5)
+        for r, (b, h, i) in enumerate(rows):
+            np.testing.assert_array_equal(orow[r], o[b, i, h])
+            assert lrow[r] == lse[b, h, i]
+        kvrows = np.array([[0, 0, 0], [1, 1, 20], [1, 0, 9]])
+        dqr, dkr, dvr = oracle.attn_bwd_rows(q, k, v, do, rows, kvrows, causal, 0.5)
+        for r, (b, h, i) in enumerate(rows):
+            np.testing.assert_allclose(dqr[r], dq[b, i, h], rtol=0, atol=1e-14)
+        for r, (b, h, j) in enumerate(kvrows):
+            np.testing.assert_allclose(dkr[r], dk[b, j, h], rtol=0, atol=1e-14)
+            np.testing.assert_allclose(dvr[r], dv[b, j, h], rtol=0, atol=1e-14)
+
+
+def test_bf16_inputs_are_taken_exactly():
+    import torch
+    w = W.WORKLOADS["tiny"].with_(N=5)
+    x = W.make_inputs(w)
+    o, lse = oracle.attn_fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+    o2, lse2 = npo.attn_fwd(x["q"].to(torch.float64).numpy(), x["k"].to(torch.float64).numpy(),
+                            x["v"].to(torch.float64).numpy(), w.causal, w.scale)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-13)
+
+
+def test_memory_wall_arithmetic_golden():
+    vals = {}
+    with open(os.path.join(GOLDEN, "memory_wall_n16384.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, val = line.split()
+                vals[key] = float(val)
+    N = int(vals["N"])
+    assert W.score_matrix_elements(N) == int(vals["elements"])
+    assert W.score_matrix_bytes(N, 2) == int(vals["bytes_per_head_2byte"])
+    assert math.floor(W.score_matrix_bytes(N, 2) / 1e5) / 10 == vals["page_megabytes"]
