@@ -1,0 +1,171 @@
+"""Python binding of libfa (include/fa.h): exact IO-aware attention on GB300.
+
+Argument marshalling only: every step of the forward and backward pass runs in
+libfa's CUDA kernels.  PyTorch supplies device memory and streams.  There is
+no fallback: if libfa.so is missing or the device is not an sm_103 GPU, calls
+raise.
+
+Layout [B, N, H, d] bf16 (contiguous); lse [B, Hq, N] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_DEVICE_TIMEOUT = 4
+
+# every entry point include/fa.h declares
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_error",
+           "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} {last_cuda_error()}".strip())
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libfa.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"libfa.so not found at {path}; build it with "
+                      "`python exact_io_aware_35_gb300/build.py`")
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_get_device_error.argtypes = [vp]
+    lib.fa_get_device_error.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_cuda_error.argtypes = []
+    lib.fa_last_cuda_error.restype = ctypes.c_char_p
+    lib.fa_debug_watchdog_probe.argtypes = [ctypes.c_uint64, vp]
+    lib.fa_debug_watchdog_probe.restype = i
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    return load_library().fa_status_string(int(s)).decode()
+
+
+def last_cuda_error() -> str:
+    return load_library().fa_last_cuda_error().decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, shape, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be [B, N, H, d]")
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    return B, N, Hq, Hkv, d
+
+
+def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
+           stream=None):
+    """Forward pass.  Returns (o, lse); o, lse are allocated if not given."""
+    lib = load_library()
+    B, N, Hq, Hkv, d = _dims(q, k)
+    _check(q, "q", (B, N, Hq, d))
+    _check(k, "k", (B, N, Hkv, d))
+    _check(v, "v", (B, N, Hkv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
+    _check(o, "o", (B, N, Hq, d))
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N))
+
+
+def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass.  Returns (dq, dk, dv); buffers are allocated if not given."""
+    lib = load_library()
+    B, N, Hq, Hkv, d = _dims(q, k)
+    _check(q, "q", (B, N, Hq, d))
+    _check(k, "k", (B, N, Hkv, d))
+    _check(v, "v", (B, N, Hkv, d))
+    _check(o, "o", (B, N, Hq, d))
+    _check(dout, "dout", (B, N, Hq, d))
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(dq, "dq", (B, N, Hq, d))
+    _check(dk, "dk", (B, N, Hkv, d))
+    _check(dv, "dv", (B, N, Hkv, d))
+    ws_bytes = fa_bwd_workspace_size(B, Hq, N)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError("workspace too small")
+    st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                    workspace.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                    _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_get_device_error(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device status."""
+    return int(load_library().fa_get_device_error(_stream_handle(stream)))
+
+
+def fa_debug_watchdog_probe(timeout_ns: int, stream=None) -> None:
+    st = load_library().fa_debug_watchdog_probe(int(timeout_ns), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_debug_watchdog_probe")

@@ -1,0 +1,260 @@
+// fa_api.cu -- the C ABI of libfa (declared in include/fa.h): argument
+// checks, TMA tensor maps, the device status word, and launches on the
+// caller's stream.  No device memory is allocated here.
+#include <stdio.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Status word written by bounded waits that run out (one per device: a
+// __device__ variable exists once per device context).
+__device__ uint32_t g_status_word;
+
+namespace {
+
+thread_local char t_last_error[256] = "";
+
+fa_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+             static_cast<int>(e));
+    return FA_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up: checks for an sm_103 device and fetches the device
+// address of the status word (no allocation).
+fa_status device_ready(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    DeviceInfo& di = g_dev[dev];
+    if (!di.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        di.supported = (major == 10 && minor == 3);
+        if (di.supported) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress(status)");
+            di.status = static_cast<uint32_t*>(p);
+        }
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e,
+                                 "cuTensorMapEncodeTiled entry point");
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        di.ready = true;
+    }
+    if (!di.supported) {
+        snprintf(t_last_error, sizeof(t_last_error), "device %d is not an sm_103 GPU", dev);
+        return FA_ERR_UNSUPPORTED;
+    }
+    *out = &di;
+    return FA_OK;
+}
+
+// Tensor map of a [B, N, H, d] bf16 tensor: dims (d, H, N, B), box
+// (64, 1, 128, 1), 128-byte swizzle; rows past N read as zero and are never
+// written.
+fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d) {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                             static_cast<cuuint64_t>(N) * H * d * 2};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_sizes(int B, int H, int Hkv, int N, int d, float scale) {
+    if (B < 1 || H < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    // every element offset and every TMA coordinate must fit in 32-bit ints
+    const long long qel = static_cast<long long>(B) * N * H * d;
+    if (qel >= (1LL << 40) || N > (1 << 30) || static_cast<long long>(B) * H * N >= (1LL << 31))
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+__global__ void watchdog_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(b, 0, status, timeout_ns, 0xFE);  // nothing ever arrives
+    __syncthreads();
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_last_cuda_error(void) { return t_last_error; }
+
+size_t fa_bwd_workspace_size(int B, int H, int N) {
+    if (B < 1 || H < 1 || N < 1) return 0;
+    const size_t bytes = 4ull * static_cast<size_t>(B) * H * N;
+    return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Hkv, int N, int d, int causal, float scale, void* stream) {
+    t_last_error[0] = 0;
+    fa_status st = check_sizes(B, H, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((st = device_ready(&di)) != FA_OK) return st;
+    FwdMaps maps;
+    if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
+    FwdArgs a;
+    a.lse = lse;
+    a.status = di->status;
+    a.B = B;
+    a.Hq = H;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.g = H / Hkv;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
+    a.timeout_ns = kWaitTimeoutNs;
+    cudaError_t e = launch_fwd(maps, a, d, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+    return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                 int Hkv, int N, int d, int causal, float scale, void* stream) {
+    t_last_error[0] = 0;
+    fa_status st = check_sizes(B, H, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !workspace ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((st = device_ready(&di)) != FA_OK) return st;
+    BwdMaps maps;
+    if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.dout, dout, B, N, H, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.dq, dq, B, N, H, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.dk, dk, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.dv, dv, B, N, Hkv, d)) != FA_OK) return st;
+    BwdArgs a;
+    a.lse = lse;
+    a.dsum = static_cast<float*>(workspace);
+    a.o = static_cast<const uint16_t*>(o);
+    a.dout = static_cast<const uint16_t*>(dout);
+    a.status = di->status;
+    a.B = B;
+    a.Hq = H;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.d = d;
+    a.g = H / Hkv;
+    a.causal = causal ? 1 : 0;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.timeout_ns = kWaitTimeoutNs;
+    cudaError_t e = launch_bwd(maps, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
+    return FA_OK;
+}
+
+fa_status fa_get_device_error(void* stream) {
+    t_last_error[0] = 0;
+    DeviceInfo* di = nullptr;
+    fa_status st = device_ready(&di);
+    if (st != FA_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word))) != cudaSuccess)
+        return cuda_fail(e, "read status word");
+    if (word != 0) {
+        const uint32_t zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess)
+            return cuda_fail(e, "clear status word");
+        snprintf(t_last_error, sizeof(t_last_error), "device status 0x%x (site %u)", word,
+                 word >> 8);
+        return (word & 0xFF) == kDevTimeout ? FA_ERR_DEVICE_TIMEOUT : FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+fa_status fa_debug_watchdog_probe(uint64_t timeout_ns, void* stream) {
+    t_last_error[0] = 0;
+    DeviceInfo* di = nullptr;
+    fa_status st = device_ready(&di);
+    if (st != FA_OK) return st;
+    if (timeout_ns < 1000ull) timeout_ns = 1000ull;
+    if (timeout_ns > 5000000000ull) timeout_ns = 5000000000ull;
+    watchdog_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "watchdog probe launch");
+    return FA_OK;
+}
+
+}  // extern "C"

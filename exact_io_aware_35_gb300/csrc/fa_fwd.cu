@@ -1,0 +1,402 @@
+// fa_fwd.cu -- exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes: O = softmax(scale * Q K^T [+ causal mask]) V and the
+// per-row log-sum-exp, one (batch, head, 256-query block) per thread block,
+// streaming 128-key blocks of K and V and folding each block into running
+// row statistics with the online-softmax update of "FlashAttention and the
+// Kernel Era", section "The Mathematics" (m_new = max(m, max S_j),
+// l_new = l * e^{m - m_new} + sum e^{S_j - m_new}) and the output update of
+// "FlashAttention 1, 2, and 3 Explained", section 2
+// (O_new = diag(e^{m_old - m_new}) O_old + P_j V_j).  The N x N score matrix
+// only ever exists one 128 x 128 tile at a time, in tensor memory.
+//
+// How it maps to sm_103a (a redesign for Blackwell, not the pages' A100/H100
+// kernels):
+//   * each CTA holds two 128-row query tiles (Q0, Q1) in shared memory and
+//     streams K_j, V_j through a ring of TMA-filled shared-memory slots;
+//   * one thread issues every tcgen05.mma: S_t = Q_t K_j^T into TMEM, then
+//     O_t += P_t V_j with P_t read straight from TMEM (bf16, written over S_t);
+//   * two softmax warpgroups, one per query tile, each thread owning one
+//     query row (one TMEM lane): load S, mask, row max, exp2, row sum, write P
+//     back to TMEM; while one warpgroup does its softmax the tensor core works
+//     on the other tile, which is the overlap of matmul and softmax that
+//     "FlashAttention and the Kernel Era" describes for FlashAttention-3;
+//   * exp2 with scale*log2(e) folded into one FMA; the running max is only
+//     moved (and O rescaled in TMEM) when the block max exceeds it by more
+//     than 2^8, which keeps l and O consistent with the same reference and is
+//     exact (only the headroom of fp32 changes);
+//   * causal: blocks above the diagonal are never loaded or multiplied;
+//     only the diagonal block is masked element by element;
+//   * the epilogue divides O by l, rounds to bf16, stages the tile in the
+//     (now free) Q buffer with the 128-byte swizzle and writes it with one TMA
+//     store; lse = (m + log2 l) * ln 2.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+    static constexpr int CHUNK = kBM * 128;          // one 64-column chunk of a 128-row tile
+    static constexpr int NCH = D / 64;               // chunks per tile
+    static constexpr int TILE = NCH * CHUNK;         // bytes of a 128 x D bf16 tile
+    static constexpr int NSLOT = (D == 128) ? 4 : 8; // K/V ring slots
+    static constexpr int SMEM_Q = 2 * TILE;
+    static constexpr int SMEM_KV = NSLOT * TILE;
+    // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
+    // o_final[2], mma_done
+    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16;
+    // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
+    static constexpr uint32_t TM_S = 0;
+    static constexpr uint32_t TM_O = 256;
+    static constexpr uint32_t TM_COLS = 512;
+    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, idle x2}
+};
+
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
+
+// Row-max and exp threshold for the lazy rescale: the reference max is only
+// moved when the new block maximum exceeds it by more than 2^8 (in log2
+// units), so unnormalised P values stay below 256.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdArgs a) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + C::SMEM_Q;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_KV);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR_Q = [&]() { return bar0; };
+    auto BAR_KVF = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto BAR_KVE = [&](int s) { return bar0 + 8u * (1 + C::NSLOT + s); };
+    auto BAR_SF = [&](int t) { return bar0 + 8u * (1 + 2 * C::NSLOT + t); };
+    auto BAR_PF = [&](int t) { return bar0 + 8u * (3 + 2 * C::NSLOT + t); };
+    auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * C::NSLOT + t); };
+    const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * C::NSLOT);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+
+    // ---- work decode: longest query blocks first, heads of one KV group adjacent
+    const int per = a.B * a.Hq;
+    const int qb = a.n_qblk - 1 - static_cast<int>(blockIdx.x) / per;
+    const int bh = static_cast<int>(blockIdx.x) % per;
+    const int b = bh / a.Hq;
+    const int h = bh % a.Hq;
+    const int hk = h / a.g;
+    const int row0 = qb * 2 * kBM;
+    const int nkv_all = (a.N + kBN - 1) / kBN;
+    // key blocks each query tile needs (causal: up to and including its diagonal)
+    const int nkv0 = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
+    const int nkv = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
+
+    // ---- set-up
+    if (warp == 0 && lane == 0) {
+        mbar_init(BAR_Q(), 1);
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(BAR_KVF(s), 1);
+            mbar_init(BAR_KVE(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR_SF(t), 1);
+            mbar_init(BAR_PF(t), 128);
+            mbar_init(BAR_OF(t), 1);
+        }
+        mbar_init(BAR_DONE, 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == kWarpLoad) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(&tmO);
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const uint64_t pol_q = l2_policy_evict_first();
+            mbar_arrive_expect_tx(BAR_Q(), 2 * C::TILE);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_4d_hint(sQ + t * C::TILE + c * C::CHUNK, &tmQ, BAR_Q(), c * 64, h,
+                                     row0 + t * kBM, b, pol_q);
+            int last_idx[C::NSLOT];
+            for (int s = 0; s < C::NSLOT; ++s) last_idx[s] = -1;
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; ++j) {
+                for (int w = 0; w < 2; ++w) {
+                    const int idx = 2 * j + w;
+                    const int slot = idx % C::NSLOT;
+                    const uint32_t ph = (idx / C::NSLOT) & 1;
+                    if (!mbar_wait(BAR_KVE(slot), ph ^ 1u, a.status, a.timeout_ns, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(BAR_KVF(slot), C::TILE);
+                    const CUtensorMap* tm = w ? &tmV : &tmK;
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d_hint(sKV + slot * C::TILE + c * C::CHUNK, tm, BAR_KVF(slot),
+                                         c * 64, hk, j * kBN, b, pol_kv);
+                    last_idx[slot] = idx;
+                }
+            }
+            // Never leave the CTA with copies in flight: wait (bounded) for the
+            // last load issued into every slot, and for Q.
+            mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 2);
+            for (int s = 0; s < C::NSLOT; ++s)
+                if (last_idx[s] >= 0)
+                    mbar_wait(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.status, a.timeout_ns, 2);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ================= MMA issuer (one thread) =================
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(kBM, D, false, true);
+            auto issue_qk = [&](int t, int slot) {
+                const uint32_t dS = tbase + C::TM_S + t * kBN;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+                    const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sKV + slot * C::TILE + off, 16, 1024);
+                    mma_bf16_ss(dS, ad, bd, IDESC_QK, ks > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int slot, bool acc) {
+                const uint32_t dO = tbase + C::TM_O + t * D;
+                const uint32_t aP = tbase + C::TM_S + t * kBN;  // P (bf16) over S_t
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    const uint64_t bd = sdesc_sw128(sKV + slot * C::TILE + ks * 2048, C::CHUNK, 1024);
+                    mma_bf16_ts(dO, aP + ks * 8, bd, IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 3);
+            if (ok) {
+                // first key block: both score tiles
+                ok = mbar_wait(BAR_KVF(0), 0, a.status, a.timeout_ns, 4);
+                if (ok) {
+                    tc_fence_after();
+                    issue_qk(0, 0);
+                    mma_commit(BAR_SF(0));
+                    issue_qk(1, 0);
+                    mma_commit(BAR_SF(1));
+                    mma_commit(BAR_KVE(0));
+                }
+            }
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vidx = 2 * j + 1;
+                const int vslot = vidx % C::NSLOT;
+                if (!(ok = mbar_wait(BAR_KVF(vslot), (vidx / C::NSLOT) & 1, a.status, a.timeout_ns, 5)))
+                    break;
+                tc_fence_after();
+                if (j < nkv0) {
+                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.status, a.timeout_ns, 6))) break;
+                    tc_fence_after();
+                    issue_pv(0, vslot, j > 0);
+                    if (j == nkv0 - 1) mma_commit(BAR_OF(0));
+                }
+                const int kidx = 2 * (j + 1);
+                const int kslot = kidx % C::NSLOT;
+                if (j + 1 < nkv) {
+                    if (!(ok = mbar_wait(BAR_KVF(kslot), (kidx / C::NSLOT) & 1, a.status,
+                                         a.timeout_ns, 7)))
+                        break;
+                    tc_fence_after();
+                    if (j + 1 < nkv0) {
+                        issue_qk(0, kslot);
+                        mma_commit(BAR_SF(0));
+                    }
+                }
+                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.status, a.timeout_ns, 8))) break;
+                tc_fence_after();
+                issue_pv(1, vslot, j > 0);
+                mma_commit(BAR_KVE(vslot));
+                if (j == nkv - 1) mma_commit(BAR_OF(1));
+                if (j + 1 < nkv) {
+                    issue_qk(1, kslot);
+                    mma_commit(BAR_SF(1));
+                    mma_commit(BAR_KVE(kslot));
+                }
+            }
+            // all issued MMAs have finished before TMEM can be released
+            mma_commit(BAR_DONE);
+            mbar_wait(BAR_DONE, 0, a.status, a.timeout_ns, 9);
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ================= softmax warpgroups (warps 0-3: tile 0, 4-7: tile 1)
+        const int t = warp >> 2;               // query tile of this warpgroup
+        const int wq = warp & 3;               // its warp owns TMEM lanes 32*wq..32*wq+31
+        const int r = wq * 32 + lane;          // row within the tile
+        const int grow = row0 + t * kBM + r;   // query index
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tbase + C::TM_S + t * kBN + lane_off;
+        const uint32_t tO = tbase + C::TM_O + t * D + lane_off;
+        const float sl2 = a.scale_log2;
+        // last key index this row may see
+        const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+        float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
+        float l = 0.f;            // running sum, relative to m_ref
+        bool ok = true;
+        const int nkv_mine = t ? nkv : nkv0;
+        for (int j = 0; j < nkv_mine; ++j) {
+            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.status, a.timeout_ns, 10 + t))) break;
+            tc_fence_after();
+            uint32_t s[kBN];
+            tmem_ld32(tS + 0, s);
+            tmem_ld32(tS + 32, s + 32);
+            tmem_ld32(tS + 64, s + 64);
+            tmem_ld32(tS + 96, s + 96);
+            tmem_wait_ld();
+            reg_fence<kBN>(s);
+            float x[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
+            const int kbase = j * kBN;
+            if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+            }
+            float mk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mk[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], x[c + i]);
+            const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                                   fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+            const float m_new = fmaxf(m_ref, mx * sl2);
+            const bool need = m_new > m_ref + kRescaleThreshold;
+            float alpha = 1.f;
+            if (need) {
+                alpha = ex2(m_ref - m_new);
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float ls[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const float p0 = ex2(fmaf(x[half * 64 + c], sl2, neg));
+                    const float p1 = ex2(fmaf(x[half * 64 + c + 1], sl2, neg));
+                    ls[(c >> 1) & 7] += p0 + p1;
+                    pk[c >> 1] = pack_bf16(p0, p1);
+                }
+                tmem_st32(tS + half * 32, pk);
+            }
+            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            // O_t was last written by the P V product of block j-1, which
+            // completed before this block's scores were committed.
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cb, o);
+                    tmem_wait_ld();
+                    reg_fence<32>(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + cb, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR_PF(t));
+        }
+        // ---- epilogue: O / l -> bf16 -> swizzled staging in Q_t's buffer -> TMA store
+        bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.status, a.timeout_ns, 12 + t);
+        const uint32_t stage = sQ + t * C::TILE;
+        if (ok_e) {
+            tc_fence_after();
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + cb, o);
+                tmem_wait_ld();
+                reg_fence<32>(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l,
+                                     __uint_as_float(o[2 * i + 1]) * inv_l);
+                const uint32_t rowbase = stage + (cb >> 6) * C::CHUNK + r * 128;
+#pragma unroll
+                for (int p4 = 0; p4 < 4; ++p4) {
+                    const int piece = ((cb & 63) >> 3) + p4;  // 16-byte piece within the row
+                    st_shared_v4(rowbase + ((piece ^ (r & 7)) << 4), w[4 * p4], w[4 * p4 + 1],
+                                 w[4 * p4 + 2], w[4 * p4 + 3]);
+                }
+            }
+            if (grow < a.N)
+                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                    (m_ref + log2f(l)) * 0.6931471805599453f;
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1 + t, 128);
+        if (ok_e && r == 0) {
+            for (int c = 0; c < C::NCH; ++c)
+                tma_store_4d(&tmO, stage + c * C::CHUNK, c * 64, h, row0 + t * kBM, b);
+            tma_store_commit();
+            tma_store_wait_read_all();
+        }
+    }
+
+    // ---- tear-down
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
+    using C = FwdCfg<D>;
+    auto kern = fa_fwd_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const long long nblk = static_cast<long long>(a.n_qblk) * a.B * a.Hq;
+    if (nblk <= 0 || nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(nblk), C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.o, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdArgs& args, int d, cudaStream_t stream) {
+    if (d == 64) return launch_fwd_d<64>(maps, args, stream);
+    if (d == 128) return launch_fwd_d<128>(maps, args, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,141 @@
+/*
+ * fa.h -- C ABI of libfa: exact, IO-aware tiled attention on one GB300
+ * (sm_103a).
+ *
+ * The operation is scaled dot-product attention with an optional causal mask,
+ *
+ *     O = softmax(scale * Q K^T [+ mask]) V,
+ *
+ * as defined on "FlashAttention and the Kernel Era", section "The
+ * Mathematics" (first equation), and on "FlashAttention 1, 2, and 3
+ * Explained", section 1 (the S, P, O equations).  The forward pass computes it
+ * block by block with the online-softmax rescaling of that page's section 2
+ * and of "The Mathematics" (running max m and running sum l), so the N x N
+ * score matrix never reaches HBM; only O and one float per query row (the
+ * log-sum-exp) are written.  The backward pass recomputes S and P from Q, K, V
+ * and that saved row statistic ("FlashAttention Kernel", the recomputation
+ * bullets; "FlashAttention", the recomputation paragraph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout is [B, N, H, d], row-major, contiguous (the flash_attn_func layout
+ *    on the "Flash Attention" page, section "Code Example"): element
+ *    (b, n, h, c) is at ((b*N + n)*H + h)*d + c.  Query-side tensors (q, o,
+ *    dout, dq) have H = Hq heads; key/value-side tensors (k, v, dk, dv) have
+ *    H = Hkv heads.  Tensors of the same call share B, N and d (Nq == Nk == N).
+ *  - Element type: bf16 (IEEE bfloat16) for q, k, v, o, dout, dq, dk, dv;
+ *    fp32 for lse and the backward workspace.  Outputs are rounded to nearest
+ *    even from fp32 accumulators.
+ *  - lse is [B, Hq, N] fp32: lse[b,h,i] = ln sum_j exp(scale * q_i . k_j) over
+ *    the keys j visible to query i (natural log of the *scaled* scores).
+ *  - GQA / MQA ("FlashAttention", the KV-cache bullets; "Flash Attention",
+ *    "Key Technical Innovations"): query head h reads key/value head
+ *    h / (Hq / Hkv); Hq must be a multiple of Hkv.  Hkv == Hq is plain
+ *    multi-head attention, Hkv == 1 is multi-query attention.
+ *  - causal != 0 masks key j from query i when j > i.  Since Nq == Nk the
+ *    top-left and bottom-right alignments coincide.
+ *  - d must be 64 or 128.  N >= 1 with no other restriction (ragged tails are
+ *    masked).  B, Hq, Hkv >= 1.
+ *  - All pointers are DEVICE pointers on the current CUDA device, 16-byte
+ *    aligned.  The caller owns every buffer; the library allocates no device
+ *    memory in these calls and keeps no pointer after a call returns.
+ *  - stream is a cudaStream_t (CUstream) handle, or NULL for the legacy
+ *    default stream.  Calls enqueue work on it and return without waiting.
+ *  - Errors: argument errors are detected on the host before any launch and
+ *    return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED with nothing enqueued.  A
+ *    launch failure returns FA_ERR_CUDA (see fa_last_cuda_error).  Every wait
+ *    inside the kernels is bounded; a wait that runs out records
+ *    FA_ERR_DEVICE_TIMEOUT in a library-owned device status word, the kernel
+ *    returns, and fa_get_device_error reports it.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, Hq % Hkv != 0 */
+    FA_ERR_UNSUPPORTED = 2,     /* d not in {64, 128}, or no sm_103 device */
+    FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded in-kernel wait ran out */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q   [B, N, Hq, d]  bf16 in
+ *   k   [B, N, Hkv, d] bf16 in
+ *   v   [B, N, Hkv, d] bf16 in
+ *   o   [B, N, Hq, d]  bf16 out: softmax(scale*QK^T [+mask]) V
+ *   lse [B, Hq, N]     fp32 out: per-row log-sum-exp of the scaled scores
+ *   H is the number of query heads (Hq).  scale is usually 1/sqrt(d).
+ * Tiled with online softmax as on "FlashAttention 1, 2, and 3 Explained",
+ * section 2 (the l and O update equations), parallel over (batch, head,
+ * query block) as on "FlashAttention Kernel" (the FlashAttention-2 bullets).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: one fp32 per query row and head
+ * (D_i = sum_c dO_ic * O_ic), i.e. 4 * B * H * N, rounded up to 256.
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N);
+
+/*
+ * Backward pass of the loss L with dL/dO = dout.
+ *   q, k, v, o, lse  as produced/consumed by fa_fwd (same B, H, Hkv, N, d,
+ *                    causal and scale)
+ *   dout [B, N, Hq, d]  bf16 in
+ *   dq   [B, N, Hq, d]  bf16 out
+ *   dk   [B, N, Hkv, d] bf16 out (summed over the Hq/Hkv query heads of a group)
+ *   dv   [B, N, Hkv, d] bf16 out (same)
+ *   workspace: device buffer of at least fa_bwd_workspace_size(B, H, N)
+ *              bytes, 256-byte aligned, owned by the caller; its contents on
+ *              entry do not matter and are overwritten.
+ * S and P are recomputed from q, k and lse ("FlashAttention Kernel",
+ * recomputation bullets).  Every output element is written by exactly one
+ * thread block; no atomics, so results are deterministic.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded wait ran
+ * out in some kernel since the last call) or FA_ERR_CUDA (the synchronise
+ * failed).
+ */
+fa_status fa_get_device_error(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Text of the last CUDA error seen by this thread inside the library
+ * (empty string if none).  Valid until the thread's next library call. */
+const char* fa_last_cuda_error(void);
+
+/*
+ * Test hook for the watchdog: launches one thread block whose thread waits on
+ * a shared-memory barrier that nothing ever signals, with the same bounded
+ * wait the attention kernels use, but a limit of `timeout_ns` nanoseconds
+ * (clamped to [1e3, 5e9]).  The wait runs out, the kernel records
+ * FA_ERR_DEVICE_TIMEOUT and returns; the GPU stays usable.  Enqueued on
+ * `stream`; read the result with fa_get_device_error.
+ */
+fa_status fa_debug_watchdog_probe(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
