@@ -24,8 +24,12 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_DEVICE_TIMEOUT = 4
 
+# fa_bwd_stage bits
+FA_BWD_DSUM, FA_BWD_DKDV, FA_BWD_DQ = 1, 2, 4
+
 # every entry point include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_error",
+EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size",
+           "fa_get_device_error",
            "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
 
 _lib = None
@@ -49,8 +53,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd.restype = i
-    lib.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_train.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_train.restype = i
+    lib.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, i, f, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_stage.argtypes = [i] + [vp] * 11 + [i, i, i, i, i, i, f, vp]
+    lib.fa_bwd_stage.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i]
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fa_get_device_error.argtypes = [vp]
@@ -101,8 +109,10 @@ def _dims(q, k):
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
-           stream=None):
-    """Forward pass.  Returns (o, lse); o, lse are allocated if not given."""
+           stream=None, o_lo=None):
+    """Forward pass.  Returns (o, lse); o, lse are allocated if not given.
+    With o_lo (a bf16 tensor shaped like q) this is the training forward
+    (fa_fwd_train): o_lo receives the low bf16 half of O for fa_bwd."""
     lib = load_library()
     B, N, Hq, Hkv, d = _dims(q, k)
     _check(q, "q", (B, N, Hq, d))
@@ -116,8 +126,14 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, ls
         lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
     _check(o, "o", (B, N, Hq, d))
     _check(lse, "lse", (B, Hq, N), torch.float32)
-    st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                    B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if o_lo is None:
+        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    else:
+        _check(o_lo, "o_lo", (B, N, Hq, d))
+        st = lib.fa_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              o_lo.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, d,
+                              int(bool(causal)), float(scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
     return o, lse
@@ -128,8 +144,11 @@ def fa_bwd_workspace_size(B: int, H: int, N: int) -> int:
 
 
 def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward pass.  Returns (dq, dk, dv); buffers are allocated if not given."""
+           dq=None, dk=None, dv=None, workspace=None, stream=None,
+           stages: int = FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, o_lo=None):
+    """Backward pass.  Returns (dq, dk, dv); buffers are allocated if not given.
+    `stages` selects a subset of the three kernels (fa_bwd_stage); o_lo is the
+    training forward's low half of O (None: D from o alone)."""
     lib = load_library()
     B, N, Hq, Hkv, d = _dims(q, k)
     _check(q, "q", (B, N, Hq, d))
@@ -151,10 +170,14 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
         workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
     if workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError("workspace too small")
-    st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                    workspace.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
-                    _stream_handle(stream))
+    if o_lo is not None:
+        _check(o_lo, "o_lo", (B, N, Hq, d))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            None if o_lo is None else o_lo.data_ptr(),
+            B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    all_stages = FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ
+    st = lib.fa_bwd(*args) if stages == all_stages else lib.fa_bwd_stage(int(stages), *args)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv

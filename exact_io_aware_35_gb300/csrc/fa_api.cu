@@ -153,11 +153,18 @@ size_t fa_bwd_workspace_size(int B, int H, int N) {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int Hkv, int N, int d, int causal, float scale, void* stream) {
+    return fa_fwd_train(q, k, v, o, nullptr, lse, B, H, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                       float* lse, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                       void* stream) {
     t_last_error[0] = 0;
     fa_status st = check_sizes(B, H, Hkv, N, d, scale);
     if (st != FA_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
+    if (o_lo && !aligned16(o_lo)) return FA_ERR_INVALID_ARG;
     DeviceInfo* di = nullptr;
     if ((st = device_ready(&di)) != FA_OK) return st;
     FwdMaps maps;
@@ -167,6 +174,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
     FwdArgs a;
     a.lse = lse;
+    a.o_lo = static_cast<uint16_t*>(o_lo);
     a.status = di->status;
     a.B = B;
     a.Hq = H;
@@ -183,15 +191,26 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
-                 int Hkv, int N, int d, int causal, float scale, void* stream) {
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 const void* o_lo, int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 void* stream) {
+    return fa_bwd_stage(FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, q, k, v, o, dout, lse, dq, dk, dv,
+                        workspace, o_lo, B, H, Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       void* workspace, const void* o_lo, int B, int H, int Hkv, int N, int d,
+                       int causal, float scale, void* stream) {
     t_last_error[0] = 0;
+    if (stages <= 0 || stages > 7) return FA_ERR_INVALID_ARG;
     fa_status st = check_sizes(B, H, Hkv, N, d, scale);
     if (st != FA_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
         !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !workspace ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FA_ERR_INVALID_ARG;
+    if (o_lo && !aligned16(o_lo)) return FA_ERR_INVALID_ARG;
     DeviceInfo* di = nullptr;
     if ((st = device_ready(&di)) != FA_OK) return st;
     BwdMaps maps;
@@ -207,6 +226,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.dsum = static_cast<float*>(workspace);
     a.o = static_cast<const uint16_t*>(o);
     a.dout = static_cast<const uint16_t*>(dout);
+    a.o_lo = static_cast<const uint16_t*>(o_lo);
     a.status = di->status;
     a.B = B;
     a.Hq = H;
@@ -218,7 +238,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.timeout_ns = kWaitTimeoutNs;
-    cudaError_t e = launch_bwd(maps, a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_bwd(maps, a, stages, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
     return FA_OK;
 }

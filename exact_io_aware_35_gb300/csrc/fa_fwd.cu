@@ -29,7 +29,8 @@
 //     only the diagonal block is masked element by element;
 //   * the epilogue divides O by l, rounds to bf16, stages the tile in the
 //     (now free) Q buffer with the 128-byte swizzle and writes it with one TMA
-//     store; lse = (m + log2 l) * ln 2.
+//     store; lse = (m + log2 l) * ln 2.  The training forward also writes
+//     o_lo = bf16(O32 - O), the rounding residual of O, with plain stores.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -342,11 +343,24 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld32(tO + cb, o);
                 tmem_wait_ld();
                 reg_fence<32>(o);
-                uint32_t w[16];
+                uint32_t w[16], wl[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l,
-                                     __uint_as_float(o[2 * i + 1]) * inv_l);
+                for (int i = 0; i < 16; ++i) {
+                    const float f0 = __uint_as_float(o[2 * i]) * inv_l;
+                    const float f1 = __uint_as_float(o[2 * i + 1]) * inv_l;
+                    w[i] = pack_bf16(f0, f1);
+                    // rounding residual for the training forward's o_lo
+                    wl[i] = pack_bf16(f0 - __uint_as_float(w[i] << 16),
+                                      f1 - __uint_as_float(w[i] & 0xFFFF0000u));
+                }
+                if (a.o_lo != nullptr && grow < a.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        a.o_lo + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * D + cb);
+#pragma unroll
+                    for (int p4 = 0; p4 < 4; ++p4)
+                        dst[p4] = make_uint4(wl[4 * p4], wl[4 * p4 + 1], wl[4 * p4 + 2],
+                                             wl[4 * p4 + 3]);
+                }
                 const uint32_t rowbase = stage + (cb >> 6) * C::CHUNK + r * 128;
 #pragma unroll
                 for (int p4 = 0; p4 < 4; ++p4) {

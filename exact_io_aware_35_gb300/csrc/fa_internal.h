@@ -19,6 +19,7 @@ constexpr int kBN = 128;
 
 struct FwdArgs {
     float* lse;          // [B, Hq, N]
+    uint16_t* o_lo;      // [B, N, Hq, d] bf16 low half of O, or null
     uint32_t* status;    // device status word
     int B, Hq, Hkv, N, g;
     int causal;
@@ -32,6 +33,7 @@ struct BwdArgs {
     float* dsum;         // [B, Hq, N] workspace: D_i = sum_c dO_ic O_ic
     const uint16_t* o;   // [B, N, Hq, d] bf16
     const uint16_t* dout;
+    const uint16_t* o_lo;  // optional low half of O (null: D from o alone)
     uint32_t* status;
     int B, Hq, Hkv, N, d, g;
     int causal;
@@ -50,6 +52,13 @@ struct BwdMaps {
 };
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdArgs& args, int d, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream);
+// The backward's kernels, one per file (d = 64 or 128).
+template <int D>
+cudaError_t launch_bwd_dkdv(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream);
+template <int D>
+cudaError_t launch_bwd_dq(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream);
+
+// stages: bit 0 dsum, bit 1 dK/dV, bit 2 dQ (run in that order)
+cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& args, int stages, cudaStream_t stream);
 
 }  // namespace fa

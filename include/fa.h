@@ -83,6 +83,20 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream);
 
 /*
+ * Forward pass for training: fa_fwd plus the low half of O.
+ *   o_lo [B, N, Hq, d] bf16 out: bf16(O32 - O), where O32 is the fp32 output
+ *        before rounding and O the bf16 value written to `o`.  o + o_lo carries
+ *        O to about 16 significant bits.
+ * fa_bwd forms D_i = sum_c dO_ic O_ic from o + o_lo when given it.  That
+ * matters when rows are peaked: there dS = P o (dP - D) is a near-cancellation
+ * and the rounding of O to bf16 alone moves dQ by more than the bf16
+ * rounding of the gradients themselves.  Same arguments and errors as fa_fwd.
+ */
+fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, void* o_lo,
+                       float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                       float scale, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: one fp32 per query row and head
  * (D_i = sum_c dO_ic * O_ic), i.e. 4 * B * H * N, rounded up to 256.
  * Returns 0 for invalid sizes.
@@ -93,6 +107,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N);
  * Backward pass of the loss L with dL/dO = dout.
  *   q, k, v, o, lse  as produced/consumed by fa_fwd (same B, H, Hkv, N, d,
  *                    causal and scale)
+ *   o_lo             the o_lo written by fa_fwd_train, or NULL (then D is
+ *                    formed from the bf16 o alone)
  *   dout [B, N, Hq, d]  bf16 in
  *   dq   [B, N, Hq, d]  bf16 out
  *   dk   [B, N, Hkv, d] bf16 out (summed over the Hq/Hkv query heads of a group)
@@ -106,8 +122,24 @@ size_t fa_bwd_workspace_size(int B, int H, int N);
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                 int B, int H, int Hkv, int N, int d, int causal, float scale,
-                 void* stream);
+                 const void* o_lo, int B, int H, int Hkv, int N, int d, int causal,
+                 float scale, void* stream);
+
+/*
+ * The three kernels of fa_bwd, callable one at a time (e.g. to time them).
+ * `stages` is a bitmask of FA_BWD_DSUM (D = rowsum(dout * o) into the
+ * workspace), FA_BWD_DKDV (dk, dv) and FA_BWD_DQ (dq); set stages run in that
+ * order.  DKDV and DQ read the D that a DSUM stage wrote into the same
+ * workspace earlier on the stream.  fa_bwd(...) is
+ * fa_bwd_stage(FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, ...).  Arguments,
+ * ownership and errors are those of fa_bwd; pointers a stage does not read
+ * or write must still be valid (they are checked, not dereferenced).
+ */
+enum { FA_BWD_DSUM = 1, FA_BWD_DKDV = 2, FA_BWD_DQ = 4 };
+fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       void* workspace, const void* o_lo, int B, int H, int Hkv, int N, int d,
+                       int causal, float scale, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+include/fa.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_io_aware_35_gb300 as fa
+    from exact_io_aware_35_gb300 import build as fa_build
+    fa_build.build()
+    return fa.load_library()
+
+
+def declared_entry_points():
+    with open(os.path.join(ROOT, "include", "fa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_error",
+              "fa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import exact_io_aware_35_gb300 as fa
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+    assert set(declared_entry_points()) <= set(fa.EXPORTS)
+
+
+def test_status_strings(lib):
+    import exact_io_aware_35_gb300 as fa
+    assert fa.status_string(0) == "FA_OK"
+    assert fa.status_string(4) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    assert lib.fa_bwd_workspace_size(2, 3, 5) == 256  # 120 bytes rounded up
+    assert lib.fa_bwd_workspace_size(4, 32, 8192) == 4 * 4 * 32 * 8192
+    assert lib.fa_bwd_workspace_size(0, 1, 1) == 0
+
+
+def _fwd(lib, ptr=16, B=1, H=1, Hkv=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.fa_fwd(ptr, ptr, ptr, ptr, ptr, B, H, Hkv, N, d, causal,
+                      ctypes.c_float(scale), None)
+
+
+def _bwd(lib, ptr=256, B=1, H=1, Hkv=1, N=128, d=64, scale=0.125, ws=256, o_lo=None):
+    return lib.fa_bwd(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ws, o_lo, B, H, Hkv, N, d,
+                      0, ctypes.c_float(scale), None)
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    import exact_io_aware_35_gb300 as fa
+    assert _fwd(lib, ptr=0) == fa.FA_ERR_INVALID_ARG          # null
+    assert _fwd(lib, ptr=8) == fa.FA_ERR_INVALID_ARG          # not 16-byte aligned
+    assert _fwd(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, H=6, Hkv=4) == fa.FA_ERR_INVALID_ARG     # Hq % Hkv != 0
+    assert _fwd(lib, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd(lib, ws=0) == fa.FA_ERR_INVALID_ARG
+    assert _bwd(lib, ws=272) == fa.FA_ERR_INVALID_ARG         # workspace not 256-aligned
+    assert _bwd(lib, o_lo=8) == fa.FA_ERR_INVALID_ARG         # o_lo misaligned
+    assert _bwd(lib, d=80) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_fwd_train(16, 16, 16, 16, 8, 16, 1, 1, 1, 128, 64, 0, ctypes.c_float(0.125),
+                            None) == fa.FA_ERR_INVALID_ARG
+    for stages in (0, 8, -1):
+        assert lib.fa_bwd_stage(stages, 256, 256, 256, 256, 256, 256, 256, 256, 256, 256, None,
+                                1, 1, 1, 128, 64, 0, ctypes.c_float(0.125),
+                                None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    import exact_io_aware_35_gb300 as fa
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q)

@@ -1,0 +1,138 @@
+"""GPU parity of fa_bwd (through the C ABI) against the float64 oracle.
+
+The backward's inputs O and lse come from the forward; every expected value
+comes from the oracle alone.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fa_workloads as W
+import oracle
+from tests.parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa(cuda_device):
+    import exact_io_aware_35_gb300 as fa
+    fa.load_library()
+    return fa
+
+
+def run_bwd(fa, x, causal, scale, train=True):
+    """Training pair: fa_fwd_train (o, o_lo, lse) then fa_bwd; train=False
+    uses the plain forward and no o_lo."""
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o_lo = torch.empty_like(q) if train else None
+    o, lse = fa.fa_fwd(q, k, v, causal=causal, scale=scale, o_lo=o_lo)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    ws = torch.full((fa.fa_bwd_workspace_size(q.shape[0], q.shape[2], q.shape[1]),), 255,
+                    dtype=torch.uint8, device=q.device)
+    fa.fa_bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+              o_lo=o_lo)
+    assert fa.fa_get_device_error() == fa.FA_OK
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+SHAPES = [
+    (1, 1, 1, 128, 64, False),
+    (1, 1, 1, 128, 128, True),
+    (1, 2, 1, 1, 64, True),
+    (1, 2, 2, 1, 128, False),
+    (2, 4, 2, 300, 64, True),
+    (2, 4, 2, 300, 64, False),
+    (1, 4, 1, 257, 128, False),
+    (1, 8, 2, 513, 128, True),
+    (2, 3, 3, 700, 64, False),
+    (1, 4, 4, 1024, 128, True),
+    (1, 16, 1, 640, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", SHAPES)
+def test_bwd_matches_oracle(fa, B, Hq, Hkv, N, d, causal):
+    w = W.Workload("t", B, Hq, Hkv, N, d, causal, 1.0 / math.sqrt(d), seed=200 + N + d)
+    x = W.make_inputs(w)
+    got = run_bwd(fa, x, causal, w.scale)
+    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], causal, w.scale)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g, r, name)
+
+
+def test_bwd_tiny_workload(fa):
+    w = W.WORKLOADS["tiny"]
+    x = W.make_inputs(w)
+    got = run_bwd(fa, x, w.causal, w.scale)
+    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], w.causal, w.scale)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g, r, name)
+
+
+def test_bwd_peaked_rows_small(fa):
+    # the peaked-row recipe (1% of K rows x8) at a size the oracle does in seconds
+    w = W.WORKLOADS["gqa32k_peaked"].with_(N=1024, Hq=8, Hkv=2)
+    x = W.make_inputs(w)
+    got = run_bwd(fa, x, True, w.scale)
+    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], True, w.scale)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g, r, name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_without_o_lo(fa, causal):
+    # the plain forward's bf16 O alone is enough on unpeaked inputs
+    w = W.Workload("t", 2, 4, 2, 384, 128, causal, 1 / math.sqrt(128), seed=31)
+    x = W.make_inputs(w)
+    got = run_bwd(fa, x, causal, w.scale, train=False)
+    ref = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], causal, w.scale)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert_close(g, r, name)
+
+
+def test_fwd_train_matches_fwd(fa):
+    # the training forward writes the same o and lse, and o + o_lo is the fp32
+    # output to ~16 bits (closer to the oracle than o alone)
+    w = W.Workload("t", 1, 4, 2, 300, 128, True, 1 / math.sqrt(128), seed=32)
+    x = W.make_inputs(w, with_dout=False)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o1, l1 = fa.fa_fwd(q, k, v, causal=True)
+    o_lo = torch.empty_like(q)
+    o2, l2 = fa.fa_fwd(q, k, v, causal=True, o_lo=o_lo)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o_ref, _ = oracle.attn_fwd(x["q"], x["k"], x["v"], True, w.scale)
+    hi = o1.cpu().double().numpy()
+    lo = o_lo.cpu().double().numpy()
+    assert np.abs(lo).max() <= np.abs(hi).max() * 2 ** -8
+    assert np.linalg.norm(hi + lo - o_ref) < 0.5 * np.linalg.norm(hi - o_ref)
+
+
+def test_bwd_stages_match_single_call(fa):
+    w = W.Workload("t", 1, 4, 2, 500, 128, True, 1 / math.sqrt(128), seed=33)
+    x = W.make_inputs(w)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o_lo = torch.empty_like(q)
+    o, lse = fa.fa_fwd(q, k, v, causal=True, o_lo=o_lo)
+    a = fa.fa_bwd(q, k, v, o, do, lse, causal=True, o_lo=o_lo)
+    ws = torch.empty(fa.fa_bwd_workspace_size(1, 4, 500), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for st in (fa.FA_BWD_DSUM, fa.FA_BWD_DKDV, fa.FA_BWD_DQ):
+        fa.fa_bwd(q, k, v, o, do, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws,
+                  stages=st, o_lo=o_lo)
+    assert fa.fa_get_device_error() == fa.FA_OK
+    for u, v_ in zip(a, (dq, dk, dv)):
+        assert torch.equal(u, v_)
+
+
+def test_bwd_deterministic(fa):
+    w = W.Workload("t", 1, 8, 2, 700, 128, True, 1 / math.sqrt(128), seed=9)
+    x = W.make_inputs(w)
+    a = run_bwd(fa, x, True, w.scale)
+    b = run_bwd(fa, x, True, w.scale)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
