@@ -1,0 +1,422 @@
+"""Benchmark of the exact-attention hot path (fa_fwd + fa_bwd) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the float64 CPU oracle, timed
+
+A step is one training forward plus one backward pass over one batch of the
+workload (default: B4 Hq32 Hkv8 N8192 d128 causal -- the N >= 8192, d = 128
+regime), inputs resident in HBM.  Timing: CUDA events on the launching stream
+around each kernel, L2 flushed (a 256 MiB write) before every step outside
+the timed events, the K timed steps bracketed by a barrier and a synchronize,
+max over ranks.  Prints one JSON line.
+
+Multi-GPU: the path shards into independent (batch, kv-head group) problems,
+so N ranks each run their own batch with no data-path collective ("weak"
+scaling); the only collective is the max of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import fa_workloads as W  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPS and % of GB300 BF16 tensor peak at N=2k–128k, d=64/128"
+DEFAULT_WORKLOAD = "gqa8k"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def rank_workload(base: W.Workload, rank: int) -> W.Workload:
+    """Rank r's share under weak scaling: the same workload shape, its own
+    batch (seed offset by 1000 * r)."""
+    return base.with_(seed=base.seed + 1000 * rank)
+
+
+def aggregate(step_ms_local: float, flops_per_rank: float, world_size: int, reduce_max=None):
+    """Whole-job throughput: the units all ranks processed divided by the
+    slowest rank's time.  reduce_max maps a local float to the max over ranks
+    (None for one process)."""
+    slowest = reduce_max(step_ms_local) if reduce_max else step_ms_local
+    return world_size * flops_per_rank / (slowest * 1e-3) / 1e12, slowest
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons (every 100 ms) and keeps
+    the samples whose timestamps fall inside the timed window."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+        self.window = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        from datetime import datetime
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]),
+                                 [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        use = inside if inside else rows
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted({n for r in use for n in r[3]}),
+                "samples": len(use), "window": "timed region" if inside else "whole run"}
+
+
+def oracle_sample(w: W.Workload, heads: int):
+    """A bounded, self-contained piece of the workload for the CPU oracle: one
+    batch element drawn with the workload's recipe, key/value head 0 and the
+    first `heads` query heads of its group, full sequence.  Returns (inputs,
+    nominal FLOPs, description)."""
+    heads = max(1, min(heads, w.Hq // w.Hkv))
+    x = W.make_inputs(w.with_(B=1))
+    sub = {"q": x["q"][:1, :, :heads].contiguous(), "k": x["k"][:1, :, :1].contiguous(),
+           "v": x["v"][:1, :, :1].contiguous(), "dout": x["dout"][:1, :, :heads].contiguous()}
+    sw = w.with_(B=1, Hq=heads, Hkv=1)
+    flops = W.fwd_flops(sw) + (W.bwd_flops(sw) if w.backward else 0.0)
+    step = W.fwd_flops(w) + (W.bwd_flops(w) if w.backward else 0.0)
+    desc = (f"one batch element, kv head 0 with {heads} query head(s), full N={w.N}, "
+            f"{'fwd+bwd' if w.backward else 'fwd'} ({flops / 1e9:.1f} nominal GFLOP, "
+            f"{flops / step:.4g} of a step)")
+    return sub, flops, desc
+
+
+def time_oracle_once(sub, w: W.Workload) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn_fwd(sub["q"], sub["k"], sub["v"], w.causal, w.scale)
+    if w.backward:
+        oracle.attn_bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.causal, w.scale)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = W.WORKLOADS[args.workload]
+    sub, flops, desc = oracle_sample(w, heads=1)
+    oracle.build()
+    for _ in range(args.warmup):
+        time_oracle_once(sub, w)
+    times = [time_oracle_once(sub, w) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "shape": W.describe(w), "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def tensor_bytes(*ts) -> int:
+    return sum(t.numel() * t.element_size() for t in ts)
+
+
+KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel")
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
+                  "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
+
+
+def kernel_work(w: W.Workload, name: str):
+    """(bound, algorithmic work per launch) of one kernel at workload w.
+    Tensor kernels: FLOPs of the GEMMs the kernel must do (2*N^2*d per head per
+    GEMM, halved under the causal mask): fwd 2 GEMMs, dK/dV 4, dQ 3.  dsum:
+    bytes of O, o_lo and dO read plus D written."""
+    g1 = W.fwd_flops(w) / 2.0  # one N x N x d GEMM over all heads
+    if name == "fa_fwd_kernel":
+        return "tensor", 2 * g1
+    if name == "fa_bwd_dkdv_kernel":
+        return "tensor", 4 * g1
+    if name == "fa_bwd_dq_kernel":
+        return "tensor", 3 * g1
+    return "hbm", 3 * w.B * w.N * w.Hq * w.d * 2 + 4 * w.B * w.Hq * w.N
+
+
+def source_hash(name: str) -> str:
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "exact_io_aware_35_gb300", "csrc")
+    for f in (KERNEL_SOURCES[name], "sm103_ptx.cuh", "fa_internal.h", "fa_bwd_common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[workload][name]
+        return e["dram_bytes_per_launch"] if e.get("source_hash") == source_hash(name) else None
+    except Exception:
+        return None
+
+
+def roofline(w: W.Workload, kern_ms: dict, peaks: dict):
+    name = max(kern_ms, key=kern_ms.get)  # dominant kernel by measured time
+    bound, work = kernel_work(w, name)
+    ms = kern_ms[name]
+    if bound == "tensor":
+        achieved = work / (ms * 1e-3) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = work / (ms * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    return {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": peaks["source"] + " burst",
+            "launch_ms": ms, "algorithmic_work_per_launch": work,
+            "traffic": measured_traffic(name, w.name)}
+
+
+def run_gpu(args):
+    import exact_io_aware_35_gb300 as fa
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    base = W.WORKLOADS[args.workload]
+    if args.batch:
+        base = base.with_(B=args.batch)
+    w = rank_workload(base, rank)
+    x = W.make_inputs(w, with_dout=w.backward)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    dvc = {n: t.to(dev) for n, t in host.items()}
+    q, k, v = dvc["q"], dvc["k"], dvc["v"]
+    do = dvc.get("dout")
+    o = torch.empty_like(q)
+    o_lo = torch.empty_like(q) if w.backward else None  # training forward
+    lse = torch.empty((w.B, w.Hq, w.N), device=dev, dtype=torch.float32)
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsb = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Hq, w.N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB of L2
+    nk = 1 + (3 if w.backward else 0)  # kernels per step
+
+    def fwd():
+        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, o_lo=o_lo)
+
+    def bwd(stages=fa.FA_BWD_DSUM | fa.FA_BWD_DKDV | fa.FA_BWD_DQ):
+        fa.fa_bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
+                  workspace=wsb, stages=stages, o_lo=o_lo)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        fwd()
+        if w.backward:
+            bwd()
+    st = fa.fa_get_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.status_string(st)} during warm-up")
+
+    # timed steps: events between the kernels (fwd | dsum | dK,dV | dQ) so each
+    # kernel's duration is measured on the stream it runs on
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        fwd()
+        ev[i][1].record()
+        if w.backward:
+            for n, stage in enumerate((fa.FA_BWD_DSUM, fa.FA_BWD_DKDV, fa.FA_BWD_DQ)):
+                bwd(stage)
+                ev[i][2 + n].record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    st = fa.fa_get_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.status_string(st)} in the timed region")
+    kern_ms = [sum(ev[i][n].elapsed_time(ev[i][n + 1]) for i in range(K)) / K for n in range(nk)]
+    fwd_ms = kern_ms[0]
+    bwd_ms = sum(kern_ms[1:])
+    step_ms = fwd_ms + bwd_ms
+
+    # ---- end to end through the public API, inputs from pinned host memory
+    outs = {"o": o, "lse": lse}
+    if w.backward:
+        outs.update({"dq": dq, "dk": dk, "dv": dv})
+    out_host = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in outs.items()}
+    h2d = tensor_bytes(*host.values())
+    d2h = tensor_bytes(*outs.values())
+
+    def e2e_step():
+        for n, t in host.items():
+            dvc[n].copy_(t, non_blocking=True)
+        fwd()
+        if w.backward:
+            bwd()
+        for n, t in outs.items():
+            out_host[n].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(t_timed0, time.time())
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    flops_step = W.fwd_flops(w) + (W.bwd_flops(w) if w.backward else 0.0)
+    t = torch.tensor([step_ms, e2e_ms] + kern_ms, dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    vals = [float(u) for u in t.tolist()]
+    step_ms, e2e_ms, kern_ms = vals[0], vals[1], vals[2:]
+    fwd_ms, bwd_ms = kern_ms[0], sum(kern_ms[1:])
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak = peaks["bf16_tflops"]
+    value, _ = aggregate(step_ms, flops_step, ws)
+    fwd_tf = W.fwd_flops(w) / (fwd_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, shape of the workload)",
+            "config": {"workload": args.workload, "shape": W.describe(w),
+                       "global_batch": w.B * ws, "seq_len": w.N,
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "frac_of_peak": value / ws / peak,
+            "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak, "fwd_ms": fwd_ms,
+            "peak_tflops": peak, "peak_source": peaks["source"] + " burst bf16",
+            "gpu_launches": nk * K}
+    if w.backward:
+        bwd_tf = W.bwd_flops(w) / (bwd_ms * 1e-3) / 1e12
+        line.update({"bwd_tflops": bwd_tf, "bwd_frac_of_peak": bwd_tf / peak, "bwd_ms": bwd_ms})
+    km = dict(zip(KERNELS[:nk], kern_ms))
+    line["kernel_ms"] = km
+    line["roofline"] = roofline(w, km, peaks)
+    line["e2e"] = {"value": aggregate(e2e_ms, flops_step, ws)[0], "unit": "TFLOPS",
+                   "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if clk is not None:
+        line["clocks"] = clk
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sub, sflops, desc = oracle_sample(base, heads=base.Hq // base.Hkv)
+        secs = time_oracle_once(sub, base)
+        line["cpu_baseline"] = {"value": sflops / secs / 1e12, "unit": "TFLOPS",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (profiling cases)")
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
