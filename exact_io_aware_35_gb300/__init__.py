@@ -28,7 +28,8 @@ FA_ERR_DEVICE_TIMEOUT = 4
 FA_BWD_DSUM, FA_BWD_DKDV, FA_BWD_DQ = 1, 2, 4
 
 # every entry point include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size",
+EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_noalloc",
+           "fa_bwd_workspace_size",
            "fa_get_device_error",
            "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
 
@@ -59,6 +60,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd.restype = i
     lib.fa_bwd_stage.argtypes = [i] + [vp] * 11 + [i, i, i, i, i, i, f, vp]
     lib.fa_bwd_stage.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i]
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fa_get_device_error.argtypes = [vp]

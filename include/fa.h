@@ -142,6 +142,30 @@ fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, 
                        int causal, float scale, void* stream);
 
 /*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory: a plug-in inside a host application that owns every device
+ * allocation, or a loop that must not call cudaMalloc mid-step.  (The pages
+ * have no counterpart; this is a library convenience.)
+ *   Arguments, outputs and errors are those of fa_bwd minus `workspace`.
+ *   D lives in a fixed array built into the library: 2^21 fp32 rows (8 MiB),
+ *   held on every GPU that loads the library until the process exits.  Calls
+ *   with B * H * N > 2^21 return FA_ERR_INVALID_ARG (with a message on
+ *   stderr) and enqueue nothing.
+ *   The first call on a device looks up the array's device address on that
+ *   device (current device, no allocation); make that first call before any
+ *   stream capture.
+ *   All calls share the one array, and it keeps the last call's contents:
+ *   calls whose work overlaps on the GPU (other streams, other threads) race
+ *   on it and must be serialised by the caller.  Nothing in it needs to start
+ *   at zero.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         const void* o_lo, int B, int H, int Hkv, int N, int d, int causal,
+                         float scale, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded wait ran
  * out in some kernel since the last call) or FA_ERR_CUDA (the synchronise
