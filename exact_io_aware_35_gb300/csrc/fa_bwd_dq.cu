@@ -7,15 +7,14 @@
 // describe for the backward pass: "FlashAttention Kernel", recomputation
 // bullet; the gradient formulas are the derivative of the forward definition).
 //
-// Pipelining: each 128-key block is split into two 64-key halves with their
-// own barriers.  Warpgroup 0 turns half a into dS while the tensor core
-// computes half b's scores and the previous half's dQ update, and vice
-// versa, so the elementwise work hides behind MMAs.  Q and dO are copied into
-// TMEM once and used as the A operand of the score MMAs, so those MMAs read
-// only K_j / V_j from shared memory.
+// Pipelining.  Every MMA is 128 wide (a tcgen05.mma of N = 64 cannot be issued
+// faster than ~46 cycles, a third more than its math takes; N = 128 runs at the
+// math rate).  S is double-buffered in TMEM, so S(j+2) is computed while the
+// two warpgroups turn block j+1 into dS (warpgroup h takes keys 64h..64h+63);
+// dQ += dS_h K_h is issued as soon as warpgroup h is done, then dP(j+2) into
+// the single dP buffer.  K and V stream through a 5-slot TMA ring.
 //
-// TMEM (512 columns): S [0,128) (half a: [0,64), half b: [64,128)),
-// dP [128,256), dQ [256,256+D), Q [384,384+D/2), dO [448,448+D/2).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), dP [256,384), dQ [384,384+D).
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -26,12 +25,12 @@ using namespace bwd;
 template <int D>
 struct DqCfg : Tiles<D> {
     using T = Tiles<D>;
-    static constexpr int NST = 2;  // K/V ring stages
-    static constexpr int OFF_KV = 2 * T::TILE;  // after Q, dO
-    static constexpr int OFF_BAR = OFF_KV + NST * 2 * T::TILE;
-    static constexpr int NBAR = 1 + 2 * NST + 1 + 2 + 2 + 1;
+    static constexpr int NSLOT = (D == 128) ? 5 : 8;  // K / V ring slots, one tile each
+    static constexpr int OFF_KV = 2 * T::TILE;          // after Q, dO
+    static constexpr int OFF_BAR = OFF_KV + NSLOT * T::TILE;
+    static constexpr int NBAR = 1 + 2 * NSLOT + 1 + 2 + 1;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_Q = 384, TM_DO = 448;
+    static constexpr uint32_t TM_S = 0, TM_DP = 256, TM_DQ = 384;
 };
 
 template <int D>
@@ -46,17 +45,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sDO = sQ + C::TILE;
-    const uint32_t sKV = sQ + C::OFF_KV;  // stage s: K at sKV + 2s*TILE, V after it
+    const uint32_t sKV = sQ + C::OFF_KV;  // slot t at sKV + t*TILE; K_j is tile 2j, V_j tile 2j+1
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t BAR_QDO = bar0;  // Q, dO tiles landed
-    auto BAR_KVF = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto BAR_KVE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
-    const uint32_t BAR_QT = bar0 + 8u * (1 + 2 * C::NST);          // Q, dO copied to TMEM
-    auto BAR_SF = [&](int hf) { return BAR_QT + 8u * (1 + hf); };  // half's S, dP ready
-    auto BAR_PF = [&](int hf) { return BAR_QT + 8u * (3 + hf); };  // half's dS written
-    const uint32_t BAR_ACC = BAR_QT + 8u * 5;
+    auto BAR_KVF = [&](int t) { return bar0 + 8u * (1 + t); };
+    auto BAR_KVE = [&](int t) { return bar0 + 8u * (1 + C::NSLOT + t); };
+    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NSLOT);       // block's S and dP ready
+    auto BAR_PF = [&](int hf) { return BAR_SDF + 8u * (1 + hf); };  // half's dS written
+    const uint32_t BAR_ACC = BAR_SDF + 8u * 3;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -72,15 +70,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_QDO, 1);
-        for (int s = 0; s < C::NST; ++s) {
-            mbar_init(BAR_KVF(s), 1);
-            mbar_init(BAR_KVE(s), 1);
+        for (int t = 0; t < C::NSLOT; ++t) {
+            mbar_init(BAR_KVF(t), 1);
+            mbar_init(BAR_KVE(t), 1);
         }
-        mbar_init(BAR_QT, 256);
-        for (int hf = 0; hf < 2; ++hf) {
-            mbar_init(BAR_SF(hf), 1);
-            mbar_init(BAR_PF(hf), 128);
-        }
+        mbar_init(BAR_SDF, 1);
+        for (int hf = 0; hf < 2; ++hf) mbar_init(BAR_PF(hf), 128);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
     }
@@ -106,87 +101,98 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sQ + c * C::CHUNK, &tmQ, BAR_QDO, c * 64, h, qi * kBM, b);
                 tma_load_4d(sDO + c * C::CHUNK, &tmDO, BAR_QDO, c * 64, h, qi * kBM, b);
             }
-            int last_j[C::NST] = {-1, -1};
-            for (int j = 0; j < nj; ++j) {
-                const int s = j % C::NST;
-                if (!mbar_wait(BAR_KVE(s), ((j / C::NST) & 1) ^ 1u, a.status, a.timeout_ns, 20))
+            int last_idx[C::NSLOT];
+            for (int t = 0; t < C::NSLOT; ++t) last_idx[t] = -1;
+            bool ok = true;
+            for (int idx = 0; idx < 2 * nj && ok; ++idx) {
+                const int t = idx % C::NSLOT;
+                if (!(ok = mbar_wait(BAR_KVE(t), ((idx / C::NSLOT) & 1) ^ 1u, a.status,
+                                     a.timeout_ns, 20)))
                     break;
-                mbar_arrive_expect_tx(BAR_KVF(s), 2 * C::TILE);
-                const uint32_t dst = sKV + 2 * s * C::TILE;
-                for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d_hint(dst + c * C::CHUNK, &tmK, BAR_KVF(s), c * 64, hk, j * kBN, b,
-                                     pol_kv);
-                    tma_load_4d_hint(dst + C::TILE + c * C::CHUNK, &tmV, BAR_KVF(s), c * 64, hk,
-                                     j * kBN, b, pol_kv);
-                }
-                last_j[s] = j;
+                mbar_arrive_expect_tx(BAR_KVF(t), C::TILE);
+                const CUtensorMap* tm = (idx & 1) ? &tmV : &tmK;
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_4d_hint(sKV + t * C::TILE + c * C::CHUNK, tm, BAR_KVF(t), c * 64, hk,
+                                     (idx >> 1) * kBN, b, pol_kv);
+                last_idx[t] = idx;
             }
-            // no copies in flight at exit: wait (bounded) for the last load of each stage
+            // no copies in flight at exit: wait (bounded) for the last load of each slot
             mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 21);
-            for (int s = 0; s < C::NST; ++s)
-                if (last_j[s] >= 0)
-                    mbar_wait(BAR_KVF(s), (last_j[s] / C::NST) & 1, a.status, a.timeout_ns, 21);
+            for (int t = 0; t < C::NSLOT; ++t)
+                if (last_idx[t] >= 0)
+                    mbar_wait(BAR_KVF(t), (last_idx[t] / C::NSLOT) & 1, a.status, a.timeout_ns, 21);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16(kBM, 64, false, false);  // S, dP halves
-            constexpr uint32_t IDESC_DQ = idesc_bf16(kBM, D, false, true);   // dQ += dS K
-            const uint32_t tS = tbase + C::TM_S, tDP = tbase + C::TM_DP, tDQ = tbase + C::TM_DQ;
-            const uint32_t tQ = tbase + C::TM_Q, tDO = tbase + C::TM_DO;
-            // scores of key half hf of the block in stage s: A = Q / dO from TMEM,
-            // B = rows 64*hf.. of K_j / V_j (K-major)
-            auto issue_s = [&](int hf, int s) {
-                const uint32_t sK = sKV + 2 * s * C::TILE, sV = sK + C::TILE;
+            constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);  // S, dP
+            constexpr uint32_t IDESC_DQ = idesc_bf16(kBM, D, false, true);     // dQ += dS K
+            const uint32_t tDP = tbase + C::TM_DP, tDQ = tbase + C::TM_DQ;
+            auto kslot = [&](int jj) { return (2 * jj) % C::NSLOT; };
+            auto vslot = [&](int jj) { return (2 * jj + 1) % C::NSLOT; };
+            auto ready = [&](int tile) {  // wait for ring tile `tile` (K_j = 2j, V_j = 2j+1)
+                const bool r = mbar_wait(BAR_KVF(tile % C::NSLOT), (tile / C::NSLOT) & 1,
+                                         a.status, a.timeout_ns, 23);
+                tc_fence_after();
+                return r;
+            };
+            // S(jj) = Q K_jj^T into S buffer jj & 1 (A = Q, B = K_jj, both K-major)
+            auto issue_s = [&](int jj) {
+                const uint32_t sK = sKV + kslot(jj) * C::TILE;
+                const uint32_t dS = tbase + C::TM_S + (jj & 1) * kBN;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32 + hf * C::HALF_ROWS;
-                    mma_bf16_ts(tS + hf * 64, tQ + ks * 8, sdesc_sw128(sK + off, 16, 1024), IDESC_S,
-                                ks > 0);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32 + hf * C::HALF_ROWS;
-                    mma_bf16_ts(tDP + hf * 64, tDO + ks * 8, sdesc_sw128(sV + off, 16, 1024),
+                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+                    mma_bf16_ss(dS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
                                 IDESC_S, ks > 0);
                 }
-                mma_commit(BAR_SF(hf));
             };
-            // dQ += dS_half K_half: dS (bf16) at columns [64*hf, 64*hf+32), K rows
-            // 64*hf.. read MN-major
-            auto issue_dq = [&](int hf, int s, bool first) {
-                const uint32_t sK = sKV + 2 * s * C::TILE;
+            // dP(jj) = dO V_jj^T into the dP buffer; the commit also covers S(jj)
+            auto issue_dp = [&](int jj) {
+                const uint32_t sV = sKV + vslot(jj) * C::TILE;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+                    mma_bf16_ss(tDP, sdesc_sw128(sDO + off, 16, 1024),
+                                sdesc_sw128(sV + off, 16, 1024), IDESC_S, ks > 0);
+                }
+                mma_commit(BAR_SDF);
+            };
+            // dQ += dS_h K_h: dS (bf16) of keys 64h.. at columns [64h, 64h+32) of S
+            // buffer jj & 1; K rows 64h.. read MN-major
+            auto issue_dq = [&](int jj, int hf) {
+                const uint32_t sK = sKV + kslot(jj) * C::TILE;
+                const uint32_t aS = tbase + C::TM_S + (jj & 1) * kBN + hf * 64;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tDQ, tS + hf * 64 + ks * 8,
+                    mma_bf16_ts(tDQ, aS + ks * 8,
                                 sdesc_sw128(sK + hf * C::HALF_ROWS + ks * 2048, C::CHUNK, 1024),
-                                IDESC_DQ, (first && ks == 0) ? 0u : 1u);
+                                IDESC_DQ, (jj == 0 && hf == 0 && ks == 0) ? 0u : 1u);
             };
-            bool ok = mbar_wait(BAR_QT, 0, a.status, a.timeout_ns, 22) &&
-                      mbar_wait(BAR_KVF(0), 0, a.status, a.timeout_ns, 23);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
-            }
+            bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && ready(0);
+            if (ok) issue_s(0);
+            if (ok && (ok = ready(1))) issue_dp(0);
+            if (ok && nj > 1 && (ok = ready(2))) issue_s(1);
             for (int j = 0; j < nj && ok; ++j) {
-                const int s = j % C::NST;
-                const int s2 = (j + 1) % C::NST;
                 if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.status, a.timeout_ns, 24))) break;
                 tc_fence_after();
-                issue_dq(0, s, j == 0);
-                if (j + 1 < nj) {
-                    if (!(ok = mbar_wait(BAR_KVF(s2), ((j + 1) / C::NST) & 1, a.status,
-                                         a.timeout_ns, 23)))
-                        break;
-                    tc_fence_after();
-                    issue_s(0, s2);
-                }
+                issue_dq(j, 0);
                 if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.status, a.timeout_ns, 24))) break;
                 tc_fence_after();
-                issue_dq(1, s, false);
-                mma_commit(BAR_KVE(s));
-                if (j + 1 < nj) issue_s(1, s2);
+                issue_dq(j, 1);
+                // K_j and V_j are free once these MMAs complete
+                mma_commit(BAR_KVE(kslot(j)));
+                mma_commit(BAR_KVE(vslot(j)));
+                // both warpgroups have read dP(j): the dP buffer may be overwritten
+                if (j + 1 < nj) {
+                    if (!(ok = ready(2 * (j + 1) + 1))) break;
+                    issue_dp(j + 1);
+                }
+                // S buffer j & 1 is read by dQ(j) above before S(j+2) lands in it
+                if (j + 2 < nj) {
+                    if (!(ok = ready(2 * (j + 2)))) break;
+                    issue_s(j + 2);
+                }
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
@@ -194,11 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < 8) {
-        const int hf = warp >> 2;  // key half of every block this warpgroup handles
+        const int hf = warp >> 2;  // keys 64*hf..64*hf+63 of every block
         const int r = (warp & 3) * 32 + lane;
         const int grow = qi * kBM + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + C::TM_S + lane_off + hf * 64;
         const uint32_t tDP = tbase + C::TM_DP + lane_off + hf * 64;
         const bool valid = grow < a.N;
         const size_t st_idx = (static_cast<size_t>(b) * a.Hq + h) * a.N + (valid ? grow : 0);
@@ -206,17 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float dval = valid ? a.dsum[st_idx] : 0.f;
         const float sl2 = a.scale_log2;
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
-        // Q (warpgroup 0) and dO (warpgroup 1) rows into TMEM as MMA A operands
-        bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 26);
-        if (ok) {
-            tile_row_to_tmem<D>(hf ? sDO : sQ, tbase + (hf ? C::TM_DO : C::TM_Q) + lane_off, r);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(BAR_QT);
+        bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
-            if (!(ok = mbar_wait(BAR_SF(hf), j & 1, a.status, a.timeout_ns, 26))) break;
+            if (!(ok = mbar_wait(BAR_SDF, j & 1, a.status, a.timeout_ns, 26))) break;
             tc_fence_after();
+            const uint32_t tS = tbase + C::TM_S + (j & 1) * kBN + lane_off + hf * 64;
             uint32_t sv[64], dp[64];
             tmem_ld32(tS, sv);
             tmem_ld32(tS + 32, sv + 32);
@@ -248,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok_e) {
             tc_fence_after();
             // dQ = scale * (dS K): each warpgroup stages half of the d columns into
-            // the Q tile's shared memory (Q now lives in TMEM)
+            // the Q tile's shared memory (no MMA reads Q any more)
             stage_rows_bf16<C::CHUNK>(tbase + C::TM_DQ + lane_off, sQ, r, hf * (D / 2),
                                       (hf + 1) * (D / 2), a.scale);
             fence_proxy_async_smem();
