@@ -248,28 +248,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qbase = qi * kBM + hf * 64;
             // causal: key r is hidden from query q when key > q
             const bool need_mask = a.causal && key > qbase;
+            const uint64_t sl2x2 = f2(sl2, sl2);
             uint32_t pk[32], dk[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
                 const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
                 const float4 d4 = *reinterpret_cast<const float4*>(dvec + c);
-                float p[4];
-                p[0] = ex2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-                p[1] = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-                p[2] = ex2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-                p[3] = ex2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+                // two columns per packed f32x2 FMA / ADD / MUL
+                float x[4], p[4], e[4];
+                f2_split(fma2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                              f2(-l4.x, -l4.y)), x[0], x[1]);
+                f2_split(fma2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
+                              f2(-l4.z, -l4.w)), x[2], x[3]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) p[u] = ex2(x[u]);
                 if (need_mask) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) p[u] = (key > qbase + c + u) ? 0.f : p[u];
                 }
-                const float ds0 = p[0] * (__uint_as_float(dp[c]) - d4.x);
-                const float ds1 = p[1] * (__uint_as_float(dp[c + 1]) - d4.y);
-                const float ds2 = p[2] * (__uint_as_float(dp[c + 2]) - d4.z);
-                const float ds3 = p[3] * (__uint_as_float(dp[c + 3]) - d4.w);
+                f2_split(mul2(f2(p[0], p[1]),
+                              add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                   f2(-d4.x, -d4.y))), e[0], e[1]);
+                f2_split(mul2(f2(p[2], p[3]),
+                              add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                                   f2(-d4.z, -d4.w))), e[2], e[3]);
                 pk[c >> 1] = pack_bf16(p[0], p[1]);
                 pk[(c >> 1) + 1] = pack_bf16(p[2], p[3]);
-                dk[c >> 1] = pack_bf16(ds0, ds1);
-                dk[(c >> 1) + 1] = pack_bf16(ds2, ds3);
+                dk[c >> 1] = pack_bf16(e[0], e[1]);
+                dk[(c >> 1) + 1] = pack_bf16(e[2], e[3]);
             }
             tmem_st32(tS, pk);   // P^T over this half's S^T columns
             tmem_st32(tDP, dk);  // dS^T over this half's dP^T columns

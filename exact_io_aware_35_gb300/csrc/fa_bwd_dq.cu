@@ -226,17 +226,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence<64>(dp);
             const int kbase = j * kBN + hf * 64;
             const bool need_mask = kbase + 63 > lim;
+            const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(nlse2, nlse2);
+            const uint64_t ndx2 = f2(-dval, -dval);
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
-                float p0 = ex2(fmaf(__uint_as_float(sv[c]), sl2, nlse2));
-                float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), sl2, nlse2));
+                // two columns per packed f32x2 FMA / ADD / MUL
+                float x0, x1;
+                f2_split(fma2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nlse2x2),
+                         x0, x1);
+                float p0 = ex2(x0), p1 = ex2(x1);
                 if (need_mask) {
                     p0 = (kbase + c > lim) ? 0.f : p0;
                     p1 = (kbase + c + 1 > lim) ? 0.f : p1;
                 }
-                pk[c >> 1] = pack_bf16(p0 * (__uint_as_float(dp[c]) - dval),
-                                       p1 * (__uint_as_float(dp[c + 1]) - dval));
+                const uint64_t t = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndx2);
+                float d0, d1;
+                f2_split(mul2(f2(p0, p1), t), d0, d1);
+                pk[c >> 1] = pack_bf16(d0, d1);
             }
             tmem_st32(tS, pk);  // dS over this half's S columns
             tmem_wait_st();

@@ -279,15 +279,16 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
             }
+            // row max: eight running maxima, three-input max instructions
             float mk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = x[i];
+            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
 #pragma unroll
-            for (int c = 8; c < kBN; c += 8)
+            for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], x[c + i]);
-            const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                                   fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
+            const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                                   fmaxf(mk[6], mk[7]));
             const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + kRescaleThreshold;
             float alpha = 1.f;
@@ -297,22 +298,27 @@ __global__ void __launch_bounds__(384, 1)
                 m_ref = m_new;
             }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float ls[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+            const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+            uint64_t ls2[4] = {0, 0, 0, 0};  // packed partial row sums
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    const float p0 = ex2(fmaf(x[half * 64 + c], sl2, neg));
-                    const float p1 = ex2(fmaf(x[half * 64 + c + 1], sl2, neg));
-                    ls[(c >> 1) & 7] += p0 + p1;
+                    float e0, e1;
+                    f2_split(fma2(f2(x[half * 64 + c], x[half * 64 + c + 1]), sl2x2, negx2), e0, e1);
+                    const float p0 = ex2(e0), p1 = ex2(e1);
+                    ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
                     pk[c >> 1] = pack_bf16(p0, p1);
                 }
                 tmem_st32(tS + half * 32, pk);
             }
-            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            {
+                const uint64_t t = add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3]));
+                float a0, a1;
+                f2_split(t, a0, a1);
+                l += a0 + a1;
+            }
             // O_t was last written by the P V product of block j-1, which
             // completed before this block's scores were committed.
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -322,8 +328,14 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_ld32(tO + cb, o);
                     tmem_wait_ld();
                     reg_fence<32>(o);
+                    const uint64_t ax2 = f2(alpha, alpha);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    for (int i = 0; i < 32; i += 2) {
+                        float u0, u1;
+                        f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2), u0, u1);
+                        o[i] = __float_as_uint(u0);
+                        o[i + 1] = __float_as_uint(u1);
+                    }
                     tmem_st32(tO + cb, o);
                 }
             }
