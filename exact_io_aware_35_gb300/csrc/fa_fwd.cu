@@ -53,11 +53,15 @@ struct FwdCfg {
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 256;
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, idle x2}
+    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, idle}
 };
 
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
+// The gate warp folds "K/V tiles landed" into the p_full barriers, so the MMA
+// thread waits on two barriers per key block instead of four: every mbarrier
+// wait in the issuing thread costs tensor-core time.
+constexpr int kWarpGate = 10;
 
 // Row-max and exp threshold for the lazy rescale: the reference max is only
 // moved when the new block maximum exceeds it by more than 2^8 (in log2
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(BAR_SF(t), 1);
-            mbar_init(BAR_PF(t), 128);
+            mbar_init(BAR_PF(t), 128 + 1);  // the tile's softmax threads and the gate
             mbar_init(BAR_OF(t), 1);
         }
         mbar_init(BAR_DONE, 1);
@@ -168,6 +172,29 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_wait(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.status, a.timeout_ns, 2);
         }
         __syncwarp();
+    } else if (warp == kWarpGate) {
+        // ================= gate: loads -> p_full =================
+        // For key block j it waits for V_j and K_{j+1}, then adds one arrival
+        // to p_full(t) for each tile t that multiplies block j, but only once
+        // that barrier's previous phase has completed, so the arrival can
+        // never be counted in the wrong phase.
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+                ok = mbar_wait(BAR_KVF(vidx % C::NSLOT), (vidx / C::NSLOT) & 1, a.status,
+                               a.timeout_ns, 5);
+                if (ok && j + 1 < nkv)
+                    ok = mbar_wait(BAR_KVF(kidx % C::NSLOT), (kidx / C::NSLOT) & 1, a.status,
+                                   a.timeout_ns, 5);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (t == 0 && j >= nkv0) continue;
+                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.status, a.timeout_ns, 7);
+                    if (ok) mbar_arrive(BAR_PF(t));
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == kWarpMma) {
         // ================= MMA issuer (one thread) =================
         if (lane == 0) {
@@ -205,12 +232,9 @@ __global__ void __launch_bounds__(384, 1)
                     mma_commit(BAR_KVE(0));
                 }
             }
+            // p_full(t) for key block j also means V_j and K_{j+1} have landed
             for (int j = 0; j < nkv && ok; ++j) {
-                const int vidx = 2 * j + 1;
-                const int vslot = vidx % C::NSLOT;
-                if (!(ok = mbar_wait(BAR_KVF(vslot), (vidx / C::NSLOT) & 1, a.status, a.timeout_ns, 5)))
-                    break;
-                tc_fence_after();
+                const int vslot = (2 * j + 1) % C::NSLOT;
                 if (j < nkv0) {
                     if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.status, a.timeout_ns, 6))) break;
                     tc_fence_after();
@@ -219,15 +243,9 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 const int kidx = 2 * (j + 1);
                 const int kslot = kidx % C::NSLOT;
-                if (j + 1 < nkv) {
-                    if (!(ok = mbar_wait(BAR_KVF(kslot), (kidx / C::NSLOT) & 1, a.status,
-                                         a.timeout_ns, 7)))
-                        break;
-                    tc_fence_after();
-                    if (j + 1 < nkv0) {
-                        issue_qk(0, kslot);
-                        mma_commit(BAR_SF(0));
-                    }
+                if (j + 1 < nkv0) {
+                    issue_qk(0, kslot);
+                    mma_commit(BAR_SF(0));
                 }
                 if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.status, a.timeout_ns, 8))) break;
                 tc_fence_after();
