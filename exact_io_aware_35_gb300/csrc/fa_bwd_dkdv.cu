@@ -11,12 +11,17 @@
 // transpose is ever materialised.  The group's query heads are summed inside
 // the CTA: no atomics.
 //
-// Pipelining: each 128-query block is split into two 64-query halves with
-// their own barriers; warpgroup hf computes half hf while the tensor core
-// works on the other half (the dV/dK update of one, the scores of the other).
+// Pipelining.  Every MMA is 128 wide: a tcgen05.mma with N = 64 costs its
+// issuing thread about as long as one with N = 128 and reads more shared
+// memory per flop.  Two 128-column TMEM regions X and Y swap roles every
+// block: S^T(i) and then P^T(i), dS^T(i) live in one, dP^T(i) in the other.
+// As soon as both warpgroups have copied dP^T(i) into registers, the tensor
+// core computes S^T(i+1) over it while they work; dV, dK += ... of block i
+// then read P^T(i) / dS^T(i) and dP^T(i+1) is written over them.  Warpgroup h
+// owns queries 64h..64h+63 of each block and writes its P^T and dS^T (bf16)
+// over the S^T columns it read.
 //
-// TMEM (512 columns): S^T [0,128) | dP^T [128,256) | dV [256,256+D) |
-// dK [256+D, 256+2D).
+// TMEM (512 columns): X [0,128) | Y [128,256) | dV [256,256+D) | dK [256+D, 256+2D).
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -33,9 +38,11 @@ struct DkdvCfg : Tiles<D> {
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
     static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
-    static constexpr int NBAR = 1 + 2 * NST + 2 + 2 + 1;
+    // barriers: K/V, stage full[NST], stage empty[NST], S^T+dP^T ready,
+    // dP^T copied to registers, P^T+dS^T written, all MMAs done
+    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256;
+    static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
 };
 
 template <int D>
@@ -60,10 +67,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t BAR_KV = bar0;
     auto BAR_STF = [&](int s) { return bar0 + 8u * (1 + s); };
     auto BAR_STE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
-    const uint32_t BAR_SF0 = bar0 + 8u * (1 + 2 * C::NST);
-    auto BAR_SF = [&](int hf) { return BAR_SF0 + 8u * hf; };        // half's S^T, dP^T ready
-    auto BAR_PF = [&](int hf) { return BAR_SF0 + 8u * (2 + hf); };  // half's P^T, dS^T written
-    const uint32_t BAR_ACC = BAR_SF0 + 8u * 4;
+    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // block's S^T, dP^T ready
+    const uint32_t BAR_LD = BAR_SDF + 8u;                   // dP^T copied to registers
+    const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T, dS^T written
+    const uint32_t BAR_ACC = BAR_SDF + 24u;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -83,10 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR_STF(s), 1 + 32);  // TMA transaction arrive + 32 lanes' vector writes
             mbar_init(BAR_STE(s), 1);
         }
-        for (int hf = 0; hf < 2; ++hf) {
-            mbar_init(BAR_SF(hf), 1);
-            mbar_init(BAR_PF(hf), 128);
-        }
+        mbar_init(BAR_SDF, 1);
+        mbar_init(BAR_LD, 256);
+        mbar_init(BAR_PF, 256);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
     }
@@ -120,6 +126,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it % C::NST;
             const int hq = hk * a.g + it / nqi;
             const int qi = qi0 + it % nqi;
+            // this block's lse2 / D, read from global memory before waiting for
+            // the stage so that their latency overlaps the wait
+            const size_t base = (static_cast<size_t>(b) * a.Hq + hq) * a.N;
+            float lv[4], dv4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = qi * kBM + lane * 4 + u;
+                // a query row past N contributes nothing: P = exp2(-inf) = 0
+                lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
+                dv4[u] = (q < a.N) ? a.dsum[base + q] : 0.f;
+            }
             if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.status, a.timeout_ns, 30)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
@@ -132,16 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             float* lse2 = vec + s * 2 * kBM;
-            float* dv = lse2 + kBM;
-            const size_t base = (static_cast<size_t>(b) * a.Hq + hq) * a.N;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = lane * 4 + u;
-                const int q = qi * kBM + c;
-                // a query row past N contributes nothing: P = exp2(-inf) = 0
-                lse2[c] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
-                dv[c] = (q < a.N) ? a.dsum[base + q] : 0.f;
-            }
+            *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+            *reinterpret_cast<float4*>(lse2 + kBM + lane * 4) =
+                make_float4(dv4[0], dv4[1], dv4[2], dv4[3]);
             mbar_arrive(BAR_STF(s));
             last_it[s] = it;
         }
@@ -154,39 +164,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16(kBN, 64, false, false);  // S^T, dP^T halves
+            constexpr uint32_t IDESC_S = idesc_bf16(kBN, kBM, false, false);  // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(kBN, D, false, true);  // dV, dK
-            const uint32_t tS = tbase + C::TM_S, tDP = tbase + C::TM_DP;
             const uint32_t tDV = tbase + C::TM_ACC, tDK = tbase + C::TM_ACC + D;
-            // S^T, dP^T for query half hf of stage s: B = rows 64*hf.. of Q_i / dO_i
-            auto issue_s = [&](int hf, int s) {
-                const uint32_t sQ = sStage + 2 * s * C::TILE, sDO = sQ + C::TILE;
+            // region of S^T(it) (then P^T, dS^T), and of dP^T(it)
+            auto reg_s = [&](int it) { return tbase + ((it & 1) ? C::TM_Y : C::TM_X); };
+            auto reg_d = [&](int it) { return tbase + ((it & 1) ? C::TM_X : C::TM_Y); };
+            auto stage_q = [&](int s) { return sStage + 2 * s * C::TILE; };
+            // dst = A B^T over the head dimension: S^T = K Q^T or dP^T = V dO^T
+            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(tS + hf * 64, sdesc_sw128(sK + off, 16, 1024),
-                                sdesc_sw128(sQ + off + hf * C::HALF_ROWS, 16, 1024), IDESC_S, ks > 0);
+                    mma_bf16_ss(dst, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
+                                IDESC_S, ks > 0);
                 }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(tDP + hf * 64, sdesc_sw128(sV + off, 16, 1024),
-                                sdesc_sw128(sDO + off + hf * C::HALF_ROWS, 16, 1024), IDESC_S,
-                                ks > 0);
-                }
-                mma_commit(BAR_SF(hf));
             };
-            // dV += P^T_h dO_h, dK += dS^T_h Q_h: P^T / dS^T (bf16) at columns
-            // [64*hf, 64*hf+32) of S^T / dP^T; dO, Q rows 64*hf.. read MN-major
-            auto issue_acc = [&](int hf, int s, bool first) {
-                const uint32_t sQ = sStage + 2 * s * C::TILE, sDO = sQ + C::TILE;
+            // dV += P^T dO, dK += dS^T Q: for queries 16ks.., P^T / dS^T (bf16) sit in
+            // columns 64h + (ks%4)*8 / 64h + 32 + (ks%4)*8 of S^T's region (h = ks/4);
+            // dO, Q rows 16ks.. are read MN-major
+            auto issue_acc = [&](int it, int s) {
+                const uint32_t sQ = stage_q(s), sDO = sQ + C::TILE, rs = reg_s(it);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t acc = (first && ks == 0) ? 0u : 1u;
-                    const uint32_t boff = hf * C::HALF_ROWS + ks * 2048;
-                    mma_bf16_ts(tDV, tS + hf * 64 + ks * 8, sdesc_sw128(sDO + boff, C::CHUNK, 1024),
+                for (int ks = 0; ks < kBM / 16; ++ks) {
+                    const uint32_t acc = (it == 0 && ks == 0) ? 0u : 1u;
+                    const uint32_t aoff = (ks >> 2) * 64 + (ks & 3) * 8;
+                    mma_bf16_ts(tDV, rs + aoff, sdesc_sw128(sDO + ks * 2048, C::CHUNK, 1024),
                                 IDESC_ACC, acc);
-                    mma_bf16_ts(tDK, tDP + hf * 64 + ks * 8, sdesc_sw128(sQ + boff, C::CHUNK, 1024),
+                    mma_bf16_ts(tDK, rs + aoff + 32, sdesc_sw128(sQ + ks * 2048, C::CHUNK, 1024),
                                 IDESC_ACC, acc);
                 }
             };
@@ -194,27 +199,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                       mbar_wait(BAR_STF(0), 0, a.status, a.timeout_ns, 33);
             if (ok) {
                 tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
+                issue_t(reg_s(0), sK, stage_q(0));
+                issue_t(reg_d(0), sV, stage_q(0) + C::TILE);
+                mma_commit(BAR_SDF);
             }
             for (int it = 0; it < n_it && ok; ++it) {
                 const int s = it % C::NST;
                 const int s2 = (it + 1) % C::NST;
-                if (!(ok = mbar_wait(BAR_PF(0), it & 1, a.status, a.timeout_ns, 34))) break;
-                tc_fence_after();
-                issue_acc(0, s, it == 0);
-                if (it + 1 < n_it) {
+                const bool more = it + 1 < n_it;
+                if (more) {
+                    // S^T(it+1) over dP^T(it), once both warpgroups hold it in registers
                     if (!(ok = mbar_wait(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.status,
                                          a.timeout_ns, 33)))
                         break;
+                    if (!(ok = mbar_wait(BAR_LD, it & 1, a.status, a.timeout_ns, 34))) break;
                     tc_fence_after();
-                    issue_s(0, s2);
+                    issue_t(reg_d(it), sK, stage_q(s2));
                 }
-                if (!(ok = mbar_wait(BAR_PF(1), it & 1, a.status, a.timeout_ns, 34))) break;
+                if (!(ok = mbar_wait(BAR_PF, it & 1, a.status, a.timeout_ns, 34))) break;
                 tc_fence_after();
-                issue_acc(1, s, false);
+                issue_acc(it, s);
                 mma_commit(BAR_STE(s));
-                if (it + 1 < n_it) issue_s(1, s2);
+                if (more) {
+                    // dP^T(it+1) over P^T(it), dS^T(it): the products above read them first
+                    issue_t(reg_s(it), sV, stage_q(s2) + C::TILE);
+                    mma_commit(BAR_SDF);
+                }
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
@@ -222,66 +232,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < 8) {
-        const int hf = warp >> 2;  // query half (0: queries 0-63, 1: 64-127) of each block
+        const int hf = warp >> 2;  // queries 64*hf..64*hf+63 of each block
         const int r = (warp & 3) * 32 + lane;
-        const int key = jb * kBN + r;
+        const int t4 = lane & 3;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + C::TM_S + lane_off + hf * 64;
-        const uint32_t tDP = tbase + C::TM_DP + lane_off + hf * 64;
+        // In the 16x256b TMEM shape a thread holds, of each 16-lane block of its
+        // warp's 32 lanes, rows lane/4 and lane/4 + 8 and the 16 columns
+        // 8j + 2(lane%4) + {0,1} of the warpgroup's 64: so it needs only 16
+        // entries of the query-indexed vectors lse2 and D.
+        const int key0 = jb * kBN + (warp & 3) * 32 + (lane >> 2);
         const float sl2 = a.scale_log2;
+        const uint64_t sl2x2 = f2(sl2, sl2);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::NST;
             const int qi = qi0 + it % nqi;
-            if (!(ok = mbar_wait(BAR_SF(hf), it & 1, a.status, a.timeout_ns, 36))) break;
+            if (!(ok = mbar_wait(BAR_SDF, it & 1, a.status, a.timeout_ns, 36))) break;
             tc_fence_after();
-            uint32_t sv[64], dp[64];
-            tmem_ld32(tS, sv);
-            tmem_ld32(tS + 32, sv + 32);
-            tmem_ld32(tDP, dp);
-            tmem_ld32(tDP + 32, dp + 32);
-            tmem_wait_ld();
-            reg_fence<64>(sv);
-            reg_fence<64>(dp);
+            const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + hf * 64 + lane_off;
+            const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + hf * 64 + lane_off;
+            // dP^T first: once both warpgroups hold it, S^T(it+1) may overwrite it
+            uint32_t dp[2][32];
+            tmem_ld16x256_x8(rd, dp[0]);
+            tmem_ld16x256_x8(rd + (16u << 16), dp[1]);
             const float* lse2 = vec + s * 2 * kBM + hf * 64;
             const float* dvec = vec + s * 2 * kBM + kBM + hf * 64;
-            const int qbase = qi * kBM + hf * 64;
-            // causal: key r is hidden from query q when key > q
-            const bool need_mask = a.causal && key > qbase;
-            const uint64_t sl2x2 = f2(sl2, sl2);
-            uint32_t pk[32], dk[32];
+            uint64_t nl[8], nd[8];  // (-lse2, -D) of the thread's column pairs
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-                const float4 d4 = *reinterpret_cast<const float4*>(dvec + c);
-                // two columns per packed f32x2 FMA / ADD / MUL
-                float x[4], p[4], e[4];
-                f2_split(fma2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
-                              f2(-l4.x, -l4.y)), x[0], x[1]);
-                f2_split(fma2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
-                              f2(-l4.z, -l4.w)), x[2], x[3]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) p[u] = ex2(x[u]);
-                if (need_mask) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) p[u] = (key > qbase + c + u) ? 0.f : p[u];
-                }
-                f2_split(mul2(f2(p[0], p[1]),
-                              add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                   f2(-d4.x, -d4.y))), e[0], e[1]);
-                f2_split(mul2(f2(p[2], p[3]),
-                              add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
-                                   f2(-d4.z, -d4.w))), e[2], e[3]);
-                pk[c >> 1] = pack_bf16(p[0], p[1]);
-                pk[(c >> 1) + 1] = pack_bf16(p[2], p[3]);
-                dk[c >> 1] = pack_bf16(e[0], e[1]);
-                dk[(c >> 1) + 1] = pack_bf16(e[2], e[3]);
+            for (int j = 0; j < 8; ++j) {
+                const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
+                const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
+                nl[j] = f2(-l2.x, -l2.y);
+                nd[j] = f2(-d2.x, -d2.y);
             }
-            tmem_st32(tS, pk);   // P^T over this half's S^T columns
-            tmem_st32(tDP, dk);  // dS^T over this half's dP^T columns
+            tmem_wait_ld();
+            reg_fence<32>(dp[0]);
+            reg_fence<32>(dp[1]);
+            tc_fence_before();
+            mbar_arrive(BAR_LD);
+            const int qbase = qi * kBM + hf * 64 + 2 * t4;  // query of the thread's column 0
+#pragma unroll
+            for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
+                const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
+                uint32_t sv[32];
+                tmem_ld16x256_x8(rs + lo, sv);
+                tmem_wait_ld();
+                reg_fence<32>(sv);
+                const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
+                // causal: key k is hidden from query q when k > q
+                const bool need_mask = a.causal && key + 8 > qbase;
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                    for (int rsel = 0; rsel < 2; ++rsel) {
+                        const int i = 4 * j + 2 * rsel;
+                        float x0, x1;
+                        f2_split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2,
+                                      nl[j]), x0, x1);
+                        float p0 = ex2(x0), p1 = ex2(x1);
+                        if (need_mask) {
+                            const int q = qbase + 8 * j, k = key + 8 * rsel;
+                            p0 = (k > q) ? 0.f : p0;
+                            p1 = (k > q + 1) ? 0.f : p1;
+                        }
+                        float e0, e1;
+                        f2_split(mul2(f2(p0, p1),
+                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
+                                           nd[j])), e0, e1);
+                        pk[2 * j + rsel] = pack_bf16(p0, p1);
+                        dk[2 * j + rsel] = pack_bf16(e0, e1);
+                    }
+                }
+                tmem_st16x128_x8(rs + lo, pk);       // P^T over the first 32 S^T columns read
+                tmem_st16x128_x8(rs + lo + 32, dk);  // dS^T over the other 32
+            }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR_PF(hf));
+            mbar_arrive(BAR_PF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 37);
         // warpgroup 0 writes dV, warpgroup 1 writes dK = scale * (dS^T Q); staging
