@@ -29,6 +29,15 @@ namespace {
 
 using namespace bwd;
 
+// Warp roles: warps 0-15 are four compute warpgroups (warpgroup w takes
+// queries 32w..32w+31 of every block: four warps per SM sub-partition keep the
+// exp2 and FMA pipes busy through each other's latencies), warp 16 issues the
+// MMAs, warp 17 loads.
+constexpr int kDkWarpMma = 16;
+constexpr int kDkWarpLoad = 17;
+constexpr int kDkThreads = 18 * 32;
+constexpr int kDkCompute = 512;  // compute threads
+
 template <int D>
 struct DkdvCfg : Tiles<D> {
     using T = Tiles<D>;
@@ -46,7 +55,7 @@ struct DkdvCfg : Tiles<D> {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDkThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -91,12 +100,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR_STE(s), 1);
         }
         mbar_init(BAR_SDF, 1);
-        mbar_init(BAR_LD, 256);
-        mbar_init(BAR_PF, 256);
+        mbar_init(BAR_LD, kDkCompute);
+        mbar_init(BAR_PF, kDkCompute);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == kDkWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -105,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == kWarpLoad) {
+    if (warp == kDkWarpLoad) {
         // TMA for tiles (lane 0); all 32 lanes fill the per-query lse2 / D vectors
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(BAR_STF(s), (last_it[s] / C::NST) & 1, a.status, a.timeout_ns, 31);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+    } else if (warp == kDkWarpMma) {
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(kBN, kBM, false, false);  // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_bf16(kBN, D, false, true);  // dV, dK
@@ -181,17 +190,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             // dV += P^T dO, dK += dS^T Q: for queries 16ks.., P^T / dS^T (bf16) sit in
-            // columns 64h + (ks%4)*8 / 64h + 32 + (ks%4)*8 of S^T's region (h = ks/4);
+            // columns 32w + (ks%2)*8 / 32w + 16 + (ks%2)*8 of S^T's region (w = ks/2);
             // dO, Q rows 16ks.. are read MN-major
             auto issue_acc = [&](int it, int s) {
                 const uint32_t sQ = stage_q(s), sDO = sQ + C::TILE, rs = reg_s(it);
 #pragma unroll
                 for (int ks = 0; ks < kBM / 16; ++ks) {
                     const uint32_t acc = (it == 0 && ks == 0) ? 0u : 1u;
-                    const uint32_t aoff = (ks >> 2) * 64 + (ks & 3) * 8;
+                    const uint32_t aoff = (ks >> 1) * 32 + (ks & 1) * 8;
                     mma_bf16_ts(tDV, rs + aoff, sdesc_sw128(sDO + ks * 2048, C::CHUNK, 1024),
                                 IDESC_ACC, acc);
-                    mma_bf16_ts(tDK, rs + aoff + 32, sdesc_sw128(sQ + ks * 2048, C::CHUNK, 1024),
+                    mma_bf16_ts(tDK, rs + aoff + 16, sdesc_sw128(sQ + ks * 2048, C::CHUNK, 1024),
                                 IDESC_ACC, acc);
                 }
             };
@@ -231,14 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 35);
         }
         __syncwarp();
-    } else if (warp < 8) {
-        const int hf = warp >> 2;  // queries 64*hf..64*hf+63 of each block
+    } else if (warp < 16) {
+        const int wg = warp >> 2;  // queries 32*wg..32*wg+31 of each block
         const int r = (warp & 3) * 32 + lane;
         const int t4 = lane & 3;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         // In the 16x256b TMEM shape a thread holds, of each 16-lane block of its
-        // warp's 32 lanes, rows lane/4 and lane/4 + 8 and the 16 columns
-        // 8j + 2(lane%4) + {0,1} of the warpgroup's 64: so it needs only 16
+        // warp's 32 lanes, rows lane/4 and lane/4 + 8 and the 8 columns
+        // 8j + 2(lane%4) + {0,1} of the warpgroup's 32: so it needs only 8
         // entries of the query-indexed vectors lse2 and D.
         const int key0 = jb * kBN + (warp & 3) * 32 + (lane >> 2);
         const float sl2 = a.scale_log2;
@@ -249,41 +258,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qi = qi0 + it % nqi;
             if (!(ok = mbar_wait(BAR_SDF, it & 1, a.status, a.timeout_ns, 36))) break;
             tc_fence_after();
-            const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + hf * 64 + lane_off;
-            const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + hf * 64 + lane_off;
-            // dP^T first: once both warpgroups hold it, S^T(it+1) may overwrite it
-            uint32_t dp[2][32];
-            tmem_ld16x256_x8(rd, dp[0]);
-            tmem_ld16x256_x8(rd + (16u << 16), dp[1]);
-            const float* lse2 = vec + s * 2 * kBM + hf * 64;
-            const float* dvec = vec + s * 2 * kBM + kBM + hf * 64;
-            uint64_t nl[8], nd[8];  // (-lse2, -D) of the thread's column pairs
+            const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + wg * 32 + lane_off;
+            const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + wg * 32 + lane_off;
+            // dP^T first: once every warpgroup holds it, S^T(it+1) may overwrite it
+            uint32_t dp[2][16];
+            tmem_ld16x256_x4(rd, dp[0]);
+            tmem_ld16x256_x4(rd + (16u << 16), dp[1]);
+            const float* lse2 = vec + s * 2 * kBM + wg * 32;
+            const float* dvec = vec + s * 2 * kBM + kBM + wg * 32;
+            uint64_t nl[4], nd[4];  // (-lse2, -D) of the thread's column pairs
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
                 const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
                 nl[j] = f2(-l2.x, -l2.y);
                 nd[j] = f2(-d2.x, -d2.y);
             }
             tmem_wait_ld();
-            reg_fence<32>(dp[0]);
-            reg_fence<32>(dp[1]);
+            reg_fence<16>(dp[0]);
+            reg_fence<16>(dp[1]);
             tc_fence_before();
             mbar_arrive(BAR_LD);
-            const int qbase = qi * kBM + hf * 64 + 2 * t4;  // query of the thread's column 0
+            const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
 #pragma unroll
             for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
                 const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
-                uint32_t sv[32];
-                tmem_ld16x256_x8(rs + lo, sv);
+                uint32_t sv[16];
+                tmem_ld16x256_x4(rs + lo, sv);
                 tmem_wait_ld();
-                reg_fence<32>(sv);
+                reg_fence<16>(sv);
                 const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
                 // causal: key k is hidden from query q when k > q
                 const bool need_mask = a.causal && key + 8 > qbase;
-                uint32_t pk[16], dk[16];
+                uint32_t pk[8], dk[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int rsel = 0; rsel < 2; ++rsel) {
                         const int i = 4 * j + 2 * rsel;
@@ -304,26 +313,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dk[2 * j + rsel] = pack_bf16(e0, e1);
                     }
                 }
-                tmem_st16x128_x8(rs + lo, pk);       // P^T over the first 32 S^T columns read
-                tmem_st16x128_x8(rs + lo + 32, dk);  // dS^T over the other 32
+                tmem_st16x128_x4(rs + lo, pk);       // P^T over the first 16 S^T columns read
+                tmem_st16x128_x4(rs + lo + 16, dk);  // dS^T over the other 16
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR_PF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 37);
-        // warpgroup 0 writes dV, warpgroup 1 writes dK = scale * (dS^T Q); staging
-        // reuses stage 0's Q (dV) and dO (dK) buffers, idle once all MMAs are done
-        const uint32_t stage = sStage + hf * C::TILE;
+        // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those
+        // of dK = scale * (dS^T Q); staging reuses stage 0's Q (dV) and dO (dK)
+        // buffers, idle once all MMAs are done
+        const int which = wg >> 1, half = wg & 1;
+        const uint32_t stage = sStage + which * C::TILE;
         if (ok_e) {
             tc_fence_after();
-            stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + hf * D + lane_off, stage, r, 0, D,
-                                      hf ? a.scale : 1.f);
+            stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + which * D + lane_off, stage, r,
+                                      half * (D / 2), (half + 1) * (D / 2), which ? a.scale : 1.f);
             fence_proxy_async_smem();
         }
-        named_bar_sync(1 + hf, 128);
-        if (ok_e && r == 0) {
-            const CUtensorMap* tm = hf ? &tmDK : &tmDV;
+        named_bar_sync(1 + which, 256);
+        if (ok_e && half == 0 && r == 0) {
+            const CUtensorMap* tm = which ? &tmDK : &tmDV;
             for (int c = 0; c < C::NCH; ++c)
                 tma_store_4d(tm, stage + c * C::CHUNK, c * 64, hk, jb * kBN, b);
             tma_store_commit();
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kDkWarpMma) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -349,7 +360,7 @@ cudaError_t launch_bwd_dkdv(const BwdMaps& m, const BwdArgs& a, cudaStream_t st)
     if (e != cudaSuccess) return e;
     const long long nblk = static_cast<long long>((a.N + kBN - 1) / kBN) * a.B * a.Hkv;
     if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(nblk), kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv,
+    kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv,
                                                               a);
     return cudaGetLastError();
 }
