@@ -7,14 +7,18 @@
 // describe for the backward pass: "FlashAttention Kernel", recomputation
 // bullet; the gradient formulas are the derivative of the forward definition).
 //
-// Pipelining.  Every MMA is 128 wide (a tcgen05.mma of N = 64 cannot be issued
-// faster than ~46 cycles, a third more than its math takes; N = 128 runs at the
-// math rate).  S is double-buffered in TMEM, so S(j+2) is computed while the
-// two warpgroups turn block j+1 into dS (warpgroup h takes keys 64h..64h+63);
-// dQ += dS_h K_h is issued as soon as warpgroup h is done, then dP(j+2) into
-// the single dP buffer.  K and V stream through a 5-slot TMA ring.
+// Pipelining.  Every MMA is 128 wide.  dP is double-buffered in TMEM and S is
+// not: as soon as both warpgroups have copied S(j) and dP(j) into registers,
+// the tensor core computes S(j+1) into the S buffer, and the warpgroups write
+// dS(j) (bf16) over the dP(j) columns they read.  dQ += dS(j) K_j then reads
+// it from there, and dP(j+2) is written over it.  dP(j+1) was computed a block
+// earlier, so the warpgroups go from block j to block j+1 without waiting for
+// the tensor core, which runs S(j+1), dQ(j) and dP(j+2) meanwhile.  Warpgroup
+// h takes keys 64h..64h+63 of every block.  K and V stream through separate
+// TMA rings in the order the MMAs first use them (K_0, V_0, V_1, K_1, V_2,
+// K_2, ...).
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256), dP [256,384), dQ [384,384+D).
+// TMEM (512 columns): S [0,128), dP0 [128,256), dP1 [256,384), dQ [384,384+D).
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -25,12 +29,16 @@ using namespace bwd;
 template <int D>
 struct DqCfg : Tiles<D> {
     using T = Tiles<D>;
-    static constexpr int NSLOT = (D == 128) ? 5 : 8;  // K / V ring slots, one tile each
-    static constexpr int OFF_KV = 2 * T::TILE;          // after Q, dO
-    static constexpr int OFF_BAR = OFF_KV + NSLOT * T::TILE;
-    static constexpr int NBAR = 1 + 2 * NSLOT + 1 + 2 + 1;
+    static constexpr int KS = 3;  // K ring slots: K_j (dQ), K_{j+1} (S), one ahead
+    static constexpr int VS = 2;  // V ring slots: V_{j+2} (dP), one ahead
+    static constexpr int OFF_K = 2 * T::TILE;  // after Q, dO
+    static constexpr int OFF_V = OFF_K + KS * T::TILE;
+    static constexpr int OFF_BAR = OFF_V + VS * T::TILE;
+    // barriers: Q/dO, K full/empty[KS], V full/empty[VS], S+dP ready, copied to
+    // registers, dS written, all MMAs done
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 4;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
-    static constexpr uint32_t TM_S = 0, TM_DP = 256, TM_DQ = 384;
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 384;
 };
 
 template <int D>
@@ -45,16 +53,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sDO = sQ + C::TILE;
-    const uint32_t sKV = sQ + C::OFF_KV;  // slot t at sKV + t*TILE; K_j is tile 2j, V_j tile 2j+1
+    const uint32_t sK = sQ + C::OFF_K;  // K_j in slot j % KS
+    const uint32_t sV = sQ + C::OFF_V;  // V_j in slot j % VS
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t BAR_QDO = bar0;  // Q, dO tiles landed
-    auto BAR_KVF = [&](int t) { return bar0 + 8u * (1 + t); };
-    auto BAR_KVE = [&](int t) { return bar0 + 8u * (1 + C::NSLOT + t); };
-    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NSLOT);       // block's S and dP ready
-    auto BAR_PF = [&](int hf) { return BAR_SDF + 8u * (1 + hf); };  // half's dS written
-    const uint32_t BAR_ACC = BAR_SDF + 8u * 3;
+    auto BAR_KF = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto BAR_KE = [&](int s) { return bar0 + 8u * (1 + C::KS + s); };
+    auto BAR_VF = [&](int s) { return bar0 + 8u * (1 + 2 * C::KS + s); };
+    auto BAR_VE = [&](int s) { return bar0 + 8u * (1 + 2 * C::KS + C::VS + s); };
+    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::KS + 2 * C::VS);  // S(j), dP(j) ready
+    const uint32_t BAR_LD = BAR_SDF + 8u;   // S(j), dP(j) copied to registers
+    const uint32_t BAR_PF = BAR_SDF + 16u;  // dS(j) written
+    const uint32_t BAR_ACC = BAR_SDF + 24u;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -70,12 +82,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_QDO, 1);
-        for (int t = 0; t < C::NSLOT; ++t) {
-            mbar_init(BAR_KVF(t), 1);
-            mbar_init(BAR_KVE(t), 1);
+        for (int s = 0; s < C::KS; ++s) {
+            mbar_init(BAR_KF(s), 1);
+            mbar_init(BAR_KE(s), 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
+            mbar_init(BAR_VF(s), 1);
+            mbar_init(BAR_VE(s), 1);
         }
         mbar_init(BAR_SDF, 1);
-        for (int hf = 0; hf < 2; ++hf) mbar_init(BAR_PF(hf), 128);
+        mbar_init(BAR_LD, 256);
+        mbar_init(BAR_PF, 256);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
     }
@@ -101,97 +118,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sQ + c * C::CHUNK, &tmQ, BAR_QDO, c * 64, h, qi * kBM, b);
                 tma_load_4d(sDO + c * C::CHUNK, &tmDO, BAR_QDO, c * 64, h, qi * kBM, b);
             }
-            int last_idx[C::NSLOT];
-            for (int t = 0; t < C::NSLOT; ++t) last_idx[t] = -1;
-            bool ok = true;
-            for (int idx = 0; idx < 2 * nj && ok; ++idx) {
-                const int t = idx % C::NSLOT;
-                if (!(ok = mbar_wait(BAR_KVE(t), ((idx / C::NSLOT) & 1) ^ 1u, a.status,
-                                     a.timeout_ns, 20)))
-                    break;
-                mbar_arrive_expect_tx(BAR_KVF(t), C::TILE);
-                const CUtensorMap* tm = (idx & 1) ? &tmV : &tmK;
+            int last_k[C::KS], last_v[C::VS];
+            for (int s = 0; s < C::KS; ++s) last_k[s] = -1;
+            for (int s = 0; s < C::VS; ++s) last_v[s] = -1;
+            // key block jj of K (isv = 0) or V (isv = 1) into its ring; the first
+            // use of a slot waits on parity 1, which a fresh barrier reports complete
+            auto load = [&](int jj, bool isv) {
+                const int ns = isv ? C::VS : C::KS;
+                const int slot = jj % ns;
+                const uint32_t ph = ((jj / ns) & 1) ^ 1u;
+                if (!mbar_wait(isv ? BAR_VE(slot) : BAR_KE(slot), ph, a.status, a.timeout_ns, 20))
+                    return false;
+                const uint32_t full = isv ? BAR_VF(slot) : BAR_KF(slot);
+                const uint32_t dst = (isv ? sV : sK) + slot * C::TILE;
+                mbar_arrive_expect_tx(full, C::TILE);
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d_hint(sKV + t * C::TILE + c * C::CHUNK, tm, BAR_KVF(t), c * 64, hk,
-                                     (idx >> 1) * kBN, b, pol_kv);
-                last_idx[t] = idx;
-            }
+                    tma_load_4d_hint(dst + c * C::CHUNK, isv ? &tmV : &tmK, full, c * 64, hk,
+                                     jj * kBN, b, pol_kv);
+                if (isv)
+                    last_v[slot] = jj;
+                else
+                    last_k[slot] = jj;
+                return true;
+            };
+            // first-use order of the MMAs: K_0, V_0, then V_i, K_i
+            bool ok = load(0, false) && load(0, true);
+            for (int i = 1; i < nj && ok; ++i) ok = load(i, true) && load(i, false);
             // no copies in flight at exit: wait (bounded) for the last load of each slot
             mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 21);
-            for (int t = 0; t < C::NSLOT; ++t)
-                if (last_idx[t] >= 0)
-                    mbar_wait(BAR_KVF(t), (last_idx[t] / C::NSLOT) & 1, a.status, a.timeout_ns, 21);
+            for (int s = 0; s < C::KS; ++s)
+                if (last_k[s] >= 0)
+                    mbar_wait(BAR_KF(s), (last_k[s] / C::KS) & 1, a.status, a.timeout_ns, 21);
+            for (int s = 0; s < C::VS; ++s)
+                if (last_v[s] >= 0)
+                    mbar_wait(BAR_VF(s), (last_v[s] / C::VS) & 1, a.status, a.timeout_ns, 21);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);  // S, dP
             constexpr uint32_t IDESC_DQ = idesc_bf16(kBM, D, false, true);     // dQ += dS K
-            const uint32_t tDP = tbase + C::TM_DP, tDQ = tbase + C::TM_DQ;
-            auto kslot = [&](int jj) { return (2 * jj) % C::NSLOT; };
-            auto vslot = [&](int jj) { return (2 * jj + 1) % C::NSLOT; };
-            auto ready = [&](int tile) {  // wait for ring tile `tile` (K_j = 2j, V_j = 2j+1)
-                const bool r = mbar_wait(BAR_KVF(tile % C::NSLOT), (tile / C::NSLOT) & 1,
-                                         a.status, a.timeout_ns, 23);
+            const uint32_t tS = tbase + C::TM_S, tDQ = tbase + C::TM_DQ;
+            auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
+            auto k_ready = [&](int jj) {
+                const bool r = mbar_wait(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.status,
+                                         a.timeout_ns, 23);
                 tc_fence_after();
                 return r;
             };
-            // S(jj) = Q K_jj^T into S buffer jj & 1 (A = Q, B = K_jj, both K-major)
-            auto issue_s = [&](int jj) {
-                const uint32_t sK = sKV + kslot(jj) * C::TILE;
-                const uint32_t dS = tbase + C::TM_S + (jj & 1) * kBN;
+            auto v_ready = [&](int jj) {
+                const bool r = mbar_wait(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.status,
+                                         a.timeout_ns, 23);
+                tc_fence_after();
+                return r;
+            };
+            // dst = A B^T over the head dimension (both K-major): S = Q K^T, dP = dO V^T
+            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
+                    mma_bf16_ss(dst, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
                                 IDESC_S, ks > 0);
                 }
             };
-            // dP(jj) = dO V_jj^T into the dP buffer; the commit also covers S(jj)
+            // dP(jj) = dO V_jj^T; V_jj's slot is free once it has run
             auto issue_dp = [&](int jj) {
-                const uint32_t sV = sKV + vslot(jj) * C::TILE;
+                issue_t(tDP(jj), sDO, sV + (jj % C::VS) * C::TILE);
+                mma_commit(BAR_VE(jj % C::VS));
+            };
+            // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
+            // of dP buffer jj & 1; K rows 16ks.. read MN-major
+            auto issue_dq = [&](int jj) {
+                const uint32_t kt = sK + (jj % C::KS) * C::TILE, aS = tDP(jj);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(tDP, sdesc_sw128(sDO + off, 16, 1024),
-                                sdesc_sw128(sV + off, 16, 1024), IDESC_S, ks > 0);
-                }
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8,
+                                sdesc_sw128(kt + ks * 2048, C::CHUNK, 1024), IDESC_DQ,
+                                (jj == 0 && ks == 0) ? 0u : 1u);
+                mma_commit(BAR_KE(jj % C::KS));
+            };
+            bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && k_ready(0);
+            if (ok) issue_t(tS, sQ, sK);
+            if (ok && (ok = v_ready(0))) {
+                issue_dp(0);
                 mma_commit(BAR_SDF);
-            };
-            // dQ += dS_h K_h: dS (bf16) of keys 64h.. at columns [64h, 64h+32) of S
-            // buffer jj & 1; K rows 64h.. read MN-major
-            auto issue_dq = [&](int jj, int hf) {
-                const uint32_t sK = sKV + kslot(jj) * C::TILE;
-                const uint32_t aS = tbase + C::TM_S + (jj & 1) * kBN + hf * 64;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tDQ, aS + ks * 8,
-                                sdesc_sw128(sK + hf * C::HALF_ROWS + ks * 2048, C::CHUNK, 1024),
-                                IDESC_DQ, (jj == 0 && hf == 0 && ks == 0) ? 0u : 1u);
-            };
-            bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && ready(0);
-            if (ok) issue_s(0);
-            if (ok && (ok = ready(1))) issue_dp(0);
-            if (ok && nj > 1 && (ok = ready(2))) issue_s(1);
+            }
+            if (ok && nj > 1 && (ok = v_ready(1))) issue_dp(1);
             for (int j = 0; j < nj && ok; ++j) {
-                if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.status, a.timeout_ns, 24))) break;
-                tc_fence_after();
-                issue_dq(j, 0);
-                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.status, a.timeout_ns, 24))) break;
-                tc_fence_after();
-                issue_dq(j, 1);
-                // K_j and V_j are free once these MMAs complete
-                mma_commit(BAR_KVE(kslot(j)));
-                mma_commit(BAR_KVE(vslot(j)));
-                // both warpgroups have read dP(j): the dP buffer may be overwritten
+                // S(j+1) into the S buffer once both warpgroups hold S(j); the
+                // commit also covers dP(j+1), issued a block earlier
                 if (j + 1 < nj) {
-                    if (!(ok = ready(2 * (j + 1) + 1))) break;
-                    issue_dp(j + 1);
+                    if (!(ok = mbar_wait(BAR_LD, j & 1, a.status, a.timeout_ns, 24))) break;
+                    if (!(ok = k_ready(j + 1))) break;
+                    issue_t(tS, sQ, sK + ((j + 1) % C::KS) * C::TILE);
+                    mma_commit(BAR_SDF);
                 }
-                // S buffer j & 1 is read by dQ(j) above before S(j+2) lands in it
+                if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 24))) break;
+                tc_fence_after();
+                issue_dq(j);
+                // dP(j+2) over dS(j): the dQ products above read it first
                 if (j + 2 < nj) {
-                    if (!(ok = ready(2 * (j + 2)))) break;
-                    issue_s(j + 2);
+                    if (!(ok = v_ready(j + 2))) break;
+                    issue_dp(j + 2);
                 }
             }
             // every issued MMA has finished before TMEM is released
@@ -204,18 +232,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane;
         const int grow = qi * kBM + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tDP = tbase + C::TM_DP + lane_off + hf * 64;
+        const uint32_t tS = tbase + C::TM_S + lane_off + hf * 64;
         const bool valid = grow < a.N;
         const size_t st_idx = (static_cast<size_t>(b) * a.Hq + h) * a.N + (valid ? grow : 0);
         const float nlse2 = valid ? -a.lse[st_idx] * kLog2e : 0.f;
         const float dval = valid ? a.dsum[st_idx] : 0.f;
         const float sl2 = a.scale_log2;
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+        const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(nlse2, nlse2);
+        const uint64_t ndx2 = f2(-dval, -dval);
         bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
             if (!(ok = mbar_wait(BAR_SDF, j & 1, a.status, a.timeout_ns, 26))) break;
             tc_fence_after();
-            const uint32_t tS = tbase + C::TM_S + (j & 1) * kBN + lane_off + hf * 64;
+            const uint32_t tDP = tbase + C::TM_DP + (j & 1) * 128 + lane_off + hf * 64;
             uint32_t sv[64], dp[64];
             tmem_ld32(tS, sv);
             tmem_ld32(tS + 32, sv + 32);
@@ -224,10 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             reg_fence<64>(sv);
             reg_fence<64>(dp);
+            // both buffers are in registers: S(j+1) may now overwrite S(j)
+            tc_fence_before();
+            mbar_arrive(BAR_LD);
             const int kbase = j * kBN + hf * 64;
             const bool need_mask = kbase + 63 > lim;
-            const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(nlse2, nlse2);
-            const uint64_t ndx2 = f2(-dval, -dval);
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
@@ -245,10 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f2_split(mul2(f2(p0, p1), t), d0, d1);
                 pk[c >> 1] = pack_bf16(d0, d1);
             }
-            tmem_st32(tS, pk);  // dS over this half's S columns
+            tmem_st32(tDP, pk);  // dS over the first 32 of this half's dP columns
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR_PF(hf));
+            mbar_arrive(BAR_PF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 27);
         if (ok_e) {
