@@ -190,9 +190,15 @@ def tensor_bytes(*ts) -> int:
     return sum(t.numel() * t.element_size() for t in ts)
 
 
+# event-timed slots of a step; the forward slot is the fa_fwd_train call (the
+# fp16 copies of q, k, v, 2 small kernels, then fa_fwd_kernel), the backward's
+# are the fa_bwd_stage steps: max |dO| then D with the fp16 copy of dO
+# (2 kernels), dK/dV, dQ
 KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel")
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
                   "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
+LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 2, "fa_bwd_dkdv_kernel": 1,
+            "fa_bwd_dq_kernel": 1}
 
 
 def kernel_work(w: W.Workload, name: str):
@@ -207,7 +213,8 @@ def kernel_work(w: W.Workload, name: str):
         return "tensor", 4 * g1
     if name == "fa_bwd_dq_kernel":
         return "tensor", 3 * g1
-    return "hbm", 3 * w.B * w.N * w.Hq * w.d * 2 + 4 * w.B * w.Hq * w.N
+    # dsum slot: read dO for its maximum, then dO, O, o_lo; write D and dO's fp16 copy
+    return "hbm", 5 * w.B * w.N * w.Hq * w.d * 2 + 4 * w.B * w.Hq * w.N
 
 
 def source_hash(name: str) -> str:
@@ -271,14 +278,18 @@ def run_gpu(args):
     lse = torch.empty((w.B, w.Hq, w.N), device=dev, dtype=torch.float32)
     if w.backward:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        wsb = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Hq, w.N), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(fa.fa_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                          device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB of L2
-    nk = 1 + (3 if w.backward else 0)  # kernels per step
+    nk = 1 + (3 if w.backward else 0)  # timed slots per step
 
     def fwd():
-        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, o_lo=o_lo)
+        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, o_lo=o_lo,
+                  workspace=wsb if w.backward else None)
 
-    def bwd(stages=fa.FA_BWD_DSUM | fa.FA_BWD_DKDV | fa.FA_BWD_DQ):
+    # the training pair on one workspace: fa_fwd_train leaves the fp16 copies of
+    # q, k, v there, so the backward copies only dout
+    def bwd(stages=fa.FA_BWD_AFTER_FWD_TRAIN):
         fa.fa_bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
                   workspace=wsb, stages=stages, o_lo=o_lo)
 
@@ -306,7 +317,8 @@ def run_gpu(args):
         fwd()
         ev[i][1].record()
         if w.backward:
-            for n, stage in enumerate((fa.FA_BWD_DSUM, fa.FA_BWD_DKDV, fa.FA_BWD_DQ)):
+            for n, stage in enumerate((fa.FA_BWD_PREP_DOUT | fa.FA_BWD_DSUM, fa.FA_BWD_DKDV,
+                                       fa.FA_BWD_DQ)):
                 bwd(stage)
                 ev[i][2 + n].record()
     torch.cuda.synchronize()
@@ -377,7 +389,8 @@ def run_gpu(args):
             "frac_of_peak": value / ws / peak,
             "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak, "fwd_ms": fwd_ms,
             "peak_tflops": peak, "peak_source": peaks["source"] + " burst bf16",
-            "gpu_launches": nk * K}
+            "gpu_launches": K * ((LAUNCHES["fa_fwd_kernel"] if w.backward else 1) +
+                                 sum(LAUNCHES[n] for n in KERNELS[1:nk]))}
     if w.backward:
         bwd_tf = W.bwd_flops(w) / (bwd_ms * 1e-3) / 1e12
         line.update({"bwd_tflops": bwd_tf, "bwd_frac_of_peak": bwd_tf / peak, "bwd_ms": bwd_ms})

@@ -25,7 +25,10 @@ FA_ERR_CUDA = 3
 FA_ERR_DEVICE_TIMEOUT = 4
 
 # fa_bwd_stage bits
-FA_BWD_DSUM, FA_BWD_DKDV, FA_BWD_DQ = 1, 2, 4
+FA_BWD_DSUM, FA_BWD_DKDV, FA_BWD_DQ, FA_BWD_PREP, FA_BWD_PREP_DOUT = 1, 2, 4, 8, 16
+FA_BWD_ALL = FA_BWD_PREP | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ
+# backward after fa_fwd_train on the same workspace: q, k, v copies already there
+FA_BWD_AFTER_FWD_TRAIN = FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_noalloc",
@@ -54,7 +57,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd.restype = i
-    lib.fa_fwd_train.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa_fwd_train.restype = i
     lib.fa_bwd.argtypes = [vp] * 11 + [i, i, i, i, i, i, f, vp]
     lib.fa_bwd.restype = i
@@ -62,8 +65,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_stage.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc.restype = i
-    lib.fa_bwd_workspace_size.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+
     lib.fa_get_device_error.argtypes = [vp]
     lib.fa_get_device_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -112,10 +116,13 @@ def _dims(q, k):
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, lse=None,
-           stream=None, o_lo=None):
+           stream=None, o_lo=None, workspace=None):
     """Forward pass.  Returns (o, lse); o, lse are allocated if not given.
     With o_lo (a bf16 tensor shaped like q) this is the training forward
-    (fa_fwd_train): o_lo receives the low bf16 half of O for fa_bwd."""
+    (fa_fwd_train): o_lo receives the low bf16 half of O for fa_bwd, and P
+    enters P V in fp16.  `workspace` is the training workspace
+    (fa_bwd_workspace_size bytes, allocated if not given); it keeps the fp16
+    copies of q, k, v for a backward that uses stages=FA_BWD_AFTER_FWD_TRAIN."""
     lib = load_library()
     B, N, Hq, Hkv, d = _dims(q, k)
     _check(q, "q", (B, N, Hq, d))
@@ -134,23 +141,28 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, ls
                         B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
     else:
         _check(o_lo, "o_lo", (B, N, Hq, d))
+        ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+        if workspace.numel() * workspace.element_size() < ws_bytes:
+            raise ValueError("workspace too small")
         st = lib.fa_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                              o_lo.data_ptr(), lse.data_ptr(), B, Hq, Hkv, N, d,
-                              int(bool(causal)), float(scale), _stream_handle(stream))
+                              o_lo.data_ptr(), lse.data_ptr(), workspace.data_ptr(), B, Hq, Hkv,
+                              N, d, int(bool(causal)), float(scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
     return o, lse
 
 
-def fa_bwd_workspace_size(B: int, H: int, N: int) -> int:
-    return int(load_library().fa_bwd_workspace_size(B, H, N))
+def fa_bwd_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, Hkv, N, d))
 
 
 def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
            dq=None, dk=None, dv=None, workspace=None, stream=None,
-           stages: int = FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, o_lo=None):
+           stages: int = FA_BWD_ALL, o_lo=None):
     """Backward pass.  Returns (dq, dk, dv); buffers are allocated if not given.
-    `stages` selects a subset of the three kernels (fa_bwd_stage); o_lo is the
+    `stages` selects a subset of the steps (fa_bwd_stage); o_lo is the
     training forward's low half of O (None: D from o alone)."""
     lib = load_library()
     B, N, Hq, Hkv, d = _dims(q, k)
@@ -168,7 +180,7 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
     _check(dq, "dq", (B, N, Hq, d))
     _check(dk, "dk", (B, N, Hkv, d))
     _check(dv, "dv", (B, N, Hkv, d))
-    ws_bytes = fa_bwd_workspace_size(B, Hq, N)
+    ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
     if workspace.numel() * workspace.element_size() < ws_bytes:
@@ -179,8 +191,7 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
             None if o_lo is None else o_lo.data_ptr(),
             B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
-    all_stages = FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ
-    st = lib.fa_bwd(*args) if stages == all_stages else lib.fa_bwd_stage(int(stages), *args)
+    st = lib.fa_bwd(*args) if stages == FA_BWD_ALL else lib.fa_bwd_stage(int(stages), *args)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv

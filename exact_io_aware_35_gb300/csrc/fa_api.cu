@@ -77,17 +77,18 @@ fa_status device_ready(DeviceInfo** out) {
     return FA_OK;
 }
 
-// Tensor map of a [B, N, H, d] bf16 tensor: dims (d, H, N, B), box
-// (64, 1, 128, 1), 128-byte swizzle; rows past N read as zero and are never
-// written.
-fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d) {
+// Tensor map of a [B, N, H, d] bf16 (or, f16 = true, fp16) tensor: dims
+// (d, H, N, B), box (64, 1, 128, 1), 128-byte swizzle; rows past N read as
+// zero and are never written.
+fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, bool f16 = false) {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                              static_cast<cuuint64_t>(N) * H * d * 2};
     cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+    CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          4, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -100,6 +101,56 @@ fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d) 
 }
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Byte offsets inside the training workspace (each 256-aligned), shared by
+// fa_fwd_train and fa_bwd: D, the fp16 copies of Q, K, V, dO, the absmax
+// words and the scales.
+struct WsLayout {
+    size_t d, q16, k16, v16, do16, absmax, scales, total;
+};
+
+WsLayout bwd_layout(int B, int H, int Hkv, int N, int d) {
+    const size_t q_el = static_cast<size_t>(B) * N * H * d, kv_el = static_cast<size_t>(B) * N * Hkv * d;
+    WsLayout w{};
+    w.d = 0;
+    w.q16 = up256(4ull * static_cast<size_t>(B) * H * N);
+    w.k16 = w.q16 + up256(2 * q_el);
+    w.v16 = w.k16 + up256(2 * kv_el);
+    w.do16 = w.v16 + up256(2 * kv_el);
+    w.absmax = w.do16 + up256(2 * q_el);
+    w.scales = w.absmax + 256;
+    w.total = w.scales + 256;
+    return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+// A job that copies the listed tensors (q, k, v, dout; null = skip) into the
+// workspace's fp16 slots.
+F16Prep prep_job(void* ws, const WsLayout& wl, const void* q, const void* k, const void* v,
+                 const void* dout, int B, int H, int Hkv, int N, int d) {
+    F16Prep p{};
+    const void* src[4] = {q, k, v, dout};
+    const size_t off[4] = {wl.q16, wl.k16, wl.v16, wl.do16};
+    const size_t nq = static_cast<size_t>(B) * N * H * d, nkv = static_cast<size_t>(B) * N * Hkv * d;
+    const size_t n[4] = {nq, nkv, nkv, nq};
+    for (int t = 0; t < 4; ++t) {
+        p.src[t] = static_cast<const uint16_t*>(src[t]);
+        p.dst[t] = at<uint16_t>(ws, off[t]);
+        p.n[t] = src[t] ? n[t] : 0;
+    }
+    p.absmax = at<uint32_t>(ws, wl.absmax);
+    p.scales = at<F16Scales>(ws, wl.scales);
+    p.d = d;
+    p.convert_mask = (q ? 1 : 0) | (k ? 2 : 0) | (v ? 4 : 0) | (dout ? 8 : 0);
+    return p;
+}
+
 
 fa_status check_sizes(int B, int H, int Hkv, int N, int d, float scale) {
     if (B < 1 || H < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
@@ -145,36 +196,52 @@ const char* fa_status_string(fa_status s) {
 
 const char* fa_last_cuda_error(void) { return t_last_error; }
 
-size_t fa_bwd_workspace_size(int B, int H, int N) {
-    if (B < 1 || H < 1 || N < 1) return 0;
-    const size_t bytes = 4ull * static_cast<size_t>(B) * H * N;
-    return (bytes + 255) & ~static_cast<size_t>(255);
+size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
+    if (check_sizes(B, H, Hkv, N, d, 1.f) != FA_OK) return 0;
+    return bwd_layout(B, H, Hkv, N, d).total;
 }
+
+
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int Hkv, int N, int d, int causal, float scale, void* stream) {
-    return fa_fwd_train(q, k, v, o, nullptr, lse, B, H, Hkv, N, d, causal, scale, stream);
+    return fa_fwd_train(q, k, v, o, nullptr, lse, nullptr, B, H, Hkv, N, d, causal, scale,
+                        stream);
 }
 
 fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, void* o_lo,
-                       float* lse, int B, int H, int Hkv, int N, int d, int causal, float scale,
-                       void* stream) {
+                       float* lse, void* workspace, int B, int H, int Hkv, int N, int d,
+                       int causal, float scale, void* stream) {
     t_last_error[0] = 0;
     fa_status st = check_sizes(B, H, Hkv, N, d, scale);
     if (st != FA_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
     if (o_lo && !aligned16(o_lo)) return FA_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
     DeviceInfo* di = nullptr;
     if ((st = device_ready(&di)) != FA_OK) return st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const WsLayout wl = bwd_layout(B, H, Hkv, N, d);
     FwdMaps maps;
     if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
     if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
-    if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
+    if (workspace) {
+        // fp16 copies of Q, K, V: V for the P V product (P then in fp16), Q and
+        // K left for a backward that runs with FA_BWD_PREP_DOUT on this workspace
+        if ((st = make_map(&maps.v, at<void>(workspace, wl.v16), B, N, Hkv, d, true)) != FA_OK)
+            return st;
+        const cudaError_t e =
+            launch_f16_prep(prep_job(workspace, wl, q, k, v, nullptr, B, H, Hkv, N, d), cs);
+        if (e != cudaSuccess) return cuda_fail(e, "fp16 copies of Q, K, V");
+    } else if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) {
+        return st;
+    }
     if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
     FwdArgs a;
     a.lse = lse;
     a.o_lo = static_cast<uint16_t*>(o_lo);
+    a.f16s = workspace ? at<const F16Scales>(workspace, wl.scales) : nullptr;
     a.status = di->status;
     a.B = B;
     a.Hq = H;
@@ -185,7 +252,7 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
     a.timeout_ns = kWaitTimeoutNs;
-    cudaError_t e = launch_fwd(maps, a, d, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_fwd(maps, a, d, cs);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
     return FA_OK;
 }
@@ -194,8 +261,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  const void* o_lo, int B, int H, int Hkv, int N, int d, int causal, float scale,
                  void* stream) {
-    return fa_bwd_stage(FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, q, k, v, o, dout, lse, dq, dk, dv,
-                        workspace, o_lo, B, H, Hkv, N, d, causal, scale, stream);
+    return fa_bwd_stage(FA_BWD_PREP | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, q, k, v, o, dout, lse,
+                        dq, dk, dv, workspace, o_lo, B, H, Hkv, N, d, causal, scale, stream);
 }
 
 fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, const void* o,
@@ -203,12 +270,26 @@ fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, 
                        void* workspace, const void* o_lo, int B, int H, int Hkv, int N, int d,
                        int causal, float scale, void* stream) {
     t_last_error[0] = 0;
-    if (stages <= 0 || stages > 7) return FA_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_INVALID_ARG;
+    return fa::bwd_run(stages, q, k, v, o, dout, lse, dq, dk, dv, static_cast<float*>(workspace),
+                       workspace, o_lo, B, H, Hkv, N, d, causal, scale, stream);
+}
+
+}  // extern "C"
+
+namespace fa {
+
+fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, float* dsum,
+                  void* f16_ws, const void* o_lo, int B, int H, int Hkv, int N, int d, int causal,
+                  float scale, void* stream) {
+    t_last_error[0] = 0;
+    if (stages <= 0 || stages > 31) return FA_ERR_INVALID_ARG;
     fa_status st = check_sizes(B, H, Hkv, N, d, scale);
     if (st != FA_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-        !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !workspace ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dsum))
         return FA_ERR_INVALID_ARG;
     if (o_lo && !aligned16(o_lo)) return FA_ERR_INVALID_ARG;
     DeviceInfo* di = nullptr;
@@ -221,9 +302,37 @@ fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, 
     if ((st = make_map(&maps.dq, dq, B, N, H, d)) != FA_OK) return st;
     if ((st = make_map(&maps.dk, dk, B, N, Hkv, d)) != FA_OK) return st;
     if ((st = make_map(&maps.dv, dv, B, N, Hkv, d)) != FA_OK) return st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const WsLayout wl = bwd_layout(B, H, Hkv, N, d);
+    if (f16_ws) {
+        if ((st = make_map(&maps.q16, at<void>(f16_ws, wl.q16), B, N, H, d, true)) != FA_OK)
+            return st;
+        if ((st = make_map(&maps.k16, at<void>(f16_ws, wl.k16), B, N, Hkv, d, true)) != FA_OK)
+            return st;
+        if ((st = make_map(&maps.v16, at<void>(f16_ws, wl.v16), B, N, Hkv, d, true)) != FA_OK)
+            return st;
+        if ((st = make_map(&maps.dout16, at<void>(f16_ws, wl.do16), B, N, H, d, true)) != FA_OK)
+            return st;
+        if (stages & (FA_BWD_PREP | FA_BWD_PREP_DOUT)) {
+            const bool all = (stages & FA_BWD_PREP) != 0;
+            F16Prep p = prep_job(f16_ws, wl, all ? q : nullptr, all ? k : nullptr,
+                                 all ? v : nullptr, dout, B, H, Hkv, N, d);
+            // with the D stage in the same call, the dsum kernel (which reads dO
+            // anyway) makes the copy of dO
+            if (stages & FA_BWD_DSUM) p.convert_mask &= ~8;
+            const cudaError_t e = launch_f16_prep(p, cs);
+            if (e != cudaSuccess) return cuda_fail(e, "fp16 operand copies");
+        }
+    }
     BwdArgs a;
     a.lse = lse;
-    a.dsum = static_cast<float*>(workspace);
+    a.dsum = dsum;
+    a.f16s = f16_ws ? at<const F16Scales>(f16_ws, wl.scales) : nullptr;
+    const bool fused_copy = f16_ws && (stages & (FA_BWD_PREP | FA_BWD_PREP_DOUT)) &&
+                            (stages & FA_BWD_DSUM);
+    a.dout16 = fused_copy ? at<uint16_t>(f16_ws, wl.do16) : nullptr;
+    a.absmax = fused_copy ? at<uint32_t>(f16_ws, wl.absmax) : nullptr;
+    a.scales_w = fused_copy ? at<F16Scales>(f16_ws, wl.scales) : nullptr;
     a.o = static_cast<const uint16_t*>(o);
     a.dout = static_cast<const uint16_t*>(dout);
     a.o_lo = static_cast<const uint16_t*>(o_lo);
@@ -238,10 +347,15 @@ fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, 
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.timeout_ns = kWaitTimeoutNs;
-    cudaError_t e = launch_bwd(maps, a, stages, static_cast<cudaStream_t>(stream));
+    if ((stages & 7) == 0) return FA_OK;
+    cudaError_t e = launch_bwd(maps, a, stages & 7, cs);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
     return FA_OK;
 }
+
+}  // namespace fa
+
+extern "C" {
 
 fa_status fa_get_device_error(void* stream) {
     t_last_error[0] = 0;

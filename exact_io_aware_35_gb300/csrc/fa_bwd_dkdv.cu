@@ -54,7 +54,11 @@ struct DkdvCfg : Tiles<D> {
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
 };
 
-template <int D>
+// F16: every operand tile is the fp16 copy (Q, K, V, dO scaled by 2^q, 2^k,
+// 2^v, 2^dout); P^T and dS^T * 2^ds are rounded to fp16.  S^T then carries
+// 2^(q+k) (folded into scale * log2 e), dP^T 2^(v+dout), dV 2^dout and dK
+// 2^(ds+q), all undone exactly.
+template <int D, bool F16>
 __global__ void __launch_bounds__(kDkThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -173,8 +177,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         __syncwarp();
     } else if (warp == kDkWarpMma) {
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16(kBN, kBM, false, false);  // S^T, dP^T
-            constexpr uint32_t IDESC_ACC = idesc_bf16(kBN, D, false, true);  // dV, dK
+            constexpr uint32_t IDESC_S = idesc_16(kBN, kBM, false, false, F16);  // S^T, dP^T
+            constexpr uint32_t IDESC_ACC = idesc_16(kBN, D, false, true, F16);  // dV, dK
             const uint32_t tDV = tbase + C::TM_ACC, tDK = tbase + C::TM_ACC + D;
             // region of S^T(it) (then P^T, dS^T), and of dP^T(it)
             auto reg_s = [&](int it) { return tbase + ((it & 1) ? C::TM_Y : C::TM_X); };
@@ -250,7 +254,15 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         // 8j + 2(lane%4) + {0,1} of the warpgroup's 32: so it needs only 8
         // entries of the query-indexed vectors lse2 and D.
         const int key0 = jb * kBN + (warp & 3) * 32 + (lane >> 2);
-        const float sl2 = a.scale_log2;
+        // fp16 path: undo 2^(q+k) on S^T; dS^T = P^T (dP^T 2^u - D 2^ds) with
+        // u = ds - v - dout, so that dS^T carries exactly 2^ds
+        int eq = 0, ek = 0, ev = 0, edo = 0;
+        if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
+        const int eds = F16 ? ld_once(&a.f16s->ds) : 0;
+        const float sl2 = a.scale_log2 * pow2f(-(eq + ek));
+        const float dsc = pow2f(eds);
+        const float dpu = pow2f(eds - ev - edo);
+        const uint64_t dpu2 = f2(dpu, dpu);
         const uint64_t sl2x2 = f2(sl2, sl2);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
@@ -272,7 +284,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
                 const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
                 nl[j] = f2(-l2.x, -l2.y);
-                nd[j] = f2(-d2.x, -d2.y);
+                nd[j] = f2(-d2.x * dsc, -d2.y * dsc);
             }
             tmem_wait_ld();
             reg_fence<16>(dp[0]);
@@ -307,10 +319,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         }
                         float e0, e1;
                         f2_split(mul2(f2(p0, p1),
-                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
-                                           nd[j])), e0, e1);
-                        pk[2 * j + rsel] = pack_bf16(p0, p1);
-                        dk[2 * j + rsel] = pack_bf16(e0, e1);
+                                      fma2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
+                                           dpu2, nd[j])), e0, e1);
+                        pk[2 * j + rsel] = pack_op<F16>(p0, p1);
+                        dk[2 * j + rsel] = pack_op<F16>(e0, e1);
                     }
                 }
                 tmem_st16x128_x4(rs + lo, pk);       // P^T over the first 16 S^T columns read
@@ -328,8 +340,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const uint32_t stage = sStage + which * C::TILE;
         if (ok_e) {
             tc_fence_after();
+            // dV carries 2^dout, dK 2^(ds+q) on the fp16 path
+            const float mul = which ? a.scale * pow2f(-(eds + eq)) : pow2f(-edo);
             stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + which * D + lane_off, stage, r,
-                                      half * (D / 2), (half + 1) * (D / 2), which ? a.scale : 1.f);
+                                      half * (D / 2), (half + 1) * (D / 2), mul);
             fence_proxy_async_smem();
         }
         named_bar_sync(1 + which, 256);
@@ -352,17 +366,26 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 
 }  // namespace
 
-template <int D>
-cudaError_t launch_bwd_dkdv(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
-    auto kern = fa_bwd_dkdv_kernel<D>;
+template <int D, bool F16>
+cudaError_t launch_dkdv(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
+    auto kern = fa_bwd_dkdv_kernel<D, F16>;
     constexpr int smem = DkdvCfg<D>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long nblk = static_cast<long long>((a.N + kBN - 1) / kBN) * a.B * a.Hkv;
     if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv,
-                                                              a);
+    if (F16)
+        kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q16, m.k16, m.v16, m.dout16,
+                                                                  m.dk, m.dv, a);
+    else
+        kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk,
+                                                                  m.dv, a);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_dkdv(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
+    return a.f16s ? launch_dkdv<D, true>(m, a, st) : launch_dkdv<D, false>(m, a, st);
 }
 
 template cudaError_t launch_bwd_dkdv<64>(const BwdMaps&, const BwdArgs&, cudaStream_t);

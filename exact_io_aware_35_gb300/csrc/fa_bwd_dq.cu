@@ -41,7 +41,11 @@ struct DqCfg : Tiles<D> {
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 384;
 };
 
-template <int D>
+// F16: Q and K tiles are the fp16 copies (scaled by 2^q, 2^k; S carries
+// 2^(q+k), folded into scale * log2 e) and dS * 2^ds is rounded to fp16, so
+// dQ carries 2^(ds+k), undone in the epilogue.  dO and V stay bf16: dP is
+// not rounded before use.
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV,
@@ -156,8 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);  // S, dP
-            constexpr uint32_t IDESC_DQ = idesc_bf16(kBM, D, false, true);     // dQ += dS K
+            constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
+            constexpr uint32_t IDESC_DP = idesc_bf16(kBM, kBN, false, false);    // dP = dO V^T
+            constexpr uint32_t IDESC_DQ = idesc_16(kBM, D, false, true, F16);    // dQ += dS K
             const uint32_t tS = tbase + C::TM_S, tDQ = tbase + C::TM_DQ;
             auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
             auto k_ready = [&](int jj) {
@@ -173,17 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return r;
             };
             // dst = A B^T over the head dimension (both K-major): S = Q K^T, dP = dO V^T
-            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB) {
+            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB, uint32_t idesc) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
                     mma_bf16_ss(dst, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
-                                IDESC_S, ks > 0);
+                                idesc, ks > 0);
                 }
             };
             // dP(jj) = dO V_jj^T; V_jj's slot is free once it has run
             auto issue_dp = [&](int jj) {
-                issue_t(tDP(jj), sDO, sV + (jj % C::VS) * C::TILE);
+                issue_t(tDP(jj), sDO, sV + (jj % C::VS) * C::TILE, IDESC_DP);
                 mma_commit(BAR_VE(jj % C::VS));
             };
             // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(BAR_KE(jj % C::KS));
             };
             bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && k_ready(0);
-            if (ok) issue_t(tS, sQ, sK);
+            if (ok) issue_t(tS, sQ, sK, IDESC_S);
             if (ok && (ok = v_ready(0))) {
                 issue_dp(0);
                 mma_commit(BAR_SDF);
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < nj) {
                     if (!(ok = mbar_wait(BAR_LD, j & 1, a.status, a.timeout_ns, 24))) break;
                     if (!(ok = k_ready(j + 1))) break;
-                    issue_t(tS, sQ, sK + ((j + 1) % C::KS) * C::TILE);
+                    issue_t(tS, sQ, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
                     mma_commit(BAR_SDF);
                 }
                 if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 24))) break;
@@ -237,10 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t st_idx = (static_cast<size_t>(b) * a.Hq + h) * a.N + (valid ? grow : 0);
         const float nlse2 = valid ? -a.lse[st_idx] * kLog2e : 0.f;
         const float dval = valid ? a.dsum[st_idx] : 0.f;
-        const float sl2 = a.scale_log2;
+        // fp16 path: undo 2^(q+k) on S; dS = P (dP - D) carries 2^ds
+        int eq = 0, ek = 0, ev = 0, edo = 0;
+        if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
+        const int eds = F16 ? ld_once(&a.f16s->ds) : 0;
+        const float sl2 = a.scale_log2 * pow2f(-(eq + ek));
+        const float dsc = pow2f(eds);
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
         const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(nlse2, nlse2);
-        const uint64_t ndx2 = f2(-dval, -dval);
+        const uint64_t ndx2 = f2(-dval * dsc, -dval * dsc), dsc2 = f2(dsc, dsc);
         bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
             if (!(ok = mbar_wait(BAR_SDF, j & 1, a.status, a.timeout_ns, 26))) break;
@@ -271,10 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p0 = (kbase + c > lim) ? 0.f : p0;
                     p1 = (kbase + c + 1 > lim) ? 0.f : p1;
                 }
-                const uint64_t t = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndx2);
+                const uint64_t t =
+                    fma2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), dsc2, ndx2);
                 float d0, d1;
                 f2_split(mul2(f2(p0, p1), t), d0, d1);
-                pk[c >> 1] = pack_bf16(d0, d1);
+                pk[c >> 1] = pack_op<F16>(d0, d1);
             }
             tmem_st32(tDP, pk);  // dS over the first 32 of this half's dP columns
             tmem_wait_st();
@@ -286,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // dQ = scale * (dS K): each warpgroup stages half of the d columns into
             // the Q tile's shared memory (no MMA reads Q any more)
-            stage_rows_bf16<C::CHUNK>(tbase + C::TM_DQ + lane_off, sQ, r, hf * (D / 2),
-                                      (hf + 1) * (D / 2), a.scale);
+            stage_rows_bf16<C::CHUNK>(
+                tbase + C::TM_DQ + lane_off, sQ, r, hf * (D / 2), (hf + 1) * (D / 2),
+                a.scale * pow2f(-(eds + ek)));
             fence_proxy_async_smem();
         }
         named_bar_sync(1, 256);
@@ -309,16 +321,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D>
-cudaError_t launch_bwd_dq(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
-    auto kern = fa_bwd_dq_kernel<D>;
+template <int D, bool F16>
+cudaError_t launch_dq(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
+    auto kern = fa_bwd_dq_kernel<D, F16>;
     constexpr int smem = DqCfg<D>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long nblk = static_cast<long long>((a.N + kBM - 1) / kBM) * a.B * a.Hq;
     if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(nblk), kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dq, a);
+    kern<<<static_cast<unsigned>(nblk), kThreads, smem, st>>>(F16 ? m.q16 : m.q, F16 ? m.k16 : m.k,
+                                                            m.v, m.dout, m.dq, a);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_dq(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
+    return a.f16s ? launch_dq<D, true>(m, a, st) : launch_dq<D, false>(m, a, st);
 }
 
 template cudaError_t launch_bwd_dq<64>(const BwdMaps&, const BwdArgs&, cudaStream_t);

@@ -68,7 +68,9 @@ constexpr int kWarpGate = 10;
 // units), so unnormalised P values stay below 256.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+// F16: P is rounded to fp16 (not bf16) and multiplies the fp16 copy of V,
+// scaled by 2^v (the training forward, whose O feeds the backward's D).
+template <int D, bool F16>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(384, 1)
         // ================= MMA issuer (one thread) =================
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
-            constexpr uint32_t IDESC_PV = idesc_bf16(kBM, D, false, true);
+            constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t dS = tbase + C::TM_S + t * kBN;
 #pragma unroll
@@ -273,6 +275,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tS = tbase + C::TM_S + t * kBN + lane_off;
         const uint32_t tO = tbase + C::TM_O + t * D + lane_off;
         const float sl2 = a.scale_log2;
+        int eq = 0, ek = 0, ev = 0, edo = 0;  // fp16 path: O carries 2^ev
+        if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
         // last key index this row may see
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
         float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
@@ -327,7 +331,7 @@ __global__ void __launch_bounds__(384, 1)
                     f2_split(fma2(f2(x[half * 64 + c], x[half * 64 + c + 1]), sl2x2, negx2), e0, e1);
                     const float p0 = ex2(e0), p1 = ex2(e1);
                     ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
-                    pk[c >> 1] = pack_bf16(p0, p1);
+                    pk[c >> 1] = pack_op<F16>(p0, p1);
                 }
                 tmem_st32(tS + half * 32, pk);
             }
@@ -366,7 +370,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t stage = sQ + t * C::TILE;
         if (ok_e) {
             tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            // O was accumulated against V * 2^v on the fp16 path
+            const float inv_l = (l > 0.f) ? pow2f(-ev) / l : 0.f;
 #pragma unroll
             for (int cb = 0; cb < D; cb += 32) {
                 uint32_t o[32];
@@ -422,10 +427,10 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D>;
+    auto kern = fa_fwd_kernel<D, F16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -438,8 +443,11 @@ cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdArgs& args, int d, cudaStream_t stream) {
-    if (d == 64) return launch_fwd_d<64>(maps, args, stream);
-    if (d == 128) return launch_fwd_d<128>(maps, args, stream);
+    const bool f16 = args.f16s != nullptr;
+    if (d == 64) return f16 ? launch_fwd_d<64, true>(maps, args, stream)
+                            : launch_fwd_d<64, false>(maps, args, stream);
+    if (d == 128) return f16 ? launch_fwd_d<128, true>(maps, args, stream)
+                             : launch_fwd_d<128, false>(maps, args, stream);
     return cudaErrorInvalidValue;
 }
 

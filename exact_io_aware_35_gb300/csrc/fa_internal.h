@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Default bound on any single in-kernel wait (ns).  No legitimate wait comes
@@ -17,9 +19,66 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 
+// fp16 operand path.  bf16 inputs are copied to fp16 after a power-of-two
+// scaling that puts each tensor's largest magnitude just under 2^15, so the
+// copy is exact for every element above max * 2^-24 (bf16 carries 8
+// significant bits, fp16 11); P, P^T (at most 2^8) and dS, dS^T (scaled by
+// the power of two that puts the bound 2 d max|dO| max|V| under 2^15) are
+// then rounded to fp16 instead of bf16 before they feed an MMA: 3 more bits
+// on the operands whose rounding the outputs amplify.  The scalings are
+// undone exactly in the kernels' epilogues (or folded into scale * log2 e).
+struct F16Scales {
+    int q, k, v, dout;  // x16 = fp16(x * 2^s) for the four operand tensors
+    int ds;             // dS16 = fp16(dS * 2^ds)
+};
+
+// One fp16-copy job: up to four tensors (slots q, k, v, dout; n = 0 skips a
+// slot).  absmax (4 words, zeroed before the job) and scales live in device
+// memory.
+struct F16Prep {
+    const uint16_t* src[4];
+    uint16_t* dst[4];
+    size_t n[4];  // elements, multiples of 8
+    uint32_t* absmax;
+    F16Scales* scales;
+    int d;
+    int convert_mask;  // slots to copy (the maxima are taken for every slot with n > 0);
+                       // 0: maxima only, a later kernel copies and writes the scales
+};
+
+cudaError_t launch_f16_prep(const F16Prep& p, cudaStream_t stream);
+
+// 15 - ceil(log2 a) for a > 0 given as float bits, clamped to [-40, 40] so
+// that every sum of three exponents the kernels form stays a normal power of
+// two; 0 for a == 0 or a non-finite maximum (the copy then carries the
+// inf/NaN just as the bf16 path would).  So the copies are exact for tensors
+// whose largest magnitude lies in [2^-25, 2^55].
+__device__ __forceinline__ int f16_exp_to_2p15(uint32_t bits) {
+    if (bits == 0u || bits >= 0x7f800000u) return 0;
+    const int E = static_cast<int>(bits >> 23);
+    const int e = (E == 0) ? -126 : (E - 127 + ((bits & 0x7fffffu) ? 1 : 0));
+    return max(-40, min(40, 15 - e));
+}
+
+// The scales of a job from the maxima of q, k, v, dout (float bits).
+__device__ __forceinline__ F16Scales f16_scales_from(const uint32_t* absmax, int d) {
+    F16Scales s;
+    s.q = f16_exp_to_2p15(absmax[0]);
+    s.k = f16_exp_to_2p15(absmax[1]);
+    s.v = f16_exp_to_2p15(absmax[2]);
+    s.dout = f16_exp_to_2p15(absmax[3]);
+    // |dS| = |P (dP - D)| <= 2 max|dP| <= 2 d max|dO| max|V|
+    const float bound = 2.f * static_cast<float>(d) * __uint_as_float(absmax[3]) *
+                        __uint_as_float(absmax[2]);
+    s.ds = f16_exp_to_2p15(__float_as_uint(bound));
+    return s;
+}
+
+
 struct FwdArgs {
     float* lse;          // [B, Hq, N]
     uint16_t* o_lo;      // [B, N, Hq, d] bf16 low half of O, or null
+    const F16Scales* f16s;  // non-null: P and V enter O += P V in fp16 (V map = fp16 copy)
     uint32_t* status;    // device status word
     int B, Hq, Hkv, N, g;
     int causal;
@@ -34,6 +93,12 @@ struct BwdArgs {
     const uint16_t* o;   // [B, N, Hq, d] bf16
     const uint16_t* dout;
     const uint16_t* o_lo;  // optional low half of O (null: D from o alone)
+    const F16Scales* f16s;  // non-null: fp16 operand path (maps *16 are the fp16 copies)
+    // non-null: the dsum kernel also writes dout16 = fp16(dout * 2^s) and the
+    // scales (the maxima are in absmax)
+    uint16_t* dout16;
+    const uint32_t* absmax;
+    F16Scales* scales_w;
     uint32_t* status;
     int B, Hq, Hkv, N, d, g;
     int causal;
@@ -49,6 +114,7 @@ struct FwdMaps {
 
 struct BwdMaps {
     CUtensorMap q, k, v, dout, dq, dk, dv;
+    CUtensorMap q16, k16, v16, dout16;  // fp16 copies (fp16 operand path only)
 };
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdArgs& args, int d, cudaStream_t stream);
@@ -57,6 +123,14 @@ template <int D>
 cudaError_t launch_bwd_dkdv(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream);
 template <int D>
 cudaError_t launch_bwd_dq(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream);
+
+// The backward behind fa_bwd_stage and fa_bwd_noalloc.  dsum: D workspace;
+// f16_ws: a workspace laid out as fa_bwd_workspace_size describes (fp16
+// operand path), or null for the bf16 path.  stages: FA_BWD_* bits.
+fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, float* dsum,
+                  void* f16_ws, const void* o_lo, int B, int H, int Hkv, int N, int d, int causal,
+                  float scale, void* stream);
 
 // stages: bit 0 dsum, bit 1 dK/dV, bit 2 dQ (run in that order)
 cudaError_t launch_bwd(const BwdMaps& maps, const BwdArgs& args, int stages, cudaStream_t stream);

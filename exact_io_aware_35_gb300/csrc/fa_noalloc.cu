@@ -65,6 +65,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     const fa_status st = fa::noalloc_scratch(&scratch);
     if (st != FA_OK) return st;
     // D needs no clearing: the first stage writes every entry the later two read.
-    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, o_lo, B, H, Hkv, N, d, causal,
-                  scale, stream);
+    // No fp16 operand copies (they would need B*N*(2H + 2Hkv)*d*2 more bytes):
+    // the bf16 operand path.
+    return fa::bwd_run(FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, q, k, v, o, dout, lse, dq, dk, dv,
+                       scratch, nullptr, o_lo, B, H, Hkv, N, d, causal, scale, stream);
 }

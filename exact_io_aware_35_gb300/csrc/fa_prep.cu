@@ -1,0 +1,82 @@
+// fa_prep.cu -- fp16 copies of the MMA operand tensors, scaled by powers of two.
+//
+// Two launches per job (up to four tensors, blockIdx.y picks one): the first
+// takes max |x| of each tensor (atomicMax on the float bit pattern, which
+// orders non-negative floats like integers), the second turns the maxima into
+// F16Scales and writes fp16(x * 2^s).  Both are HBM-bound grid-stride loops
+// over 16-byte vectors (8 elements).  The exponent puts max |x| * 2^s in
+// (2^14, 2^15], so every element at or above max * 2^-24 converts exactly;
+// smaller ones round at 2^-24 of the maximum.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) f16_absmax_kernel(const F16Prep p) {
+    const int t = blockIdx.y;
+    const size_t n8 = p.n[t] / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(p.src[t]);
+    uint32_t m = 0;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = src[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // |x| of each bf16 half as the bits of an fp32 value
+            m = max(m, (w[j] & 0x7fffu) << 16);
+            m = max(m, w[j] & 0x7fff0000u);
+        }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(p.absmax + t, m);
+}
+
+__global__ void __launch_bounds__(kPrepThreads) f16_convert_kernel(const F16Prep p) {
+    const int t = blockIdx.y;
+    const F16Scales s = f16_scales_from(p.absmax, p.d);
+    if (blockIdx.x == 0 && t == 0 && threadIdx.x == 0) *p.scales = s;
+    const int e = (t == 0) ? s.q : (t == 1) ? s.k : (t == 2) ? s.v : s.dout;
+    const float mul = pow2f(e);
+    const size_t n8 = ((p.convert_mask >> t) & 1) ? p.n[t] / 8 : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(p.src[t]);
+    uint4* dst = reinterpret_cast<uint4*>(p.dst[t]);
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = src[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = pack_f16(__uint_as_float(w[j] << 16) * mul,
+                            __uint_as_float(w[j] & 0xffff0000u) * mul);
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_f16_prep(const F16Prep& p, cudaStream_t st) {
+    size_t nmax = 0;
+    for (int t = 0; t < 4; ++t) nmax = p.n[t] > nmax ? p.n[t] : nmax;
+    // enough blocks to fill the GPU several times over, at most one vector per thread
+    const size_t want = (nmax / 8 + kPrepThreads - 1) / kPrepThreads;
+    const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
+    // only the maxima of the tensors in this job start over: a job that copies
+    // dout alone keeps the q, k, v maxima an earlier job left (the scales are
+    // always recomputed from all four)
+    cudaError_t e = cudaSuccess;
+    for (int t = 0; t < 4 && e == cudaSuccess; ++t)
+        if (p.n[t] > 0) e = cudaMemsetAsync(p.absmax + t, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    f16_absmax_kernel<<<dim3(gx, 4), kPrepThreads, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.convert_mask == 0) return cudaSuccess;  // a later kernel converts and writes the scales
+    f16_convert_kernel<<<dim3(gx, 4), kPrepThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

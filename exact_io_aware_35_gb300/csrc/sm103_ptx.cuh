@@ -247,6 +247,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
            ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same with A and B in fp16 (a/b format fields 0) when f16, else bf16.
+__host__ __device__ constexpr uint32_t idesc_16(uint32_t M, uint32_t N, bool a_mn, bool b_mn,
+                                                bool f16) {
+    return f16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10)))
+               : idesc_bf16(M, N, a_mn, b_mn);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
 //   offset >> 4, 46-47 version (1), 49-51 base offset (0: atoms 1024-aligned),
@@ -399,6 +406,37 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// An MMA operand pair (lo in bits 0..15): fp16 when F16, else bf16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_op(float lo, float hi) {
+    return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+
+// Load ints once, with a volatile load: the compiler must keep the
+// values in registers instead of re-reading them inside a later loop (a
+// re-read on the softmax warps' critical path cost 4% of a kernel).
+__device__ __forceinline__ void ld_once_v4(const int* p, int& a, int& b, int& c, int& d) {
+    asm volatile("ld.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "l"(p));
+}
+__device__ __forceinline__ int ld_once(const int* p) {
+    int a;
+    asm volatile("ld.global.s32 %0, [%1];" : "=r"(a) : "l"(p));
+    return a;
+}
+
+// 2^e as a float, for e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2f(int e) {
+    return __int_as_float((127 + e) << 23);
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic): lo in bits 0..31.

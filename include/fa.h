@@ -37,8 +37,20 @@
  *  - d must be 64 or 128.  N >= 1 with no other restriction (ragged tails are
  *    masked).  B, Hq, Hkv >= 1.
  *  - All pointers are DEVICE pointers on the current CUDA device, 16-byte
- *    aligned.  The caller owns every buffer; the library allocates no device
- *    memory in these calls and keeps no pointer after a call returns.
+ *    aligned (workspaces: 256-byte aligned).  The caller owns every buffer;
+ *    the library allocates no device memory in these calls and keeps no
+ *    pointer after a call returns.
+ *  - Operand precision.  Every product is accumulated in fp32.  The scores
+ *    S = Q K^T (forward) use the bf16 inputs as given.  Where a rounded
+ *    intermediate feeds a product -- P in O += P V, and P, dS in the
+ *    backward's dV, dK, dQ products -- the training forward and fa_bwd round
+ *    it to fp16 and multiply it with an fp16 copy of the other operand (the
+ *    bf16 inputs scaled by a power of two chosen from the tensor's largest
+ *    magnitude, which makes the copy exact for every element above 2^-24 of
+ *    that maximum, for maxima in [2^-25, 2^55]; the scaling is undone
+ *    exactly).  fp16 keeps 3 more bits than bf16, which the peaked-row
+ *    near-cancellation dS = P o (dP - D) needs.  fa_fwd (inference) and
+ *    fa_bwd_noalloc round those intermediates to bf16 instead.
  *  - stream is a cudaStream_t (CUstream) handle, or NULL for the legacy
  *    default stream.  Calls enqueue work on it and return without waiting.
  *  - Errors: argument errors are detected on the host before any launch and
@@ -83,25 +95,33 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream);
 
 /*
- * Forward pass for training: fa_fwd plus the low half of O.
- *   o_lo [B, N, Hq, d] bf16 out: bf16(O32 - O), where O32 is the fp32 output
- *        before rounding and O the bf16 value written to `o`.  o + o_lo carries
- *        O to about 16 significant bits.
- * fa_bwd forms D_i = sum_c dO_ic O_ic from o + o_lo when given it.  That
- * matters when rows are peaked: there dS = P o (dP - D) is a near-cancellation
- * and the rounding of O to bf16 alone moves dQ by more than the bf16
- * rounding of the gradients themselves.  Same arguments and errors as fa_fwd.
+ * Forward pass for training: fa_fwd plus the low half of O, with P rounded
+ * to fp16 for the P V product.
+ *   o_lo [B, N, Hq, d] bf16 out (or NULL): bf16(O32 - O), where O32 is the
+ *        fp32 output before rounding and O the bf16 value written to `o`.
+ *        o + o_lo carries O to about 16 significant bits.
+ *   workspace: the training workspace, fa_bwd_workspace_size(B, H, Hkv, N, d)
+ *        bytes, 256-byte aligned, caller-owned, contents irrelevant on entry;
+ *        NULL rounds P to bf16 as fa_fwd does.  The call leaves the fp16
+ *        copies of q, k, v (and their scales) in it, so that a backward on the
+ *        same workspace and the same q, k, v need only copy dout
+ *        (fa_bwd_stage with FA_BWD_PREP_DOUT instead of FA_BWD_PREP).
+ * fa_bwd forms D_i = sum_c dO_ic O_ic from o + o_lo when given it.  Both
+ * matter when rows are peaked: there dS = P o (dP - D) is a near-cancellation
+ * and the roundings of P and of O alone move dQ by more than the rounding of
+ * the gradients themselves.  Other arguments and errors as fa_fwd.
  */
 fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, void* o_lo,
-                       float* lse, int B, int H, int Hkv, int N, int d, int causal,
-                       float scale, void* stream);
+                       float* lse, void* workspace, int B, int H, int Hkv, int N, int d,
+                       int causal, float scale, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: one fp32 per query row and head
- * (D_i = sum_c dO_ic * O_ic), i.e. 4 * B * H * N, rounded up to 256.
- * Returns 0 for invalid sizes.
+ * Bytes of the training workspace (fa_fwd_train, fa_bwd): one fp32 per query row and head
+ * (D_i = sum_c dO_ic * O_ic, 4 * B * H * N bytes), the fp16 copies of q, k,
+ * v, dout (2 * B * N * (2 * H + 2 * Hkv) * d bytes) and 512 bytes of scale
+ * data, each part rounded up to 256.  Returns 0 for invalid sizes.
  */
-size_t fa_bwd_workspace_size(int B, int H, int N);
+size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
 
 /*
  * Backward pass of the loss L with dL/dO = dout.
@@ -113,9 +133,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N);
  *   dq   [B, N, Hq, d]  bf16 out
  *   dk   [B, N, Hkv, d] bf16 out (summed over the Hq/Hkv query heads of a group)
  *   dv   [B, N, Hkv, d] bf16 out (same)
- *   workspace: device buffer of at least fa_bwd_workspace_size(B, H, N)
- *              bytes, 256-byte aligned, owned by the caller; its contents on
- *              entry do not matter and are overwritten.
+ *   workspace: device buffer of at least fa_bwd_workspace_size(B, H, Hkv,
+ *              N, d) bytes, 256-byte aligned, owned by the caller; its
+ *              contents on entry do not matter and are overwritten.
  * S and P are recomputed from q, k and lse ("FlashAttention Kernel",
  * recomputation bullets).  Every output element is written by exactly one
  * thread block; no atomics, so results are deterministic.
@@ -126,16 +146,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, void* stream);
 
 /*
- * The three kernels of fa_bwd, callable one at a time (e.g. to time them).
- * `stages` is a bitmask of FA_BWD_DSUM (D = rowsum(dout * o) into the
- * workspace), FA_BWD_DKDV (dk, dv) and FA_BWD_DQ (dq); set stages run in that
- * order.  DKDV and DQ read the D that a DSUM stage wrote into the same
- * workspace earlier on the stream.  fa_bwd(...) is
- * fa_bwd_stage(FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, ...).  Arguments,
- * ownership and errors are those of fa_bwd; pointers a stage does not read
- * or write must still be valid (they are checked, not dereferenced).
+ * The steps of fa_bwd, callable one at a time (e.g. to time them).  `stages`
+ * is a bitmask of FA_BWD_PREP (the fp16 copies of q, k, v, dout and their
+ * scales into the workspace), FA_BWD_PREP_DOUT (the copy of dout only: the
+ * workspace must hold fa_fwd_train's copies of the same q, k, v),
+ * FA_BWD_DSUM (D = rowsum(dout * o) into the workspace), FA_BWD_DKDV (dk, dv)
+ * and FA_BWD_DQ (dq); set stages run in the order PREP(_DOUT), DSUM, DKDV,
+ * DQ.  DKDV and DQ read what the earlier stages wrote into the same workspace
+ * earlier on the stream.  fa_bwd(...) is
+ * fa_bwd_stage(FA_BWD_PREP | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, ...); a
+ * training step that ran fa_fwd_train on the workspace can use
+ * FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ.
+ * Arguments, ownership and errors are those of fa_bwd; pointers a stage does
+ * not read or write must still be valid (they are checked, not dereferenced).
  */
-enum { FA_BWD_DSUM = 1, FA_BWD_DKDV = 2, FA_BWD_DQ = 4 };
+enum { FA_BWD_DSUM = 1, FA_BWD_DKDV = 2, FA_BWD_DQ = 4, FA_BWD_PREP = 8, FA_BWD_PREP_DOUT = 16 };
 fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
                        void* workspace, const void* o_lo, int B, int H, int Hkv, int N, int d,
@@ -146,7 +171,9 @@ fa_status fa_bwd_stage(int stages, const void* q, const void* k, const void* v, 
  * device memory: a plug-in inside a host application that owns every device
  * allocation, or a loop that must not call cudaMalloc mid-step.  (The pages
  * have no counterpart; this is a library convenience.)
- *   Arguments, outputs and errors are those of fa_bwd minus `workspace`.
+ *   Arguments, outputs and errors are those of fa_bwd minus `workspace`,
+ *   except that P and dS are rounded to bf16, not fp16, before their
+ *   products (there is no room for fp16 operand copies).
  *   D lives in a fixed array built into the library: 2^21 fp32 rows (8 MiB),
  *   held on every GPU that loads the library until the process exits.  Calls
  *   with B * H * N > 2^21 return FA_ERR_INVALID_ARG (with a message on

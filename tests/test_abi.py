@@ -45,10 +45,21 @@ def test_status_strings(lib):
     assert fa.status_string(99) == "FA_ERR_UNKNOWN"
 
 
+def _up256(x):
+    return (x + 255) // 256 * 256
+
+
 def test_workspace_size(lib):
-    assert lib.fa_bwd_workspace_size(2, 3, 5) == 256  # 120 bytes rounded up
-    assert lib.fa_bwd_workspace_size(4, 32, 8192) == 4 * 4 * 32 * 8192
-    assert lib.fa_bwd_workspace_size(0, 1, 1) == 0
+    # D (4 bytes per query row and head), fp16 copies of q, k, v, dout, 512 bytes of scales
+    def bwd(B, H, Hkv, N, d):
+        return (_up256(4 * B * H * N) + 2 * _up256(2 * B * N * H * d) +
+                2 * _up256(2 * B * N * Hkv * d) + 512)
+    assert lib.fa_bwd_workspace_size(2, 3, 1, 5, 64) == bwd(2, 3, 1, 5, 64) == 11008
+    assert lib.fa_bwd_workspace_size(4, 32, 8, 8192, 128) == bwd(4, 32, 8, 8192, 128)
+    assert lib.fa_bwd_workspace_size(0, 1, 1, 1, 64) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 1, 1, 96) == 0     # unsupported d
+    assert lib.fa_bwd_workspace_size(1, 6, 4, 1, 64) == 0     # Hq % Hkv != 0
+
 
 
 def _fwd(lib, ptr=16, B=1, H=1, Hkv=1, N=128, d=64, causal=0, scale=0.125):
@@ -77,9 +88,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert _bwd(lib, ws=272) == fa.FA_ERR_INVALID_ARG         # workspace not 256-aligned
     assert _bwd(lib, o_lo=8) == fa.FA_ERR_INVALID_ARG         # o_lo misaligned
     assert _bwd(lib, d=80) == fa.FA_ERR_UNSUPPORTED
-    assert lib.fa_fwd_train(16, 16, 16, 16, 8, 16, 1, 1, 1, 128, 64, 0, ctypes.c_float(0.125),
-                            None) == fa.FA_ERR_INVALID_ARG
-    for stages in (0, 8, -1):
+    assert lib.fa_fwd_train(16, 16, 16, 16, 8, 16, None, 1, 1, 1, 128, 64, 0,
+                            ctypes.c_float(0.125), None) == fa.FA_ERR_INVALID_ARG  # o_lo
+    assert lib.fa_fwd_train(16, 16, 16, 16, 16, 16, 272, 1, 1, 1, 128, 64, 0,
+                            ctypes.c_float(0.125), None) == fa.FA_ERR_INVALID_ARG  # workspace
+    for stages in (0, 32, -1):
         assert lib.fa_bwd_stage(stages, 256, 256, 256, 256, 256, 256, 256, 256, 256, 256, None,
                                 1, 1, 1, 128, 64, 0, ctypes.c_float(0.125),
                                 None) == fa.FA_ERR_INVALID_ARG
