@@ -8,15 +8,18 @@
 // bullet; the gradient formulas are the derivative of the forward definition).
 //
 // Pipelining.  Every MMA is 128 wide.  dP is double-buffered in TMEM and S is
-// not: as soon as both warpgroups have copied S(j) and dP(j) into registers,
-// the tensor core computes S(j+1) into the S buffer, and the warpgroups write
-// dS(j) (bf16) over the dP(j) columns they read.  dQ += dS(j) K_j then reads
-// it from there, and dP(j+2) is written over it.  dP(j+1) was computed a block
-// earlier, so the warpgroups go from block j to block j+1 without waiting for
-// the tensor core, which runs S(j+1), dQ(j) and dP(j+2) meanwhile.  Warpgroup
-// h takes keys 64h..64h+63 of every block.  K and V stream through separate
-// TMA rings in the order the MMAs first use them (K_0, V_0, V_1, K_1, V_2,
-// K_2, ...).
+// not: as soon as both warpgroups have copied S(j) and dP(j) into registers
+// (barrier LD), the tensor core computes S(j+1) into the S buffer and dP(j+1)
+// into the other dP buffer, while the warpgroups write dS(j) (bf16 or fp16)
+// over the dP(j) columns they read.  dQ += dS(j) K_j then reads it from there
+// (barrier PF).  The warpgroups go from block j to block j+1 without waiting
+// for the tensor core, which runs S(j+1), dP(j+1) and dQ(j) meanwhile.
+// Warpgroup h takes keys 64h..64h+63 of every block.  K and V stream through
+// separate TMA rings; a gate warp adds one arrival to LD(j) once K_{j+1} and
+// V_{j+1} have landed, so the MMA thread waits on LD and PF only (every wait
+// in the issuing thread costs tensor-core time).  Only LD carries the gate:
+// the warpgroups reach LD(j+1) only after S(j+1), which waits for LD(j), so no
+// arrival can land in the wrong phase.
 //
 // TMEM (512 columns): S [0,128), dP0 [128,256), dP1 [256,384), dQ [384,384+D).
 #include "fa_bwd_common.cuh"
@@ -30,7 +33,7 @@ template <int D>
 struct DqCfg : Tiles<D> {
     using T = Tiles<D>;
     static constexpr int KS = 3;  // K ring slots: K_j (dQ), K_{j+1} (S), one ahead
-    static constexpr int VS = 2;  // V ring slots: V_{j+2} (dP), one ahead
+    static constexpr int VS = 2;  // V ring slots: V_{j+1} (dP), one ahead
     static constexpr int OFF_K = 2 * T::TILE;  // after Q, dO
     static constexpr int OFF_V = OFF_K + KS * T::TILE;
     static constexpr int OFF_BAR = OFF_V + VS * T::TILE;
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR_VE(s), 1);
         }
         mbar_init(BAR_SDF, 1);
-        mbar_init(BAR_LD, 256);
+        mbar_init(BAR_LD, 256 + 1);  // compute threads and the gate
         mbar_init(BAR_PF, 256);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
@@ -145,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     last_k[slot] = jj;
                 return true;
             };
-            // first-use order of the MMAs: K_0, V_0, then V_i, K_i
-            bool ok = load(0, false) && load(0, true);
-            for (int i = 1; i < nj && ok; ++i) ok = load(i, true) && load(i, false);
+            // first-use order of the MMAs: K_0, V_0, K_1, V_1, ...
+            bool ok = true;
+            for (int i = 0; i < nj && ok; ++i) ok = load(i, false) && load(i, true);
             // no copies in flight at exit: wait (bounded) for the last load of each slot
             mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 21);
             for (int s = 0; s < C::KS; ++s)
@@ -156,6 +159,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < C::VS; ++s)
                 if (last_v[s] >= 0)
                     mbar_wait(BAR_VF(s), (last_v[s] / C::VS) & 1, a.status, a.timeout_ns, 21);
+        }
+        __syncwarp();
+    } else if (warp == kWarpGate) {
+        // ================= gate: K_{j+1}, V_{j+1} landed -> LD(j) =================
+        // Its arrival on LD(j) comes only after LD's previous phase is over.
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < nj && ok; ++j) {
+                if (j + 1 < nj)
+                    ok = mbar_wait(BAR_KF((j + 1) % C::KS), ((j + 1) / C::KS) & 1, a.status,
+                                   a.timeout_ns, 28) &&
+                         mbar_wait(BAR_VF((j + 1) % C::VS), ((j + 1) / C::VS) & 1, a.status,
+                                   a.timeout_ns, 28);
+                if (ok && j > 0) ok = mbar_wait(BAR_LD, (j - 1) & 1, a.status, a.timeout_ns, 28);
+                if (ok) mbar_arrive(BAR_LD);
+            }
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -171,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return r;
             };
-            auto v_ready = [&](int jj) {
+            auto v_ready = [&](int jj) {  // (prologue only; the gate covers the loop)
                 const bool r = mbar_wait(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.status,
                                          a.timeout_ns, 23);
                 tc_fence_after();
@@ -208,24 +227,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_dp(0);
                 mma_commit(BAR_SDF);
             }
-            if (ok && nj > 1 && (ok = v_ready(1))) issue_dp(1);
             for (int j = 0; j < nj && ok; ++j) {
-                // S(j+1) into the S buffer once both warpgroups hold S(j); the
-                // commit also covers dP(j+1), issued a block earlier
+                // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j);
+                // dP(j+1) into the other dP buffer, over dS(j-1), which dQ(j-1)
+                // (issued earlier by this thread) has read; K_{j+1} and V_{j+1}
+                // have landed (the gate's arrival on LD)
                 if (j + 1 < nj) {
                     if (!(ok = mbar_wait(BAR_LD, j & 1, a.status, a.timeout_ns, 24))) break;
-                    if (!(ok = k_ready(j + 1))) break;
+                    tc_fence_after();
                     issue_t(tS, sQ, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
+                    issue_dp(j + 1);
                     mma_commit(BAR_SDF);
                 }
                 if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 24))) break;
                 tc_fence_after();
                 issue_dq(j);
-                // dP(j+2) over dS(j): the dQ products above read it first
-                if (j + 2 < nj) {
-                    if (!(ok = v_ready(j + 2))) break;
-                    issue_dp(j + 2);
-                }
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
