@@ -15,22 +15,30 @@ namespace {
 
 constexpr int kPrepThreads = 256;
 
+__device__ __forceinline__ uint32_t absmax8(uint4 v, uint32_t m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // |x| of each bf16 half as the bits of an fp32 value
+        m = max(m, (w[j] & 0x7fffu) << 16);
+        m = max(m, w[j] & 0x7fff0000u);
+    }
+    return m;
+}
+
 __global__ void __launch_bounds__(kPrepThreads) f16_absmax_kernel(const F16Prep p) {
     const int t = blockIdx.y;
     const size_t n8 = p.n[t] / 8;
     const uint4* src = reinterpret_cast<const uint4*>(p.src[t]);
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     uint32_t m = 0;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const uint4 v = src[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // |x| of each bf16 half as the bits of an fp32 value
-            m = max(m, (w[j] & 0x7fffu) << 16);
-            m = max(m, w[j] & 0x7fff0000u);
-        }
+    // four independent 16-byte loads in flight per thread
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        m = absmax8(d, absmax8(c, absmax8(b, absmax8(a, m))));
     }
+    for (; i < n8; i += stride) m = absmax8(src[i], m);
     m = __reduce_max_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(p.absmax + t, m);
 }
@@ -44,17 +52,24 @@ __global__ void __launch_bounds__(kPrepThreads) f16_convert_kernel(const F16Prep
     const size_t n8 = ((p.convert_mask >> t) & 1) ? p.n[t] / 8 : 0;
     const uint4* src = reinterpret_cast<const uint4*>(p.src[t]);
     uint4* dst = reinterpret_cast<uint4*>(p.dst[t]);
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const uint4 v = src[i];
+    auto cvt8 = [&](uint4 v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             o[j] = pack_f16(__uint_as_float(w[j] << 16) * mul,
                             __uint_as_float(w[j] & 0xffff0000u) * mul);
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // two independent 16-byte loads in flight per thread
+    for (; i + stride < n8; i += 2 * stride) {
+        const uint4 a = src[i], b = src[i + stride];
+        dst[i] = cvt8(a);
+        dst[i + stride] = cvt8(b);
     }
+    for (; i < n8; i += stride) dst[i] = cvt8(src[i]);
 }
 
 }  // namespace
@@ -62,9 +77,9 @@ __global__ void __launch_bounds__(kPrepThreads) f16_convert_kernel(const F16Prep
 cudaError_t launch_f16_prep(const F16Prep& p, cudaStream_t st) {
     size_t nmax = 0;
     for (int t = 0; t < 4; ++t) nmax = p.n[t] > nmax ? p.n[t] : nmax;
-    // enough blocks to fill the GPU several times over, at most one vector per thread
+    // up to 8 blocks per SM of this GPU's 152 (grid-stride loops cover the rest)
     const size_t want = (nmax / 8 + kPrepThreads - 1) / kPrepThreads;
-    const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
+    const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 1216 ? 1216 : want));
     // only the maxima of the tensors in this job start over: a job that copies
     // dout alone keeps the q, k, v maxima an earlier job left (the scales are
     // always recomputed from all four)
