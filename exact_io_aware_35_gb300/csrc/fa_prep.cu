@@ -33,12 +33,16 @@ __global__ void __launch_bounds__(kPrepThreads) f16_absmax_kernel(const F16Prep 
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     uint32_t m = 0;
-    // four independent 16-byte loads in flight per thread
+    // Back to front (element n8-1-i), four independent 16-byte loads in flight
+    // per thread: the front of the tensor is then what L2 holds when the copy
+    // (or the D kernel) reads it front to back right after.
+    const uint4* end = src + n8 - 1;
     for (; i + 3 * stride < n8; i += 4 * stride) {
-        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        const uint4 a = *(end - i), b = *(end - i - stride), c = *(end - i - 2 * stride),
+                    d = *(end - i - 3 * stride);
         m = absmax8(d, absmax8(c, absmax8(b, absmax8(a, m))));
     }
-    for (; i < n8; i += stride) m = absmax8(src[i], m);
+    for (; i < n8; i += stride) m = absmax8(*(end - i), m);
     m = __reduce_max_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(p.absmax + t, m);
 }
