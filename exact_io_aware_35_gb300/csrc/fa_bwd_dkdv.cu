@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         }
         const uint64_t pol_q = l2_policy_evict_last();
         int last_it[C::NST] = {-1, -1};
+        // fp16 path: D is staged times 2^ds, the scale of dP^T (V dO^T of the
+        // copies carries exactly 2^ds: the copy of dO is scaled by ds - v)
+        const float dsc = F16 ? pow2f(ld_once(&a.f16s->ds)) : 1.f;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::NST;
             const int hq = hk * a.g + it / nqi;
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const int q = qi * kBM + lane * 4 + u;
                 // a query row past N contributes nothing: P = exp2(-inf) = 0
                 lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
-                dv4[u] = (q < a.N) ? a.dsum[base + q] : 0.f;
+                dv4[u] = (q < a.N) ? a.dsum[base + q] * dsc : 0.f;
             }
             if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.status, a.timeout_ns, 30)) break;
             if (lane == 0) {
@@ -254,15 +257,16 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         // 8j + 2(lane%4) + {0,1} of the warpgroup's 32: so it needs only 8
         // entries of the query-indexed vectors lse2 and D.
         const int key0 = jb * kBN + (warp & 3) * 32 + (lane >> 2);
-        // fp16 path: undo 2^(q+k) on S^T; dS^T = P^T (dP^T 2^u - D 2^ds) with
-        // u = ds - v - dout, so that dS^T carries exactly 2^ds
+        // fp16 path: undo 2^(q+k) on S^T; dP^T and the staged D both carry
+        // 2^ds, so dS^T = P^T (dP^T - D) does too
         int eq = 0, ek = 0, ev = 0, edo = 0;
         if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
         const int eds = F16 ? ld_once(&a.f16s->ds) : 0;
         const float sl2 = a.scale_log2 * pow2f(-(eq + ek));
-        const float dsc = pow2f(eds);
-        const float dpu = pow2f(eds - ev - edo);
-        const uint64_t dpu2 = f2(dpu, dpu);
+        // the epilogue factor, formed here so the exponents die before the loop:
+        // dV carries 2^dout, dK scale * 2^(ds+q) on the fp16 path
+        const int which = wg >> 1, half = wg & 1;
+        const float mul_e = which ? a.scale * pow2f(-(eds + eq)) : pow2f(-edo);
         const uint64_t sl2x2 = f2(sl2, sl2);
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
                 const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
                 nl[j] = f2(-l2.x, -l2.y);
-                nd[j] = f2(-d2.x * dsc, -d2.y * dsc);
+                nd[j] = f2(-d2.x, -d2.y);
             }
             tmem_wait_ld();
             reg_fence<16>(dp[0]);
@@ -319,8 +323,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         }
                         float e0, e1;
                         f2_split(mul2(f2(p0, p1),
-                                      fma2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
-                                           dpu2, nd[j])), e0, e1);
+                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
+                                           nd[j])), e0, e1);
                         pk[2 * j + rsel] = pack_op<F16>(p0, p1);
                         dk[2 * j + rsel] = pack_op<F16>(e0, e1);
                     }
@@ -336,14 +340,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those
         // of dK = scale * (dS^T Q); staging reuses stage 0's Q (dV) and dO (dK)
         // buffers, idle once all MMAs are done
-        const int which = wg >> 1, half = wg & 1;
         const uint32_t stage = sStage + which * C::TILE;
         if (ok_e) {
             tc_fence_after();
             // dV carries 2^dout, dK 2^(ds+q) on the fp16 path
-            const float mul = which ? a.scale * pow2f(-(eds + eq)) : pow2f(-edo);
             stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + which * D + lane_off, stage, r,
-                                      half * (D / 2), (half + 1) * (D / 2), mul);
+                                      half * (D / 2), (half + 1) * (D / 2), mul_e);
             fence_proxy_async_smem();
         }
         named_bar_sync(1 + which, 256);

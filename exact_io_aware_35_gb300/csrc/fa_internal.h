@@ -20,13 +20,12 @@ constexpr int kBM = 128;
 constexpr int kBN = 128;
 
 // fp16 operand path.  bf16 inputs are copied to fp16 after a power-of-two
-// scaling that puts each tensor's largest magnitude just under 2^15, so the
-// copy is exact for every element above max * 2^-24 (bf16 carries 8
-// significant bits, fp16 11); P, P^T (at most 2^8) and dS, dS^T (scaled by
-// the power of two that puts the bound 2 d max|dO| max|V| under 2^15) are
-// then rounded to fp16 instead of bf16 before they feed an MMA: 3 more bits
-// on the operands whose rounding the outputs amplify.  The scalings are
-// undone exactly in the kernels' epilogues (or folded into scale * log2 e).
+// scaling (f16_scales_from), exact for all but the tiniest elements (bf16
+// carries 8 significant bits, fp16 11); P, P^T (at most 2^8) and dS, dS^T
+// (scaled so that the bound 2 d max|dO| max|V| lands under 2^15) are then
+// rounded to fp16 instead of bf16 before they feed an MMA: 3 more bits on the
+// operands whose rounding the outputs amplify.  The scalings are undone
+// exactly in the kernels' epilogues (or folded into scale * log2 e).
 struct F16Scales {
     int q, k, v, dout;  // x16 = fp16(x * 2^s) for the four operand tensors
     int ds;             // dS16 = fp16(dS * 2^ds)
@@ -48,32 +47,37 @@ struct F16Prep {
 
 cudaError_t launch_f16_prep(const F16Prep& p, cudaStream_t stream);
 
-// 15 - ceil(log2 a) for a > 0 given as float bits, clamped to [-40, 40] so
-// that every sum of three exponents the kernels form stays a normal power of
-// two; 0 for a == 0 or a non-finite maximum (the copy then carries the
-// inf/NaN just as the bf16 path would).  So the copies are exact for tensors
-// whose largest magnitude lies in [2^-25, 2^55].
-__device__ __forceinline__ int f16_exp_to_2p15(uint32_t bits) {
+// target - ceil(log2 a) for a > 0 given as float bits, clamped to [-40, 40];
+// 0 for a == 0 or a non-finite maximum (the copy then carries the inf/NaN
+// just as the bf16 path would).  So max * 2^s lands in (2^(target-1),
+// 2^target], and the exponent sums the kernels form stay normal powers of two.
+__device__ __forceinline__ int f16_exp_to(uint32_t bits, int target) {
     if (bits == 0u || bits >= 0x7f800000u) return 0;
     const int E = static_cast<int>(bits >> 23);
     const int e = (E == 0) ? -126 : (E - 127 + ((bits & 0x7fffffu) ? 1 : 0));
-    return max(-40, min(40, 15 - e));
+    return max(-40, min(40, target - e));
 }
 
-// The scales of a job from the maxima of q, k, v, dout (float bits).
+// The scales from the maxima of q, k, v, dout (float bits).  q, k go to just
+// under 2^15.  dS is bounded by 2 d max|dO| max|V| and goes under 2^15.  V
+// goes under 2^4 and dO gets ds - v, so that V dO^T (fp16 copies) carries
+// exactly 2^ds, the scale dS needs, with no extra multiply; that puts the
+// copy of dO under 2^(12 - log2(2d)) (16 at d = 128).  A bf16 value converts
+// to fp16 exactly when its exponent lies in [-17, 15], so the copies of q, k
+// are exact for elements above 2^-31 of the maximum and those of v, dO above
+// 2^-19 (smaller ones round at an absolute 2^-24 of the scaled values).
 __device__ __forceinline__ F16Scales f16_scales_from(const uint32_t* absmax, int d) {
     F16Scales s;
-    s.q = f16_exp_to_2p15(absmax[0]);
-    s.k = f16_exp_to_2p15(absmax[1]);
-    s.v = f16_exp_to_2p15(absmax[2]);
-    s.dout = f16_exp_to_2p15(absmax[3]);
+    s.q = f16_exp_to(absmax[0], 15);
+    s.k = f16_exp_to(absmax[1], 15);
+    s.v = f16_exp_to(absmax[2], 4);
     // |dS| = |P (dP - D)| <= 2 max|dP| <= 2 d max|dO| max|V|
     const float bound = 2.f * static_cast<float>(d) * __uint_as_float(absmax[3]) *
                         __uint_as_float(absmax[2]);
-    s.ds = f16_exp_to_2p15(__float_as_uint(bound));
+    s.ds = f16_exp_to(__float_as_uint(bound), 15);
+    s.dout = s.ds - s.v;
     return s;
 }
-
 
 struct FwdArgs {
     float* lse;          // [B, Hq, N]

@@ -4,9 +4,9 @@
 // takes max |x| of each tensor (atomicMax on the float bit pattern, which
 // orders non-negative floats like integers), the second turns the maxima into
 // F16Scales and writes fp16(x * 2^s).  Both are HBM-bound grid-stride loops
-// over 16-byte vectors (8 elements).  The exponent puts max |x| * 2^s in
-// (2^14, 2^15], so every element at or above max * 2^-24 converts exactly;
-// smaller ones round at 2^-24 of the maximum.
+// over 16-byte vectors (8 elements).  The exponents (f16_scales_from) put
+// the scaled maxima well inside fp16's range, which keeps the copies exact
+// for all but elements many orders of magnitude below the maximum.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 

@@ -46,8 +46,8 @@
  *    backward's dV, dK, dQ products -- the training forward and fa_bwd round
  *    it to fp16 and multiply it with an fp16 copy of the other operand (the
  *    bf16 inputs scaled by a power of two chosen from the tensor's largest
- *    magnitude, which makes the copy exact for every element above 2^-24 of
- *    that maximum, for maxima in [2^-25, 2^55]; the scaling is undone
+ *    magnitude, which makes the copy exact for every element above 2^-19 of
+ *    that maximum, for maxima in [2^-25, 2^36]; the scaling is undone
  *    exactly).  fp16 keeps 3 more bits than bf16, which the peaked-row
  *    near-cancellation dS = P o (dP - D) needs.  fa_fwd (inference) and
  *    fa_bwd_noalloc round those intermediates to bf16 instead.
