@@ -192,12 +192,12 @@ def tensor_bytes(*ts) -> int:
 
 # event-timed slots of a step; the forward slot is the fa_fwd_train call (the
 # fp16 copies of q, k, v, 2 small kernels, then fa_fwd_kernel), the backward's
-# are the fa_bwd_stage steps: max |dO| then D with the fp16 copy of dO
-# (2 kernels), dK/dV, dQ
-KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel")
+# are the fa_bwd_stage steps: D with max |dO|, dQ (which also writes the fp16
+# copy of dO), dK/dV
+KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel")
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
                   "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
-LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 2, "fa_bwd_dkdv_kernel": 1,
+LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 1, "fa_bwd_dkdv_kernel": 1,
             "fa_bwd_dq_kernel": 1}
 
 
@@ -213,8 +213,8 @@ def kernel_work(w: W.Workload, name: str):
         return "tensor", 4 * g1
     if name == "fa_bwd_dq_kernel":
         return "tensor", 3 * g1
-    # dsum slot: read dO for its maximum, then dO, O, o_lo; write D and dO's fp16 copy
-    return "hbm", 5 * w.B * w.N * w.Hq * w.d * 2 + 4 * w.B * w.Hq * w.N
+    # dsum slot: read dO, O, o_lo (max |dO| on the way); write D
+    return "hbm", 3 * w.B * w.N * w.Hq * w.d * 2 + 4 * w.B * w.Hq * w.N
 
 
 def source_hash(name: str) -> str:
@@ -293,6 +293,8 @@ def run_gpu(args):
         fa.fa_bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
                   workspace=wsb, stages=stages, o_lo=o_lo)
 
+    # the backward's slots, in the order of KERNELS[1:]
+    bwd_stages = (fa.FA_BWD_PREP_DOUT | fa.FA_BWD_DSUM, fa.FA_BWD_DQ, fa.FA_BWD_DKDV)
     clocks = ClockSampler(local)
     clocks.start()
     for _ in range(args.warmup):
@@ -303,7 +305,7 @@ def run_gpu(args):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {fa.status_string(st)} during warm-up")
 
-    # timed steps: events between the kernels (fwd | dsum | dK,dV | dQ) so each
+    # timed steps: events between the kernels (fwd | dsum | dQ | dK,dV) so each
     # kernel's duration is measured on the stream it runs on
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
@@ -317,8 +319,7 @@ def run_gpu(args):
         fwd()
         ev[i][1].record()
         if w.backward:
-            for n, stage in enumerate((fa.FA_BWD_PREP_DOUT | fa.FA_BWD_DSUM, fa.FA_BWD_DKDV,
-                                       fa.FA_BWD_DQ)):
+            for n, stage in enumerate(bwd_stages):
                 bwd(stage)
                 ev[i][2 + n].record()
     torch.cuda.synchronize()

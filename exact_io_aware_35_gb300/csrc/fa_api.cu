@@ -315,12 +315,17 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
             return st;
         if (stages & (FA_BWD_PREP | FA_BWD_PREP_DOUT)) {
             const bool all = (stages & FA_BWD_PREP) != 0;
+            // max |dO| comes from the dsum kernel when D is formed in the same
+            // call (it reads dO anyway), else from the prep kernels
+            const bool max_in_dsum = (stages & FA_BWD_DSUM) != 0;
             F16Prep p = prep_job(f16_ws, wl, all ? q : nullptr, all ? k : nullptr,
-                                 all ? v : nullptr, dout, B, H, Hkv, N, d);
-            // with the D stage in the same call, the dsum kernel (which reads dO
-            // anyway) makes the copy of dO
-            if (stages & FA_BWD_DSUM) p.convert_mask &= ~8;
-            const cudaError_t e = launch_f16_prep(p, cs);
+                                 all ? v : nullptr, max_in_dsum ? nullptr : dout, B, H, Hkv, N, d);
+            p.convert_mask &= ~8;  // the dQ kernel writes the copy of dO
+            cudaError_t e = cudaSuccess;
+            if (max_in_dsum)
+                e = cudaMemsetAsync(at<uint32_t>(f16_ws, wl.absmax) + 3, 0, sizeof(uint32_t), cs);
+            if (e == cudaSuccess && (p.n[0] | p.n[1] | p.n[2] | p.n[3]) != 0)
+                e = launch_f16_prep(p, cs);
             if (e != cudaSuccess) return cuda_fail(e, "fp16 operand copies");
         }
     }
@@ -328,11 +333,12 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
     a.lse = lse;
     a.dsum = dsum;
     a.f16s = f16_ws ? at<const F16Scales>(f16_ws, wl.scales) : nullptr;
-    const bool fused_copy = f16_ws && (stages & (FA_BWD_PREP | FA_BWD_PREP_DOUT)) &&
-                            (stages & FA_BWD_DSUM);
-    a.dout16 = fused_copy ? at<uint16_t>(f16_ws, wl.do16) : nullptr;
-    a.absmax = fused_copy ? at<uint32_t>(f16_ws, wl.absmax) : nullptr;
-    a.scales_w = fused_copy ? at<F16Scales>(f16_ws, wl.scales) : nullptr;
+    a.dout16 = f16_ws ? at<uint16_t>(f16_ws, wl.do16) : nullptr;
+    a.absmax = f16_ws ? at<uint32_t>(f16_ws, wl.absmax) : nullptr;
+    a.scales_w = f16_ws ? at<F16Scales>(f16_ws, wl.scales) : nullptr;
+    a.dout_max = f16_ws && (stages & (FA_BWD_PREP | FA_BWD_PREP_DOUT)) && (stages & FA_BWD_DSUM)
+                     ? at<uint32_t>(f16_ws, wl.absmax) + 3
+                     : nullptr;
     a.o = static_cast<const uint16_t*>(o);
     a.dout = static_cast<const uint16_t*>(dout);
     a.o_lo = static_cast<const uint16_t*>(o_lo);

@@ -12,7 +12,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr int kWarpGate = 10;  // dQ kernel: loads landed -> the MMA thread's LD barrier
-constexpr int kThreads = 384;  // WG0, WG1 compute; warp 8 MMA; warp 9 TMA; 10 gate; 11 idle
+constexpr int kWarpCopy = 11;  // dQ kernel: the fp16 copy of the dO tile
+constexpr int kThreads = 384;  // WG0, WG1 compute; warp 8 MMA; warp 9 TMA; 10 gate; 11 copy
 
 template <int D>
 struct Tiles {

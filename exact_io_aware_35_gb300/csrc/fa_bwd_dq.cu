@@ -44,6 +44,16 @@ struct DqCfg : Tiles<D> {
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 384;
 };
 
+// The fp16 operand scales from the four maxima in absmax (one 16-byte load).
+template <int D>
+__device__ __forceinline__ F16Scales scales_of(const uint32_t* absmax) {
+    int m[4];
+    ld_once_v4(reinterpret_cast<const int*>(absmax), m[0], m[1], m[2], m[3]);
+    const uint32_t u[4] = {static_cast<uint32_t>(m[0]), static_cast<uint32_t>(m[1]),
+                           static_cast<uint32_t>(m[2]), static_cast<uint32_t>(m[3])};
+    return f16_scales_from(u, D);
+}
+
 // F16: Q and K tiles are the fp16 copies (scaled by 2^q, 2^k; S carries
 // 2^(q+k), folded into scale * log2 e) and dS * 2^ds is rounded to fp16, so
 // dQ carries 2^(ds+k), undone in the epilogue.  dO and V stay bf16: dP is
@@ -177,6 +187,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp == kWarpCopy) {
+        // ============ copy: dO tile -> fp16(dO * 2^s) (fp16 operand path) ============
+        // The scales come from the maxima in absmax (taken before this kernel);
+        // block 0 stores them for the dK/dV kernel, which also reads the copy.
+        if (F16) {
+            const F16Scales sc = scales_of<D>(a.absmax);
+            if (blockIdx.x == 0 && lane == 0) *a.scales_w = sc;
+            const float mul = pow2f(sc.dout);
+            if (mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 29)) {
+                constexpr int PPR = D / 8;     // 16-byte pieces per row
+                constexpr int RPP = 32 / PPR;  // rows per pass of the warp
+                const int pc = lane % PPR, c = pc >> 3, pp = pc & 7;
+                uint16_t* dst = a.dout16 + (static_cast<size_t>(b) * a.N * a.Hq + h) * D + pc * 8;
+#pragma unroll 4
+                for (int r0 = 0; r0 < kBM; r0 += RPP) {
+                    const int r = r0 + lane / PPR;
+                    const int grow = qi * kBM + r;
+                    if (grow < a.N) {
+                        uint32_t w[4];
+                        ld_shared_v4(sDO + c * C::CHUNK + r * 128 + ((pp ^ (r & 7)) << 4), w);
+                        uint32_t hv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            hv[i] = pack_f16(bf16lo(w[i]) * mul, bf16hi(w[i]) * mul);
+                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(grow) * a.Hq * D) =
+                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
@@ -259,9 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float nlse2 = valid ? -a.lse[st_idx] * kLog2e : 0.f;
         const float dval = valid ? a.dsum[st_idx] : 0.f;
         // fp16 path: undo 2^(q+k) on S; dS = P (dP - D) carries 2^ds
-        int eq = 0, ek = 0, ev = 0, edo = 0;
-        if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
-        const int eds = F16 ? ld_once(&a.f16s->ds) : 0;
+        int eq = 0, ek = 0, eds = 0;
+        if (F16) {
+            const F16Scales sc = scales_of<D>(a.absmax);
+            eq = sc.q;
+            ek = sc.k;
+            eds = sc.ds;
+        }
         const float sl2 = a.scale_log2 * pow2f(-(eq + ek));
         const float dsc = pow2f(eds);
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;

@@ -98,11 +98,14 @@ struct BwdArgs {
     const uint16_t* dout;
     const uint16_t* o_lo;  // optional low half of O (null: D from o alone)
     const F16Scales* f16s;  // non-null: fp16 operand path (maps *16 are the fp16 copies)
-    // non-null: the dsum kernel also writes dout16 = fp16(dout * 2^s) and the
-    // scales (the maxima are in absmax)
+    // fp16 operand path: absmax holds max|q|, max|k|, max|v|, max|dout| as float
+    // bits; the dQ kernel forms the scales from it, writes them to scales_w (for
+    // the dK/dV kernel) and writes dout16 = fp16(dout * 2^s) from the dout tiles
+    // it loads anyway
     uint16_t* dout16;
     const uint32_t* absmax;
     F16Scales* scales_w;
+    uint32_t* dout_max;  // non-null: the dsum kernel also takes max|dout| into it
     uint32_t* status;
     int B, Hq, Hkv, N, d, g;
     int causal;

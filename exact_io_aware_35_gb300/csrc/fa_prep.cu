@@ -93,7 +93,7 @@ cudaError_t launch_f16_prep(const F16Prep& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     f16_absmax_kernel<<<dim3(gx, 4), kPrepThreads, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (p.convert_mask == 0) return cudaSuccess;  // a later kernel converts and writes the scales
+    if (p.convert_mask == 0) return cudaSuccess;  // the maxima alone (the dQ kernel copies dO)
     f16_convert_kernel<<<dim3(gx, 4), kPrepThreads, 0, st>>>(p);
     return cudaGetLastError();
 }

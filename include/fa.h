@@ -103,9 +103,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  *   workspace: the training workspace, fa_bwd_workspace_size(B, H, Hkv, N, d)
  *        bytes, 256-byte aligned, caller-owned, contents irrelevant on entry;
  *        NULL rounds P to bf16 as fa_fwd does.  The call leaves the fp16
- *        copies of q, k, v (and their scales) in it, so that a backward on the
- *        same workspace and the same q, k, v need only copy dout
- *        (fa_bwd_stage with FA_BWD_PREP_DOUT instead of FA_BWD_PREP).
+ *        copies of q, k, v (and their maxima) in it, so that a backward on
+ *        the same workspace and the same q, k, v skips them (fa_bwd_stage
+ *        with FA_BWD_PREP_DOUT instead of FA_BWD_PREP).
  * fa_bwd forms D_i = sum_c dO_ic O_ic from o + o_lo when given it.  Both
  * matter when rows are peaked: there dS = P o (dP - D) is a near-cancellation
  * and the roundings of P and of O alone move dQ by more than the rounding of
@@ -147,13 +147,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
 /*
  * The steps of fa_bwd, callable one at a time (e.g. to time them).  `stages`
- * is a bitmask of FA_BWD_PREP (the fp16 copies of q, k, v, dout and their
- * scales into the workspace), FA_BWD_PREP_DOUT (the copy of dout only: the
+ * is a bitmask of FA_BWD_PREP (max |x| of q, k, v, dout and the fp16 copies
+ * of q, k, v into the workspace), FA_BWD_PREP_DOUT (max |dout| only: the
  * workspace must hold fa_fwd_train's copies of the same q, k, v),
- * FA_BWD_DSUM (D = rowsum(dout * o) into the workspace), FA_BWD_DKDV (dk, dv)
- * and FA_BWD_DQ (dq); set stages run in the order PREP(_DOUT), DSUM, DKDV,
- * DQ.  DKDV and DQ read what the earlier stages wrote into the same workspace
- * earlier on the stream.  fa_bwd(...) is
+ * FA_BWD_DSUM (D = rowsum(dout * o) into the workspace; in a call with
+ * FA_BWD_PREP or FA_BWD_PREP_DOUT it also takes max |dout|, which the prep
+ * kernels then skip), FA_BWD_DQ (dq; it also writes the fp16 copy of dout and
+ * the scales into the workspace) and FA_BWD_DKDV (dk, dv; it reads that copy);
+ * set stages run in the order PREP(_DOUT), DSUM, DQ, DKDV.  Each stage reads
+ * what the earlier stages wrote into the same workspace earlier on the stream,
+ * so DKDV must follow a DQ of the same inputs.  fa_bwd(...) is
  * fa_bwd_stage(FA_BWD_PREP | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ, ...); a
  * training step that ran fa_fwd_train on the workspace can use
  * FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_DQ.

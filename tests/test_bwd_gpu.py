@@ -144,7 +144,9 @@ def test_bwd_stages_match_single_call(fa):
     ws = torch.empty(fa.fa_bwd_workspace_size(1, 4, 2, 500, 128), dtype=torch.uint8,
                      device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for st in (fa.FA_BWD_PREP, fa.FA_BWD_DSUM, fa.FA_BWD_DKDV, fa.FA_BWD_DQ):
+    # one stage per call, in the documented order (DQ writes the fp16 copy of
+    # dout that DKDV reads)
+    for st in (fa.FA_BWD_PREP, fa.FA_BWD_DSUM, fa.FA_BWD_DQ, fa.FA_BWD_DKDV):
         fa.fa_bwd(q, k, v, o, do, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws,
                   stages=st, o_lo=o_lo)
     assert fa.fa_get_device_error() == fa.FA_OK
@@ -165,9 +167,16 @@ def test_bwd_after_fwd_train_reuses_copies(fa):
     a = fa.fa_bwd(q, k, v, o, do, lse, causal=True, o_lo=o_lo, workspace=ws,
                   stages=fa.FA_BWD_AFTER_FWD_TRAIN)
     b = fa.fa_bwd(q, k, v, o, do, lse, causal=True, o_lo=o_lo)
+    # the same backward split as a timed training step splits it: max |dout|
+    # with D, then dQ (with the copy of dout), then dK, dV
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for st in (fa.FA_BWD_PREP_DOUT | fa.FA_BWD_DSUM, fa.FA_BWD_DQ, fa.FA_BWD_DKDV):
+        fa.fa_bwd(q, k, v, o, do, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws,
+                  stages=st, o_lo=o_lo)
     assert fa.fa_get_device_error() == fa.FA_OK
-    for u, v_ in zip(a, b):
+    for u, v_, w_ in zip(a, b, (dq, dk, dv)):
         assert torch.equal(u, v_)
+        assert torch.equal(u, w_)
 
 
 def test_bwd_deterministic(fa):
