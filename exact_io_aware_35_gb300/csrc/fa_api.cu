@@ -228,11 +228,14 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
     if (workspace) {
         // fp16 copies of Q, K, V: V for the P V product (P then in fp16), Q and
-        // K left for a backward that runs with FA_BWD_PREP_DOUT on this workspace
+        // K left for a backward that runs with FA_BWD_PREP_DOUT on this workspace.
+        // The prep kernels take the three maxima and copy K and V; the forward
+        // kernel copies the Q tiles it loads anyway.
         if ((st = make_map(&maps.v, at<void>(workspace, wl.v16), B, N, Hkv, d, true)) != FA_OK)
             return st;
-        const cudaError_t e =
-            launch_f16_prep(prep_job(workspace, wl, q, k, v, nullptr, B, H, Hkv, N, d), cs);
+        F16Prep p = prep_job(workspace, wl, q, k, v, nullptr, B, H, Hkv, N, d);
+        p.convert_mask &= ~1;
+        const cudaError_t e = launch_f16_prep(p, cs);
         if (e != cudaSuccess) return cuda_fail(e, "fp16 copies of Q, K, V");
     } else if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) {
         return st;
@@ -242,6 +245,7 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.lse = lse;
     a.o_lo = static_cast<uint16_t*>(o_lo);
     a.f16s = workspace ? at<const F16Scales>(workspace, wl.scales) : nullptr;
+    a.q16 = workspace ? at<uint16_t>(workspace, wl.q16) : nullptr;
     a.status = di->status;
     a.B = B;
     a.Hq = H;

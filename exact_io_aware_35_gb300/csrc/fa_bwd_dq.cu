@@ -195,27 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const F16Scales sc = scales_of<D>(a.absmax);
             if (blockIdx.x == 0 && lane == 0) *a.scales_w = sc;
             const float mul = pow2f(sc.dout);
-            if (mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 29)) {
-                constexpr int PPR = D / 8;     // 16-byte pieces per row
-                constexpr int RPP = 32 / PPR;  // rows per pass of the warp
-                const int pc = lane % PPR, c = pc >> 3, pp = pc & 7;
-                uint16_t* dst = a.dout16 + (static_cast<size_t>(b) * a.N * a.Hq + h) * D + pc * 8;
-#pragma unroll 4
-                for (int r0 = 0; r0 < kBM; r0 += RPP) {
-                    const int r = r0 + lane / PPR;
-                    const int grow = qi * kBM + r;
-                    if (grow < a.N) {
-                        uint32_t w[4];
-                        ld_shared_v4(sDO + c * C::CHUNK + r * 128 + ((pp ^ (r & 7)) << 4), w);
-                        uint32_t hv[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            hv[i] = pack_f16(bf16lo(w[i]) * mul, bf16hi(w[i]) * mul);
-                        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(grow) * a.Hq * D) =
-                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                    }
-                }
-            }
+            const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
+            uint16_t* dst = a.dout16 + (static_cast<size_t>(b) * a.N + qi * kBM) * row_el + h * D;
+            if (mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 29))
+                warp_tile_to_f16<D>(sDO, dst, row_el, a.N - qi * kBM, mul, lane);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {

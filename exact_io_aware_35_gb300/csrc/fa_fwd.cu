@@ -46,14 +46,14 @@ struct FwdCfg {
     static constexpr int SMEM_Q = 2 * TILE;
     static constexpr int SMEM_KV = NSLOT * TILE;
     // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
-    // o_final[2], mma_done
-    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1;
+    // o_final[2], mma_done, q_copied
+    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1;
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16;
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 256;
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, idle}
+    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, copy}
 };
 
 constexpr int kWarpMma = 8;
@@ -62,6 +62,9 @@ constexpr int kWarpLoad = 9;
 // thread waits on two barriers per key block instead of four: every mbarrier
 // wait in the issuing thread costs tensor-core time.
 constexpr int kWarpGate = 10;
+// The training forward's copy warp writes the fp16 copy of the CTA's Q tiles
+// (for the backward) while the tiles sit in shared memory anyway.
+constexpr int kWarpCopy = 11;
 
 // Row-max and exp threshold for the lazy rescale: the reference max is only
 // moved when the new block maximum exceeds it by more than 2^8 (in log2
@@ -91,6 +94,7 @@ __global__ void __launch_bounds__(384, 1)
     auto BAR_PF = [&](int t) { return bar0 + 8u * (3 + 2 * C::NSLOT + t); };
     auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * C::NSLOT + t); };
     const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * C::NSLOT);
+    const uint32_t BAR_QC = bar0 + 8u * (8 + 2 * C::NSLOT);  // Q tiles read by the copy warp
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -121,6 +125,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(BAR_OF(t), 1);
         }
         mbar_init(BAR_DONE, 1);
+        mbar_init(BAR_QC, 1);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -195,6 +200,24 @@ __global__ void __launch_bounds__(384, 1)
                     if (ok) mbar_arrive(BAR_PF(t));
                 }
             }
+        }
+        __syncwarp();
+    } else if (warp == kWarpCopy) {
+        // ================= copy: Q tiles -> fp16(q * 2^s) =================
+        // Only the training forward (F16 with q16 set); the epilogues, which
+        // stage O in the Q buffers, wait for BAR_QC.
+        if (F16 && a.q16 != nullptr) {
+            const float mul = pow2f(ld_once(&a.f16s->q));
+            const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
+            if (mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 15)) {
+                for (int t = 0; t < 2; ++t)
+                    warp_tile_to_f16<D>(sQ + t * C::TILE,
+                                        a.q16 + (static_cast<size_t>(b) * a.N + row0 + t * kBM) *
+                                                    row_el + h * D,
+                                        row_el, a.N - (row0 + t * kBM), mul, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR_QC);  // also after a failed wait: never blocks the epilogue
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -367,6 +390,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging in Q_t's buffer -> TMA store
         bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.status, a.timeout_ns, 12 + t);
+        if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
+            ok_e = ok_e && mbar_wait(BAR_QC, 0, a.status, a.timeout_ns, 14);
         const uint32_t stage = sQ + t * C::TILE;
         if (ok_e) {
             tc_fence_after();

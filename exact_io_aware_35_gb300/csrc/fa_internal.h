@@ -83,6 +83,7 @@ struct FwdArgs {
     float* lse;          // [B, Hq, N]
     uint16_t* o_lo;      // [B, N, Hq, d] bf16 low half of O, or null
     const F16Scales* f16s;  // non-null: P and V enter O += P V in fp16 (V map = fp16 copy)
+    uint16_t* q16;       // non-null (with f16s): the kernel writes fp16(q * 2^s.q) here
     uint32_t* status;    // device status word
     int B, Hq, Hkv, N, g;
     int causal;

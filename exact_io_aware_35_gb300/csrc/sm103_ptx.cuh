@@ -494,6 +494,37 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&v)[4]) {
                  : "memory");
 }
 
+// One warp writes a 128 x D bf16 tile held in shared memory (TMA layout:
+// 64-column chunks of 128 rows x 128 bytes, the 16-byte pieces of row r
+// swizzled by r % 8) to global memory as fp16(x * mul).  Tile row r goes to
+// dst + r * row_stride elements, for r < rows only (rows past the tensor's
+// end are the TMA's zero fill).  Each pass of the warp covers 32 / (D / 8)
+// whole rows, so its stores are contiguous runs of D * 2 bytes.
+template <int D>
+__device__ __forceinline__ void warp_tile_to_f16(uint32_t tile, uint16_t* dst, size_t row_stride,
+                                                 int rows, float mul, int lane) {
+    constexpr int CHUNK = 128 * 128;
+    constexpr int PPR = D / 8;     // 16-byte pieces per row
+    constexpr int RPP = 32 / PPR;  // rows per pass
+    const int pc = lane % PPR, c = pc >> 3, pp = pc & 7;
+    dst += pc * 8;
+#pragma unroll 4
+    for (int r0 = 0; r0 < 128; r0 += RPP) {
+        const int r = r0 + lane / PPR;
+        if (r < rows) {
+            uint32_t w[4];
+            ld_shared_v4(tile + c * CHUNK + r * 128 + ((pp ^ (r & 7)) << 4), w);
+            uint32_t hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                hv[i] = pack_f16(__uint_as_float(w[i] << 16) * mul,
+                                 __uint_as_float(w[i] & 0xffff0000u) * mul);
+            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * row_stride) =
+                make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+    }
+}
+
 // Warpgroup-wide register re-allocation (all 128 threads of the warpgroup).
 template <int n>
 __device__ __forceinline__ void setmaxnreg_inc() {
