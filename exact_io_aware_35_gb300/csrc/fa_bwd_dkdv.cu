@@ -15,11 +15,16 @@
 // issuing thread about as long as one with N = 128 and reads more shared
 // memory per flop.  Two 128-column TMEM regions X and Y swap roles every
 // block: S^T(i) and then P^T(i), dS^T(i) live in one, dP^T(i) in the other.
-// As soon as both warpgroups have copied dP^T(i) into registers, the tensor
-// core computes S^T(i+1) over it while they work; dV, dK += ... of block i
-// then read P^T(i) / dS^T(i) and dP^T(i+1) is written over them.  Warpgroup h
-// owns queries 64h..64h+63 of each block and writes its P^T and dS^T (bf16)
-// over the S^T columns it read.
+// As soon as all warpgroups have copied dP^T(i) into registers, the tensor
+// core computes S^T(i+1) over it while they work; dV += P^T dO of block i
+// starts as soon as P^T(i) is written (the warpgroups store dS^T(i), already
+// formed in registers, after signalling P^T), dK += dS^T Q once dS^T(i) is,
+// and dP^T(i+1) is then written over both.  Warpgroup w owns queries
+// 32w..32w+31 of each block and writes its P^T and dS^T (16-bit pairs) over
+// the S^T columns it read.  (Tried and dropped: 64-query sub-blocks with two
+// TMEM buffers of 64-wide S^T and dP^T, which would hide the hand-off
+// entirely; the 64-wide products ran at about 100 cycles per MMA in the
+// kernel, and the whole was 24% slower.)
 //
 // TMEM (512 columns): X [0,128) | Y [128,256) | dV [256,256+D) | dK [256+D, 256+2D).
 #include "fa_bwd_common.cuh"
@@ -48,8 +53,8 @@ struct DkdvCfg : Tiles<D> {
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
     static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
     // barriers: K/V, stage full[NST], stage empty[NST], S^T+dP^T ready,
-    // dP^T copied to registers, P^T+dS^T written, all MMAs done
-    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1;
+    // dP^T copied to registers, P^T written, dS^T written, all MMAs done
+    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
 };
@@ -82,8 +87,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     auto BAR_STE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
     const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // block's S^T, dP^T ready
     const uint32_t BAR_LD = BAR_SDF + 8u;                   // dP^T copied to registers
-    const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T, dS^T written
-    const uint32_t BAR_ACC = BAR_SDF + 24u;
+    const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T written
+    const uint32_t BAR_DSF = BAR_SDF + 24u;                 // dS^T written
+    const uint32_t BAR_ACC = BAR_SDF + 32u;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_init(BAR_SDF, 1);
         mbar_init(BAR_LD, kDkCompute);
         mbar_init(BAR_PF, kDkCompute);
+        mbar_init(BAR_DSF, kDkCompute);
         mbar_init(BAR_ACC, 1);
         fence_barrier_init();
     }
@@ -187,36 +194,36 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             auto reg_s = [&](int it) { return tbase + ((it & 1) ? C::TM_Y : C::TM_X); };
             auto reg_d = [&](int it) { return tbase + ((it & 1) ? C::TM_X : C::TM_Y); };
             auto stage_q = [&](int s) { return sStage + 2 * s * C::TILE; };
+            // descriptors built once per tile; each MMA only moves the start address
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, 16);
             // dst = A B^T over the head dimension: S^T = K Q^T or dP^T = V dO^T
-            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB) {
+            auto issue_t = [&](uint32_t dst, uint32_t a_lo, uint32_t sB) {
+                const uint32_t b_lo = sdesc_lo(sB, 16);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dst, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
-                                IDESC_S, ks > 0);
+                    mma_bf16_ss(dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_S, ks > 0);
                 }
             };
-            // dV += P^T dO, dK += dS^T Q: for queries 16ks.., P^T / dS^T (bf16) sit in
-            // columns 32w + (ks%2)*8 / 32w + 16 + (ks%2)*8 of S^T's region (w = ks/2);
-            // dO, Q rows 16ks.. are read MN-major
-            auto issue_acc = [&](int it, int s) {
-                const uint32_t sQ = stage_q(s), sDO = sQ + C::TILE, rs = reg_s(it);
+            // dV += P^T dO (dk = false) or dK += dS^T Q (dk = true): for queries
+            // 16ks.., P^T / dS^T (16-bit pairs) sit in columns 32w + (ks%2)*8 /
+            // 32w + 16 + (ks%2)*8 of S^T's region (w = ks/2); dO, Q rows 16ks.. are
+            // read MN-major
+            auto issue_acc = [&](int it, int s, bool dk) {
+                const uint32_t b_lo = sdesc_lo(stage_q(s) + (dk ? 0 : C::TILE), C::CHUNK);
+                const uint32_t rs = reg_s(it) + (dk ? 16 : 0);
 #pragma unroll
-                for (int ks = 0; ks < kBM / 16; ++ks) {
-                    const uint32_t acc = (it == 0 && ks == 0) ? 0u : 1u;
-                    const uint32_t aoff = (ks >> 1) * 32 + (ks & 1) * 8;
-                    mma_bf16_ts(tDV, rs + aoff, sdesc_sw128(sDO + ks * 2048, C::CHUNK, 1024),
-                                IDESC_ACC, acc);
-                    mma_bf16_ts(tDK, rs + aoff + 16, sdesc_sw128(sQ + ks * 2048, C::CHUNK, 1024),
-                                IDESC_ACC, acc);
-                }
+                for (int ks = 0; ks < kBM / 16; ++ks)
+                    mma_bf16_ts(dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
+                                sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
             };
             bool ok = mbar_wait(BAR_KV, 0, a.status, a.timeout_ns, 32) &&
                       mbar_wait(BAR_STF(0), 0, a.status, a.timeout_ns, 33);
             if (ok) {
                 tc_fence_after();
-                issue_t(reg_s(0), sK, stage_q(0));
-                issue_t(reg_d(0), sV, stage_q(0) + C::TILE);
+                issue_t(reg_s(0), k_lo, stage_q(0));
+                issue_t(reg_d(0), v_lo, stage_q(0) + C::TILE);
                 mma_commit(BAR_SDF);
             }
             for (int it = 0; it < n_it && ok; ++it) {
@@ -230,15 +237,19 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         break;
                     if (!(ok = mbar_wait(BAR_LD, it & 1, a.status, a.timeout_ns, 34))) break;
                     tc_fence_after();
-                    issue_t(reg_d(it), sK, stage_q(s2));
+                    issue_t(reg_d(it), k_lo, stage_q(s2));
                 }
+                // dV as soon as P^T is written, dK once dS^T is
                 if (!(ok = mbar_wait(BAR_PF, it & 1, a.status, a.timeout_ns, 34))) break;
                 tc_fence_after();
-                issue_acc(it, s);
+                issue_acc(it, s, false);
+                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.status, a.timeout_ns, 38))) break;
+                tc_fence_after();
+                issue_acc(it, s, true);
                 mma_commit(BAR_STE(s));
                 if (more) {
                     // dP^T(it+1) over P^T(it), dS^T(it): the products above read them first
-                    issue_t(reg_s(it), sV, stage_q(s2) + C::TILE);
+                    issue_t(reg_s(it), v_lo, stage_q(s2) + C::TILE);
                     mma_commit(BAR_SDF);
                 }
             }
@@ -296,6 +307,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR_LD);
             const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
+            // P^T first (the tensor core starts dV += P^T dO on it), then dS^T
+            uint32_t dk[2][8];
 #pragma unroll
             for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
                 const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
@@ -306,7 +319,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
                 // causal: key k is hidden from query q when k > q
                 const bool need_mask = a.causal && key + 8 > qbase;
-                uint32_t pk[8], dk[8];
+                uint32_t pk[8];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -326,15 +339,19 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                                       add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
                                            nd[j])), e0, e1);
                         pk[2 * j + rsel] = pack_op<F16>(p0, p1);
-                        dk[2 * j + rsel] = pack_op<F16>(e0, e1);
+                        dk[lb][2 * j + rsel] = pack_op<F16>(e0, e1);
                     }
                 }
-                tmem_st16x128_x4(rs + lo, pk);       // P^T over the first 16 S^T columns read
-                tmem_st16x128_x4(rs + lo + 16, dk);  // dS^T over the other 16
+                tmem_st16x128_x4(rs + lo, pk);  // P^T over the first 16 S^T columns read
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR_PF);
+            tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
+            tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR_DSF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 37);
         // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those

@@ -220,33 +220,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return r;
             };
+            // descriptors: K-major tiles (S, dP operands) and the MN-major K tile
+            // (dQ), built once; each MMA only moves the start address
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t q_lo = sdesc_lo(sQ, 16), do_lo = sdesc_lo(sDO, 16);
             // dst = A B^T over the head dimension (both K-major): S = Q K^T, dP = dO V^T
-            auto issue_t = [&](uint32_t dst, uint32_t sA, uint32_t sB, uint32_t idesc) {
+            auto issue_t = [&](uint32_t dst, uint32_t a_lo, uint32_t sB, uint32_t idesc) {
+                const uint32_t b_lo = sdesc_lo(sB, 16);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dst, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024),
-                                idesc, ks > 0);
+                    mma_bf16_ss(dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), idesc, ks > 0);
                 }
             };
             // dP(jj) = dO V_jj^T; V_jj's slot is free once it has run
             auto issue_dp = [&](int jj) {
-                issue_t(tDP(jj), sDO, sV + (jj % C::VS) * C::TILE, IDESC_DP);
+                issue_t(tDP(jj), do_lo, sV + (jj % C::VS) * C::TILE, IDESC_DP);
                 mma_commit(BAR_VE(jj % C::VS));
             };
             // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
             // of dP buffer jj & 1; K rows 16ks.. read MN-major
             auto issue_dq = [&](int jj) {
-                const uint32_t kt = sK + (jj % C::KS) * C::TILE, aS = tDP(jj);
+                const uint32_t k_lo = sdesc_lo(sK + (jj % C::KS) * C::TILE, C::CHUNK), aS = tDP(jj);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8,
-                                sdesc_sw128(kt + ks * 2048, C::CHUNK, 1024), IDESC_DQ,
-                                (jj == 0 && ks == 0) ? 0u : 1u);
+                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
+                                IDESC_DQ, (jj == 0 && ks == 0) ? 0u : 1u);
                 mma_commit(BAR_KE(jj % C::KS));
             };
             bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && k_ready(0);
-            if (ok) issue_t(tS, sQ, sK, IDESC_S);
+            if (ok) issue_t(tS, q_lo, sK, IDESC_S);
             if (ok && (ok = v_ready(0))) {
                 issue_dp(0);
                 mma_commit(BAR_SDF);
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < nj) {
                     if (!(ok = mbar_wait(BAR_LD, j & 1, a.status, a.timeout_ns, 24))) break;
                     tc_fence_after();
-                    issue_t(tS, sQ, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
+                    issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
                     issue_dp(j + 1);
                     mma_commit(BAR_SDF);
                 }

@@ -225,24 +225,27 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
+            // descriptors built once per tile; each MMA only moves the start address
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t q_lo = sdesc_lo(sQ, 16);
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t dS = tbase + C::TM_S + t * kBN;
+                const uint32_t a_lo = q_lo + ((t * C::TILE) >> 4);
+                const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, 16);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sKV + slot * C::TILE + off, 16, 1024);
-                    mma_bf16_ss(dS, ad, bd, IDESC_QK, ks > 0);
+                    mma_bf16_ss(dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK, ks > 0);
                 }
             };
             auto issue_pv = [&](int t, int slot, bool acc) {
                 const uint32_t dO = tbase + C::TM_O + t * D;
                 const uint32_t aP = tbase + C::TM_S + t * kBN;  // P (bf16) over S_t
+                const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
 #pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    const uint64_t bd = sdesc_sw128(sKV + slot * C::TILE + ks * 2048, C::CHUNK, 1024);
-                    mma_bf16_ts(dO, aP + ks * 8, bd, IDESC_PV, (acc || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    mma_bf16_ts(dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
+                                (acc || ks > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 3);
             if (ok) {

@@ -272,6 +272,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// sdesc_sw128 in two halves, so that moving the start address by a constant
+// costs the issuing thread one 32-bit add: the low word holds the start
+// address (16-byte units, bits 0-13) and the leading offset (bits 16-29), the
+// high word the stride offset, the fixed bit 46 and the swizzle mode.  Shared
+// addresses stay below 2^18, so the address field never carries into the
+// leading offset.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+// The descriptor of (lo, hi) with its start address `off` bytes further.
+__device__ __forceinline__ uint64_t sdesc_at(uint32_t lo, uint32_t hi, uint32_t off) {
+    return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
+}
+
 // TMEM -> registers: warp reads 32 lanes (its quarter) x 32 columns; thread t
 // gets lane (base lane + t), columns col..col+31.  Call tmem_wait_ld() and
 // reg_fence() before using the values.
