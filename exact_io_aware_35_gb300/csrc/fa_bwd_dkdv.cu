@@ -160,6 +160,15 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
                 dv4[u] = (q < a.N) ? a.dsum[base + q] * dsc : 0.f;
             }
+            // L2 prefetch of the Q, dO tiles two steps ahead (no slot needed)
+            if (lane == 0 && it + 2 < n_it) {
+                const int it2 = it + 2;
+                const int hq2 = hk * a.g + it2 / nqi, q2 = (qi0 + it2 % nqi) * kBM;
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_prefetch_4d(&tmQ, c * 64, hq2, q2, b, pol_q);
+                    tma_prefetch_4d(&tmDO, c * 64, hq2, q2, b, pol_q);
+                }
+            }
             if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.status, a.timeout_ns, 30)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
