@@ -39,9 +39,10 @@ def _load():
         lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D, _D, _D, _D, i, i, i, i, i, i, d]
         lib.oracle_attn_bwd_rows.argtypes = [_D, _D, _D, _D, _LL, i, _D, _LL, i, _D, _D,
                                              i, i, i, i, i, i, d]
+        lib.oracle_attn_fwd_kv.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i, i, i, d]
         lib.oracle_num_threads.argtypes = []
         for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_bwd,
-                  lib.oracle_attn_bwd_rows, lib.oracle_num_threads):
+                  lib.oracle_attn_bwd_rows, lib.oracle_attn_fwd_kv, lib.oracle_num_threads):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -83,6 +84,27 @@ def attn_fwd(q, k, v, causal: bool, scale: float):
                                  B, Hq, Hkv, N, d, int(bool(causal)), float(scale))
     if rc:
         raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
+    return o, lse
+
+
+def attn_fwd_kv(q, k, v, causal: bool, scale: float):
+    """Forward with Nq query rows against Nk keys (q [B,Nq,Hq,d], k, v
+    [B,Nk,Hkv,d]); causal means query i sees keys j <= i + Nk - Nq (the
+    queries are the sequence's last Nq positions).  Returns (o [B,Nq,Hq,d],
+    lse [B,Hq,Nq]) in float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape:
+        raise ValueError("expected [B, N, H, d] arrays")
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or Hq % Hkv:
+        raise ValueError(f"incompatible shapes q{q.shape} k{k.shape}")
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, Nq))
+    rc = _load().oracle_attn_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                    Nq, Nk, d, int(bool(causal)), float(scale))
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_kv failed ({rc})")
     return o, lse
 
 

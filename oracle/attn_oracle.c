@@ -165,6 +165,59 @@ int oracle_attn_fwd_rows(const double* q, const double* k, const double* v, cons
     return fail ? 2 : 0;
 }
 
+/* Forward with separate query and key/value lengths (the split-KV decode
+ * entry): q, o [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d]; lse [B, Hq, Nq].  The
+ * queries are the last Nq positions of a sequence of Nk, so under the causal
+ * mask query i sees keys j <= i + (Nk - Nq) (Nq == Nk gives j <= i, as in
+ * oracle_attn_fwd); the causal case needs Nq <= Nk.  Same two-pass softmax of
+ * the definition per row. */
+int oracle_attn_fwd_kv(const double* q, const double* k, const double* v, double* o,
+                       double* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                       double scale) {
+    if (check_args(B, Hq, Hkv, Nq, d) || Nk < 1 || (causal && Nq > Nk)) return 1;
+    const int g = Hq / Hkv;
+    const long long total = (long long)B * Hq * Nq;
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)Nk);
+        if (!p) {
+#pragma omp atomic write
+            fail = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long long t = 0; t < total; ++t) {
+            if (!p) continue;
+            const int i = (int)(t % Nq);
+            const int h = (int)((t / Nq) % Hq);
+            const int b = (int)(t / ((long long)Nq * Hq));
+            const int hk = h / g;
+            const int nvis = causal ? i + (Nk - Nq) + 1 : Nk;
+            const double* qi = q + IDX4(b, i, h, 0, Nq, Hq, d);
+            double m = -INFINITY;
+            for (int j = 0; j < nvis; ++j) {
+                p[j] = scale * dot(qi, k + IDX4(b, j, hk, 0, Nk, Hkv, d), d);
+                if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < nvis; ++j) {
+                p[j] = exp(p[j] - m);
+                l += p[j];
+            }
+            double* oi = o + IDX4(b, i, h, 0, Nq, Hq, d);
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            for (int j = 0; j < nvis; ++j) {
+                const double w = p[j] / l;
+                const double* vj = v + IDX4(b, j, hk, 0, Nk, Hkv, d);
+                for (int c = 0; c < d; ++c) oi[c] += w * vj[c];
+            }
+            lse[((size_t)b * Hq + h) * Nq + i] = m + log(l);
+        }
+        free(p);
+    }
+    return fail ? 2 : 0;
+}
+
 /* Query-major part of the backward for row (b, h, i): fills dq_row (may be
  * NULL) and returns lse_i; *D_out receives D_i = sum_j P_ij dP_ij. */
 static double bwd_query_row(const double* q, const double* k, const double* v, const double* dout,

@@ -53,6 +53,25 @@ def attn_fwd(q, k, v, causal: bool, scale: float):
     return o, lse
 
 
+def attn_fwd_kv(q, k, v, causal: bool, scale: float):
+    """Nq queries against Nk keys; causal: query i sees keys j <= i + Nk - Nq."""
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    vis = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * (q[b, :, h] @ k[b, :, h // g].T)
+            if causal:
+                s = np.where(vis, s, -np.inf)
+            p, lse[b, h] = _softmax_rows(s)
+            o[b, :, h] = p @ v[b, :, h // g]
+    return o, lse
+
+
 def attn_probs(q, k, causal: bool, scale: float, b: int = 0, h: int = 0) -> np.ndarray:
     """The probability matrix P of one (batch, head), for invariant checks."""
     q = np.asarray(q, dtype=np.float64)

@@ -271,3 +271,103 @@ def test_memory_wall_arithmetic_golden():
     assert W.score_matrix_elements(N) == int(vals["elements"])
     assert W.score_matrix_bytes(N, 2) == int(vals["bytes_per_head_2byte"])
     assert math.floor(W.score_matrix_bytes(N, 2) / 1e5) / 10 == vals["page_megabytes"]
+
+
+# ---- Nq queries against Nk keys (the split-KV decode entry) ----
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_oracle_with_equal_lengths_is_the_square_oracle(causal):
+    q, k, v = qkv(N=17, seed=30)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.4)
+    o2, lse2 = oracle.attn_fwd_kv(q, k, v, causal, 0.4)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_oracle_matches_numpy(causal):
+    q = rnd((2, 5, 6, 8), 31)
+    k, v = rnd((2, 23, 2, 8), 32), rnd((2, 23, 2, 8), 33)
+    o, lse = oracle.attn_fwd_kv(q, k, v, causal, 0.3)
+    o2, lse2 = npo.attn_fwd_kv(q, k, v, causal, 0.3)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+def test_kv_causal_queries_are_the_last_rows_of_the_square_problem():
+    # the reading of the causal mask for Nq < Nk: the Nq queries are the last
+    # Nq positions of the sequence, so they equal the last rows of the square
+    # causal problem over all Nk positions
+    Nk, Nq = 29, 6
+    qf, k, v = qkv(N=Nk, seed=34)
+    o, lse = oracle.attn_fwd(qf, k, v, True, 0.45)
+    o2, lse2 = oracle.attn_fwd_kv(qf[:, Nk - Nq:], k, v, True, 0.45)
+    np.testing.assert_allclose(o2, o[:, Nk - Nq:], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[:, :, Nk - Nq:], rtol=0, atol=1e-13)
+
+
+def test_kv_single_causal_query_sees_every_key():
+    q = rnd((1, 1, 4, 8), 35)
+    k, v = rnd((1, 40, 2, 8), 36), rnd((1, 40, 2, 8), 37)
+    oc, lc = oracle.attn_fwd_kv(q, k, v, True, 0.5)
+    on, ln = oracle.attn_fwd_kv(q, k, v, False, 0.5)
+    np.testing.assert_array_equal(oc, on)
+    np.testing.assert_array_equal(lc, ln)
+
+
+def _merge_in_order(parts):
+    # the online-softmax update applied chunk after chunk, each chunk given as
+    # its normalised output and lse ("FlashAttention 1, 2, and 3 Explained",
+    # section 2, the two-block l and O update): running (m, l, unnormalised O)
+    m = l = acc = None
+    for o_c, lse_c in parts:
+        lse_t = np.transpose(lse_c, (0, 2, 1))[..., None]  # [B, Nq, Hq, 1]
+        if m is None:
+            m, l, acc = lse_t, np.ones_like(lse_t), o_c.copy()
+            continue
+        m_new = np.maximum(m, lse_t)
+        a_old, a_new = np.exp(m - m_new), np.exp(lse_t - m_new)
+        acc = (a_old * l * acc + a_new * o_c) / (a_old * l + a_new)
+        l = a_old * l + a_new
+        m = m_new
+    return acc, np.transpose((m + np.log(l))[..., 0], (0, 2, 1))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_chunked_kv_merge_in_order_equals_full(causal):
+    # ring attention's per-chunk results, merged in ring order, equal the
+    # whole; chunks may be empty for a causal query (lse = -inf there)
+    Nq, Nk = 4, 37
+    q = rnd((2, Nq, 4, 8), 38)
+    k, v = rnd((2, Nk, 2, 8), 39), rnd((2, Nk, 2, 8), 40)
+    o, lse = oracle.attn_fwd_kv(q, k, v, causal, 0.35)
+    bounds = [0, 10, 11, 25, Nk]
+    parts = []
+    for c0, c1 in zip(bounds[:-1], bounds[1:]):
+        # keys [c0, c1): the queries keep their positions Nk - Nq + i, so a
+        # causal chunk sees keys j <= Nk - Nq + i, i.e. the square problem's
+        # mask shifted by the chunk start
+        kc, vc = k[:, c0:c1], v[:, c0:c1]
+        if causal:
+            # chunk key j' = c0 + j is visible iff c0 + j <= Nk - Nq + i
+            oc, lc = npo.attn_fwd_kv(q, kc, vc, False, 0.35)
+            vis = (np.arange(c0, c1)[None, :] <= (Nk - Nq) + np.arange(Nq)[:, None])
+            oc = np.zeros_like(oc)
+            lc = np.full_like(lc, -np.inf)
+            for b in range(2):
+                for h in range(4):
+                    s = 0.35 * (q[b, :, h] @ kc[b, :, h // 2].T)
+                    s = np.where(vis, s, -np.inf)
+                    for i in range(Nq):
+                        if not vis[i].any():
+                            continue
+                        mm = s[i].max()
+                        e = np.exp(s[i] - mm)
+                        lc[b, h, i] = mm + np.log(e.sum())
+                        oc[b, i, h] = (e / e.sum()) @ vc[b, :, h // 2]
+        else:
+            oc, lc = oracle.attn_fwd_kv(q, kc, vc, False, 0.35)
+        parts.append((oc, lc))
+    om, lm = _merge_in_order(parts)
+    np.testing.assert_allclose(om, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
