@@ -32,7 +32,8 @@ FA_BWD_AFTER_FWD_TRAIN = FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_D
 
 # every entry point include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_noalloc",
-           "fa_bwd_workspace_size",
+           "fa_bwd_workspace_size", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
+           "fa_fwd_splitkv_workspace_size",
            "fa_get_device_error",
            "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
 
@@ -67,6 +68,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_fwd_splitkv.argtypes = [vp] * 6 + [i] * 7 + [f, i, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_num_splits.argtypes = [i] * 8
+    lib.fa_fwd_splitkv_num_splits.restype = i
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i] * 8
+    lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
 
     lib.fa_get_device_error.argtypes = [vp]
     lib.fa_get_device_error.restype = i
@@ -195,6 +202,53 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_fwd_splitkv_num_splits(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
+                              causal: bool = False, num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_splitkv_num_splits(B, H, Hkv, Nq, Nk, d, int(bool(causal)),
+                                                        int(num_splits)))
+
+
+def fa_fwd_splitkv_workspace_size(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int,
+                                  causal: bool = False, num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_splitkv_workspace_size(B, H, Hkv, Nq, Nk, d,
+                                                            int(bool(causal)), int(num_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                   num_splits: int = 0, o=None, lse=None, workspace=None, stream=None):
+    """Split-KV forward (fa_fwd_splitkv): q [B, Nq, H, d] against k, v
+    [B, Nk, Hkv, d]; causal means the queries are the sequence's last Nq
+    positions.  num_splits <= 0 lets the library choose.  Returns (o, lse)."""
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be [B, N, H, d]")
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    _check(q, "q", (B, Nq, Hq, d))
+    _check(k, "k", (B, Nk, Hkv, d))
+    _check(v, "v", (B, Nk, Hkv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    _check(o, "o", (B, Nq, Hq, d))
+    _check(lse, "lse", (B, Hq, Nq), torch.float32)
+    ws_bytes = fa_fwd_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, d, causal, num_splits)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    if ws_bytes and workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError("workspace too small")
+    st = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), None if workspace is None else workspace.data_ptr(),
+                            B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                            int(num_splits), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_splitkv")
+    return o, lse
 
 
 def fa_get_device_error(stream=None) -> int:

@@ -78,14 +78,15 @@ fa_status device_ready(DeviceInfo** out) {
 }
 
 // Tensor map of a [B, N, H, d] bf16 (or, f16 = true, fp16) tensor: dims
-// (d, H, N, B), box (64, 1, 128, 1), 128-byte swizzle; rows past N read as
-// zero and are never written.
-fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, bool f16 = false) {
+// (d, H, N, B), box (64, heads, rows, 1), 128-byte swizzle; rows past N read
+// as zero and are never written.
+fa_status make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, bool f16 = false,
+                   int rows = kBM, int heads = 1) {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                              static_cast<cuuint64_t>(N) * H * d * 2};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(heads), static_cast<cuuint32_t>(rows), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                           4, const_cast<void*>(ptr), dims,
@@ -364,6 +365,138 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
 }
 
 }  // namespace fa
+
+namespace fa {
+namespace {
+
+// How a split-KV call is cut: qpt queries of all g heads per 128-row tile,
+// and the key blocks into splits of blocks_per_split blocks.  num_splits <= 0
+// picks enough splits for two CTAs per SM of this GPU's 152 (at most one per
+// two key blocks).
+struct DecodePlan {
+    int g, qpt, n_qt, splits, blocks_per_split;
+};
+
+fa_status decode_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, int num_splits,
+                      DecodePlan* pl) {
+    if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int g = H / Hkv;
+    if (g > kBM) return FA_ERR_UNSUPPORTED;
+    const long long qel = static_cast<long long>(B) * Nq * H * d;
+    const long long kel = static_cast<long long>(B) * Nk * Hkv * d;
+    if (qel >= (1LL << 40) || kel >= (1LL << 40) || Nq > (1 << 30) || Nk > (1 << 30) ||
+        static_cast<long long>(B) * H * Nq >= (1LL << 31))
+        return FA_ERR_INVALID_ARG;
+    pl->g = g;
+    pl->qpt = kBM / g;
+    pl->n_qt = (Nq + pl->qpt - 1) / pl->qpt;
+    const int nblk = (Nk + kBN - 1) / kBN;
+    const long long units = static_cast<long long>(B) * Hkv * pl->n_qt;
+    int splits = num_splits;
+    if (splits <= 0) {
+        // at least two blocks per SM, at most one split per two key blocks; among
+        // those, the first count whose blocks fill their last wave to 90%
+        const int cap = (nblk + 1) / 2 < 1024 ? (nblk + 1) / 2 : 1024;
+        const long long want = (2LL * 152 + units - 1) / units;
+        splits = static_cast<int>(want > cap ? cap : want);
+        for (int s2 = splits; s2 <= cap; ++s2) {
+            const int bps = (nblk + s2 - 1) / s2;
+            const long long ctas = units * ((nblk + bps - 1) / bps);
+            const long long waves = (ctas + 151) / 152;
+            if (ctas * 10 >= waves * 152 * 9) {
+                splits = s2;
+                break;
+            }
+        }
+    }
+    if (splits > nblk) splits = nblk;
+    if (splits < 1) splits = 1;
+    pl->blocks_per_split = (nblk + splits - 1) / splits;
+    pl->splits = (nblk + pl->blocks_per_split - 1) / pl->blocks_per_split;  // none empty
+    if (units * pl->splits > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// Workspace of a call with `splits` > 1: fp32 O_s [splits, B, H, Nq, d], then
+// lse_s [splits, B, H, Nq], each part rounded up to 256 bytes.
+size_t decode_part_bytes(int B, int H, int Nq, int d, int splits, size_t* lse_off) {
+    const size_t rows = static_cast<size_t>(splits) * B * H * Nq;
+    *lse_off = up256(rows * d * 4);
+    return *lse_off + up256(rows * 4);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                              int num_splits) {
+    fa::DecodePlan pl;
+    if (fa::decode_plan(B, H, Hkv, Nq, Nk, d, causal, num_splits, &pl) != FA_OK) return 0;
+    return pl.splits;
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                                     int num_splits) {
+    fa::DecodePlan pl;
+    if (fa::decode_plan(B, H, Hkv, Nq, Nk, d, causal, num_splits, &pl) != FA_OK) return 0;
+    if (pl.splits == 1) return 0;
+    size_t off = 0;
+    return fa::decode_part_bytes(B, H, Nq, d, pl.splits, &off);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         void* workspace, int B, int H, int Hkv, int Nq, int Nk, int d,
+                         int causal, float scale, int num_splits, void* stream) {
+    t_last_error[0] = 0;
+    fa::DecodePlan pl;
+    fa_status st = fa::decode_plan(B, H, Hkv, Nq, Nk, d, causal, num_splits, &pl);
+    if (st != FA_OK) return st;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    if (pl.splits > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((st = device_ready(&di)) != FA_OK) return st;
+    DecodeMaps maps;
+    if ((st = make_map(&maps.q, q, B, Nq, H, d, false, pl.qpt, pl.g)) != FA_OK) return st;
+    if ((st = make_map(&maps.k, k, B, Nk, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.v, v, B, Nk, Hkv, d)) != FA_OK) return st;
+    DecodeArgs a;
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.part_o = nullptr;
+    a.part_lse = nullptr;
+    if (pl.splits > 1) {
+        size_t lse_off = 0;
+        fa::decode_part_bytes(B, H, Nq, d, pl.splits, &lse_off);
+        a.part_o = static_cast<float*>(workspace);
+        a.part_lse = at<float>(workspace, lse_off);
+    }
+    a.status = di->status;
+    a.B = B;
+    a.Hq = H;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.g = pl.g;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.qpt = pl.qpt;
+    a.n_qt = pl.n_qt;
+    a.splits = pl.splits;
+    a.blocks_per_split = pl.blocks_per_split;
+    a.timeout_ns = kWaitTimeoutNs;
+    const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_splitkv launch");
+    return FA_OK;
+}
+
+}  // extern "C"
 
 extern "C" {
 

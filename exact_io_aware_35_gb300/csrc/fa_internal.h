@@ -115,6 +115,31 @@ struct BwdArgs {
     uint64_t timeout_ns;
 };
 
+// Split-KV forward (fa_decode.cu): Nq queries of the g heads of a KV group
+// per 128-row tile (qpt queries x g heads), the key blocks cut into `splits`
+// ranges of blocks_per_split blocks.
+struct DecodeArgs {
+    uint16_t* o;        // [B, Nq, Hq, d] bf16
+    float* lse;         // [B, Hq, Nq]
+    float* part_o;      // splits > 1: [splits, B, Hq, Nq, d] fp32 workspace
+    float* part_lse;    // splits > 1: [splits, B, Hq, Nq]
+    uint32_t* status;
+    int B, Hq, Hkv, Nq, Nk, g;
+    int causal;         // query i sees keys j <= i + Nk - Nq
+    float scale_log2;
+    int qpt, n_qt;      // queries per tile, query tiles
+    int splits, blocks_per_split;
+    uint64_t timeout_ns;
+};
+
+struct DecodeMaps {
+    CUtensorMap q;      // box 64 x g x qpt x 1
+    CUtensorMap k, v;   // box 64 x 1 x 128 x 1
+};
+
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int d,
+                          cudaStream_t stream);
+
 // Tensor maps of one call (all 4-D: d, H, N, B; box 64 x 1 x 128 x 1).
 struct FwdMaps {
     CUtensorMap q, k, v, o;

@@ -196,6 +196,45 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          float scale, void* stream);
 
 /*
+ * Split-KV forward (FlashDecoding): Nq queries against Nk keys and values,
+ * the key range cut into splits that run as separate thread blocks, then an
+ * exact merge of the splits' results ("FlashAttention Kernel", the
+ * FlashDecoding mentions: parallel over the key/value length, then combined;
+ * the merge is the two-block online-softmax update of "FlashAttention 1, 2,
+ * and 3 Explained", section 2).  For decoding: the queries are the last Nq
+ * positions of a sequence of Nk.
+ *   q    [B, Nq, H, d]   bf16 in
+ *   k, v [B, Nk, Hkv, d] bf16 in
+ *   o    [B, Nq, H, d]   bf16 out
+ *   lse  [B, H, Nq]      fp32 out, natural log of the scaled scores' sum
+ *   causal: query i sees keys j <= i + Nk - Nq (needs Nq <= Nk; with
+ *        Nq == Nk this is fa_fwd's mask)
+ *   num_splits: number of key ranges, <= 0 for the library's choice (enough
+ *        thread blocks for two per SM); clamped to the number of 128-key
+ *        blocks, and reduced so that no range is empty.
+ *   workspace: fa_fwd_splitkv_workspace_size(...) bytes (fp32 per-split
+ *        results), 256-byte aligned, caller-owned; may be NULL when that size
+ *        is 0 (one split: the kernel writes o and lse itself).
+ * The g = H / Hkv query heads of a key/value head are processed together
+ * (128 / g queries of all g heads per 128-row tile), so K and V are read from
+ * HBM once.  d in {64, 128}; g <= 128.  Errors as fa_fwd; FA_ERR_INVALID_ARG
+ * also for causal with Nq > Nk and for a missing workspace.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         void* workspace, int B, int H, int Hkv, int Nq, int Nk, int d,
+                         int causal, float scale, int num_splits, void* stream);
+
+/* The split count fa_fwd_splitkv uses for these arguments (0: invalid sizes). */
+int fa_fwd_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                              int num_splits);
+
+/* Workspace bytes fa_fwd_splitkv needs for these arguments: 0 when it uses one
+ * split (or the sizes are invalid), else (splits * B * H * Nq) * (d + 1) fp32
+ * values, each part rounded up to 256 bytes. */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                                     int num_splits);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded wait ran
  * out in some kernel since the last call) or FA_ERR_CUDA (the synchronise

@@ -105,3 +105,45 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q)
+
+
+def test_splitkv_plan_and_workspace(lib):
+    import exact_io_aware_35_gb300 as fa
+    # one split: no workspace
+    assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 1, 100, 128, 0, 1) == 1
+    assert lib.fa_fwd_splitkv_workspace_size(1, 8, 2, 1, 100, 128, 0, 1) == 0
+    # requested splits are clamped to the 128-key blocks and never left empty
+    assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 1, 1000, 128, 0, 50) == 8
+    assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 1, 1000, 128, 0, 3) == 3
+    assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 1, 1000, 128, 0, 5) == 4  # 2 blocks each
+    # fp32 O_s and lse_s per (split, batch, head, query), each rounded to 256
+    n = 3 * 2 * 8 * 5
+    assert lib.fa_fwd_splitkv_workspace_size(2, 8, 2, 5, 1000, 64, 1, 3) == \
+        _up256(n * 64 * 4) + _up256(n * 4)
+    # the library's choice: enough blocks for two per SM, at most one split per two key blocks
+    s = lib.fa_fwd_splitkv_num_splits(8, 32, 8, 1, 32768, 128, 1, 0)
+    assert s >= 2 and 8 * 8 * s >= 2 * 152 and s <= 128
+    assert fa.fa_fwd_splitkv_num_splits(8, 32, 8, 1, 32768, 128, True) == s
+    # invalid sizes
+    assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 10, 5, 128, 1, 0) == 0   # causal Nq > Nk
+    assert lib.fa_fwd_splitkv_num_splits(1, 6, 4, 1, 5, 128, 0, 0) == 0    # Hq % Hkv
+    assert lib.fa_fwd_splitkv_num_splits(1, 256, 1, 1, 5, 128, 0, 0) == 0  # g > 128
+    assert lib.fa_fwd_splitkv_workspace_size(1, 8, 2, 1, 100, 96, 0, 0) == 0
+
+
+def test_splitkv_invalid_arguments_rejected_on_host(lib):
+    import exact_io_aware_35_gb300 as fa
+
+    def call(ptr=256, ws=256, B=1, H=8, Hkv=2, Nq=1, Nk=1000, d=128, causal=0, scale=0.1,
+             splits=4):
+        return lib.fa_fwd_splitkv(ptr, ptr, ptr, ptr, ptr, ws, B, H, Hkv, Nq, Nk, d, causal,
+                                  ctypes.c_float(scale), splits, None)
+    assert call(ptr=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ptr=8) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=0) == fa.FA_ERR_INVALID_ARG          # several splits need a workspace
+    assert call(ws=272) == fa.FA_ERR_INVALID_ARG        # not 256-aligned
+    assert call(Nq=2000, causal=1) == fa.FA_ERR_INVALID_ARG
+    assert call(Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(H=256, Hkv=1) == fa.FA_ERR_UNSUPPORTED
