@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the float64 CPU oracle, timed
+    python bench.py --workload decode32k      # the split-KV decode path (its own line)
 
 A step is one training forward plus one backward pass over one batch of the
 workload (default: B4 Hq32 Hkv8 N8192 d128 causal -- the N >= 8192, d = 128
@@ -33,6 +34,8 @@ import torch  # noqa: E402
 import fa_workloads as W  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 BF16 tensor peak at N=2k–128k, d=64/128"
+DECODE_METRIC = ("split-KV decode attention: GB/s of the compulsory HBM bytes (K, V, Q, O, lse) "
+                 "and % of the measured HBM copy bandwidth")
 DEFAULT_WORKLOAD = "gqa8k"
 
 
@@ -196,6 +199,7 @@ def tensor_bytes(*ts) -> int:
 # copy of dO), dK/dV
 KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel")
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
+                  "fa_decode_split_kernel": "fa_decode.cu",
                   "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
 LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 1, "fa_bwd_dkdv_kernel": 1,
             "fa_bwd_dq_kernel": 1}
@@ -416,17 +420,186 @@ def run_gpu(args):
     return 0
 
 
+def decode_oracle_sample(w: W.DecodeWorkload):
+    """Batch element 0 of the decode workload (all heads) for the CPU oracle."""
+    x = W.make_decode_inputs(w.with_(B=1))
+    sw = w.with_(B=1)
+    flops = W.decode_flops(sw)
+    desc = (f"batch element 0 of {w.B}, all {w.Hq} heads, Nq={w.Nq}, Nk={w.Nk} "
+            f"({flops / 1e9:.2f} nominal GFLOP, {1 / w.B:.4g} of a step)")
+    return x, flops, desc
+
+
+def time_decode_oracle(x, w: W.DecodeWorkload) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn_fwd_kv(x["q"], x["k"], x["v"], w.causal, w.scale)
+    return time.perf_counter() - t0
+
+
+def run_decode_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = W.DECODE_WORKLOADS[args.workload]
+    x, flops, desc = decode_oracle_sample(w)
+    oracle.build()
+    for _ in range(args.warmup):
+        time_decode_oracle(x, w)
+    times = [time_decode_oracle(x, w) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    gbs = W.decode_min_bytes(w.with_(B=1)) / (ms * 1e-3) / 1e9
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "shape": W.describe_decode(w), "sample": desc},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_decode(args):
+    """One step = one fa_fwd_splitkv call (split kernel + combine kernel) over
+    the decode workload, inputs resident in HBM, L2 flushed before each."""
+    import exact_io_aware_35_gb300 as fa
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    base = W.DECODE_WORKLOADS[args.workload]
+    if args.batch:
+        base = base.with_(B=args.batch)
+    w = base.with_(seed=base.seed + 1000 * rank)
+    x = W.make_decode_inputs(w)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    dvc = {n: t.to(dev) for n, t in host.items()}
+    q, k, v = dvc["q"], dvc["k"], dvc["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Nq), device=dev, dtype=torch.float32)
+    splits = fa.fa_fwd_splitkv_num_splits(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.causal)
+    wsb = fa.fa_fwd_splitkv_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.causal)
+    wsp = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_fwd_splitkv(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, workspace=wsp)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error during warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error in the timed region")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+
+    out_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    h2d = tensor_bytes(*host.values())
+    d2h = tensor_bytes(o, lse)
+
+    def e2e_step():
+        for n, t in host.items():
+            dvc[n].copy_(t, non_blocking=True)
+        step()
+        out_host["o"].copy_(o, non_blocking=True)
+        out_host["lse"].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(t_timed0, time.time())
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / K
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms = (float(u) for u in t.tolist())
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    nbytes = W.decode_min_bytes(w) * ws
+    flops = W.decode_flops(w) * ws
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {"metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, shape of the workload)",
+            "config": {"workload": args.workload, "shape": W.describe_decode(w),
+                       "global_batch": w.B * ws, "seq_len": w.Nk, "splits": splits,
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "frac_of_peak": gbs / ws / peaks["hbm_gbs"], "tflops": flops / (ms * 1e-3) / 1e12,
+            "peak_gbs": peaks["hbm_gbs"], "peak_source": peaks["source"] + " HBM copy",
+            "gpu_launches": K * (2 if splits > 1 else 1),
+            "roofline": {"kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+                         "bound": "hbm", "achieved": gbs / ws, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / ws / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"] + " copy", "launch_ms": ms,
+                         "algorithmic_work_per_launch": W.decode_min_bytes(w),
+                         "traffic": measured_traffic("fa_decode_split_kernel", args.workload)},
+            "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
+    if clk is not None:
+        line["clocks"] = clk
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        xs, sflops, desc = decode_oracle_sample(base)
+        secs = time_decode_oracle(xs, base)
+        line["cpu_baseline"] = {"value": W.decode_min_bytes(base.with_(B=1)) / secs / 1e9,
+                                "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
+    if args.workload in W.DECODE_WORKLOADS:
+        return run_decode_reference(args) if args.impl == "reference" else run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -371,8 +371,7 @@ namespace {
 
 // How a split-KV call is cut: qpt queries of all g heads per 128-row tile,
 // and the key blocks into splits of blocks_per_split blocks.  num_splits <= 0
-// picks enough splits for two CTAs per SM of this GPU's 152 (at most one per
-// two key blocks).
+// picks the count with the shortest estimated time on this GPU's 152 SMs.
 struct DecodePlan {
     int g, qpt, n_qt, splits, blocks_per_split;
 };
@@ -396,18 +395,18 @@ fa_status decode_plan(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, 
     const long long units = static_cast<long long>(B) * Hkv * pl->n_qt;
     int splits = num_splits;
     if (splits <= 0) {
-        // at least two blocks per SM, at most one split per two key blocks; among
-        // those, the first count whose blocks fill their last wave to 90%
-        const int cap = (nblk + 1) / 2 < 1024 ? (nblk + 1) / 2 : 1024;
-        const long long want = (2LL * 152 + units - 1) / units;
-        splits = static_cast<int>(want > cap ? cap : want);
-        for (int s2 = splits; s2 <= cap; ++s2) {
+        // One CTA per SM (the K/V ring takes the shared memory), so the time
+        // is about waves x (blocks per split + ~3 blocks of set-up); take the
+        // count that minimises it (the smallest on ties).
+        const int cap = nblk < 1024 ? nblk : 1024;
+        long long best = -1;
+        for (int s2 = 1; s2 <= cap; ++s2) {
             const int bps = (nblk + s2 - 1) / s2;
             const long long ctas = units * ((nblk + bps - 1) / bps);
-            const long long waves = (ctas + 151) / 152;
-            if (ctas * 10 >= waves * 152 * 9) {
+            const long long cost = ((ctas + 151) / 152) * (bps + 3);
+            if (best < 0 || cost < best) {
+                best = cost;
                 splits = s2;
-                break;
             }
         }
     }

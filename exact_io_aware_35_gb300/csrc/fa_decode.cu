@@ -389,41 +389,59 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 // Merges the splits of every (batch, head, query) row: with m = max_s lse_s
 // and w_s = e^{lse_s - m}, O = sum_s w_s O_s / sum_s w_s and
 // lse = m + ln sum_s w_s (the two-block online-softmax update applied across
-// the splits).  One warp per row, D/32 consecutive columns per lane.
+// the splits).  One block of 256 threads per row: all threads take the
+// maximum over the splits together, then thread (group, column) sums the
+// splits s = group (mod 256 / D) of one column, and the groups are added in
+// shared memory.
 template <int D>
 __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecodeArgs a) {
-    const long long rows = static_cast<long long>(a.B) * a.Hq * a.Nq;
-    const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= rows) return;
-    const size_t stride = static_cast<size_t>(rows);
+    constexpr int G = 256 / D;  // split groups
+    __shared__ float red[8];
+    __shared__ float part[G][D + 1];
+    __shared__ float wpart[G];
+    const size_t rows = static_cast<size_t>(a.B) * a.Hq * a.Nq;
+    const size_t row = blockIdx.x;
+    const int t = threadIdx.x;
     float m = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) m = fmaxf(m, a.part_lse[s * stride + wid]);
-    constexpr int PER = D / 32;
-    float acc[PER];
+    for (int s = t; s < a.splits; s += 256) m = fmaxf(m, a.part_lse[s * rows + row]);
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-        const float ls = a.part_lse[s * stride + wid];
-        if (ls == -INFINITY) continue;  // a split no query key reaches
-        const float w = expf(ls - m);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((t & 31) == 0) red[t >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    const int grp = t / D, c = t % D;
+    float acc = 0.f, wsum = 0.f;
+#pragma unroll 4
+    for (int s = grp; s < a.splits; s += G) {
+        const float ls = a.part_lse[s * rows + row];
+        // a split that no key of this query reaches has lse = -inf, weight 0
+        const float w = (ls == -INFINITY) ? 0.f : expf(ls - m);
         wsum += w;
-        const float* src = a.part_o + (s * stride + wid) * D + lane * PER;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, src[i], acc[i]);
+        acc = fmaf(w, a.part_o[(s * rows + row) * D + c], acc);
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    // row wid = (b, h, n) -> output [B, Nq, Hq, D]
-    const int n = static_cast<int>(wid % a.Nq);
-    const long long bh = wid / a.Nq;
-    const int h = static_cast<int>(bh % a.Hq);
-    const int b = static_cast<int>(bh / a.Hq);
-    uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.Nq + n) * a.Hq + h) * D + lane * PER;
+    part[grp][c] = acc;
+    if (c == 0) wpart[grp] = wsum;
+    __syncthreads();
+    if (grp == 0) {
+        float tot = 0.f, wt = 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; i += 2)
-        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16(acc[i] * inv, acc[i + 1] * inv);
-    if (lane == 0) a.lse[wid] = m + logf(wsum);
+        for (int g2 = 0; g2 < G; ++g2) {
+            tot += part[g2][c];
+            wt += wpart[g2];
+        }
+        const float inv = wt > 0.f ? 1.f / wt : 0.f;
+        // row = (b, h, n) -> output [B, Nq, Hq, D]
+        const int n = static_cast<int>(row % a.Nq);
+        const size_t bh = row / a.Nq;
+        const int h = static_cast<int>(bh % a.Hq);
+        const int b = static_cast<int>(bh / a.Hq);
+        const float val = tot * inv;
+        uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.Nq + n) * a.Hq + h) * D + c;
+        *dst = static_cast<uint16_t>(pack_bf16(val, 0.f) & 0xffffu);
+        if (c == 0) a.lse[row] = m + logf(wt);
+    }
 }
 
 template <int D>
@@ -438,10 +456,9 @@ cudaError_t launch_decode_d(const DecodeMaps& mp, const DecodeArgs& a, cudaStrea
     kern<<<static_cast<unsigned>(nblk), C::THREADS, C::SMEM_BYTES, st>>>(mp.q, mp.k, mp.v, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.splits > 1) {
-        const long long warps = static_cast<long long>(a.B) * a.Hq * a.Nq;
-        const long long blocks = (warps * 32 + 255) / 256;
-        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        fa_decode_combine_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+        const long long rows = static_cast<long long>(a.B) * a.Hq * a.Nq;
+        if (rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        fa_decode_combine_kernel<D><<<static_cast<unsigned>(rows), 256, 0, st>>>(a);
         e = cudaGetLastError();
     }
     return e;

@@ -56,6 +56,66 @@ WORKLOADS = {
 WORKLOAD_ORDER = ["tiny", "gpt2s", "gqa8k", "gqa32k_peaked", "mqa128k"]
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq queries (the last Nq positions of a sequence) against Nk keys and
+    values: the split-KV decode shape."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    scale: float
+    seed: int = 0
+
+    def with_(self, **kw) -> "DecodeWorkload":
+        return replace(self, **kw)
+
+
+# Decode against a long cache: GQA at 32k (8 sequences, one new token each),
+# MQA at 128k (the long-context workload's head layout).
+DECODE_WORKLOADS = {
+    "decode32k": DecodeWorkload("decode32k", 8, 32, 8, 1, 32768, 128, True, _s(128), seed=5),
+    "decode128k_mqa": DecodeWorkload("decode128k_mqa", 1, 16, 1, 1, 131072, 128, True, _s(128),
+                                     seed=6),
+}
+
+
+def describe_decode(w: DecodeWorkload) -> str:
+    return (f"B{w.B} Hq{w.Hq} Hkv{w.Hkv} Nq{w.Nq} Nk{w.Nk} d{w.d} "
+            f"{'causal' if w.causal else 'non-causal'} scale={w.scale:.6g}")
+
+
+def make_decode_inputs(w: DecodeWorkload):
+    """q [B, Nq, Hq, d], k, v [B, Nk, Hkv, d]: bf16 N(0, 1) draws in that order."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    q = torch.randn((w.B, w.Nq, w.Hq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Nk, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Nk, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+
+
+def decode_flops(w: DecodeWorkload) -> float:
+    """4 * d FLOPs per visible (query, key) pair per head; under the causal
+    mask query i sees Nk - Nq + i + 1 keys."""
+    if w.causal:
+        pairs = w.Nq * (w.Nk - w.Nq) + w.Nq * (w.Nq + 1) // 2
+    else:
+        pairs = w.Nq * w.Nk
+    return 4.0 * w.B * w.Hq * w.d * pairs
+
+
+def decode_min_bytes(w: DecodeWorkload) -> int:
+    """K and V read once, Q read and O written once (bf16), lse written (fp32)."""
+    kv = 2 * w.B * w.Nk * w.Hkv * w.d * 2
+    qo = 2 * w.B * w.Nq * w.Hq * w.d * 2
+    return kv + qo + 4 * w.B * w.Hq * w.Nq
+
+
 def describe(w: Workload) -> str:
     return (f"B{w.B} Hq{w.Hq} Hkv{w.Hkv} N{w.N} d{w.d} "
             f"{'causal' if w.causal else 'non-causal'} scale={w.scale:.6g}")

@@ -120,10 +120,19 @@ def test_splitkv_plan_and_workspace(lib):
     n = 3 * 2 * 8 * 5
     assert lib.fa_fwd_splitkv_workspace_size(2, 8, 2, 5, 1000, 64, 1, 3) == \
         _up256(n * 64 * 4) + _up256(n * 4)
-    # the library's choice: enough blocks for two per SM, at most one split per two key blocks
-    s = lib.fa_fwd_splitkv_num_splits(8, 32, 8, 1, 32768, 128, 1, 0)
-    assert s >= 2 and 8 * 8 * s >= 2 * 152 and s <= 128
-    assert fa.fa_fwd_splitkv_num_splits(8, 32, 8, 1, 32768, 128, True) == s
+    # the library's choice: the count with the least waves x (blocks per split + 3)
+    # on 152 SMs, one CTA each (units = batch x kv heads x query tiles)
+    def cost(units, nblk, s2):
+        bps = -(-nblk // s2)
+        ctas = units * -(-nblk // bps)
+        return -(-ctas // 152) * (bps + 3)
+    for (B, H, Hkv, Nq, Nk) in ((8, 32, 8, 1, 32768), (1, 16, 1, 1, 131072), (2, 8, 1, 40, 5000)):
+        s = lib.fa_fwd_splitkv_num_splits(B, H, Hkv, Nq, Nk, 128, 1, 0)
+        g = H // Hkv
+        units = B * Hkv * -(-Nq // (128 // g))
+        nblk = -(-Nk // 128)
+        assert cost(units, nblk, s) == min(cost(units, nblk, x) for x in range(1, nblk + 1))
+        assert fa.fa_fwd_splitkv_num_splits(B, H, Hkv, Nq, Nk, 128, True) == s
     # invalid sizes
     assert lib.fa_fwd_splitkv_num_splits(1, 8, 2, 10, 5, 128, 1, 0) == 0   # causal Nq > Nk
     assert lib.fa_fwd_splitkv_num_splits(1, 6, 4, 1, 5, 128, 0, 0) == 0    # Hq % Hkv

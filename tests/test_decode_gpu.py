@@ -114,3 +114,32 @@ def test_decode_bench_shape_sampled(fa):
                                             1 / math.sqrt(d))
         assert_close(o[b:b + 1], o_ref, f"o[b={b}]")
         assert_lse_close(lse[b:b + 1], lse_ref)
+
+
+def test_ring_chunks_merged_in_order(fa):
+    # The math ring attention depends on, on one GPU with no communication:
+    # each key/value chunk's (O_c, lse_c) from its own call, merged on the host
+    # in ring order with the two-block online-softmax update, equals the whole.
+    # Queries are the sequence's last Nq positions (causal): every chunk before
+    # the last is fully visible, the last one carries the causal edge.
+    B, Nq, Nk, Hq, Hkv, d = 2, 3, 1500, 8, 2, 128
+    q, k, v = inputs(B, Nq, Nk, Hq, Hkv, d, seed=11)
+    scale = 1 / math.sqrt(d)
+    bounds = [0, 256, 600, 1100, Nk]
+    m = l = acc = None
+    for c0, c1 in zip(bounds[:-1], bounds[1:]):
+        last = c1 == Nk
+        o_c, lse_c = run(fa, q, k[:, c0:c1].contiguous(), v[:, c0:c1].contiguous(), last, scale, 1)
+        o_c = o_c.double().numpy()
+        lse_t = np.transpose(lse_c.double().numpy(), (0, 2, 1))[..., None]
+        if m is None:
+            m, l, acc = lse_t, np.ones_like(lse_t), o_c
+            continue
+        m_new = np.maximum(m, lse_t)
+        a_old, a_new = np.exp(m - m_new), np.exp(lse_t - m_new)
+        acc = (a_old * l * acc + a_new * o_c) / (a_old * l + a_new)
+        l = a_old * l + a_new
+        m = m_new
+    o_ref, lse_ref = oracle.attn_fwd_kv(q, k, v, True, scale)
+    assert_close(acc, o_ref, "merged o")
+    assert_lse_close(np.transpose((m + np.log(l))[..., 0], (0, 2, 1)), lse_ref)
