@@ -40,6 +40,9 @@ def _load():
         lib.oracle_attn_bwd_rows.argtypes = [_D, _D, _D, _D, _LL, i, _D, _LL, i, _D, _D,
                                              i, i, i, i, i, i, d]
         lib.oracle_attn_fwd_kv.argtypes = [_D, _D, _D, _D, _D, i, i, i, i, i, i, i, d]
+        lib.oracle_attn_fwd_blockmask.argtypes = [_D, _D, _D, _D, _D, ctypes.c_void_p, i, i, i,
+                                                  i, i, i, i, d]
+        lib.oracle_attn_fwd_blockmask.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_bwd,
                   lib.oracle_attn_bwd_rows, lib.oracle_attn_fwd_kv, lib.oracle_num_threads):
@@ -105,6 +108,26 @@ def attn_fwd_kv(q, k, v, causal: bool, scale: float):
                                     Nq, Nk, d, int(bool(causal)), float(scale))
     if rc:
         raise RuntimeError(f"oracle_attn_fwd_kv failed ({rc})")
+    return o, lse
+
+
+def attn_fwd_blockmask(q, k, v, block_mask, block: int, causal: bool, scale: float):
+    """Forward under a block mask [Hq, nb, nb] (nonzero = the block is
+    computed; nb = ceil(N / block)); rows with no visible key get O = 0 and
+    lse = -inf.  Returns (o [B,N,Hq,d], lse [B,Hq,N]) in float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, Hq, Hkv, d = _shapes(q, k)
+    nb = (N + block - 1) // block
+    mask = np.ascontiguousarray(np.asarray(block_mask).astype(np.uint8))
+    if mask.shape != (Hq, nb, nb):
+        raise ValueError(f"block mask shape {mask.shape}, expected {(Hq, nb, nb)}")
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, N))
+    rc = _load().oracle_attn_fwd_blockmask(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                           mask.ctypes.data, int(block), B, Hq, Hkv, N, d,
+                                           int(bool(causal)), float(scale))
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_blockmask failed ({rc})")
     return o, lse
 
 

@@ -218,6 +218,72 @@ int oracle_attn_fwd_kv(const double* q, const double* k, const double* v, double
     return fail ? 2 : 0;
 }
 
+/* Forward under a block mask (block-sparse attention): query i of head h may
+ * see key j only when mask[h][i / bs][j / bs] != 0 (bs x bs blocks,
+ * nb = ceil(N / bs) blocks per side, mask [Hq, nb, nb]), and under the
+ * causal mask also only when j <= i.  A row with no visible key has O = 0
+ * and lse = -inf (the value that adds nothing when partial results are
+ * merged).  Otherwise the same two-pass softmax of the definition. */
+int oracle_attn_fwd_blockmask(const double* q, const double* k, const double* v, double* o,
+                              double* lse, const unsigned char* mask, int bs, int B, int Hq,
+                              int Hkv, int N, int d, int causal, double scale) {
+    if (check_args(B, Hq, Hkv, N, d) || bs < 1) return 1;
+    const int g = Hq / Hkv;
+    const int nb = (N + bs - 1) / bs;
+    const long long total = (long long)B * Hq * N;
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+        unsigned char* vis = (unsigned char*)malloc((size_t)N);
+        if (!p || !vis) {
+#pragma omp atomic write
+            fail = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long long t = 0; t < total; ++t) {
+            if (!p || !vis) continue;
+            const int i = (int)(t % N);
+            const int h = (int)((t / N) % Hq);
+            const int b = (int)(t / ((long long)N * Hq));
+            const int hk = h / g;
+            const unsigned char* mrow = mask + ((size_t)h * nb + i / bs) * nb;
+            const double* qi = q + IDX4(b, i, h, 0, N, Hq, d);
+            double m = -INFINITY;
+            int any = 0;
+            for (int j = 0; j < N; ++j) {
+                vis[j] = (unsigned char)(mrow[j / bs] != 0 && (!causal || j <= i));
+                if (!vis[j]) continue;
+                any = 1;
+                p[j] = scale * dot(qi, k + IDX4(b, j, hk, 0, N, Hkv, d), d);
+                if (p[j] > m) m = p[j];
+            }
+            double* oi = o + IDX4(b, i, h, 0, N, Hq, d);
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            if (!any) {
+                lse[((size_t)b * Hq + h) * N + i] = -INFINITY;
+                continue;
+            }
+            double l = 0.0;
+            for (int j = 0; j < N; ++j)
+                if (vis[j]) {
+                    p[j] = exp(p[j] - m);
+                    l += p[j];
+                }
+            for (int j = 0; j < N; ++j) {
+                if (!vis[j]) continue;
+                const double w = p[j] / l;
+                const double* vj = v + IDX4(b, j, hk, 0, N, Hkv, d);
+                for (int c = 0; c < d; ++c) oi[c] += w * vj[c];
+            }
+            lse[((size_t)b * Hq + h) * N + i] = m + log(l);
+        }
+        free(p);
+        free(vis);
+    }
+    return fail ? 2 : 0;
+}
+
 /* Query-major part of the backward for row (b, h, i): fills dq_row (may be
  * NULL) and returns lse_i; *D_out receives D_i = sum_j P_ij dP_ij. */
 static double bwd_query_row(const double* q, const double* k, const double* v, const double* dout,

@@ -72,6 +72,30 @@ def attn_fwd_kv(q, k, v, causal: bool, scale: float):
     return o, lse
 
 
+def attn_fwd_blockmask(q, k, v, block_mask, block: int, causal: bool, scale: float):
+    """Block-sparse forward: element mask = block mask expanded (and causal);
+    empty rows give O = 0, lse = -inf."""
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    blk = np.arange(N) // block
+    o = np.zeros_like(q)
+    lse = np.full((B, Hq, N), -np.inf)
+    for h in range(Hq):
+        vis = np.asarray(block_mask[h])[blk[:, None], blk[None, :]] != 0
+        if causal:
+            vis &= np.tril(np.ones((N, N), dtype=bool))
+        rows = vis.any(axis=1)
+        for b in range(B):
+            s = np.where(vis, scale * (q[b, :, h] @ k[b, :, h // g].T), -np.inf)
+            s = s[rows]
+            p, l = _softmax_rows(s)
+            o[b, rows, h] = p @ v[b, :, h // g]
+            lse[b, h, rows] = l
+    return o, lse
+
+
 def attn_probs(q, k, causal: bool, scale: float, b: int = 0, h: int = 0) -> np.ndarray:
     """The probability matrix P of one (batch, head), for invariant checks."""
     q = np.asarray(q, dtype=np.float64)

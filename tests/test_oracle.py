@@ -371,3 +371,77 @@ def test_chunked_kv_merge_in_order_equals_full(causal):
     om, lm = _merge_in_order(parts)
     np.testing.assert_allclose(om, o, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
+
+
+# ---- block-sparse forward (a block mask over bs x bs blocks) ----
+
+def _mask(Hq, nb, seed, density=0.5):
+    return (np.random.default_rng(seed).random((Hq, nb, nb)) < density).astype(np.uint8)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blockmask_all_ones_is_dense(causal):
+    q, k, v = qkv(N=23, seed=50)
+    o, lse = oracle.attn_fwd(q, k, v, causal, 0.4)
+    m = np.ones((4, 6, 6), dtype=np.uint8)  # blocks of 4, nb = 6
+    o2, lse2 = oracle.attn_fwd_blockmask(q, k, v, m, 4, causal, 0.4)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blockmask_c_matches_numpy(causal):
+    q, k, v = qkv(N=30, seed=51)
+    m = _mask(4, 4, seed=52)  # blocks of 8 over N = 30 (ragged last block)
+    o, lse = oracle.attn_fwd_blockmask(q, k, v, m, 8, causal, 0.3)
+    o2, lse2 = npo.attn_fwd_blockmask(q, k, v, m, 8, causal, 0.3)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isinf(lse), np.isinf(lse2))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse[fin], lse2[fin], rtol=0, atol=1e-12)
+
+
+def test_blockmask_block_diagonal_is_independent_blocks():
+    # each query block sees only its own key block: attention block by block
+    q, k, v = qkv(N=24, seed=53)
+    m = np.zeros((4, 3, 3), dtype=np.uint8)
+    for i in range(3):
+        m[:, i, i] = 1
+    o, lse = oracle.attn_fwd_blockmask(q, k, v, m, 8, False, 0.5)
+    for i in range(3):
+        sl = slice(8 * i, 8 * i + 8)
+        ob, lb = oracle.attn_fwd(q[:, sl], k[:, sl], v[:, sl], False, 0.5)
+        np.testing.assert_allclose(o[:, sl], ob, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, sl], lb, rtol=0, atol=1e-13)
+
+
+def test_blockmask_empty_rows_are_zero_and_minus_infinity():
+    q, k, v = qkv(N=16, seed=54)
+    m = np.ones((4, 2, 2), dtype=np.uint8)
+    m[1, 1, :] = 0       # head 1, query block 1: nothing visible
+    m[2, 0, 0] = 0       # head 2, query block 0 under causal: only block 0 is visible -> empty
+    o, lse = oracle.attn_fwd_blockmask(q, k, v, m, 8, True, 0.5)
+    assert (o[:, 8:, 1] == 0).all() and np.isneginf(lse[:, 1, 8:]).all()
+    assert (o[:, :8, 2] == 0).all() and np.isneginf(lse[:, 2, :8]).all()
+    assert np.isfinite(lse[:, 0]).all() and np.isfinite(lse[:, 3]).all()
+
+
+def test_blockmask_rows_merge_from_their_blocks():
+    # a query row under a block mask is the in-order merge of its visible
+    # blocks' separate results: the split-KV merge applied to a sparse row
+    q, k, v = qkv(N=32, seed=55)
+    m = _mask(4, 4, seed=56, density=0.6)
+    m[:, :, 0] = 1  # every row sees at least block 0
+    o, lse = oracle.attn_fwd_blockmask(q, k, v, m, 8, False, 0.45)
+    for h in range(4):
+        for qb in range(4):
+            parts = []
+            for kb in range(4):
+                if not m[h, qb, kb]:
+                    continue
+                sl = slice(8 * kb, 8 * kb + 8)
+                oc, lc = oracle.attn_fwd_kv(q[:, 8 * qb:8 * qb + 8], k[:, sl], v[:, sl], False, 0.45)
+                parts.append((oc, lc))
+            om, lm = _merge_in_order(parts)
+            np.testing.assert_allclose(om[:, :, h], o[:, 8 * qb:8 * qb + 8, h], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lm[:, h], lse[:, h, 8 * qb:8 * qb + 8], rtol=0, atol=1e-12)
