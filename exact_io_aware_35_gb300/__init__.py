@@ -33,7 +33,7 @@ FA_BWD_AFTER_FWD_TRAIN = FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_D
 # every entry point include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_noalloc",
            "fa_bwd_workspace_size", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
-           "fa_fwd_splitkv_workspace_size",
+           "fa_fwd_splitkv_workspace_size", "fa_fwd_blocksparse",
            "fa_get_device_error",
            "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
 
@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_splitkv_num_splits.restype = i
     lib.fa_fwd_splitkv_workspace_size.argtypes = [i] * 8
     lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+    lib.fa_fwd_blocksparse.argtypes = [vp] * 6 + [i] * 6 + [f, vp]
+    lib.fa_fwd_blocksparse.restype = i
 
     lib.fa_get_device_error.argtypes = [vp]
     lib.fa_get_device_error.restype = i
@@ -248,6 +250,37 @@ def fa_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                             int(num_splits), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_splitkv")
+    return o, lse
+
+
+def fa_fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None,
+                       o=None, lse=None, stream=None):
+    """Block-sparse forward (fa_fwd_blocksparse): block_mask is a CUDA uint8
+    (or bool) tensor [H, nb, nb], nb = ceil(N / 128), nonzero = the block is
+    computed.  Returns (o, lse); rows with no visible key get o = 0 and
+    lse = -inf."""
+    lib = load_library()
+    B, N, Hq, Hkv, d = _dims(q, k)
+    _check(q, "q", (B, N, Hq, d))
+    _check(k, "k", (B, N, Hkv, d))
+    _check(v, "v", (B, N, Hkv, d))
+    nb = (N + 127) // 128
+    if block_mask.dtype == torch.bool:
+        block_mask = block_mask.to(torch.uint8)
+    _check(block_mask, "block_mask", (Hq, nb, nb), torch.uint8)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
+    _check(o, "o", (B, N, Hq, d))
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    st = lib.fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), block_mask.data_ptr(), B, Hq, Hkv, N, d,
+                                int(bool(causal)), float(scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_blocksparse")
     return o, lse
 
 

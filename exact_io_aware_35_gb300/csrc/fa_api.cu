@@ -483,15 +483,62 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
     a.Nq = Nq;
     a.Nk = Nk;
     a.g = pl.g;
+    a.gp = pl.g;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.qpt = pl.qpt;
     a.n_qt = pl.n_qt;
     a.splits = pl.splits;
     a.blocks_per_split = pl.blocks_per_split;
+    a.block_mask = nullptr;
+    a.nkb = 0;
     a.timeout_ns = kWaitTimeoutNs;
     const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_splitkv launch");
+    return FA_OK;
+}
+
+fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const uint8_t* block_mask, int B, int H, int Hkv, int N, int d,
+                             int causal, float scale, void* stream) {
+    t_last_error[0] = 0;
+    fa_status st = check_sizes(B, H, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !block_mask)
+        return FA_ERR_INVALID_ARG;
+    const int nb = (N + kBM - 1) / kBM;
+    if (static_cast<long long>(B) * H * nb > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((st = device_ready(&di)) != FA_OK) return st;
+    DecodeMaps maps;
+    if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
+    DecodeArgs a;
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.part_o = nullptr;
+    a.part_lse = nullptr;
+    a.status = di->status;
+    a.B = B;
+    a.Hq = H;
+    a.Hkv = Hkv;
+    a.Nq = N;
+    a.Nk = N;
+    a.g = H / Hkv;
+    a.gp = 1;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.qpt = kBM;
+    a.n_qt = nb;
+    a.splits = 1;
+    a.blocks_per_split = nb;
+    a.block_mask = block_mask;
+    a.nkb = nb;
+    a.timeout_ns = kWaitTimeoutNs;
+    const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_blocksparse launch");
     return FA_OK;
 }
 

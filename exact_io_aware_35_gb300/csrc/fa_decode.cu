@@ -27,6 +27,10 @@
 //   * with one split the kernel writes bf16 O and lse itself; with several,
 //     fp32 (O_s, lse_s) per split go to the caller's workspace and
 //     fa_decode_combine_kernel merges them.
+// The same kernel serves the block-sparse forward ("FlashAttention Kernel":
+// block-sparse FlashAttention skips the blocks a sparsity mask zeroes): one
+// head's 128 queries per tile, one split, and every role walks only the key
+// blocks the tile's mask row selects.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -45,6 +49,27 @@ struct DecCfg {
     static constexpr int SMEM_BYTES = 1024 + TILE + NSLOT * TILE + NBAR * 8 + 16;
     static constexpr uint32_t TM_S = 0, TM_O = 256;   // S0 [0,128), S1 [128,256), O [256, 256+D)
     static constexpr int THREADS = 192;               // softmax warps 0-3, MMA warp 4, TMA warp 5
+};
+
+// The key blocks a CTA visits: every block of [lo, hi), or, under a block
+// mask, those of [lo, hi) whose mask byte is nonzero.  Every role walks the
+// same sequence.
+struct KeyBlocks {
+    const uint8_t* row;
+    int lo, hi;
+    __device__ int next(int kb) const {
+        ++kb;
+        if (row)
+            while (kb < hi && row[kb] == 0) ++kb;
+        return kb;
+    }
+    __device__ int first() const { return next(lo - 1); }
+    __device__ int count() const {
+        if (!row) return hi > lo ? hi - lo : 0;
+        int n = 0;
+        for (int x = lo; x < hi; ++x) n += row[x] != 0;
+        return n;
+    }
 };
 
 constexpr int kDecWarpMma = 4;
@@ -76,22 +101,26 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     const int warp = warp_id();
     const int lane = lane_id();
 
-    // ---- work decode: split fastest, then query tile, then (batch, kv head)
+    // ---- work decode: split fastest, then query tile, then (batch, head group)
     int t = static_cast<int>(blockIdx.x);
     const int split = t % a.splits;
     t /= a.splits;
     const int qt = t % a.n_qt;
     t /= a.n_qt;
-    const int b = t / a.Hkv;
-    const int hk = t % a.Hkv;
+    const int n_hg = a.Hq / a.gp;
+    const int b = t / n_hg;
+    const int h0 = (t % n_hg) * a.gp;                  // first query head of the tile
+    const int hk = h0 / a.g;                           // the key/value head they share
     const int q0 = qt * a.qpt;                         // first query of the tile
     const int nq_tile = min(a.qpt, a.Nq - q0);         // queries in this tile
-    const int rows = nq_tile * a.g;                    // valid tile rows
+    const int rows = nq_tile * a.gp;                   // valid tile rows
     const int nkv_all = (a.Nk + kBN - 1) / kBN;
     const int jb0 = split * a.blocks_per_split;
     int jb1 = min(jb0 + a.blocks_per_split, nkv_all);
     if (a.causal) jb1 = min(jb1, (q0 + nq_tile - 1 + a.Nk - a.Nq) / kBN + 1);
-    const int nkv = max(0, jb1 - jb0);
+    KeyBlocks blocks{nullptr, jb0, jb1};
+    if (a.block_mask) blocks.row = a.block_mask + (static_cast<size_t>(h0) * a.n_qt + qt) * a.nkb;
+    const int nkv = blocks.count();
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_Q, 1);
@@ -110,7 +139,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     // tile rows the TMA box does not cover start at zero (the MMA reads all 128)
     if (warp < 4) {
         const int r = threadIdx.x;
-        if (r >= a.g * a.qpt) {
+        if (r >= a.gp * a.qpt) {
             for (int c = 0; c < C::NCH; ++c)
                 for (int p = 0; p < 8; ++p)
                     st_shared_v4(sQ + c * C::CHUNK + r * 128 + p * 16, 0u, 0u, 0u, 0u);
@@ -133,13 +162,14 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             const uint64_t pol = l2_policy_evict_first();  // K, V are read once
-            mbar_arrive_expect_tx(BAR_Q, C::NCH * a.g * a.qpt * 128);
+            mbar_arrive_expect_tx(BAR_Q, C::NCH * a.gp * a.qpt * 128);
             for (int c = 0; c < C::NCH; ++c)
-                tma_load_4d(sQ + c * C::CHUNK, &tmQ, BAR_Q, c * 64, hk * a.g, q0, b);
+                tma_load_4d(sQ + c * C::CHUNK, &tmQ, BAR_Q, c * 64, h0, q0, b);
             int last_idx[C::NSLOT];
             for (int s = 0; s < C::NSLOT; ++s) last_idx[s] = -1;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
+            int kb = blocks.first();
+            for (int j = 0; j < nkv && ok; ++j, kb = blocks.next(kb)) {
                 for (int w = 0; w < 2; ++w) {  // K_j then V_j
                     const int idx = 2 * j + w;
                     const int slot = idx % C::NSLOT;
@@ -149,7 +179,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                     mbar_arrive_expect_tx(BAR_KVF(slot), C::TILE);
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d_hint(sKV + slot * C::TILE + c * C::CHUNK, w ? &tmV : &tmK,
-                                         BAR_KVF(slot), c * 64, hk, (jb0 + j) * kBN, b, pol);
+                                         BAR_KVF(slot), c * 64, hk, kb * kBN, b, pol);
                     last_idx[slot] = idx;
                 }
             }
@@ -223,15 +253,16 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         // ================= softmax: one tile row per thread =================
         const int r = threadIdx.x;  // tile row = TMEM lane
         const bool valid = r < rows;
-        const int qn = q0 + (valid ? r / a.g : 0);     // query index
-        const int h = hk * a.g + (valid ? r % a.g : 0);  // query head
+        const int qn = q0 + (valid ? r / a.gp : 0);  // query index
+        const int h = h0 + (valid ? r % a.gp : 0);   // query head
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t tO = tbase + C::TM_O + lane_off;
         const float sl2 = a.scale_log2;
         const int lim = a.causal ? min(qn + a.Nk - a.Nq, a.Nk - 1) : a.Nk - 1;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
+        int kb = blocks.first();
+        for (int j = 0; j < nkv; ++j, kb = blocks.next(kb)) {
             if (!(ok = mbar_wait(BAR_SF(j & 1), (j >> 1) & 1, a.status, a.timeout_ns, 46))) break;
             tc_fence_after();
             const uint32_t tS = tbase + C::TM_S + (j & 1) * kBN + lane_off;
@@ -245,7 +276,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             float x[kBN];
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
-            const int kbase = (jb0 + j) * kBN;
+            const int kbase = kb * kBN;
             if (kbase + kBN - 1 > lim) {  // causal edge or ragged tail
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
@@ -451,7 +482,7 @@ cudaError_t launch_decode_d(const DecodeMaps& mp, const DecodeArgs& a, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const long long nblk = static_cast<long long>(a.B) * a.Hkv * a.n_qt * a.splits;
+    const long long nblk = static_cast<long long>(a.B) * (a.Hq / a.gp) * a.n_qt * a.splits;
     if (nblk <= 0 || nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<static_cast<unsigned>(nblk), C::THREADS, C::SMEM_BYTES, st>>>(mp.q, mp.k, mp.v, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

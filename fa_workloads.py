@@ -116,6 +116,35 @@ def decode_min_bytes(w: DecodeWorkload) -> int:
     return kv + qo + 4 * w.B * w.Hq * w.Nq
 
 
+def block_sparse_mask(Hq: int, N: int, seed: int, window: int = 2, density: float = 0.1):
+    """A synthetic block mask [Hq, nb, nb] (uint8, nb = ceil(N / 128)): per
+    head, a local window of query block i +- `window` key blocks, key block 0
+    (every query sees the first tokens), and each other block with probability
+    `density`, drawn from the seed."""
+    nb = (N + 127) // 128
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    i = torch.arange(nb)
+    local = (i[:, None] - i[None, :]).abs() <= window
+    m = torch.rand((Hq, nb, nb), generator=g) < density
+    m |= local
+    m[:, :, 0] = True
+    return m.to(torch.uint8)
+
+
+def block_sparse_flops(mask, N: int, d: int, B: int, causal: bool) -> float:
+    """FLOPs of the 128 x 128 blocks the kernel computes (QK^T and PV, 4 * 128
+    * 128 * d each, ragged edge blocks at their true size), summed over heads
+    and the batch; under the causal mask blocks above the diagonal are skipped
+    and diagonal blocks count in full, as they are computed."""
+    nb = (N + 127) // 128
+    rows = torch.tensor([min(128, N - 128 * x) for x in range(nb)], dtype=torch.float64)
+    m = mask.to(torch.float64)
+    if causal:
+        m = m * torch.tril(torch.ones(nb, nb, dtype=torch.float64))
+    return float(4.0 * d * B * (m * rows[:, None] * rows[None, :]).sum())
+
+
 def describe(w: Workload) -> str:
     return (f"B{w.B} Hq{w.Hq} Hkv{w.Hkv} N{w.N} d{w.d} "
             f"{'causal' if w.causal else 'non-causal'} scale={w.scale:.6g}")

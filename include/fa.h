@@ -235,6 +235,23 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int 
                                      int num_splits);
 
 /*
+ * Block-sparse forward: fa_fwd computed only over the 128 x 128 blocks a
+ * block mask selects ("FlashAttention Kernel": block-sparse FlashAttention
+ * skips the blocks a sparsity mask zeroes).
+ *   q, k, v, o, lse, B, H, Hkv, N, d, causal, scale: as fa_fwd
+ *   block_mask: device bytes [H, nb, nb] with nb = ceil(N / 128); query i of
+ *        head h may see key j only when block_mask[h][i / 128][j / 128] != 0
+ *        (and, with causal, j <= i).  Read only.
+ * A query row with no visible key gets o = 0 and lse = -inf.  Each thread
+ * block takes one 128-query tile of one head and visits only the key blocks
+ * its mask row selects.  Errors as fa_fwd; FA_ERR_INVALID_ARG also for a
+ * null block_mask.
+ */
+fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const uint8_t* block_mask, int B, int H, int Hkv, int N, int d,
+                             int causal, float scale, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded wait ran
  * out in some kernel since the last call) or FA_ERR_CUDA (the synchronise

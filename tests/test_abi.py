@@ -156,3 +156,17 @@ def test_splitkv_invalid_arguments_rejected_on_host(lib):
     assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
     assert call(H=256, Hkv=1) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_blocksparse_invalid_arguments_rejected_on_host(lib):
+    import exact_io_aware_35_gb300 as fa
+
+    def call(ptr=256, mask=256, N=1000, d=128, H=4, Hkv=2, scale=0.1):
+        return lib.fa_fwd_blocksparse(ptr, ptr, ptr, ptr, ptr, mask, 1, H, Hkv, N, d, 0,
+                                      ctypes.c_float(scale), None)
+    assert call(mask=None) == fa.FA_ERR_INVALID_ARG
+    assert call(ptr=8) == fa.FA_ERR_INVALID_ARG
+    assert call(N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(H=6, Hkv=4) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
