@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the float64 CPU oracle, timed
     python bench.py --workload decode32k      # the split-KV decode path (its own line)
+    python bench.py --workload sparse8k       # the block-sparse forward (its own line)
 
 A step is one training forward plus one backward pass over one batch of the
 workload (default: B4 Hq32 Hkv8 N8192 d128 causal -- the N >= 8192, d = 128
@@ -34,6 +35,10 @@ import torch  # noqa: E402
 import fa_workloads as W  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOPS and % of GB300 BF16 tensor peak at N=2k–128k, d=64/128"
+SPARSE_METRIC = ("block-sparse attention forward: TFLOPS of the computed 128x128 blocks and % of "
+                 "GB300 BF16 tensor peak")
+# block-sparse forward: the gqa8k shape with a synthetic block mask
+SPARSE_WORKLOADS = {"sparse8k": ("gqa8k", 24)}
 DECODE_METRIC = ("split-KV decode attention: GB/s of the compulsory HBM bytes (K, V, Q, O, lse) "
                  "and % of the measured HBM copy bandwidth")
 DEFAULT_WORKLOAD = "gqa8k"
@@ -594,13 +599,156 @@ def run_decode(args):
     return 0
 
 
+def run_sparse(args):
+    """One step = one fa_fwd_blocksparse call over the gqa8k shape under a
+    local-window + first-block + random block mask; the dense causal fa_fwd
+    on the same inputs is timed beside it for the saving."""
+    import exact_io_aware_35_gb300 as fa
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    wname, mseed = SPARSE_WORKLOADS[args.workload]
+    base = W.WORKLOADS[wname]
+    if args.batch:
+        base = base.with_(B=args.batch)
+    w = base.with_(seed=base.seed + 1000 * rank)
+    x = W.make_inputs(w, with_dout=False)
+    mask_h = W.block_sparse_mask(w.Hq, w.N, seed=mseed)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    dvc = {n: t.to(dev) for n, t in host.items()}
+    q, k, v = dvc["q"], dvc["k"], dvc["v"]
+    mask = mask_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), device=dev, dtype=torch.float32)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_fwd_blocksparse(q, k, v, mask, causal=w.causal, scale=w.scale, o=o, lse=lse)
+
+    def dense():
+        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+        dense()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error during warm-up")
+    K = args.steps
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record()
+            fn()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    ms = timed(step)
+    dense_ms = timed(dense)
+    if ws > 1:
+        torch.distributed.barrier()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error in the timed region")
+    out_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    h2d = tensor_bytes(*host.values())
+    d2h = tensor_bytes(o, lse)
+
+    def e2e_step():
+        for n, t in host.items():
+            dvc[n].copy_(t, non_blocking=True)
+        step()
+        out_host["o"].copy_(o, non_blocking=True)
+        out_host["lse"].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(t_timed0, time.time())
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / K
+    t = torch.tensor([ms, e2e_ms, dense_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms, dense_ms = (float(u) for u in t.tolist())
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    flops = W.block_sparse_flops(mask_h, w.N, w.d, w.B, w.causal) * ws
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    nb = (w.N + 127) // 128
+    tri = torch.tril(torch.ones(nb, nb)) if w.causal else torch.ones(nb, nb)
+    density = float((mask_h.float() * tri).sum() / (w.Hq * tri.sum()))
+    line = {"metric": SPARSE_METRIC, "value": tf, "unit": "TFLOPS", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, shape of the workload; seeded block mask)",
+            "config": {"workload": args.workload, "shape": W.describe(w),
+                       "mask": f"local window +-2 blocks, key block 0, 10% random; "
+                               f"{density:.3f} of the causal blocks",
+                       "global_batch": w.B * ws, "seq_len": w.N,
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "frac_of_peak": tf / ws / peak, "peak_tflops": peak,
+            "peak_source": peaks["source"] + " burst bf16",
+            "dense_causal_ms": dense_ms, "speedup_vs_dense": dense_ms / ms,
+            "gpu_launches": K,
+            "roofline": {"kernel": "fa_decode_split_kernel (block-mask walk)", "bound": "tensor",
+                         "achieved": tf / ws, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / ws / peak, "peak_source": peaks["source"] + " burst",
+                         "launch_ms": ms, "algorithmic_work_per_launch": flops / ws,
+                         "traffic": None},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
+    if clk is not None:
+        line["clocks"] = clk
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        # one head of batch element 0 under its mask row
+        xs = W.make_inputs(base.with_(B=1), with_dout=False)
+        sub = (xs["q"][:, :, :1], xs["k"][:, :, :1], xs["v"][:, :, :1])
+        t0 = time.perf_counter()
+        oracle.attn_fwd_blockmask(*sub, mask_h[:1].numpy(), 128, w.causal, w.scale)
+        secs = time.perf_counter() - t0
+        sflops = W.block_sparse_flops(mask_h[:1], w.N, w.d, 1, w.causal)
+        line["cpu_baseline"] = {"value": sflops / secs / 1e12, "unit": "TFLOPS",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": "batch element 0, head 0 under its mask", "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
+                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
+                    sorted(SPARSE_WORKLOADS))
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
@@ -608,6 +756,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.workload in W.DECODE_WORKLOADS:
         return run_decode_reference(args) if args.impl == "reference" else run_decode(args)
+    if args.workload in SPARSE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the block-sparse line has no "
+                              "reference arm; the oracle is timed in its cpu_baseline"}))
+            return 0
+        return run_sparse(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
