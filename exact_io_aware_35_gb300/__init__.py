@@ -33,7 +33,8 @@ FA_BWD_AFTER_FWD_TRAIN = FA_BWD_PREP_DOUT | FA_BWD_DSUM | FA_BWD_DKDV | FA_BWD_D
 # every entry point include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_train", "fa_bwd", "fa_bwd_stage", "fa_bwd_noalloc",
            "fa_bwd_workspace_size", "fa_fwd_splitkv", "fa_fwd_splitkv_num_splits",
-           "fa_fwd_splitkv_workspace_size", "fa_fwd_blocksparse",
+           "fa_fwd_splitkv_workspace_size", "fa_fwd_blocksparse", "fa_fwd_fp8",
+           "fa_fwd_fp8_workspace_size",
            "fa_get_device_error",
            "fa_status_string", "fa_last_cuda_error", "fa_debug_watchdog_probe")
 
@@ -76,6 +77,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
     lib.fa_fwd_blocksparse.argtypes = [vp] * 6 + [i] * 6 + [f, vp]
     lib.fa_fwd_blocksparse.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp] * 6 + [i] * 6 + [f, i, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_workspace_size.argtypes = [i] * 5
+    lib.fa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
 
     lib.fa_get_device_error.argtypes = [vp]
     lib.fa_get_device_error.restype = i
@@ -281,6 +286,43 @@ def fa_fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float |
                                 int(bool(causal)), float(scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_blocksparse")
+    return o, lse
+
+
+FA_FP8_ROTATE = 1
+
+
+def fa_fwd_fp8_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_fp8_workspace_size(B, H, Hkv, N, d))
+
+
+def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, rotate: bool = True,
+               o=None, lse=None, workspace=None, stream=None):
+    """FP8 (e4m3) forward (fa_fwd_fp8), d = 128: bf16 q, k, v in, bf16 o and
+    fp32 lse out; rotate = incoherent processing of q and k.  Returns (o, lse)."""
+    lib = load_library()
+    B, N, Hq, Hkv, d = _dims(q, k)
+    _check(q, "q", (B, N, Hq, d))
+    _check(k, "k", (B, N, Hkv, d))
+    _check(v, "v", (B, N, Hkv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
+    _check(o, "o", (B, N, Hq, d))
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    ws_bytes = fa_fwd_fp8_workspace_size(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError("workspace too small")
+    st = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        workspace.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                        FA_FP8_ROTATE if rotate else 0, _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return o, lse
 
 

@@ -544,6 +544,128 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
 
 }  // extern "C"
 
+namespace fa {
+namespace {
+
+// A tiled 4-D tensor map over bytes (e4m3), 128-byte swizzle.
+fa_status make_map_u8(CUtensorMap* m, const void* ptr, const cuuint64_t (&dims)[4],
+                      const cuuint64_t (&strides)[3], const cuuint32_t (&box)[4]) {
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr),
+                          const_cast<cuuint64_t*>(dims), const_cast<cuuint64_t*>(strides),
+                          const_cast<cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(t_last_error, sizeof(t_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+// Byte offsets of the FP8 workspace: q8, k8, vt8, sq, sk, sv, vmax (each
+// 256-aligned).
+struct Fp8Layout {
+    size_t q8, k8, vt8, sq, sk, sv, vmax, total;
+    int nb, ldv;
+};
+
+Fp8Layout fp8_layout(int B, int H, int Hkv, int N) {
+    Fp8Layout L{};
+    L.nb = (N + 127) / 128;
+    L.ldv = (N + 15) / 16 * 16;
+    L.q8 = 0;
+    L.k8 = L.q8 + up256(static_cast<size_t>(B) * N * H * 128);
+    L.vt8 = L.k8 + up256(static_cast<size_t>(B) * N * Hkv * 128);
+    L.sq = L.vt8 + up256(static_cast<size_t>(B) * Hkv * 128 * L.ldv);
+    L.sk = L.sq + up256(static_cast<size_t>(B) * H * L.nb * 4);
+    L.sv = L.sk + up256(static_cast<size_t>(B) * Hkv * L.nb * 4);
+    L.vmax = L.sv + up256(static_cast<size_t>(B) * Hkv * 4);
+    L.total = L.vmax + up256(static_cast<size_t>(B) * Hkv * 4);
+    return L;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+size_t fa_fwd_fp8_workspace_size(int B, int H, int Hkv, int N, int d) {
+    if (check_sizes(B, H, Hkv, N, d, 1.f) != FA_OK || d != 128) return 0;
+    return fa::fp8_layout(B, H, Hkv, N).total;
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                     void* workspace, int B, int H, int Hkv, int N, int d, int causal,
+                     float scale, int flags, void* stream) {
+    t_last_error[0] = 0;
+    fa_status st = check_sizes(B, H, Hkv, N, d, scale);
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (flags & ~FA_FP8_ROTATE) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((st = device_ready(&di)) != FA_OK) return st;
+    const fa::Fp8Layout L = fa::fp8_layout(B, H, Hkv, N);
+    Fp8Maps maps;
+    {
+        const cuuint64_t dq[4] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                                  static_cast<cuuint64_t>(B)};
+        const cuuint64_t sq[3] = {128, static_cast<cuuint64_t>(H) * 128,
+                                  static_cast<cuuint64_t>(N) * H * 128};
+        const cuuint64_t dk[4] = {128, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(N),
+                                  static_cast<cuuint64_t>(B)};
+        const cuuint64_t sk[3] = {128, static_cast<cuuint64_t>(Hkv) * 128,
+                                  static_cast<cuuint64_t>(N) * Hkv * 128};
+        const cuuint64_t dv[4] = {static_cast<cuuint64_t>(L.ldv), 128,
+                                  static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(B)};
+        const cuuint64_t sv[3] = {static_cast<cuuint64_t>(L.ldv),
+                                  static_cast<cuuint64_t>(L.ldv) * 128,
+                                  static_cast<cuuint64_t>(L.ldv) * 128 * Hkv};
+        const cuuint32_t box_rows[4] = {128, 1, 128, 1};
+        const cuuint32_t box_vt[4] = {128, 128, 1, 1};
+        if ((st = fa::make_map_u8(&maps.q8, at<void>(workspace, L.q8), dq, sq, box_rows)) != FA_OK)
+            return st;
+        if ((st = fa::make_map_u8(&maps.k8, at<void>(workspace, L.k8), dk, sk, box_rows)) != FA_OK)
+            return st;
+        if ((st = fa::make_map_u8(&maps.vt8, at<void>(workspace, L.vt8), dv, sv, box_vt)) != FA_OK)
+            return st;
+    }
+    Fp8Args a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.q8 = at<uint8_t>(workspace, L.q8);
+    a.k8 = at<uint8_t>(workspace, L.k8);
+    a.vt8 = at<uint8_t>(workspace, L.vt8);
+    a.sq = at<float>(workspace, L.sq);
+    a.sk = at<float>(workspace, L.sk);
+    a.sv = at<float>(workspace, L.sv);
+    a.vmax = at<uint32_t>(workspace, L.vmax);
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.status = di->status;
+    a.B = B;
+    a.Hq = H;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.g = H / Hkv;
+    a.ldv = L.ldv;
+    a.nb = L.nb;
+    a.causal = causal ? 1 : 0;
+    a.rotate = (flags & FA_FP8_ROTATE) ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f * (a.rotate ? 1.f / 128.f : 1.f);
+    a.timeout_ns = kWaitTimeoutNs;
+    const cudaError_t e = launch_fp8(maps, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
+    return FA_OK;
+}
+
+}  // extern "C"
+
 extern "C" {
 
 fa_status fa_get_device_error(void* stream) {

@@ -1,0 +1,451 @@
+// fa_fp8.cu -- FP8 (e4m3) attention forward for sm_103a, head dimension 128.
+//
+// What it computes: O = softmax(scale * Q K^T [+ causal]) V and lse, as
+// fa_fwd, with Q, K, V and P entering the products as e4m3 values -- the
+// low-precision forward the pages describe for FlashAttention-3: block
+// quantisation (one scale per block instead of per tensor) and "incoherent
+// processing", a random orthogonal rotation of Q and K that spreads outliers
+// before they are quantised ("FlashAttention and the Kernel Era", the FP8
+// paragraph; "FlashAttention 1, 2, and 3 Explained", section 4).
+//
+//   * Quantisation (three small kernels): every 128-row block of each head of
+//     Q and of K gets its own scale amax / 448 (448 = the largest e4m3); with
+//     rotation on, the rows are first multiplied by diag(s) H, H the 128-point
+//     Walsh-Hadamard matrix (unnormalised, so H H^T = 128 I, folded into the
+//     softmax scale) and s fixed random signs, which leaves Q K^T unchanged.
+//     V gets one scale per head and is stored transposed (d rows x keys), the
+//     K-major layout the P V product needs as its B operand.
+//   * Forward: one 128-query tile of one head per CTA, two CTAs per SM (16 KB
+//     tiles, 256 TMEM columns each: S, then P in e4m3 over it, and O), so one
+//     CTA's products overlap the other's softmax.  S = Q8 K8^T and O += P8 V8
+//     are tcgen05.mma kind::f8f6f4 (K = 32 per instruction); S is scaled by
+//     scale * log2 e * sq * sk_j in the softmax; P (at most 2^8 under the lazy
+//     rescale, inside e4m3's range) is rounded to e4m3 and written back to
+//     TMEM as the A operand of P V; O is multiplied by sv / l at the end.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kF8Tile = 128 * 128;  // bytes of a 128 x 128 e4m3 tile
+constexpr int kF8Slots = 4;         // K / V^T ring slots (two key blocks)
+constexpr int kF8Threads = 192;     // softmax warps 0-3, MMA warp 4, TMA warp 5
+constexpr int kF8WarpMma = 4;
+constexpr int kF8WarpLoad = 5;
+constexpr float kE4m3Max = 448.f;
+
+// The fixed sign of column c in the rotation diag(s) H: the top bit of
+// c * 2654435761 (mod 2^32) -- a multiplicative hash, the same on every call.
+__device__ __forceinline__ float rot_sign(int c) {
+    return ((static_cast<uint32_t>(c) * 2654435761u) >> 31) ? -1.f : 1.f;
+}
+
+// x[i] = element 4 * lane + i of a 128-element row held by one warp.  In
+// place: y[k] = sum_c (-1)^popcount(k & c) x[c] (the Walsh-Hadamard transform
+// in natural order), butterflies over strides 1, 2 inside the lane and 4..64
+// across lanes.
+__device__ __forceinline__ void hadamard128(float (&x)[4], int lane) {
+    float a = x[0] + x[1], b = x[0] - x[1];
+    x[0] = a;
+    x[1] = b;
+    a = x[2] + x[3];
+    b = x[2] - x[3];
+    x[2] = a;
+    x[3] = b;
+    a = x[0] + x[2];
+    b = x[0] - x[2];
+    x[0] = a;
+    x[2] = b;
+    a = x[1] + x[3];
+    b = x[1] - x[3];
+    x[1] = a;
+    x[3] = b;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float y = __shfl_xor_sync(0xffffffffu, x[i], s);
+            x[i] = (lane & s) ? (y - x[i]) : (x[i] + y);
+        }
+}
+
+// One 128-row block of one head of q or k: two passes over the rows (max |x|,
+// then the quantised bytes), one warp per row at a time.
+__global__ void __launch_bounds__(128) fp8_rows_kernel(const uint16_t* __restrict__ x,
+                                                       uint8_t* __restrict__ x8,
+                                                       float* __restrict__ sx, int N, int H,
+                                                       int nb, int rotate) {
+    __shared__ float red[4];
+    const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blk * 128;
+    auto load = [&](int n, float (&v)[4]) {
+        const uint2 u = *reinterpret_cast<const uint2*>(
+            x + ((static_cast<size_t>(b) * N + n) * H + h) * 128 + 4 * lane);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xffff0000u);
+        if (rotate) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] *= rot_sign(4 * lane + i);
+            hadamard128(v, lane);
+        }
+    };
+    float m = 0.f;
+    for (int rr = warp; rr < 128; rr += 4) {
+        const int n = r0 + rr;
+        if (n >= N) break;
+        float v[4];
+        load(n, v);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    const float inv = m > 0.f ? kE4m3Max / m : 1.f;
+    if (threadIdx.x == 0) sx[(static_cast<size_t>(b) * H + h) * nb + blk] = m > 0.f ? m / kE4m3Max : 1.f;
+    for (int rr = warp; rr < 128; rr += 4) {
+        const int n = r0 + rr;
+        if (n >= N) break;
+        float v[4];
+        load(n, v);
+        *reinterpret_cast<uint32_t*>(x8 + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
+                                     4 * lane) =
+            pack_e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+    }
+}
+
+// max |v| of each 128-key block of each (batch, kv head) into vmax (float bits,
+// atomicMax: non-negative floats order like their bits).
+__global__ void __launch_bounds__(128) fp8_vmax_kernel(const uint16_t* __restrict__ v,
+                                                       uint32_t* __restrict__ vmax, int N,
+                                                       int Hkv) {
+    const int blk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < 128 * 16; i += 128) {  // 16-byte pieces of the block
+        const int n = blk * 128 + i / 16;
+        if (n >= N) break;
+        const uint4 u = *reinterpret_cast<const uint4*>(
+            v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + (i % 16) * 8);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = max(m, (w[j] & 0x7fffu) << 16);
+            m = max(m, w[j] & 0x7fff0000u);
+        }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(vmax + static_cast<size_t>(b) * Hkv + hk, m);
+}
+
+// V^T in e4m3 with one scale per head: each CTA turns a 128-key block into
+// 128 rows (one per head-dimension column) of 128 bytes; keys past N are 0.
+__global__ void __launch_bounds__(128) fp8_vt_kernel(const uint16_t* __restrict__ v,
+                                                     const uint32_t* __restrict__ vmax,
+                                                     uint8_t* __restrict__ vt8,
+                                                     float* __restrict__ sv, int N, int Hkv,
+                                                     int ldv) {
+    __shared__ uint16_t tile[128][128 + 8];  // [key][column]
+    const int blk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const float m = __uint_as_float(vmax[static_cast<size_t>(b) * Hkv + hk]);
+    const float inv = m > 0.f ? kE4m3Max / m : 1.f;
+    if (blk == 0 && threadIdx.x == 0) sv[static_cast<size_t>(b) * Hkv + hk] = m > 0.f ? m / kE4m3Max : 1.f;
+    for (int i = threadIdx.x; i < 128 * 16; i += 128) {
+        const int kk = i / 16, c8 = (i % 16) * 8;
+        const int n = blk * 128 + kk;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N)
+            u = *reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + c8);
+        *reinterpret_cast<uint4*>(&tile[kk][c8]) = u;
+    }
+    __syncthreads();
+    const int c = threadIdx.x;  // head-dimension column = output row
+    uint8_t* dst = vt8 + ((static_cast<size_t>(b) * Hkv + hk) * 128 + c) * ldv + blk * 128;
+    for (int k16 = 0; k16 < 128; k16 += 16) {
+        if (blk * 128 + k16 >= ldv) break;
+        uint32_t w[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                f[e] = __uint_as_float(static_cast<uint32_t>(tile[k16 + 4 * q4 + e][c]) << 16) * inv;
+            w[q4] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + k16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__global__ void __launch_bounds__(kF8Threads, 2)
+    fa_fp8_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmVt, const Fp8Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + kF8Tile;  // slot s at s * kF8Tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF8Tile + kF8Slots * kF8Tile);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kF8Slots + 4);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t BAR_Q = bar0;
+    auto BAR_KVF = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto BAR_KVE = [&](int s) { return bar0 + 8u * (1 + kF8Slots + s); };
+    const uint32_t BAR_SF = bar0 + 8u * (1 + 2 * kF8Slots);  // S(j) ready
+    const uint32_t BAR_PF = BAR_SF + 8u;                      // P(j) written, O rescaled
+    const uint32_t BAR_OF = BAR_SF + 16u;                     // all products done
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+    const int per = a.B * a.Hq;
+    const int qt = a.nb - 1 - static_cast<int>(blockIdx.x) / per;  // longest tiles first
+    const int bh = static_cast<int>(blockIdx.x) % per;
+    const int b = bh / a.Hq;
+    const int h = bh % a.Hq;
+    const int hk = h / a.g;
+    const int nkv = a.causal ? min(qt + 1, a.nb) : a.nb;
+
+    if (warp == 0 && lane == 0) {
+        mbar_init(BAR_Q, 1);
+        for (int s = 0; s < kF8Slots; ++s) {
+            mbar_init(BAR_KVF(s), 1);
+            mbar_init(BAR_KVE(s), 1);
+        }
+        mbar_init(BAR_SF, 1);
+        mbar_init(BAR_PF, 128);
+        mbar_init(BAR_OF, 1);
+        fence_barrier_init();
+    }
+    if (warp == kF8WarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;  // S / P [0, 128), O [128, 256)
+
+    if (warp == kF8WarpLoad) {
+        // ================= TMA producer: Q, then K_j, V^T_j alternately =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmVt);
+            const uint64_t pol = l2_policy_evict_last();  // re-read by every query tile
+            mbar_arrive_expect_tx(BAR_Q, kF8Tile);
+            tma_load_4d(sQ, &tmQ, BAR_Q, 0, h, qt * 128, b);
+            int last_idx[kF8Slots];
+            for (int s = 0; s < kF8Slots; ++s) last_idx[s] = -1;
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; ++j)
+                for (int w = 0; w < 2 && ok; ++w) {
+                    const int idx = 2 * j + w, slot = idx % kF8Slots;
+                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / kF8Slots) & 1) ^ 1u, a.status,
+                                         a.timeout_ns, 50)))
+                        break;
+                    mbar_arrive_expect_tx(BAR_KVF(slot), kF8Tile);
+                    if (w == 0)
+                        tma_load_4d_hint(sKV + slot * kF8Tile, &tmK, BAR_KVF(slot), 0, hk, j * 128,
+                                         b, pol);
+                    else
+                        tma_load_4d_hint(sKV + slot * kF8Tile, &tmVt, BAR_KVF(slot), j * 128, 0,
+                                         hk, b, pol);
+                    last_idx[slot] = idx;
+                }
+            mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 51);
+            for (int s = 0; s < kF8Slots; ++s)
+                if (last_idx[s] >= 0)
+                    mbar_wait(BAR_KVF(s), (last_idx[s] / kF8Slots) & 1, a.status, a.timeout_ns, 51);
+        }
+        __syncwarp();
+    } else if (warp == kF8WarpMma) {
+        // ================= MMA issuer: S(0); then per block PV(j), S(j+1) =================
+        // S and P share TMEM columns 0-127: S(j+1) is issued after PV(j), which
+        // reads P(j), so the tensor core's in-order execution keeps them apart
+        if (lane == 0) {
+            constexpr uint32_t ID = idesc_e4m3(128, 128);
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t q_lo = sdesc_lo(sQ, 16);
+            const uint32_t tS = tbase, tO = tbase + 128;
+            auto landed = [&](int idx) {
+                const bool r = mbar_wait(BAR_KVF(idx % kF8Slots), (idx / kF8Slots) & 1, a.status,
+                                         a.timeout_ns, 52);
+                tc_fence_after();
+                return r;
+            };
+            auto issue_s = [&](int j) {
+                const int slot = (2 * j) % kF8Slots;
+                const uint32_t k_lo = sdesc_lo(sKV + slot * kF8Tile, 16);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // 32 e4m3 = 32 bytes of the 128-byte rows
+                    mma_f8_ss(tS, sdesc_at(q_lo, HI, ks * 32), sdesc_at(k_lo, HI, ks * 32), ID,
+                              ks > 0);
+                mma_commit(BAR_SF);
+                mma_commit(BAR_KVE(slot));
+            };
+            bool ok = mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 53) && landed(0);
+            if (ok) issue_s(0);
+            for (int j = 0; j < nkv && ok; ++j) {
+                if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 54))) break;
+                tc_fence_after();
+                if (!(ok = landed(2 * j + 1))) break;
+                const int vslot = (2 * j + 1) % kF8Slots;
+                const uint32_t v_lo = sdesc_lo(sKV + vslot * kF8Tile, 16);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // 32 keys = 8 TMEM columns of P
+                    mma_f8_ts(tO, tS + ks * 8, sdesc_at(v_lo, HI, ks * 32), ID,
+                              (j > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(BAR_KVE(vslot));
+                if (j + 1 < nkv) {
+                    if (!(ok = landed(2 * j + 2))) break;
+                    issue_s(j + 1);
+                }
+            }
+            mma_commit(BAR_OF);
+            mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 55);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax: one query row per thread =================
+        const int r = threadIdx.x;
+        const int grow = qt * 128 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tbase + lane_off, tO = tbase + 128 + lane_off;
+        const float sq = a.sq[(static_cast<size_t>(b) * a.Hq + h) * a.nb + qt];
+        const float* skrow = a.sk + (static_cast<size_t>(b) * a.Hkv + hk) * a.nb;
+        const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            if (!(ok = mbar_wait(BAR_SF, j & 1, a.status, a.timeout_ns, 56))) break;
+            tc_fence_after();
+            const float sl2 = a.scale_log2 * sq * skrow[j];
+            uint32_t s[128];
+            tmem_ld32(tS + 0, s);
+            tmem_ld32(tS + 32, s + 32);
+            tmem_ld32(tS + 64, s + 64);
+            tmem_ld32(tS + 96, s + 96);
+            tmem_wait_ld();
+            reg_fence<128>(s);
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]) * sl2;
+            const int kbase = j * 128;
+            if (kbase + 127 > lim) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+            }
+            float mk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
+#pragma unroll
+            for (int c = 16; c < 128; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
+            const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                                   fmaxf(mk[6], mk[7]));
+            const float m_new = fmaxf(m_ref, mx);
+            const bool need = m_new > m_ref + 8.f;  // lazy rescale: P stays <= 2^8 < 448
+            float alpha = 1.f;
+            if (need) {
+                alpha = ex2(m_ref - m_new);
+                l *= alpha;
+                m_ref = m_new;
+            }
+            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float ls = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                const float p0 = ex2(x[c] + neg), p1 = ex2(x[c + 1] + neg);
+                const float p2 = ex2(x[c + 2] + neg), p3 = ex2(x[c + 3] + neg);
+                ls += (p0 + p1) + (p2 + p3);
+                pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            l += ls;
+            tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S
+            // O was last written by PV(j-1), which finished before S(j)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int cb = 0; cb < 128; cb += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cb, o);
+                    tmem_wait_ld();
+                    reg_fence<32>(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + cb, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR_PF);
+        }
+        // ---- epilogue: O * sv / l -> bf16, plain stores; lse
+        const bool ok_e = ok && mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 57);
+        if (ok_e) {
+            tc_fence_after();
+            const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;
+            uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * 128;
+#pragma unroll
+            for (int cb = 0; cb < 128; cb += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + cb, o);
+                tmem_wait_ld();
+                reg_fence<32>(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+                if (grow < a.N)
+#pragma unroll
+                    for (int p4 = 0; p4 < 4; ++p4)
+                        reinterpret_cast<uint4*>(dst + cb)[p4] =
+                            make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
+            }
+            if (grow < a.N)
+                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                    (m_ref + log2f(l)) * 0.6931471805599453f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kF8WarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 256);
+    }
+}
+
+constexpr int kF8Smem = 1024 + kF8Tile + kF8Slots * kF8Tile + (2 * kF8Slots + 4) * 8 + 16;
+
+}  // namespace
+
+cudaError_t launch_fp8(const Fp8Maps& m, const Fp8Args& a, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(a.vmax, 0, sizeof(uint32_t) * a.B * a.Hkv, st);
+    if (e != cudaSuccess) return e;
+    fp8_rows_kernel<<<dim3(a.nb, a.Hq, a.B), 128, 0, st>>>(a.q, a.q8, a.sq, a.N, a.Hq, a.nb,
+                                                           a.rotate);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fp8_rows_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.k, a.k8, a.sk, a.N, a.Hkv, a.nb,
+                                                            a.rotate);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fp8_vmax_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.v, a.vmax, a.N, a.Hkv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fp8_vt_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.v, a.vmax, a.vt8, a.sv, a.N, a.Hkv,
+                                                          a.ldv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kF8Smem)) != cudaSuccess)
+        return e;
+    const long long nblk = static_cast<long long>(a.nb) * a.B * a.Hq;
+    if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    fa_fp8_fwd_kernel<<<static_cast<unsigned>(nblk), kF8Threads, kF8Smem, st>>>(m.q8, m.k8, m.vt8,
+                                                                              a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

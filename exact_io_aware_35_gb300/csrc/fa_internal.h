@@ -145,6 +145,42 @@ struct DecodeMaps {
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int d,
                           cudaStream_t stream);
 
+// FP8 (e4m3) forward (fa_fp8.cu), d = 128.  q8, k8: [B, N, H, 128] bytes, one
+// scale per (batch, head, 128-row block) (sq, sk: [B, H, nb]); vt8: V^T per
+// head, [B, Hkv, 128, ldv] bytes (ldv = N rounded up to 16, padding zero),
+// one scale per (batch, kv head) (sv: [B, Hkv]).  Element = byte * scale.
+struct Fp8Args {
+    // inputs of the quantisation (bf16) and its outputs
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    uint8_t* q8;
+    uint8_t* k8;
+    uint8_t* vt8;
+    float* sq;
+    float* sk;
+    float* sv;
+    uint32_t* vmax;     // [B, Hkv] max |v| as float bits (zeroed before the prep)
+    // the forward
+    uint16_t* o;        // [B, N, Hq, 128] bf16
+    float* lse;         // [B, Hq, N]
+    uint32_t* status;
+    int B, Hq, Hkv, N, g, ldv, nb;
+    int causal;
+    int rotate;         // q, k rows multiplied by diag(signs) H_128 before quantising
+    float scale_log2;   // scale * log2(e), / 128 when rotated (H_128 H_128^T = 128 I)
+    uint64_t timeout_ns;
+};
+
+struct Fp8Maps {
+    CUtensorMap q8, k8;  // dims (128, H, N, B) bytes, box 128 x 1 x 128 x 1
+    CUtensorMap vt8;     // dims (ldv, 128, Hkv, B) bytes, box 128 x 128 x 1 x 1
+};
+
+// Quantisation of q, k, v into the fp8 buffers of `args` (three kernels and a
+// memset), then the forward kernel.
+cudaError_t launch_fp8(const Fp8Maps& maps, const Fp8Args& args, cudaStream_t stream);
+
 // Tensor maps of one call (all 4-D: d, H, N, B; box 64 x 1 x 128 x 1).
 struct FwdMaps {
     CUtensorMap q, k, v, o;

@@ -252,6 +252,31 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
                              int causal, float scale, void* stream);
 
 /*
+ * FP8 (e4m3) forward, head dimension 128: fa_fwd with Q, K, V and P entering
+ * the products as e4m3 values behind block quantisation ("FlashAttention and
+ * the Kernel Era", the FP8 paragraph; "FlashAttention 1, 2, and 3 Explained",
+ * section 4: FP8 with block quantisation and incoherent processing).
+ *   q, k, v, o, lse, B, H, Hkv, N, causal, scale: as fa_fwd (bf16 in and out);
+ *        d must be 128 (FA_ERR_UNSUPPORTED otherwise)
+ *   workspace: fa_fwd_fp8_workspace_size(...) bytes, 256-byte aligned,
+ *        caller-owned: the e4m3 copies (q and k with one scale per
+ *        128-row block of each head, v transposed with one scale per head)
+ *   flags: 0 or FA_FP8_ROTATE -- multiply the rows of q and k by a fixed
+ *        random-sign Walsh-Hadamard matrix before quantising them (Q K^T is
+ *        unchanged; outliers are spread over the row)
+ * Accuracy: e4m3 keeps 4 significant bits, so O carries relative errors of a
+ * few percent per element where bf16 carries a fraction of one; the library
+ * tests bound rel-L2 by 5e-2 on N(0, 1) inputs.  Errors as fa_fwd.
+ */
+enum { FA_FP8_ROTATE = 1 };
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                     void* workspace, int B, int H, int Hkv, int N, int d, int causal,
+                     float scale, int flags, void* stream);
+
+/* Bytes of the FP8 forward's workspace (0 for invalid sizes or d != 128). */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (a bounded wait ran
  * out in some kernel since the last call) or FA_ERR_CUDA (the synchronise

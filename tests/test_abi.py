@@ -170,3 +170,24 @@ def test_blocksparse_invalid_arguments_rejected_on_host(lib):
     assert call(H=6, Hkv=4) == fa.FA_ERR_INVALID_ARG
     assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp8_workspace_and_invalid_arguments(lib):
+    import exact_io_aware_35_gb300 as fa
+    B, H, Hkv, N = 2, 4, 2, 300
+    nb, ldv = 3, 304
+    want = (_up256(B * N * H * 128) + _up256(B * N * Hkv * 128) + _up256(B * Hkv * 128 * ldv) +
+            _up256(B * H * nb * 4) + _up256(B * Hkv * nb * 4) + 2 * _up256(B * Hkv * 4))
+    assert lib.fa_fwd_fp8_workspace_size(B, H, Hkv, N, 128) == want
+    assert lib.fa_fwd_fp8_workspace_size(B, H, Hkv, N, 64) == 0
+
+    def call(ptr=256, ws=256, d=128, flags=1, N=300, scale=0.1):
+        return lib.fa_fwd_fp8(ptr, ptr, ptr, ptr, ptr, ws, 1, 4, 2, N, d, 1,
+                              ctypes.c_float(scale), flags, None)
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert call(ws=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=272) == fa.FA_ERR_INVALID_ARG
+    assert call(flags=2) == fa.FA_ERR_INVALID_ARG
+    assert call(ptr=8) == fa.FA_ERR_INVALID_ARG
+    assert call(N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG

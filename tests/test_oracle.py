@@ -445,3 +445,62 @@ def test_blockmask_rows_merge_from_their_blocks():
             om, lm = _merge_in_order(parts)
             np.testing.assert_allclose(om[:, :, h], o[:, 8 * qb:8 * qb + 8, h], rtol=0, atol=1e-12)
             np.testing.assert_allclose(lm[:, h], lse[:, h, 8 * qb:8 * qb + 8], rtol=0, atol=1e-12)
+
+
+# ---- the FP8 model (block quantisation, incoherent processing) ----
+
+from oracle import fp8 as f8  # noqa: E402
+
+
+def test_e4m3_rounding_fixes_every_value_and_ties_go_even():
+    vals = f8.e4m3_values()
+    assert len(vals) == 254 and vals.max() == 448.0 and vals[vals > 0].min() == 2.0 ** -9
+    np.testing.assert_array_equal(f8.e4m3_round(vals), vals)
+    pos = np.unique(vals[vals >= 0])
+    mids = (pos[:-1] + pos[1:]) / 2
+    got = f8.e4m3_round(mids)
+    # a midpoint goes to the neighbour whose mantissa is even
+    lo_even = np.array([int(round(p / 2.0 ** (max(np.floor(np.log2(p)), -6) - 3))) % 2 == 0
+                        if p > 0 else True for p in pos[:-1]])
+    np.testing.assert_array_equal(got, np.where(lo_even, pos[:-1], pos[1:]))
+    # nearest otherwise, and saturation
+    x = np.random.default_rng(60).uniform(-500, 500, 2000)
+    y = f8.e4m3_round(x)
+    inside = np.abs(x) <= 448
+    nearest = vals[np.abs(x[inside, None] - vals[None, :]).argmin(axis=1)]
+    np.testing.assert_array_equal(np.abs(y[inside]), np.abs(nearest))
+    assert (np.abs(y[~inside]) == 448).all()
+
+
+def test_hadamard_rotation_preserves_scores():
+    H = f8.hadamard()
+    np.testing.assert_array_equal(H @ H.T, 128 * np.eye(128))
+    s = f8.rot_signs()
+    assert set(np.unique(s)) == {-1.0, 1.0}
+    q, k = rnd((7, 128), 61), rnd((9, 128), 62)
+    qr, kr = (q * s) @ H.T, (k * s) @ H.T
+    np.testing.assert_allclose(qr @ kr.T, 128 * (q @ k.T), rtol=1e-12, atol=1e-10)
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_model_without_rounding_is_exact_attention(rotate, causal):
+    # with the e4m3 rounding switched off, the model's rotation, block scales,
+    # lazy-rescaled online softmax and normalisation give the exact result
+    q, k, v = rnd((1, 300, 4, 128), 63), rnd((1, 300, 2, 128), 64), rnd((1, 300, 2, 128), 65)
+    o, lse = f8.attn_fwd_fp8(q, k, v, causal, 0.09, rotate, quantize=False)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 0.09)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-11)
+
+
+def test_fp8_block_scales_map_block_maxima_to_448():
+    x = rnd((1, 200, 2, 128), 66) * np.array([1.0, 50.0])[None, None, :, None]
+    y = f8.quantize_blocks(x, rotate=False)
+    for h in range(2):
+        for r0 in (0, 128):
+            blk, yb = x[0, r0:r0 + 128, h], y[0, r0:r0 + 128, h]
+            i = np.unravel_index(np.abs(blk).argmax(), blk.shape)
+            # the maximum maps to 448, which e4m3 holds exactly
+            assert abs(yb[i] - blk[i]) <= 1e-12 * abs(blk[i])
+            assert np.abs(yb - blk).max() <= np.abs(blk).max() * 2.0 ** -4
