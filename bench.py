@@ -4,6 +4,7 @@
     python bench.py --impl reference ...      # the float64 CPU oracle, timed
     python bench.py --workload decode32k      # the split-KV decode path (its own line)
     python bench.py --workload sparse8k       # the block-sparse forward (its own line)
+    python bench.py --workload fp8_8k         # the FP8 (e4m3) forward (its own line)
 
 A step is one training forward plus one backward pass over one batch of the
 workload (default: B4 Hq32 Hkv8 N8192 d128 causal -- the N >= 8192, d = 128
@@ -39,6 +40,9 @@ SPARSE_METRIC = ("block-sparse attention forward: TFLOPS of the computed 128x128
                  "GB300 BF16 tensor peak")
 # block-sparse forward: the gqa8k shape with a synthetic block mask
 SPARSE_WORKLOADS = {"sparse8k": ("gqa8k", 24)}
+FP8_METRIC = ("FP8 (e4m3) attention forward: nominal TFLOPS (4*B*H*N^2*d, halved causal) and % of "
+              "GB300 FP8 tensor peak (measured bf16 peak x the nominal fp8/bf16 ratio 2)")
+FP8_WORKLOADS = {"fp8_8k": "gqa8k"}
 DECODE_METRIC = ("split-KV decode attention: GB/s of the compulsory HBM bytes (K, V, Q, O, lse) "
                  "and % of the measured HBM copy bandwidth")
 DEFAULT_WORKLOAD = "gqa8k"
@@ -741,6 +745,144 @@ def run_sparse(args):
     return 0
 
 
+def run_fp8(args):
+    """One step = one fa_fwd_fp8 call (quantisation of q, k, v + the FP8
+    forward) over the gqa8k shape; the bf16 inference fa_fwd on the same
+    inputs is timed beside it."""
+    import exact_io_aware_35_gb300 as fa
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    base = W.WORKLOADS[FP8_WORKLOADS[args.workload]]
+    if args.batch:
+        base = base.with_(B=args.batch)
+    w = base.with_(seed=base.seed + 1000 * rank)
+    x = W.make_inputs(w, with_dout=False)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    dvc = {n: t.to(dev) for n, t in host.items()}
+    q, k, v = dvc["q"], dvc["k"], dvc["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), device=dev, dtype=torch.float32)
+    wsp = torch.empty(fa.fa_fwd_fp8_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.fa_fwd_fp8(q, k, v, causal=w.causal, scale=w.scale, rotate=True, o=o, lse=lse,
+                      workspace=wsp)
+
+    def quant():
+        fa.fa_fwd_fp8(q, k, v, causal=w.causal, scale=w.scale, rotate=True, o=o, lse=lse,
+                      workspace=wsp, stage=fa.FA_FP8_QUANTIZE_ONLY)
+
+    def attend():
+        fa.fa_fwd_fp8(q, k, v, causal=w.causal, scale=w.scale, rotate=True, o=o, lse=lse,
+                      workspace=wsp, stage=fa.FA_FP8_ATTEND_ONLY)
+
+    def bf16():
+        fa.fa_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+        bf16()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error during warm-up")
+    K = args.steps
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record()
+            fn()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = time.time()
+    ms = timed(step)
+    quant_ms = timed(quant)
+    attn_ms = timed(attend)
+    bf16_ms = timed(bf16)
+    if ws > 1:
+        torch.distributed.barrier()
+    if fa.fa_get_device_error() != fa.FA_OK:
+        raise RuntimeError("device status error in the timed region")
+    out_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    h2d = tensor_bytes(*host.values())
+    d2h = tensor_bytes(o, lse)
+
+    def e2e_step():
+        for n, t in host.items():
+            dvc[n].copy_(t, non_blocking=True)
+        step()
+        out_host["o"].copy_(o, non_blocking=True)
+        out_host["lse"].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(t_timed0, time.time())
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / K
+    t = torch.tensor([ms, e2e_ms, bf16_ms, quant_ms, attn_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms, bf16_ms, quant_ms, attn_ms = (float(u) for u in t.tolist())
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    flops = W.fwd_flops(w) * ws
+    tf = flops / (ms * 1e-3) / 1e12
+    attn_tf = flops / ws / (attn_ms * 1e-3) / 1e12
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    line = {"metric": FP8_METRIC, "value": tf, "unit": "TFLOPS", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (bf16 in and out)",
+            "data": "synthetic (seeded N(0,1) bf16, shape of the workload)",
+            "config": {"workload": args.workload, "shape": W.describe(w),
+                       "global_batch": w.B * ws, "seq_len": w.N,
+                       "quantisation": "q, k per 128-row block and head, rotated; v per head",
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                       "l2": "flushed by a 256 MiB write before every timed step"},
+            "frac_of_peak": tf / ws / peak8, "peak_tflops": peak8,
+            "peak_source": peaks["source"] + " burst bf16 x 2 (nominal fp8/bf16 ratio)",
+            "bf16_fwd_ms": bf16_ms, "speedup_vs_bf16": bf16_ms / ms,
+            "quantise_ms": quant_ms, "attention_ms": attn_ms,
+            "attention_tflops": attn_tf, "attention_speedup_vs_bf16": bf16_ms / attn_ms,
+            "gpu_launches": K * 5,
+            "roofline": {"kernel": "fa_fp8_fwd_kernel (FA_FP8_ATTEND_ONLY call)",
+                         "bound": "tensor", "achieved": attn_tf, "peak": peak8,
+                         "unit": "TFLOP/s", "frac": attn_tf / peak8,
+                         "peak_source": peaks["source"] + " burst bf16 x 2", "launch_ms": attn_ms,
+                         "algorithmic_work_per_launch": flops / ws, "traffic": None},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
+    if clk is not None:
+        line["clocks"] = clk
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,7 +890,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
-                    sorted(SPARSE_WORKLOADS))
+                    sorted(SPARSE_WORKLOADS) + sorted(FP8_WORKLOADS))
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling cases)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
@@ -756,12 +898,13 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.workload in W.DECODE_WORKLOADS:
         return run_decode_reference(args) if args.impl == "reference" else run_decode(args)
-    if args.workload in SPARSE_WORKLOADS:
+    if args.workload in SPARSE_WORKLOADS or args.workload in FP8_WORKLOADS:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the block-sparse line has no "
-                              "reference arm; the oracle is timed in its cpu_baseline"}))
+            print(json.dumps({"impl": "reference", "unavailable": "this line (block-sparse or "
+                              "FP8 forward) has no reference arm; the exact oracle is the "
+                              "comparison in its tests"}))
             return 0
-        return run_sparse(args)
+        return run_sparse(args) if args.workload in SPARSE_WORKLOADS else run_fp8(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -289,7 +289,7 @@ def fa_fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float |
     return o, lse
 
 
-FA_FP8_ROTATE = 1
+FA_FP8_ROTATE, FA_FP8_QUANTIZE_ONLY, FA_FP8_ATTEND_ONLY = 1, 2, 4
 
 
 def fa_fwd_fp8_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
@@ -297,9 +297,10 @@ def fa_fwd_fp8_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
 
 
 def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, rotate: bool = True,
-               o=None, lse=None, workspace=None, stream=None):
+               o=None, lse=None, workspace=None, stream=None, stage: int = 0):
     """FP8 (e4m3) forward (fa_fwd_fp8), d = 128: bf16 q, k, v in, bf16 o and
-    fp32 lse out; rotate = incoherent processing of q and k.  Returns (o, lse)."""
+    fp32 lse out; rotate = incoherent processing of q and k; stage 0 = both
+    steps, FA_FP8_QUANTIZE_ONLY or FA_FP8_ATTEND_ONLY = one.  Returns (o, lse)."""
     lib = load_library()
     B, N, Hq, Hkv, d = _dims(q, k)
     _check(q, "q", (B, N, Hq, d))
@@ -320,7 +321,7 @@ def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, rotate
         raise ValueError("workspace too small")
     st = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                         workspace.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
-                        FA_FP8_ROTATE if rotate else 0, _stream_handle(stream))
+                        (FA_FP8_ROTATE if rotate else 0) | int(stage), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_fp8")
     return o, lse

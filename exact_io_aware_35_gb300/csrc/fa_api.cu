@@ -603,7 +603,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     fa_status st = check_sizes(B, H, Hkv, N, d, scale);
     if (st != FA_OK) return st;
     if (d != 128) return FA_ERR_UNSUPPORTED;
-    if (flags & ~FA_FP8_ROTATE) return FA_ERR_INVALID_ARG;
+    if (flags & ~(FA_FP8_ROTATE | FA_FP8_QUANTIZE_ONLY | FA_FP8_ATTEND_ONLY)) return FA_ERR_INVALID_ARG;
+    if ((flags & FA_FP8_QUANTIZE_ONLY) && (flags & FA_FP8_ATTEND_ONLY)) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FA_ERR_INVALID_ARG;
@@ -657,6 +658,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     a.nb = L.nb;
     a.causal = causal ? 1 : 0;
     a.rotate = (flags & FA_FP8_ROTATE) ? 1 : 0;
+    a.quantize = (flags & FA_FP8_ATTEND_ONLY) ? 0 : 1;
+    a.attend = (flags & FA_FP8_QUANTIZE_ONLY) ? 0 : 1;
     a.scale_log2 = scale * 1.4426950408889634f * (a.rotate ? 1.f / 128.f : 1.f);
     a.timeout_ns = kWaitTimeoutNs;
     const cudaError_t e = launch_fp8(maps, a, static_cast<cudaStream_t>(stream));

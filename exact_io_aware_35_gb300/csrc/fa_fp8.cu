@@ -70,52 +70,59 @@ __device__ __forceinline__ void hadamard128(float (&x)[4], int lane) {
         }
 }
 
-// One 128-row block of one head of q or k: two passes over the rows (max |x|,
-// then the quantised bytes), one warp per row at a time.
-__global__ void __launch_bounds__(128) fp8_rows_kernel(const uint16_t* __restrict__ x,
+// One 128-row block of one head of q or k, in one pass: 8 warps of 16 rows
+// each hold their (rotated) rows in registers -- all 16 loads in flight at
+// once -- while the block's max |x| is reduced, then write the bytes.
+__global__ void __launch_bounds__(256) fp8_rows_kernel(const uint16_t* __restrict__ x,
                                                        uint8_t* __restrict__ x8,
                                                        float* __restrict__ sx, int N, int H,
                                                        int nb, int rotate) {
-    __shared__ float red[4];
+    constexpr int RPW = 16;  // rows per warp
+    __shared__ float red[8];
     const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = blk * 128;
-    auto load = [&](int n, float (&v)[4]) {
-        const uint2 u = *reinterpret_cast<const uint2*>(
-            x + ((static_cast<size_t>(b) * N + n) * H + h) * 128 + 4 * lane);
-        v[0] = __uint_as_float(u.x << 16);
-        v[1] = __uint_as_float(u.x & 0xffff0000u);
-        v[2] = __uint_as_float(u.y << 16);
-        v[3] = __uint_as_float(u.y & 0xffff0000u);
+    const int r0 = blk * 128 + warp * RPW;
+    float v[RPW][4];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int n = r0 + rr;
+        uint2 u = make_uint2(0u, 0u);
+        if (n < N)
+            u = *reinterpret_cast<const uint2*>(x + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
+                                                4 * lane);
+        v[rr][0] = __uint_as_float(u.x << 16);
+        v[rr][1] = __uint_as_float(u.x & 0xffff0000u);
+        v[rr][2] = __uint_as_float(u.y << 16);
+        v[rr][3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
         if (rotate) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] *= rot_sign(4 * lane + i);
-            hadamard128(v, lane);
+            for (int i = 0; i < 4; ++i) v[rr][i] *= rot_sign(4 * lane + i);
+            hadamard128(v[rr], lane);
         }
-    };
-    float m = 0.f;
-    for (int rr = warp; rr < 128; rr += 4) {
-        const int n = r0 + rr;
-        if (n >= N) break;
-        float v[4];
-        load(n, v);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[rr][0]), fabsf(v[rr][1])),
+                           fmaxf(fabsf(v[rr][2]), fabsf(v[rr][3]))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) red[warp] = m;
     __syncthreads();
-    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
     const float inv = m > 0.f ? kE4m3Max / m : 1.f;
-    if (threadIdx.x == 0) sx[(static_cast<size_t>(b) * H + h) * nb + blk] = m > 0.f ? m / kE4m3Max : 1.f;
-    for (int rr = warp; rr < 128; rr += 4) {
+    if (threadIdx.x == 0)
+        sx[(static_cast<size_t>(b) * H + h) * nb + blk] = m > 0.f ? m / kE4m3Max : 1.f;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
         const int n = r0 + rr;
-        if (n >= N) break;
-        float v[4];
-        load(n, v);
-        *reinterpret_cast<uint32_t*>(x8 + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
-                                     4 * lane) =
-            pack_e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+        if (n < N)
+            *reinterpret_cast<uint32_t*>(x8 + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
+                                         4 * lane) =
+                pack_e4m3x4(v[rr][0] * inv, v[rr][1] * inv, v[rr][2] * inv, v[rr][3] * inv);
     }
 }
 
@@ -322,6 +329,8 @@ __global__ void __launch_bounds__(kF8Threads, 2)
         for (int j = 0; j < nkv; ++j) {
             if (!(ok = mbar_wait(BAR_SF, j & 1, a.status, a.timeout_ns, 56))) break;
             tc_fence_after();
+            // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
+            // and every exponent is one FMA, two columns per packed f32x2 op
             const float sl2 = a.scale_log2 * sq * skrow[j];
             uint32_t s[128];
             tmem_ld32(tS + 0, s);
@@ -330,23 +339,22 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             tmem_ld32(tS + 96, s + 96);
             tmem_wait_ld();
             reg_fence<128>(s);
-            float x[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(s[c]) * sl2;
             const int kbase = j * 128;
             if (kbase + 127 > lim) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+                for (int c = 0; c < 128; ++c)
+                    s[c] = (kbase + c > lim) ? __float_as_uint(-INFINITY) : s[c];
             }
             float mk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
+            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
 #pragma unroll
             for (int c = 16; c < 128; c += 16)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
+                for (int i = 0; i < 8; ++i)
+                    mk[i] = fmax3(mk[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
             const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
-                                   fmaxf(mk[6], mk[7]));
+                                   fmaxf(mk[6], mk[7])) * sl2;
             const float m_new = fmaxf(m_ref, mx);
             const bool need = m_new > m_ref + 8.f;  // lazy rescale: P stays <= 2^8 < 448
             float alpha = 1.f;
@@ -356,16 +364,26 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                 m_ref = m_new;
             }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float ls = 0.f;
+            const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+            uint64_t ls2[2] = {0, 0};
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-                const float p0 = ex2(x[c] + neg), p1 = ex2(x[c + 1] + neg);
-                const float p2 = ex2(x[c + 2] + neg), p3 = ex2(x[c + 3] + neg);
-                ls += (p0 + p1) + (p2 + p3);
+                float e0, e1, e2, e3;
+                f2_split(fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, negx2),
+                         e0, e1);
+                f2_split(fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2,
+                              negx2), e2, e3);
+                const float p0 = ex2(e0), p1 = ex2(e1), p2 = ex2(e2), p3 = ex2(e3);
+                ls2[0] = add2(ls2[0], f2(p0, p1));
+                ls2[1] = add2(ls2[1], f2(p2, p3));
                 pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
             }
-            l += ls;
+            {
+                float a0, a1;
+                f2_split(add2(ls2[0], ls2[1]), a0, a1);
+                l += a0 + a1;
+            }
             tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S
             // O was last written by PV(j-1), which finished before S(j)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -425,12 +443,14 @@ constexpr int kF8Smem = 1024 + kF8Tile + kF8Slots * kF8Tile + (2 * kF8Slots + 4)
 }  // namespace
 
 cudaError_t launch_fp8(const Fp8Maps& m, const Fp8Args& a, cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(a.vmax, 0, sizeof(uint32_t) * a.B * a.Hkv, st);
-    if (e != cudaSuccess) return e;
-    fp8_rows_kernel<<<dim3(a.nb, a.Hq, a.B), 128, 0, st>>>(a.q, a.q8, a.sq, a.N, a.Hq, a.nb,
+    cudaError_t e = cudaSuccess;
+    if (a.quantize) {
+    if ((e = cudaMemsetAsync(a.vmax, 0, sizeof(uint32_t) * a.B * a.Hkv, st)) != cudaSuccess)
+        return e;
+    fp8_rows_kernel<<<dim3(a.nb, a.Hq, a.B), 256, 0, st>>>(a.q, a.q8, a.sq, a.N, a.Hq, a.nb,
                                                            a.rotate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    fp8_rows_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.k, a.k8, a.sk, a.N, a.Hkv, a.nb,
+    fp8_rows_kernel<<<dim3(a.nb, a.Hkv, a.B), 256, 0, st>>>(a.k, a.k8, a.sk, a.N, a.Hkv, a.nb,
                                                             a.rotate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fp8_vmax_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.v, a.vmax, a.N, a.Hkv);
@@ -438,6 +458,8 @@ cudaError_t launch_fp8(const Fp8Maps& m, const Fp8Args& a, cudaStream_t st) {
     fp8_vt_kernel<<<dim3(a.nb, a.Hkv, a.B), 128, 0, st>>>(a.v, a.vmax, a.vt8, a.sv, a.N, a.Hkv,
                                                           a.ldv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (!a.attend) return cudaSuccess;
     if ((e = cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kF8Smem)) != cudaSuccess)
         return e;

@@ -168,6 +168,7 @@ struct Fp8Args {
     int B, Hq, Hkv, N, g, ldv, nb;
     int causal;
     int rotate;         // q, k rows multiplied by diag(signs) H_128 before quantising
+    int quantize, attend;  // which of the two steps to run
     float scale_log2;   // scale * log2(e), / 128 when rotated (H_128 H_128^T = 128 I)
     uint64_t timeout_ns;
 };

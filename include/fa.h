@@ -261,14 +261,18 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
  *   workspace: fa_fwd_fp8_workspace_size(...) bytes, 256-byte aligned,
  *        caller-owned: the e4m3 copies (q and k with one scale per
  *        128-row block of each head, v transposed with one scale per head)
- *   flags: 0 or FA_FP8_ROTATE -- multiply the rows of q and k by a fixed
+ *   flags: FA_FP8_ROTATE -- multiply the rows of q and k by a fixed
  *        random-sign Walsh-Hadamard matrix before quantising them (Q K^T is
- *        unchanged; outliers are spread over the row)
+ *        unchanged; outliers are spread over the row); FA_FP8_QUANTIZE_ONLY
+ *        -- make the e4m3 copies and stop; FA_FP8_ATTEND_ONLY -- skip the
+ *        copies and use those an earlier call with the same q, k, v and
+ *        FA_FP8_ROTATE setting left in the workspace (e.g. a cache quantised
+ *        once); not both
  * Accuracy: e4m3 keeps 4 significant bits, so O carries relative errors of a
  * few percent per element where bf16 carries a fraction of one; the library
  * tests bound rel-L2 by 5e-2 on N(0, 1) inputs.  Errors as fa_fwd.
  */
-enum { FA_FP8_ROTATE = 1 };
+enum { FA_FP8_ROTATE = 1, FA_FP8_QUANTIZE_ONLY = 2, FA_FP8_ATTEND_ONLY = 4 };
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                      void* workspace, int B, int H, int Hkv, int N, int d, int causal,
                      float scale, int flags, void* stream);

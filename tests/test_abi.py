@@ -187,7 +187,8 @@ def test_fp8_workspace_and_invalid_arguments(lib):
     assert call(d=64) == fa.FA_ERR_UNSUPPORTED
     assert call(ws=0) == fa.FA_ERR_INVALID_ARG
     assert call(ws=272) == fa.FA_ERR_INVALID_ARG
-    assert call(flags=2) == fa.FA_ERR_INVALID_ARG
+    assert call(flags=8) == fa.FA_ERR_INVALID_ARG
+    assert call(flags=6) == fa.FA_ERR_INVALID_ARG   # quantise only and attend only
     assert call(ptr=8) == fa.FA_ERR_INVALID_ARG
     assert call(N=0) == fa.FA_ERR_INVALID_ARG
     assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG

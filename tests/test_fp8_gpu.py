@@ -124,3 +124,20 @@ def test_fp8_bench_shape_sampled(fa):
     assert np.abs(lse_got - lse_r).max() <= TOL_EXACT_LSE
     # the gqa8k recipe draws 0.5 N(0, 1): the algorithm's error is smaller there
     assert rel <= 5e-2, rel
+
+
+def test_quantise_then_attend_equals_one_call(fa):
+    q, k, v = inputs(1, 400, 4, 2, seed=72)
+    o1, l1 = run(fa, q, k, v, True, 0.09, True)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_size(1, 4, 2, 400, 128), dtype=torch.uint8,
+                     device="cuda")
+    o2 = torch.full_like(qd, float("nan"))
+    l2 = torch.full((1, 4, 400), float("nan"), device="cuda")
+    fa.fa_fwd_fp8(qd, kd, vd, causal=True, scale=0.09, o=o2, lse=l2, workspace=ws,
+                  stage=fa.FA_FP8_QUANTIZE_ONLY)
+    assert torch.isnan(o2).all()  # nothing but the copies
+    fa.fa_fwd_fp8(qd, kd, vd, causal=True, scale=0.09, o=o2, lse=l2, workspace=ws,
+                  stage=fa.FA_FP8_ATTEND_ONLY)
+    assert fa.fa_get_device_error() == fa.FA_OK
+    assert torch.equal(o1, o2.cpu()) and torch.equal(l1, l2.cpu())
