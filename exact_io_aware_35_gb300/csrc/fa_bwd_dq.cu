@@ -38,8 +38,8 @@ struct DqCfg : Tiles<D> {
     static constexpr int OFF_V = OFF_K + KS * T::TILE;
     static constexpr int OFF_BAR = OFF_V + VS * T::TILE;
     // barriers: Q/dO, K full/empty[KS], V full/empty[VS], S+dP ready, copied to
-    // registers, dS written, all MMAs done
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 4;
+    // registers, dS written, all MMAs done, dS written seen by the MMA thread
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 384;
 };
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t BAR_LD = BAR_SDF + 8u;   // S(j), dP(j) copied to registers
     const uint32_t BAR_PF = BAR_SDF + 16u;  // dS(j) written
     const uint32_t BAR_ACC = BAR_SDF + 24u;
+    const uint32_t BAR_PFS = BAR_SDF + 32u;  // the MMA thread has seen PF(j) complete
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR_LD, 256 + 1);  // compute threads and the gate
         mbar_init(BAR_PF, 256);
         mbar_init(BAR_ACC, 1);
+        mbar_init(BAR_PFS, 1);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(BAR_SDF);
                 }
                 if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 24))) break;
+                mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
                 tc_fence_after();
                 issue_dq(j);
             }
@@ -337,6 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tDP, pk);  // dS over the first 32 of this half's dP columns
             tmem_wait_st();
             tc_fence_before();
+            // S(j), dP(j) were issued before the MMA thread waits for PF(j-1):
+            // arriving on PF(j) only once that thread has seen PF(j-1) keeps a
+            // fast warp's arrival out of PF(j-1)'s phase and PF from running
+            // two phases ahead of the thread's parity wait
+            if (j > 0 && !(ok = mbar_wait(BAR_PFS, (j - 1) & 1, a.status, a.timeout_ns, 39))) break;
             mbar_arrive(BAR_PF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 27);

@@ -1,0 +1,708 @@
+"""Models of the kernels' mbarrier hand-off protocols, run on the CPU under
+random schedules.
+
+Each kernel's roles (TMA producer, MMA issuer, softmax / compute warpgroups,
+gate and copy warps) are written as generators that yield the same waits,
+arrivals, loads, MMAs and commits, in the same order, as the CUDA code.  TMA
+loads land in any order; the tensor core runs one CTA's MMAs and commits in
+issue order (a commit arrives once everything issued before it has run).
+
+Every shared-memory tile and TMEM region carries a tag naming what it holds
+(K(3), S(1,2), P(1,2), dS(5), O(0,4), ...).  An access names the tag it
+expects, so a schedule in which the tensor core reads a tile before its load
+landed, overwrites S before the softmax read it, or accumulates into O before
+the softmax rescaled it, fails.  The barriers check what the hardware cannot:
+
+* every arrival belongs to the phase it was meant for (an early arrival would
+  complete the wrong phase);
+* a parity wait for phase p is evaluated only while the barrier is at phase
+  p or p + 1 (two phases on, the parity answers wrongly);
+* no schedule deadlocks, and the CTA never exits with a load or an MMA in
+  flight (TMEM and shared memory are released at exit).
+
+The planted-mistake cases at the end change one step of a model (the dQ
+gate's first design, which ended in a launch failure on the GPU; a forward
+S(j+1) issued before P(j) was consumed; a dropped wait) and must fail, which
+shows the checks would catch such a change.
+"""
+import random
+from collections import deque
+
+import pytest
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.phase = name, count, count, 0
+
+    def arrive(self, n, phase):
+        if phase != self.phase:
+            raise ProtocolError(f"{self.name}: arrival for phase {phase} at phase {self.phase}")
+        self.pending -= n
+        if self.pending < 0:
+            raise ProtocolError(f"{self.name}: too many arrivals in phase {phase}")
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def done(self, phase):
+        if self.phase > phase + 1:
+            raise ProtocolError(f"{self.name}: wait for phase {phase} at phase {self.phase}")
+        return self.phase > phase
+
+
+class Cta:
+    """Barriers, buffer tags, loads in flight and the tensor core's queue."""
+
+    def __init__(self, bars):
+        self.bars = {n: Bar(n, c) for n, c in bars.items()}
+        self.mem = {}
+        self.inflight = set()
+        self.loads = []
+        self.tc = deque()
+
+    def read(self, reads, who):
+        for buf, tag in reads.items():
+            if buf in self.inflight:
+                raise ProtocolError(f"{who}: reads {buf} while a load into it is in flight")
+            if self.mem.get(buf) != tag:
+                raise ProtocolError(f"{who}: {buf} holds {self.mem.get(buf)}, expected {tag}")
+
+    def write(self, writes, who):
+        for buf, tag in writes.items():
+            if buf in self.inflight:
+                raise ProtocolError(f"{who}: writes {buf} while a load into it is in flight")
+            self.mem[buf] = tag
+
+    def step(self, who, op):
+        """Carry out a role's op; False when it is a wait that must repeat."""
+        kind = op[0]
+        if kind == "wait":
+            try:
+                return self.bars[op[1]].done(op[2])
+            except ProtocolError as e:
+                raise ProtocolError(f"{who}: {e}") from None
+        if kind == "arrive":
+            self.bars[op[1]].arrive(op[2], op[3])
+        elif kind == "load":
+            _, bar, phase, writes = op
+            for buf in writes:
+                if buf in self.inflight:
+                    raise ProtocolError(f"{who}: second load into {buf}")
+                self.inflight.add(buf)
+            self.loads.append((bar, phase, writes))
+        elif kind in ("mma", "commit"):
+            self.tc.append(op)
+        elif kind == "read":
+            self.read(op[1], who)
+        elif kind == "write":
+            self.write(op[1], who)
+        else:
+            raise ValueError(op)
+        return True
+
+    def land(self, i):
+        bar, phase, writes = self.loads.pop(i)
+        for buf, tag in writes.items():
+            self.inflight.discard(buf)
+            self.mem[buf] = tag
+        self.bars[bar].arrive(1, phase)
+
+    def run_tc(self):
+        op = self.tc.popleft()
+        if op[0] == "commit":
+            self.bars[op[1]].arrive(1, op[2])
+        else:
+            _, name, reads, writes = op
+            self.read(reads, name)
+            self.write(writes, name)
+
+
+def simulate(model, seed, max_steps=500000):
+    """model(rnd) -> (barrier counts, {role: generator}); rnd draws the
+    data-dependent choices (whether a row's reference maximum moves)."""
+    rnd = random.Random(seed)
+    bars, roles = model(random.Random(seed + 1000003))
+    cta = Cta(bars)
+    # every role, the loads and the tensor core get their own speed, so that
+    # any of them may run far ahead of the others
+    speed = {r: rnd.choice((0.05, 0.3, 1.0)) for r in sorted(roles)}
+    p_load, p_tc = rnd.choice((0.05, 0.3, 1.0)), rnd.choice((0.05, 0.3, 1.0))
+    cur = {}
+    for r, g in roles.items():
+        op = next(g, None)
+        if op is not None:
+            cur[r] = op
+    for _ in range(max_steps):
+        if not cur:
+            if cta.tc or cta.loads:
+                raise ProtocolError(f"exit with work in flight: {list(cta.tc)[:2]} {cta.loads[:2]}")
+            return
+        progressed = False
+        for r in rnd.sample(sorted(cur), len(cur)):
+            if rnd.random() >= speed[r]:
+                continue
+            if cta.step(r, cur[r]):
+                progressed = True
+                op = next(roles[r], None)
+                if op is None:
+                    del cur[r]
+                else:
+                    cur[r] = op
+        if cta.loads and rnd.random() < p_load:
+            cta.land(rnd.randrange(len(cta.loads)))
+            progressed = True
+        if cta.tc and rnd.random() < p_tc:
+            cta.run_tc()
+            progressed = True
+        if not progressed and not cta.tc and not cta.loads and all(
+                op[0] == "wait" and not cta.step(r, op) for r, op in cur.items()):
+            raise ProtocolError(f"deadlock: {cur}")
+    raise ProtocolError("did not finish")
+
+
+def each_seed(model, seeds=range(60)):
+    for seed in seeds:
+        simulate(model, seed)
+
+
+def fails_on_some_seed(model, seeds=range(80)):
+    for seed in seeds:
+        try:
+            simulate(model, seed)
+        except ProtocolError:
+            return True
+    return False
+
+
+def kv_ring_producer(n_blocks, nslot, first, tiles=("K", "V"), skip_empty=False):
+    """The forward-style producer: Q, then K_j, V_j of every key block
+    through one ring of nslot tiles; at exit it waits for its last loads."""
+    last = {}
+    yield ("load", "Q", 0, first)
+    for j in range(n_blocks):
+        for w, nm in enumerate(tiles):
+            idx = 2 * j + w
+            s = idx % nslot
+            if not skip_empty:
+                yield ("wait", f"E{s}", idx // nslot - 1)  # a slot's first use passes
+            yield ("load", f"F{s}", idx // nslot, {f"kv{s}": f"{nm}({j})"})
+            last[s] = idx // nslot
+    yield ("wait", "Q", 0)
+    for s, ph in last.items():
+        yield ("wait", f"F{s}", ph)
+
+
+def ring_bars(nslot):
+    bars = {}
+    for s in range(nslot):
+        bars[f"F{s}"] = bars[f"E{s}"] = 1
+    return bars
+
+
+# ---------------------------------------------------------------- dQ kernel
+def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False):
+    """Eight compute warps (w, q): key half w (64 columns of S, dP) and TMEM
+    lanes 32q.. (query rows); each arrives on its own.  The MMA thread
+    arrives on PFS once it has seen dS(j) complete; a warp waits for that
+    before its dS(j+1) arrival, so PF is never a phase ahead of its waiter."""
+    warps = [(w, q) for w in (0, 1) for q in range(4)]
+
+    def model(rnd):
+        bars = {"QDO": 1, "SDF": 1, "LD": 257, "PF": 257 if first_gate_design else 256, "ACC": 1,
+                "PFS": 1}
+        for nm, ns in (("K", KS), ("V", VS)):
+            for s in range(ns):
+                bars[f"{nm}F{s}"] = bars[f"{nm}E{s}"] = 1
+
+        def every(pre, tag):
+            return {f"{pre}.{w}.{q}": tag for w, q in warps}
+
+        def producer():
+            yield ("load", "QDO", 0, dict(every("Q", "Q"), dO="dO"))
+            last = {}
+            for i in range(nj):
+                for nm, ns in (("K", KS), ("V", VS)):
+                    s = i % ns
+                    yield ("wait", f"{nm}E{s}", i // ns - 1)
+                    yield ("load", f"{nm}F{s}", i // ns, {f"{nm}{s}": f"{nm}({i})"})
+                    last[f"{nm}F{s}"] = i // ns
+            yield ("wait", "QDO", 0)
+            for bar, ph in last.items():
+                yield ("wait", bar, ph)
+
+        def gate():
+            for j in range(nj):
+                if j + 1 < nj:
+                    yield ("wait", f"KF{(j + 1) % KS}", (j + 1) // KS)
+                    yield ("wait", f"VF{(j + 1) % VS}", (j + 1) // VS)
+                if j > 0:
+                    yield ("wait", "LD", j - 1)
+                yield ("arrive", "LD", 1, j)
+                if first_gate_design:
+                    # it also held dS(j) back until V_{j+2} had landed
+                    if j + 2 < nj:
+                        yield ("wait", f"VF{(j + 2) % VS}", (j + 2) // VS)
+                    if j > 0:
+                        yield ("wait", "PF", j - 1)
+                    yield ("arrive", "PF", 1, j)
+
+        def copy():
+            yield ("wait", "QDO", 0)
+            yield ("read", {"dO": "dO"})
+
+        def s_mma(jj):
+            return ("mma", f"S({jj})", dict(every("Q", "Q"), **{f"K{jj % KS}": f"K({jj})"}),
+                    every("S", f"S({jj})"))
+
+        def dp_mma(jj):
+            return ("mma", f"dP({jj})", {"dO": "dO", f"V{jj % VS}": f"V({jj})"},
+                    every(f"DP{jj & 1}", f"dP({jj})"))
+
+        def mma():
+            yield ("wait", "QDO", 0)
+            yield ("wait", "KF0", 0)
+            yield s_mma(0)
+            yield ("wait", "VF0", 0)
+            yield dp_mma(0)
+            yield ("commit", "VE0", 0)
+            yield ("commit", "SDF", 0)
+            for j in range(nj):
+                if j + 1 < nj:
+                    yield ("wait", "LD", j)
+                    yield s_mma(j + 1)
+                    yield dp_mma(j + 1)
+                    yield ("commit", f"VE{(j + 1) % VS}", (j + 1) // VS)
+                    yield ("commit", "SDF", j + 1)
+                yield ("wait", "PF", j)
+                if handshake:
+                    yield ("arrive", "PFS", 1, j)
+                reads = dict(every(f"DP{j & 1}", f"dS({j})"), **{f"K{j % KS}": f"K({j})"})
+                if j > 0:
+                    reads["dQ"] = f"dQ({j - 1})"
+                yield ("mma", f"dQ({j})", reads, {"dQ": f"dQ({j})"})
+                yield ("commit", f"KE{j % KS}", j // KS)
+            yield ("commit", "ACC", 0)
+            yield ("wait", "ACC", 0)
+
+        def compute(w, q):
+            me = f"{w}.{q}"
+            for j in range(nj):
+                yield ("wait", "SDF", j)
+                yield ("read", {f"S.{me}": f"S({j})", f"DP{j & 1}.{me}": f"dP({j})"})
+                yield ("arrive", "LD", 32, j)
+                yield ("write", {f"DP{j & 1}.{me}": f"dS({j})"})
+                if handshake and j > 0:
+                    yield ("wait", "PFS", j - 1)
+                yield ("arrive", "PF", 32, j)
+            yield ("wait", "ACC", 0)
+            yield ("read", {"dQ": f"dQ({nj - 1})"})
+            yield ("write", {f"Q.{me}": "dQ out"})  # staging in the Q tile
+
+        roles = {"prod": producer(), "gate": gate(), "copy": copy(), "mma": mma()}
+        for w, q in warps:
+            roles[f"c{w}{q}"] = compute(w, q)
+        return bars, roles
+
+    return model
+
+
+# -------------------------------------------------------------- dK/dV kernel
+def dkdv_model(n_it, NST=2, dk_before_dsf=False):
+    """Sixteen compute warps (g, q): query columns 32g.. of the transposed
+    tiles (warpgroup g) and key rows 32q.. (TMEM lanes)."""
+    warps = [(g, q) for g in range(4) for q in range(4)]
+
+    def model(rnd):
+        bars = {"KV": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1}
+        for s in range(NST):
+            bars[f"STF{s}"] = 1 + 32  # the load, and the 32 lanes' vector writes
+            bars[f"STE{s}"] = 1
+
+        def reg_s(it):  # S^T(it), then P^T(it) / dS^T(it)
+            return "Y" if it & 1 else "X"
+
+        def reg_d(it):  # dP^T(it)
+            return "X" if it & 1 else "Y"
+
+        def region(r, tag):
+            return {f"{r}.{g}.{q}.{c}": tag for g, q in warps for c in "pd"}
+
+        def producer():
+            yield ("load", "KV", 0, {"K": "K", "V": "V"})
+            last = {}
+            for it in range(n_it):
+                s = it % NST
+                yield ("wait", f"STE{s}", it // NST - 1)
+                yield ("load", f"STF{s}", it // NST, {f"stage{s}": f"QdO({it})"})
+                yield ("write", {f"vec{s}": f"lse,D({it})"})
+                yield ("arrive", f"STF{s}", 32, it // NST)
+                last[s] = it // NST
+            yield ("wait", "KV", 0)
+            for s, ph in last.items():
+                yield ("wait", f"STF{s}", ph)
+
+        def st_mma(it):
+            return ("mma", f"S^T({it})", {"K": "K", f"stage{it % NST}": f"QdO({it})"},
+                    region(reg_s(it), f"S^T({it})"))
+
+        def dpt_mma(it):
+            return ("mma", f"dP^T({it})", {"V": "V", f"stage{it % NST}": f"QdO({it})"},
+                    region(reg_d(it), f"dP^T({it})"))
+
+        def acc_mma(it, dk):
+            nm, c, tag = ("dK", "d", "dS^T") if dk else ("dV", "p", "P^T")
+            reads = {f"{reg_s(it)}.{g}.{q}.{c}": f"{tag}({it})" for g, q in warps}
+            reads[f"stage{it % NST}"] = f"QdO({it})"
+            if it > 0:
+                reads[nm] = f"{nm}({it - 1})"
+            return ("mma", f"{nm}({it})", reads, {nm: f"{nm}({it})"})
+
+        def mma():
+            yield ("wait", "KV", 0)
+            yield ("wait", "STF0", 0)
+            yield st_mma(0)
+            yield dpt_mma(0)
+            yield ("commit", "SDF", 0)
+            for it in range(n_it):
+                s, s2 = it % NST, (it + 1) % NST
+                more = it + 1 < n_it
+                if more:
+                    yield ("wait", f"STF{s2}", (it + 1) // NST)
+                    yield ("wait", "LD", it)
+                    yield st_mma(it + 1)  # over dP^T(it)
+                yield ("wait", "PF", it)
+                yield acc_mma(it, False)
+                if not dk_before_dsf:
+                    yield ("wait", "DSF", it)
+                yield acc_mma(it, True)
+                yield ("commit", f"STE{s}", it // NST)
+                if more:
+                    yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
+                    yield ("commit", "SDF", it + 1)
+            yield ("commit", "ACC", 0)
+            yield ("wait", "ACC", 0)
+
+        def compute(g, q):
+            me = f"{g}.{q}"
+            for it in range(n_it):
+                s = it % NST
+                rs, rd = reg_s(it), reg_d(it)
+                yield ("wait", "SDF", it)
+                yield ("read", {f"{rd}.{me}.p": f"dP^T({it})", f"{rd}.{me}.d": f"dP^T({it})",
+                                f"vec{s}": f"lse,D({it})"})
+                yield ("arrive", "LD", 32, it)
+                yield ("read", {f"{rs}.{me}.p": f"S^T({it})", f"{rs}.{me}.d": f"S^T({it})"})
+                yield ("write", {f"{rs}.{me}.p": f"P^T({it})"})
+                yield ("arrive", "PF", 32, it)
+                yield ("write", {f"{rs}.{me}.d": f"dS^T({it})"})
+                yield ("arrive", "DSF", 32, it)
+            yield ("wait", "ACC", 0)
+            yield ("read", {"dV": f"dV({n_it - 1})", "dK": f"dK({n_it - 1})"})
+            yield ("write", {"stage0": "out"})  # staging in stage 0's tiles
+
+        roles = {"prod": producer(), "mma": mma()}
+        for g, q in warps:
+            roles[f"c{g}{q}"] = compute(g, q)
+        return bars, roles
+
+    return model
+
+
+# ------------------------------------------------------------ forward kernel
+def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
+    """Two query tiles: tile 0 multiplies key blocks [0, nkv0), tile 1
+    [0, nkv) (nkv0 < nkv on the causal diagonal); four softmax warps per
+    tile, warp q owning rows 32q.. of S_t and O_t."""
+    rows = range(4)
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
+        bars.update(ring_bars(NSLOT))
+        n_of = (nkv0, nkv)
+
+        def tile(pre, t, tag):
+            return {f"{pre}.{t}.{q}": tag for q in rows}
+
+        def gate():
+            for j in range(nkv):
+                v, kn = 2 * j + 1, 2 * j + 2
+                yield ("wait", f"F{v % NSLOT}", v // NSLOT)
+                if j + 1 < nkv:
+                    yield ("wait", f"F{kn % NSLOT}", kn // NSLOT)
+                for t in (0, 1):
+                    if j >= n_of[t]:
+                        continue
+                    if j > 0:
+                        yield ("wait", f"PF{t}", j - 1)
+                    yield ("arrive", f"PF{t}", 1, j)
+
+        def copy():
+            yield ("wait", "Q", 0)
+            yield ("read", dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            yield ("arrive", "QC", 1, 0)
+
+        def qk(t, j):
+            slot = (2 * j) % NSLOT
+            return ("mma", f"QK({t},{j})", dict(tile("Q", t, "Q"), **{f"kv{slot}": f"K({j})"}),
+                    tile("S", t, f"S({t},{j})"))
+
+        def pv(t, j):
+            slot = (2 * j + 1) % NSLOT
+            reads = dict(tile("S", t, f"P({t},{j})"), **{f"kv{slot}": f"V({j})"})
+            if j > 0:
+                reads.update(tile("O", t, f"O({t},{j - 1})"))
+            return ("mma", f"PV({t},{j})", reads, tile("O", t, f"O({t},{j})"))
+
+        def mma():
+            yield ("wait", "Q", 0)
+            yield ("wait", "F0", 0)
+            yield qk(0, 0)
+            yield ("commit", "SF0", 0)
+            yield qk(1, 0)
+            yield ("commit", "SF1", 0)
+            yield ("commit", "E0", 0)
+            for j in range(nkv):
+                vslot, kidx = (2 * j + 1) % NSLOT, 2 * (j + 1)
+                kslot = kidx % NSLOT
+                if j < nkv0:
+                    yield ("wait", "PF0", j)
+                    yield pv(0, j)
+                    if j == nkv0 - 1:
+                        yield ("commit", "OF0", 0)
+                if j + 1 < nkv0:
+                    yield qk(0, j + 1)
+                    yield ("commit", "SF0", j + 1)
+                if early_qk and j + 1 < nkv:
+                    yield qk(1, j + 1)
+                yield ("wait", "PF1", j)
+                yield pv(1, j)
+                yield ("commit", f"E{vslot}", (2 * j + 1) // NSLOT)
+                if j == nkv - 1:
+                    yield ("commit", "OF1", 0)
+                if j + 1 < nkv:
+                    if not early_qk:
+                        yield qk(1, j + 1)
+                    yield ("commit", "SF1", j + 1)
+                    yield ("commit", f"E{kslot}", kidx // NSLOT)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def softmax(t, q):
+            me = f"{t}.{q}"
+            for j in range(n_of[t]):
+                yield ("wait", f"SF{t}", j)
+                yield ("read", {f"S.{me}": f"S({t},{j})"})
+                yield ("write", {f"S.{me}": f"P({t},{j})"})
+                if j > 0 and rnd.random() < 0.5:  # the reference max moved
+                    yield ("read", {f"O.{me}": f"O({t},{j - 1})"})
+                    yield ("write", {f"O.{me}": f"O({t},{j - 1})"})
+                yield ("arrive", f"PF{t}", 32, j)
+            yield ("wait", f"OF{t}", 0)
+            if copy_q:
+                yield ("wait", "QC", 0)
+            yield ("read", {f"O.{me}": f"O({t},{n_of[t] - 1})"})
+            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
+
+        q_tiles = dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q"))
+        roles = {"prod": kv_ring_producer(nkv, NSLOT, q_tiles), "gate": gate(), "mma": mma()}
+        for t in (0, 1):
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
+        if copy_q:
+            roles["copy"] = copy()
+        return bars, roles
+
+    return model
+
+
+# ----------------------------------------------- split-KV (decode) kernel
+def decode_model(nkv, NSLOT=6, skip_pvd_wait=False):
+    """Four softmax warps, warp q owning rows 32q.. of S0, S1 and O."""
+    rows = range(4)
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 128, "PF1": 128, "PVD": 1, "OF": 1}
+        bars.update(ring_bars(NSLOT))
+
+        def every(pre, tag):
+            return {f"{pre}.{q}": tag for q in rows}
+
+        def landed(idx):
+            return ("wait", f"F{idx % NSLOT}", idx // NSLOT)
+
+        def issue_s(j):
+            idx = 2 * j
+            yield landed(idx)
+            yield ("mma", f"S({j})", {"Q": "Q", f"kv{idx % NSLOT}": f"K({j})"},
+                   every(f"S{j & 1}", f"S({j})"))
+            yield ("commit", f"SF{j & 1}", j >> 1)
+            yield ("commit", f"E{idx % NSLOT}", idx // NSLOT)
+
+        def mma():
+            if nkv == 0:
+                return
+            yield ("wait", "Q", 0)
+            yield from issue_s(0)
+            for j in range(nkv):
+                if j + 1 < nkv:
+                    yield from issue_s(j + 1)
+                yield ("wait", f"PF{j & 1}", j >> 1)
+                idx = 2 * j + 1
+                yield landed(idx)
+                reads = dict(every(f"S{j & 1}", f"P({j})"), **{f"kv{idx % NSLOT}": f"V({j})"})
+                if j > 0:
+                    reads.update(every("O", f"O({j - 1})"))
+                yield ("mma", f"PV({j})", reads, every("O", f"O({j})"))
+                yield ("commit", f"E{idx % NSLOT}", idx // NSLOT)
+                yield ("commit", "PVD", j)
+            yield ("commit", "OF", 0)
+            yield ("wait", "OF", 0)
+
+        def softmax(q):
+            for j in range(nkv):
+                yield ("wait", f"SF{j & 1}", j >> 1)
+                yield ("read", {f"S{j & 1}.{q}": f"S({j})"})
+                yield ("write", {f"S{j & 1}.{q}": f"P({j})"})
+                if j > 0 and rnd.random() < 0.5:  # the reference max moved
+                    if not skip_pvd_wait:
+                        yield ("wait", "PVD", j - 1)
+                    yield ("read", {f"O.{q}": f"O({j - 1})"})
+                    yield ("write", {f"O.{q}": f"O({j - 1})"})
+                yield ("arrive", f"PF{j & 1}", 32, j >> 1)
+            if nkv > 0:
+                yield ("wait", "OF", 0)
+                yield ("read", {f"O.{q}": f"O({nkv - 1})"})
+
+        roles = {"prod": kv_ring_producer(nkv, NSLOT, {"Q": "Q"}), "mma": mma()}
+        for q in rows:
+            roles[f"s{q}"] = softmax(q)
+        return bars, roles
+
+    return model
+
+
+# ------------------------------------- single S buffer (the FP8 forward) -----
+def single_s_model(nkv, NSLOT=4, skip_empty=False):
+    """Four softmax warps over one S buffer (P written over S)."""
+    rows = range(4)
+
+    def model(rnd):
+        bars = {"Q": 1, "SF": 1, "PF": 128, "OF": 1}
+        bars.update(ring_bars(NSLOT))
+
+        def every(pre, tag):
+            return {f"{pre}.{q}": tag for q in rows}
+
+        def landed(idx):
+            return ("wait", f"F{idx % NSLOT}", idx // NSLOT)
+
+        def issue_s(j):
+            idx = 2 * j
+            yield landed(idx)
+            yield ("mma", f"S({j})", {"Q": "Q", f"kv{idx % NSLOT}": f"K({j})"},
+                   every("S", f"S({j})"))
+            yield ("commit", "SF", j)
+            yield ("commit", f"E{idx % NSLOT}", idx // NSLOT)
+
+        def mma():
+            yield ("wait", "Q", 0)
+            yield from issue_s(0)
+            for j in range(nkv):
+                yield ("wait", "PF", j)
+                idx = 2 * j + 1
+                yield landed(idx)
+                reads = dict(every("S", f"P({j})"), **{f"kv{idx % NSLOT}": f"V^T({j})"})
+                if j > 0:
+                    reads.update(every("O", f"O({j - 1})"))
+                yield ("mma", f"PV({j})", reads, every("O", f"O({j})"))
+                yield ("commit", f"E{idx % NSLOT}", idx // NSLOT)
+                if j + 1 < nkv:
+                    yield from issue_s(j + 1)
+            yield ("commit", "OF", 0)
+            yield ("wait", "OF", 0)
+
+        def softmax(q):
+            for j in range(nkv):
+                yield ("wait", "SF", j)
+                yield ("read", {f"S.{q}": f"S({j})"})
+                yield ("write", {f"S.{q}": f"P({j})"})
+                if j > 0 and rnd.random() < 0.5:
+                    yield ("read", {f"O.{q}": f"O({j - 1})"})
+                    yield ("write", {f"O.{q}": f"O({j - 1})"})
+                yield ("arrive", "PF", 32, j)
+            yield ("wait", "OF", 0)
+            yield ("read", {f"O.{q}": f"O({nkv - 1})"})
+
+        prod = kv_ring_producer(nkv, NSLOT, {"Q": "Q"}, tiles=("K", "V^T"), skip_empty=skip_empty)
+        roles = {"prod": prod, "mma": mma()}
+        for q in rows:
+            roles[f"s{q}"] = softmax(q)
+        return bars, roles
+
+    return model
+
+
+# ------------------------------------------------------------------ the kernels
+@pytest.mark.parametrize("nj", [1, 2, 3, 4, 7, 20])
+def test_dq_protocol(nj):
+    each_seed(dq_model(nj))
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
+def test_dkdv_protocol(n_it):
+    each_seed(dkdv_model(n_it))
+
+
+@pytest.mark.parametrize("nkv0,nkv,nslot", [(1, 1, 4), (1, 2, 4), (2, 3, 4), (5, 6, 4), (8, 8, 4),
+                                            (3, 4, 8), (9, 9, 8)])
+@pytest.mark.parametrize("copy_q", [True, False])
+def test_forward_protocol(nkv0, nkv, nslot, copy_q):
+    each_seed(fwd_model(nkv0, nkv, nslot, copy_q))
+
+
+@pytest.mark.parametrize("nkv,nslot", [(0, 6), (1, 6), (2, 6), (3, 6), (7, 6), (20, 6), (13, 12)])
+def test_decode_protocol(nkv, nslot):
+    each_seed(decode_model(nkv, nslot))
+
+
+@pytest.mark.parametrize("nkv", [1, 2, 3, 9])
+def test_single_s_protocol(nkv):
+    each_seed(single_s_model(nkv))
+
+
+# ------------------------------------------------------- planted mistakes
+def test_dq_first_gate_design_is_caught():
+    assert fails_on_some_seed(dq_model(12, handshake=False, first_gate_design=True))
+
+
+def test_dq_without_handshake_is_caught():
+    # without it, a warp that runs a block ahead adds its dS(j) arrival to the
+    # phase of dS(j-1), or dS(j+1) completes before the MMA thread has seen
+    # dS(j), and its parity wait reads the phase as open
+    assert fails_on_some_seed(dq_model(6, handshake=False))
+
+
+def test_forward_early_score_product_is_caught():
+    # S(1, j+1) issued before the softmax has handed P(1, j) back
+    assert fails_on_some_seed(fwd_model(3, 4, early_qk=True))
+
+
+def test_decode_rescale_without_pv_wait_is_caught():
+    # O rescaled while P(j-1) V_{j-1} may still be accumulating into it
+    assert fails_on_some_seed(decode_model(12, skip_pvd_wait=True))
+
+
+def test_dkdv_dk_before_ds_is_caught():
+    # dK += dS^T Q issued before the warpgroups have written dS^T
+    assert fails_on_some_seed(dkdv_model(4, dk_before_dsf=True))
+
+
+def test_ring_without_empty_wait_is_caught():
+    # a load into a ring slot whose previous tile an MMA still has to read
+    assert fails_on_some_seed(single_s_model(9, skip_empty=True))
