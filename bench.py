@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -97,9 +98,14 @@ class ClockSampler:
         self.window = None
 
     def start(self):
+        # the raw samples are kept in FA_BENCH_CLOCKS_DIR when it is set, else
+        # in a temporary file removed once the summary is taken
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            keep = os.environ.get("FA_BENCH_CLOCKS_DIR")
+            d = keep or tempfile.gettempdir()
+            os.makedirs(d, exist_ok=True)
+            self.keep = bool(keep)
+            self.path = os.path.join(d, f"clocks_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
@@ -135,6 +141,8 @@ class ClockSampler:
                                  [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
                 except ValueError:
                     continue
+        if not self.keep:
+            os.remove(self.path)
         if not rows:
             return None
         inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
