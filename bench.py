@@ -216,7 +216,7 @@ def tensor_bytes(*ts) -> int:
 # copy of dO), dK/dV
 KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel")
 KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
-                  "fa_decode_split_kernel": "fa_decode.cu",
+                  "fa_decode_split_kernel": "fa_decode.cu", "fa_fp8_fwd_kernel": "fa_fp8.cu",
                   "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
 LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 1, "fa_bwd_dkdv_kernel": 1,
             "fa_bwd_dq_kernel": 1}
@@ -938,7 +938,8 @@ def run_fp8(args):
                          "bound": "tensor", "achieved": attn_tf, "peak": peak8,
                          "unit": "TFLOP/s", "frac": attn_tf / peak8,
                          "peak_source": peaks["source"] + " burst bf16 x 2", "launch_ms": attn_ms,
-                         "algorithmic_work_per_launch": flops / ws, "traffic": None},
+                         "algorithmic_work_per_launch": flops / ws,
+                         "traffic": measured_traffic("fa_fp8_fwd_kernel", args.workload)},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
     if clk is not None:
