@@ -239,12 +239,19 @@ def kernel_work(w: W.Workload, name: str):
 
 
 def source_hash(name: str) -> str:
+    """Hash of the code (comments and whitespace removed) of a kernel's source
+    file and the shared headers: the stored DRAM counts stay valid across
+    edits that change only comments."""
     import hashlib
+    import re
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "exact_io_aware_35_gb300", "csrc")
     for f in (KERNEL_SOURCES[name], "sm103_ptx.cuh", "fa_internal.h", "fa_bwd_common.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -19,7 +19,11 @@
 // V_{j+1} have landed, so the MMA thread waits on LD and PF only (every wait
 // in the issuing thread costs tensor-core time).  Only LD carries the gate:
 // the warpgroups reach LD(j+1) only after S(j+1), which waits for LD(j), so no
-// arrival can land in the wrong phase.
+// arrival can land in the wrong phase.  PF needs one more step, because S(j+1)
+// is committed before the MMA thread waits for PF(j): the MMA thread arrives
+// on PFS once it has seen PF(j) complete, and a warp waits for that before its
+// PF(j+1) arrival.  Without it a warp that ran a block ahead could arrive in
+// PF(j)'s phase, or PF could complete twice under the MMA thread's parity wait.
 //
 // TMEM (512 columns): S [0,128), dP0 [128,256), dP1 [256,384), dQ [384,384+D).
 #include "fa_bwd_common.cuh"
