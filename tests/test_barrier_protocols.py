@@ -1,11 +1,14 @@
 """Models of the kernels' mbarrier hand-off protocols, run on the CPU under
 random schedules.
 
-Each kernel's roles (TMA producer, MMA issuer, softmax / compute warpgroups,
-gate and copy warps) are written as generators that yield the same waits,
-arrivals, loads, MMAs and commits, in the same order, as the CUDA code.  TMA
-loads land in any order; the tensor core runs one CTA's MMAs and commits in
-issue order (a commit arrives once everything issued before it has run).
+Each kernel's roles (TMA producer, MMA issuer, gate and copy warps, and every
+softmax / compute warp on its own, since each warp arrives on a barrier by
+itself) are written as generators that yield the same waits, arrivals, loads,
+MMAs and commits, in the same order, as the CUDA code.  TMA loads land in any
+order; the tensor core runs one CTA's MMAs and commits in issue order (a
+commit arrives once everything issued before it has run).  Every role, the
+loads and the tensor core get a random speed per schedule, so that any of
+them may run far ahead of the others.
 
 Every shared-memory tile and TMEM region carries a tag naming what it holds
 (K(3), S(1,2), P(1,2), dS(5), O(0,4), ...).  An access names the tag it
@@ -20,10 +23,12 @@ the softmax rescaled it, fails.  The barriers check what the hardware cannot:
 * no schedule deadlocks, and the CTA never exits with a load or an MMA in
   flight (TMEM and shared memory are released at exit).
 
-The planted-mistake cases at the end change one step of a model (the dQ
-gate's first design, which ended in a launch failure on the GPU; a forward
-S(j+1) issued before P(j) was consumed; a dropped wait) and must fail, which
-shows the checks would catch such a change.
+The planted-mistake cases at the end change one step of a model and must
+fail, which shows the checks would catch such a change: the dQ gate's first
+design (it ended in a launch failure on the GPU), the dQ kernel without its
+PF handshake (the model found that gap), a forward S(j+1) issued before P(j)
+was consumed, a rescale of O without waiting for P V, dK issued before dS^T
+was written, and a ring load without its empty-slot wait.
 """
 import random
 from collections import deque
