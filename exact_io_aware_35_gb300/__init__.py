@@ -121,6 +121,15 @@ def _check(t: torch.Tensor, name: str, shape, dtype=torch.bfloat16):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _on_device(device, **tensors):
+    """Every given tensor must sit on `device` (q's): the kernels take raw
+    pointers, and a tensor on another GPU would be read through the wrong
+    device's address space."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, q on {device}")
+
+
 def _dims(q, k):
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q, k must be [B, N, H, d]")
@@ -151,8 +160,11 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, ls
     _check(o, "o", (B, N, Hq, d))
     _check(lse, "lse", (B, Hq, N), torch.float32)
     if o_lo is None:
-        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                        B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+        _on_device(q.device, k=k, v=v, o=o, lse=lse)
+        with torch.cuda.device(q.device):
+            st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                            _stream_handle(stream))
     else:
         _check(o_lo, "o_lo", (B, N, Hq, d))
         ws_bytes = fa_bwd_workspace_size(B, Hq, Hkv, N, d)
@@ -160,9 +172,12 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, o=None, ls
             workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
         if workspace.numel() * workspace.element_size() < ws_bytes:
             raise ValueError("workspace too small")
-        st = lib.fa_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                              o_lo.data_ptr(), lse.data_ptr(), workspace.data_ptr(), B, Hq, Hkv,
-                              N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+        _on_device(q.device, k=k, v=v, o=o, lse=lse, o_lo=o_lo, workspace=workspace)
+        with torch.cuda.device(q.device):
+            st = lib.fa_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  o_lo.data_ptr(), lse.data_ptr(), workspace.data_ptr(), B, Hq,
+                                  Hkv, N, d, int(bool(causal)), float(scale),
+                                  _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
     return o, lse
@@ -201,11 +216,14 @@ def fa_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = No
         raise ValueError("workspace too small")
     if o_lo is not None:
         _check(o_lo, "o_lo", (B, N, Hq, d))
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-            None if o_lo is None else o_lo.data_ptr(),
-            B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
-    st = lib.fa_bwd(*args) if stages == FA_BWD_ALL else lib.fa_bwd_stage(int(stages), *args)
+    _on_device(q.device, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv,
+               workspace=workspace, o_lo=o_lo)
+    with torch.cuda.device(q.device):
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                None if o_lo is None else o_lo.data_ptr(),
+                B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+        st = lib.fa_bwd(*args) if stages == FA_BWD_ALL else lib.fa_bwd_stage(int(stages), *args)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
@@ -249,10 +267,12 @@ def fa_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
         workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
     if ws_bytes and workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError("workspace too small")
-    st = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), None if workspace is None else workspace.data_ptr(),
-                            B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
-                            int(num_splits), _stream_handle(stream))
+    _on_device(q.device, k=k, v=v, o=o, lse=lse, workspace=workspace)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), None if workspace is None else workspace.data_ptr(),
+                                B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+                                int(num_splits), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_splitkv")
     return o, lse
@@ -281,9 +301,11 @@ def fa_fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float |
         lse = torch.empty((B, Hq, N), device=q.device, dtype=torch.float32)
     _check(o, "o", (B, N, Hq, d))
     _check(lse, "lse", (B, Hq, N), torch.float32)
-    st = lib.fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                lse.data_ptr(), block_mask.data_ptr(), B, Hq, Hkv, N, d,
-                                int(bool(causal)), float(scale), _stream_handle(stream))
+    _on_device(q.device, k=k, v=v, o=o, lse=lse, block_mask=block_mask)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), block_mask.data_ptr(), B, Hq, Hkv, N, d,
+                                    int(bool(causal)), float(scale), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_blocksparse")
     return o, lse
@@ -319,9 +341,12 @@ def fa_fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, rotate
         workspace = torch.empty(max(ws_bytes, 256), device=q.device, dtype=torch.uint8)
     if workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError("workspace too small")
-    st = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                        workspace.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
-                        (FA_FP8_ROTATE if rotate else 0) | int(stage), _stream_handle(stream))
+    _on_device(q.device, k=k, v=v, o=o, lse=lse, workspace=workspace)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), workspace.data_ptr(), B, Hq, Hkv, N, d,
+                            int(bool(causal)), float(scale),
+                            (FA_FP8_ROTATE if rotate else 0) | int(stage), _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_fp8")
     return o, lse

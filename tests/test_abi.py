@@ -107,6 +107,18 @@ def test_binding_refuses_cpu_tensors(lib):
         fa.fa_fwd(q, q, q)
 
 
+def test_binding_refuses_tensors_on_another_device():
+    # every wrapper checks that each tensor sits on q's device before it
+    # passes raw pointers to the library
+    import torch
+
+    import exact_io_aware_35_gb300 as fa
+    a = torch.zeros(2)
+    fa._on_device(a.device, k=a, v=None)
+    with pytest.raises(ValueError, match="k is on cpu"):
+        fa._on_device(torch.device("cuda", 0), k=a)
+
+
 def test_splitkv_plan_and_workspace(lib):
     import exact_io_aware_35_gb300 as fa
     # one split: no workspace
