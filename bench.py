@@ -818,6 +818,79 @@ def run_sparse(args):
     return 0
 
 
+def reference_line(args, metric, value, unit, ms, shape, desc):
+    """The JSON line of a reference arm: the oracle timed on the host cores."""
+    import oracle
+    return {"impl": "reference", "metric": metric, "value": value, "unit": unit,
+            "n_gpus": dist_env()[0], "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "shape": shape, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_sparse_reference(args):
+    """The block-mask oracle on one head of batch element 0 under its mask row
+    (the sample the GPU line's CPU baseline uses)."""
+    if dist_env()[1] != 0:
+        return 0
+    import oracle
+    wname, mseed = SPARSE_WORKLOADS[args.workload]
+    w = W.WORKLOADS[wname]
+    mask_h = W.block_sparse_mask(w.Hq, w.N, seed=mseed)
+    xs = W.make_inputs(w.with_(B=1), with_dout=False)
+    sub = (xs["q"][:, :, :1], xs["k"][:, :, :1], xs["v"][:, :, :1])
+    oracle.build()
+
+    def once():
+        t0 = time.perf_counter()
+        oracle.attn_fwd_blockmask(*sub, mask_h[:1].numpy(), 128, w.causal, w.scale)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        once()
+    ms = 1e3 * sum(once() for _ in range(args.steps)) / args.steps
+    sflops = W.block_sparse_flops(mask_h[:1], w.N, w.d, 1, w.causal)
+    desc = (f"batch element 0, head 0 under its mask, full N={w.N} "
+            f"({sflops / 1e9:.1f} GFLOP of computed blocks)")
+    print(json.dumps(reference_line(args, SPARSE_METRIC, sflops / (ms * 1e-3) / 1e12, "TFLOPS",
+                                    ms, W.describe(w), desc)), flush=True)
+    return 0
+
+
+def run_fp8_reference(args):
+    """The float64 model of the FP8 forward (block quantisation, rotation,
+    lazy rescale, e4m3 P) on one head over the first 2048 positions of batch
+    element 0: the model walks rows and blocks in Python, so the sample is
+    kept well under a second per step."""
+    if dist_env()[1] != 0:
+        return 0
+    from oracle import fp8 as ofp8
+    w = W.WORKLOADS[FP8_WORKLOADS[args.workload]]
+    n = min(2048, w.N)
+    xs = W.make_inputs(w.with_(B=1), with_dout=False)
+    q, k, v = (xs[c][:, :n, :1].contiguous() for c in ("q", "k", "v"))
+
+    def once():
+        t0 = time.perf_counter()
+        ofp8.attn_fwd_fp8(q, k, v, w.causal, w.scale, rotate=True)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        once()
+    ms = 1e3 * sum(once() for _ in range(args.steps)) / args.steps
+    sw = w.with_(B=1, Hq=1, Hkv=1, N=n)
+    flops = W.fwd_flops(sw)
+    desc = (f"batch element 0, head 0, positions 0..{n - 1} through the float64 model of the "
+            f"FP8 forward ({flops / 1e9:.2f} nominal GFLOP)")
+    print(json.dumps(reference_line(args, FP8_METRIC, flops / (ms * 1e-3) / 1e12, "TFLOPS", ms,
+                                    W.describe(w), desc)), flush=True)
+    return 0
+
+
 def run_fp8(args):
     """One step = one fa_fwd_fp8 call (quantisation of q, k, v + the FP8
     forward) over the gqa8k shape; the bf16 inference fa_fwd on the same
@@ -972,13 +1045,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.workload in W.DECODE_WORKLOADS:
         return run_decode_reference(args) if args.impl == "reference" else run_decode(args)
-    if args.workload in SPARSE_WORKLOADS or args.workload in FP8_WORKLOADS:
-        if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "this line (block-sparse or "
-                              "FP8 forward) has no reference arm; the exact oracle is the "
-                              "comparison in its tests"}))
-            return 0
-        return run_sparse(args) if args.workload in SPARSE_WORKLOADS else run_fp8(args)
+    if args.workload in SPARSE_WORKLOADS:
+        return run_sparse_reference(args) if args.impl == "reference" else run_sparse(args)
+    if args.workload in FP8_WORKLOADS:
+        return run_fp8_reference(args) if args.impl == "reference" else run_fp8(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
