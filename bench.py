@@ -868,9 +868,21 @@ def run_fp8_reference(args):
     kept well under a second per step."""
     if dist_env()[1] != 0:
         return 0
-    from oracle import fp8 as ofp8
     w = W.WORKLOADS[FP8_WORKLOADS[args.workload]]
-    n = min(2048, w.N)
+    once, flops, desc = fp8_model_sample(w)
+    for _ in range(args.warmup):
+        once()
+    ms = 1e3 * sum(once() for _ in range(args.steps)) / args.steps
+    print(json.dumps(reference_line(args, FP8_METRIC, flops / (ms * 1e-3) / 1e12, "TFLOPS", ms,
+                                    W.describe(w), desc)), flush=True)
+    return 0
+
+
+def fp8_model_sample(w: W.Workload, n: int = 2048):
+    """(timed call, nominal FLOPs, description) of the float64 FP8 model on
+    head 0 of batch element 0 over its first n positions."""
+    from oracle import fp8 as ofp8
+    n = min(n, w.N)
     xs = W.make_inputs(w.with_(B=1), with_dout=False)
     q, k, v = (xs[c][:, :n, :1].contiguous() for c in ("q", "k", "v"))
 
@@ -879,16 +891,10 @@ def run_fp8_reference(args):
         ofp8.attn_fwd_fp8(q, k, v, w.causal, w.scale, rotate=True)
         return time.perf_counter() - t0
 
-    for _ in range(args.warmup):
-        once()
-    ms = 1e3 * sum(once() for _ in range(args.steps)) / args.steps
-    sw = w.with_(B=1, Hq=1, Hkv=1, N=n)
-    flops = W.fwd_flops(sw)
+    flops = W.fwd_flops(w.with_(B=1, Hq=1, Hkv=1, N=n))
     desc = (f"batch element 0, head 0, positions 0..{n - 1} through the float64 model of the "
             f"FP8 forward ({flops / 1e9:.2f} nominal GFLOP)")
-    print(json.dumps(reference_line(args, FP8_METRIC, flops / (ms * 1e-3) / 1e12, "TFLOPS", ms,
-                                    W.describe(w), desc)), flush=True)
-    return 0
+    return once, flops, desc
 
 
 def run_fp8(args):
@@ -1024,6 +1030,13 @@ def run_fp8(args):
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
     if clk is not None:
         line["clocks"] = clk
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        once, sflops, desc = fp8_model_sample(w)
+        secs = once()
+        line["cpu_baseline"] = {"value": sflops / secs / 1e12, "unit": "TFLOPS",
+                                "cores": oracle.num_threads(), "kind": "oracle (float64 FP8 model)",
+                                "sample": desc, "seconds": secs}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
