@@ -210,16 +210,22 @@ def tensor_bytes(*ts) -> int:
     return sum(t.numel() * t.element_size() for t in ts)
 
 
-# event-timed slots of a step; the forward slot is the fa_fwd_train call (the
-# fp16 copies of q, k, v, 2 small kernels, then fa_fwd_kernel), the backward's
-# are the fa_bwd_stage steps: D with max |dO|, dQ (which also writes the fp16
-# copy of dO), dK/dV
-KERNELS = ("fa_fwd_kernel", "fa_bwd_dsum_kernel", "fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel")
-KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", "fa_bwd_dsum_kernel": "fa_bwd.cu",
+# event-timed slots of a step.  The forward slot of a training step is the
+# fa_fwd_train call: the maxima and fp16 copies of q, k, v (f16_absmax_kernel,
+# f16_convert_kernel), then fa_fwd_kernel -- three launches, named for the
+# call; a forward-only workload times the fa_fwd call, one fa_fwd_kernel.
+# The backward's slots are the fa_bwd_stage steps: D with max |dO|, dQ (which
+# also writes the fp16 copy of dO), dK/dV.
+FWD_TRAIN_SLOT = "fa_fwd_train_call"
+KERNELS = (FWD_TRAIN_SLOT, "fa_bwd_dsum_kernel", "fa_bwd_dq_kernel", "fa_bwd_dkdv_kernel")
+KERNEL_SOURCES = {"fa_fwd_kernel": "fa_fwd.cu", FWD_TRAIN_SLOT: "fa_fwd.cu",
+                  "fa_bwd_dsum_kernel": "fa_bwd.cu",
                   "fa_decode_split_kernel": "fa_decode.cu", "fa_fp8_fwd_kernel": "fa_fp8.cu",
                   "fa_bwd_dkdv_kernel": "fa_bwd_dkdv.cu", "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
-LAUNCHES = {"fa_fwd_kernel": 3, "fa_bwd_dsum_kernel": 1, "fa_bwd_dkdv_kernel": 1,
-            "fa_bwd_dq_kernel": 1}
+LAUNCHES = {FWD_TRAIN_SLOT: 3, "fa_fwd_kernel": 1, "fa_bwd_dsum_kernel": 1,
+            "fa_bwd_dkdv_kernel": 1, "fa_bwd_dq_kernel": 1}
+# the arithmetic of the training step, which the "dtype" key names
+TRAIN_DTYPE = "bf16 I/O; P, dS as fp16 against exact scaled fp16 copies; fp32 accumulate"
 
 
 def kernel_work(w: W.Workload, name: str):
@@ -228,7 +234,7 @@ def kernel_work(w: W.Workload, name: str):
     GEMM, halved under the causal mask): fwd 2 GEMMs, dK/dV 4, dQ 3.  dsum:
     bytes of O, o_lo and dO read plus D written."""
     g1 = W.fwd_flops(w) / 2.0  # one N x N x d GEMM over all heads
-    if name == "fa_fwd_kernel":
+    if name in ("fa_fwd_kernel", FWD_TRAIN_SLOT):
         return "tensor", 2 * g1
     if name == "fa_bwd_dkdv_kernel":
         return "tensor", 4 * g1
@@ -458,11 +464,13 @@ def run_gpu(args):
         return 0
 
     peak = peaks["bf16_tflops"]
+    slots = KERNELS[:nk] if w.backward else ("fa_fwd_kernel",)
     value, _ = aggregate(step_ms, flops_step, ws)
     fwd_tf = W.fwd_flops(w) / (fwd_ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": TRAIN_DTYPE if w.backward else "bf16 (bf16 P; fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16, shape of the workload)",
             "config": {"workload": args.workload, "shape": W.describe(w),
                        "global_batch": w.B * ws, "seq_len": w.N,
@@ -471,12 +479,11 @@ def run_gpu(args):
             "frac_of_peak": value / ws / peak,
             "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak, "fwd_ms": fwd_ms,
             "peak_tflops": peak, "peak_source": peaks["source"] + " burst bf16",
-            "gpu_launches": K * ((LAUNCHES["fa_fwd_kernel"] if w.backward else 1) +
-                                 sum(LAUNCHES[n] for n in KERNELS[1:nk]))}
+            "gpu_launches": K * sum(LAUNCHES[n] for n in slots)}
     if w.backward:
         bwd_tf = W.bwd_flops(w) / (bwd_ms * 1e-3) / 1e12
         line.update({"bwd_tflops": bwd_tf, "bwd_frac_of_peak": bwd_tf / peak, "bwd_ms": bwd_ms})
-    km = dict(zip(KERNELS[:nk], kern_ms))
+    km = dict(zip(slots, kern_ms))
     line["kernel_ms"] = km
     line["roofline"] = roofline(w, km, peaks)
     line["e2e"] = {"value": aggregate(e2e_ms, flops_step, ws)[0], "unit": "TFLOPS",

@@ -88,7 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.argtypes = []
     lib.fa_last_cuda_error.restype = ctypes.c_char_p
-    lib.fa_debug_watchdog_probe.argtypes = [ctypes.c_uint64, vp]
+    lib.fa_debug_watchdog_probe.argtypes = [ctypes.c_uint64, i, vp]
     lib.fa_debug_watchdog_probe.restype = i
     _lib = lib
     return lib
@@ -357,7 +357,10 @@ def fa_get_device_error(stream=None) -> int:
     return int(load_library().fa_get_device_error(_stream_handle(stream)))
 
 
-def fa_debug_watchdog_probe(timeout_ns: int, stream=None) -> None:
-    st = load_library().fa_debug_watchdog_probe(int(timeout_ns), _stream_handle(stream))
+def fa_debug_watchdog_probe(timeout_ns: int, num_blocks: int = 1, stream=None) -> None:
+    """Launches num_blocks blocks whose waits nothing satisfies (limit
+    timeout_ns); read the outcome with fa_get_device_error."""
+    st = load_library().fa_debug_watchdog_probe(int(timeout_ns), int(num_blocks),
+                                                _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_debug_watchdog_probe")

@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include <cudaTypedefs.h>
 
 #include "fa.h"
@@ -12,13 +14,29 @@
 
 namespace fa {
 
-// Status word written by bounded waits that run out (one per device: a
-// __device__ variable exists once per device context).
-__device__ uint32_t g_status_word;
+// Status words written by bounded waits that run out (one pair per device: a
+// __device__ variable exists once per device context): [0] the first failure
+// since the host last read it, [1] the id of the last launch that failed.
+__device__ uint32_t g_status_word[2];
 
 namespace {
 
 thread_local char t_last_error[256] = "";
+
+// Launch ids for the bounded waits: every launch gets its own nonzero id, so
+// that its thread blocks can tell a failure of their own launch (stop at
+// once) from one an earlier launch left in the status words.
+std::atomic<uint32_t> g_launch_counter{0};
+
+Watch make_watch(uint32_t* status, uint64_t timeout_ns = kWaitTimeoutNs) {
+    uint32_t id = 0;
+    while (id == 0) id = g_launch_counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    Watch w;
+    w.status = status;
+    w.timeout_ns = timeout_ns;
+    w.launch = id;
+    return w;
+}
 
 fa_status cuda_fail(cudaError_t e, const char* where) {
     snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
@@ -165,7 +183,7 @@ fa_status check_sizes(int B, int H, int Hkv, int N, int d, float scale) {
     return FA_OK;
 }
 
-__global__ void watchdog_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
+__global__ void watchdog_probe_kernel(const Watch w) {
     __shared__ __align__(8) uint64_t bar;
     const uint32_t b = smem_u32(&bar);
     if (threadIdx.x == 0) {
@@ -173,7 +191,7 @@ __global__ void watchdog_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
         fence_barrier_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) mbar_wait(b, 0, status, timeout_ns, 0xFE);  // nothing ever arrives
+    if (threadIdx.x == 0) mbar_wait(b, 0, w, 0xFE);  // nothing ever arrives
     __syncthreads();
 }
 
@@ -247,7 +265,6 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.o_lo = static_cast<uint16_t*>(o_lo);
     a.f16s = workspace ? at<const F16Scales>(workspace, wl.scales) : nullptr;
     a.q16 = workspace ? at<uint16_t>(workspace, wl.q16) : nullptr;
-    a.status = di->status;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
@@ -256,7 +273,7 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
-    a.timeout_ns = kWaitTimeoutNs;
+    a.watch = make_watch(di->status);
     cudaError_t e = launch_fwd(maps, a, d, cs);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
     return FA_OK;
@@ -347,7 +364,6 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
     a.o = static_cast<const uint16_t*>(o);
     a.dout = static_cast<const uint16_t*>(dout);
     a.o_lo = static_cast<const uint16_t*>(o_lo);
-    a.status = di->status;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
@@ -357,7 +373,7 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
     a.causal = causal ? 1 : 0;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.timeout_ns = kWaitTimeoutNs;
+    a.watch = make_watch(di->status);
     if ((stages & 7) == 0) return FA_OK;
     cudaError_t e = launch_bwd(maps, a, stages & 7, cs);
     if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
@@ -476,7 +492,6 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
         a.part_o = static_cast<float*>(workspace);
         a.part_lse = at<float>(workspace, lse_off);
     }
-    a.status = di->status;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
@@ -492,7 +507,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
     a.blocks_per_split = pl.blocks_per_split;
     a.block_mask = nullptr;
     a.nkb = 0;
-    a.timeout_ns = kWaitTimeoutNs;
+    a.watch = make_watch(di->status);
     const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_splitkv launch");
     return FA_OK;
@@ -520,7 +535,6 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
     a.lse = lse;
     a.part_o = nullptr;
     a.part_lse = nullptr;
-    a.status = di->status;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
@@ -536,7 +550,7 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
     a.blocks_per_split = nb;
     a.block_mask = block_mask;
     a.nkb = nb;
-    a.timeout_ns = kWaitTimeoutNs;
+    a.watch = make_watch(di->status);
     const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_blocksparse launch");
     return FA_OK;
@@ -648,7 +662,6 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     a.vmax = at<uint32_t>(workspace, L.vmax);
     a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
-    a.status = di->status;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
@@ -661,7 +674,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     a.quantize = (flags & FA_FP8_ATTEND_ONLY) ? 0 : 1;
     a.attend = (flags & FA_FP8_QUANTIZE_ONLY) ? 0 : 1;
     a.scale_log2 = scale * 1.4426950408889634f * (a.rotate ? 1.f / 128.f : 1.f);
-    a.timeout_ns = kWaitTimeoutNs;
+    a.watch = make_watch(di->status);
     const cudaError_t e = launch_fp8(maps, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
     return FA_OK;
@@ -682,6 +695,7 @@ fa_status fa_get_device_error(void* stream) {
     if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word))) != cudaSuccess)
         return cuda_fail(e, "read status word");
     if (word != 0) {
+        // word [1] (the failed launch's id) stays: ids are never reused
         const uint32_t zero = 0;
         if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero))) != cudaSuccess)
             return cuda_fail(e, "clear status word");
@@ -692,14 +706,17 @@ fa_status fa_get_device_error(void* stream) {
     return FA_OK;
 }
 
-fa_status fa_debug_watchdog_probe(uint64_t timeout_ns, void* stream) {
+fa_status fa_debug_watchdog_probe(uint64_t timeout_ns, int num_blocks, void* stream) {
     t_last_error[0] = 0;
     DeviceInfo* di = nullptr;
     fa_status st = device_ready(&di);
     if (st != FA_OK) return st;
     if (timeout_ns < 1000ull) timeout_ns = 1000ull;
     if (timeout_ns > 5000000000ull) timeout_ns = 5000000000ull;
-    watchdog_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status, timeout_ns);
+    if (num_blocks < 1) num_blocks = 1;
+    if (num_blocks > (1 << 20)) num_blocks = 1 << 20;
+    watchdog_probe_kernel<<<num_blocks, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        make_watch(di->status, timeout_ns));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "watchdog probe launch");
     return FA_OK;

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     tma_prefetch_4d(&tmDO, c * 64, hq2, q2, b, pol_q);
                 }
             }
-            if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.status, a.timeout_ns, 30)) break;
+            if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.watch, 30)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
                 const uint32_t dst = sStage + 2 * s * C::TILE;
@@ -188,10 +188,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             last_it[s] = it;
         }
         if (lane == 0) {  // no copies in flight at exit
-            mbar_wait(BAR_KV, 0, a.status, a.timeout_ns, 31);
+            mbar_drain(BAR_KV, 0, a.watch, 31);
             for (int s = 0; s < C::NST; ++s)
                 if (last_it[s] >= 0)
-                    mbar_wait(BAR_STF(s), (last_it[s] / C::NST) & 1, a.status, a.timeout_ns, 31);
+                    mbar_drain(BAR_STF(s), (last_it[s] / C::NST) & 1, a.watch, 31);
         }
         __syncwarp();
     } else if (warp == kDkWarpMma) {
@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     mma_bf16_ts(dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
                                 sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
             };
-            bool ok = mbar_wait(BAR_KV, 0, a.status, a.timeout_ns, 32) &&
-                      mbar_wait(BAR_STF(0), 0, a.status, a.timeout_ns, 33);
+            bool ok = mbar_wait(BAR_KV, 0, a.watch, 32) &&
+                      mbar_wait(BAR_STF(0), 0, a.watch, 33);
             if (ok) {
                 tc_fence_after();
                 issue_t(reg_s(0), k_lo, stage_q(0));
@@ -241,18 +241,17 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const bool more = it + 1 < n_it;
                 if (more) {
                     // S^T(it+1) over dP^T(it), once both warpgroups hold it in registers
-                    if (!(ok = mbar_wait(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.status,
-                                         a.timeout_ns, 33)))
+                    if (!(ok = mbar_wait(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.watch, 33)))
                         break;
-                    if (!(ok = mbar_wait(BAR_LD, it & 1, a.status, a.timeout_ns, 34))) break;
+                    if (!(ok = mbar_wait(BAR_LD, it & 1, a.watch, 34))) break;
                     tc_fence_after();
                     issue_t(reg_d(it), k_lo, stage_q(s2));
                 }
                 // dV as soon as P^T is written, dK once dS^T is
-                if (!(ok = mbar_wait(BAR_PF, it & 1, a.status, a.timeout_ns, 34))) break;
+                if (!(ok = mbar_wait(BAR_PF, it & 1, a.watch, 34))) break;
                 tc_fence_after();
                 issue_acc(it, s, false);
-                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.status, a.timeout_ns, 38))) break;
+                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.watch, 38))) break;
                 tc_fence_after();
                 issue_acc(it, s, true);
                 mma_commit(BAR_STE(s));
@@ -264,7 +263,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
-            mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 35);
+            mbar_drain(BAR_ACC, 0, a.watch, 35);
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -292,7 +291,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::NST;
             const int qi = qi0 + it % nqi;
-            if (!(ok = mbar_wait(BAR_SDF, it & 1, a.status, a.timeout_ns, 36))) break;
+            if (!(ok = mbar_wait(BAR_SDF, it & 1, a.watch, 36))) break;
             tc_fence_after();
             const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + wg * 32 + lane_off;
             const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + wg * 32 + lane_off;
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR_DSF);
         }
-        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 37);
+        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.watch, 37);
         // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those
         // of dK = scale * (dS^T Q); staging reuses stage 0's Q (dV) and dO (dK)
         // buffers, idle once all MMAs are done

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ns = isv ? C::VS : C::KS;
                 const int slot = jj % ns;
                 const uint32_t ph = ((jj / ns) & 1) ^ 1u;
-                if (!mbar_wait(isv ? BAR_VE(slot) : BAR_KE(slot), ph, a.status, a.timeout_ns, 20))
+                if (!mbar_wait(isv ? BAR_VE(slot) : BAR_KE(slot), ph, a.watch, 20))
                     return false;
                 const uint32_t full = isv ? BAR_VF(slot) : BAR_KF(slot);
                 const uint32_t dst = (isv ? sV : sK) + slot * C::TILE;
@@ -168,13 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int i = 0; i < nj && ok; ++i) ok = load(i, false) && load(i, true);
             // no copies in flight at exit: wait (bounded) for the last load of each slot
-            mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 21);
+            mbar_drain(BAR_QDO, 0, a.watch, 21);
             for (int s = 0; s < C::KS; ++s)
                 if (last_k[s] >= 0)
-                    mbar_wait(BAR_KF(s), (last_k[s] / C::KS) & 1, a.status, a.timeout_ns, 21);
+                    mbar_drain(BAR_KF(s), (last_k[s] / C::KS) & 1, a.watch, 21);
             for (int s = 0; s < C::VS; ++s)
                 if (last_v[s] >= 0)
-                    mbar_wait(BAR_VF(s), (last_v[s] / C::VS) & 1, a.status, a.timeout_ns, 21);
+                    mbar_drain(BAR_VF(s), (last_v[s] / C::VS) & 1, a.watch, 21);
         }
         __syncwarp();
     } else if (warp == kWarpGate) {
@@ -184,11 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int j = 0; j < nj && ok; ++j) {
                 if (j + 1 < nj)
-                    ok = mbar_wait(BAR_KF((j + 1) % C::KS), ((j + 1) / C::KS) & 1, a.status,
-                                   a.timeout_ns, 28) &&
-                         mbar_wait(BAR_VF((j + 1) % C::VS), ((j + 1) / C::VS) & 1, a.status,
-                                   a.timeout_ns, 28);
-                if (ok && j > 0) ok = mbar_wait(BAR_LD, (j - 1) & 1, a.status, a.timeout_ns, 28);
+                    ok = mbar_wait(BAR_KF((j + 1) % C::KS), ((j + 1) / C::KS) & 1, a.watch, 28) &&
+                         mbar_wait(BAR_VF((j + 1) % C::VS), ((j + 1) / C::VS) & 1, a.watch, 28);
+                if (ok && j > 0) ok = mbar_wait(BAR_LD, (j - 1) & 1, a.watch, 28);
                 if (ok) mbar_arrive(BAR_LD);
             }
         }
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mul = pow2f(sc.dout);
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
             uint16_t* dst = a.dout16 + (static_cast<size_t>(b) * a.N + qi * kBM) * row_el + h * D;
-            if (mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 29))
+            if (mbar_wait(BAR_QDO, 0, a.watch, 29))
                 warp_tile_to_f16<D>(sDO, dst, row_el, a.N - qi * kBM, mul, lane);
         }
         __syncwarp();
@@ -215,14 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tS = tbase + C::TM_S, tDQ = tbase + C::TM_DQ;
             auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
             auto k_ready = [&](int jj) {
-                const bool r = mbar_wait(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.status,
-                                         a.timeout_ns, 23);
+                const bool r = mbar_wait(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.watch, 23);
                 tc_fence_after();
                 return r;
             };
             auto v_ready = [&](int jj) {  // (prologue only; the gate covers the loop)
-                const bool r = mbar_wait(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.status,
-                                         a.timeout_ns, 23);
+                const bool r = mbar_wait(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.watch, 23);
                 tc_fence_after();
                 return r;
             };
@@ -254,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 IDESC_DQ, (jj == 0 && ks == 0) ? 0u : 1u);
                 mma_commit(BAR_KE(jj % C::KS));
             };
-            bool ok = mbar_wait(BAR_QDO, 0, a.status, a.timeout_ns, 22) && k_ready(0);
+            bool ok = mbar_wait(BAR_QDO, 0, a.watch, 22) && k_ready(0);
             if (ok) issue_t(tS, q_lo, sK, IDESC_S);
             if (ok && (ok = v_ready(0))) {
                 issue_dp(0);
@@ -266,20 +262,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (issued earlier by this thread) has read; K_{j+1} and V_{j+1}
                 // have landed (the gate's arrival on LD)
                 if (j + 1 < nj) {
-                    if (!(ok = mbar_wait(BAR_LD, j & 1, a.status, a.timeout_ns, 24))) break;
+                    if (!(ok = mbar_wait(BAR_LD, j & 1, a.watch, 24))) break;
                     tc_fence_after();
                     issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
                     issue_dp(j + 1);
                     mma_commit(BAR_SDF);
                 }
-                if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 24))) break;
+                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 24))) break;
                 mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
                 tc_fence_after();
                 issue_dq(j);
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
-            mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 25);
+            mbar_drain(BAR_ACC, 0, a.watch, 25);
         }
         __syncwarp();
     } else if (warp < 8) {
@@ -307,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ndx2 = f2(-dval * dsc, -dval * dsc), dsc2 = f2(dsc, dsc);
         bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
-            if (!(ok = mbar_wait(BAR_SDF, j & 1, a.status, a.timeout_ns, 26))) break;
+            if (!(ok = mbar_wait(BAR_SDF, j & 1, a.watch, 26))) break;
             tc_fence_after();
             const uint32_t tDP = tbase + C::TM_DP + (j & 1) * 128 + lane_off + hf * 64;
             uint32_t sv[64], dp[64];
@@ -348,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // arriving on PF(j) only once that thread has seen PF(j-1) keeps a
             // fast warp's arrival out of PF(j-1)'s phase and PF from running
             // two phases ahead of the thread's parity wait
-            if (j > 0 && !(ok = mbar_wait(BAR_PFS, (j - 1) & 1, a.status, a.timeout_ns, 39))) break;
+            if (j > 0 && !(ok = mbar_wait(BAR_PFS, (j - 1) & 1, a.watch, 39))) break;
             mbar_arrive(BAR_PF);
         }
-        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.status, a.timeout_ns, 27);
+        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.watch, 27);
         if (ok_e) {
             tc_fence_after();
             // dQ = scale * (dS K): each warpgroup stages half of the d columns into

@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                 for (int w = 0; w < 2; ++w) {  // K_j then V_j
                     const int idx = 2 * j + w;
                     const int slot = idx % C::NSLOT;
-                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / C::NSLOT) & 1) ^ 1u, a.status,
-                                         a.timeout_ns, 40)))
+                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / C::NSLOT) & 1) ^ 1u, a.watch, 40)))
                         break;
                     mbar_arrive_expect_tx(BAR_KVF(slot), C::TILE);
                     for (int c = 0; c < C::NCH; ++c)
@@ -184,10 +183,10 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                 }
             }
             // no copies in flight at exit
-            mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 41);
+            mbar_drain(BAR_Q, 0, a.watch, 41);
             for (int s = 0; s < C::NSLOT; ++s)
                 if (last_idx[s] >= 0)
-                    mbar_wait(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.status, a.timeout_ns,
+                    mbar_drain(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.watch,
                               41);
         }
         __syncwarp();
@@ -204,8 +203,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             auto slot_of = [&](int j, int w) { return (2 * j + w) % C::NSLOT; };
             auto landed = [&](int j, int w) {
                 const int idx = 2 * j + w;
-                const bool r = mbar_wait(BAR_KVF(idx % C::NSLOT), (idx / C::NSLOT) & 1, a.status,
-                                         a.timeout_ns, 42);
+                const bool r = mbar_wait(BAR_KVF(idx % C::NSLOT), (idx / C::NSLOT) & 1, a.watch, 42);
                 tc_fence_after();
                 return r;
             };
@@ -230,7 +228,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                 mma_commit(BAR_KVE(slot_of(j, 1)));
                 mma_commit(BAR_PVD);
             };
-            bool ok = mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 43);
+            bool ok = mbar_wait(BAR_Q, 0, a.watch, 43);
             if (ok && (ok = landed(0, 0))) issue_s(0);
             for (int j = 0; j < nkv && ok; ++j) {
                 // S(j+1) into the other buffer: its previous content, P(j-1), was
@@ -239,14 +237,14 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                     if (!(ok = landed(j + 1, 0))) break;
                     issue_s(j + 1);
                 }
-                if (!(ok = mbar_wait(BAR_PF(j & 1), (j >> 1) & 1, a.status, a.timeout_ns, 44)))
+                if (!(ok = mbar_wait(BAR_PF(j & 1), (j >> 1) & 1, a.watch, 44)))
                     break;
                 tc_fence_after();
                 if (!(ok = landed(j, 1))) break;
                 issue_pv(j);
             }
             mma_commit(BAR_OF);
-            mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 45);
+            mbar_drain(BAR_OF, 0, a.watch, 45);
         }
         __syncwarp();
     } else {
@@ -263,7 +261,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         bool ok = true;
         int kb = blocks.first();
         for (int j = 0; j < nkv; ++j, kb = blocks.next(kb)) {
-            if (!(ok = mbar_wait(BAR_SF(j & 1), (j >> 1) & 1, a.status, a.timeout_ns, 46))) break;
+            if (!(ok = mbar_wait(BAR_SF(j & 1), (j >> 1) & 1, a.watch, 46))) break;
             tc_fence_after();
             const uint32_t tS = tbase + C::TM_S + (j & 1) * kBN + lane_off;
             uint32_t s[kBN];
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             // O was last written by PV(j-1), which may still be running: wait
             // for it before rescaling (rare: only when the reference max moves)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                if (!(ok = mbar_wait(BAR_PVD, (j - 1) & 1, a.status, a.timeout_ns, 47))) break;
+                if (!(ok = mbar_wait(BAR_PVD, (j - 1) & 1, a.watch, 47))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cb = 0; cb < D; cb += 32) {
@@ -350,7 +348,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         }
         // ---- epilogue: O / l and lse, straight to the output (one split) or
         // to this split's fp32 slot of the workspace
-        const bool ok_e = ok && (nkv == 0 || mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 48));
+        const bool ok_e = ok && (nkv == 0 || mbar_wait(BAR_OF, 0, a.watch, 48));
         if (ok_e) {
             if (nkv > 0) tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

@@ -250,8 +250,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             for (int j = 0; j < nkv && ok; ++j)
                 for (int w = 0; w < 2 && ok; ++w) {
                     const int idx = 2 * j + w, slot = idx % kF8Slots;
-                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / kF8Slots) & 1) ^ 1u, a.status,
-                                         a.timeout_ns, 50)))
+                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / kF8Slots) & 1) ^ 1u, a.watch, 50)))
                         break;
                     mbar_arrive_expect_tx(BAR_KVF(slot), kF8Tile);
                     if (w == 0)
@@ -262,10 +261,10 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                                          hk, b, pol);
                     last_idx[slot] = idx;
                 }
-            mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 51);
+            mbar_drain(BAR_Q, 0, a.watch, 51);
             for (int s = 0; s < kF8Slots; ++s)
                 if (last_idx[s] >= 0)
-                    mbar_wait(BAR_KVF(s), (last_idx[s] / kF8Slots) & 1, a.status, a.timeout_ns, 51);
+                    mbar_drain(BAR_KVF(s), (last_idx[s] / kF8Slots) & 1, a.watch, 51);
         }
         __syncwarp();
     } else if (warp == kF8WarpMma) {
@@ -278,8 +277,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             const uint32_t q_lo = sdesc_lo(sQ, 16);
             const uint32_t tS = tbase, tO = tbase + 128;
             auto landed = [&](int idx) {
-                const bool r = mbar_wait(BAR_KVF(idx % kF8Slots), (idx / kF8Slots) & 1, a.status,
-                                         a.timeout_ns, 52);
+                const bool r = mbar_wait(BAR_KVF(idx % kF8Slots), (idx / kF8Slots) & 1, a.watch, 52);
                 tc_fence_after();
                 return r;
             };
@@ -293,10 +291,10 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                 mma_commit(BAR_SF);
                 mma_commit(BAR_KVE(slot));
             };
-            bool ok = mbar_wait(BAR_Q, 0, a.status, a.timeout_ns, 53) && landed(0);
+            bool ok = mbar_wait(BAR_Q, 0, a.watch, 53) && landed(0);
             if (ok) issue_s(0);
             for (int j = 0; j < nkv && ok; ++j) {
-                if (!(ok = mbar_wait(BAR_PF, j & 1, a.status, a.timeout_ns, 54))) break;
+                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 54))) break;
                 tc_fence_after();
                 if (!(ok = landed(2 * j + 1))) break;
                 const int vslot = (2 * j + 1) % kF8Slots;
@@ -312,7 +310,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                 }
             }
             mma_commit(BAR_OF);
-            mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 55);
+            mbar_drain(BAR_OF, 0, a.watch, 55);
         }
         __syncwarp();
     } else {
@@ -327,7 +325,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
-            if (!(ok = mbar_wait(BAR_SF, j & 1, a.status, a.timeout_ns, 56))) break;
+            if (!(ok = mbar_wait(BAR_SF, j & 1, a.watch, 56))) break;
             tc_fence_after();
             // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
             // and every exponent is one FMA, two columns per packed f32x2 op
@@ -403,7 +401,7 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             mbar_arrive(BAR_PF);
         }
         // ---- epilogue: O * sv / l -> bf16, plain stores; lse
-        const bool ok_e = ok && mbar_wait(BAR_OF, 0, a.status, a.timeout_ns, 57);
+        const bool ok_e = ok && mbar_wait(BAR_OF, 0, a.watch, 57);
         if (ok_e) {
             tc_fence_after();
             const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(384, 1)
                     const int idx = 2 * j + w;
                     const int slot = idx % C::NSLOT;
                     const uint32_t ph = (idx / C::NSLOT) & 1;
-                    if (!mbar_wait(BAR_KVE(slot), ph ^ 1u, a.status, a.timeout_ns, 1)) {
+                    if (!mbar_wait(BAR_KVE(slot), ph ^ 1u, a.watch, 1)) {
                         ok = false;
                         break;
                     }
@@ -173,10 +173,10 @@ __global__ void __launch_bounds__(384, 1)
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
             // last load issued into every slot, and for Q.
-            mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 2);
+            mbar_drain(BAR_Q(), 0, a.watch, 2);
             for (int s = 0; s < C::NSLOT; ++s)
                 if (last_idx[s] >= 0)
-                    mbar_wait(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.status, a.timeout_ns, 2);
+                    mbar_drain(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.watch, 2);
         }
         __syncwarp();
     } else if (warp == kWarpGate) {
@@ -189,14 +189,12 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int j = 0; j < nkv && ok; ++j) {
                 const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-                ok = mbar_wait(BAR_KVF(vidx % C::NSLOT), (vidx / C::NSLOT) & 1, a.status,
-                               a.timeout_ns, 5);
+                ok = mbar_wait(BAR_KVF(vidx % C::NSLOT), (vidx / C::NSLOT) & 1, a.watch, 5);
                 if (ok && j + 1 < nkv)
-                    ok = mbar_wait(BAR_KVF(kidx % C::NSLOT), (kidx / C::NSLOT) & 1, a.status,
-                                   a.timeout_ns, 5);
+                    ok = mbar_wait(BAR_KVF(kidx % C::NSLOT), (kidx / C::NSLOT) & 1, a.watch, 5);
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (t == 0 && j >= nkv0) continue;
-                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.status, a.timeout_ns, 7);
+                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.watch, 7);
                     if (ok) mbar_arrive(BAR_PF(t));
                 }
             }
@@ -209,7 +207,7 @@ __global__ void __launch_bounds__(384, 1)
         if (F16 && a.q16 != nullptr) {
             const float mul = pow2f(ld_once(&a.f16s->q));
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
-            if (mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 15)) {
+            if (mbar_wait(BAR_Q(), 0, a.watch, 15)) {
                 for (int t = 0; t < 2; ++t)
                     warp_tile_to_f16<D>(sQ + t * C::TILE,
                                         a.q16 + (static_cast<size_t>(b) * a.N + row0 + t * kBM) *
@@ -247,10 +245,10 @@ __global__ void __launch_bounds__(384, 1)
                     mma_bf16_ts(dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
                                 (acc || ks > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(BAR_Q(), 0, a.status, a.timeout_ns, 3);
+            bool ok = mbar_wait(BAR_Q(), 0, a.watch, 3);
             if (ok) {
                 // first key block: both score tiles
-                ok = mbar_wait(BAR_KVF(0), 0, a.status, a.timeout_ns, 4);
+                ok = mbar_wait(BAR_KVF(0), 0, a.watch, 4);
                 if (ok) {
                     tc_fence_after();
                     issue_qk(0, 0);
@@ -264,7 +262,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = 0; j < nkv && ok; ++j) {
                 const int vslot = (2 * j + 1) % C::NSLOT;
                 if (j < nkv0) {
-                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.status, a.timeout_ns, 6))) break;
+                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.watch, 6))) break;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
                     if (j == nkv0 - 1) mma_commit(BAR_OF(0));
@@ -275,7 +273,7 @@ __global__ void __launch_bounds__(384, 1)
                     issue_qk(0, kslot);
                     mma_commit(BAR_SF(0));
                 }
-                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.status, a.timeout_ns, 8))) break;
+                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.watch, 8))) break;
                 tc_fence_after();
                 issue_pv(1, vslot, j > 0);
                 mma_commit(BAR_KVE(vslot));
@@ -288,7 +286,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             // all issued MMAs have finished before TMEM can be released
             mma_commit(BAR_DONE);
-            mbar_wait(BAR_DONE, 0, a.status, a.timeout_ns, 9);
+            mbar_drain(BAR_DONE, 0, a.watch, 9);
         }
         __syncwarp();
     } else if (warp < 8) {
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         const int nkv_mine = t ? nkv : nkv0;
         for (int j = 0; j < nkv_mine; ++j) {
-            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.status, a.timeout_ns, 10 + t))) break;
+            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
             tc_fence_after();
             uint32_t s[kBN];
             tmem_ld32(tS + 0, s);
@@ -392,9 +390,9 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive(BAR_PF(t));
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging in Q_t's buffer -> TMA store
-        bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.status, a.timeout_ns, 12 + t);
+        bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.watch, 12 + t);
         if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
-            ok_e = ok_e && mbar_wait(BAR_QC, 0, a.status, a.timeout_ns, 14);
+            ok_e = ok_e && mbar_wait(BAR_QC, 0, a.watch, 14);
         const uint32_t stage = sQ + t * C::TILE;
         if (ok_e) {
             tc_fence_after();

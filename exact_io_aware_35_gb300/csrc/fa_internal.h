@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "fa.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 
@@ -84,12 +85,11 @@ struct FwdArgs {
     uint16_t* o_lo;      // [B, N, Hq, d] bf16 low half of O, or null
     const F16Scales* f16s;  // non-null: P and V enter O += P V in fp16 (V map = fp16 copy)
     uint16_t* q16;       // non-null (with f16s): the kernel writes fp16(q * 2^s.q) here
-    uint32_t* status;    // device status word
     int B, Hq, Hkv, N, g;
     int causal;
     float scale_log2;    // scale * log2(e)
     int n_qblk;          // ceil(N / 256): CTA query blocks (two 128-row tiles each)
-    uint64_t timeout_ns;
+    Watch watch;         // status words, time limit and id of the launch
 };
 
 struct BwdArgs {
@@ -107,12 +107,11 @@ struct BwdArgs {
     const uint32_t* absmax;
     F16Scales* scales_w;
     uint32_t* dout_max;  // non-null: the dsum kernel also takes max|dout| into it
-    uint32_t* status;
     int B, Hq, Hkv, N, d, g;
     int causal;
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
-    uint64_t timeout_ns;
+    Watch watch;         // status words, time limit and id of the launch
 };
 
 // Split-KV forward (fa_decode.cu): Nq queries of gp heads sharing a KV head
@@ -123,7 +122,6 @@ struct DecodeArgs {
     float* lse;         // [B, Hq, Nq]
     float* part_o;      // splits > 1: [splits, B, Hq, Nq, d] fp32 workspace
     float* part_lse;    // splits > 1: [splits, B, Hq, Nq]
-    uint32_t* status;
     int B, Hq, Hkv, Nq, Nk, g;
     int causal;         // query i sees keys j <= i + Nk - Nq
     float scale_log2;
@@ -134,7 +132,7 @@ struct DecodeArgs {
     // computed (then gp == 1, qpt == 128 and splits == 1); null: every block
     const uint8_t* block_mask;
     int nkb;
-    uint64_t timeout_ns;
+    Watch watch;         // status words, time limit and id of the launch
 };
 
 struct DecodeMaps {
@@ -164,13 +162,12 @@ struct Fp8Args {
     // the forward
     uint16_t* o;        // [B, N, Hq, 128] bf16
     float* lse;         // [B, Hq, N]
-    uint32_t* status;
     int B, Hq, Hkv, N, g, ldv, nb;
     int causal;
     int rotate;         // q, k rows multiplied by diag(signs) H_128 before quantising
     int quantize, attend;  // which of the two steps to run
     float scale_log2;   // scale * log2(e), / 128 when rotated (H_128 H_128^T = 128 I)
-    uint64_t timeout_ns;
+    Watch watch;         // status words, time limit and id of the launch
 };
 
 struct Fp8Maps {

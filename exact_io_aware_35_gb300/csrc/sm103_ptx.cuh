@@ -57,45 +57,63 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// What a bounded wait needs: the library's device status words and this
+// launch's limits.  status[0] holds the first failure recorded since the host
+// last read it (kDevTimeout | site << 8); status[1] holds the id of the last
+// launch in which a wait ran out.  Every launch gets its own nonzero id from
+// the host, so a stale id left by an earlier launch never matches.
+struct Watch {
+    uint32_t* status;
+    uint64_t timeout_ns;
+    uint32_t launch;
+};
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Waits for the phase with the given parity to complete, for at most
-// timeout_ns.  On time-out records kDevTimeout | (site << 8) in *status (first
-// failure wins) and returns false; the caller then stops issuing work.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status,
-                                          uint64_t timeout_ns, uint32_t site) {
+// w.timeout_ns.  On time-out it records kDevTimeout | (site << 8) in
+// status[0] (first failure wins) and the launch's id in status[1], and
+// returns false; the caller then stops issuing work.  A wait that is still
+// pending when another thread block of the same launch has recorded a
+// time-out also returns false (it looks every 16 polls), so one failure ends
+// the whole launch within microseconds instead of costing every later wait
+// its own full limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Watch& w,
+                                          uint32_t site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) {
-            atomicCAS(status, 0u, kDevTimeout | (site << 8));
-            return false;
+        if ((++n & 15u) == 0) {
+            if (ld_volatile_u32(w.status + 1) == w.launch) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+                atomicCAS(w.status, 0u, kDevTimeout | (site << 8));
+                atomicExch(w.status + 1, w.launch);
+                return false;
+            }
         }
     }
     return true;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Like mbar_wait, but polls with the non-suspending test_wait: the caller
-// resumes as soon as the phase completes.  For the single MMA-issuing thread,
-// whose wake-up latency is on the critical path.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, uint32_t* status,
-                                               uint64_t timeout_ns, uint32_t site) {
-    if (mbar_test_wait(bar, parity)) return true;
+// The wait a thread block makes before it exits for work it has itself put
+// in flight -- its last TMA loads, its last MMAs -- which completes without
+// any other thread's help.  It does not give up when another block failed
+// (leaving with copies into shared memory or MMAs into tensor memory still
+// running is what it exists to prevent); it is bounded by the time limit
+// alone.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, const Watch& w,
+                                           uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t n = 0;
-    while (!mbar_test_wait(bar, parity)) {
-        if ((++n & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
-            atomicCAS(status, 0u, kDevTimeout | (site << 8));
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            atomicCAS(w.status, 0u, kDevTimeout | (site << 8));
+            atomicExch(w.status + 1, w.launch);
             return false;
         }
     }

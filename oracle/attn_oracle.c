@@ -18,7 +18,7 @@
  * page, "The Mathematics of Online Softmax", first paragraph), then multiplies
  * by V.  Nothing is tiled or fused.
  *
- * Readings of points the pages leave open (each is listed in the design doc):
+ * Readings of points the pages leave open:
  *   - scale multiplies Q K^T before the mask; the pages' default is 1/sqrt(d).
  *   - causal: key j is visible to query i iff j <= i (Nq == Nk, so top-left
  *     and bottom-right alignment coincide).

@@ -110,6 +110,21 @@ def quantize_heads(v: np.ndarray, quantize: bool = True):
     return out
 
 
+# The reference maximum of the online softmax moves only when a block's
+# maximum exceeds it by more than this many log2 units (a factor 2^8).
+LAZY_THRESHOLD = 8.0
+
+
+def row_sum_terms(p: np.ndarray) -> np.ndarray:
+    """What the running row sum l adds for one block: the unrounded P."""
+    return p
+
+
+def pv_operand(p: np.ndarray, quantize: bool) -> np.ndarray:
+    """P as it enters the P V product: rounded to e4m3, no scale (P <= 2^8)."""
+    return e4m3_round(p) if quantize else p
+
+
 def attn_fwd_fp8(q, k, v, causal: bool, scale: float, rotate: bool, quantize: bool = True):
     """The model of fa_fwd_fp8.  Returns (o [B,N,Hq,d], lse [B,Hq,N])."""
     q8 = quantize_blocks(q, rotate, quantize)
@@ -120,7 +135,6 @@ def attn_fwd_fp8(q, k, v, causal: bool, scale: float, rotate: bool, quantize: bo
     g = Hq // k8.shape[2]
     o = np.zeros((B, N, Hq, d))
     lse = np.zeros((B, Hq, N))
-    rnd = e4m3_round if quantize else (lambda t: t)
     for b in range(B):
         for h in range(Hq):
             x_all = sl2 * (q8[b, :, h] @ k8[b, :, h // g].T)  # [N, N], log2 units
@@ -130,14 +144,14 @@ def attn_fwd_fp8(q, k, v, causal: bool, scale: float, rotate: bool, quantize: bo
                 for j0 in range(0, lim + 1, 128):
                     x = x_all[i, j0:min(j0 + 128, lim + 1)]
                     m_new = max(m_ref, float(x.max()))
-                    if m_new > m_ref + 8.0:
+                    if m_new > m_ref + LAZY_THRESHOLD:
                         alpha = np.exp2(m_ref - m_new) if np.isfinite(m_ref) else 0.0
                         l *= alpha
                         acc *= alpha
                         m_ref = m_new
                     p = np.exp2(x - m_ref)
-                    l += p.sum()
-                    acc += rnd(p) @ v8[b, j0:j0 + len(x), h // g]
+                    l += row_sum_terms(p).sum()
+                    acc += pv_operand(p, quantize) @ v8[b, j0:j0 + len(x), h // g]
                 o[b, i, h] = acc / l
                 lse[b, h, i] = (m_ref + np.log2(l)) * np.log(2.0)
     return o, lse

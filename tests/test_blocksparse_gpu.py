@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from tests.guards import Guarded, check_all
 from tests.parity import assert_close, assert_lse_close
 
 pytestmark = pytest.mark.gpu
@@ -39,14 +40,17 @@ def local_mask(Hq, nb, width):
 
 
 def run(fa, q, k, v, mask, causal, scale):
+    """fa_fwd_blocksparse with NaN-filled outputs between guard canaries
+    (tests/guards.py)."""
     qd = q.cuda()
     B, N, Hq, d = q.shape
-    o = torch.full_like(qd, float("nan"))
-    lse = torch.full((B, Hq, N), float("nan"), device=qd.device)
-    fa.fa_fwd_blocksparse(qd, k.cuda(), v.cuda(), mask.cuda(), causal=causal, scale=scale, o=o,
-                          lse=lse)
+    o = Guarded(qd.shape, qd.dtype, qd.device)
+    lse = Guarded((B, Hq, N), torch.float32, qd.device)
+    fa.fa_fwd_blocksparse(qd, k.cuda(), v.cuda(), mask.cuda(), causal=causal, scale=scale, o=o.t,
+                          lse=lse.t)
     assert fa.fa_get_device_error() == fa.FA_OK
-    return o.cpu(), lse.cpu()
+    check_all(o=o, lse=lse)
+    return o.t.cpu(), lse.t.cpu()
 
 
 def check(o, lse, o_ref, lse_ref):

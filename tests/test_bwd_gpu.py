@@ -11,6 +11,7 @@ import torch
 
 import fa_workloads as W
 import oracle
+from tests.guards import Guarded, check_all
 from tests.parity import TOL_MAXABS, TOL_RELL2, assert_close, errors
 
 pytestmark = pytest.mark.gpu
@@ -25,20 +26,27 @@ def fa(cuda_device):
 
 def run_bwd(fa, x, causal, scale, train=True):
     """Training pair: fa_fwd_train (o, o_lo, lse) then fa_bwd; train=False
-    uses the plain forward and no o_lo."""
+    uses the plain forward and no o_lo.  Every buffer the library writes sits
+    between guard canaries (tests/guards.py), checked after the launches."""
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
-    o_lo = torch.empty_like(q) if train else None
-    o, lse = fa.fa_fwd(q, k, v, causal=causal, scale=scale, o_lo=o_lo)
-    dq = torch.full_like(q, float("nan"))
-    dk = torch.full_like(k, float("nan"))
-    dv = torch.full_like(v, float("nan"))
     B, N, Hq, d = q.shape
-    ws = torch.full((fa.fa_bwd_workspace_size(B, Hq, k.shape[2], N, d),), 255,
-                    dtype=torch.uint8, device=q.device)
-    fa.fa_bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-              o_lo=o_lo)
+    Hkv = k.shape[2]
+    o = Guarded(q.shape, q.dtype, q.device)
+    lse = Guarded((B, Hq, N), torch.float32, q.device)
+    o_lo = Guarded(q.shape, q.dtype, q.device) if train else None
+    wsb = fa.fa_bwd_workspace_size(B, Hq, Hkv, N, d)
+    ws_f = Guarded((wsb,), torch.uint8, q.device, fill=255) if train else None
+    fa.fa_fwd(q, k, v, causal=causal, scale=scale, o=o.t, lse=lse.t,
+              o_lo=o_lo.t if train else None, workspace=ws_f.t if train else None)
+    dq = Guarded(q.shape, q.dtype, q.device)
+    dk = Guarded(k.shape, k.dtype, k.device)
+    dv = Guarded(v.shape, v.dtype, v.device)
+    ws = Guarded((wsb,), torch.uint8, q.device, fill=255)
+    fa.fa_bwd(q, k, v, o.t, do, lse.t, causal=causal, scale=scale, dq=dq.t, dk=dk.t, dv=dv.t,
+              workspace=ws.t, o_lo=o_lo.t if train else None)
     assert fa.fa_get_device_error() == fa.FA_OK
-    return dq.cpu(), dk.cpu(), dv.cpu()
+    check_all(o=o, lse=lse, o_lo=o_lo, fwd_workspace=ws_f, dq=dq, dk=dk, dv=dv, workspace=ws)
+    return dq.t.cpu(), dk.t.cpu(), dv.t.cpu()
 
 
 SHAPES = [

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from tests.guards import Guarded, check_all
 from tests.parity import assert_close, assert_lse_close
 
 pytestmark = pytest.mark.gpu
@@ -28,13 +29,20 @@ def inputs(B, Nq, Nk, Hq, Hkv, d, seed, s=1.0):
 
 
 def run(fa, q, k, v, causal, scale, splits):
+    """fa_fwd_splitkv with NaN-filled outputs and its fp32 workspace between
+    guard canaries (tests/guards.py)."""
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     B, Nq, Hq, d = q.shape
-    o = torch.full_like(qd, float("nan"))
-    lse = torch.full((B, Hq, Nq), float("nan"), device=qd.device)
-    fa.fa_fwd_splitkv(qd, kd, vd, causal=causal, scale=scale, num_splits=splits, o=o, lse=lse)
+    Nk, Hkv = k.shape[1], k.shape[2]
+    o = Guarded(qd.shape, qd.dtype, qd.device)
+    lse = Guarded((B, Hq, Nq), torch.float32, qd.device)
+    wsb = fa.fa_fwd_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, d, causal, splits)
+    ws = Guarded((wsb,), torch.uint8, qd.device, fill=255) if wsb else None
+    fa.fa_fwd_splitkv(qd, kd, vd, causal=causal, scale=scale, num_splits=splits, o=o.t,
+                      lse=lse.t, workspace=ws.t if ws else None)
     assert fa.fa_get_device_error() == fa.FA_OK
-    return o.cpu(), lse.cpu()
+    check_all(o=o, lse=lse, workspace=ws)
+    return o.t.cpu(), lse.t.cpu()
 
 
 # (B, Nq, Nk, Hq, Hkv, d, causal, splits): decode (Nq = 1), a few queries, several

@@ -1,19 +1,24 @@
 """GPU checks of the FP8 (e4m3) forward (fa_fwd_fp8, through the C ABI):
-against the float64 model of its arithmetic (oracle/fp8.py) closely, and
-against the exact oracle within the tolerance e4m3 allows.
+against the float64 model of its arithmetic (oracle/fp8.py, pinned by
+tests/test_fp8_model.py) closely, and against the exact oracle within fixed
+bounds that e4m3 allows.
 
-Tolerances.  e4m3 keeps 4 significant bits: each rounding of Q, K (after the
-block scale), V and P moves a value by up to 2^-4 of itself, so against the
-exact result the output carries errors of several percent (rel-L2 about 5e-2
-for O, up to ~0.1 in lse on these N(0, 1)-shaped inputs with scale
-1/sqrt(128)).  Those errors belong to the FP8 algorithm, not to the kernel, so
-the bound against the exact result is relative to the model's own error: the
-kernel may exceed the model's rel-L2 (and lse max-abs) against the exact
-result by at most 10% plus 2e-3 (5e-3 for lse), with absolute caps of 0.1
-(0.2 for lse).  Against the model, which makes the same roundings, only the
-kernel's fp32 arithmetic (exp2, accumulation order) and the bf16 output
-differ, except where such a difference moves a value across an e4m3 rounding
-boundary: rel-L2 <= 1e-2 for O, max-abs <= 1e-2 for lse.
+Fixed bounds against the exact result.  e4m3 keeps 4 significant bits: each
+rounding moves a value by up to 2^-4 of itself, uniformly, i.e. 2^-4 / sqrt(3)
+= 3.6% RMS.  The rounding of V alone carries that relative error into O; the
+roundings of Q and K move each score by about 3.6% * sqrt(2) of its spread
+(5% for N(0, 1) inputs at scale 1/sqrt(128)), which moves P and hence O by a
+few percent more.  lse carries the score error itself where a row sees few
+keys (early causal rows): one score's rounding error has a standard deviation
+of scale * sqrt(2 d / 768) * sigma_q * sigma_k, 0.051 for N(0, 1) inputs, and
+the largest over thousands of rows reaches about 3 of those.  So on N(0, 1)
+inputs O is within rel-L2 6e-2 and lse within 0.15 of the exact result (the
+model itself measures 4.4-5.2e-2 and up to 0.087 on the cases below), and on
+0.5 N(0, 1) inputs -- the bench recipe, whose scores spread a quarter as much
+-- within rel-L2 5e-2 and lse 5e-2 (the model: 3.4-3.8e-2, up to 0.022).  Against the model, which makes the same roundings,
+only the kernel's fp32 arithmetic (exp2, accumulation order) and the bf16
+output differ, except where such a difference moves a value across an e4m3
+rounding boundary: rel-L2 <= 1e-2 for O, max-abs <= 1e-2 for lse.
 """
 import math
 
@@ -23,18 +28,16 @@ import torch
 
 import oracle
 from oracle import fp8 as f8
+from tests.guards import Guarded, check_all
 from tests.parity import errors
 
 pytestmark = pytest.mark.gpu
 
-TOL_EXACT_RELL2 = 0.1   # absolute caps against the exact result
-TOL_EXACT_LSE = 0.2
+# fixed bounds against the exact result: N(0, 1) inputs, and the bench's 0.5 N(0, 1)
+TOL_EXACT_RELL2, TOL_EXACT_LSE = 6e-2, 0.15
+TOL_EXACT_RELL2_HALF, TOL_EXACT_LSE_HALF = 5e-2, 5e-2
 TOL_MODEL_RELL2 = 1e-2  # against the model of the same arithmetic
 TOL_MODEL_LSE = 1e-2
-
-
-def no_worse_than_model(err_kernel, err_model, slack):
-    return err_kernel <= 1.1 * err_model + slack
 
 
 @pytest.fixture(scope="module")
@@ -57,12 +60,16 @@ def inputs(B, N, Hq, Hkv, seed, s=1.0, outliers=0.0):
 
 
 def run(fa, q, k, v, causal, scale, rotate):
-    o = torch.full_like(q.cuda(), float("nan"))
-    lse = torch.full((q.shape[0], q.shape[2], q.shape[1]), float("nan"), device="cuda")
+    B, N, Hq, d = q.shape
+    o = Guarded(q.shape, q.dtype, "cuda")
+    lse = Guarded((B, Hq, N), torch.float32, "cuda")
+    ws = Guarded((fa.fa_fwd_fp8_workspace_size(B, Hq, k.shape[2], N, d),), torch.uint8, "cuda",
+                 fill=255)
     fa.fa_fwd_fp8(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, rotate=rotate,
-                  o=o, lse=lse)
+                  o=o.t, lse=lse.t, workspace=ws.t)
     assert fa.fa_get_device_error() == fa.FA_OK
-    return o.cpu(), lse.cpu()
+    check_all(o=o, lse=lse, workspace=ws)
+    return o.t.cpu(), lse.t.cpu()
 
 
 CASES = [  # (B, N, Hq, Hkv, causal, rotate)
@@ -86,12 +93,12 @@ def test_fp8_matches_model_and_oracle(fa, B, N, Hq, Hkv, causal, rotate):
     _, rel_mx = errors(o_m, o_x)  # the algorithm's own error
     lse_g = lse.double().numpy()
     lse_err, lse_err_m = np.abs(lse_g - lse_x).max(), np.abs(lse_m - lse_x).max()
+    print(f"fp8 o rel-L2: vs model {rel_m:.3e}, vs exact {rel_x:.3e} (model vs exact "
+          f"{rel_mx:.3e}); lse vs exact {lse_err:.3e} (model {lse_err_m:.3e})")
     assert rel_m <= TOL_MODEL_RELL2, f"rel-L2 vs the fp8 model {rel_m:.3e}"
     assert np.abs(lse_g - lse_m).max() <= TOL_MODEL_LSE
-    assert no_worse_than_model(rel_x, rel_mx, 2e-3), (rel_x, rel_mx)
     assert rel_x <= TOL_EXACT_RELL2, f"rel-L2 vs exact {rel_x:.3e}"
-    assert no_worse_than_model(lse_err, lse_err_m, 5e-3), (lse_err, lse_err_m)
-    assert lse_err <= TOL_EXACT_LSE
+    assert lse_err <= TOL_EXACT_LSE, f"lse vs exact {lse_err:.3e}"
 
 
 def test_rotation_reduces_error_with_outlier_channels(fa):
@@ -120,10 +127,11 @@ def test_fp8_bench_shape_sampled(fa):
     got = np.stack([o[0, i, h].double().numpy() for _, h, i in rows])
     lse_got = np.array([lse[0, h, i].item() for _, h, i in rows])
     rel = np.linalg.norm(got - o_r) / np.linalg.norm(o_r)
-    assert rel <= TOL_EXACT_RELL2, rel
-    assert np.abs(lse_got - lse_r).max() <= TOL_EXACT_LSE
-    # the gqa8k recipe draws 0.5 N(0, 1): the algorithm's error is smaller there
-    assert rel <= 5e-2, rel
+    lse_err = np.abs(lse_got - lse_r).max()
+    print(f"fp8 bench shape: o rel-L2 vs exact {rel:.3e}, lse {lse_err:.3e}")
+    # the gqa8k recipe draws 0.5 N(0, 1): the half-spread bounds
+    assert rel <= TOL_EXACT_RELL2_HALF, rel
+    assert lse_err <= TOL_EXACT_LSE_HALF, lse_err
 
 
 def test_quantise_then_attend_equals_one_call(fa):

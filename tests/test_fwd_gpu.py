@@ -7,6 +7,7 @@ import torch
 
 import fa_workloads as W
 import oracle
+from tests.guards import Guarded, check_all
 from tests.parity import assert_close, assert_lse_close
 
 pytestmark = pytest.mark.gpu
@@ -20,13 +21,15 @@ def fa(cuda_device):
 
 
 def run_fwd(fa, x, causal, scale):
+    """fa_fwd with NaN-filled outputs between guard canaries (tests/guards.py)."""
     q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
     B, N, Hq, d = q.shape
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full((B, Hq, N), float("nan"), device=q.device)
-    fa.fa_fwd(q, k, v, causal=causal, scale=scale, o=o, lse=lse)
+    o = Guarded(q.shape, q.dtype, q.device)
+    lse = Guarded((B, Hq, N), torch.float32, q.device)
+    fa.fa_fwd(q, k, v, causal=causal, scale=scale, o=o.t, lse=lse.t)
     assert fa.fa_get_device_error() == fa.FA_OK
-    return o.cpu(), lse.cpu()
+    check_all(o=o, lse=lse)
+    return o.t.cpu(), lse.t.cpu()
 
 
 # (B, Hq, Hkv, N, d, causal): several tiles, ragged tails, N=1, GQA and MQA
