@@ -317,25 +317,36 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False):
 
 
 # -------------------------------------------------------------- dK/dV kernel
-def dkdv_model(n_it, NST=2, dk_before_dsf=False):
+def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
     """Sixteen compute warps (g, q): query columns 32g.. of the transposed
-    tiles (warpgroup g) and key rows 32q.. (TMEM lanes)."""
+    tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  P^T goes over the
+    S^T columns a warp read; dS^T goes to shared memory, over the stage's dO
+    tile (ds_in_do, d = 128) or into a buffer of its own (d = 64), once the
+    MMA thread's DVD commit after dV(it) has completed."""
     warps = [(g, q) for g in range(4) for q in range(4)]
 
     def model(rnd):
-        bars = {"KV": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1}
+        bars = {"KV": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1, "DVD": 1}
         for s in range(NST):
             bars[f"STF{s}"] = 1 + 32  # the load, and the 32 lanes' vector writes
             bars[f"STE{s}"] = 1
 
-        def reg_s(it):  # S^T(it), then P^T(it) / dS^T(it)
+        def reg_s(it):  # S^T(it), then P^T(it)
             return "Y" if it & 1 else "X"
 
         def reg_d(it):  # dP^T(it)
             return "X" if it & 1 else "Y"
 
         def region(r, tag):
-            return {f"{r}.{g}.{q}.{c}": tag for g, q in warps for c in "pd"}
+            return {f"{r}.{g}.{q}": tag for g, q in warps}
+
+        def ds_buf(it, g, q):  # the shared-memory rows of dS^T(it) warp (g, q) writes
+            return f"dO{it % NST}.{g}.{q}" if ds_in_do else f"DS.{g}.{q}"
+
+        def stage_load(it):
+            tags = {f"Q{it % NST}": f"Q({it})"}
+            tags.update({f"dO{it % NST}.{g}.{q}": f"dO({it})" for g, q in warps})
+            return tags
 
         def producer():
             yield ("load", "KV", 0, {"K": "K", "V": "V"})
@@ -343,7 +354,7 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False):
             for it in range(n_it):
                 s = it % NST
                 yield ("wait", f"STE{s}", it // NST - 1)
-                yield ("load", f"STF{s}", it // NST, {f"stage{s}": f"QdO({it})"})
+                yield ("load", f"STF{s}", it // NST, stage_load(it))
                 yield ("write", {f"vec{s}": f"lse,D({it})"})
                 yield ("arrive", f"STF{s}", 32, it // NST)
                 last[s] = it // NST
@@ -352,20 +363,27 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False):
                 yield ("wait", f"STF{s}", ph)
 
         def st_mma(it):
-            return ("mma", f"S^T({it})", {"K": "K", f"stage{it % NST}": f"QdO({it})"},
+            return ("mma", f"S^T({it})", {"K": "K", f"Q{it % NST}": f"Q({it})"},
                     region(reg_s(it), f"S^T({it})"))
 
         def dpt_mma(it):
-            return ("mma", f"dP^T({it})", {"V": "V", f"stage{it % NST}": f"QdO({it})"},
-                    region(reg_d(it), f"dP^T({it})"))
+            reads = {"V": "V"}
+            reads.update({f"dO{it % NST}.{g}.{q}": f"dO({it})" for g, q in warps})
+            return ("mma", f"dP^T({it})", reads, region(reg_d(it), f"dP^T({it})"))
 
-        def acc_mma(it, dk):
-            nm, c, tag = ("dK", "d", "dS^T") if dk else ("dV", "p", "P^T")
-            reads = {f"{reg_s(it)}.{g}.{q}.{c}": f"{tag}({it})" for g, q in warps}
-            reads[f"stage{it % NST}"] = f"QdO({it})"
+        def dv_mma(it):
+            reads = {f"{reg_s(it)}.{g}.{q}": f"P^T({it})" for g, q in warps}
+            reads.update({f"dO{it % NST}.{g}.{q}": f"dO({it})" for g, q in warps})
             if it > 0:
-                reads[nm] = f"{nm}({it - 1})"
-            return ("mma", f"{nm}({it})", reads, {nm: f"{nm}({it})"})
+                reads["dV"] = f"dV({it - 1})"
+            return ("mma", f"dV({it})", reads, {"dV": f"dV({it})"})
+
+        def dk_mma(it):
+            reads = {ds_buf(it, g, q): f"dS^T({it})" for g, q in warps}
+            reads[f"Q{it % NST}"] = f"Q({it})"
+            if it > 0:
+                reads["dK"] = f"dK({it - 1})"
+            return ("mma", f"dK({it})", reads, {"dK": f"dK({it})"})
 
         def mma():
             yield ("wait", "KV", 0)
@@ -381,14 +399,15 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False):
                     yield ("wait", "LD", it)
                     yield st_mma(it + 1)  # over dP^T(it)
                 yield ("wait", "PF", it)
-                yield acc_mma(it, False)
+                yield dv_mma(it)
+                yield ("commit", "DVD", it)
+                if more:
+                    yield dpt_mma(it + 1)  # over P^T(it)
+                    yield ("commit", "SDF", it + 1)
                 if not dk_before_dsf:
                     yield ("wait", "DSF", it)
-                yield acc_mma(it, True)
+                yield dk_mma(it)
                 yield ("commit", f"STE{s}", it // NST)
-                if more:
-                    yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
-                    yield ("commit", "SDF", it + 1)
             yield ("commit", "ACC", 0)
             yield ("wait", "ACC", 0)
 
@@ -398,17 +417,18 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False):
                 s = it % NST
                 rs, rd = reg_s(it), reg_d(it)
                 yield ("wait", "SDF", it)
-                yield ("read", {f"{rd}.{me}.p": f"dP^T({it})", f"{rd}.{me}.d": f"dP^T({it})",
-                                f"vec{s}": f"lse,D({it})"})
+                yield ("read", {f"{rd}.{me}": f"dP^T({it})", f"vec{s}": f"lse,D({it})"})
                 yield ("arrive", "LD", 32, it)
-                yield ("read", {f"{rs}.{me}.p": f"S^T({it})", f"{rs}.{me}.d": f"S^T({it})"})
-                yield ("write", {f"{rs}.{me}.p": f"P^T({it})"})
+                yield ("read", {f"{rs}.{me}": f"S^T({it})"})
+                yield ("write", {f"{rs}.{me}": f"P^T({it})"})
                 yield ("arrive", "PF", 32, it)
-                yield ("write", {f"{rs}.{me}.d": f"dS^T({it})"})
+                if not skip_dvd:
+                    yield ("wait", "DVD", it)
+                yield ("write", {ds_buf(it, g, q): f"dS^T({it})"})
                 yield ("arrive", "DSF", 32, it)
             yield ("wait", "ACC", 0)
             yield ("read", {"dV": f"dV({n_it - 1})", "dK": f"dK({n_it - 1})"})
-            yield ("write", {"stage0": "out"})  # staging in stage 0's tiles
+            yield ("write", {"Q0": "out"})  # staging in stage 0's tiles
 
         roles = {"prod": producer(), "mma": mma()}
         for g, q in warps:
@@ -418,7 +438,6 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False):
     return model
 
 
-# ------------------------------------------------------------ forward kernel
 def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
     """Two query tiles: tile 0 multiplies key blocks [0, nkv0), tile 1
     [0, nkv) (nkv0 < nkv on the causal diagonal); four softmax warps per
@@ -660,8 +679,9 @@ def test_dq_protocol(nj):
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
-def test_dkdv_protocol(n_it):
-    each_seed(dkdv_model(n_it))
+@pytest.mark.parametrize("ds_in_do", [True, False])
+def test_dkdv_protocol(n_it, ds_in_do):
+    each_seed(dkdv_model(n_it, ds_in_do=ds_in_do))
 
 
 @pytest.mark.parametrize("nkv0,nkv,nslot", [(1, 1, 4), (1, 2, 4), (2, 3, 4), (5, 6, 4), (8, 8, 4),
@@ -706,6 +726,13 @@ def test_decode_rescale_without_pv_wait_is_caught():
 def test_dkdv_dk_before_ds_is_caught():
     # dK += dS^T Q issued before the warpgroups have written dS^T
     assert fails_on_some_seed(dkdv_model(4, dk_before_dsf=True))
+
+
+@pytest.mark.parametrize("ds_in_do", [True, False])
+def test_dkdv_ds_write_without_dv_done_is_caught(ds_in_do):
+    # dS^T written over the dO tile before dV(it) has read it (d = 128), or
+    # into its own buffer before dK(it-1) has read the previous one (d = 64)
+    assert fails_on_some_seed(dkdv_model(5, ds_in_do=ds_in_do, skip_dvd=True))
 
 
 def test_ring_without_empty_wait_is_caught():

@@ -32,7 +32,7 @@ pytestmark = pytest.mark.gpu
 
 # max-abs error beyond bf16 output rounding of dQ, dK, dV on the peaked-row
 # recipe (bf16 P and dS), the limit include/fa.h states for fa_bwd_noalloc
-NOALLOC_PEAKED_MAXABS = 0.5
+NOALLOC_PEAKED_MAXABS = 0.15
 
 
 def _noalloc(lib, t, B, H, Hkv, N, d, causal, scale):
