@@ -61,14 +61,20 @@ class Bar:
 
 
 class Cta:
-    """Barriers, buffer tags, loads in flight and the tensor core's queue."""
+    """Barriers, buffer tags, loads in flight and the tensor core's queues:
+    one per issuing thread, each run in order (a commit arrives once
+    everything its thread issued before it has run), the queues of two
+    issuing threads interleaved in any order."""
 
     def __init__(self, bars):
         self.bars = {n: Bar(n, c) for n, c in bars.items()}
         self.mem = {}
         self.inflight = set()
         self.loads = []
-        self.tc = deque()
+        self.tcq = {}
+
+    def tc_busy(self):
+        return any(self.tcq.values())
 
     def read(self, reads, who):
         for buf, tag in reads.items():
@@ -101,7 +107,7 @@ class Cta:
                 self.inflight.add(buf)
             self.loads.append((bar, phase, writes))
         elif kind in ("mma", "commit"):
-            self.tc.append(op)
+            self.tcq.setdefault(who, deque()).append(op)
         elif kind == "read":
             self.read(op[1], who)
         elif kind == "write":
@@ -117,8 +123,8 @@ class Cta:
             self.mem[buf] = tag
         self.bars[bar].arrive(1, phase)
 
-    def run_tc(self):
-        op = self.tc.popleft()
+    def run_tc(self, rnd):
+        op = self.tcq[rnd.choice(sorted(w for w, q in self.tcq.items() if q))].popleft()
         if op[0] == "commit":
             self.bars[op[1]].arrive(1, op[2])
         else:
@@ -144,8 +150,8 @@ def simulate(model, seed, max_steps=500000):
             cur[r] = op
     for _ in range(max_steps):
         if not cur:
-            if cta.tc or cta.loads:
-                raise ProtocolError(f"exit with work in flight: {list(cta.tc)[:2]} {cta.loads[:2]}")
+            if cta.tc_busy() or cta.loads:
+                raise ProtocolError(f"exit with work in flight: {cta.tcq} {cta.loads[:2]}")
             return
         progressed = False
         for r in rnd.sample(sorted(cur), len(cur)):
@@ -161,10 +167,10 @@ def simulate(model, seed, max_steps=500000):
         if cta.loads and rnd.random() < p_load:
             cta.land(rnd.randrange(len(cta.loads)))
             progressed = True
-        if cta.tc and rnd.random() < p_tc:
-            cta.run_tc()
+        if cta.tc_busy() and rnd.random() < p_tc:
+            cta.run_tc(rnd)
             progressed = True
-        if not progressed and not cta.tc and not cta.loads and all(
+        if not progressed and not cta.tc_busy() and not cta.loads and all(
                 op[0] == "wait" and not cta.step(r, op) for r, op in cur.items()):
             raise ProtocolError(f"deadlock: {cur}")
     raise ProtocolError("did not finish")
@@ -210,16 +216,23 @@ def ring_bars(nslot):
 
 
 # ---------------------------------------------------------------- dQ kernel
-def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False):
+def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuers=False,
+             single_dqd=False, skip_dqd=False):
     """Eight compute warps (w, q): key half w (64 columns of S, dP) and TMEM
     lanes 32q.. (query rows); each arrives on its own.  The MMA thread
     arrives on PFS once it has seen dS(j) complete; a warp waits for that
-    before its dS(j+1) arrival, so PF is never a phase ahead of its waiter."""
+    before its dS(j+1) arrival, so PF is never a phase ahead of its waiter.
+    two_issuers: S and dP are issued by one thread, dQ by another (its own
+    tensor-core queue); dQ(j) reads dS(j) in dP buffer j % 2, which dP(j+2)
+    overwrites, so the dQ thread commits DQD(j % 2) after dQ(j) and the S/dP
+    thread waits for it (phase j // 2) before dP(j+2); the dQ thread, which
+    waits for PF, is the one that arrives on PFS.  single_dqd (one DQD
+    barrier for both buffers) and skip_dqd are planted mistakes."""
     warps = [(w, q) for w in (0, 1) for q in range(4)]
 
     def model(rnd):
         bars = {"QDO": 1, "SDF": 1, "LD": 257, "PF": 257 if first_gate_design else 256, "ACC": 1,
-                "PFS": 1}
+                "PFS": 1, "DQD0": 1, "DQD1": 1, "DONE": 1}
         for nm, ns in (("K", KS), ("V", VS)):
             for s in range(ns):
                 bars[f"{nm}F{s}"] = bars[f"{nm}E{s}"] = 1
@@ -280,17 +293,46 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False):
                 if j + 1 < nj:
                     yield ("wait", "LD", j)
                     yield s_mma(j + 1)
+                    if two_issuers and j + 1 >= 2 and not skip_dqd:
+                        # dQ(j-1), the last reader of dP buffer (j+1) % 2
+                        if single_dqd:
+                            yield ("wait", "DQD0", j - 1)
+                        else:
+                            yield ("wait", f"DQD{(j + 1) & 1}", (j - 1) >> 1)
                     yield dp_mma(j + 1)
                     yield ("commit", f"VE{(j + 1) % VS}", (j + 1) // VS)
                     yield ("commit", "SDF", j + 1)
+                if two_issuers:
+                    continue
                 yield ("wait", "PF", j)
                 if handshake:
                     yield ("arrive", "PFS", 1, j)
-                reads = dict(every(f"DP{j & 1}", f"dS({j})"), **{f"K{j % KS}": f"K({j})"})
-                if j > 0:
-                    reads["dQ"] = f"dQ({j - 1})"
-                yield ("mma", f"dQ({j})", reads, {"dQ": f"dQ({j})"})
+                yield dq_mma(j)
                 yield ("commit", f"KE{j % KS}", j // KS)
+            if two_issuers:
+                yield ("commit", "DONE", 0)
+                yield ("wait", "DONE", 0)
+            else:
+                yield ("commit", "ACC", 0)
+                yield ("wait", "ACC", 0)
+
+        def dq_mma(j):
+            reads = dict(every(f"DP{j & 1}", f"dS({j})"), **{f"K{j % KS}": f"K({j})"})
+            if j > 0:
+                reads["dQ"] = f"dQ({j - 1})"
+            return ("mma", f"dQ({j})", reads, {"dQ": f"dQ({j})"})
+
+        def mma_dq():
+            for j in range(nj):
+                yield ("wait", "PF", j)
+                if handshake:
+                    yield ("arrive", "PFS", 1, j)
+                yield dq_mma(j)
+                yield ("commit", f"KE{j % KS}", j // KS)
+                if single_dqd:
+                    yield ("commit", "DQD0", j)
+                else:
+                    yield ("commit", f"DQD{j & 1}", j >> 1)
             yield ("commit", "ACC", 0)
             yield ("wait", "ACC", 0)
 
@@ -309,6 +351,8 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False):
             yield ("write", {f"Q.{me}": "dQ out"})  # staging in the Q tile
 
         roles = {"prod": producer(), "gate": gate(), "copy": copy(), "mma": mma()}
+        if two_issuers:
+            roles["mmaq"] = mma_dq()
         for w, q in warps:
             roles[f"c{w}{q}"] = compute(w, q)
         return bars, roles
@@ -674,8 +718,9 @@ def single_s_model(nkv, NSLOT=4, skip_empty=False):
 
 # ------------------------------------------------------------------ the kernels
 @pytest.mark.parametrize("nj", [1, 2, 3, 4, 7, 20])
-def test_dq_protocol(nj):
-    each_seed(dq_model(nj))
+@pytest.mark.parametrize("two_issuers", [False, True])
+def test_dq_protocol(nj, two_issuers):
+    each_seed(dq_model(nj, two_issuers=two_issuers))
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
@@ -711,6 +756,17 @@ def test_dq_without_handshake_is_caught():
     # phase of dS(j-1), or dS(j+1) completes before the MMA thread has seen
     # dS(j), and its parity wait reads the phase as open
     assert fails_on_some_seed(dq_model(6, handshake=False))
+
+
+def test_dq_two_issuers_without_dq_done_is_caught():
+    # dP(j+2) written over dS(j) before the other thread's dQ(j) has read it
+    assert fails_on_some_seed(dq_model(8, two_issuers=True, skip_dqd=True))
+
+
+def test_dq_two_issuers_single_dq_done_barrier_is_caught():
+    # one DQD barrier for both dP buffers: the dQ thread can complete two of
+    # its phases before the S/dP thread waits, and the parity then aliases
+    assert fails_on_some_seed(dq_model(8, two_issuers=True, single_dqd=True))
 
 
 def test_forward_early_score_product_is_caught():
