@@ -794,3 +794,304 @@ def test_dkdv_ds_write_without_dv_done_is_caught(ds_in_do):
 def test_ring_without_empty_wait_is_caught():
     # a load into a ring slot whose previous tile an MMA still has to read
     assert fails_on_some_seed(single_s_model(9, skip_empty=True))
+
+
+# ----------------------------------------------- the forward's time-out path
+# The kernels bound every mbarrier wait.  A wait that runs out records the
+# failure (status word) and returns false; a pending wait of the same launch
+# that sees a recorded failure returns false within a few polls; the waits a
+# block makes for its own copies and MMAs before it exits (mbar_drain) ignore
+# other blocks' failures and give up on their time limit alone.  Every other
+# wait in the kernels is either hardware-bounded (tcgen05.wait::ld/st, the TMA
+# store's wait_group.read) or a bar.sync that every participating thread
+# reaches on every path.  The model below runs the forward kernel's roles as
+# generators that receive each bounded wait's result, exactly as the CUDA code
+# branches on it, with named barriers (bar.sync) and the block-wide teardown
+# barrier that block until every participant arrives.  Faults: waits that run
+# out at random (any wait, any time), or an arrival that never happens.  In
+# every schedule the block must reach its teardown (no bar.sync left waiting),
+# with no load or MMA in flight, and with the failure recorded when a wait ran
+# out.
+
+
+def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=2000000):
+    rnd = random.Random(seed)
+    bars, roles = model(random.Random(seed + 7))
+    cta = Cta(bars)
+    state = {"failed": False}
+    speed = {r: rnd.choice((0.05, 0.3, 1.0)) for r in sorted(roles)}
+    p_load, p_tc = rnd.choice((0.05, 0.3, 1.0)), rnd.choice((0.05, 0.3, 1.0))
+    cur, polls, nbar = {}, {}, {}
+
+    def advance(r, value):
+        try:
+            cur[r] = op = roles[r].send(value)
+        except StopIteration:
+            del cur[r]
+            return
+        if op[0] == "nbar":  # a thread arrives at bar.sync as soon as it reaches it
+            _, name, count = op
+            waiting = nbar.setdefault(name, set())
+            waiting.add(r)
+            if len(waiting) == count:
+                del nbar[name]
+                for w in sorted(waiting):
+                    advance(w, None)
+
+    for r in roles:
+        advance(r, None)
+    for _ in range(max_steps):
+        if not cur:
+            if cta.tc_busy() or cta.loads:
+                raise ProtocolError(f"exit with work in flight: {cta.tcq} {cta.loads[:2]}")
+            return state["failed"]
+        progressed = False
+        for r in rnd.sample(sorted(cur), len(cur)):
+            if r not in cur or rnd.random() >= speed[r]:
+                continue
+            op = cur[r]
+            if op[0] == "twait":
+                _, bar, phase, mode = op
+                try:
+                    done = cta.bars[bar].done(phase)
+                except ProtocolError as e:
+                    raise ProtocolError(f"{r}: {e}") from None
+                if done:
+                    polls.pop(r, None)
+                    advance(r, True)
+                    progressed = True
+                    continue
+                polls[r] = polls.get(r, 0) + 1
+                runs_out = polls[r] > (50 * limit if mode == "drain" else limit) or (
+                    mode == "abort" and rnd.random() < p_spurious)
+                gives_up = mode == "abort" and state["failed"] and polls[r] >= 16
+                if runs_out or gives_up:
+                    state["failed"] |= runs_out
+                    polls.pop(r, None)
+                    advance(r, False)
+                    progressed = True
+            elif op[0] == "nbar":
+                continue  # released by the last participant's arrival
+            else:
+                cta.step(r, op)
+                advance(r, None)
+                progressed = True
+        if cta.loads and rnd.random() < p_load:
+            cta.land(rnd.randrange(len(cta.loads)))
+            progressed = True
+        if cta.tc_busy() and rnd.random() < p_tc:
+            cta.run_tc(rnd)
+            progressed = True
+        if (not progressed and not cta.tc_busy() and not cta.loads and cur
+                and all(op[0] == "nbar" for op in cur.values())):
+            raise ProtocolError(f"bar.sync never completes: {nbar}")
+    raise ProtocolError("did not finish")
+
+
+def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
+    """The forward kernel's roles with every bounded wait's two outcomes:
+    producer, gate, copy warp, MMA thread and the eight softmax warps (four
+    per query tile), the epilogue's bar.sync over a tile's four warps, and the
+    teardown __syncthreads over every role.  drop = (t, j): the gate's
+    arrival on p_full(t) for key block j never happens (a protocol fault)."""
+    rows = range(4)
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
+        bars.update(ring_bars(NSLOT))
+        n_of = (nkv0, nkv)
+        n_roles = 3 + 8 + (1 if copy_q else 0)
+
+        def tile(pre, t, tag):
+            return {f"{pre}.{t}.{q}": tag for q in rows}
+
+        def teardown():
+            yield ("nbar", "syncthreads", n_roles)
+
+        def producer():
+            last = {}
+            yield ("load", "Q", 0, dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            ok = True
+            for j in range(nkv):
+                for w, nm in enumerate(("K", "V")):
+                    idx = 2 * j + w
+                    s = idx % NSLOT
+                    ok = yield ("twait", f"E{s}", idx // NSLOT - 1, "abort")
+                    if not ok:
+                        break
+                    yield ("load", f"F{s}", idx // NSLOT, {f"kv{s}": f"{nm}({j})"})
+                    last[s] = idx // NSLOT
+                if not ok:
+                    break
+            yield ("twait", "Q", 0, "drain")
+            for s, ph in last.items():
+                yield ("twait", f"F{s}", ph, "drain")
+            yield from teardown()
+
+        def gate():
+            ok = True
+            for j in range(nkv):
+                v, kn = 2 * j + 1, 2 * j + 2
+                ok = yield ("twait", f"F{v % NSLOT}", v // NSLOT, "abort")
+                if ok and j + 1 < nkv:
+                    ok = yield ("twait", f"F{kn % NSLOT}", kn // NSLOT, "abort")
+                for t in (0, 1):
+                    if not ok:
+                        break
+                    if j >= n_of[t]:
+                        continue
+                    if j > 0:
+                        ok = yield ("twait", f"PF{t}", j - 1, "abort")
+                    if ok and (t, j) != drop:
+                        yield ("arrive", f"PF{t}", 1, j)
+                if not ok:
+                    break
+            yield from teardown()
+
+        def copy():
+            ok = yield ("twait", "Q", 0, "abort")
+            if ok:
+                yield ("read", dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            yield ("arrive", "QC", 1, 0)  # also after a failed wait
+            yield from teardown()
+
+        def qk(t, j):
+            slot = (2 * j) % NSLOT
+            return ("mma", f"QK({t},{j})", dict(tile("Q", t, "Q"), **{f"kv{slot}": f"K({j})"}),
+                    tile("S", t, f"S({t},{j})"))
+
+        def pv(t, j):
+            slot = (2 * j + 1) % NSLOT
+            reads = dict(tile("S", t, f"P({t},{j})"), **{f"kv{slot}": f"V({j})"})
+            if j > 0:
+                reads.update(tile("O", t, f"O({t},{j - 1})"))
+            return ("mma", f"PV({t},{j})", reads, tile("O", t, f"O({t},{j})"))
+
+        def mma():
+            ok = yield ("twait", "Q", 0, "abort")
+            if ok:
+                ok = yield ("twait", "F0", 0, "abort")
+                if ok:
+                    yield qk(0, 0)
+                    yield ("commit", "SF0", 0)
+                    yield qk(1, 0)
+                    yield ("commit", "SF1", 0)
+                    yield ("commit", "E0", 0)
+            for j in range(nkv):
+                if not ok:
+                    break
+                vslot, kidx = (2 * j + 1) % NSLOT, 2 * (j + 1)
+                kslot = kidx % NSLOT
+                if j < nkv0:
+                    ok = yield ("twait", "PF0", j, "abort")
+                    if not ok:
+                        break
+                    yield pv(0, j)
+                    if j == nkv0 - 1:
+                        yield ("commit", "OF0", 0)
+                if j + 1 < nkv0:
+                    yield qk(0, j + 1)
+                    yield ("commit", "SF0", j + 1)
+                ok = yield ("twait", "PF1", j, "abort")
+                if not ok:
+                    break
+                yield pv(1, j)
+                yield ("commit", f"E{vslot}", (2 * j + 1) // NSLOT)
+                if j == nkv - 1:
+                    yield ("commit", "OF1", 0)
+                if j + 1 < nkv:
+                    yield qk(1, j + 1)
+                    yield ("commit", "SF1", j + 1)
+                    yield ("commit", f"E{kslot}", kidx // NSLOT)
+            yield ("commit", "DONE", 0)
+            yield ("twait", "DONE", 0, "drain")
+            yield from teardown()
+
+        def softmax(t, q):
+            ok = True
+            for j in range(n_of[t]):
+                ok = yield ("twait", f"SF{t}", j, "abort")
+                if not ok:
+                    break
+                yield ("read", {f"S.{t}.{q}": f"S({t},{j})"})
+                yield ("write", {f"S.{t}.{q}": f"P({t},{j})"})
+                if j > 0 and rnd.random() < 0.5:  # the lazy rescale of O
+                    yield ("read", {f"O.{t}.{q}": f"O({t},{j - 1})"})
+                    yield ("write", {f"O.{t}.{q}": f"O({t},{j - 1})"})
+                yield ("arrive", f"PF{t}", 32, j)
+            ok_e = ok and (yield ("twait", f"OF{t}", 0, "abort"))
+            if copy_q:
+                ok_e = ok_e and (yield ("twait", "QC", 0, "abort"))
+            if ok_e:
+                yield ("read", {f"O.{t}.{q}": f"O({t},{n_of[t] - 1})"})
+                yield ("write", {f"Q.{t}.{q}": "O out"})  # staging in the Q buffer
+            yield ("nbar", f"epilogue{t}", 4)
+            yield from teardown()
+
+        roles = {"prod": producer(), "gate": gate(), "mma": mma()}
+        if copy_q:
+            roles["copy"] = copy()
+        for t in (0, 1):
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
+        return bars, roles
+
+    return model
+
+
+FWD_TIMEOUT_SHAPES = [(1, 2, 4), (2, 3, 4), (5, 6, 4), (4, 4, 8)]
+
+
+@pytest.mark.parametrize("nkv0,nkv,nslot", FWD_TIMEOUT_SHAPES)
+def test_forward_without_faults_never_times_out(nkv0, nkv, nslot):
+    for seed in range(30):
+        failed = simulate_with_timeouts(fwd_timeout_model(nkv0, nkv, nslot), seed, limit=10 ** 6)
+        assert not failed
+
+
+@pytest.mark.parametrize("nkv0,nkv,nslot", FWD_TIMEOUT_SHAPES)
+@pytest.mark.parametrize("copy_q", [True, False])
+def test_forward_any_wait_running_out_ends_the_block_cleanly(nkv0, nkv, nslot, copy_q):
+    # waits run out at random; whichever do, every role reaches the teardown,
+    # the epilogue's bar.sync completes and nothing is left in flight
+    n_failed = 0
+    for seed in range(120):
+        n_failed += simulate_with_timeouts(fwd_timeout_model(nkv0, nkv, nslot, copy_q), seed,
+                                           p_spurious=0.01, limit=300)
+    assert n_failed > 60  # the fault path ran in most schedules
+
+
+@pytest.mark.parametrize("drop", [(0, 0), (1, 0), (1, 2), (0, 1)])
+def test_forward_lost_arrival_is_reported_and_ends_the_block(drop):
+    # an arrival on p_full that never comes: the waits on it run out, the
+    # failure is recorded, and the block still exits cleanly
+    for seed in range(40):
+        assert simulate_with_timeouts(fwd_timeout_model(2, 3, 4, drop=drop), seed, limit=2000)
+
+
+def test_timeout_model_catches_a_partner_left_in_bar_sync():
+    # planted: a softmax warp that leaves on a failed wait without reaching
+    # the epilogue's bar.sync strands its three partners there
+    def model(rnd):
+        bars, roles = fwd_timeout_model(2, 3, 4, drop=(1, 1))(rnd)
+        inner = roles["s13"]
+
+        def deserter():
+            value = None
+            while True:
+                op = inner.send(value)
+                if op[0] == "nbar" and op[1].startswith("epilogue"):
+                    return
+                value = yield op
+        roles["s13"] = deserter()
+        return bars, roles
+
+    caught = False
+    for seed in range(20):
+        try:
+            simulate_with_timeouts(model, seed, limit=2000)
+        except ProtocolError:
+            caught = True
+            break
+    assert caught
