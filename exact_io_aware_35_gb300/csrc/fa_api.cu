@@ -273,6 +273,7 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
+    a.block_mask = nullptr;
     a.watch = make_watch(di->status);
     cudaError_t e = launch_fwd(maps, a, d, cs);
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
@@ -526,32 +527,28 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
     if (static_cast<long long>(B) * H * nb > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     DeviceInfo* di = nullptr;
     if ((st = device_ready(&di)) != FA_OK) return st;
-    DecodeMaps maps;
+    FwdMaps maps;
     if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
     if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
     if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
-    DecodeArgs a;
-    a.o = static_cast<uint16_t*>(o);
+    if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
+    // the forward kernel, each of its two query tiles walking its own mask row
+    FwdArgs a;
     a.lse = lse;
-    a.part_o = nullptr;
-    a.part_lse = nullptr;
+    a.o_lo = nullptr;
+    a.f16s = nullptr;
+    a.q16 = nullptr;
     a.B = B;
     a.Hq = H;
     a.Hkv = Hkv;
-    a.Nq = N;
-    a.Nk = N;
+    a.N = N;
     a.g = H / Hkv;
-    a.gp = 1;
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.qpt = kBM;
-    a.n_qt = nb;
-    a.splits = 1;
-    a.blocks_per_split = nb;
+    a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
     a.block_mask = block_mask;
-    a.nkb = nb;
     a.watch = make_watch(di->status);
-    const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_fwd(maps, a, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_blocksparse launch");
     return FA_OK;
 }

@@ -6,31 +6,25 @@
 // lse * log2(e) and D for the block's queries staged by the TMA warp.  For
 // each, S^T = K Q_i^T and dP^T = V dO_i^T are recomputed into TMEM (keys on
 // the TMEM lanes), turned into P^T = exp2(S^T * scale * log2(e) - lse2) and
-// dS^T = P^T o (dP^T - D); dV += P^T dO_i takes P^T straight from TMEM as the
-// A operand and dK += dS^T Q_i takes dS^T from shared memory, where the
-// threads that formed it wrote it in the K-major operand layout -- so no
+// dS^T = P^T o (dP^T - D) in place (bf16), and dV += P^T dO_i,
+// dK += dS^T Q_i take P^T / dS^T straight from TMEM as the A operand -- so no
 // transpose is ever materialised.  The group's query heads are summed inside
 // the CTA: no atomics.
 //
 // Pipelining.  Every MMA is 128 wide: a tcgen05.mma with N = 64 costs its
 // issuing thread about as long as one with N = 128 and reads more shared
 // memory per flop.  Two 128-column TMEM regions X and Y swap roles every
-// block: S^T(i) and then P^T(i) live in one, dP^T(i) in the other.  As soon
-// as all warpgroups have copied dP^T(i) into registers, the tensor core
-// computes S^T(i+1) over it while they work.  dV += P^T dO of block i takes
-// P^T straight from TMEM as the A operand once it is written, and dP^T(i+1)
-// then goes over it at once.  dS^T(i), formed in registers together with
-// P^T, goes to shared memory instead: over the stage's dO tile, whose last
-// reader is dV(i) (barrier DVD, committed after dV(i)), or at d = 64, where
-// that tile is too small, into a buffer of its own, free by then as well
-// (dK(i-1) ran before dV(i)).  So dK += dS^T Q(i) reads both operands from
-// shared memory and runs after dP^T(i+1), off the chain that paces a block:
-// dS^T(i) written -> dV(i) -> dP^T(i+1) -> the next block's elementwise step.
-// Warpgroup w owns queries 32w..32w+31 of each block and writes its P^T
-// (16-bit pairs) over the S^T columns it read.  (Tried and dropped: 64-query
-// sub-blocks with two TMEM buffers of 64-wide S^T and dP^T; the 64-wide
-// products ran at about 100 cycles per MMA in the kernel, and the whole was
-// 24% slower.)
+// block: S^T(i) and then P^T(i), dS^T(i) live in one, dP^T(i) in the other.
+// As soon as all warpgroups have copied dP^T(i) into registers, the tensor
+// core computes S^T(i+1) over it while they work; dV += P^T dO of block i
+// starts as soon as P^T(i) is written (the warpgroups store dS^T(i), already
+// formed in registers, after signalling P^T), dK += dS^T Q once dS^T(i) is,
+// and dP^T(i+1) is then written over both.  Warpgroup w owns queries
+// 32w..32w+31 of each block and writes its P^T and dS^T (16-bit pairs) over
+// the S^T columns it read.  (Tried and dropped: 64-query sub-blocks with two
+// TMEM buffers of 64-wide S^T and dP^T, which would hide the hand-off
+// entirely; the 64-wide products ran at about 100 cycles per MMA in the
+// kernel, and the whole was 24% slower.)
 //
 // TMEM (512 columns): X [0,128) | Y [128,256) | dV [256,256+D) | dK [256+D, 256+2D).
 #include "fa_bwd_common.cuh"
@@ -57,16 +51,10 @@ struct DkdvCfg : Tiles<D> {
     static constexpr int OFF_STAGE = 2 * T::TILE;
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
-    // dS^T (128 keys x 128 queries, 16-bit, K-major) goes over the stage's dO
-    // tile when that is as large (d = 128), else into a buffer of its own
-    static constexpr bool DS_IN_DO = (T::TILE == 2 * T::CHUNK);
-    static constexpr int DS_BYTES = DS_IN_DO ? 0 : 2 * T::CHUNK;
-    static constexpr int OFF_DS = OFF_VEC + NST * VEC_BYTES;
-    static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+    static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
     // barriers: K/V, stage full[NST], stage empty[NST], S^T+dP^T ready,
-    // dP^T copied to registers, P^T written, dS^T written, all MMAs done,
-    // dV done
-    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1 + 1;
+    // dP^T copied to registers, P^T written, dS^T written, all MMAs done
+    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
 };
@@ -102,11 +90,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T written
     const uint32_t BAR_DSF = BAR_SDF + 24u;                 // dS^T written
     const uint32_t BAR_ACC = BAR_SDF + 32u;
-    const uint32_t BAR_DVD = BAR_SDF + 40u;                 // dV(it) done: dS^T(it) may be written
-    // where dS^T(it) goes: stage s's dO tile, or the kernel's own buffer
-    auto ds_tile = [&](int s) {
-        return C::DS_IN_DO ? sStage + (2 * s + 1) * C::TILE : sK + C::OFF_DS;
-    };
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -131,7 +114,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_init(BAR_PF, kDkCompute);
         mbar_init(BAR_DSF, kDkCompute);
         mbar_init(BAR_ACC, 1);
-        mbar_init(BAR_DVD, 1);
         fence_barrier_init();
     }
     if (warp == kDkWarpMma) {
@@ -233,25 +215,16 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     mma_bf16_ss(dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_S, ks > 0);
                 }
             };
-            // dV += P^T dO: for queries 16ks.., P^T (16-bit pairs) sits in columns
-            // 32w + (ks%2)*8 of S^T's region (w = ks/2); dO rows 16ks.. are read
-            // MN-major
-            auto issue_dv = [&](int it, int s) {
-                const uint32_t b_lo = sdesc_lo(stage_q(s) + C::TILE, C::CHUNK);
-                const uint32_t rs = reg_s(it);
+            // dV += P^T dO (dk = false) or dK += dS^T Q (dk = true): for queries
+            // 16ks.., P^T / dS^T (16-bit pairs) sit in columns 32w + (ks%2)*8 /
+            // 32w + 16 + (ks%2)*8 of S^T's region (w = ks/2); dO, Q rows 16ks.. are
+            // read MN-major
+            auto issue_acc = [&](int it, int s, bool dk) {
+                const uint32_t b_lo = sdesc_lo(stage_q(s) + (dk ? 0 : C::TILE), C::CHUNK);
+                const uint32_t rs = reg_s(it) + (dk ? 16 : 0);
 #pragma unroll
                 for (int ks = 0; ks < kBM / 16; ++ks)
-                    mma_bf16_ts(tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
-                                sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
-            };
-            // dK += dS^T Q: dS^T K-major from shared memory (queries 16ks.. at
-            // chunk ks/4, byte 32(ks%4) of each key row), Q rows 16ks.. MN-major
-            auto issue_dk = [&](int it, int s) {
-                const uint32_t a_lo = sdesc_lo(ds_tile(s), 16);
-                const uint32_t b_lo = sdesc_lo(stage_q(s), C::CHUNK);
-#pragma unroll
-                for (int ks = 0; ks < kBM / 16; ++ks)
-                    mma_bf16_ss(tDK, sdesc_at(a_lo, HI, (ks >> 2) * C::CHUNK + (ks & 3) * 32),
+                    mma_bf16_ts(dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
                                 sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
             };
             bool ok = mbar_wait(BAR_KV, 0, a.watch, 32) &&
@@ -274,21 +247,19 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     tc_fence_after();
                     issue_t(reg_d(it), k_lo, stage_q(s2));
                 }
-                // dV as soon as P^T is written; dP^T(it+1) over P^T(it) right after
-                // it (the tensor core runs one thread's MMAs in order); dK once
-                // dS^T is in shared memory, off the chain to the next block
+                // dV as soon as P^T is written, dK once dS^T is
                 if (!(ok = mbar_wait(BAR_PF, it & 1, a.watch, 34))) break;
                 tc_fence_after();
-                issue_dv(it, s);
-                mma_commit(BAR_DVD);
+                issue_acc(it, s, false);
+                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.watch, 38))) break;
+                tc_fence_after();
+                issue_acc(it, s, true);
+                mma_commit(BAR_STE(s));
                 if (more) {
+                    // dP^T(it+1) over P^T(it), dS^T(it): the products above read them first
                     issue_t(reg_s(it), v_lo, stage_q(s2) + C::TILE);
                     mma_commit(BAR_SDF);
                 }
-                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.watch, 38))) break;
-                tc_fence_after();
-                issue_dk(it, s);
-                mma_commit(BAR_STE(s));
             }
             // every issued MMA has finished before TMEM is released
             mma_commit(BAR_ACC);
@@ -384,28 +355,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR_PF);
-            // dS^T into shared memory (K-major, 128-byte swizzle: key row r at
-            // r * 128, queries in 16-byte pieces of 8, piece p at (p ^ r % 8) * 16),
-            // once dV(it) has read the tile it goes over.  The thread's pair
-            // (8j + 2(lane%4), +1) of its warpgroup's 32 queries is 4 bytes of
-            // piece 4(wg%2) + j; the 32 lanes of one store cover 8 key rows x 4
-            // words, one per bank.
-            if (!(ok = mbar_wait(BAR_DVD, it & 1, a.watch, 60))) break;
-            {
-                const uint32_t base = ds_tile(s) + (wg >> 1) * C::CHUNK + 4 * t4;
-                const int sw = lane >> 2;  // key row % 8
-#pragma unroll
-                for (int lb = 0; lb < 2; ++lb)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int rsel = 0; rsel < 2; ++rsel) {
-                            const int row = (warp & 3) * 32 + 16 * lb + 8 * rsel + sw;
-                            st_shared_b32(base + row * 128 + ((((wg & 1) * 4 + j) ^ sw) << 4),
-                                          dk[lb][2 * j + rsel]);
-                        }
-            }
-            fence_proxy_async_smem();
+            tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
+            tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
+            tmem_wait_st();
+            tc_fence_before();
             mbar_arrive(BAR_DSF);
         }
         const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.watch, 37);

@@ -42,9 +42,8 @@ struct DqCfg : Tiles<D> {
     static constexpr int OFF_V = OFF_K + KS * T::TILE;
     static constexpr int OFF_BAR = OFF_V + VS * T::TILE;
     // barriers: Q/dO, K full/empty[KS], V full/empty[VS], S+dP ready, copied to
-    // registers, dS written, the dQ thread's MMAs done, dS written seen by the
-    // dQ thread, dQ(j) done per dP buffer [2], the S/dP thread's MMAs done
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5 + 3;
+    // registers, dS written, all MMAs done, dS written seen by the MMA thread
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 5;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 384;
 };
@@ -88,11 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::KS + 2 * C::VS);  // S(j), dP(j) ready
     const uint32_t BAR_LD = BAR_SDF + 8u;   // S(j), dP(j) copied to registers
     const uint32_t BAR_PF = BAR_SDF + 16u;  // dS(j) written
-    const uint32_t BAR_ACC = BAR_SDF + 24u;  // the dQ thread's last MMA done: dQ final
-    const uint32_t BAR_PFS = BAR_SDF + 32u;  // the dQ thread has seen PF(j) complete
-    // dQ(j) done, one barrier per dP buffer (j % 2): dP(j+2) overwrites dS(j)
-    auto BAR_DQD = [&](int buf) { return BAR_SDF + 40u + 8u * buf; };
-    const uint32_t BAR_DONE = BAR_SDF + 56u;  // the S/dP thread's last MMA done
+    const uint32_t BAR_ACC = BAR_SDF + 24u;
+    const uint32_t BAR_PFS = BAR_SDF + 32u;  // the MMA thread has seen PF(j) complete
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -121,9 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR_PF, 256);
         mbar_init(BAR_ACC, 1);
         mbar_init(BAR_PFS, 1);
-        mbar_init(BAR_DQD(0), 1);
-        mbar_init(BAR_DQD(1), 1);
-        mbar_init(BAR_DONE, 1);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -134,14 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-
-    // shared by the two MMA-issuing threads: instruction descriptors, the
-    // dP buffers, and the fixed high words of the shared-memory descriptors
-    constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
-    constexpr uint32_t IDESC_DP = idesc_bf16(kBM, kBN, false, false);    // dP = dO V^T
-    constexpr uint32_t IDESC_DQ = idesc_16(kBM, D, false, true, F16);    // dQ += dS K
-    constexpr uint32_t HI = sdesc_hi(1024);
-    auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
 
     if (warp == kWarpLoad) {
         if (lane == 0) {
@@ -220,39 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_tile_to_f16<D>(sDO, dst, row_el, a.N - qi * kBM, mul, lane);
         }
         __syncwarp();
-        // ================= dQ issuer (one thread) =================
-        // It runs on another SM sub-partition than the S/dP issuer, so the two
-        // issue streams do not queue behind each other and the compute warps.
-        if (lane == 0) {
-            const uint32_t tDQ = tbase + C::TM_DQ;
-            bool ok = true;
-            for (int j = 0; j < nj && ok; ++j) {
-                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 62))) break;
-                mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
-                tc_fence_after();
-                // dQ += dS(j) K_j: dS (16-bit) of keys 16ks.. at columns
-                // 64(ks/4) + (ks%4)*8 of dP buffer j % 2; K rows 16ks.. read
-                // MN-major.  K_j is in place: S(j), which the warps read
-                // before writing dS(j), read it.
-                const uint32_t k_lo = sdesc_lo(sK + (j % C::KS) * C::TILE, C::CHUNK), aS = tDP(j);
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
-                                IDESC_DQ, (j == 0 && ks == 0) ? 0u : 1u);
-                // K_j's slot is free (S(j) finished before dS(j) was written),
-                // and so is dP buffer j % 2 for dP(j+2)
-                mma_commit(BAR_KE(j % C::KS));
-                mma_commit(BAR_DQD(j & 1));
-            }
-            // every issued MMA has finished before TMEM is released
-            mma_commit(BAR_ACC);
-            mbar_drain(BAR_ACC, 0, a.watch, 63);
-        }
-        __syncwarp();
     } else if (warp == kWarpMma) {
-        // ================= S and dP issuer (one thread) =================
         if (lane == 0) {
-            const uint32_t tS = tbase + C::TM_S;
+            constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
+            constexpr uint32_t IDESC_DP = idesc_bf16(kBM, kBN, false, false);    // dP = dO V^T
+            constexpr uint32_t IDESC_DQ = idesc_16(kBM, D, false, true, F16);    // dQ += dS K
+            const uint32_t tS = tbase + C::TM_S, tDQ = tbase + C::TM_DQ;
+            auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
             auto k_ready = [&](int jj) {
                 const bool r = mbar_wait(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.watch, 23);
                 tc_fence_after();
@@ -263,8 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return r;
             };
-            // descriptors: K-major tiles (S, dP operands), built once; each MMA
-            // only moves the start address
+            // descriptors: K-major tiles (S, dP operands) and the MN-major K tile
+            // (dQ), built once; each MMA only moves the start address
+            constexpr uint32_t HI = sdesc_hi(1024);
             const uint32_t q_lo = sdesc_lo(sQ, 16), do_lo = sdesc_lo(sDO, 16);
             // dst = A B^T over the head dimension (both K-major): S = Q K^T, dP = dO V^T
             auto issue_t = [&](uint32_t dst, uint32_t a_lo, uint32_t sB, uint32_t idesc) {
@@ -280,31 +240,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_t(tDP(jj), do_lo, sV + (jj % C::VS) * C::TILE, IDESC_DP);
                 mma_commit(BAR_VE(jj % C::VS));
             };
+            // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
+            // of dP buffer jj & 1; K rows 16ks.. read MN-major
+            auto issue_dq = [&](int jj) {
+                const uint32_t k_lo = sdesc_lo(sK + (jj % C::KS) * C::TILE, C::CHUNK), aS = tDP(jj);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
+                                IDESC_DQ, (jj == 0 && ks == 0) ? 0u : 1u);
+                mma_commit(BAR_KE(jj % C::KS));
+            };
             bool ok = mbar_wait(BAR_QDO, 0, a.watch, 22) && k_ready(0);
             if (ok) issue_t(tS, q_lo, sK, IDESC_S);
             if (ok && (ok = v_ready(0))) {
                 issue_dp(0);
                 mma_commit(BAR_SDF);
             }
-            for (int j = 0; j + 1 < nj && ok; ++j) {
-                // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j)
-                // and K_{j+1}, V_{j+1} have landed (the gate's arrival on LD);
-                // dP(j+1) into dP buffer (j+1) % 2 once the dQ thread's dQ(j-1)
-                // has read dS(j-1) there
-                if (!(ok = mbar_wait(BAR_LD, j & 1, a.watch, 24))) break;
-                tc_fence_after();
-                issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
-                if (j >= 1) {
-                    if (!(ok = mbar_wait(BAR_DQD((j + 1) & 1), ((j - 1) >> 1) & 1, a.watch, 61)))
-                        break;
+            for (int j = 0; j < nj && ok; ++j) {
+                // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j);
+                // dP(j+1) into the other dP buffer, over dS(j-1), which dQ(j-1)
+                // (issued earlier by this thread) has read; K_{j+1} and V_{j+1}
+                // have landed (the gate's arrival on LD)
+                if (j + 1 < nj) {
+                    if (!(ok = mbar_wait(BAR_LD, j & 1, a.watch, 24))) break;
                     tc_fence_after();
+                    issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
+                    issue_dp(j + 1);
+                    mma_commit(BAR_SDF);
                 }
-                issue_dp(j + 1);
-                mma_commit(BAR_SDF);
+                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 24))) break;
+                mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
+                tc_fence_after();
+                issue_dq(j);
             }
             // every issued MMA has finished before TMEM is released
-            mma_commit(BAR_DONE);
-            mbar_drain(BAR_DONE, 0, a.watch, 25);
+            mma_commit(BAR_ACC);
+            mbar_drain(BAR_ACC, 0, a.watch, 25);
         }
         __syncwarp();
     } else if (warp < 8) {

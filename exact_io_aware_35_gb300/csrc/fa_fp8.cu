@@ -15,13 +15,14 @@
 //     softmax scale) and s fixed random signs, which leaves Q K^T unchanged.
 //     V gets one scale per head and is stored transposed (d rows x keys), the
 //     K-major layout the P V product needs as its B operand.
-//   * Forward: one 128-query tile of one head per CTA, two CTAs per SM (16 KB
-//     tiles, 256 TMEM columns each: S, then P in e4m3 over it, and O), so one
-//     CTA's products overlap the other's softmax.  S = Q8 K8^T and O += P8 V8
-//     are tcgen05.mma kind::f8f6f4 (K = 32 per instruction); S is scaled by
-//     scale * log2 e * sq * sk_j in the softmax; P (at most 2^8 under the lazy
-//     rescale, inside e4m3's range) is rounded to e4m3 and written back to
-//     TMEM as the A operand of P V; O is multiplied by sv / l at the end.
+//   * Forward: two 128-query tiles of one head per CTA (16 KB e4m3 tiles, all
+//     512 TMEM columns: S0, S1, O0, O1), the products of one tile overlapping
+//     the softmax of the other as in the bf16 forward.  S = Q8 K8^T and
+//     O += P8 V8 are tcgen05.mma kind::f8f6f4 (K = 32 per instruction); S is
+//     scaled by scale * log2 e * sq * sk_j in the softmax; P (at most 2^8
+//     under the lazy rescale, inside e4m3's range) is rounded to e4m3 and
+//     written back to TMEM as the A operand of P V; O is multiplied by sv / l
+//     at the end.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -29,10 +30,13 @@ namespace fa {
 namespace {
 
 constexpr int kF8Tile = 128 * 128;  // bytes of a 128 x 128 e4m3 tile
-constexpr int kF8Slots = 4;         // K / V^T ring slots (two key blocks)
-constexpr int kF8Threads = 192;     // softmax warps 0-3, MMA warp 4, TMA warp 5
-constexpr int kF8WarpMma = 4;
-constexpr int kF8WarpLoad = 5;
+constexpr int kF8Slots = 8;         // K / V^T ring slots (four key blocks)
+constexpr int kF8Threads = 352;     // softmax warps 0-7 (two tiles), MMA 8, TMA 9, gate 10
+constexpr int kF8WarpMma = 8;
+constexpr int kF8WarpLoad = 9;
+constexpr int kF8WarpGate = 10;
+// barriers: Q, K/V full[slots], empty[slots], s_full[2], p_full[2], o_final[2], done
+constexpr int kF8Bars = 1 + 2 * kF8Slots + 2 + 2 + 2 + 1;
 constexpr float kE4m3Max = 448.f;
 
 // The fixed sign of column c in the rotation diag(s) H: the top bit of
@@ -187,33 +191,47 @@ __global__ void __launch_bounds__(128) fp8_vt_kernel(const uint16_t* __restrict_
     }
 }
 
-__global__ void __launch_bounds__(kF8Threads, 2)
+// The forward.  One CTA per (batch, head, 256-query block): two 128-row
+// query tiles in shared memory, K_j and V^T_j streamed through one ring, and
+// the matmul/softmax interleave of the bf16 forward -- the tensor core runs
+// one tile's products while the other tile's softmax runs -- with every
+// product a kind::f8f6f4 MMA (K = 32 per instruction).  TMEM: S0 | S1 | O0 |
+// O1, 128 columns each; P (e4m3, four per 32-bit column) goes over the first
+// 32 columns of its S and feeds P V from TMEM.  Warps 0-3 do the softmax of
+// tile 0, 4-7 of tile 1 (one query row per thread), warp 8 issues MMAs, warp
+// 9 loads, warp 10 is the gate: it folds "V_j and K_{j+1} landed" into the
+// p_full barriers, so the MMA thread waits on two barriers per key block.
+__global__ void __launch_bounds__(kF8Threads, 1)
     fa_fp8_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmVt, const Fp8Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sKV = sQ + kF8Tile;  // slot s at s * kF8Tile
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF8Tile + kF8Slots * kF8Tile);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kF8Slots + 4);
+    const uint32_t sQ = smem_u32(smem);  // Q0, Q1
+    const uint32_t sKV = sQ + 2 * kF8Tile;  // slot s at s * kF8Tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kF8Tile + kF8Slots * kF8Tile);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kF8Bars);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t BAR_Q = bar0;
     auto BAR_KVF = [&](int s) { return bar0 + 8u * (1 + s); };
     auto BAR_KVE = [&](int s) { return bar0 + 8u * (1 + kF8Slots + s); };
-    const uint32_t BAR_SF = bar0 + 8u * (1 + 2 * kF8Slots);  // S(j) ready
-    const uint32_t BAR_PF = BAR_SF + 8u;                      // P(j) written, O rescaled
-    const uint32_t BAR_OF = BAR_SF + 16u;                     // all products done
+    auto BAR_SF = [&](int t) { return bar0 + 8u * (1 + 2 * kF8Slots + t); };  // S_t(j) ready
+    auto BAR_PF = [&](int t) { return bar0 + 8u * (3 + 2 * kF8Slots + t); };  // P_t(j) written
+    auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * kF8Slots + t); };  // O_t final
+    const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * kF8Slots);
 
     const int warp = warp_id();
     const int lane = lane_id();
     const int per = a.B * a.Hq;
-    const int qt = a.nb - 1 - static_cast<int>(blockIdx.x) / per;  // longest tiles first
+    const int n_qblk = (a.nb + 1) / 2;
+    const int qb = n_qblk - 1 - static_cast<int>(blockIdx.x) / per;  // longest blocks first
     const int bh = static_cast<int>(blockIdx.x) % per;
     const int b = bh / a.Hq;
     const int h = bh % a.Hq;
     const int hk = h / a.g;
-    const int nkv = a.causal ? min(qt + 1, a.nb) : a.nb;
+    // key blocks tile t = 0, 1 (query blocks 2qb, 2qb + 1) multiplies
+    const int nkv0 = a.causal ? min(2 * qb + 1, a.nb) : a.nb;
+    const int nkv = a.causal ? min(2 * qb + 2, a.nb) : a.nb;
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_Q, 1);
@@ -221,29 +239,33 @@ __global__ void __launch_bounds__(kF8Threads, 2)
             mbar_init(BAR_KVF(s), 1);
             mbar_init(BAR_KVE(s), 1);
         }
-        mbar_init(BAR_SF, 1);
-        mbar_init(BAR_PF, 128);
-        mbar_init(BAR_OF, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR_SF(t), 1);
+            mbar_init(BAR_PF(t), 128 + 1);  // the tile's softmax threads and the gate
+            mbar_init(BAR_OF(t), 1);
+        }
+        mbar_init(BAR_DONE, 1);
         fence_barrier_init();
     }
     if (warp == kF8WarpMma) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tbase = *tmem_slot;  // S / P [0, 128), O [128, 256)
+    const uint32_t tbase = *tmem_slot;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 
     if (warp == kF8WarpLoad) {
-        // ================= TMA producer: Q, then K_j, V^T_j alternately =================
+        // ================= TMA producer: Q0, Q1, then K_j, V^T_j alternately =================
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmVt);
-            const uint64_t pol = l2_policy_evict_last();  // re-read by every query tile
-            mbar_arrive_expect_tx(BAR_Q, kF8Tile);
-            tma_load_4d(sQ, &tmQ, BAR_Q, 0, h, qt * 128, b);
+            const uint64_t pol = l2_policy_evict_last();  // re-read by every query block
+            mbar_arrive_expect_tx(BAR_Q, 2 * kF8Tile);  // rows past N read as zero
+            for (int t = 0; t < 2; ++t)
+                tma_load_4d(sQ + t * kF8Tile, &tmQ, BAR_Q, 0, h, (2 * qb + t) * 128, b);
             int last_idx[kF8Slots];
             for (int s = 0; s < kF8Slots; ++s) last_idx[s] = -1;
             bool ok = true;
@@ -267,65 +289,102 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                     mbar_drain(BAR_KVF(s), (last_idx[s] / kF8Slots) & 1, a.watch, 51);
         }
         __syncwarp();
+    } else if (warp == kF8WarpGate) {
+        // ================= gate: V_j and K_{j+1} landed -> p_full(t) =================
+        // one arrival per tile that multiplies block j, made only after that
+        // barrier's previous phase is over, so it can never count in the wrong one
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+                ok = mbar_wait(BAR_KVF(vidx % kF8Slots), (vidx / kF8Slots) & 1, a.watch, 58);
+                if (ok && j + 1 < nkv)
+                    ok = mbar_wait(BAR_KVF(kidx % kF8Slots), (kidx / kF8Slots) & 1, a.watch, 58);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (t == 0 && j >= nkv0) continue;
+                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.watch, 59);
+                    if (ok) mbar_arrive(BAR_PF(t));
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == kF8WarpMma) {
-        // ================= MMA issuer: S(0); then per block PV(j), S(j+1) =================
-        // S and P share TMEM columns 0-127: S(j+1) is issued after PV(j), which
-        // reads P(j), so the tensor core's in-order execution keeps them apart
+        // ================= MMA issuer: PV0(j), S0(j+1), PV1(j), S1(j+1) =================
+        // S_t and P_t share TMEM columns: S_t(j+1) is issued after PV_t(j),
+        // which reads P_t(j), and the tensor core runs one thread's MMAs in order
         if (lane == 0) {
             constexpr uint32_t ID = idesc_e4m3(128, 128);
             constexpr uint32_t HI = sdesc_hi(1024);
             const uint32_t q_lo = sdesc_lo(sQ, 16);
-            const uint32_t tS = tbase, tO = tbase + 128;
-            auto landed = [&](int idx) {
-                const bool r = mbar_wait(BAR_KVF(idx % kF8Slots), (idx / kF8Slots) & 1, a.watch, 52);
-                tc_fence_after();
-                return r;
-            };
-            auto issue_s = [&](int j) {
-                const int slot = (2 * j) % kF8Slots;
-                const uint32_t k_lo = sdesc_lo(sKV + slot * kF8Tile, 16);
+            auto issue_s = [&](int t, int j) {
+                const uint32_t k_lo = sdesc_lo(sKV + ((2 * j) % kF8Slots) * kF8Tile, 16);
+                const uint32_t a_lo = q_lo + ((t * kF8Tile) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)  // 32 e4m3 = 32 bytes of the 128-byte rows
-                    mma_f8_ss(tS, sdesc_at(q_lo, HI, ks * 32), sdesc_at(k_lo, HI, ks * 32), ID,
-                              ks > 0);
-                mma_commit(BAR_SF);
-                mma_commit(BAR_KVE(slot));
+                    mma_f8_ss(tbase + t * 128, sdesc_at(a_lo, HI, ks * 32), sdesc_at(k_lo, HI, ks * 32),
+                              ID, ks > 0);
             };
-            bool ok = mbar_wait(BAR_Q, 0, a.watch, 53) && landed(0);
-            if (ok) issue_s(0);
-            for (int j = 0; j < nkv && ok; ++j) {
-                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 54))) break;
-                tc_fence_after();
-                if (!(ok = landed(2 * j + 1))) break;
-                const int vslot = (2 * j + 1) % kF8Slots;
-                const uint32_t v_lo = sdesc_lo(sKV + vslot * kF8Tile, 16);
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t v_lo = sdesc_lo(sKV + ((2 * j + 1) % kF8Slots) * kF8Tile, 16);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)  // 32 keys = 8 TMEM columns of P
-                    mma_f8_ts(tO, tS + ks * 8, sdesc_at(v_lo, HI, ks * 32), ID,
-                              (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_f8_ts(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
+                              sdesc_at(v_lo, HI, ks * 32), ID, (j > 0 || ks > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(BAR_Q, 0, a.watch, 53);
+            if (ok && (ok = mbar_wait(BAR_KVF(0), 0, a.watch, 53))) {
+                tc_fence_after();
+                issue_s(0, 0);
+                mma_commit(BAR_SF(0));
+                issue_s(1, 0);
+                mma_commit(BAR_SF(1));
+                mma_commit(BAR_KVE(0));
+            }
+            // p_full(t) for block j also means V_j and K_{j+1} have landed
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int vslot = (2 * j + 1) % kF8Slots, kslot = (2 * j + 2) % kF8Slots;
+                if (j < nkv0) {
+                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.watch, 54))) break;
+                    tc_fence_after();
+                    issue_pv(0, j);
+                    if (j == nkv0 - 1) mma_commit(BAR_OF(0));
+                }
+                if (j + 1 < nkv0) {
+                    issue_s(0, j + 1);
+                    mma_commit(BAR_SF(0));
+                }
+                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.watch, 54))) break;
+                tc_fence_after();
+                issue_pv(1, j);
                 mma_commit(BAR_KVE(vslot));
+                if (j == nkv - 1) mma_commit(BAR_OF(1));
                 if (j + 1 < nkv) {
-                    if (!(ok = landed(2 * j + 2))) break;
-                    issue_s(j + 1);
+                    issue_s(1, j + 1);
+                    mma_commit(BAR_SF(1));
+                    mma_commit(BAR_KVE(kslot));
                 }
             }
-            mma_commit(BAR_OF);
-            mbar_drain(BAR_OF, 0, a.watch, 55);
+            mma_commit(BAR_DONE);
+            mbar_drain(BAR_DONE, 0, a.watch, 55);
         }
         __syncwarp();
     } else {
         // ================= softmax: one query row per thread =================
-        const int r = threadIdx.x;
+        const int t = warp >> 2;   // query tile
+        const int wq = warp & 3;   // TMEM lanes 32 wq ..
+        const int r = wq * 32 + lane;
+        const int qt = 2 * qb + t;  // 128-row query block of the tile
         const int grow = qt * 128 + r;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tbase + lane_off, tO = tbase + 128 + lane_off;
-        const float sq = a.sq[(static_cast<size_t>(b) * a.Hq + h) * a.nb + qt];
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tbase + t * 128 + lane_off, tO = tbase + 256 + t * 128 + lane_off;
+        const float sq = qt < a.nb ? a.sq[(static_cast<size_t>(b) * a.Hq + h) * a.nb + qt] : 0.f;
         const float* skrow = a.sk + (static_cast<size_t>(b) * a.Hkv + hk) * a.nb;
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+        const int nkv_mine = t ? nkv : nkv0;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (!(ok = mbar_wait(BAR_SF, j & 1, a.watch, 56))) break;
+        for (int j = 0; j < nkv_mine; ++j) {
+            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.watch, 56))) break;
             tc_fence_after();
             // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
             // and every exponent is one FMA, two columns per packed f32x2 op
@@ -382,8 +441,8 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                 f2_split(add2(ls2[0], ls2[1]), a0, a1);
                 l += a0 + a1;
             }
-            tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S
-            // O was last written by PV(j-1), which finished before S(j)
+            tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S_t
+            // O_t was last written by PV_t(j-1), which finished before S_t(j)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
                 for (int cb = 0; cb < 128; cb += 32) {
@@ -391,18 +450,26 @@ __global__ void __launch_bounds__(kF8Threads, 2)
                     tmem_ld32(tO + cb, o);
                     tmem_wait_ld();
                     reg_fence<32>(o);
+                    const uint64_t ax2 = f2(alpha, alpha);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    for (int i = 0; i < 32; i += 2) {
+                        float u0, u1;
+                        f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2),
+                                 u0, u1);
+                        o[i] = __float_as_uint(u0);
+                        o[i + 1] = __float_as_uint(u1);
+                    }
                     tmem_st32(tO + cb, o);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR_PF);
+            mbar_arrive(BAR_PF(t));
         }
-        // ---- epilogue: O * sv / l -> bf16, plain stores; lse
-        const bool ok_e = ok && mbar_wait(BAR_OF, 0, a.watch, 57);
-        if (ok_e) {
+        // ---- epilogue: O * sv / l -> bf16, plain stores (one 256-byte row per
+        // thread); lse
+        const bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.watch, 57);
+        if (ok_e && grow < a.N) {
             tc_fence_after();
             const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;
             uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * 128;
@@ -416,15 +483,13 @@ __global__ void __launch_bounds__(kF8Threads, 2)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
-                if (grow < a.N)
 #pragma unroll
-                    for (int p4 = 0; p4 < 4; ++p4)
-                        reinterpret_cast<uint4*>(dst + cb)[p4] =
-                            make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
+                for (int p4 = 0; p4 < 4; ++p4)
+                    reinterpret_cast<uint4*>(dst + cb)[p4] =
+                        make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
             }
-            if (grow < a.N)
-                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
-                    (m_ref + log2f(l)) * 0.6931471805599453f;
+            a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                (m_ref + log2f(l)) * 0.6931471805599453f;
         }
     }
 
@@ -432,11 +497,11 @@ __global__ void __launch_bounds__(kF8Threads, 2)
     __syncthreads();
     if (warp == kF8WarpMma) {
         tc_fence_after();
-        tmem_dealloc(tbase, 256);
+        tmem_dealloc(tbase, 512);
     }
 }
 
-constexpr int kF8Smem = 1024 + kF8Tile + kF8Slots * kF8Tile + (2 * kF8Slots + 4) * 8 + 16;
+constexpr int kF8Smem = 1024 + 2 * kF8Tile + kF8Slots * kF8Tile + kF8Bars * 8 + 16;
 
 }  // namespace
 
@@ -461,7 +526,7 @@ cudaError_t launch_fp8(const Fp8Maps& m, const Fp8Args& a, cudaStream_t st) {
     if ((e = cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kF8Smem)) != cudaSuccess)
         return e;
-    const long long nblk = static_cast<long long>(a.nb) * a.B * a.Hq;
+    const long long nblk = static_cast<long long>((a.nb + 1) / 2) * a.B * a.Hq;
     if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     fa_fp8_fwd_kernel<<<static_cast<unsigned>(nblk), kF8Threads, kF8Smem, st>>>(m.q8, m.k8, m.vt8,
                                                                               a);

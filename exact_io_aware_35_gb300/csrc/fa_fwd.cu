@@ -71,9 +71,45 @@ constexpr int kWarpCopy = 11;
 // units), so unnormalised P values stay below 256.
 constexpr float kRescaleThreshold = 8.0f;
 
+// The key blocks the CTA's two query tiles multiply.  Tile t takes the
+// blocks below n[t] (the causal diagonal or the ragged end), and, with a block
+// mask (SPARSE), only those whose mask byte is set.  Every role walks the
+// union of the two tiles' blocks in increasing order, the i-th union block
+// occupying ring entries 2i (K) and 2i + 1 (V); without a mask the union is
+// 0 .. n[1] - 1 and tile 0 just stops one block early on the diagonal.
+template <bool SPARSE>
+struct TileBlocks {
+    int n[2];
+    const uint8_t* row[2];  // SPARSE: the tiles' mask rows (null: the tile has no block)
+    __device__ __forceinline__ bool has(int t, int u) const {
+        if (u >= n[t]) return false;
+        return SPARSE ? (row[t] != nullptr && row[t][u] != 0) : true;
+    }
+    __device__ __forceinline__ int next(int u) const {  // next union block after u, or -1
+        if constexpr (!SPARSE) {
+            return u + 1 < n[1] ? u + 1 : -1;
+        } else {
+            const int hi = max(n[0], n[1]);
+            for (++u; u < hi; ++u)
+                if (has(0, u) || has(1, u)) return u;
+            return -1;
+        }
+    }
+    __device__ __forceinline__ int next_of(int t, int u) const {  // tile t's next block, or -1
+        if constexpr (!SPARSE) {
+            return u + 1 < n[t] ? u + 1 : -1;
+        } else {
+            for (++u; u < n[t]; ++u)
+                if (has(t, u)) return u;
+            return -1;
+        }
+    }
+};
+
 // F16: P is rounded to fp16 (not bf16) and multiplies the fp16 copy of V,
 // scaled by 2^v (the training forward, whose O feeds the backward's D).
-template <int D, bool F16>
+// SPARSE: the tiles multiply only the key blocks a.block_mask selects.
+template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -108,9 +144,17 @@ __global__ void __launch_bounds__(384, 1)
     const int hk = h / a.g;
     const int row0 = qb * 2 * kBM;
     const int nkv_all = (a.N + kBN - 1) / kBN;
-    // key blocks each query tile needs (causal: up to and including its diagonal)
-    const int nkv0 = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
-    const int nkv = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
+    // key blocks below each query tile's limit (causal: up to and including its
+    // diagonal), and with a mask only those it selects
+    TileBlocks<SPARSE> blk;
+    blk.n[0] = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
+    blk.n[1] = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
+    blk.row[0] = blk.row[1] = nullptr;
+    if (SPARSE)
+        for (int t = 0; t < 2; ++t)
+            if (2 * qb + t < nkv_all)
+                blk.row[t] = a.block_mask + (static_cast<size_t>(h) * nkv_all + 2 * qb + t) * nkv_all;
+    const int u_first = SPARSE ? blk.next(-1) : 0;  // first union block (-1: none)
 
     // ---- set-up
     if (warp == 0 && lane == 0) {
@@ -154,9 +198,9 @@ __global__ void __launch_bounds__(384, 1)
             int last_idx[C::NSLOT];
             for (int s = 0; s < C::NSLOT; ++s) last_idx[s] = -1;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
+            for (int i = 0, u = u_first; u >= 0 && ok; ++i, u = blk.next(u)) {
                 for (int w = 0; w < 2; ++w) {
-                    const int idx = 2 * j + w;
+                    const int idx = 2 * i + w;
                     const int slot = idx % C::NSLOT;
                     const uint32_t ph = (idx / C::NSLOT) & 1;
                     if (!mbar_wait(BAR_KVE(slot), ph ^ 1u, a.watch, 1)) {
@@ -167,7 +211,7 @@ __global__ void __launch_bounds__(384, 1)
                     const CUtensorMap* tm = w ? &tmV : &tmK;
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d_hint(sKV + slot * C::TILE + c * C::CHUNK, tm, BAR_KVF(slot),
-                                         c * 64, hk, j * kBN, b, pol_kv);
+                                         c * 64, hk, u * kBN, b, pol_kv);
                     last_idx[slot] = idx;
                 }
             }
@@ -187,16 +231,20 @@ __global__ void __launch_bounds__(384, 1)
         // never be counted in the wrong phase.
         if (lane == 0) {
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+            int cnt[2] = {0, 0};  // blocks each tile has multiplied so far
+            for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
+                const int un = blk.next(u);
+                const int vidx = 2 * i + 1, kidx = 2 * i + 2;
                 ok = mbar_wait(BAR_KVF(vidx % C::NSLOT), (vidx / C::NSLOT) & 1, a.watch, 5);
-                if (ok && j + 1 < nkv)
+                if (ok && un >= 0)
                     ok = mbar_wait(BAR_KVF(kidx % C::NSLOT), (kidx / C::NSLOT) & 1, a.watch, 5);
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (t == 0 && j >= nkv0) continue;
-                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.watch, 7);
+                    if (!blk.has(t, u)) continue;
+                    if (cnt[t] > 0) ok = mbar_wait(BAR_PF(t), (cnt[t] - 1) & 1, a.watch, 7);
                     if (ok) mbar_arrive(BAR_PF(t));
+                    ++cnt[t];
                 }
+                u = un;
             }
         }
         __syncwarp();
@@ -246,43 +294,61 @@ __global__ void __launch_bounds__(384, 1)
                                 (acc || ks > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(BAR_Q(), 0, a.watch, 3);
-            if (ok) {
-                // first key block: both score tiles
+            if (ok && u_first >= 0) {
+                // first union block: the score tiles of the tiles that have it
                 ok = mbar_wait(BAR_KVF(0), 0, a.watch, 4);
                 if (ok) {
                     tc_fence_after();
-                    issue_qk(0, 0);
-                    mma_commit(BAR_SF(0));
-                    issue_qk(1, 0);
-                    mma_commit(BAR_SF(1));
+                    for (int t = 0; t < 2; ++t)
+                        if (blk.has(t, u_first)) {
+                            issue_qk(t, 0);
+                            mma_commit(BAR_SF(t));
+                        }
                     mma_commit(BAR_KVE(0));
                 }
             }
-            // p_full(t) for key block j also means V_j and K_{j+1} have landed
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vslot = (2 * j + 1) % C::NSLOT;
-                if (j < nkv0) {
-                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.watch, 6))) break;
+            // Per union block u (ring entries 2i, 2i + 1), with un the next one:
+            // PV0(u), S0(un), PV1(u), S1(un) for the tiles that have them.  p_full(t)
+            // for u also means V(u) and K(un) have landed (the gate), and at
+            // least one tile has u, so no S(un) is issued before one such wait;
+            // S_t(un) follows PV_t of the tile's last block, which read P_t.
+            int cnt[2] = {0, 0};
+            for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
+                const int un = blk.next(u);
+                const int vslot = (2 * i + 1) % C::NSLOT;
+                const int kslot = (2 * i + 2) % C::NSLOT;
+                const bool h0 = blk.has(0, u), h0n = un >= 0 && blk.has(0, un);
+                if (h0) {
+                    if (!(ok = mbar_wait(BAR_PF(0), cnt[0] & 1, a.watch, 6))) break;
                     tc_fence_after();
-                    issue_pv(0, vslot, j > 0);
-                    if (j == nkv0 - 1) mma_commit(BAR_OF(0));
+                    issue_pv(0, vslot, cnt[0] > 0);
+                    ++cnt[0];
+                    if (blk.next_of(0, u) < 0) mma_commit(BAR_OF(0));
+                    if (h0n) {
+                        issue_qk(0, kslot);
+                        mma_commit(BAR_SF(0));
+                    }
                 }
-                const int kidx = 2 * (j + 1);
-                const int kslot = kidx % C::NSLOT;
-                if (j + 1 < nkv0) {
-                    issue_qk(0, kslot);
-                    mma_commit(BAR_SF(0));
+                if (blk.has(1, u)) {
+                    if (!(ok = mbar_wait(BAR_PF(1), cnt[1] & 1, a.watch, 8))) break;
+                    tc_fence_after();
+                    issue_pv(1, vslot, cnt[1] > 0);
+                    ++cnt[1];
                 }
-                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.watch, 8))) break;
-                tc_fence_after();
-                issue_pv(1, vslot, j > 0);
                 mma_commit(BAR_KVE(vslot));
-                if (j == nkv - 1) mma_commit(BAR_OF(1));
-                if (j + 1 < nkv) {
-                    issue_qk(1, kslot);
-                    mma_commit(BAR_SF(1));
+                if (blk.has(1, u) && blk.next_of(1, u) < 0) mma_commit(BAR_OF(1));
+                if (un >= 0) {
+                    if (blk.has(1, un)) {
+                        issue_qk(1, kslot);
+                        mma_commit(BAR_SF(1));
+                    }
+                    if (!h0 && h0n) {
+                        issue_qk(0, kslot);
+                        mma_commit(BAR_SF(0));
+                    }
                     mma_commit(BAR_KVE(kslot));
                 }
+                u = un;
             }
             // all issued MMAs have finished before TMEM can be released
             mma_commit(BAR_DONE);
@@ -306,8 +372,9 @@ __global__ void __launch_bounds__(384, 1)
         float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
         float l = 0.f;            // running sum, relative to m_ref
         bool ok = true;
-        const int nkv_mine = t ? nkv : nkv0;
-        for (int j = 0; j < nkv_mine; ++j) {
+        const int u0 = blk.has(t, 0) ? 0 : blk.next_of(t, 0);  // the tile's first block
+        int j = 0;                                               // blocks done so far
+        for (int u = u0; u >= 0; u = blk.next_of(t, u), ++j) {
             if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
             tc_fence_after();
             uint32_t s[kBN];
@@ -320,7 +387,7 @@ __global__ void __launch_bounds__(384, 1)
             float x[kBN];
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
-            const int kbase = j * kBN;
+            const int kbase = u * kBN;
             if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
@@ -390,7 +457,12 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive(BAR_PF(t));
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging in Q_t's buffer -> TMA store
-        bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.watch, 12 + t);
+        // (a tile with no key block -- block-sparse only -- writes O = 0 and
+        // lse = -inf: no MMA ever wrote its O, and only the Q load, which must
+        // land before the buffer is reused, touched its staging buffer)
+        const bool any = u0 >= 0;
+        bool ok_e = ok && (any ? mbar_wait(BAR_OF(t), 0, a.watch, 12 + t)
+                               : mbar_wait(BAR_Q(), 0, a.watch, 16));
         if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
             ok_e = ok_e && mbar_wait(BAR_QC, 0, a.watch, 14);
         const uint32_t stage = sQ + t * C::TILE;
@@ -404,6 +476,9 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld32(tO + cb, o);
                 tmem_wait_ld();
                 reg_fence<32>(o);
+                if (SPARSE && !any)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
                 uint32_t w[16], wl[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -453,10 +528,10 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool SPARSE>
 cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, F16>;
+    auto kern = fa_fwd_kernel<D, F16, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -470,10 +545,16 @@ cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdArgs& args, int d, cudaStream_t stream) {
     const bool f16 = args.f16s != nullptr;
-    if (d == 64) return f16 ? launch_fwd_d<64, true>(maps, args, stream)
-                            : launch_fwd_d<64, false>(maps, args, stream);
-    if (d == 128) return f16 ? launch_fwd_d<128, true>(maps, args, stream)
-                             : launch_fwd_d<128, false>(maps, args, stream);
+    if (args.block_mask != nullptr) {  // block-sparse: the inference forward's arithmetic
+        if (f16) return cudaErrorInvalidValue;
+        if (d == 64) return launch_fwd_d<64, false, true>(maps, args, stream);
+        if (d == 128) return launch_fwd_d<128, false, true>(maps, args, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (d == 64) return f16 ? launch_fwd_d<64, true, false>(maps, args, stream)
+                            : launch_fwd_d<64, false, false>(maps, args, stream);
+    if (d == 128) return f16 ? launch_fwd_d<128, true, false>(maps, args, stream)
+                             : launch_fwd_d<128, false, false>(maps, args, stream);
     return cudaErrorInvalidValue;
 }
 

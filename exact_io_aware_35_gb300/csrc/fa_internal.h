@@ -89,6 +89,9 @@ struct FwdArgs {
     int causal;
     float scale_log2;    // scale * log2(e)
     int n_qblk;          // ceil(N / 256): CTA query blocks (two 128-row tiles each)
+    // block-sparse: [Hq, nb, nb] bytes (nb = ceil(N / 128)), nonzero = the
+    // 128 x 128 block is computed; null: every block (up to the causal limit)
+    const uint8_t* block_mask;
     Watch watch;         // status words, time limit and id of the launch
 };
 

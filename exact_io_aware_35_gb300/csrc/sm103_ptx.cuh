@@ -554,10 +554,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
-__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t a) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),

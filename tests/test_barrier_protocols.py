@@ -222,8 +222,9 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
     lanes 32q.. (query rows); each arrives on its own.  The MMA thread
     arrives on PFS once it has seen dS(j) complete; a warp waits for that
     before its dS(j+1) arrival, so PF is never a phase ahead of its waiter.
-    two_issuers: S and dP are issued by one thread, dQ by another (its own
-    tensor-core queue); dQ(j) reads dS(j) in dP buffer j % 2, which dP(j+2)
+    two_issuers (a variant that was tried and measured slower, not the
+    kernel's protocol): S and dP are issued by one thread, dQ by another (its
+    own tensor-core queue); dQ(j) reads dS(j) in dP buffer j % 2, which dP(j+2)
     overwrites, so the dQ thread commits DQD(j % 2) after dQ(j) and the S/dP
     thread waits for it (phase j // 2) before dP(j+2); the dQ thread, which
     waits for PF, is the one that arrives on PFS.  single_dqd (one DQD
@@ -361,12 +362,16 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
 
 
 # -------------------------------------------------------------- dK/dV kernel
-def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
+def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, skip_dvd=False):
     """Sixteen compute warps (g, q): query columns 32g.. of the transposed
-    tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  P^T goes over the
-    S^T columns a warp read; dS^T goes to shared memory, over the stage's dO
-    tile (ds_in_do, d = 128) or into a buffer of its own (d = 64), once the
-    MMA thread's DVD commit after dV(it) has completed."""
+    tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  The kernel's
+    protocol (ds_smem False): P^T and dS^T go over the S^T columns a warp
+    read (halves 'p' and 'd'), dV after P^T, dK after dS^T, then dP^T(it+1)
+    over both.  A variant that was tried and measured slower (ds_smem True):
+    dS^T goes to shared memory instead -- over the stage's dO tile (ds_in_do,
+    d = 128) or into a buffer of its own (d = 64) -- once the MMA thread's
+    DVD commit after dV(it) has completed, so dP^T(it+1) follows dV(it) and
+    dK(it) reads dS^T from shared memory after it."""
     warps = [(g, q) for g in range(4) for q in range(4)]
 
     def model(rnd):
@@ -375,16 +380,18 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
             bars[f"STF{s}"] = 1 + 32  # the load, and the 32 lanes' vector writes
             bars[f"STE{s}"] = 1
 
-        def reg_s(it):  # S^T(it), then P^T(it)
+        def reg_s(it):  # S^T(it), then P^T(it) (/ dS^T(it))
             return "Y" if it & 1 else "X"
 
         def reg_d(it):  # dP^T(it)
             return "X" if it & 1 else "Y"
 
         def region(r, tag):
-            return {f"{r}.{g}.{q}": tag for g, q in warps}
+            return {f"{r}.{g}.{q}.{c}": tag for g, q in warps for c in "pd"}
 
-        def ds_buf(it, g, q):  # the shared-memory rows of dS^T(it) warp (g, q) writes
+        def ds_buf(it, g, q):  # where warp (g, q) writes dS^T(it)
+            if not ds_smem:
+                return f"{reg_s(it)}.{g}.{q}.d"
             return f"dO{it % NST}.{g}.{q}" if ds_in_do else f"DS.{g}.{q}"
 
         def stage_load(it):
@@ -416,7 +423,7 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
             return ("mma", f"dP^T({it})", reads, region(reg_d(it), f"dP^T({it})"))
 
         def dv_mma(it):
-            reads = {f"{reg_s(it)}.{g}.{q}": f"P^T({it})" for g, q in warps}
+            reads = {f"{reg_s(it)}.{g}.{q}.p": f"P^T({it})" for g, q in warps}
             reads.update({f"dO{it % NST}.{g}.{q}": f"dO({it})" for g, q in warps})
             if it > 0:
                 reads["dV"] = f"dV({it - 1})"
@@ -444,14 +451,18 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
                     yield st_mma(it + 1)  # over dP^T(it)
                 yield ("wait", "PF", it)
                 yield dv_mma(it)
-                yield ("commit", "DVD", it)
-                if more:
-                    yield dpt_mma(it + 1)  # over P^T(it)
-                    yield ("commit", "SDF", it + 1)
+                if ds_smem:
+                    yield ("commit", "DVD", it)
+                    if more:
+                        yield dpt_mma(it + 1)  # over P^T(it)
+                        yield ("commit", "SDF", it + 1)
                 if not dk_before_dsf:
                     yield ("wait", "DSF", it)
                 yield dk_mma(it)
                 yield ("commit", f"STE{s}", it // NST)
+                if more and not ds_smem:
+                    yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
+                    yield ("commit", "SDF", it + 1)
             yield ("commit", "ACC", 0)
             yield ("wait", "ACC", 0)
 
@@ -461,12 +472,13 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_in_do=True, skip_dvd=False):
                 s = it % NST
                 rs, rd = reg_s(it), reg_d(it)
                 yield ("wait", "SDF", it)
-                yield ("read", {f"{rd}.{me}": f"dP^T({it})", f"vec{s}": f"lse,D({it})"})
+                yield ("read", {f"{rd}.{me}.p": f"dP^T({it})", f"{rd}.{me}.d": f"dP^T({it})",
+                                f"vec{s}": f"lse,D({it})"})
                 yield ("arrive", "LD", 32, it)
-                yield ("read", {f"{rs}.{me}": f"S^T({it})"})
-                yield ("write", {f"{rs}.{me}": f"P^T({it})"})
+                yield ("read", {f"{rs}.{me}.p": f"S^T({it})", f"{rs}.{me}.d": f"S^T({it})"})
+                yield ("write", {f"{rs}.{me}.p": f"P^T({it})"})
                 yield ("arrive", "PF", 32, it)
-                if not skip_dvd:
+                if ds_smem and not skip_dvd:
                     yield ("wait", "DVD", it)
                 yield ("write", {ds_buf(it, g, q): f"dS^T({it})"})
                 yield ("arrive", "DSF", 32, it)
@@ -589,6 +601,162 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
     return model
 
 
+def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
+    """The forward kernel's protocol with its key blocks given per tile
+    (block-sparse masks; the dense kernel is blocks0 = range(nkv0), blocks1 =
+    range(nkv)).  Every role walks the union of the two sets in increasing
+    order, the i-th union block in ring entries 2i (K) and 2i + 1 (V).  Per
+    union block u with next union block un: PV0(u) and S0(un) if tile 0 has
+    them, PV1(u), V(u)'s slot released, S1(un), then S0(un) when tile 0 had
+    no u (deferred behind tile 1's p_full wait, which is the one that says
+    K(un) has landed), K(un)'s slot released.  defer_qk0=False issues that
+    S0(un) before tile 1's wait: a planted mistake."""
+    rows = range(4)
+    sets = (sorted(set(blocks0)), sorted(set(blocks1)))
+    union = sorted(set(sets[0]) | set(sets[1]))
+
+    def has(t, u):
+        return u in sets[t]
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
+        bars.update(ring_bars(NSLOT))
+
+        def tile(pre, t, tag):
+            return {f"{pre}.{t}.{q}": tag for q in rows}
+
+        def producer():
+            last = {}
+            yield ("load", "Q", 0, dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            for i, u in enumerate(union):
+                for w, nm in enumerate(("K", "V")):
+                    idx = 2 * i + w
+                    s = idx % NSLOT
+                    yield ("wait", f"E{s}", idx // NSLOT - 1)
+                    yield ("load", f"F{s}", idx // NSLOT, {f"kv{s}": f"{nm}({u})"})
+                    last[s] = idx // NSLOT
+            yield ("wait", "Q", 0)
+            for s, ph in last.items():
+                yield ("wait", f"F{s}", ph)
+
+        def gate():
+            cnt = [0, 0]
+            for i, u in enumerate(union):
+                v, kn = 2 * i + 1, 2 * i + 2
+                yield ("wait", f"F{v % NSLOT}", v // NSLOT)
+                if i + 1 < len(union):
+                    yield ("wait", f"F{kn % NSLOT}", kn // NSLOT)
+                for t in (0, 1):
+                    if not has(t, u):
+                        continue
+                    if cnt[t] > 0:
+                        yield ("wait", f"PF{t}", cnt[t] - 1)
+                    yield ("arrive", f"PF{t}", 1, cnt[t])
+                    cnt[t] += 1
+
+        def copy():
+            yield ("wait", "Q", 0)
+            yield ("read", dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            yield ("arrive", "QC", 1, 0)
+
+        def qk(t, i, u):
+            slot = (2 * i) % NSLOT
+            return ("mma", f"QK({t},{u})", dict(tile("Q", t, "Q"), **{f"kv{slot}": f"K({u})"}),
+                    tile("S", t, f"S({t},{u})"))
+
+        def pv(t, i, u, prev):
+            slot = (2 * i + 1) % NSLOT
+            reads = dict(tile("S", t, f"P({t},{u})"), **{f"kv{slot}": f"V({u})"})
+            if prev is not None:
+                reads.update(tile("O", t, f"O({t},{prev})"))
+            return ("mma", f"PV({t},{u})", reads, tile("O", t, f"O({t},{u})"))
+
+        def mma():
+            if not union:
+                yield ("commit", "DONE", 0)
+                yield ("wait", "DONE", 0)
+                return
+            yield ("wait", "Q", 0)
+            yield ("wait", "F0", 0)
+            sf = [0, 0]
+            for t in (0, 1):
+                if has(t, union[0]):
+                    yield qk(t, 0, union[0])
+                    yield ("commit", f"SF{t}", sf[t])
+                    sf[t] += 1
+            yield ("commit", "E0", 0)
+            cnt, prev = [0, 0], [None, None]
+            for i, u in enumerate(union):
+                un = union[i + 1] if i + 1 < len(union) else None
+                vslot, kslot = (2 * i + 1) % NSLOT, (2 * i + 2) % NSLOT
+                h0, h0n = has(0, u), un is not None and has(0, un)
+                if not defer_qk0 and not h0 and h0n:
+                    yield qk(0, i + 1, un)
+                    yield ("commit", "SF0", sf[0])
+                    sf[0] += 1
+                if h0:
+                    yield ("wait", "PF0", cnt[0])
+                    yield pv(0, i, u, prev[0])
+                    cnt[0], prev[0] = cnt[0] + 1, u
+                    if u == sets[0][-1]:
+                        yield ("commit", "OF0", 0)
+                    if h0n:
+                        yield qk(0, i + 1, un)
+                        yield ("commit", "SF0", sf[0])
+                        sf[0] += 1
+                if has(1, u):
+                    yield ("wait", "PF1", cnt[1])
+                    yield pv(1, i, u, prev[1])
+                    cnt[1], prev[1] = cnt[1] + 1, u
+                yield ("commit", f"E{vslot}", (2 * i + 1) // NSLOT)
+                if has(1, u) and u == sets[1][-1]:
+                    yield ("commit", "OF1", 0)
+                if un is not None:
+                    if has(1, un):
+                        yield qk(1, i + 1, un)
+                        yield ("commit", "SF1", sf[1])
+                        sf[1] += 1
+                    if defer_qk0 and not h0 and h0n:
+                        yield qk(0, i + 1, un)
+                        yield ("commit", "SF0", sf[0])
+                        sf[0] += 1
+                    yield ("commit", f"E{kslot}", (2 * i + 2) // NSLOT)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def softmax(t, q):
+            me = f"{t}.{q}"
+            prev = None
+            for j, u in enumerate(sets[t]):
+                yield ("wait", f"SF{t}", j)
+                yield ("read", {f"S.{me}": f"S({t},{u})"})
+                yield ("write", {f"S.{me}": f"P({t},{u})"})
+                if prev is not None and rnd.random() < 0.5:  # the reference max moved
+                    yield ("read", {f"O.{me}": f"O({t},{prev})"})
+                    yield ("write", {f"O.{me}": f"O({t},{prev})"})
+                yield ("arrive", f"PF{t}", 32, j)
+                prev = u
+            if sets[t]:
+                yield ("wait", f"OF{t}", 0)
+                yield ("read", {f"O.{me}": f"O({t},{prev})"})
+            else:  # a tile with no block stages zeros, once its Q tile has landed
+                yield ("wait", "Q", 0)
+            if copy_q:
+                yield ("wait", "QC", 0)
+            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
+
+        roles = {"prod": producer(), "gate": gate(), "mma": mma()}
+        for t in (0, 1):
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
+        if copy_q:
+            roles["copy"] = copy()
+        return bars, roles
+
+    return model
+
+
 # ----------------------------------------------- split-KV (decode) kernel
 def decode_model(nkv, NSLOT=6, skip_pvd_wait=False):
     """Four softmax warps, warp q owning rows 32q.. of S0, S1 and O."""
@@ -655,9 +823,13 @@ def decode_model(nkv, NSLOT=6, skip_pvd_wait=False):
     return model
 
 
-# ------------------------------------- single S buffer (the FP8 forward) -----
+# ---------------------- single S buffer (one-tile forward; no kernel uses it now)
+# The FP8 forward now has the bf16 forward's two-tile protocol (fwd_model with
+# no copy warp, which test_forward_protocol runs).  This model of the earlier
+# one-tile protocol stays as the ring-without-empty-wait planted-mistake case.
 def single_s_model(nkv, NSLOT=4, skip_empty=False):
-    """Four softmax warps over one S buffer (P written over S)."""
+    """Four softmax warps over one S buffer (P written over S), a ring of
+    NSLOT K / V^T tiles."""
     rows = range(4)
 
     def model(rnd):
@@ -724,9 +896,14 @@ def test_dq_protocol(nj, two_issuers):
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
+def test_dkdv_protocol(n_it):
+    each_seed(dkdv_model(n_it))
+
+
+@pytest.mark.parametrize("n_it", [1, 3, 16])
 @pytest.mark.parametrize("ds_in_do", [True, False])
-def test_dkdv_protocol(n_it, ds_in_do):
-    each_seed(dkdv_model(n_it, ds_in_do=ds_in_do))
+def test_dkdv_smem_ds_variant_protocol(n_it, ds_in_do):
+    each_seed(dkdv_model(n_it, ds_smem=True, ds_in_do=ds_in_do))
 
 
 @pytest.mark.parametrize("nkv0,nkv,nslot", [(1, 1, 4), (1, 2, 4), (2, 3, 4), (5, 6, 4), (8, 8, 4),
@@ -734,6 +911,40 @@ def test_dkdv_protocol(n_it, ds_in_do):
 @pytest.mark.parametrize("copy_q", [True, False])
 def test_forward_protocol(nkv0, nkv, nslot, copy_q):
     each_seed(fwd_model(nkv0, nkv, nslot, copy_q))
+
+
+UNION_CASES = [  # (tile 0's key blocks, tile 1's key blocks, ring slots)
+    (range(3), range(4), 4),                   # the dense causal diagonal
+    (range(6), range(6), 8),                   # dense, non-causal
+    ([0, 9], range(10), 4),                    # tile 0's blocks far apart in the union
+    (range(10), [0, 9], 4),
+    ([2, 5], [0, 1, 7], 4),                    # disjoint sets
+    ([], [0, 3, 4], 4),                        # a tile with no block
+    ([1, 2], [], 4),
+    ([], [], 4),
+    ([0, 2, 4, 6], [1, 3, 5, 7], 4),           # alternating
+]
+
+
+@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES)
+@pytest.mark.parametrize("copy_q", [False, True])
+def test_forward_union_protocol(b0, b1, nslot, copy_q):
+    each_seed(fwd_union_model(b0, b1, nslot, copy_q))
+
+
+def test_forward_union_random_masks():
+    rnd = random.Random(5)
+    for _ in range(40):
+        nb = rnd.randrange(1, 12)
+        b0 = [u for u in range(nb) if rnd.random() < 0.4]
+        b1 = [u for u in range(nb) if rnd.random() < 0.4]
+        each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8))), seeds=range(8))
+
+
+def test_forward_union_early_score_of_the_idle_tile_is_caught():
+    # S0(un) issued before tile 1's p_full wait, although tile 0 had no u:
+    # nothing yet says K(un) has landed
+    assert fails_on_some_seed(fwd_union_model([4], [0, 1, 2, 3, 4], 4, defer_qk0=False))
 
 
 @pytest.mark.parametrize("nkv,nslot", [(0, 6), (1, 6), (2, 6), (3, 6), (7, 6), (20, 6), (13, 12)])
@@ -788,7 +999,7 @@ def test_dkdv_dk_before_ds_is_caught():
 def test_dkdv_ds_write_without_dv_done_is_caught(ds_in_do):
     # dS^T written over the dO tile before dV(it) has read it (d = 128), or
     # into its own buffer before dK(it-1) has read the previous one (d = 64)
-    assert fails_on_some_seed(dkdv_model(5, ds_in_do=ds_in_do, skip_dvd=True))
+    assert fails_on_some_seed(dkdv_model(5, ds_smem=True, ds_in_do=ds_in_do, skip_dvd=True))
 
 
 def test_ring_without_empty_wait_is_caught():

@@ -112,6 +112,30 @@ def test_empty_mask_rows(fa):
     assert (o[0, 256:, 1] == 0).all() and (o[0, :128, 0] == 0).all()
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_staggered_masks_of_one_thread_block(fa, causal):
+    # a thread block holds two query tiles (query blocks 2i and 2i+1) and
+    # streams the union of their key blocks: here the even query blocks see
+    # only their first and last visible key blocks while the odd ones see all,
+    # so one tile's blocks lie far apart in the union (longer than the K/V
+    # ring), and some tiles see nothing at all
+    N, Hq = 1400, 2
+    nb = (N + 127) // 128
+    q, k, v = inputs(1, N, Hq, 1, 128, seed=25)
+    mask = torch.ones(Hq, nb, nb, dtype=torch.uint8)
+    for i in range(0, nb, 2):
+        last = i if causal else nb - 1
+        mask[:, i, :] = 0
+        mask[:, i, 0] = 1
+        mask[:, i, last] = 1
+    mask[1, 4, :] = 0  # an empty tile beside a full one (query blocks 4, 5)
+    mask[1, 7, :] = 0  # and the other way round (query blocks 6, 7)
+    o, lse = run(fa, q, k, v, mask, causal, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.attn_fwd_blockmask(q, k, v, mask.numpy(), 128, causal,
+                                               1 / math.sqrt(128))
+    check(o, lse, o_ref, lse_ref)
+
+
 def test_blocksparse_bench_shape_sampled(fa):
     # the block-sparse bench shape: gqa8k's head layout (Hq32 Hkv8, N 8192,
     # d 128, causal) with a local-window-plus-random mask; oracle on one head
