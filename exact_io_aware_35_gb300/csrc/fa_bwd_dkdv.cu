@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     tma_prefetch_4d(&tmDO, c * 64, hq2, q2, b, pol_q);
                 }
             }
-            if (!mbar_wait(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.watch, 30)) break;
+            if (!mbar_wait_warp(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.watch, 30)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
                 const uint32_t dst = sStage + 2 * s * C::TILE;
@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         }
         __syncwarp();
     } else if (warp == kDkWarpMma) {
-        if (lane == 0) {
+        {
+            const uint32_t leader = elect_one();
             constexpr uint32_t IDESC_S = idesc_16(kBN, kBM, false, false, F16);  // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_16(kBN, D, false, true, F16);  // dV, dK
             const uint32_t tDV = tbase + C::TM_ACC, tDK = tbase + C::TM_ACC + D;
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_S, ks > 0);
+                    mma_bf16_ss_w(leader, dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_S, ks > 0);
                 }
             };
             // dV += P^T dO (dk = false) or dK += dS^T Q (dk = true): for queries
@@ -224,16 +225,16 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const uint32_t rs = reg_s(it) + (dk ? 16 : 0);
 #pragma unroll
                 for (int ks = 0; ks < kBM / 16; ++ks)
-                    mma_bf16_ts(dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
+                    mma_bf16_ts_w(leader, dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
                                 sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
             };
-            bool ok = mbar_wait(BAR_KV, 0, a.watch, 32) &&
-                      mbar_wait(BAR_STF(0), 0, a.watch, 33);
+            bool ok = mbar_wait_warp(BAR_KV, 0, a.watch, 32) &&
+                      mbar_wait_warp(BAR_STF(0), 0, a.watch, 33);
             if (ok) {
                 tc_fence_after();
                 issue_t(reg_s(0), k_lo, stage_q(0));
                 issue_t(reg_d(0), v_lo, stage_q(0) + C::TILE);
-                mma_commit(BAR_SDF);
+                mma_commit_w(leader, BAR_SDF);
             }
             for (int it = 0; it < n_it && ok; ++it) {
                 const int s = it % C::NST;
@@ -241,28 +242,28 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const bool more = it + 1 < n_it;
                 if (more) {
                     // S^T(it+1) over dP^T(it), once both warpgroups hold it in registers
-                    if (!(ok = mbar_wait(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.watch, 33)))
+                    if (!(ok = mbar_wait_warp(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.watch, 33)))
                         break;
-                    if (!(ok = mbar_wait(BAR_LD, it & 1, a.watch, 34))) break;
+                    if (!(ok = mbar_wait_warp(BAR_LD, it & 1, a.watch, 34))) break;
                     tc_fence_after();
                     issue_t(reg_d(it), k_lo, stage_q(s2));
                 }
                 // dV as soon as P^T is written, dK once dS^T is
-                if (!(ok = mbar_wait(BAR_PF, it & 1, a.watch, 34))) break;
+                if (!(ok = mbar_wait_warp(BAR_PF, it & 1, a.watch, 34))) break;
                 tc_fence_after();
                 issue_acc(it, s, false);
-                if (!(ok = mbar_wait(BAR_DSF, it & 1, a.watch, 38))) break;
+                if (!(ok = mbar_wait_warp(BAR_DSF, it & 1, a.watch, 38))) break;
                 tc_fence_after();
                 issue_acc(it, s, true);
-                mma_commit(BAR_STE(s));
+                mma_commit_w(leader, BAR_STE(s));
                 if (more) {
                     // dP^T(it+1) over P^T(it), dS^T(it): the products above read them first
                     issue_t(reg_s(it), v_lo, stage_q(s2) + C::TILE);
-                    mma_commit(BAR_SDF);
+                    mma_commit_w(leader, BAR_SDF);
                 }
             }
             // every issued MMA has finished before TMEM is released
-            mma_commit(BAR_ACC);
+            mma_commit_w(leader, BAR_ACC);
             mbar_drain(BAR_ACC, 0, a.watch, 35);
         }
         __syncwarp();
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::NST;
             const int qi = qi0 + it % nqi;
-            if (!(ok = mbar_wait(BAR_SDF, it & 1, a.watch, 36))) break;
+            if (!(ok = mbar_wait_warp(BAR_SDF, it & 1, a.watch, 36))) break;
             tc_fence_after();
             const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + wg * 32 + lane_off;
             const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + wg * 32 + lane_off;
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR_DSF);
         }
-        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.watch, 37);
+        const bool ok_e = ok && mbar_wait_warp(BAR_ACC, 0, a.watch, 37);
         // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those
         // of dK = scale * (dS^T Q); staging reuses stage 0's Q (dV) and dO (dK)
         // buffers, idle once all MMAs are done

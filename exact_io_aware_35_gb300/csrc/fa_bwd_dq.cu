@@ -201,24 +201,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mul = pow2f(sc.dout);
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
             uint16_t* dst = a.dout16 + (static_cast<size_t>(b) * a.N + qi * kBM) * row_el + h * D;
-            if (mbar_wait(BAR_QDO, 0, a.watch, 29))
+            if (mbar_wait_warp(BAR_QDO, 0, a.watch, 29))
                 warp_tile_to_f16<D>(sDO, dst, row_el, a.N - qi * kBM, mul, lane);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
+        // ================= MMA issuer (the whole warp; the leader lane issues) =================
+        {
+            const uint32_t leader = elect_one();
             constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
             constexpr uint32_t IDESC_DP = idesc_bf16(kBM, kBN, false, false);    // dP = dO V^T
             constexpr uint32_t IDESC_DQ = idesc_16(kBM, D, false, true, F16);    // dQ += dS K
             const uint32_t tS = tbase + C::TM_S, tDQ = tbase + C::TM_DQ;
             auto tDP = [&](int jj) { return tbase + C::TM_DP + (jj & 1) * 128; };
             auto k_ready = [&](int jj) {
-                const bool r = mbar_wait(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.watch, 23);
+                const bool r = mbar_wait_warp(BAR_KF(jj % C::KS), (jj / C::KS) & 1, a.watch, 23);
                 tc_fence_after();
                 return r;
             };
             auto v_ready = [&](int jj) {  // (prologue only; the gate covers the loop)
-                const bool r = mbar_wait(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.watch, 23);
+                const bool r = mbar_wait_warp(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.watch, 23);
                 tc_fence_after();
                 return r;
             };
@@ -232,13 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), idesc, ks > 0);
+                    mma_bf16_ss_w(leader, dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), idesc, ks > 0);
                 }
             };
             // dP(jj) = dO V_jj^T; V_jj's slot is free once it has run
             auto issue_dp = [&](int jj) {
                 issue_t(tDP(jj), do_lo, sV + (jj % C::VS) * C::TILE, IDESC_DP);
-                mma_commit(BAR_VE(jj % C::VS));
+                mma_commit_w(leader, BAR_VE(jj % C::VS));
             };
             // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
             // of dP buffer jj & 1; K rows 16ks.. read MN-major
@@ -246,15 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_lo = sdesc_lo(sK + (jj % C::KS) * C::TILE, C::CHUNK), aS = tDP(jj);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts(tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
+                    mma_bf16_ts_w(leader, tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
                                 IDESC_DQ, (jj == 0 && ks == 0) ? 0u : 1u);
-                mma_commit(BAR_KE(jj % C::KS));
+                mma_commit_w(leader, BAR_KE(jj % C::KS));
             };
-            bool ok = mbar_wait(BAR_QDO, 0, a.watch, 22) && k_ready(0);
+            bool ok = mbar_wait_warp(BAR_QDO, 0, a.watch, 22) && k_ready(0);
             if (ok) issue_t(tS, q_lo, sK, IDESC_S);
             if (ok && (ok = v_ready(0))) {
                 issue_dp(0);
-                mma_commit(BAR_SDF);
+                mma_commit_w(leader, BAR_SDF);
             }
             for (int j = 0; j < nj && ok; ++j) {
                 // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j);
@@ -262,19 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (issued earlier by this thread) has read; K_{j+1} and V_{j+1}
                 // have landed (the gate's arrival on LD)
                 if (j + 1 < nj) {
-                    if (!(ok = mbar_wait(BAR_LD, j & 1, a.watch, 24))) break;
+                    if (!(ok = mbar_wait_warp(BAR_LD, j & 1, a.watch, 24))) break;
                     tc_fence_after();
                     issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
                     issue_dp(j + 1);
-                    mma_commit(BAR_SDF);
+                    mma_commit_w(leader, BAR_SDF);
                 }
-                if (!(ok = mbar_wait(BAR_PF, j & 1, a.watch, 24))) break;
-                mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
+                if (!(ok = mbar_wait_warp(BAR_PF, j & 1, a.watch, 24))) break;
+                if (leader) mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
                 tc_fence_after();
                 issue_dq(j);
             }
             // every issued MMA has finished before TMEM is released
-            mma_commit(BAR_ACC);
+            mma_commit_w(leader, BAR_ACC);
             mbar_drain(BAR_ACC, 0, a.watch, 25);
         }
         __syncwarp();
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ndx2 = f2(-dval * dsc, -dval * dsc), dsc2 = f2(dsc, dsc);
         bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
-            if (!(ok = mbar_wait(BAR_SDF, j & 1, a.watch, 26))) break;
+            if (!(ok = mbar_wait_warp(BAR_SDF, j & 1, a.watch, 26))) break;
             tc_fence_after();
             const uint32_t tDP = tbase + C::TM_DP + (j & 1) * 128 + lane_off + hf * 64;
             uint32_t sv[64], dp[64];
@@ -344,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // arriving on PF(j) only once that thread has seen PF(j-1) keeps a
             // fast warp's arrival out of PF(j-1)'s phase and PF from running
             // two phases ahead of the thread's parity wait
-            if (j > 0 && !(ok = mbar_wait(BAR_PFS, (j - 1) & 1, a.watch, 39))) break;
+            if (j > 0 && !(ok = mbar_wait_warp(BAR_PFS, (j - 1) & 1, a.watch, 39))) break;
             mbar_arrive(BAR_PF);
         }
-        const bool ok_e = ok && mbar_wait(BAR_ACC, 0, a.watch, 27);
+        const bool ok_e = ok && mbar_wait_warp(BAR_ACC, 0, a.watch, 27);
         if (ok_e) {
             tc_fence_after();
             // dQ = scale * (dS K): each warpgroup stages half of the d columns into

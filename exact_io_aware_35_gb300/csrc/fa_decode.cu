@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         bool ok = true;
         int kb = blocks.first();
         for (int j = 0; j < nkv; ++j, kb = blocks.next(kb)) {
-            if (!(ok = mbar_wait(BAR_SF(j & 1), (j >> 1) & 1, a.watch, 46))) break;
+            if (!(ok = mbar_wait_warp(BAR_SF(j & 1), (j >> 1) & 1, a.watch, 46))) break;
             tc_fence_after();
             const uint32_t tS = tbase + C::TM_S + (j & 1) * kBN + lane_off;
             uint32_t s[kBN];
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             // O was last written by PV(j-1), which may still be running: wait
             // for it before rescaling (rare: only when the reference max moves)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                if (!(ok = mbar_wait(BAR_PVD, (j - 1) & 1, a.watch, 47))) break;
+                if (!(ok = mbar_wait_warp(BAR_PVD, (j - 1) & 1, a.watch, 47))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cb = 0; cb < D; cb += 32) {
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         }
         // ---- epilogue: O / l and lse, straight to the output (one split) or
         // to this split's fp32 slot of the workspace
-        const bool ok_e = ok && (nkv == 0 || mbar_wait(BAR_OF, 0, a.watch, 48));
+        const bool ok_e = ok && (nkv == 0 || mbar_wait_warp(BAR_OF, 0, a.watch, 48));
         if (ok_e) {
             if (nkv > 0) tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

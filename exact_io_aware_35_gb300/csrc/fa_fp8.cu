@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv_mine; ++j) {
-            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.watch, 56))) break;
+            if (!(ok = mbar_wait_warp(BAR_SF(t), j & 1, a.watch, 56))) break;
             tc_fence_after();
             // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
             // and every exponent is one FMA, two columns per packed f32x2 op
@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         // ---- epilogue: O * sv / l -> bf16, plain stores (one 256-byte row per
         // thread); lse
-        const bool ok_e = ok && mbar_wait(BAR_OF(t), 0, a.watch, 57);
-        if (ok_e && grow < a.N) {
+        const bool ok_e = ok && mbar_wait_warp(BAR_OF(t), 0, a.watch, 57);
+        if (ok_e) {  // every lane takes part in the (warp-collective) TMEM loads
             tc_fence_after();
             const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;
             uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * 128;
@@ -483,13 +483,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+                if (grow < a.N)
 #pragma unroll
-                for (int p4 = 0; p4 < 4; ++p4)
-                    reinterpret_cast<uint4*>(dst + cb)[p4] =
-                        make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
+                    for (int p4 = 0; p4 < 4; ++p4)
+                        reinterpret_cast<uint4*>(dst + cb)[p4] =
+                            make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
             }
-            a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
-                (m_ref + log2f(l)) * 0.6931471805599453f;
+            if (grow < a.N)
+                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                    (m_ref + log2f(l)) * 0.6931471805599453f;
         }
     }
 

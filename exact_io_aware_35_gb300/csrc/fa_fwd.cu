@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(384, 1)
         if (F16 && a.q16 != nullptr) {
             const float mul = pow2f(ld_once(&a.f16s->q));
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
-            if (mbar_wait(BAR_Q(), 0, a.watch, 15)) {
+            if (mbar_wait_warp(BAR_Q(), 0, a.watch, 15)) {
                 for (int t = 0; t < 2; ++t)
                     warp_tile_to_f16<D>(sQ + t * C::TILE,
                                         a.q16 + (static_cast<size_t>(b) * a.N + row0 + t * kBM) *
@@ -267,8 +267,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ================= MMA issuer (one thread) =================
-        if (lane == 0) {
+        // ================= MMA issuer (the whole warp; the leader lane issues) =================
+        {
+            const uint32_t leader = elect_one();
             constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
             constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
             // descriptors built once per tile; each MMA only moves the start address
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss(dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK, ks > 0);
+                    mma_bf16_ss_w(leader, dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK, ks > 0);
                 }
             };
             auto issue_pv = [&](int t, int slot, bool acc) {
@@ -290,21 +291,21 @@ __global__ void __launch_bounds__(384, 1)
                 const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts(dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
+                    mma_bf16_ts_w(leader, dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
                                 (acc || ks > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(BAR_Q(), 0, a.watch, 3);
+            bool ok = mbar_wait_warp(BAR_Q(), 0, a.watch, 3);
             if (ok && u_first >= 0) {
                 // first union block: the score tiles of the tiles that have it
-                ok = mbar_wait(BAR_KVF(0), 0, a.watch, 4);
+                ok = mbar_wait_warp(BAR_KVF(0), 0, a.watch, 4);
                 if (ok) {
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t)
                         if (blk.has(t, u_first)) {
                             issue_qk(t, 0);
-                            mma_commit(BAR_SF(t));
+                            mma_commit_w(leader, BAR_SF(t));
                         }
-                    mma_commit(BAR_KVE(0));
+                    mma_commit_w(leader, BAR_KVE(0));
                 }
             }
             // Per union block u (ring entries 2i, 2i + 1), with un the next one:
@@ -319,39 +320,39 @@ __global__ void __launch_bounds__(384, 1)
                 const int kslot = (2 * i + 2) % C::NSLOT;
                 const bool h0 = blk.has(0, u), h0n = un >= 0 && blk.has(0, un);
                 if (h0) {
-                    if (!(ok = mbar_wait(BAR_PF(0), cnt[0] & 1, a.watch, 6))) break;
+                    if (!(ok = mbar_wait_warp(BAR_PF(0), cnt[0] & 1, a.watch, 6))) break;
                     tc_fence_after();
                     issue_pv(0, vslot, cnt[0] > 0);
                     ++cnt[0];
-                    if (blk.next_of(0, u) < 0) mma_commit(BAR_OF(0));
+                    if (blk.next_of(0, u) < 0) mma_commit_w(leader, BAR_OF(0));
                     if (h0n) {
                         issue_qk(0, kslot);
-                        mma_commit(BAR_SF(0));
+                        mma_commit_w(leader, BAR_SF(0));
                     }
                 }
                 if (blk.has(1, u)) {
-                    if (!(ok = mbar_wait(BAR_PF(1), cnt[1] & 1, a.watch, 8))) break;
+                    if (!(ok = mbar_wait_warp(BAR_PF(1), cnt[1] & 1, a.watch, 8))) break;
                     tc_fence_after();
                     issue_pv(1, vslot, cnt[1] > 0);
                     ++cnt[1];
                 }
-                mma_commit(BAR_KVE(vslot));
-                if (blk.has(1, u) && blk.next_of(1, u) < 0) mma_commit(BAR_OF(1));
+                mma_commit_w(leader, BAR_KVE(vslot));
+                if (blk.has(1, u) && blk.next_of(1, u) < 0) mma_commit_w(leader, BAR_OF(1));
                 if (un >= 0) {
                     if (blk.has(1, un)) {
                         issue_qk(1, kslot);
-                        mma_commit(BAR_SF(1));
+                        mma_commit_w(leader, BAR_SF(1));
                     }
                     if (!h0 && h0n) {
                         issue_qk(0, kslot);
-                        mma_commit(BAR_SF(0));
+                        mma_commit_w(leader, BAR_SF(0));
                     }
-                    mma_commit(BAR_KVE(kslot));
+                    mma_commit_w(leader, BAR_KVE(kslot));
                 }
                 u = un;
             }
             // all issued MMAs have finished before TMEM can be released
-            mma_commit(BAR_DONE);
+            mma_commit_w(leader, BAR_DONE);
             mbar_drain(BAR_DONE, 0, a.watch, 9);
         }
         __syncwarp();
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u0 = blk.has(t, 0) ? 0 : blk.next_of(t, 0);  // the tile's first block
         int j = 0;                                               // blocks done so far
         for (int u = u0; u >= 0; u = blk.next_of(t, u), ++j) {
-            if (!(ok = mbar_wait(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
+            if (!(ok = mbar_wait_warp(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
             tc_fence_after();
             uint32_t s[kBN];
             tmem_ld32(tS + 0, s);
@@ -461,10 +462,10 @@ __global__ void __launch_bounds__(384, 1)
         // lse = -inf: no MMA ever wrote its O, and only the Q load, which must
         // land before the buffer is reused, touched its staging buffer)
         const bool any = u0 >= 0;
-        bool ok_e = ok && (any ? mbar_wait(BAR_OF(t), 0, a.watch, 12 + t)
-                               : mbar_wait(BAR_Q(), 0, a.watch, 16));
+        bool ok_e = ok && (any ? mbar_wait_warp(BAR_OF(t), 0, a.watch, 12 + t)
+                               : mbar_wait_warp(BAR_Q(), 0, a.watch, 16));
         if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
-            ok_e = ok_e && mbar_wait(BAR_QC, 0, a.watch, 14);
+            ok_e = ok_e && mbar_wait_warp(BAR_QC, 0, a.watch, 14);
         const uint32_t stage = sQ + t * C::TILE;
         if (ok_e) {
             tc_fence_after();

@@ -100,6 +100,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     return true;
 }
 
+// mbar_wait by every lane of a warp, with one answer for the whole warp (a
+// lane whose wait ran out while another's completed makes the warp give up),
+// so that a warp-wide role's control flow never diverges.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Watch& w,
+                                               uint32_t site) {
+    const bool ok = mbar_wait(bar, parity, w, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // The wait a thread block makes before it exits for work it has itself put
 // in flight -- its last TMA loads, its last MMAs -- which completes without
 // any other thread's help.  It does not give up when another block failed
@@ -256,6 +265,56 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The MMA-issuing roles run warp-wide: every lane executes the role's loop
+// (its barrier waits, its descriptor arithmetic, which the whole warp then
+// holds as warp-uniform values), and only the lane elect.sync picks issues the
+// single-thread tcgen05 instructions.  `leader` is that lane's flag.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r;
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], issued by the leader lane only
+__device__ __forceinline__ void mma_bf16_ss_w(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc], issued by the leader lane only
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+
+// mma_commit by the leader lane only
+__device__ __forceinline__ void mma_commit_w(uint32_t leader, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(leader)
         : "memory");
 }
 
