@@ -46,31 +46,25 @@ struct FwdCfg {
     static constexpr int SMEM_Q = 2 * TILE;
     static constexpr int SMEM_KV = NSLOT * TILE;
     // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
-    // o_final[2], mma_done, q_copied, row-max exchange[2]
-    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 2;
-    // the two column halves of a row exchange their partial maxima (and, at
-    // the end, row sums) through [tile][parity][half][row] floats
-    static constexpr int XBUF_BYTES = 2 * 2 * 2 * kBM * 4;
-    static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16 + XBUF_BYTES;
+    // o_final[2], mma_done, q_copied
+    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16;
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 256;
     static constexpr uint32_t TM_COLS = 512;
-    // softmax: warpgroups 0-1 (tile 0, key columns 0-63 / 64-127), 2-3 (tile
-    // 1); then the MMA, TMA, gate and copy warps
-    static constexpr int THREADS = 640;
+    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, copy}
 };
 
-constexpr int kWarpMma = 16;
-constexpr int kWarpLoad = 17;
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
 // The gate warp folds "K/V tiles landed" into the p_full barriers, so the MMA
 // thread waits on two barriers per key block instead of four: every mbarrier
 // wait in the issuing thread costs tensor-core time.
-constexpr int kWarpGate = 18;
+constexpr int kWarpGate = 10;
 // The training forward's copy warp writes the fp16 copy of the CTA's Q tiles
 // (for the backward) while the tiles sit in shared memory anyway.
-constexpr int kWarpCopy = 19;
+constexpr int kWarpCopy = 11;
 
 // Row-max and exp threshold for the lazy rescale: the reference max is only
 // moved when the new block maximum exceeds it by more than 2^8 (in log2
@@ -116,7 +110,7 @@ struct TileBlocks {
 // scaled by 2^v (the training forward, whose O feeds the backward's D).
 // SPARSE: the tiles multiply only the key blocks a.block_mask selects.
 template <int D, bool F16, bool SPARSE>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdArgs a) {
@@ -137,9 +131,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * C::NSLOT + t); };
     const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * C::NSLOT);
     const uint32_t BAR_QC = bar0 + 8u * (8 + 2 * C::NSLOT);  // Q tiles read by the copy warp
-    // row-max (and row-sum) exchange between the two column halves of tile t
-    auto BAR_MX = [&](int t) { return bar0 + 8u * (9 + 2 * C::NSLOT + t); };
-    float* xbuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -174,9 +165,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(BAR_SF(t), 1);
-            mbar_init(BAR_PF(t), 256 + 1);  // the tile's softmax threads and the gate
+            mbar_init(BAR_PF(t), 128 + 1);  // the tile's softmax threads and the gate
             mbar_init(BAR_OF(t), 1);
-            mbar_init(BAR_MX(t), 256);      // the tile's softmax threads
         }
         mbar_init(BAR_DONE, 1);
         mbar_init(BAR_QC, 1);
@@ -295,16 +285,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     mma_bf16_ss_w(leader, dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK, ks > 0);
                 }
             };
-            // P (16-bit pairs) of keys 64h.. sits in S_t's columns 64h..64h+31
-            // (each column half writes within its own S columns)
             auto issue_pv = [&](int t, int slot, bool acc) {
                 const uint32_t dO = tbase + C::TM_O + t * D;
-                const uint32_t aP = tbase + C::TM_S + t * kBN;
+                const uint32_t aP = tbase + C::TM_S + t * kBN;  // P (bf16) over S_t
                 const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts_w(leader, dO, aP + (ks >> 2) * 64 + (ks & 3) * 8,
-                                  sdesc_at(b_lo, HI, ks * 2048), IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+                    mma_bf16_ts_w(leader, dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
+                                (acc || ks > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait_warp(BAR_Q(), 0, a.watch, 3);
             if (ok && u_first >= 0) {
@@ -368,70 +356,54 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             mbar_drain(BAR_DONE, 0, a.watch, 9);
         }
         __syncwarp();
-    } else if (warp < 16) {
-        // ============ softmax: warpgroups 2t and 2t+1 share tile t's rows ============
-        // Each query row (TMEM lane) is split between two threads, one per
-        // column half h: each reads its 64 key columns of S_t, the two swap
-        // their partial maxima through shared memory and the exchange barrier,
-        // both take the same row maximum and rescale decision, and each turns
-        // its 64 columns into P and its half of the row sum.  Two threads per
-        // row double the warps working on a tile's softmax, the part of the
-        // key-block loop that paces the kernel.
-        const int t = warp >> 3;                // query tile
-        const int hh = (warp >> 2) & 1;         // column half: keys 64 hh .. 64 hh + 63
-        const int wq = warp & 3;                // TMEM lanes 32 wq ..
-        const int r = wq * 32 + lane;           // row within the tile
-        const int grow = row0 + t * kBM + r;    // query index
+    } else if (warp < 8) {
+        // ================= softmax warpgroups (warps 0-3: tile 0, 4-7: tile 1)
+        const int t = warp >> 2;               // query tile of this warpgroup
+        const int wq = warp & 3;               // its warp owns TMEM lanes 32*wq..32*wq+31
+        const int r = wq * 32 + lane;          // row within the tile
+        const int grow = row0 + t * kBM + r;   // query index
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t tS = tbase + C::TM_S + t * kBN + hh * 64 + lane_off;
+        const uint32_t tS = tbase + C::TM_S + t * kBN + lane_off;
         const uint32_t tO = tbase + C::TM_O + t * D + lane_off;
         const float sl2 = a.scale_log2;
         int eq = 0, ek = 0, ev = 0, edo = 0;  // fp16 path: O carries 2^ev
         if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
         // last key index this row may see
         const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
-        // xbuf[t][parity][half][row]
-        auto xslot = [&](int par, int half) { return xbuf + ((t * 2 + par) * 2 + half) * kBM + r; };
         float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
-        float l = 0.f;            // this half's running sum, relative to m_ref
+        float l = 0.f;            // running sum, relative to m_ref
         bool ok = true;
         const int u0 = blk.has(t, 0) ? 0 : blk.next_of(t, 0);  // the tile's first block
         int j = 0;                                               // blocks done so far
         for (int u = u0; u >= 0; u = blk.next_of(t, u), ++j) {
             if (!(ok = mbar_wait_warp(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
             tc_fence_after();
-            const int kbase = u * kBN + hh * 64;  // key of this half's column 0
-            const bool masked = kbase + 63 > lim;  // diagonal block or ragged tail
-            // pass 1: this half's row maximum (raw scores; sl2 > 0)
+            uint32_t s[kBN];
+            tmem_ld32(tS + 0, s);
+            tmem_ld32(tS + 32, s + 32);
+            tmem_ld32(tS + 64, s + 64);
+            tmem_ld32(tS + 96, s + 96);
+            tmem_wait_ld();
+            reg_fence<kBN>(s);
+            float x[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
+            const int kbase = u * kBN;
+            if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+            }
+            // row max: eight running maxima, three-input max instructions
             float mk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = -INFINITY;
+            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t sv[32];
-                tmem_ld32(tS + c2 * 32, sv);
-                tmem_wait_ld();
-                reg_fence<32>(sv);
+            for (int c = 16; c < kBN; c += 16)
 #pragma unroll
-                for (int c = 0; c < 32; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float x0 = __uint_as_float(sv[c + i]), x1 = __uint_as_float(sv[c + 8 + i]);
-                        if (masked) {
-                            x0 = (kbase + c2 * 32 + c + i > lim) ? -INFINITY : x0;
-                            x1 = (kbase + c2 * 32 + c + 8 + i > lim) ? -INFINITY : x1;
-                        }
-                        mk[i] = fmax3(mk[i], x0, x1);
-                    }
-            }
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
             const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
                                    fmaxf(mk[6], mk[7]));
-            // swap partial maxima with the other half of the row
-            *xslot(j & 1, hh) = mx;
-            mbar_arrive(BAR_MX(t));
-            if (!(ok = mbar_wait_warp(BAR_MX(t), j & 1, a.watch, 17))) break;
-            const float mrow = fmaxf(mx, *xslot(j & 1, hh ^ 1));  // the same in both halves
-            const float m_new = fmaxf(m_ref, mrow * sl2);
+            const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + kRescaleThreshold;
             float alpha = 1.f;
             if (need) {
@@ -441,42 +413,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
-            uint64_t ls2[2] = {0, 0};  // packed partial row sums
-            // pass 2: P of 32 columns at a time, into this half's first 32 S
-            // columns (chunk c2's 32 keys -> 16 columns; its own S is already read)
+            uint64_t ls2[4] = {0, 0, 0, 0};  // packed partial row sums
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t sv[32];
-                tmem_ld32(tS + c2 * 32, sv);
-                tmem_wait_ld();
-                reg_fence<32>(sv);
-                uint32_t pk[16];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
-                    if (masked) {
-                        x0 = (kbase + c2 * 32 + c > lim) ? -INFINITY : x0;
-                        x1 = (kbase + c2 * 32 + c + 1 > lim) ? -INFINITY : x1;
-                    }
+                for (int c = 0; c < 64; c += 2) {
                     float e0, e1;
-                    f2_split(fma2(f2(x0, x1), sl2x2, negx2), e0, e1);
+                    f2_split(fma2(f2(x[half * 64 + c], x[half * 64 + c + 1]), sl2x2, negx2), e0, e1);
                     const float p0 = ex2(e0), p1 = ex2(e1);
-                    ls2[(c >> 1) & 1] = add2(ls2[(c >> 1) & 1], f2(p0, p1));
+                    ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
                     pk[c >> 1] = pack_op<F16>(p0, p1);
                 }
-                tmem_st16(tS + c2 * 16, pk);
+                tmem_st32(tS + half * 32, pk);
             }
             {
+                const uint64_t t = add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3]));
                 float a0, a1;
-                f2_split(add2(ls2[0], ls2[1]), a0, a1);
+                f2_split(t, a0, a1);
                 l += a0 + a1;
             }
             // O_t was last written by the P V product of block j-1, which
-            // completed before this block's scores were committed; each half
-            // rescales its D/2 columns of O_t
+            // completed before this block's scores were committed.
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cb = hh * (D / 2); cb < (hh + 1) * (D / 2); cb += 32) {
+                for (int cb = 0; cb < D; cb += 32) {
                     uint32_t o[32];
                     tmem_ld32(tO + cb, o);
                     tmem_wait_ld();
@@ -501,16 +462,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         // lse = -inf: no MMA ever wrote its O, and only the Q load, which must
         // land before the buffer is reused, touched its staging buffer)
         const bool any = u0 >= 0;
-        // the row sum: both halves' partial sums (relative to the same m_ref),
-        // added in the same order in both threads
-        float lrow = l;
-        if (ok && any) {
-            *xslot(j & 1, hh) = l;
-            mbar_arrive(BAR_MX(t));
-            ok = mbar_wait_warp(BAR_MX(t), j & 1, a.watch, 17);
-            const float lo = *xslot(j & 1, hh ^ 1);
-            lrow = hh == 0 ? l + lo : lo + l;
-        }
         bool ok_e = ok && (any ? mbar_wait_warp(BAR_OF(t), 0, a.watch, 12 + t)
                                : mbar_wait_warp(BAR_Q(), 0, a.watch, 16));
         if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
@@ -519,9 +470,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (ok_e) {
             tc_fence_after();
             // O was accumulated against V * 2^v on the fp16 path
-            const float inv_l = (lrow > 0.f) ? pow2f(-ev) / lrow : 0.f;
+            const float inv_l = (l > 0.f) ? pow2f(-ev) / l : 0.f;
 #pragma unroll
-            for (int cb = hh * (D / 2); cb < (hh + 1) * (D / 2); cb += 32) {
+            for (int cb = 0; cb < D; cb += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + cb, o);
                 tmem_wait_ld();
@@ -555,13 +506,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                                  w[4 * p4 + 2], w[4 * p4 + 3]);
                 }
             }
-            if (hh == 0 && grow < a.N)
+            if (grow < a.N)
                 a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
-                    (m_ref + log2f(lrow)) * 0.6931471805599453f;
+                    (m_ref + log2f(l)) * 0.6931471805599453f;
             fence_proxy_async_smem();
         }
-        named_bar_sync(1 + t, 256);
-        if (ok_e && hh == 0 && r == 0) {
+        named_bar_sync(1 + t, 128);
+        if (ok_e && r == 0) {
             for (int c = 0; c < C::NCH; ++c)
                 tma_store_4d(&tmO, stage + c * C::CHUNK, c * 64, h, row0 + t * kBM, b);
             tma_store_commit();

@@ -494,8 +494,114 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     return model
 
 
-def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, single_x=False,
-                    early_qk=False):
+def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
+    """Two query tiles: tile 0 multiplies key blocks [0, nkv0), tile 1
+    [0, nkv) (nkv0 < nkv on the causal diagonal); four softmax warps per
+    tile, warp q owning rows 32q.. of S_t and O_t."""
+    rows = range(4)
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
+        bars.update(ring_bars(NSLOT))
+        n_of = (nkv0, nkv)
+
+        def tile(pre, t, tag):
+            return {f"{pre}.{t}.{q}": tag for q in rows}
+
+        def gate():
+            for j in range(nkv):
+                v, kn = 2 * j + 1, 2 * j + 2
+                yield ("wait", f"F{v % NSLOT}", v // NSLOT)
+                if j + 1 < nkv:
+                    yield ("wait", f"F{kn % NSLOT}", kn // NSLOT)
+                for t in (0, 1):
+                    if j >= n_of[t]:
+                        continue
+                    if j > 0:
+                        yield ("wait", f"PF{t}", j - 1)
+                    yield ("arrive", f"PF{t}", 1, j)
+
+        def copy():
+            yield ("wait", "Q", 0)
+            yield ("read", dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            yield ("arrive", "QC", 1, 0)
+
+        def qk(t, j):
+            slot = (2 * j) % NSLOT
+            return ("mma", f"QK({t},{j})", dict(tile("Q", t, "Q"), **{f"kv{slot}": f"K({j})"}),
+                    tile("S", t, f"S({t},{j})"))
+
+        def pv(t, j):
+            slot = (2 * j + 1) % NSLOT
+            reads = dict(tile("S", t, f"P({t},{j})"), **{f"kv{slot}": f"V({j})"})
+            if j > 0:
+                reads.update(tile("O", t, f"O({t},{j - 1})"))
+            return ("mma", f"PV({t},{j})", reads, tile("O", t, f"O({t},{j})"))
+
+        def mma():
+            yield ("wait", "Q", 0)
+            yield ("wait", "F0", 0)
+            yield qk(0, 0)
+            yield ("commit", "SF0", 0)
+            yield qk(1, 0)
+            yield ("commit", "SF1", 0)
+            yield ("commit", "E0", 0)
+            for j in range(nkv):
+                vslot, kidx = (2 * j + 1) % NSLOT, 2 * (j + 1)
+                kslot = kidx % NSLOT
+                if j < nkv0:
+                    yield ("wait", "PF0", j)
+                    yield pv(0, j)
+                    if j == nkv0 - 1:
+                        yield ("commit", "OF0", 0)
+                if j + 1 < nkv0:
+                    yield qk(0, j + 1)
+                    yield ("commit", "SF0", j + 1)
+                if early_qk and j + 1 < nkv:
+                    yield qk(1, j + 1)
+                yield ("wait", "PF1", j)
+                yield pv(1, j)
+                yield ("commit", f"E{vslot}", (2 * j + 1) // NSLOT)
+                if j == nkv - 1:
+                    yield ("commit", "OF1", 0)
+                if j + 1 < nkv:
+                    if not early_qk:
+                        yield qk(1, j + 1)
+                    yield ("commit", "SF1", j + 1)
+                    yield ("commit", f"E{kslot}", kidx // NSLOT)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def softmax(t, q):
+            me = f"{t}.{q}"
+            for j in range(n_of[t]):
+                yield ("wait", f"SF{t}", j)
+                yield ("read", {f"S.{me}": f"S({t},{j})"})
+                yield ("write", {f"S.{me}": f"P({t},{j})"})
+                if j > 0 and rnd.random() < 0.5:  # the reference max moved
+                    yield ("read", {f"O.{me}": f"O({t},{j - 1})"})
+                    yield ("write", {f"O.{me}": f"O({t},{j - 1})"})
+                yield ("arrive", f"PF{t}", 32, j)
+            yield ("wait", f"OF{t}", 0)
+            if copy_q:
+                yield ("wait", "QC", 0)
+            yield ("read", {f"O.{me}": f"O({t},{n_of[t] - 1})"})
+            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
+
+        q_tiles = dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q"))
+        roles = {"prod": kv_ring_producer(nkv, NSLOT, q_tiles), "gate": gate(), "mma": mma()}
+        for t in (0, 1):
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
+        if copy_q:
+            roles["copy"] = copy()
+        return bars, roles
+
+    return model
+
+
+def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
     """The forward kernel's protocol with its key blocks given per tile
     (block-sparse masks; the dense kernel is blocks0 = range(nkv0), blocks1 =
     range(nkv)).  Every role walks the union of the two sets in increasing
@@ -504,17 +610,8 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
     them, PV1(u), V(u)'s slot released, S1(un), then S0(un) when tile 0 had
     no u (deferred behind tile 1's p_full wait, which is the one that says
     K(un) has landed), K(un)'s slot released.  defer_qk0=False issues that
-    S0(un) before tile 1's wait: a planted mistake.
-
-    Each row is split between two softmax warps (column halves h = 0, 1):
-    per block each writes its partial maximum to its slot of the exchange
-    buffer (two slots per half, by block parity), arrives on MX(t) and, once
-    MX(t) has completed, reads the other half's slot; after the last block the
-    same exchange carries the halves' row sums.  single_x (one slot per half
-    instead of two) is a planted mistake, and so is early_qk: S1(un) issued
-    before PV1(u) has consumed P1(u), which S1 overwrites."""
+    S0(un) before tile 1's wait: a planted mistake."""
     rows = range(4)
-    halves = (0, 1)
     sets = (sorted(set(blocks0)), sorted(set(blocks1)))
     union = sorted(set(sets[0]) | set(sets[1]))
 
@@ -522,12 +619,12 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
         return u in sets[t]
 
     def model(rnd):
-        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 257, "PF1": 257, "OF0": 1, "OF1": 1,
-                "DONE": 1, "QC": 1, "MX0": 256, "MX1": 256}
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
         bars.update(ring_bars(NSLOT))
 
         def tile(pre, t, tag):
-            return {f"{pre}.{t}.{h}.{q}": tag for q in rows for h in halves}
+            return {f"{pre}.{t}.{q}": tag for q in rows}
 
         def producer():
             last = {}
@@ -608,9 +705,6 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
                         yield qk(0, i + 1, un)
                         yield ("commit", "SF0", sf[0])
                         sf[0] += 1
-                early = early_qk and un is not None and has(1, un)
-                if early:
-                    yield qk(1, i + 1, un)
                 if has(1, u):
                     yield ("wait", "PF1", cnt[1])
                     yield pv(1, i, u, prev[1])
@@ -620,8 +714,7 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
                     yield ("commit", "OF1", 0)
                 if un is not None:
                     if has(1, un):
-                        if not early:
-                            yield qk(1, i + 1, un)
+                        yield qk(1, i + 1, un)
                         yield ("commit", "SF1", sf[1])
                         sf[1] += 1
                     if defer_qk0 and not h0 and h0n:
@@ -632,23 +725,11 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
             yield ("commit", "DONE", 0)
             yield ("wait", "DONE", 0)
 
-        def xslot(t, j, h, q):
-            return f"X.{t}.{0 if single_x else j & 1}.{h}.{q}"
-
-        def exchange(t, j, h, q, what):
-            yield ("write", {xslot(t, j, h, q): f"{what}({t},{j})"})
-            yield ("arrive", f"MX{t}", 32, j)
-            yield ("wait", f"MX{t}", j)
-            yield ("read", {xslot(t, j, 1 - h, q): f"{what}({t},{j})"})
-
-        def softmax(t, h, q):
-            me = f"{t}.{h}.{q}"
+        def softmax(t, q):
+            me = f"{t}.{q}"
             prev = None
-            j = -1
             for j, u in enumerate(sets[t]):
                 yield ("wait", f"SF{t}", j)
-                yield ("read", {f"S.{me}": f"S({t},{u})"})
-                yield from exchange(t, j, h, q, "max")
                 yield ("read", {f"S.{me}": f"S({t},{u})"})
                 yield ("write", {f"S.{me}": f"P({t},{u})"})
                 if prev is not None and rnd.random() < 0.5:  # the reference max moved
@@ -657,7 +738,6 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
                 yield ("arrive", f"PF{t}", 32, j)
                 prev = u
             if sets[t]:
-                yield from exchange(t, j + 1, h, q, "sum")
                 yield ("wait", f"OF{t}", 0)
                 yield ("read", {f"O.{me}": f"O({t},{prev})"})
             else:  # a tile with no block stages zeros, once its Q tile has landed
@@ -668,9 +748,8 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, sin
 
         roles = {"prod": producer(), "gate": gate(), "mma": mma()}
         for t in (0, 1):
-            for h in halves:
-                for q in rows:
-                    roles[f"s{t}{h}{q}"] = softmax(t, h, q)
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
         if copy_q:
             roles["copy"] = copy()
         return bars, roles
@@ -745,8 +824,8 @@ def decode_model(nkv, NSLOT=6, skip_pvd_wait=False):
 
 
 # ---------------------- single S buffer (one-tile forward; no kernel uses it now)
-# The FP8 forward now has the bf16 forward's two-tile protocol (fwd_union_model
-# with dense block sets and no copy warp, which test_forward_protocol runs).  This model of the earlier
+# The FP8 forward now has the bf16 forward's two-tile protocol (fwd_model with
+# no copy warp, which test_forward_protocol runs).  This model of the earlier
 # one-tile protocol stays as the ring-without-empty-wait planted-mistake case.
 def single_s_model(nkv, NSLOT=4, skip_empty=False):
     """Four softmax warps over one S buffer (P written over S), a ring of
@@ -831,8 +910,7 @@ def test_dkdv_smem_ds_variant_protocol(n_it, ds_in_do):
                                             (3, 4, 8), (9, 9, 8)])
 @pytest.mark.parametrize("copy_q", [True, False])
 def test_forward_protocol(nkv0, nkv, nslot, copy_q):
-    # the dense forward: tile 0 multiplies blocks 0 .. nkv0 - 1, tile 1 0 .. nkv - 1
-    each_seed(fwd_union_model(range(nkv0), range(nkv), nslot, copy_q), seeds=range(30))
+    each_seed(fwd_model(nkv0, nkv, nslot, copy_q))
 
 
 UNION_CASES = [  # (tile 0's key blocks, tile 1's key blocks, ring slots)
@@ -863,17 +941,10 @@ def test_forward_union_random_masks():
         each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8))), seeds=range(8))
 
 
-def test_forward_split_row_exchange_with_one_slot_is_caught():
-    # one exchange slot per half: a half that runs a block ahead overwrites
-    # its partial maximum before the other half has read the previous one
-    assert fails_on_some_seed(fwd_union_model(range(6), range(6), 8, single_x=True))
-
-
 def test_forward_union_early_score_of_the_idle_tile_is_caught():
     # S0(un) issued before tile 1's p_full wait, although tile 0 had no u:
     # nothing yet says K(un) has landed
-    assert fails_on_some_seed(fwd_union_model([4], [0, 1, 2, 3, 4], 4, defer_qk0=False),
-                              seeds=range(400))
+    assert fails_on_some_seed(fwd_union_model([4], [0, 1, 2, 3, 4], 4, defer_qk0=False))
 
 
 @pytest.mark.parametrize("nkv,nslot", [(0, 6), (1, 6), (2, 6), (3, 6), (7, 6), (20, 6), (13, 12)])
@@ -911,7 +982,7 @@ def test_dq_two_issuers_single_dq_done_barrier_is_caught():
 
 def test_forward_early_score_product_is_caught():
     # S(1, j+1) issued before the softmax has handed P(1, j) back
-    assert fails_on_some_seed(fwd_union_model(range(3), range(4), early_qk=True))
+    assert fails_on_some_seed(fwd_model(3, 4, early_qk=True))
 
 
 def test_decode_rescale_without_pv_wait_is_caught():
@@ -1030,22 +1101,21 @@ def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=200
 
 def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
     """The forward kernel's roles with every bounded wait's two outcomes:
-    producer, gate, copy warp, MMA thread and the sixteen softmax warps (eight
-    per query tile: two column halves of each row, which exchange partial
-    maxima and sums through MX), the epilogue's bar.sync over a tile's eight
-    warps, and the teardown __syncthreads over every role.  drop = (t, j): the gate's
+    producer, gate, copy warp, MMA thread and the eight softmax warps (four
+    per query tile), the epilogue's bar.sync over a tile's four warps, and the
+    teardown __syncthreads over every role.  drop = (t, j): the gate's
     arrival on p_full(t) for key block j never happens (a protocol fault)."""
     rows = range(4)
 
     def model(rnd):
-        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 257, "PF1": 257, "OF0": 1, "OF1": 1,
-                "DONE": 1, "QC": 1, "MX0": 256, "MX1": 256}
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "QC": 1}
         bars.update(ring_bars(NSLOT))
         n_of = (nkv0, nkv)
-        n_roles = 3 + 16 + (1 if copy_q else 0)
+        n_roles = 3 + 8 + (1 if copy_q else 0)
 
         def tile(pre, t, tag):
-            return {f"{pre}.{t}.{h}.{q}": tag for q in rows for h in (0, 1)}
+            return {f"{pre}.{t}.{q}": tag for q in rows}
 
         def teardown():
             yield ("nbar", "syncthreads", n_roles)
@@ -1149,50 +1219,33 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
             yield ("twait", "DONE", 0, "drain")
             yield from teardown()
 
-        def softmax(t, h, q):
-            me = f"{t}.{h}.{q}"
+        def softmax(t, q):
             ok = True
-            j = 0
             for j in range(n_of[t]):
                 ok = yield ("twait", f"SF{t}", j, "abort")
                 if not ok:
                     break
-                yield ("read", {f"S.{me}": f"S({t},{j})"})
-                yield ("write", {f"X.{t}.{j & 1}.{h}.{q}": f"max({j})"})
-                yield ("arrive", f"MX{t}", 32, j)
-                ok = yield ("twait", f"MX{t}", j, "abort")
-                if not ok:
-                    break
-                yield ("read", {f"X.{t}.{j & 1}.{1 - h}.{q}": f"max({j})"})
-                yield ("write", {f"S.{me}": f"P({t},{j})"})
+                yield ("read", {f"S.{t}.{q}": f"S({t},{j})"})
+                yield ("write", {f"S.{t}.{q}": f"P({t},{j})"})
                 if j > 0 and rnd.random() < 0.5:  # the lazy rescale of O
-                    yield ("read", {f"O.{me}": f"O({t},{j - 1})"})
-                    yield ("write", {f"O.{me}": f"O({t},{j - 1})"})
+                    yield ("read", {f"O.{t}.{q}": f"O({t},{j - 1})"})
+                    yield ("write", {f"O.{t}.{q}": f"O({t},{j - 1})"})
                 yield ("arrive", f"PF{t}", 32, j)
-            else:
-                j = n_of[t]
-            if ok:  # the row sums' exchange
-                yield ("write", {f"X.{t}.{j & 1}.{h}.{q}": f"sum({j})"})
-                yield ("arrive", f"MX{t}", 32, j)
-                ok = yield ("twait", f"MX{t}", j, "abort")
-                if ok:
-                    yield ("read", {f"X.{t}.{j & 1}.{1 - h}.{q}": f"sum({j})"})
             ok_e = ok and (yield ("twait", f"OF{t}", 0, "abort"))
             if copy_q:
                 ok_e = ok_e and (yield ("twait", "QC", 0, "abort"))
             if ok_e:
-                yield ("read", {f"O.{me}": f"O({t},{n_of[t] - 1})"})
-                yield ("write", {f"Q.{me}": "O out"})  # staging in the Q buffer
-            yield ("nbar", f"epilogue{t}", 8)
+                yield ("read", {f"O.{t}.{q}": f"O({t},{n_of[t] - 1})"})
+                yield ("write", {f"Q.{t}.{q}": "O out"})  # staging in the Q buffer
+            yield ("nbar", f"epilogue{t}", 4)
             yield from teardown()
 
         roles = {"prod": producer(), "gate": gate(), "mma": mma()}
         if copy_q:
             roles["copy"] = copy()
         for t in (0, 1):
-            for h in (0, 1):
-                for q in rows:
-                    roles[f"s{t}{h}{q}"] = softmax(t, h, q)
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
         return bars, roles
 
     return model
@@ -1233,7 +1286,7 @@ def test_timeout_model_catches_a_partner_left_in_bar_sync():
     # the epilogue's bar.sync strands its three partners there
     def model(rnd):
         bars, roles = fwd_timeout_model(2, 3, 4, drop=(1, 1))(rnd)
-        inner = roles["s113"]
+        inner = roles["s13"]
 
         def deserter():
             value = None
@@ -1242,7 +1295,7 @@ def test_timeout_model_catches_a_partner_left_in_bar_sync():
                 if op[0] == "nbar" and op[1].startswith("epilogue"):
                     return
                 value = yield op
-        roles["s113"] = deserter()
+        roles["s13"] = deserter()
         return bars, roles
 
     caught = False
