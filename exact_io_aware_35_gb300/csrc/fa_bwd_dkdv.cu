@@ -15,11 +15,14 @@
 // issuing thread about as long as one with N = 128 and reads more shared
 // memory per flop.  Two 128-column TMEM regions X and Y swap roles every
 // block: S^T(i) and then P^T(i), dS^T(i) live in one, dP^T(i) in the other.
-// As soon as all warpgroups have copied dP^T(i) into registers, the tensor
-// core computes S^T(i+1) over it while they work; dV += P^T dO of block i
-// starts as soon as P^T(i) is written (the warpgroups store dS^T(i), already
-// formed in registers, after signalling P^T), dK += dS^T Q once dS^T(i) is,
-// and dP^T(i+1) is then written over both.  Warpgroup w owns queries
+// The warps' work on a block comes in two steps, so that its exponentials
+// run while the tensor core is busy with the block before: P^T(i) as soon as
+// S^T(i) is in TMEM (then dV += P^T dO of block i starts), and dS^T(i) =
+// P^T(i) (dP^T(i) - D) once dP^T(i) is (P^T kept in registers, rounded as it
+// entered the product).  As soon as all warpgroups have copied dP^T(i) into
+// registers, the tensor core computes S^T(i+1) over it; dK += dS^T Q follows
+// dS^T(i), and dP^T(i+1) is then written over P^T(i), dS^T(i).  The tensor
+// core's order per block: dV(i), S^T(i+1), dK(i), dP^T(i+1).  Warpgroup w owns queries
 // 32w..32w+31 of each block and writes its P^T and dS^T (16-bit pairs) over
 // the S^T columns it read.  (Tried and dropped: 64-query sub-blocks with two
 // TMEM buffers of 64-wide S^T and dP^T, which would hide the hand-off
@@ -52,9 +55,9 @@ struct DkdvCfg : Tiles<D> {
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
     static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
-    // barriers: K/V, stage full[NST], stage empty[NST], S^T+dP^T ready,
-    // dP^T copied to registers, P^T written, dS^T written, all MMAs done
-    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1;
+    // barriers: K/V, stage full[NST], stage empty[NST], dP^T ready, dP^T
+    // copied to registers, P^T written, dS^T written, all MMAs done, S^T ready
+    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1 + 1;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
 };
@@ -85,11 +88,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t BAR_KV = bar0;
     auto BAR_STF = [&](int s) { return bar0 + 8u * (1 + s); };
     auto BAR_STE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
-    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // block's S^T, dP^T ready
+    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // block's dP^T ready
     const uint32_t BAR_LD = BAR_SDF + 8u;                   // dP^T copied to registers
     const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T written
     const uint32_t BAR_DSF = BAR_SDF + 24u;                 // dS^T written
     const uint32_t BAR_ACC = BAR_SDF + 32u;
+    const uint32_t BAR_STR = BAR_SDF + 40u;                 // block's S^T ready
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_init(BAR_PF, kDkCompute);
         mbar_init(BAR_DSF, kDkCompute);
         mbar_init(BAR_ACC, 1);
+        mbar_init(BAR_STR, 1);
         fence_barrier_init();
     }
     if (warp == kDkWarpMma) {
@@ -233,31 +238,35 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             if (ok) {
                 tc_fence_after();
                 issue_t(reg_s(0), k_lo, stage_q(0));
+                mma_commit_w(leader, BAR_STR);
                 issue_t(reg_d(0), v_lo, stage_q(0) + C::TILE);
                 mma_commit_w(leader, BAR_SDF);
             }
+            // per block: dV(it) once P^T(it) is written; S^T(it+1) over dP^T(it)
+            // once every warp holds dP^T(it); dK(it) once dS^T(it) is written;
+            // dP^T(it+1) over P^T(it), dS^T(it), which the two products above
+            // read first.  The warps form P^T(it+1) from S^T(it+1) while the
+            // tensor core runs dK(it) and dP^T(it+1).
             for (int it = 0; it < n_it && ok; ++it) {
                 const int s = it % C::NST;
                 const int s2 = (it + 1) % C::NST;
                 const bool more = it + 1 < n_it;
+                if (!(ok = mbar_wait_warp(BAR_PF, it & 1, a.watch, 34))) break;
+                tc_fence_after();
+                issue_acc(it, s, false);
                 if (more) {
-                    // S^T(it+1) over dP^T(it), once both warpgroups hold it in registers
                     if (!(ok = mbar_wait_warp(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.watch, 33)))
                         break;
                     if (!(ok = mbar_wait_warp(BAR_LD, it & 1, a.watch, 34))) break;
                     tc_fence_after();
                     issue_t(reg_d(it), k_lo, stage_q(s2));
+                    mma_commit_w(leader, BAR_STR);
                 }
-                // dV as soon as P^T is written, dK once dS^T is
-                if (!(ok = mbar_wait_warp(BAR_PF, it & 1, a.watch, 34))) break;
-                tc_fence_after();
-                issue_acc(it, s, false);
                 if (!(ok = mbar_wait_warp(BAR_DSF, it & 1, a.watch, 38))) break;
                 tc_fence_after();
                 issue_acc(it, s, true);
                 mma_commit_w(leader, BAR_STE(s));
                 if (more) {
-                    // dP^T(it+1) over P^T(it), dS^T(it): the products above read them first
                     issue_t(reg_s(it), v_lo, stage_q(s2) + C::TILE);
                     mma_commit_w(leader, BAR_SDF);
                 }
@@ -292,32 +301,21 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::NST;
             const int qi = qi0 + it % nqi;
-            if (!(ok = mbar_wait_warp(BAR_SDF, it & 1, a.watch, 36))) break;
-            tc_fence_after();
             const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + wg * 32 + lane_off;
             const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + wg * 32 + lane_off;
-            // dP^T first: once every warpgroup holds it, S^T(it+1) may overwrite it
-            uint32_t dp[2][16];
-            tmem_ld16x256_x4(rd, dp[0]);
-            tmem_ld16x256_x4(rd + (16u << 16), dp[1]);
             const float* lse2 = vec + s * 2 * kBM + wg * 32;
             const float* dvec = vec + s * 2 * kBM + kBM + wg * 32;
-            uint64_t nl[4], nd[4];  // (-lse2, -D) of the thread's column pairs
+            const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
+            // ---- P^T = exp2(S^T scale log2 e - lse2), as soon as S^T is in TMEM
+            if (!(ok = mbar_wait_warp(BAR_STR, it & 1, a.watch, 36))) break;
+            tc_fence_after();
+            uint64_t nl[4];  // -lse2 of the thread's column pairs
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
-                const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
                 nl[j] = f2(-l2.x, -l2.y);
-                nd[j] = f2(-d2.x, -d2.y);
             }
-            tmem_wait_ld();
-            reg_fence<16>(dp[0]);
-            reg_fence<16>(dp[1]);
-            tc_fence_before();
-            mbar_arrive(BAR_LD);
-            const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
-            // P^T first (the tensor core starts dV += P^T dO on it), then dS^T
-            uint32_t dk[2][8];
+            uint32_t pk[2][8];  // P^T (16-bit pairs), kept for dS^T
 #pragma unroll
             for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
                 const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
@@ -328,7 +326,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
                 // causal: key k is hidden from query q when k > q
                 const bool need_mask = a.causal && key + 8 > qbase;
-                uint32_t pk[8];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -343,19 +340,47 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                             p0 = (k > q) ? 0.f : p0;
                             p1 = (k > q + 1) ? 0.f : p1;
                         }
-                        float e0, e1;
-                        f2_split(mul2(f2(p0, p1),
-                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
-                                           nd[j])), e0, e1);
-                        pk[2 * j + rsel] = pack_op<F16>(p0, p1);
-                        dk[lb][2 * j + rsel] = pack_op<F16>(e0, e1);
+                        pk[lb][2 * j + rsel] = pack_op<F16>(p0, p1);
                     }
                 }
-                tmem_st16x128_x4(rs + lo, pk);  // P^T over the first 16 S^T columns read
+                tmem_st16x128_x4(rs + lo, pk[lb]);  // P^T over the first 16 S^T columns read
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR_PF);
+            // ---- dS^T = P^T (dP^T - D), once dP^T is in TMEM (from the rounded P^T)
+            if (!(ok = mbar_wait_warp(BAR_SDF, it & 1, a.watch, 40))) break;
+            tc_fence_after();
+            uint32_t dp[2][16];
+            tmem_ld16x256_x4(rd, dp[0]);
+            tmem_ld16x256_x4(rd + (16u << 16), dp[1]);
+            uint64_t nd[4];  // -D of the thread's column pairs
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
+                nd[j] = f2(-d2.x, -d2.y);
+            }
+            tmem_wait_ld();
+            reg_fence<16>(dp[0]);
+            reg_fence<16>(dp[1]);
+            // every warp holds dP^T: S^T(it+1) may overwrite it
+            tc_fence_before();
+            mbar_arrive(BAR_LD);
+            uint32_t dk[2][8];
+#pragma unroll
+            for (int lb = 0; lb < 2; ++lb)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int rsel = 0; rsel < 2; ++rsel) {
+                        const int i = 4 * j + 2 * rsel;
+                        float p0, p1, e0, e1;
+                        unpack_op<F16>(pk[lb][2 * j + rsel], p0, p1);
+                        f2_split(mul2(f2(p0, p1),
+                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
+                                           nd[j])), e0, e1);
+                        dk[lb][2 * j + rsel] = pack_op<F16>(e0, e1);
+                    }
             tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
             tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
             tmem_wait_st();

@@ -562,6 +562,22 @@ __device__ __forceinline__ uint32_t pack_op(float lo, float hi) {
     return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
 
+// The two values of a pack_op pair, exactly.
+template <bool F16>
+__device__ __forceinline__ void unpack_op(uint32_t w, float& lo, float& hi) {
+    if (F16) {
+        asm("{\n\t.reg .f16 a, b;\n\t"
+            "mov.b32 {a, b}, %2;\n\t"
+            "cvt.f32.f16 %0, a;\n\t"
+            "cvt.f32.f16 %1, b;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(w));
+    } else {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xFFFF0000u);
+    }
+}
+
 // Load ints once, with a volatile load: the compiler must keep the
 // values in registers instead of re-reading them inside a later loop (a
 // re-read on the softmax warps' critical path cost 4% of a kernel).

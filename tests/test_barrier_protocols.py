@@ -362,12 +362,18 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
 
 
 # -------------------------------------------------------------- dK/dV kernel
-def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, skip_dvd=False):
+def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, skip_dvd=False,
+               p_before_str=False):
     """Sixteen compute warps (g, q): query columns 32g.. of the transposed
     tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  The kernel's
-    protocol (ds_smem False): P^T and dS^T go over the S^T columns a warp
-    read (halves 'p' and 'd'), dV after P^T, dK after dS^T, then dP^T(it+1)
-    over both.  A variant that was tried and measured slower (ds_smem True):
+    protocol (ds_smem False): a warp forms P^T(it) as soon as S^T(it) is in
+    TMEM (barrier STR) and writes it over the S^T columns it read (half 'p'),
+    then, once dP^T(it) is in TMEM (SDF), copies dP^T(it) to registers (LD)
+    and writes dS^T(it) over the other half ('d').  The MMA thread: dV(it)
+    after P^T, S^T(it+1) over dP^T(it) after LD, dK(it) after dS^T, then
+    dP^T(it+1) over P^T(it), dS^T(it).  p_before_str (P^T formed without
+    waiting for S^T) is a planted mistake.  A variant that was tried and
+    measured slower (ds_smem True, with the earlier single-step compute):
     dS^T goes to shared memory instead -- over the stage's dO tile (ds_in_do,
     d = 128) or into a buffer of its own (d = 64) -- once the MMA thread's
     DVD commit after dV(it) has completed, so dP^T(it+1) follows dV(it) and
@@ -375,7 +381,8 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     warps = [(g, q) for g in range(4) for q in range(4)]
 
     def model(rnd):
-        bars = {"KV": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1, "DVD": 1}
+        bars = {"KV": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1, "DVD": 1,
+                "STR": 1}
         for s in range(NST):
             bars[f"STF{s}"] = 1 + 32  # the load, and the 32 lanes' vector writes
             bars[f"STE{s}"] = 1
@@ -436,6 +443,54 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
                 reads["dK"] = f"dK({it - 1})"
             return ("mma", f"dK({it})", reads, {"dK": f"dK({it})"})
 
+        def mma_two_step():
+            yield ("wait", "KV", 0)
+            yield ("wait", "STF0", 0)
+            yield st_mma(0)
+            yield ("commit", "STR", 0)
+            yield dpt_mma(0)
+            yield ("commit", "SDF", 0)
+            for it in range(n_it):
+                s, s2 = it % NST, (it + 1) % NST
+                more = it + 1 < n_it
+                yield ("wait", "PF", it)
+                yield dv_mma(it)
+                if more:
+                    yield ("wait", f"STF{s2}", (it + 1) // NST)
+                    yield ("wait", "LD", it)
+                    yield st_mma(it + 1)  # over dP^T(it)
+                    yield ("commit", "STR", it + 1)
+                if not dk_before_dsf:
+                    yield ("wait", "DSF", it)
+                yield dk_mma(it)
+                yield ("commit", f"STE{s}", it // NST)
+                if more:
+                    yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
+                    yield ("commit", "SDF", it + 1)
+            yield ("commit", "ACC", 0)
+            yield ("wait", "ACC", 0)
+
+        def compute_two_step(g, q):
+            me = f"{g}.{q}"
+            for it in range(n_it):
+                s = it % NST
+                rs, rd = reg_s(it), reg_d(it)
+                if not p_before_str:
+                    yield ("wait", "STR", it)
+                yield ("read", {f"{rs}.{me}.p": f"S^T({it})", f"{rs}.{me}.d": f"S^T({it})",
+                                f"vec{s}": f"lse,D({it})"})
+                yield ("write", {f"{rs}.{me}.p": f"P^T({it})"})
+                yield ("arrive", "PF", 32, it)
+                yield ("wait", "SDF", it)
+                yield ("read", {f"{rd}.{me}.p": f"dP^T({it})", f"{rd}.{me}.d": f"dP^T({it})",
+                                f"vec{s}": f"lse,D({it})"})
+                yield ("arrive", "LD", 32, it)
+                yield ("write", {ds_buf(it, g, q): f"dS^T({it})"})
+                yield ("arrive", "DSF", 32, it)
+            yield ("wait", "ACC", 0)
+            yield ("read", {"dV": f"dV({n_it - 1})", "dK": f"dK({n_it - 1})"})
+            yield ("write", {"Q0": "out"})  # staging in stage 0's tiles
+
         def mma():
             yield ("wait", "KV", 0)
             yield ("wait", "STF0", 0)
@@ -486,9 +541,14 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
             yield ("read", {"dV": f"dV({n_it - 1})", "dK": f"dK({n_it - 1})"})
             yield ("write", {"Q0": "out"})  # staging in stage 0's tiles
 
-        roles = {"prod": producer(), "mma": mma()}
-        for g, q in warps:
-            roles[f"c{g}{q}"] = compute(g, q)
+        if ds_smem:
+            roles = {"prod": producer(), "mma": mma()}
+            for g, q in warps:
+                roles[f"c{g}{q}"] = compute(g, q)
+        else:
+            roles = {"prod": producer(), "mma": mma_two_step()}
+            for g, q in warps:
+                roles[f"c{g}{q}"] = compute_two_step(g, q)
         return bars, roles
 
     return model
@@ -993,6 +1053,11 @@ def test_decode_rescale_without_pv_wait_is_caught():
 def test_dkdv_dk_before_ds_is_caught():
     # dK += dS^T Q issued before the warpgroups have written dS^T
     assert fails_on_some_seed(dkdv_model(4, dk_before_dsf=True))
+
+
+def test_dkdv_p_before_s_ready_is_caught():
+    # P^T formed from the region before S^T has been written there
+    assert fails_on_some_seed(dkdv_model(4, p_before_str=True))
 
 
 @pytest.mark.parametrize("ds_in_do", [True, False])
