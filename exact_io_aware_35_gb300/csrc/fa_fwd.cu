@@ -46,12 +46,17 @@ struct FwdCfg {
     static constexpr int SMEM_Q = 2 * TILE;
     static constexpr int SMEM_KV = NSLOT * TILE;
     // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
-    // o_final[2], mma_done, q_copied
-    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1;
+    // o_final[2], mma_done, q_copied, s_empty[2], pv_done[2]
+    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 2 + 2;
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16;
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
+    // and, at D = 64, P0 [384,448) P1 [448,512): P (fp16 or bf16 pairs) gets
+    // columns of its own instead of overwriting S_t (SPLITP), so the next
+    // score product of a tile need not wait for the P V product before it.
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 256;
+    static constexpr bool SPLITP = (D == 64);
+    static constexpr uint32_t TM_P = 256 + 2 * D;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, copy}
 };
@@ -131,6 +136,9 @@ __global__ void __launch_bounds__(384, 1)
     auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * C::NSLOT + t); };
     const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * C::NSLOT);
     const uint32_t BAR_QC = bar0 + 8u * (8 + 2 * C::NSLOT);  // Q tiles read by the copy warp
+    // SPLITP only: S_t is in the softmax's registers / PV_t has finished
+    auto BAR_SE = [&](int t) { return bar0 + 8u * (9 + 2 * C::NSLOT + t); };
+    auto BAR_PVD = [&](int t) { return bar0 + 8u * (11 + 2 * C::NSLOT + t); };
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -167,6 +175,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(BAR_SF(t), 1);
             mbar_init(BAR_PF(t), 128 + 1);  // the tile's softmax threads and the gate
             mbar_init(BAR_OF(t), 1);
+            mbar_init(BAR_SE(t), 4);  // one arrival per softmax warp of the tile
+            mbar_init(BAR_PVD(t), 1);
         }
         mbar_init(BAR_DONE, 1);
         mbar_init(BAR_QC, 1);
@@ -287,7 +297,8 @@ __global__ void __launch_bounds__(384, 1)
             };
             auto issue_pv = [&](int t, int slot, bool acc) {
                 const uint32_t dO = tbase + C::TM_O + t * D;
-                const uint32_t aP = tbase + C::TM_S + t * kBN;  // P (bf16) over S_t
+                // P: its own columns (SPLITP), else over S_t
+                const uint32_t aP = tbase + (C::SPLITP ? C::TM_P + t * (kBN / 2) : C::TM_S + t * kBN);
                 const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
@@ -295,6 +306,65 @@ __global__ void __launch_bounds__(384, 1)
                                 (acc || ks > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait_warp(BAR_Q(), 0, a.watch, 3);
+            if constexpr (C::SPLITP) {
+                // Per union block u (ring entries 2i, 2i + 1) with next union
+                // block un, tile by tile: S_t(un) once the tile's softmax holds
+                // S_t(u) in registers (s_empty) and K(un) has landed, then
+                // PV_t(u) on p_full(t) (which also says V(u) has landed, the
+                // gate), committed to pv_done(t): the softmax writes P_t and
+                // rescales O_t only after it.
+                int nqk[2] = {0, 0}, cnt[2] = {0, 0};
+                if (ok && u_first >= 0) {
+                    ok = mbar_wait_warp(BAR_KVF(0), 0, a.watch, 4);
+                    if (ok) {
+                        tc_fence_after();
+                        for (int t = 0; t < 2; ++t)
+                            if (blk.has(t, u_first)) {
+                                issue_qk(t, 0);
+                                mma_commit_w(leader, BAR_SF(t));
+                                ++nqk[t];
+                            }
+                        mma_commit_w(leader, BAR_KVE(0));
+                    }
+                }
+                for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
+                    const int un = blk.next(u);
+                    const int vslot = (2 * i + 1) % C::NSLOT;
+                    const int kidx = 2 * i + 2;
+                    const int kslot = kidx % C::NSLOT;
+                    bool k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (un >= 0 && blk.has(t, un)) {
+                            if (nqk[t] > 0 &&
+                                !(ok = mbar_wait_warp(BAR_SE(t), (nqk[t] - 1) & 1, a.watch, 17 + t)))
+                                break;
+                            if (!k_ready) {
+                                if (!(ok = mbar_wait_warp(BAR_KVF(kslot), (kidx / C::NSLOT) & 1,
+                                                          a.watch, 19)))
+                                    break;
+                                k_ready = true;
+                            }
+                            tc_fence_after();
+                            issue_qk(t, kslot);
+                            mma_commit_w(leader, BAR_SF(t));
+                            ++nqk[t];
+                        }
+                        if (blk.has(t, u)) {
+                            if (!(ok = mbar_wait_warp(BAR_PF(t), cnt[t] & 1, a.watch, 6 + 2 * t)))
+                                break;
+                            tc_fence_after();
+                            issue_pv(t, vslot, cnt[t] > 0);
+                            mma_commit_w(leader, BAR_PVD(t));
+                            ++cnt[t];
+                            if (blk.next_of(t, u) < 0) mma_commit_w(leader, BAR_OF(t));
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_w(leader, BAR_KVE(vslot));
+                    if (un >= 0) mma_commit_w(leader, BAR_KVE(kslot));
+                    u = un;
+                }
+            } else {
             if (ok && u_first >= 0) {
                 // first union block: the score tiles of the tiles that have it
                 ok = mbar_wait_warp(BAR_KVF(0), 0, a.watch, 4);
@@ -351,6 +421,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 u = un;
             }
+            }  // SPLITP
             // all issued MMAs have finished before TMEM can be released
             mma_commit_w(leader, BAR_DONE);
             mbar_drain(BAR_DONE, 0, a.watch, 9);
@@ -365,6 +436,8 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tbase + C::TM_S + t * kBN + lane_off;
         const uint32_t tO = tbase + C::TM_O + t * D + lane_off;
+        // where P goes: its own columns (SPLITP), else over S_t
+        const uint32_t tP = C::SPLITP ? tbase + C::TM_P + t * (kBN / 2) + lane_off : tS;
         const float sl2 = a.scale_log2;
         int eq = 0, ek = 0, ev = 0, edo = 0;  // fp16 path: O carries 2^ev
         if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
@@ -385,6 +458,11 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld32(tS + 96, s + 96);
             tmem_wait_ld();
             reg_fence<kBN>(s);
+            if constexpr (C::SPLITP) {  // S_t may now be overwritten by the next score product
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR_SE(t));
+            }
             float x[kBN];
 #pragma unroll
             for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
@@ -411,6 +489,10 @@ __global__ void __launch_bounds__(384, 1)
                 l *= alpha;
                 m_ref = m_new;
             }
+            if (C::SPLITP && j > 0) {  // PV_t of the previous block still reads P_t, writes O_t
+                if (!(ok = mbar_wait_warp(BAR_PVD(t), (j - 1) & 1, a.watch, 20 + t))) break;
+                tc_fence_after();
+            }
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
             const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
             uint64_t ls2[4] = {0, 0, 0, 0};  // packed partial row sums
@@ -425,7 +507,7 @@ __global__ void __launch_bounds__(384, 1)
                     ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
                     pk[c >> 1] = pack_op<F16>(p0, p1);
                 }
-                tmem_st32(tS + half * 32, pk);
+                tmem_st32(tP + half * 32, pk);
             }
             {
                 const uint64_t t = add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3]));
@@ -434,7 +516,8 @@ __global__ void __launch_bounds__(384, 1)
                 l += a0 + a1;
             }
             // O_t was last written by the P V product of block j-1, which
-            // completed before this block's scores were committed.
+            // completed before this block's scores were committed (SPLITP:
+            // before pv_done, waited for above).
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
                 for (int cb = 0; cb < D; cb += 32) {

@@ -661,7 +661,8 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
     return model
 
 
-def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
+def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, split_p=False,
+                    mistake=None):
     """The forward kernel's protocol with its key blocks given per tile
     (block-sparse masks; the dense kernel is blocks0 = range(nkv0), blocks1 =
     range(nkv)).  Every role walks the union of the two sets in increasing
@@ -670,7 +671,15 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
     them, PV1(u), V(u)'s slot released, S1(un), then S0(un) when tile 0 had
     no u (deferred behind tile 1's p_full wait, which is the one that says
     K(un) has landed), K(un)'s slot released.  defer_qk0=False issues that
-    S0(un) before tile 1's wait: a planted mistake."""
+    S0(un) before tile 1's wait: a planted mistake.
+
+    split_p: the d = 64 layout, where P_t has TMEM columns of its own.  A
+    softmax warp arrives on s_empty(t) once its rows of S_t are in registers,
+    and waits for pv_done(t) (the tile's previous P V product) before it
+    writes P_t or rescales O_t.  Per union block u the MMA thread issues, per
+    tile, S_t(un) as soon as s_empty(t) and K(un) allow, then PV_t(u) on
+    p_full(t).  mistake plants an error: "no_se_wait", "no_k_wait" or
+    "no_pvd_wait"."""
     rows = range(4)
     sets = (sorted(set(blocks0)), sorted(set(blocks1)))
     union = sorted(set(sets[0]) | set(sets[1]))
@@ -681,6 +690,8 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
     def model(rnd):
         bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
                 "DONE": 1, "QC": 1}
+        if split_p:
+            bars.update({"SE0": 4, "SE1": 4, "PVD0": 1, "PVD1": 1})
         bars.update(ring_bars(NSLOT))
 
         def tile(pre, t, tag):
@@ -727,10 +738,53 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
 
         def pv(t, i, u, prev):
             slot = (2 * i + 1) % NSLOT
-            reads = dict(tile("S", t, f"P({t},{u})"), **{f"kv{slot}": f"V({u})"})
+            reads = dict(tile("P" if split_p else "S", t, f"P({t},{u})"),
+                         **{f"kv{slot}": f"V({u})"})
             if prev is not None:
                 reads.update(tile("O", t, f"O({t},{prev})"))
             return ("mma", f"PV({t},{u})", reads, tile("O", t, f"O({t},{u})"))
+
+        def mma_split():
+            if not union:
+                yield ("commit", "DONE", 0)
+                yield ("wait", "DONE", 0)
+                return
+            yield ("wait", "Q", 0)
+            yield ("wait", "F0", 0)
+            nqk, cnt, prev = [0, 0], [0, 0], [None, None]
+            for t in (0, 1):
+                if has(t, union[0]):
+                    yield qk(t, 0, union[0])
+                    yield ("commit", f"SF{t}", nqk[t])
+                    nqk[t] += 1
+            yield ("commit", "E0", 0)
+            for i, u in enumerate(union):
+                un = union[i + 1] if i + 1 < len(union) else None
+                vslot, kidx = (2 * i + 1) % NSLOT, 2 * i + 2
+                kslot = kidx % NSLOT
+                k_ready = False
+                for t in (0, 1):
+                    if un is not None and has(t, un):
+                        if nqk[t] > 0 and mistake != "no_se_wait":
+                            yield ("wait", f"SE{t}", nqk[t] - 1)
+                        if not k_ready and mistake != "no_k_wait":
+                            yield ("wait", f"F{kslot}", kidx // NSLOT)
+                            k_ready = True
+                        yield qk(t, i + 1, un)
+                        yield ("commit", f"SF{t}", nqk[t])
+                        nqk[t] += 1
+                    if has(t, u):
+                        yield ("wait", f"PF{t}", cnt[t])
+                        yield pv(t, i, u, prev[t])
+                        yield ("commit", f"PVD{t}", cnt[t])
+                        cnt[t], prev[t] = cnt[t] + 1, u
+                        if u == sets[t][-1]:
+                            yield ("commit", f"OF{t}", 0)
+                yield ("commit", f"E{vslot}", (2 * i + 1) // NSLOT)
+                if un is not None:
+                    yield ("commit", f"E{kslot}", kidx // NSLOT)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
 
         def mma():
             if not union:
@@ -791,7 +845,13 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
             for j, u in enumerate(sets[t]):
                 yield ("wait", f"SF{t}", j)
                 yield ("read", {f"S.{me}": f"S({t},{u})"})
-                yield ("write", {f"S.{me}": f"P({t},{u})"})
+                if split_p:
+                    yield ("arrive", f"SE{t}", 1, j)
+                    if j > 0 and mistake != "no_pvd_wait":
+                        yield ("wait", f"PVD{t}", j - 1)
+                    yield ("write", {f"P.{me}": f"P({t},{u})"})
+                else:
+                    yield ("write", {f"S.{me}": f"P({t},{u})"})
                 if prev is not None and rnd.random() < 0.5:  # the reference max moved
                     yield ("read", {f"O.{me}": f"O({t},{prev})"})
                     yield ("write", {f"O.{me}": f"O({t},{prev})"})
@@ -806,12 +866,169 @@ def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True):
                 yield ("wait", "QC", 0)
             yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
 
-        roles = {"prod": producer(), "gate": gate(), "mma": mma()}
+        roles = {"prod": producer(), "gate": gate(), "mma": mma_split() if split_p else mma()}
         for t in (0, 1):
             for q in rows:
                 roles[f"s{t}{q}"] = softmax(t, q)
         if copy_q:
             roles["copy"] = copy()
+        return bars, roles
+
+    return model
+
+
+def stream_entries(sets):
+    """Ring order of the block-sparse forward: K_0(0), K_1(0), then per step k,
+    tile by tile, V_t(k) and K_t(k+1) of the tiles that still have blocks (a
+    tile's k-th block is the k-th of its own set)."""
+    cnt = [len(sets[0]), len(sets[1])]
+    seq = [(t, "K", 0) for t in (0, 1) if cnt[t] > 0]
+    for k in range(max(cnt)):
+        for t in (0, 1):
+            if k < cnt[t]:
+                seq.append((t, "V", k))
+                if k + 1 < cnt[t]:
+                    seq.append((t, "K", k + 1))
+    return {e: i for i, e in enumerate(seq)}
+
+
+def fwd_stream_model(blocks0, blocks1, NSLOT=4, split_p=False, mistake=None):
+    """The block-sparse forward: each query tile streams K and V of its own
+    key blocks (no sharing between the tiles), all through one ring in the
+    order stream_entries gives; the two tiles advance by step k (the k-th block
+    of each), with the dense kernel's per-tile order: PV_t(k) then S_t(k+1)
+    (split_p: S_t(k+1) first, behind s_empty(t) and its K landing).  The
+    gate adds to p_full(t) once V_t(k) and K_t(k+1) have landed.  mistake:
+    "no_kve_order" releases V_t(k)'s slot before PV_t(k) is issued;
+    "shared_index" gives tile 1 tile 0's ring entries."""
+    rows = range(4)
+    sets = (sorted(set(blocks0)), sorted(set(blocks1)))
+    cnt = [len(sets[0]), len(sets[1])]
+    idx = stream_entries(sets)
+    if mistake == "shared_index":
+        idx = {(t, w, k): idx.get((0, w, k), i) for (t, w, k), i in idx.items()}
+
+    def model(rnd):
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+                "DONE": 1, "SE0": 4, "SE1": 4, "PVD0": 1, "PVD1": 1}
+        bars.update(ring_bars(NSLOT))
+
+        def tile(pre, t, tag):
+            return {f"{pre}.{t}.{q}": tag for q in rows}
+
+        def ent(t, w, k):
+            e = idx[(t, w, k)]
+            return e % NSLOT, e // NSLOT
+
+        def name(t, w, k):
+            return f"{w}{t}({sets[t][k]})"
+
+        def producer():
+            last = {}
+            yield ("load", "Q", 0, dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
+            for (t, w, k), e in sorted(stream_entries(sets).items(), key=lambda x: x[1]):
+                s = e % NSLOT
+                yield ("wait", f"E{s}", e // NSLOT - 1)
+                yield ("load", f"F{s}", e // NSLOT, {f"kv{s}": name(t, w, k)})
+                last[s] = e // NSLOT
+            yield ("wait", "Q", 0)
+            for s, ph in last.items():
+                yield ("wait", f"F{s}", ph)
+
+        def gate():
+            for k in range(max(cnt, default=0)):
+                for t in (0, 1):
+                    if k >= cnt[t]:
+                        continue
+                    s, ph = ent(t, "V", k)
+                    yield ("wait", f"F{s}", ph)
+                    if k + 1 < cnt[t]:
+                        s, ph = ent(t, "K", k + 1)
+                        yield ("wait", f"F{s}", ph)
+                    if k > 0:
+                        yield ("wait", f"PF{t}", k - 1)
+                    yield ("arrive", f"PF{t}", 1, k)
+
+        def qk(t, k):
+            s, _ = ent(t, "K", k)
+            return ("mma", f"QK{t}({k})", dict(tile("Q", t, "Q"), **{f"kv{s}": name(t, "K", k)}),
+                    tile("S", t, f"S{t}({k})"))
+
+        def pv(t, k):
+            s, _ = ent(t, "V", k)
+            reads = dict(tile("P" if split_p else "S", t, f"P{t}({k})"),
+                         **{f"kv{s}": name(t, "V", k)})
+            if k > 0:
+                reads.update(tile("O", t, f"O{t}({k - 1})"))
+            return ("mma", f"PV{t}({k})", reads, tile("O", t, f"O{t}({k})"))
+
+        def release(t, w, k):
+            s, ph = ent(t, w, k)
+            return ("commit", f"E{s}", ph)
+
+        def mma():
+            yield ("wait", "Q", 0)
+            for t in (0, 1):
+                if cnt[t] > 0:
+                    s, ph = ent(t, "K", 0)
+                    yield ("wait", f"F{s}", ph)
+                    yield qk(t, 0)
+                    yield ("commit", f"SF{t}", 0)
+                    yield release(t, "K", 0)
+            for k in range(max(cnt, default=0)):
+                for t in (0, 1):
+                    if split_p and k + 1 < cnt[t]:
+                        yield ("wait", f"SE{t}", k)
+                        s, ph = ent(t, "K", k + 1)
+                        yield ("wait", f"F{s}", ph)
+                        yield qk(t, k + 1)
+                        yield ("commit", f"SF{t}", k + 1)
+                        yield release(t, "K", k + 1)
+                    if k < cnt[t]:
+                        if mistake == "no_kve_order":
+                            yield release(t, "V", k)
+                        yield ("wait", f"PF{t}", k)
+                        yield pv(t, k)
+                        if split_p:
+                            yield ("commit", f"PVD{t}", k)
+                        if mistake != "no_kve_order":
+                            yield release(t, "V", k)
+                        if k == cnt[t] - 1:
+                            yield ("commit", f"OF{t}", 0)
+                    if not split_p and k + 1 < cnt[t]:
+                        yield qk(t, k + 1)
+                        yield ("commit", f"SF{t}", k + 1)
+                        yield release(t, "K", k + 1)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def softmax(t, q):
+            me = f"{t}.{q}"
+            for k in range(cnt[t]):
+                yield ("wait", f"SF{t}", k)
+                yield ("read", {f"S.{me}": f"S{t}({k})"})
+                if split_p:
+                    yield ("arrive", f"SE{t}", 1, k)
+                    if k > 0:
+                        yield ("wait", f"PVD{t}", k - 1)
+                    yield ("write", {f"P.{me}": f"P{t}({k})"})
+                else:
+                    yield ("write", {f"S.{me}": f"P{t}({k})"})
+                if k > 0 and rnd.random() < 0.5:  # the reference max moved
+                    yield ("read", {f"O.{me}": f"O{t}({k - 1})"})
+                    yield ("write", {f"O.{me}": f"O{t}({k - 1})"})
+                yield ("arrive", f"PF{t}", 32, k)
+            if cnt[t]:
+                yield ("wait", f"OF{t}", 0)
+                yield ("read", {f"O.{me}": f"O{t}({cnt[t] - 1})"})
+            else:  # a tile with no block stages zeros, once its Q tile has landed
+                yield ("wait", "Q", 0)
+            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
+
+        roles = {"prod": producer(), "gate": gate(), "mma": mma()}
+        for t in (0, 1):
+            for q in rows:
+                roles[f"s{t}{q}"] = softmax(t, q)
         return bars, roles
 
     return model
@@ -999,6 +1216,50 @@ def test_forward_union_random_masks():
         b0 = [u for u in range(nb) if rnd.random() < 0.4]
         b1 = [u for u in range(nb) if rnd.random() < 0.4]
         each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8))), seeds=range(8))
+
+
+@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES + [(range(16), range(16), 8)])
+@pytest.mark.parametrize("copy_q", [False, True])
+def test_forward_split_p_protocol(b0, b1, nslot, copy_q):
+    each_seed(fwd_union_model(b0, b1, nslot, copy_q, split_p=True))
+
+
+def test_forward_split_p_random_masks():
+    rnd = random.Random(7)
+    for _ in range(40):
+        nb = rnd.randrange(1, 12)
+        b0 = [u for u in range(nb) if rnd.random() < 0.4]
+        b1 = [u for u in range(nb) if rnd.random() < 0.4]
+        each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8)), split_p=True), seeds=range(8))
+
+
+@pytest.mark.parametrize("mistake", ["no_se_wait", "no_k_wait", "no_pvd_wait"])
+def test_forward_split_p_planted_mistakes_are_caught(mistake):
+    assert fails_on_some_seed(fwd_union_model(range(6), range(6), 8, split_p=True,
+                                              mistake=mistake))
+
+
+@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES + [([0, 3, 4, 9], [1, 2, 3, 4, 5, 6, 8], 5),
+                                                 ([0, 1, 2], [0, 1, 2], 5)])
+@pytest.mark.parametrize("split_p", [False, True])
+def test_forward_stream_protocol(b0, b1, nslot, split_p):
+    each_seed(fwd_stream_model(b0, b1, nslot, split_p))
+
+
+def test_forward_stream_random_masks():
+    rnd = random.Random(11)
+    for _ in range(40):
+        nb = rnd.randrange(1, 14)
+        b0 = [u for u in range(nb) if rnd.random() < 0.5]
+        b1 = [u for u in range(nb) if rnd.random() < 0.5]
+        each_seed(fwd_stream_model(b0, b1, rnd.choice((4, 5, 8)), rnd.random() < 0.5),
+                  seeds=range(8))
+
+
+@pytest.mark.parametrize("mistake", ["no_kve_order", "shared_index"])
+def test_forward_stream_planted_mistakes_are_caught(mistake):
+    assert fails_on_some_seed(fwd_stream_model([0, 2, 3, 5], [1, 2, 4, 5, 6], 4,
+                                               mistake=mistake))
 
 
 def test_forward_union_early_score_of_the_idle_tile_is_caught():
