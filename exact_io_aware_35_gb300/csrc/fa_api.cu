@@ -48,6 +48,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool ready = false;
     bool supported = false;
+    int num_sms = 0;
     uint32_t* status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -69,6 +70,8 @@ fa_status device_ready(DeviceInfo** out) {
         if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
         di.supported = (major == 10 && minor == 3);
+        if ((e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
         if (di.supported) {
             void* p = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess)
@@ -259,8 +262,8 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     } else if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) {
         return st;
     }
-    if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
     FwdArgs a;
+    a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.o_lo = static_cast<uint16_t*>(o_lo);
     a.f16s = workspace ? at<const F16Scales>(workspace, wl.scales) : nullptr;
@@ -273,6 +276,7 @@ fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, voi
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
+    a.num_ctas = di->num_sms;
     a.block_mask = nullptr;
     a.watch = make_watch(di->status);
     cudaError_t e = launch_fwd(maps, a, d, cs);
@@ -531,9 +535,9 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
     if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
     if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
     if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
-    if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
     // the forward kernel, each of its two query tiles walking its own mask row
     FwdArgs a;
+    a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.o_lo = nullptr;
     a.f16s = nullptr;
@@ -546,6 +550,7 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
     a.causal = causal ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
+    a.num_ctas = di->num_sms;
     a.block_mask = block_mask;
     a.watch = make_watch(di->status);
     const cudaError_t e = launch_fwd(maps, a, d, static_cast<cudaStream_t>(stream));

@@ -1,10 +1,10 @@
 // fa_fwd.cu -- exact attention forward for sm_103a (tcgen05 + TMEM + TMA).
 //
 // What it computes: O = softmax(scale * Q K^T [+ causal mask]) V and the
-// per-row log-sum-exp, one (batch, head, 256-query block) per thread block,
-// streaming 128-key blocks of K and V and folding each block into running
-// row statistics with the online-softmax update of "FlashAttention and the
-// Kernel Era", section "The Mathematics" (m_new = max(m, max S_j),
+// per-row log-sum-exp, one (batch, head, 256-query block) work item at a
+// time, streaming 128-key blocks of K and V and folding each block into
+// running row statistics with the online-softmax update of "FlashAttention
+// and the Kernel Era", section "The Mathematics" (m_new = max(m, max S_j),
 // l_new = l * e^{m - m_new} + sum e^{S_j - m_new}) and the output update of
 // "FlashAttention 1, 2, and 3 Explained", section 2
 // (O_new = diag(e^{m_old - m_new}) O_old + P_j V_j).  The N x N score matrix
@@ -12,10 +12,17 @@
 //
 // How it maps to sm_103a (a redesign for Blackwell, not the pages' A100/H100
 // kernels):
-//   * each CTA holds two 128-row query tiles (Q0, Q1) in shared memory and
-//     streams K_j, V_j through a ring of TMA-filled shared-memory slots;
-//   * one thread issues every tcgen05.mma: S_t = Q_t K_j^T into TMEM, then
-//     O_t += P_t V_j with P_t read straight from TMEM (bf16, written over S_t);
+//   * persistent CTAs, one per SM, each walking work items (longest first);
+//     the K/V ring, the barrier phases and TMEM run on from one item to the
+//     next, so an item's Q and first K/V loads and first score product
+//     overlap the previous item's last blocks and epilogue;
+//   * each item is two 128-row query tiles (Q0, Q1) in shared memory; K_j,
+//     V_j stream through a ring of TMA-filled shared-memory slots;
+//   * S_t = Q_t K_j^T and O_t += P_t V_j on the tensor core, accumulators and
+//     P in TMEM.  At d = 128 one thread issues every product, P overwrites
+//     S_t, and S_t(j+1) follows PV_t(j); at d = 64 P has TMEM columns of its
+//     own and each tile has its own issuing thread, which issues S_t(j+1) as
+//     soon as the softmax holds S_t(j) in registers;
 //   * two softmax warpgroups, one per query tile, each thread owning one
 //     query row (one TMEM lane): load S, mask, row max, exp2, row sum, write P
 //     back to TMEM; while one warpgroup does its softmax the tensor core works
@@ -27,48 +34,53 @@
 //     exact (only the headroom of fp32 changes);
 //   * causal: blocks above the diagonal are never loaded or multiplied;
 //     only the diagonal block is masked element by element;
-//   * the epilogue divides O by l, rounds to bf16, stages the tile in the
-//     (now free) Q buffer with the 128-byte swizzle and writes it with one TMA
-//     store; lse = (m + log2 l) * ln 2.  The training forward also writes
-//     o_lo = bf16(O32 - O), the rounding residual of O, with plain stores.
+//   * the epilogue divides O by l, rounds to bf16 and writes each row from
+//     its thread's registers straight to global memory (no staging, so the
+//     Q buffers are free for the next item); lse = (m + log2 l) * ln 2.  The
+//     training forward also writes o_lo = bf16(O32 - O), the rounding
+//     residual of O, and the fp16 copy of Q for the backward.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
 namespace {
 
-template <int D>
+template <int D, bool SPARSE>
 struct FwdCfg {
     static constexpr int CHUNK = kBM * 128;          // one 64-column chunk of a 128-row tile
     static constexpr int NCH = D / 64;               // chunks per tile
     static constexpr int TILE = NCH * CHUNK;         // bytes of a 128 x D bf16 tile
-    static constexpr int NSLOT = (D == 128) ? 4 : 8; // K/V ring slots
+    static constexpr int NSLOT = (D == 128) ? 4 : 8;  // K/V ring slots
     static constexpr int SMEM_Q = 2 * TILE;
     static constexpr int SMEM_KV = NSLOT * TILE;
-    // barriers: q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
-    // o_final[2], mma_done, q_copied, s_empty[2], pv_done[2]
-    static constexpr int NBAR = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 2 + 2;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SMEM_Q + SMEM_KV + NBAR * 8 + 16;
+    // the epilogue's per-warp transpose buffers: 32 rows x 64 bytes per softmax warp
+    static constexpr int SMEM_STAGE = 8 * 2048;
+    // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
+    // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done
+    static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1;
+    static constexpr int SMEM_BYTES =
+        1024 /*align slack*/ + SMEM_Q + SMEM_KV + SMEM_STAGE + NBAR * 8 + 16;
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
     // and, at D = 64, P0 [384,448) P1 [448,512): P (fp16 or bf16 pairs) gets
-    // columns of its own instead of overwriting S_t (SPLITP), so the next
-    // score product of a tile need not wait for the P V product before it.
+    // columns of its own instead of overwriting S_t (SPLITP).
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 256;
     static constexpr bool SPLITP = (D == 64);
     static constexpr uint32_t TM_P = 256 + 2 * D;
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int THREADS = 384;              // softmax WG0, WG1, WG2 = {MMA, TMA, gate, copy}
+    static constexpr int THREADS = 384;  // softmax WG0, WG1, WG2 = {MMA, TMA, gate/MMA 1, copy}
+    // dense SPLITP: both tiles' issuers release every shared ring entry
+    static constexpr uint32_t KVE_COUNT = (SPLITP && !SPARSE) ? 2u : 1u;
 };
 
-constexpr int kWarpMma = 8;
+constexpr int kWarpMma = 8;   // the MMA issuer (tile 0's at d = 64); allocates TMEM
 constexpr int kWarpLoad = 9;
-// The gate warp folds "K/V tiles landed" into the p_full barriers, so the MMA
-// thread waits on two barriers per key block instead of four: every mbarrier
-// wait in the issuing thread costs tensor-core time.
+// d = 128: the gate warp folds "K/V tiles landed" into the p_full barriers,
+// so the MMA thread waits on two barriers per key block instead of four.
+// d = 64: tile 1's MMA issuer.
 constexpr int kWarpGate = 10;
-// The training forward's copy warp writes the fp16 copy of the CTA's Q tiles
-// (for the backward) while the tiles sit in shared memory anyway.
+// The training forward's copy warp writes the fp16 copy of the item's Q
+// tiles (for the backward) while the tiles sit in shared memory anyway.
 constexpr int kWarpCopy = 11;
 
 // Row-max and exp threshold for the lazy rescale: the reference max is only
@@ -76,12 +88,17 @@ constexpr int kWarpCopy = 11;
 // units), so unnormalised P values stay below 256.
 constexpr float kRescaleThreshold = 8.0f;
 
-// The key blocks the CTA's two query tiles multiply.  Tile t takes the
+// The key blocks an item's two query tiles multiply.  Tile t takes the
 // blocks below n[t] (the causal diagonal or the ragged end), and, with a block
-// mask (SPARSE), only those whose mask byte is set.  Every role walks the
-// union of the two tiles' blocks in increasing order, the i-th union block
-// occupying ring entries 2i (K) and 2i + 1 (V); without a mask the union is
-// 0 .. n[1] - 1 and tile 0 just stops one block early on the diagonal.
+// mask (SPARSE), only those whose mask byte is set.
+//   Dense: the tiles share K_j, V_j; every role walks j = 0 .. n[1] - 1, block
+//   j in the item's ring entries 2j (K) and 2j + 1 (V), and tile 0 just stops
+//   one block early on the diagonal.
+//   SPARSE: each tile streams the K and V of its own blocks (the two mask
+//   rows differ, and a shared walk would idle one tile on every block only
+//   the other has).  The tiles advance by step k, the k-th block of each; the
+//   ring holds K_0(0), K_1(0), then per step, tile by tile, V_t(k) and
+//   K_t(k+1) of the tiles that still have blocks.
 template <bool SPARSE>
 struct TileBlocks {
     int n[2];
@@ -89,16 +106,6 @@ struct TileBlocks {
     __device__ __forceinline__ bool has(int t, int u) const {
         if (u >= n[t]) return false;
         return SPARSE ? (row[t] != nullptr && row[t][u] != 0) : true;
-    }
-    __device__ __forceinline__ int next(int u) const {  // next union block after u, or -1
-        if constexpr (!SPARSE) {
-            return u + 1 < n[1] ? u + 1 : -1;
-        } else {
-            const int hi = max(n[0], n[1]);
-            for (++u; u < hi; ++u)
-                if (has(0, u) || has(1, u)) return u;
-            return -1;
-        }
     }
     __device__ __forceinline__ int next_of(int t, int u) const {  // tile t's next block, or -1
         if constexpr (!SPARSE) {
@@ -109,6 +116,35 @@ struct TileBlocks {
             return -1;
         }
     }
+    __device__ __forceinline__ int first_of(int t) const {  // tile t's first block, or -1
+        return has(t, 0) ? 0 : next_of(t, 0);
+    }
+};
+
+// One work item: (batch, head, 256-query block), longest blocks first, the
+// heads of one KV group adjacent.
+template <bool SPARSE>
+struct Item {
+    int b, h, hk, row0;
+    TileBlocks<SPARSE> blk;
+    __device__ __forceinline__ Item(int w, const FwdArgs& a) {
+        const int per = a.B * a.Hq;
+        const int qb = a.n_qblk - 1 - w / per;
+        const int bh = w % per;
+        b = bh / a.Hq;
+        h = bh % a.Hq;
+        hk = h / a.g;
+        row0 = qb * 2 * kBM;
+        const int nkv_all = (a.N + kBN - 1) / kBN;
+        blk.n[0] = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
+        blk.n[1] = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
+        blk.row[0] = blk.row[1] = nullptr;
+        if (SPARSE)
+            for (int t = 0; t < 2; ++t)
+                if (2 * qb + t < nkv_all)
+                    blk.row[t] =
+                        a.block_mask + (static_cast<size_t>(h) * nkv_all + 2 * qb + t) * nkv_all;
+    }
 };
 
 // F16: P is rounded to fp16 (not bf16) and multiplies the fp16 copy of V,
@@ -117,69 +153,52 @@ struct TileBlocks {
 template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FwdArgs a) {
-    using C = FwdCfg<D>;
+                  const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+    using C = FwdCfg<D, SPARSE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + C::SMEM_Q;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_KV);
+    const uint32_t sStage = sKV + C::SMEM_KV;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_KV + C::SMEM_STAGE);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
     const uint32_t bar0 = smem_u32(bars);
-    auto BAR_Q = [&]() { return bar0; };
-    auto BAR_KVF = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto BAR_KVE = [&](int s) { return bar0 + 8u * (1 + C::NSLOT + s); };
-    auto BAR_SF = [&](int t) { return bar0 + 8u * (1 + 2 * C::NSLOT + t); };
-    auto BAR_PF = [&](int t) { return bar0 + 8u * (3 + 2 * C::NSLOT + t); };
-    auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * C::NSLOT + t); };
-    const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * C::NSLOT);
-    const uint32_t BAR_QC = bar0 + 8u * (8 + 2 * C::NSLOT);  // Q tiles read by the copy warp
+    const uint32_t BAR_Q = bar0;        // the item's Q tiles landed
+    const uint32_t BAR_QE = bar0 + 8u;  // the item's Q tiles no longer read
+    auto BAR_KVF = [&](int s) { return bar0 + 8u * (2 + s); };
+    auto BAR_KVE = [&](int s) { return bar0 + 8u * (2 + C::NSLOT + s); };
+    auto BAR_SF = [&](int t) { return bar0 + 8u * (2 + 2 * C::NSLOT + t); };
+    auto BAR_PF = [&](int t) { return bar0 + 8u * (4 + 2 * C::NSLOT + t); };
+    auto BAR_OF = [&](int t) { return bar0 + 8u * (6 + 2 * C::NSLOT + t); };
     // SPLITP only: S_t is in the softmax's registers / PV_t has finished
-    auto BAR_SE = [&](int t) { return bar0 + 8u * (9 + 2 * C::NSLOT + t); };
-    auto BAR_PVD = [&](int t) { return bar0 + 8u * (11 + 2 * C::NSLOT + t); };
+    auto BAR_SE = [&](int t) { return bar0 + 8u * (8 + 2 * C::NSLOT + t); };
+    auto BAR_PVD = [&](int t) { return bar0 + 8u * (10 + 2 * C::NSLOT + t); };
+    const uint32_t BAR_DONE = bar0 + 8u * (12 + 2 * C::NSLOT);
 
     const int warp = warp_id();
     const int lane = lane_id();
-
-    // ---- work decode: longest query blocks first, heads of one KV group adjacent
-    const int per = a.B * a.Hq;
-    const int qb = a.n_qblk - 1 - static_cast<int>(blockIdx.x) / per;
-    const int bh = static_cast<int>(blockIdx.x) % per;
-    const int b = bh / a.Hq;
-    const int h = bh % a.Hq;
-    const int hk = h / a.g;
-    const int row0 = qb * 2 * kBM;
-    const int nkv_all = (a.N + kBN - 1) / kBN;
-    // key blocks below each query tile's limit (causal: up to and including its
-    // diagonal), and with a mask only those it selects
-    TileBlocks<SPARSE> blk;
-    blk.n[0] = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
-    blk.n[1] = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
-    blk.row[0] = blk.row[1] = nullptr;
-    if (SPARSE)
-        for (int t = 0; t < 2; ++t)
-            if (2 * qb + t < nkv_all)
-                blk.row[t] = a.block_mask + (static_cast<size_t>(h) * nkv_all + 2 * qb + t) * nkv_all;
-    const int u_first = SPARSE ? blk.next(-1) : 0;  // first union block (-1: none)
+    const int n_items = a.n_qblk * a.B * a.Hq;
+    const bool copy_q = F16 && a.q16 != nullptr;
+    constexpr int kIssuers = C::SPLITP ? 2 : 1;
 
     // ---- set-up
     if (warp == 0 && lane == 0) {
-        mbar_init(BAR_Q(), 1);
+        mbar_init(BAR_Q, 1);
+        mbar_init(BAR_QE, kIssuers + (copy_q ? 1 : 0));
         for (int s = 0; s < C::NSLOT; ++s) {
             mbar_init(BAR_KVF(s), 1);
-            mbar_init(BAR_KVE(s), 1);
+            mbar_init(BAR_KVE(s), C::KVE_COUNT);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(BAR_SF(t), 1);
-            mbar_init(BAR_PF(t), 128 + 1);  // the tile's softmax threads and the gate
+            // the tile's softmax threads, and at d = 128 the gate
+            mbar_init(BAR_PF(t), C::SPLITP ? 128 : 128 + 1);
             mbar_init(BAR_OF(t), 1);
             mbar_init(BAR_SE(t), 4);  // one arrival per softmax warp of the tile
             mbar_init(BAR_PVD(t), 1);
         }
-        mbar_init(BAR_DONE, 1);
-        mbar_init(BAR_QC, 1);
+        mbar_init(BAR_DONE, kIssuers);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -190,249 +209,358 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // Registers: the launch gives every thread 168 (384 x 168 = 64,512); each
+    // role below starts by moving its warpgroup's share: the softmax
+    // warpgroups, which hold a 128-column row each, take 208 and the issue /
+    // copy warpgroup keeps 80 (2 x 128 x 208 + 128 x 80 = 63,488).
+
+    constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
+    constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
+    constexpr uint32_t HI = sdesc_hi(1024);
+    // S_t = Q_t K^T from the K tile in ring slot `slot`
+    auto issue_qk = [&](uint32_t leader, int t, int slot) {
+        const uint32_t dS = tbase + C::TM_S + t * kBN;
+        const uint32_t a_lo = sdesc_lo(sQ + t * C::TILE, 16);
+        const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, 16);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+            mma_bf16_ss_w(leader, dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK,
+                          ks > 0);
+        }
+    };
+    // O_t (+)= P_t V from the V tile in ring slot `slot`
+    auto issue_pv = [&](uint32_t leader, int t, int slot, bool acc) {
+        const uint32_t dO = tbase + C::TM_O + t * D;
+        const uint32_t aP = tbase + (C::SPLITP ? C::TM_P + t * (kBN / 2) : C::TM_S + t * kBN);
+        const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_bf16_ts_w(leader, dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
+                          (acc || ks > 0) ? 1u : 0u);
+    };
 
     if (warp == kWarpLoad) {
         // ================= TMA producer =================
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            tma_prefetch_desc(&tmO);
             const uint64_t pol_kv = l2_policy_evict_last();
             const uint64_t pol_q = l2_policy_evict_first();
-            mbar_arrive_expect_tx(BAR_Q(), 2 * C::TILE);
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d_hint(sQ + t * C::TILE + c * C::CHUNK, &tmQ, BAR_Q(), c * 64, h,
-                                     row0 + t * kBM, b, pol_q);
             int last_idx[C::NSLOT];
             for (int s = 0; s < C::NSLOT; ++s) last_idx[s] = -1;
             bool ok = true;
-            for (int i = 0, u = u_first; u >= 0 && ok; ++i, u = blk.next(u)) {
-                for (int w = 0; w < 2; ++w) {
-                    const int idx = 2 * i + w;
-                    const int slot = idx % C::NSLOT;
-                    const uint32_t ph = (idx / C::NSLOT) & 1;
-                    if (!mbar_wait(BAR_KVE(slot), ph ^ 1u, a.watch, 1)) {
-                        ok = false;
-                        break;
-                    }
+            int e = 0;   // ring entry, running over the items
+            int it = 0;  // items started
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+                const Item<SPARSE> I(w, a);
+                // the previous item's score products and q copy are done with Q
+                if (it > 0 && !(ok = mbar_wait(BAR_QE, (it - 1) & 1, a.watch, 22))) break;
+                mbar_arrive_expect_tx(BAR_Q, 2 * C::TILE);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d_hint(sQ + t * C::TILE + c * C::CHUNK, &tmQ, BAR_Q, c * 64, I.h,
+                                         I.row0 + t * kBM, I.b, pol_q);
+                auto load = [&](const CUtensorMap* tm, int u) {
+                    const int slot = e % C::NSLOT;
+                    const uint32_t ph = (e / C::NSLOT) & 1;
+                    if (!(ok = mbar_wait(BAR_KVE(slot), ph ^ 1u, a.watch, 1))) return;
                     mbar_arrive_expect_tx(BAR_KVF(slot), C::TILE);
-                    const CUtensorMap* tm = w ? &tmV : &tmK;
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_4d_hint(sKV + slot * C::TILE + c * C::CHUNK, tm, BAR_KVF(slot),
-                                         c * 64, hk, u * kBN, b, pol_kv);
-                    last_idx[slot] = idx;
+                                         c * 64, I.hk, u * kBN, I.b, pol_kv);
+                    last_idx[slot] = e++;
+                };
+                if constexpr (SPARSE) {
+                    int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                    for (int t = 0; t < 2 && ok; ++t)
+                        if (u[t] >= 0) load(&tmK, u[t]);
+                    while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (u[t] < 0) continue;
+                            load(&tmV, u[t]);
+                            const int un = I.blk.next_of(t, u[t]);
+                            if (ok && un >= 0) load(&tmK, un);
+                            u[t] = un;
+                        }
+                    }
+                } else {
+                    for (int u = 0; u < I.blk.n[1] && ok; ++u) {
+                        load(&tmK, u);
+                        if (ok) load(&tmV, u);
+                    }
                 }
             }
             // Never leave the CTA with copies in flight: wait (bounded) for the
-            // last load issued into every slot, and for Q.
-            mbar_drain(BAR_Q(), 0, a.watch, 2);
+            // last load issued into every slot, and for the last Q.
+            if (it > 0) mbar_drain(BAR_Q, (it - 1) & 1, a.watch, 2);
             for (int s = 0; s < C::NSLOT; ++s)
                 if (last_idx[s] >= 0)
                     mbar_drain(BAR_KVF(s), (last_idx[s] / C::NSLOT) & 1, a.watch, 2);
         }
         __syncwarp();
+    } else if ((warp == kWarpMma || warp == kWarpGate) && C::SPLITP) {
+        // ================= d = 64: tile t's MMA issuer (warp-wide; the leader issues) ======
+        // Per block k of the tile: S_t(k+1) once the softmax holds S_t(k) in
+        // registers (s_empty) and K(k+1) has landed, then PV_t(k) on p_full(t)
+        // once V(k) has landed, committed to pv_done(t): the softmax writes
+        // P_t and rescales O_t only after it.  Each ring entry is released
+        // right after the product that reads it (dense entries by both
+        // issuers).
+        setmaxnreg_dec<80>();
+        const int t = (warp == kWarpMma) ? 0 : 1;
+        const uint32_t leader = elect_one();
+        bool ok = true;
+        int e = 0, it = 0, nqk = 0, npv = 0;
+        auto qk = [&](int ek) {  // S_t from ring entry ek
+            if (nqk > 0 && !(ok = mbar_wait_warp(BAR_SE(t), (nqk - 1) & 1, a.watch, 17 + t))) return;
+            if (!(ok = mbar_wait_warp(BAR_KVF(ek % C::NSLOT), (ek / C::NSLOT) & 1, a.watch, 19)))
+                return;
+            tc_fence_after();
+            issue_qk(leader, t, ek % C::NSLOT);
+            mma_commit_w(leader, BAR_SF(t));
+            mma_commit_w(leader, BAR_KVE(ek % C::NSLOT));
+            ++nqk;
+        };
+        auto pv = [&](int ev, bool acc, bool last) {  // O_t (+)= P_t V from ring entry ev
+            if (!(ok = mbar_wait_warp(BAR_KVF(ev % C::NSLOT), (ev / C::NSLOT) & 1, a.watch, 23 + t)))
+                return;
+            if (!(ok = mbar_wait_warp(BAR_PF(t), npv & 1, a.watch, 6 + 2 * t))) return;
+            tc_fence_after();
+            issue_pv(leader, t, ev % C::NSLOT, acc);
+            mma_commit_w(leader, BAR_PVD(t));
+            mma_commit_w(leader, BAR_KVE(ev % C::NSLOT));
+            if (last) mma_commit_w(leader, BAR_OF(t));
+            ++npv;
+        };
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+            const Item<SPARSE> I(w, a);
+            if (!(ok = mbar_wait_warp(BAR_Q, it & 1, a.watch, 3))) break;
+            if constexpr (SPARSE) {
+                // walk both tiles' streams to find this tile's ring entries
+                int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                int ek0 = -1;
+                for (int tt = 0; tt < 2; ++tt)
+                    if (u[tt] >= 0) {
+                        if (tt == t) ek0 = e;
+                        ++e;
+                    }
+                if (ek0 >= 0) qk(ek0);
+                int k = 0;
+                while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                    for (int tt = 0; tt < 2 && ok; ++tt) {
+                        if (u[tt] < 0) continue;
+                        const int ev = e++;
+                        const int un = I.blk.next_of(tt, u[tt]);
+                        const int ek = un >= 0 ? e++ : -1;
+                        if (tt == t) {
+                            if (ek >= 0) qk(ek);
+                            if (ok) pv(ev, k > 0, un < 0);
+                            ++k;
+                        }
+                        u[tt] = un;
+                    }
+                }
+            } else {
+                const int n = I.blk.n[t], n1 = I.blk.n[1];
+                for (int k = 0; k <= n && ok; ++k) {
+                    if (k < n) qk(e + 2 * k);
+                    if (ok && k > 0) pv(e + 2 * (k - 1) + 1, k > 1, k == n);
+                }
+                // tile 0 stops short of tile 1 on the causal diagonal: release
+                // the entries of the blocks past its limit, each once its
+                // slot's previous use has been released (so the arrival
+                // lands in the right phase)
+                if (t == 0)
+                    for (int ee = e + 2 * n; ee < e + 2 * n1 && ok; ++ee) {
+                        const int s = ee % C::NSLOT, ph = ee / C::NSLOT;
+                        if (ph > 0) ok = mbar_wait_warp(BAR_KVE(s), (ph - 1) & 1, a.watch, 25);
+                        if (ok && leader) mbar_arrive(BAR_KVE(s));
+                        __syncwarp();
+                    }
+                e += 2 * n1;
+            }
+            // the item's score products read Q; q_empty lets the producer reload it
+            mma_commit_w(leader, BAR_QE);
+        }
+        // all issued MMAs have finished before TMEM can be released
+        mma_commit_w(leader, BAR_DONE);
+        if (t == 0) mbar_drain(BAR_DONE, 0, a.watch, 9);
+        __syncwarp();
     } else if (warp == kWarpGate) {
-        // ================= gate: loads -> p_full =================
-        // For key block j it waits for V_j and K_{j+1}, then adds one arrival
-        // to p_full(t) for each tile t that multiplies block j, but only once
-        // that barrier's previous phase has completed, so the arrival can
-        // never be counted in the wrong phase.
+        // ================= d = 128 gate: loads -> p_full =================
+        // For block k of tile t it waits for V(k) and K(k+1), then adds one
+        // arrival to p_full(t), but only once that barrier's previous phase
+        // has completed, so the arrival can never be counted in the wrong
+        // phase.
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             bool ok = true;
+            int e = 0;
             int cnt[2] = {0, 0};  // blocks each tile has multiplied so far
-            for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
-                const int un = blk.next(u);
-                const int vidx = 2 * i + 1, kidx = 2 * i + 2;
-                ok = mbar_wait(BAR_KVF(vidx % C::NSLOT), (vidx / C::NSLOT) & 1, a.watch, 5);
-                if (ok && un >= 0)
-                    ok = mbar_wait(BAR_KVF(kidx % C::NSLOT), (kidx / C::NSLOT) & 1, a.watch, 5);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!blk.has(t, u)) continue;
-                    if (cnt[t] > 0) ok = mbar_wait(BAR_PF(t), (cnt[t] - 1) & 1, a.watch, 7);
-                    if (ok) mbar_arrive(BAR_PF(t));
-                    ++cnt[t];
+            auto arrive = [&](int t) {
+                if (ok && cnt[t] > 0) ok = mbar_wait(BAR_PF(t), (cnt[t] - 1) & 1, a.watch, 7);
+                if (ok) mbar_arrive(BAR_PF(t));
+                ++cnt[t];
+            };
+            auto landed = [&](int ee) {
+                if (ok) ok = mbar_wait(BAR_KVF(ee % C::NSLOT), (ee / C::NSLOT) & 1, a.watch, 5);
+            };
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+                const Item<SPARSE> I(w, a);
+                if constexpr (SPARSE) {
+                    int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                    e += (u[0] >= 0) + (u[1] >= 0);  // the K_t(0)
+                    while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (u[t] < 0) continue;
+                            landed(e++);
+                            const int un = I.blk.next_of(t, u[t]);
+                            if (un >= 0) landed(e++);
+                            arrive(t);
+                            u[t] = un;
+                        }
+                    }
+                } else {
+                    const int n1 = I.blk.n[1];
+                    for (int u = 0; u < n1 && ok; ++u) {
+                        landed(e + 2 * u + 1);
+                        if (u + 1 < n1) landed(e + 2 * u + 2);
+                        for (int t = 0; t < 2; ++t)
+                            if (u < I.blk.n[t]) arrive(t);
+                    }
+                    e += 2 * n1;
                 }
-                u = un;
             }
         }
         __syncwarp();
     } else if (warp == kWarpCopy) {
         // ================= copy: Q tiles -> fp16(q * 2^s) =================
-        // Only the training forward (F16 with q16 set); the epilogues, which
-        // stage O in the Q buffers, wait for BAR_QC.
-        if (F16 && a.q16 != nullptr) {
+        // Only the training forward (F16 with q16 set); then q_empty also
+        // waits for this warp.
+        setmaxnreg_dec<80>();
+        if (copy_q) {
             const float mul = pow2f(ld_once(&a.f16s->q));
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
-            if (mbar_wait_warp(BAR_Q(), 0, a.watch, 15)) {
+            int it = 0;
+            for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++it) {
+                const Item<SPARSE> I(w, a);
+                if (!mbar_wait_warp(BAR_Q, it & 1, a.watch, 15)) break;
                 for (int t = 0; t < 2; ++t)
-                    warp_tile_to_f16<D>(sQ + t * C::TILE,
-                                        a.q16 + (static_cast<size_t>(b) * a.N + row0 + t * kBM) *
-                                                    row_el + h * D,
-                                        row_el, a.N - (row0 + t * kBM), mul, lane);
+                    warp_tile_to_f16<D>(
+                        sQ + t * C::TILE,
+                        a.q16 + (static_cast<size_t>(I.b) * a.N + I.row0 + t * kBM) * row_el + I.h * D,
+                        row_el, a.N - (I.row0 + t * kBM), mul, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR_QE);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR_QC);  // also after a failed wait: never blocks the epilogue
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ================= MMA issuer (the whole warp; the leader lane issues) =================
-        {
-            const uint32_t leader = elect_one();
-            constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
-            constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
-            // descriptors built once per tile; each MMA only moves the start address
-            constexpr uint32_t HI = sdesc_hi(1024);
-            const uint32_t q_lo = sdesc_lo(sQ, 16);
-            auto issue_qk = [&](int t, int slot) {
-                const uint32_t dS = tbase + C::TM_S + t * kBN;
-                const uint32_t a_lo = q_lo + ((t * C::TILE) >> 4);
-                const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, 16);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-                    mma_bf16_ss_w(leader, dS, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_QK, ks > 0);
+        // ================= d = 128 MMA issuer (the whole warp; the leader lane issues) ======
+        setmaxnreg_dec<80>();
+        const uint32_t leader = elect_one();
+        bool ok = true;
+        int e = 0, it = 0;
+        int cnt[2] = {0, 0};  // p_full phases waited, per tile
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+            const Item<SPARSE> I(w, a);
+            if (!(ok = mbar_wait_warp(BAR_Q, it & 1, a.watch, 3))) break;
+            if constexpr (SPARSE) {
+                // Per step k, tile by tile: PV_t(k) on p_full(t) (V_t(k) and
+                // K_t(k+1) landed, the gate), then S_t(k+1).  Every ring entry is
+                // released right after the product that reads it.
+                int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (u[t] < 0) continue;
+                    const int ek = e++;
+                    if (!(ok = mbar_wait_warp(BAR_KVF(ek % C::NSLOT), (ek / C::NSLOT) & 1, a.watch, 4)))
+                        break;
+                    tc_fence_after();
+                    issue_qk(leader, t, ek % C::NSLOT);
+                    mma_commit_w(leader, BAR_SF(t));
+                    mma_commit_w(leader, BAR_KVE(ek % C::NSLOT));
                 }
-            };
-            auto issue_pv = [&](int t, int slot, bool acc) {
-                const uint32_t dO = tbase + C::TM_O + t * D;
-                // P: its own columns (SPLITP), else over S_t
-                const uint32_t aP = tbase + (C::SPLITP ? C::TM_P + t * (kBN / 2) : C::TM_S + t * kBN);
-                const uint32_t b_lo = sdesc_lo(sKV + slot * C::TILE, C::CHUNK);
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts_w(leader, dO, aP + ks * 8, sdesc_at(b_lo, HI, ks * 2048), IDESC_PV,
-                                (acc || ks > 0) ? 1u : 0u);
-            };
-            bool ok = mbar_wait_warp(BAR_Q(), 0, a.watch, 3);
-            if constexpr (C::SPLITP) {
-                // Per union block u (ring entries 2i, 2i + 1) with next union
-                // block un, tile by tile: S_t(un) once the tile's softmax holds
-                // S_t(u) in registers (s_empty) and K(un) has landed, then
-                // PV_t(u) on p_full(t) (which also says V(u) has landed, the
-                // gate), committed to pv_done(t): the softmax writes P_t and
-                // rescales O_t only after it.
-                int nqk[2] = {0, 0}, cnt[2] = {0, 0};
-                if (ok && u_first >= 0) {
-                    ok = mbar_wait_warp(BAR_KVF(0), 0, a.watch, 4);
-                    if (ok) {
-                        tc_fence_after();
-                        for (int t = 0; t < 2; ++t)
-                            if (blk.has(t, u_first)) {
-                                issue_qk(t, 0);
-                                mma_commit_w(leader, BAR_SF(t));
-                                ++nqk[t];
-                            }
-                        mma_commit_w(leader, BAR_KVE(0));
-                    }
-                }
-                for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
-                    const int un = blk.next(u);
-                    const int vslot = (2 * i + 1) % C::NSLOT;
-                    const int kidx = 2 * i + 2;
-                    const int kslot = kidx % C::NSLOT;
-                    bool k_ready = false;
+                int k = 0;
+                while (ok && (u[0] >= 0 || u[1] >= 0)) {
                     for (int t = 0; t < 2 && ok; ++t) {
-                        if (un >= 0 && blk.has(t, un)) {
-                            if (nqk[t] > 0 &&
-                                !(ok = mbar_wait_warp(BAR_SE(t), (nqk[t] - 1) & 1, a.watch, 17 + t)))
-                                break;
-                            if (!k_ready) {
-                                if (!(ok = mbar_wait_warp(BAR_KVF(kslot), (kidx / C::NSLOT) & 1,
-                                                          a.watch, 19)))
-                                    break;
-                                k_ready = true;
-                            }
-                            tc_fence_after();
-                            issue_qk(t, kslot);
+                        if (u[t] < 0) continue;
+                        const int ev = e++;
+                        const int un = I.blk.next_of(t, u[t]);
+                        const int ek = un >= 0 ? e++ : -1;
+                        if (!(ok = mbar_wait_warp(BAR_PF(t), cnt[t] & 1, a.watch, 6 + 2 * t))) break;
+                        tc_fence_after();
+                        issue_pv(leader, t, ev % C::NSLOT, k > 0);
+                        mma_commit_w(leader, BAR_KVE(ev % C::NSLOT));
+                        ++cnt[t];
+                        if (un < 0) mma_commit_w(leader, BAR_OF(t));
+                        if (ek >= 0) {
+                            issue_qk(leader, t, ek % C::NSLOT);
                             mma_commit_w(leader, BAR_SF(t));
-                            ++nqk[t];
+                            mma_commit_w(leader, BAR_KVE(ek % C::NSLOT));
                         }
-                        if (blk.has(t, u)) {
-                            if (!(ok = mbar_wait_warp(BAR_PF(t), cnt[t] & 1, a.watch, 6 + 2 * t)))
-                                break;
-                            tc_fence_after();
-                            issue_pv(t, vslot, cnt[t] > 0);
-                            mma_commit_w(leader, BAR_PVD(t));
-                            ++cnt[t];
-                            if (blk.next_of(t, u) < 0) mma_commit_w(leader, BAR_OF(t));
-                        }
+                        u[t] = un;
                     }
-                    if (!ok) break;
-                    mma_commit_w(leader, BAR_KVE(vslot));
-                    if (un >= 0) mma_commit_w(leader, BAR_KVE(kslot));
-                    u = un;
+                    ++k;
                 }
             } else {
-            if (ok && u_first >= 0) {
-                // first union block: the score tiles of the tiles that have it
-                ok = mbar_wait_warp(BAR_KVF(0), 0, a.watch, 4);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t)
-                        if (blk.has(t, u_first)) {
-                            issue_qk(t, 0);
-                            mma_commit_w(leader, BAR_SF(t));
+                // Per key block u (item entries 2u, 2u + 1): PV0(u) and S0(u + 1)
+                // while tile 0 has them, PV1(u), S1(u + 1).  p_full(t) for u also
+                // means V(u) and K(u + 1) have landed (the gate); S_t(u + 1)
+                // follows PV_t(u), which read P_t over S_t.  The item's first
+                // S_t follows the previous item's last PV_t the same way.
+                const int n0 = I.blk.n[0], n1 = I.blk.n[1];
+                if (!(ok = mbar_wait_warp(BAR_KVF(e % C::NSLOT), (e / C::NSLOT) & 1, a.watch, 4)))
+                    break;
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t) {
+                    issue_qk(leader, t, e % C::NSLOT);
+                    mma_commit_w(leader, BAR_SF(t));
+                }
+                mma_commit_w(leader, BAR_KVE(e % C::NSLOT));
+                for (int u = 0; u < n1 && ok; ++u) {
+                    const int vslot = (e + 2 * u + 1) % C::NSLOT;
+                    const int kslot = (e + 2 * u + 2) % C::NSLOT;
+                    if (u < n0) {
+                        if (!(ok = mbar_wait_warp(BAR_PF(0), cnt[0] & 1, a.watch, 6))) break;
+                        tc_fence_after();
+                        issue_pv(leader, 0, vslot, u > 0);
+                        ++cnt[0];
+                        if (u == n0 - 1) mma_commit_w(leader, BAR_OF(0));
+                        if (u + 1 < n0) {
+                            issue_qk(leader, 0, kslot);
+                            mma_commit_w(leader, BAR_SF(0));
                         }
-                    mma_commit_w(leader, BAR_KVE(0));
-                }
-            }
-            // Per union block u (ring entries 2i, 2i + 1), with un the next one:
-            // PV0(u), S0(un), PV1(u), S1(un) for the tiles that have them.  p_full(t)
-            // for u also means V(u) and K(un) have landed (the gate), and at
-            // least one tile has u, so no S(un) is issued before one such wait;
-            // S_t(un) follows PV_t of the tile's last block, which read P_t.
-            int cnt[2] = {0, 0};
-            for (int i = 0, u = u_first; u >= 0 && ok; ++i) {
-                const int un = blk.next(u);
-                const int vslot = (2 * i + 1) % C::NSLOT;
-                const int kslot = (2 * i + 2) % C::NSLOT;
-                const bool h0 = blk.has(0, u), h0n = un >= 0 && blk.has(0, un);
-                if (h0) {
-                    if (!(ok = mbar_wait_warp(BAR_PF(0), cnt[0] & 1, a.watch, 6))) break;
-                    tc_fence_after();
-                    issue_pv(0, vslot, cnt[0] > 0);
-                    ++cnt[0];
-                    if (blk.next_of(0, u) < 0) mma_commit_w(leader, BAR_OF(0));
-                    if (h0n) {
-                        issue_qk(0, kslot);
-                        mma_commit_w(leader, BAR_SF(0));
                     }
-                }
-                if (blk.has(1, u)) {
                     if (!(ok = mbar_wait_warp(BAR_PF(1), cnt[1] & 1, a.watch, 8))) break;
                     tc_fence_after();
-                    issue_pv(1, vslot, cnt[1] > 0);
+                    issue_pv(leader, 1, vslot, u > 0);
                     ++cnt[1];
-                }
-                mma_commit_w(leader, BAR_KVE(vslot));
-                if (blk.has(1, u) && blk.next_of(1, u) < 0) mma_commit_w(leader, BAR_OF(1));
-                if (un >= 0) {
-                    if (blk.has(1, un)) {
-                        issue_qk(1, kslot);
+                    mma_commit_w(leader, BAR_KVE(vslot));
+                    if (u == n1 - 1) mma_commit_w(leader, BAR_OF(1));
+                    if (u + 1 < n1) {
+                        issue_qk(leader, 1, kslot);
                         mma_commit_w(leader, BAR_SF(1));
+                        mma_commit_w(leader, BAR_KVE(kslot));
                     }
-                    if (!h0 && h0n) {
-                        issue_qk(0, kslot);
-                        mma_commit_w(leader, BAR_SF(0));
-                    }
-                    mma_commit_w(leader, BAR_KVE(kslot));
                 }
-                u = un;
+                e += 2 * n1;
             }
-            }  // SPLITP
-            // all issued MMAs have finished before TMEM can be released
-            mma_commit_w(leader, BAR_DONE);
-            mbar_drain(BAR_DONE, 0, a.watch, 9);
+            // the item's score products read Q; q_empty lets the producer reload it
+            mma_commit_w(leader, BAR_QE);
         }
+        // all issued MMAs have finished before TMEM can be released
+        mma_commit_w(leader, BAR_DONE);
+        mbar_drain(BAR_DONE, 0, a.watch, 9);
         __syncwarp();
     } else if (warp < 8) {
         // ================= softmax warpgroups (warps 0-3: tile 0, 4-7: tile 1)
+        setmaxnreg_inc<208>();
         const int t = warp >> 2;               // query tile of this warpgroup
         const int wq = warp & 3;               // its warp owns TMEM lanes 32*wq..32*wq+31
         const int r = wq * 32 + lane;          // row within the tile
-        const int grow = row0 + t * kBM + r;   // query index
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tbase + C::TM_S + t * kBN + lane_off;
         const uint32_t tO = tbase + C::TM_O + t * D + lane_off;
@@ -441,165 +569,182 @@ __global__ void __launch_bounds__(384, 1)
         const float sl2 = a.scale_log2;
         int eq = 0, ek = 0, ev = 0, edo = 0;  // fp16 path: O carries 2^ev
         if (F16) ld_once_v4(&a.f16s->q, eq, ek, ev, edo);
-        // last key index this row may see
-        const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
-        float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
-        float l = 0.f;            // running sum, relative to m_ref
         bool ok = true;
-        const int u0 = blk.has(t, 0) ? 0 : blk.next_of(t, 0);  // the tile's first block
-        int j = 0;                                               // blocks done so far
-        for (int u = u0; u >= 0; u = blk.next_of(t, u), ++j) {
-            if (!(ok = mbar_wait_warp(BAR_SF(t), j & 1, a.watch, 10 + t))) break;
-            tc_fence_after();
-            uint32_t s[kBN];
-            tmem_ld32(tS + 0, s);
-            tmem_ld32(tS + 32, s + 32);
-            tmem_ld32(tS + 64, s + 64);
-            tmem_ld32(tS + 96, s + 96);
-            tmem_wait_ld();
-            reg_fence<kBN>(s);
-            if constexpr (C::SPLITP) {  // S_t may now be overwritten by the next score product
+        int nsf = 0, npf = 0, nof = 0;  // phases of s_full, p_full, o_final so far
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+            const Item<SPARSE> I(w, a);
+            const int grow = I.row0 + t * kBM + r;  // query index
+            // last key index this row may see
+            const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+            float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
+            float l = 0.f;            // running sum, relative to m_ref
+            const int u0 = I.blk.first_of(t);
+            int j = 0;  // blocks of this item done so far
+            for (int u = u0; u >= 0; u = I.blk.next_of(t, u), ++j) {
+                if (!(ok = mbar_wait_warp(BAR_SF(t), nsf & 1, a.watch, 10 + t))) break;
+                ++nsf;
+                tc_fence_after();
+                uint32_t s[kBN];
+                tmem_ld32(tS + 0, s);
+                tmem_ld32(tS + 32, s + 32);
+                tmem_ld32(tS + 64, s + 64);
+                tmem_ld32(tS + 96, s + 96);
+                tmem_wait_ld();
+                reg_fence<kBN>(s);
+                if constexpr (C::SPLITP) {  // S_t may now be overwritten by the next score product
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR_SE(t));
+                }
+                float x[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
+                const int kbase = u * kBN;
+                if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+                }
+                // row max: eight running maxima, three-input max instructions
+                float mk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
+#pragma unroll
+                for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
+                const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                                       fmaxf(mk[6], mk[7]));
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool need = m_new > m_ref + kRescaleThreshold;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                // SPLITP: PV_t of the previous block still reads P_t and writes
+                // O_t (the item's first block: the epilogue already waited for
+                // the previous item's last one)
+                if (C::SPLITP && j > 0) {
+                    if (!(ok = mbar_wait_warp(BAR_PVD(t), (npf - 1) & 1, a.watch, 20 + t))) break;
+                    tc_fence_after();
+                }
+                const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+                uint64_t ls2[4] = {0, 0, 0, 0};  // packed partial row sums
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        float e0, e1;
+                        f2_split(fma2(f2(x[half * 64 + c], x[half * 64 + c + 1]), sl2x2, negx2), e0,
+                                 e1);
+                        const float p0 = ex2(e0), p1 = ex2(e1);
+                        ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
+                        pk[c >> 1] = pack_op<F16>(p0, p1);
+                    }
+                    tmem_st32(tP + half * 32, pk);
+                }
+                {
+                    const uint64_t sum2 = add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3]));
+                    float a0, a1;
+                    f2_split(sum2, a0, a1);
+                    l += a0 + a1;
+                }
+                // O_t was last written by the P V product of block j-1, which
+                // completed before this block's scores were committed (SPLITP:
+                // before pv_done, waited for above).
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int cb = 0; cb < D; cb += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cb, o);
+                        tmem_wait_ld();
+                        reg_fence<32>(o);
+                        const uint64_t ax2 = f2(alpha, alpha);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float v0, v1;
+                            f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2),
+                                     v0, v1);
+                            o[i] = __float_as_uint(v0);
+                            o[i + 1] = __float_as_uint(v1);
+                        }
+                        tmem_st32(tO + cb, o);
+                    }
+                }
+                tmem_wait_st();
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR_SE(t));
+                mbar_arrive(BAR_PF(t));
+                ++npf;
             }
-            float x[kBN];
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
-            const int kbase = u * kBN;
-            if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
-            }
-            // row max: eight running maxima, three-input max instructions
-            float mk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(x[i], x[i + 8]);
-#pragma unroll
-            for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], x[c + i], x[c + 8 + i]);
-            const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
-                                   fmaxf(mk[6], mk[7]));
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool need = m_new > m_ref + kRescaleThreshold;
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2(m_ref - m_new);
-                l *= alpha;
-                m_ref = m_new;
-            }
-            if (C::SPLITP && j > 0) {  // PV_t of the previous block still reads P_t, writes O_t
-                if (!(ok = mbar_wait_warp(BAR_PVD(t), (j - 1) & 1, a.watch, 20 + t))) break;
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16, each row from its thread straight to
+            // global memory.  A tile with no key block (block-sparse only) writes
+            // O = 0 and lse = -inf.  The next item's first P V product overwrites
+            // O_t only after this tile's next p_full arrival, which follows the
+            // loads below.
+            const bool any = u0 >= 0;
+            if (any) {
+                if (!(ok = mbar_wait_warp(BAR_OF(t), nof & 1, a.watch, 12 + t))) break;
+                ++nof;
                 tc_fence_after();
             }
-            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
-            uint64_t ls2[4] = {0, 0, 0, 0};  // packed partial row sums
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float e0, e1;
-                    f2_split(fma2(f2(x[half * 64 + c], x[half * 64 + c + 1]), sl2x2, negx2), e0, e1);
-                    const float p0 = ex2(e0), p1 = ex2(e1);
-                    ls2[(c >> 1) & 3] = add2(ls2[(c >> 1) & 3], f2(p0, p1));
-                    pk[c >> 1] = pack_op<F16>(p0, p1);
-                }
-                tmem_st32(tP + half * 32, pk);
-            }
-            {
-                const uint64_t t = add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3]));
-                float a0, a1;
-                f2_split(t, a0, a1);
-                l += a0 + a1;
-            }
-            // O_t was last written by the P V product of block j-1, which
-            // completed before this block's scores were committed (SPLITP:
-            // before pv_done, waited for above).
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int cb = 0; cb < D; cb += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + cb, o);
-                    tmem_wait_ld();
-                    reg_fence<32>(o);
-                    const uint64_t ax2 = f2(alpha, alpha);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float u0, u1;
-                        f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2), u0, u1);
-                        o[i] = __float_as_uint(u0);
-                        o[i + 1] = __float_as_uint(u1);
-                    }
-                    tmem_st32(tO + cb, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR_PF(t));
-        }
-        // ---- epilogue: O / l -> bf16 -> swizzled staging in Q_t's buffer -> TMA store
-        // (a tile with no key block -- block-sparse only -- writes O = 0 and
-        // lse = -inf: no MMA ever wrote its O, and only the Q load, which must
-        // land before the buffer is reused, touched its staging buffer)
-        const bool any = u0 >= 0;
-        bool ok_e = ok && (any ? mbar_wait_warp(BAR_OF(t), 0, a.watch, 12 + t)
-                               : mbar_wait_warp(BAR_Q(), 0, a.watch, 16));
-        if (F16 && a.q16 != nullptr)  // the copy warp is done with the Q buffers
-            ok_e = ok_e && mbar_wait_warp(BAR_QC, 0, a.watch, 14);
-        const uint32_t stage = sQ + t * C::TILE;
-        if (ok_e) {
-            tc_fence_after();
             // O was accumulated against V * 2^v on the fp16 path
             const float inv_l = (l > 0.f) ? pow2f(-ev) / l : 0.f;
+            // Rows reach global memory through this warp's transpose buffer: a
+            // thread writes its row's 64-byte piece of a 32-column chunk, then
+            // each store instruction writes whole pieces of eight rows (the
+            // 16-byte quarters of row R at R * 64 + 16 * (q ^ ((R >> 1) & 3)),
+            // which keeps both sides free of bank conflicts).
+            const uint32_t stg = sStage + warp * 2048;
+            const int wrow0 = I.row0 + t * kBM + wq * 32;  // the warp's first query
+            auto store_chunk = [&](uint16_t* dstT, const uint32_t (&wv)[16], int cb) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    st_shared_v4(stg + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4), wv[4 * q4],
+                                 wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int s8 = 0; s8 < 4; ++s8) {
+                    const int R = 8 * s8 + (lane >> 2), q4 = lane & 3;
+                    uint32_t v[4];
+                    ld_shared_v4(stg + R * 64 + ((q4 ^ ((R >> 1) & 3)) << 4), v);
+                    if (wrow0 + R < a.N)
+                        *reinterpret_cast<uint4*>(
+                            dstT + ((static_cast<size_t>(I.b) * a.N + wrow0 + R) * a.Hq + I.h) * D +
+                            cb + q4 * 8) = make_uint4(v[0], v[1], v[2], v[3]);
+                }
+                __syncwarp();
+            };
 #pragma unroll
             for (int cb = 0; cb < D; cb += 32) {
                 uint32_t o[32];
-                tmem_ld32(tO + cb, o);
-                tmem_wait_ld();
-                reg_fence<32>(o);
-                if (SPARSE && !any)
+                if (any) {
+                    tmem_ld32(tO + cb, o);
+                    tmem_wait_ld();
+                    reg_fence<32>(o);
+                } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
-                uint32_t w[16], wl[16];
+                }
+                uint32_t wv[16], wl[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float f0 = __uint_as_float(o[2 * i]) * inv_l;
                     const float f1 = __uint_as_float(o[2 * i + 1]) * inv_l;
-                    w[i] = pack_bf16(f0, f1);
+                    wv[i] = pack_bf16(f0, f1);
                     // rounding residual for the training forward's o_lo
-                    wl[i] = pack_bf16(f0 - __uint_as_float(w[i] << 16),
-                                      f1 - __uint_as_float(w[i] & 0xFFFF0000u));
+                    wl[i] = pack_bf16(f0 - __uint_as_float(wv[i] << 16),
+                                      f1 - __uint_as_float(wv[i] & 0xFFFF0000u));
                 }
-                if (a.o_lo != nullptr && grow < a.N) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        a.o_lo + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * D + cb);
-#pragma unroll
-                    for (int p4 = 0; p4 < 4; ++p4)
-                        dst[p4] = make_uint4(wl[4 * p4], wl[4 * p4 + 1], wl[4 * p4 + 2],
-                                             wl[4 * p4 + 3]);
-                }
-                const uint32_t rowbase = stage + (cb >> 6) * C::CHUNK + r * 128;
-#pragma unroll
-                for (int p4 = 0; p4 < 4; ++p4) {
-                    const int piece = ((cb & 63) >> 3) + p4;  // 16-byte piece within the row
-                    st_shared_v4(rowbase + ((piece ^ (r & 7)) << 4), w[4 * p4], w[4 * p4 + 1],
-                                 w[4 * p4 + 2], w[4 * p4 + 3]);
-                }
+                store_chunk(a.o, wv, cb);
+                if (a.o_lo != nullptr) store_chunk(a.o_lo, wl, cb);
             }
             if (grow < a.N)
-                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                a.lse[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.N + grow] =
                     (m_ref + log2f(l)) * 0.6931471805599453f;
-            fence_proxy_async_smem();
-        }
-        named_bar_sync(1 + t, 128);
-        if (ok_e && r == 0) {
-            for (int c = 0; c < C::NCH; ++c)
-                tma_store_4d(&tmO, stage + c * C::CHUNK, c * 64, h, row0 + t * kBM, b);
-            tma_store_commit();
-            tma_store_wait_read_all();
         }
     }
 
@@ -614,14 +759,20 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D, bool F16, bool SPARSE>
 cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, SPARSE>;
     auto kern = fa_fwd_kernel<D, F16, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const long long nblk = static_cast<long long>(a.n_qblk) * a.B * a.Hq;
-    if (nblk <= 0 || nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(nblk), C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, m.o, a);
+    const long long items = static_cast<long long>(a.n_qblk) * a.B * a.Hq;
+    if (items <= 0 || items > 0x7fffffffLL || a.num_ctas <= 0) return cudaErrorInvalidConfiguration;
+    // Dense: persistent, one CTA per SM (shared memory and registers allow no
+    // more), items dealt out longest first.  Block-sparse items differ in
+    // length with the mask, which a fixed deal would leave unbalanced: one CTA
+    // per item, balanced by the hardware's block scheduler.
+    const long long ctas = SPARSE ? items : (items < a.num_ctas ? items : a.num_ctas);
+    const unsigned grid = static_cast<unsigned>(ctas);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, a);
     return cudaGetLastError();
 }
 

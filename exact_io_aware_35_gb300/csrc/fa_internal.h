@@ -81,6 +81,7 @@ __device__ __forceinline__ F16Scales f16_scales_from(const uint32_t* absmax, int
 }
 
 struct FwdArgs {
+    uint16_t* o;         // [B, N, Hq, d] bf16
     float* lse;          // [B, Hq, N]
     uint16_t* o_lo;      // [B, N, Hq, d] bf16 low half of O, or null
     const F16Scales* f16s;  // non-null: P and V enter O += P V in fp16 (V map = fp16 copy)
@@ -88,7 +89,8 @@ struct FwdArgs {
     int B, Hq, Hkv, N, g;
     int causal;
     float scale_log2;    // scale * log2(e)
-    int n_qblk;          // ceil(N / 256): CTA query blocks (two 128-row tiles each)
+    int n_qblk;          // ceil(N / 256): query blocks (two 128-row tiles each)
+    int num_ctas;        // persistent CTAs to launch at most (the device's SM count)
     // block-sparse: [Hq, nb, nb] bytes (nb = ceil(N / 128)), nonzero = the
     // 128 x 128 block is computed; null: every block (up to the causal limit)
     const uint8_t* block_mask;
@@ -184,7 +186,7 @@ cudaError_t launch_fp8(const Fp8Maps& maps, const Fp8Args& args, cudaStream_t st
 
 // Tensor maps of one call (all 4-D: d, H, N, B; box 64 x 1 x 128 x 1).
 struct FwdMaps {
-    CUtensorMap q, k, v, o;
+    CUtensorMap q, k, v;
 };
 
 struct BwdMaps {

@@ -555,9 +555,11 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
 
 
 def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
-    """Two query tiles: tile 0 multiplies key blocks [0, nkv0), tile 1
+    """One CTA per work item with two query tiles (the FP8 forward runs it
+    with no copy warp): tile 0 multiplies key blocks [0, nkv0), tile 1
     [0, nkv) (nkv0 < nkv on the causal diagonal); four softmax warps per
-    tile, warp q owning rows 32q.. of S_t and O_t."""
+    tile, warp q owning rows 32q.. of S_t and O_t; the epilogue stages O in
+    Q_t's buffer."""
     rows = range(4)
 
     def model(rnd):
@@ -661,222 +663,6 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
     return model
 
 
-def fwd_union_model(blocks0, blocks1, NSLOT=4, copy_q=False, defer_qk0=True, split_p=False,
-                    mistake=None):
-    """The forward kernel's protocol with its key blocks given per tile
-    (block-sparse masks; the dense kernel is blocks0 = range(nkv0), blocks1 =
-    range(nkv)).  Every role walks the union of the two sets in increasing
-    order, the i-th union block in ring entries 2i (K) and 2i + 1 (V).  Per
-    union block u with next union block un: PV0(u) and S0(un) if tile 0 has
-    them, PV1(u), V(u)'s slot released, S1(un), then S0(un) when tile 0 had
-    no u (deferred behind tile 1's p_full wait, which is the one that says
-    K(un) has landed), K(un)'s slot released.  defer_qk0=False issues that
-    S0(un) before tile 1's wait: a planted mistake.
-
-    split_p: the d = 64 layout, where P_t has TMEM columns of its own.  A
-    softmax warp arrives on s_empty(t) once its rows of S_t are in registers,
-    and waits for pv_done(t) (the tile's previous P V product) before it
-    writes P_t or rescales O_t.  Per union block u the MMA thread issues, per
-    tile, S_t(un) as soon as s_empty(t) and K(un) allow, then PV_t(u) on
-    p_full(t).  mistake plants an error: "no_se_wait", "no_k_wait" or
-    "no_pvd_wait"."""
-    rows = range(4)
-    sets = (sorted(set(blocks0)), sorted(set(blocks1)))
-    union = sorted(set(sets[0]) | set(sets[1]))
-
-    def has(t, u):
-        return u in sets[t]
-
-    def model(rnd):
-        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
-                "DONE": 1, "QC": 1}
-        if split_p:
-            bars.update({"SE0": 4, "SE1": 4, "PVD0": 1, "PVD1": 1})
-        bars.update(ring_bars(NSLOT))
-
-        def tile(pre, t, tag):
-            return {f"{pre}.{t}.{q}": tag for q in rows}
-
-        def producer():
-            last = {}
-            yield ("load", "Q", 0, dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
-            for i, u in enumerate(union):
-                for w, nm in enumerate(("K", "V")):
-                    idx = 2 * i + w
-                    s = idx % NSLOT
-                    yield ("wait", f"E{s}", idx // NSLOT - 1)
-                    yield ("load", f"F{s}", idx // NSLOT, {f"kv{s}": f"{nm}({u})"})
-                    last[s] = idx // NSLOT
-            yield ("wait", "Q", 0)
-            for s, ph in last.items():
-                yield ("wait", f"F{s}", ph)
-
-        def gate():
-            cnt = [0, 0]
-            for i, u in enumerate(union):
-                v, kn = 2 * i + 1, 2 * i + 2
-                yield ("wait", f"F{v % NSLOT}", v // NSLOT)
-                if i + 1 < len(union):
-                    yield ("wait", f"F{kn % NSLOT}", kn // NSLOT)
-                for t in (0, 1):
-                    if not has(t, u):
-                        continue
-                    if cnt[t] > 0:
-                        yield ("wait", f"PF{t}", cnt[t] - 1)
-                    yield ("arrive", f"PF{t}", 1, cnt[t])
-                    cnt[t] += 1
-
-        def copy():
-            yield ("wait", "Q", 0)
-            yield ("read", dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
-            yield ("arrive", "QC", 1, 0)
-
-        def qk(t, i, u):
-            slot = (2 * i) % NSLOT
-            return ("mma", f"QK({t},{u})", dict(tile("Q", t, "Q"), **{f"kv{slot}": f"K({u})"}),
-                    tile("S", t, f"S({t},{u})"))
-
-        def pv(t, i, u, prev):
-            slot = (2 * i + 1) % NSLOT
-            reads = dict(tile("P" if split_p else "S", t, f"P({t},{u})"),
-                         **{f"kv{slot}": f"V({u})"})
-            if prev is not None:
-                reads.update(tile("O", t, f"O({t},{prev})"))
-            return ("mma", f"PV({t},{u})", reads, tile("O", t, f"O({t},{u})"))
-
-        def mma_split():
-            if not union:
-                yield ("commit", "DONE", 0)
-                yield ("wait", "DONE", 0)
-                return
-            yield ("wait", "Q", 0)
-            yield ("wait", "F0", 0)
-            nqk, cnt, prev = [0, 0], [0, 0], [None, None]
-            for t in (0, 1):
-                if has(t, union[0]):
-                    yield qk(t, 0, union[0])
-                    yield ("commit", f"SF{t}", nqk[t])
-                    nqk[t] += 1
-            yield ("commit", "E0", 0)
-            for i, u in enumerate(union):
-                un = union[i + 1] if i + 1 < len(union) else None
-                vslot, kidx = (2 * i + 1) % NSLOT, 2 * i + 2
-                kslot = kidx % NSLOT
-                k_ready = False
-                for t in (0, 1):
-                    if un is not None and has(t, un):
-                        if nqk[t] > 0 and mistake != "no_se_wait":
-                            yield ("wait", f"SE{t}", nqk[t] - 1)
-                        if not k_ready and mistake != "no_k_wait":
-                            yield ("wait", f"F{kslot}", kidx // NSLOT)
-                            k_ready = True
-                        yield qk(t, i + 1, un)
-                        yield ("commit", f"SF{t}", nqk[t])
-                        nqk[t] += 1
-                    if has(t, u):
-                        yield ("wait", f"PF{t}", cnt[t])
-                        yield pv(t, i, u, prev[t])
-                        yield ("commit", f"PVD{t}", cnt[t])
-                        cnt[t], prev[t] = cnt[t] + 1, u
-                        if u == sets[t][-1]:
-                            yield ("commit", f"OF{t}", 0)
-                yield ("commit", f"E{vslot}", (2 * i + 1) // NSLOT)
-                if un is not None:
-                    yield ("commit", f"E{kslot}", kidx // NSLOT)
-            yield ("commit", "DONE", 0)
-            yield ("wait", "DONE", 0)
-
-        def mma():
-            if not union:
-                yield ("commit", "DONE", 0)
-                yield ("wait", "DONE", 0)
-                return
-            yield ("wait", "Q", 0)
-            yield ("wait", "F0", 0)
-            sf = [0, 0]
-            for t in (0, 1):
-                if has(t, union[0]):
-                    yield qk(t, 0, union[0])
-                    yield ("commit", f"SF{t}", sf[t])
-                    sf[t] += 1
-            yield ("commit", "E0", 0)
-            cnt, prev = [0, 0], [None, None]
-            for i, u in enumerate(union):
-                un = union[i + 1] if i + 1 < len(union) else None
-                vslot, kslot = (2 * i + 1) % NSLOT, (2 * i + 2) % NSLOT
-                h0, h0n = has(0, u), un is not None and has(0, un)
-                if not defer_qk0 and not h0 and h0n:
-                    yield qk(0, i + 1, un)
-                    yield ("commit", "SF0", sf[0])
-                    sf[0] += 1
-                if h0:
-                    yield ("wait", "PF0", cnt[0])
-                    yield pv(0, i, u, prev[0])
-                    cnt[0], prev[0] = cnt[0] + 1, u
-                    if u == sets[0][-1]:
-                        yield ("commit", "OF0", 0)
-                    if h0n:
-                        yield qk(0, i + 1, un)
-                        yield ("commit", "SF0", sf[0])
-                        sf[0] += 1
-                if has(1, u):
-                    yield ("wait", "PF1", cnt[1])
-                    yield pv(1, i, u, prev[1])
-                    cnt[1], prev[1] = cnt[1] + 1, u
-                yield ("commit", f"E{vslot}", (2 * i + 1) // NSLOT)
-                if has(1, u) and u == sets[1][-1]:
-                    yield ("commit", "OF1", 0)
-                if un is not None:
-                    if has(1, un):
-                        yield qk(1, i + 1, un)
-                        yield ("commit", "SF1", sf[1])
-                        sf[1] += 1
-                    if defer_qk0 and not h0 and h0n:
-                        yield qk(0, i + 1, un)
-                        yield ("commit", "SF0", sf[0])
-                        sf[0] += 1
-                    yield ("commit", f"E{kslot}", (2 * i + 2) // NSLOT)
-            yield ("commit", "DONE", 0)
-            yield ("wait", "DONE", 0)
-
-        def softmax(t, q):
-            me = f"{t}.{q}"
-            prev = None
-            for j, u in enumerate(sets[t]):
-                yield ("wait", f"SF{t}", j)
-                yield ("read", {f"S.{me}": f"S({t},{u})"})
-                if split_p:
-                    yield ("arrive", f"SE{t}", 1, j)
-                    if j > 0 and mistake != "no_pvd_wait":
-                        yield ("wait", f"PVD{t}", j - 1)
-                    yield ("write", {f"P.{me}": f"P({t},{u})"})
-                else:
-                    yield ("write", {f"S.{me}": f"P({t},{u})"})
-                if prev is not None and rnd.random() < 0.5:  # the reference max moved
-                    yield ("read", {f"O.{me}": f"O({t},{prev})"})
-                    yield ("write", {f"O.{me}": f"O({t},{prev})"})
-                yield ("arrive", f"PF{t}", 32, j)
-                prev = u
-            if sets[t]:
-                yield ("wait", f"OF{t}", 0)
-                yield ("read", {f"O.{me}": f"O({t},{prev})"})
-            else:  # a tile with no block stages zeros, once its Q tile has landed
-                yield ("wait", "Q", 0)
-            if copy_q:
-                yield ("wait", "QC", 0)
-            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
-
-        roles = {"prod": producer(), "gate": gate(), "mma": mma_split() if split_p else mma()}
-        for t in (0, 1):
-            for q in rows:
-                roles[f"s{t}{q}"] = softmax(t, q)
-        if copy_q:
-            roles["copy"] = copy()
-        return bars, roles
-
-    return model
-
-
 def stream_entries(sets):
     """Ring order of the block-sparse forward: K_0(0), K_1(0), then per step k,
     tile by tile, V_t(k) and K_t(k+1) of the tiles that still have blocks (a
@@ -892,143 +678,328 @@ def stream_entries(sets):
     return {e: i for i, e in enumerate(seq)}
 
 
-def fwd_stream_model(blocks0, blocks1, NSLOT=4, split_p=False, mistake=None):
-    """The block-sparse forward: each query tile streams K and V of its own
-    key blocks (no sharing between the tiles), all through one ring in the
-    order stream_entries gives; the two tiles advance by step k (the k-th block
-    of each), with the dense kernel's per-tile order: PV_t(k) then S_t(k+1)
-    (split_p: S_t(k+1) first, behind s_empty(t) and its K landing).  The
-    gate adds to p_full(t) once V_t(k) and K_t(k+1) have landed.  mistake:
-    "no_kve_order" releases V_t(k)'s slot before PV_t(k) is issued;
-    "shared_index" gives tile 1 tile 0's ring entries."""
+def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=False,
+                         mistake=None, timeouts=False, drop=None):
+    """The persistent forward: one CTA walks `items`, each a pair (tile 0's key
+    blocks, tile 1's key blocks).  Dense items (sparse=False) share K and V
+    between the tiles, ring entries K(u), V(u) per block of tile 1's range;
+    sparse items stream each tile's own blocks (stream_entries order).  The
+    ring, the barrier phases and the tensor-core queues run on across items.
+    O goes from TMEM straight to global memory, so the Q buffers are free for
+    the next item once its score products and the copy warp are done with
+    them (q_empty: one commit per issuer, one arrival from the copy warp).
+
+    split_p (d = 64): P_t has columns of its own, and each tile has its own
+    MMA issuer: S_t(k+1) as soon as s_empty(t) and K_t(k+1) allow (so also
+    the first product of the next item), PV_t(k) on p_full(t) once V_t(k) has
+    landed, committed to pv_done(t).  Dense rings are then released by both
+    issuers (kv_empty counts 2); tile 0's issuer releases the entries of the
+    blocks past its causal limit with plain arrivals once the slot's previous
+    phase has completed.  Otherwise (d = 128) one issuer, P over S_t, and a
+    gate warp folding V(k), K(k+1) landed into p_full(t).
+
+    timeouts: every wait is bounded (simulate_with_timeouts decides its
+    outcome) and each role takes the kernel's failure path: it stops issuing,
+    drains its own loads / MMAs, and meets the others at the teardown
+    __syncthreads.  drop = (t, n): the n-th arrival for tile t that a partner
+    owes (the gate's on p_full at d = 128, the softmax warps' on s_empty at
+    d = 64) never happens.
+
+    mistake: "no_q_empty" (Q reloaded without q_empty), "early_arrive" (tile
+    0's issuer arrives on kv_empty without the previous-phase wait),
+    "no_k_wait" (a score product before its K tile has landed), "no_pvd_wait"
+    (P_t written before the previous P V product has read it), "no_of_wait"
+    (the epilogue reads O without o_final), "no_drain" (the producer exits
+    without waiting for its last loads).  (The s_empty wait before an item's
+    first score product is implied by q_empty: the issuer's commit to it
+    follows its last P V product, which followed the softmax's p_full; the
+    kernel keeps the wait anyway.)"""
     rows = range(4)
-    sets = (sorted(set(blocks0)), sorted(set(blocks1)))
-    cnt = [len(sets[0]), len(sets[1])]
-    idx = stream_entries(sets)
-    if mistake == "shared_index":
-        idx = {(t, w, k): idx.get((0, w, k), i) for (t, w, k), i in idx.items()}
+    items = [(sorted(set(a)), sorted(set(b))) for a, b in items]
+    nissue = 2 if split_p else 1
+    n_roles = 1 + nissue + (0 if split_p else 1) + 8 + (1 if copy_q else 0)
+
+    def entries(it):
+        """the item's ring entries in order: (owner, kind, k) with owner a
+        tile, or "both" for a dense entry (k is then the block)"""
+        b0, b1 = it
+        if not sparse:
+            assert b0 == list(range(len(b0))) and b1 == list(range(len(b1)))
+            assert len(b0) <= len(b1)
+            return [e for u in range(len(b1)) for e in (("both", "K", u), ("both", "V", u))]
+        return [e for e, _ in sorted(stream_entries(it).items(), key=lambda x: x[1])]
+
+    ent, base = {}, 0
+    for i, it in enumerate(items):
+        seq = entries(it)
+        for j, e in enumerate(seq):
+            ent[(i,) + e] = base + j
+        base += len(seq)
+
+    def W(bar, phase, mode="abort"):
+        return ("twait", bar, phase, mode) if timeouts else ("wait", bar, phase)
 
     def model(rnd):
-        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
-                "DONE": 1, "SE0": 4, "SE1": 4, "PVD0": 1, "PVD1": 1}
-        bars.update(ring_bars(NSLOT))
+        bars = {"Q": 1, "QE": nissue + (1 if copy_q else 0), "DONE": nissue}
+        for t in (0, 1):
+            bars.update({f"SF{t}": 1, f"PF{t}": 128 if split_p else 129, f"OF{t}": 1,
+                         f"SE{t}": 4, f"PVD{t}": 1})
+        for s in range(NSLOT):
+            bars[f"F{s}"] = 1
+            bars[f"E{s}"] = 2 if (split_p and not sparse) else 1
 
         def tile(pre, t, tag):
             return {f"{pre}.{t}.{q}": tag for q in rows}
 
-        def ent(t, w, k):
-            e = idx[(t, w, k)]
+        def teardown():
+            if timeouts:
+                yield ("nbar", "syncthreads", n_roles)
+
+        def slot(i, t, w, k):
+            e = ent[(i, "both" if not sparse else t, w, items[i][t][k] if not sparse else k)]
             return e % NSLOT, e // NSLOT
 
-        def name(t, w, k):
-            return f"{w}{t}({sets[t][k]})"
+        def kv_tag(i, t, w, k):
+            return f"{w}{'' if not sparse else t}({i},{items[i][t][k]})"
 
         def producer():
-            last = {}
-            yield ("load", "Q", 0, dict(tile("Q", 0, "Q"), **tile("Q", 1, "Q")))
-            for (t, w, k), e in sorted(stream_entries(sets).items(), key=lambda x: x[1]):
-                s = e % NSLOT
-                yield ("wait", f"E{s}", e // NSLOT - 1)
-                yield ("load", f"F{s}", e // NSLOT, {f"kv{s}": name(t, w, k)})
-                last[s] = e // NSLOT
-            yield ("wait", "Q", 0)
-            for s, ph in last.items():
-                yield ("wait", f"F{s}", ph)
+            last, ok, nq = {}, True, 0
+            for i, it in enumerate(items):
+                if i > 0 and mistake != "no_q_empty":
+                    ok = (yield W("QE", i - 1)) is not False
+                    if not ok:
+                        break
+                yield ("load", "Q", i, dict(tile("Q", 0, f"Q{i}"), **tile("Q", 1, f"Q{i}")))
+                nq = i + 1
+                for e in entries(it):
+                    owner, w, k = e
+                    g = ent[(i,) + e]
+                    s = g % NSLOT
+                    ok = (yield W(f"E{s}", g // NSLOT - 1)) is not False
+                    if not ok:
+                        break
+                    tag = f"{w}({i},{k})" if owner == "both" else f"{w}{owner}({i},{it[owner][k]})"
+                    yield ("load", f"F{s}", g // NSLOT, {f"kv{s}": tag})
+                    last[s] = g // NSLOT
+                if not ok:
+                    break
+            if mistake != "no_drain":
+                if nq:
+                    yield W("Q", nq - 1, "drain")
+                for s, ph in last.items():
+                    yield W(f"F{s}", ph, "drain")
+            yield from teardown()
 
-        def gate():
-            for k in range(max(cnt, default=0)):
-                for t in (0, 1):
-                    if k >= cnt[t]:
-                        continue
-                    s, ph = ent(t, "V", k)
-                    yield ("wait", f"F{s}", ph)
-                    if k + 1 < cnt[t]:
-                        s, ph = ent(t, "K", k + 1)
-                        yield ("wait", f"F{s}", ph)
-                    if k > 0:
-                        yield ("wait", f"PF{t}", k - 1)
-                    yield ("arrive", f"PF{t}", 1, k)
+        def qk(i, t, k):
+            s, _ = slot(i, t, "K", k)
+            return ("mma", f"QK{t}({i},{k})", dict(tile("Q", t, f"Q{i}"), **{f"kv{s}": kv_tag(i, t, "K", k)}),
+                    tile("S", t, f"S{t}({i},{k})"))
 
-        def qk(t, k):
-            s, _ = ent(t, "K", k)
-            return ("mma", f"QK{t}({k})", dict(tile("Q", t, "Q"), **{f"kv{s}": name(t, "K", k)}),
-                    tile("S", t, f"S{t}({k})"))
-
-        def pv(t, k):
-            s, _ = ent(t, "V", k)
-            reads = dict(tile("P" if split_p else "S", t, f"P{t}({k})"),
-                         **{f"kv{s}": name(t, "V", k)})
+        def pv(i, t, k):
+            s, _ = slot(i, t, "V", k)
+            reads = dict(tile("P" if split_p else "S", t, f"P{t}({i},{k})"),
+                         **{f"kv{s}": kv_tag(i, t, "V", k)})
             if k > 0:
-                reads.update(tile("O", t, f"O{t}({k - 1})"))
-            return ("mma", f"PV{t}({k})", reads, tile("O", t, f"O{t}({k})"))
+                reads.update(tile("O", t, f"O{t}({i},{k - 1})"))
+            return ("mma", f"PV{t}({i},{k})", reads, tile("O", t, f"O{t}({i},{k})"))
 
-        def release(t, w, k):
-            s, ph = ent(t, w, k)
+        def release(i, t, w, k):
+            s, ph = slot(i, t, w, k)
             return ("commit", f"E{s}", ph)
 
-        def mma():
-            yield ("wait", "Q", 0)
-            for t in (0, 1):
-                if cnt[t] > 0:
-                    s, ph = ent(t, "K", 0)
-                    yield ("wait", f"F{s}", ph)
-                    yield qk(t, 0)
-                    yield ("commit", f"SF{t}", 0)
-                    yield release(t, "K", 0)
-            for k in range(max(cnt, default=0)):
-                for t in (0, 1):
-                    if split_p and k + 1 < cnt[t]:
-                        yield ("wait", f"SE{t}", k)
-                        s, ph = ent(t, "K", k + 1)
-                        yield ("wait", f"F{s}", ph)
-                        yield qk(t, k + 1)
-                        yield ("commit", f"SF{t}", k + 1)
-                        yield release(t, "K", k + 1)
-                    if k < cnt[t]:
-                        if mistake == "no_kve_order":
-                            yield release(t, "V", k)
-                        yield ("wait", f"PF{t}", k)
-                        yield pv(t, k)
-                        if split_p:
-                            yield ("commit", f"PVD{t}", k)
-                        if mistake != "no_kve_order":
-                            yield release(t, "V", k)
-                        if k == cnt[t] - 1:
-                            yield ("commit", f"OF{t}", 0)
-                    if not split_p and k + 1 < cnt[t]:
-                        yield qk(t, k + 1)
-                        yield ("commit", f"SF{t}", k + 1)
-                        yield release(t, "K", k + 1)
+        def gate():  # d = 128: V(k), K(k+1) landed -> p_full(t)
+            pf, ok = [0, 0], True
+            for i, it in enumerate(items):
+                if not sparse:
+                    steps = [(u, [t for t in (0, 1) if u < len(it[t])]) for u in range(len(it[1]))]
+                else:
+                    steps = [(k, [t for t in (0, 1) if k < len(it[t])])
+                             for k in range(max(len(it[0]), len(it[1]), 0))]
+                for k, tiles in steps:
+                    waits = []  # (tile, kind, k) of the entries that must have landed
+                    if not sparse:  # dense: one pair serves both tiles
+                        waits = [(1, "V", k)] + ([(1, "K", k + 1)] if k + 1 < len(it[1]) else [])
+                    for t in tiles:
+                        if sparse:
+                            waits = [(t, "V", k)] + ([(t, "K", k + 1)] if k + 1 < len(it[t]) else [])
+                        for (tt, w, kk) in waits:
+                            s, ph = slot(i, tt, w, kk)
+                            if ok:
+                                ok = (yield W(f"F{s}", ph)) is not False
+                        waits = []
+                        if ok and pf[t] > 0:
+                            ok = (yield W(f"PF{t}", pf[t] - 1)) is not False
+                        if not ok:
+                            break
+                        if (t, pf[t]) != drop:
+                            yield ("arrive", f"PF{t}", 1, pf[t])
+                        pf[t] += 1
+                    if not ok:
+                        break
+                if not ok:
+                    break
+            yield from teardown()
+
+        def issuer_split(t):
+            nqk = npv = nof = 0
+            ok = True
+            for i, it in enumerate(items):
+                ok = (yield W("Q", i)) is not False
+                if not ok:
+                    break
+                bl = it[t]
+                for k in range(len(bl) + 1):
+                    if k < len(bl):  # S_t(k) (k = 0: the item's first)
+                        if nqk > 0:
+                            ok = (yield W(f"SE{t}", nqk - 1)) is not False
+                        s, ph = slot(i, t, "K", k)
+                        if ok and mistake != "no_k_wait":
+                            ok = (yield W(f"F{s}", ph)) is not False
+                        if not ok:
+                            break
+                        yield qk(i, t, k)
+                        yield ("commit", f"SF{t}", nqk)
+                        yield release(i, t, "K", k)
+                        nqk += 1
+                    if k > 0:  # PV_t(k - 1)
+                        s, ph = slot(i, t, "V", k - 1)
+                        ok = (yield W(f"F{s}", ph)) is not False
+                        if ok:
+                            ok = (yield W(f"PF{t}", npv)) is not False
+                        if not ok:
+                            break
+                        yield pv(i, t, k - 1)
+                        yield ("commit", f"PVD{t}", npv)
+                        yield release(i, t, "V", k - 1)
+                        npv += 1
+                        if k == len(bl):
+                            yield ("commit", f"OF{t}", nof)
+                            nof += 1
+                if ok and not sparse and t == 0:  # blocks past tile 0's limit
+                    for u in range(len(it[0]), len(it[1])):
+                        for w in ("K", "V"):
+                            s, ph = slot(i, 1, w, u)
+                            if mistake != "early_arrive":
+                                ok = (yield W(f"E{s}", ph - 1)) is not False
+                            if not ok:
+                                break
+                            yield ("arrive", f"E{s}", 1, ph)
+                        if not ok:
+                            break
+                if not ok:
+                    break
+                yield ("commit", "QE", i)
             yield ("commit", "DONE", 0)
-            yield ("wait", "DONE", 0)
+            if t == 0:
+                yield W("DONE", 0, "drain")
+            yield from teardown()
+
+        def issuer_single():
+            npv, nof, nsf = [0, 0], [0, 0], [0, 0]
+            ok = True
+            for i, it in enumerate(items):
+                ok = (yield W("Q", i)) is not False
+                for t in (0, 1):
+                    if not ok:
+                        break
+                    if it[t]:
+                        s, ph = slot(i, t, "K", 0)
+                        if sparse or t == 0:
+                            ok = (yield W(f"F{s}", ph)) is not False
+                            if not ok:
+                                break
+                        yield qk(i, t, 0)
+                        yield ("commit", f"SF{t}", nsf[t])
+                        nsf[t] += 1
+                        if sparse or t == 1:
+                            yield release(i, t, "K", 0)
+                steps = len(it[1]) if not sparse else max(len(it[0]), len(it[1]), 0)
+                for k in range(steps):
+                    for t in (0, 1):
+                        if not ok or k >= len(it[t]):
+                            continue
+                        ok = (yield W(f"PF{t}", npv[t])) is not False
+                        if not ok:
+                            break
+                        yield pv(i, t, k)
+                        npv[t] += 1
+                        if sparse or t == 1:
+                            yield release(i, t, "V", k)
+                        if k == len(it[t]) - 1:
+                            yield ("commit", f"OF{t}", nof[t])
+                            nof[t] += 1
+                        if k + 1 < len(it[t]):
+                            yield qk(i, t, k + 1)
+                            yield ("commit", f"SF{t}", nsf[t])
+                            nsf[t] += 1
+                            if sparse or t == 1:
+                                yield release(i, t, "K", k + 1)
+                    if not ok:
+                        break
+                if not ok:
+                    break
+                yield ("commit", "QE", i)
+            yield ("commit", "DONE", 0)
+            yield W("DONE", 0, "drain")
+            yield from teardown()
+
+        def copy():
+            for i in range(len(items)):
+                ok = (yield W("Q", i)) is not False
+                if not ok:
+                    break
+                yield ("read", dict(tile("Q", 0, f"Q{i}"), **tile("Q", 1, f"Q{i}")))
+                yield ("arrive", "QE", 1, i)
+            yield from teardown()
 
         def softmax(t, q):
             me = f"{t}.{q}"
-            for k in range(cnt[t]):
-                yield ("wait", f"SF{t}", k)
-                yield ("read", {f"S.{me}": f"S{t}({k})"})
-                if split_p:
-                    yield ("arrive", f"SE{t}", 1, k)
-                    if k > 0:
-                        yield ("wait", f"PVD{t}", k - 1)
-                    yield ("write", {f"P.{me}": f"P{t}({k})"})
-                else:
-                    yield ("write", {f"S.{me}": f"P{t}({k})"})
-                if k > 0 and rnd.random() < 0.5:  # the reference max moved
-                    yield ("read", {f"O.{me}": f"O{t}({k - 1})"})
-                    yield ("write", {f"O.{me}": f"O{t}({k - 1})"})
-                yield ("arrive", f"PF{t}", 32, k)
-            if cnt[t]:
-                yield ("wait", f"OF{t}", 0)
-                yield ("read", {f"O.{me}": f"O{t}({cnt[t] - 1})"})
-            else:  # a tile with no block stages zeros, once its Q tile has landed
-                yield ("wait", "Q", 0)
-            yield ("write", {f"Q.{me}": "O tile"})  # staging in Q_t's buffer
+            nsf = npv = nof = 0
+            ok = True
+            for i, it in enumerate(items):
+                bl = it[t]
+                for k in range(len(bl)):
+                    ok = (yield W(f"SF{t}", nsf)) is not False
+                    if not ok:
+                        break
+                    nsf += 1
+                    yield ("read", {f"S.{me}": f"S{t}({i},{k})"})
+                    if split_p:
+                        if (t, nsf - 1) != drop:
+                            yield ("arrive", f"SE{t}", 1, nsf - 1)
+                        if k > 0 and mistake != "no_pvd_wait":
+                            ok = (yield W(f"PVD{t}", npv - 1)) is not False
+                            if not ok:
+                                break
+                        yield ("write", {f"P.{me}": f"P{t}({i},{k})"})
+                    else:
+                        yield ("write", {f"S.{me}": f"P{t}({i},{k})"})
+                    if k > 0 and rnd.random() < 0.5:  # the reference max moved
+                        yield ("read", {f"O.{me}": f"O{t}({i},{k - 1})"})
+                        yield ("write", {f"O.{me}": f"O{t}({i},{k - 1})"})
+                    yield ("arrive", f"PF{t}", 32, npv)
+                    npv += 1
+                if not ok:
+                    break
+                if bl:
+                    if mistake != "no_of_wait":
+                        ok = (yield W(f"OF{t}", nof)) is not False
+                        if not ok:
+                            break
+                    nof += 1
+                    yield ("read", {f"O.{me}": f"O{t}({i},{len(bl) - 1})"})
+            yield from teardown()
 
-        roles = {"prod": producer(), "gate": gate(), "mma": mma()}
+        roles = {"prod": producer()}
+        if split_p:
+            roles["mma0"], roles["mma1"] = issuer_split(0), issuer_split(1)
+        else:
+            roles["mma"], roles["gate"] = issuer_single(), gate()
         for t in (0, 1):
             for q in rows:
                 roles[f"s{t}{q}"] = softmax(t, q)
+        if copy_q:
+            roles["copy"] = copy()
         return bars, roles
 
     return model
@@ -1190,82 +1161,52 @@ def test_forward_protocol(nkv0, nkv, nslot, copy_q):
     each_seed(fwd_model(nkv0, nkv, nslot, copy_q))
 
 
-UNION_CASES = [  # (tile 0's key blocks, tile 1's key blocks, ring slots)
-    (range(3), range(4), 4),                   # the dense causal diagonal
-    (range(6), range(6), 8),                   # dense, non-causal
-    ([0, 9], range(10), 4),                    # tile 0's blocks far apart in the union
-    (range(10), [0, 9], 4),
-    ([2, 5], [0, 1, 7], 4),                    # disjoint sets
-    ([], [0, 3, 4], 4),                        # a tile with no block
-    ([1, 2], [], 4),
-    ([], [], 4),
-    ([0, 2, 4, 6], [1, 3, 5, 7], 4),           # alternating
+PERSISTENT_DENSE = [  # (tile 0's blocks, tile 1's blocks) per item: causal diagonal and full rows
+    [(range(3), range(4)), (range(4), range(4)), (range(1), range(2)), (range(5), range(6))],
+    [(range(1), range(1))] * 4,
+    [(range(7), range(8)), (range(2), range(3))],
+]
+PERSISTENT_SPARSE = [
+    [([0, 2, 3], [1, 2]), ([], [0, 3]), ([1], []), ([], []), ([0, 1, 2, 3], [0, 1, 2, 3])],
+    [([0, 1, 5], [0, 4, 5, 6]), ([2], [2]), ([0, 3, 6], [1])],
 ]
 
 
-@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES)
+@pytest.mark.parametrize("items", range(len(PERSISTENT_DENSE)))
+@pytest.mark.parametrize("split_p,nslot", [(False, 4), (True, 8), (True, 4)])
 @pytest.mark.parametrize("copy_q", [False, True])
-def test_forward_union_protocol(b0, b1, nslot, copy_q):
-    each_seed(fwd_union_model(b0, b1, nslot, copy_q))
+def test_forward_persistent_dense_protocol(items, split_p, nslot, copy_q):
+    each_seed(fwd_persistent_model(PERSISTENT_DENSE[items], nslot, split_p=split_p, copy_q=copy_q),
+              seeds=range(40))
 
 
-def test_forward_union_random_masks():
-    rnd = random.Random(5)
-    for _ in range(40):
-        nb = rnd.randrange(1, 12)
-        b0 = [u for u in range(nb) if rnd.random() < 0.4]
-        b1 = [u for u in range(nb) if rnd.random() < 0.4]
-        each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8))), seeds=range(8))
+@pytest.mark.parametrize("items", range(len(PERSISTENT_SPARSE)))
+@pytest.mark.parametrize("split_p,nslot", [(False, 5), (False, 4), (True, 8)])
+def test_forward_persistent_sparse_protocol(items, split_p, nslot):
+    each_seed(fwd_persistent_model(PERSISTENT_SPARSE[items], nslot, split_p=split_p, sparse=True),
+              seeds=range(40))
 
 
-@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES + [(range(16), range(16), 8)])
-@pytest.mark.parametrize("copy_q", [False, True])
-def test_forward_split_p_protocol(b0, b1, nslot, copy_q):
-    each_seed(fwd_union_model(b0, b1, nslot, copy_q, split_p=True))
+def test_forward_persistent_random_masks():
+    rnd = random.Random(13)
+    for _ in range(25):
+        items = []
+        for _ in range(rnd.randrange(1, 5)):
+            nb = rnd.randrange(1, 9)
+            items.append(([u for u in range(nb) if rnd.random() < 0.5],
+                          [u for u in range(nb) if rnd.random() < 0.5]))
+        split_p = rnd.random() < 0.5
+        each_seed(fwd_persistent_model(items, 8 if split_p else rnd.choice((4, 5)), split_p=split_p,
+                                       sparse=True), seeds=range(8))
 
 
-def test_forward_split_p_random_masks():
-    rnd = random.Random(7)
-    for _ in range(40):
-        nb = rnd.randrange(1, 12)
-        b0 = [u for u in range(nb) if rnd.random() < 0.4]
-        b1 = [u for u in range(nb) if rnd.random() < 0.4]
-        each_seed(fwd_union_model(b0, b1, rnd.choice((4, 8)), split_p=True), seeds=range(8))
-
-
-@pytest.mark.parametrize("mistake", ["no_se_wait", "no_k_wait", "no_pvd_wait"])
-def test_forward_split_p_planted_mistakes_are_caught(mistake):
-    assert fails_on_some_seed(fwd_union_model(range(6), range(6), 8, split_p=True,
-                                              mistake=mistake))
-
-
-@pytest.mark.parametrize("b0,b1,nslot", UNION_CASES + [([0, 3, 4, 9], [1, 2, 3, 4, 5, 6, 8], 5),
-                                                 ([0, 1, 2], [0, 1, 2], 5)])
-@pytest.mark.parametrize("split_p", [False, True])
-def test_forward_stream_protocol(b0, b1, nslot, split_p):
-    each_seed(fwd_stream_model(b0, b1, nslot, split_p))
-
-
-def test_forward_stream_random_masks():
-    rnd = random.Random(11)
-    for _ in range(40):
-        nb = rnd.randrange(1, 14)
-        b0 = [u for u in range(nb) if rnd.random() < 0.5]
-        b1 = [u for u in range(nb) if rnd.random() < 0.5]
-        each_seed(fwd_stream_model(b0, b1, rnd.choice((4, 5, 8)), rnd.random() < 0.5),
-                  seeds=range(8))
-
-
-@pytest.mark.parametrize("mistake", ["no_kve_order", "shared_index"])
-def test_forward_stream_planted_mistakes_are_caught(mistake):
-    assert fails_on_some_seed(fwd_stream_model([0, 2, 3, 5], [1, 2, 4, 5, 6], 4,
-                                               mistake=mistake))
-
-
-def test_forward_union_early_score_of_the_idle_tile_is_caught():
-    # S0(un) issued before tile 1's p_full wait, although tile 0 had no u:
-    # nothing yet says K(un) has landed
-    assert fails_on_some_seed(fwd_union_model([4], [0, 1, 2, 3, 4], 4, defer_qk0=False))
+@pytest.mark.parametrize("mistake,split_p", [("no_q_empty", False), ("no_q_empty", True),
+                                             ("early_arrive", True), ("no_of_wait", False),
+                                             ("no_of_wait", True), ("no_k_wait", True),
+                                             ("no_pvd_wait", True)])
+def test_forward_persistent_planted_mistakes_are_caught(mistake, split_p):
+    assert fails_on_some_seed(fwd_persistent_model(PERSISTENT_DENSE[0], 8 if split_p else 4,
+                                                   split_p=split_p, copy_q=True, mistake=mistake))
 
 
 @pytest.mark.parametrize("nkv,nslot", [(0, 6), (1, 6), (2, 6), (3, 6), (7, 6), (20, 6), (13, 12)])
@@ -1351,13 +1292,15 @@ def test_ring_without_empty_wait_is_caught():
 # out.
 
 
-def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=2000000):
+def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=2000000,
+                           p_load=None):
     rnd = random.Random(seed)
     bars, roles = model(random.Random(seed + 7))
     cta = Cta(bars)
     state = {"failed": False}
     speed = {r: rnd.choice((0.05, 0.3, 1.0)) for r in sorted(roles)}
-    p_load, p_tc = rnd.choice((0.05, 0.3, 1.0)), rnd.choice((0.05, 0.3, 1.0))
+    p_load0, p_tc = rnd.choice((0.05, 0.3, 1.0)), rnd.choice((0.05, 0.3, 1.0))
+    p_load = p_load0 if p_load is None else p_load  # a fixed rate: slow copies
     cur, polls, nbar = {}, {}, {}
 
     def advance(r, value):
@@ -1372,6 +1315,9 @@ def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=200
             waiting.add(r)
             if len(waiting) == count:
                 del nbar[name]
+                if name == "syncthreads" and (cta.tc_busy() or cta.loads):
+                    # the block exits (and frees its TMEM) right after this barrier
+                    raise ProtocolError(f"teardown with work in flight: {cta.tcq} {cta.loads[:2]}")
                 for w in sorted(waiting):
                     advance(w, None)
 
@@ -1426,7 +1372,8 @@ def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=200
 
 
 def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
-    """The forward kernel's roles with every bounded wait's two outcomes:
+    """The one-item two-tile forward's roles (the FP8 forward, copy_q=False)
+    with every bounded wait's two outcomes:
     producer, gate, copy warp, MMA thread and the eight softmax warps (four
     per query tile), the epilogue's bar.sync over a tile's four warps, and the
     teardown __syncthreads over every role.  drop = (t, j): the gate's
@@ -1575,6 +1522,61 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
         return bars, roles
 
     return model
+
+
+PERSISTENT_TIMEOUT_CASES = [  # (items, ring slots, split_p, sparse, copy_q)
+    (PERSISTENT_DENSE[0], 4, False, False, True),
+    (PERSISTENT_DENSE[0], 8, True, False, True),
+    (PERSISTENT_DENSE[2], 4, False, False, False),
+    (PERSISTENT_SPARSE[0], 5, False, True, False),
+    (PERSISTENT_SPARSE[1], 8, True, True, False),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
+def test_persistent_forward_without_faults_never_times_out(case):
+    items, nslot, split_p, sparse, copy_q = PERSISTENT_TIMEOUT_CASES[case]
+    for seed in range(20):
+        assert not simulate_with_timeouts(
+            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True), seed,
+            limit=10 ** 6)
+
+
+@pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
+def test_persistent_forward_any_wait_running_out_ends_the_block_cleanly(case):
+    # waits run out at random; whichever do, every role reaches the teardown
+    # and nothing is left in flight
+    items, nslot, split_p, sparse, copy_q = PERSISTENT_TIMEOUT_CASES[case]
+    n_failed = 0
+    for seed in range(80):
+        n_failed += simulate_with_timeouts(
+            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True), seed,
+            p_spurious=0.01, limit=300)
+    assert n_failed > 40  # the fault path ran in most schedules
+
+
+@pytest.mark.parametrize("split_p,drop", [(False, (0, 0)), (False, (1, 3)), (True, (0, 1)),
+                                          (True, (1, 4))])
+def test_persistent_forward_lost_arrival_is_reported_and_ends_the_block(split_p, drop):
+    for seed in range(30):
+        assert simulate_with_timeouts(
+            fwd_persistent_model(PERSISTENT_DENSE[0], 8 if split_p else 4, split_p, False, True,
+                                 timeouts=True, drop=drop), seed, limit=2000)
+
+
+def test_persistent_forward_exit_without_drain_is_caught():
+    caught = False
+    for seed in range(40):
+        try:
+            # copies that take long to land, so some are still in flight when
+            # a failed block reaches its teardown
+            simulate_with_timeouts(fwd_persistent_model(PERSISTENT_DENSE[0], 4, copy_q=True,
+                                                        timeouts=True, mistake="no_drain"),
+                                   seed, p_spurious=0.02, limit=300, p_load=0.002)
+        except ProtocolError:
+            caught = True
+            break
+    assert caught
 
 
 FWD_TIMEOUT_SHAPES = [(1, 2, 4), (2, 3, 4), (5, 6, 4), (4, 4, 8)]
