@@ -14,7 +14,9 @@
 // over the dP(j) columns they read.  dQ += dS(j) K_j then reads it from there
 // (barrier PF).  The warpgroups go from block j to block j+1 without waiting
 // for the tensor core, which runs S(j+1), dP(j+1) and dQ(j) meanwhile.
-// Warpgroup h takes keys 64h..64h+63 of every block.  K and V stream through
+// Four compute warpgroups: warpgroup h takes keys 32h..32h+31 of every block
+// and writes their dS into the first 16 of its own 32 dP columns, which keeps
+// the chain of loads, exponentials and stores per block short.  K and V stream through
 // separate TMA rings; a gate warp adds one arrival to LD(j) once K_{j+1} and
 // V_{j+1} have landed, so the MMA thread waits on LD and PF only (every wait
 // in the issuing thread costs tensor-core time).  Only LD carries the gate:
@@ -32,6 +34,14 @@ namespace fa {
 namespace {
 
 using namespace bwd;
+
+// 16 compute warps (four warpgroups), then the MMA, TMA, gate and copy warps
+constexpr int kDqCompute = 512;
+constexpr int kDqWarpMma = 16;
+constexpr int kDqWarpLoad = 17;
+constexpr int kDqWarpGate = 18;
+constexpr int kDqWarpCopy = 19;
+constexpr int kDqThreads = 640;
 
 template <int D>
 struct DqCfg : Tiles<D> {
@@ -63,7 +73,7 @@ __device__ __forceinline__ F16Scales scales_of(const uint32_t* absmax) {
 // dQ carries 2^(ds+k), undone in the epilogue.  dO and V stay bf16: dP is
 // not rounded before use.
 template <int D, bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmDO,
@@ -113,13 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR_VE(s), 1);
         }
         mbar_init(BAR_SDF, 1);
-        mbar_init(BAR_LD, 256 + 1);  // compute threads and the gate
-        mbar_init(BAR_PF, 256);
+        mbar_init(BAR_LD, kDqCompute + 1);  // compute threads and the gate
+        mbar_init(BAR_PF, kDqCompute);
         mbar_init(BAR_ACC, 1);
         mbar_init(BAR_PFS, 1);
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == kDqWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -127,8 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // Registers: 640 threads launch with 96 each (61,440); the compute
+    // warpgroups take 104 and the issue warpgroup keeps 64
+    // (512 x 104 + 128 x 64 = 61,440).
 
-    if (warp == kWarpLoad) {
+    if (warp == kDqWarpLoad) {
+        setmaxnreg_dec<64>();
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
@@ -177,9 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_drain(BAR_VF(s), (last_v[s] / C::VS) & 1, a.watch, 21);
         }
         __syncwarp();
-    } else if (warp == kWarpGate) {
+    } else if (warp == kDqWarpGate) {
         // ================= gate: K_{j+1}, V_{j+1} landed -> LD(j) =================
         // Its arrival on LD(j) comes only after LD's previous phase is over.
+        setmaxnreg_dec<64>();
         if (lane == 0) {
             bool ok = true;
             for (int j = 0; j < nj && ok; ++j) {
@@ -191,10 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == kWarpCopy) {
+    } else if (warp == kDqWarpCopy) {
         // ============ copy: dO tile -> fp16(dO * 2^s) (fp16 operand path) ============
         // The scales come from the maxima in absmax (taken before this kernel);
         // block 0 stores them for the dK/dV kernel, which also reads the copy.
+        setmaxnreg_dec<64>();
         if (F16) {
             const F16Scales sc = scales_of<D>(a.absmax);
             if (blockIdx.x == 0 && lane == 0) *a.scales_w = sc;
@@ -205,8 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_tile_to_f16<D>(sDO, dst, row_el, a.N - qi * kBM, mul, lane);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+    } else if (warp == kDqWarpMma) {
         // ================= MMA issuer (the whole warp; the leader lane issues) =================
+        setmaxnreg_dec<64>();
         {
             const uint32_t leader = elect_one();
             constexpr uint32_t IDESC_S = idesc_16(kBM, kBN, false, false, F16);  // S = Q K^T
@@ -242,14 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_t(tDP(jj), do_lo, sV + (jj % C::VS) * C::TILE, IDESC_DP);
                 mma_commit_w(leader, BAR_VE(jj % C::VS));
             };
-            // dQ += dS(jj) K_jj: dS (bf16) of keys 16ks.. at columns 64(ks/4) + (ks%4)*8
-            // of dP buffer jj & 1; K rows 16ks.. read MN-major
+            // dQ += dS(jj) K_jj: dS (packed pairs) of keys 16ks.. at columns
+            // 32(ks/2) + (ks%2)*8 of dP buffer jj & 1; K rows 16ks.. read MN-major
             auto issue_dq = [&](int jj) {
                 const uint32_t k_lo = sdesc_lo(sK + (jj % C::KS) * C::TILE, C::CHUNK), aS = tDP(jj);
 #pragma unroll
                 for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_bf16_ts_w(leader, tDQ, aS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_at(k_lo, HI, ks * 2048),
-                                IDESC_DQ, (jj == 0 && ks == 0) ? 0u : 1u);
+                    mma_bf16_ts_w(leader, tDQ, aS + (ks >> 1) * 32 + (ks & 1) * 8,
+                                  sdesc_at(k_lo, HI, ks * 2048), IDESC_DQ,
+                                  (jj == 0 && ks == 0) ? 0u : 1u);
                 mma_commit_w(leader, BAR_KE(jj % C::KS));
             };
             bool ok = mbar_wait_warp(BAR_QDO, 0, a.watch, 22) && k_ready(0);
@@ -280,12 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(BAR_ACC, 0, a.watch, 25);
         }
         __syncwarp();
-    } else if (warp < 8) {
-        const int hf = warp >> 2;  // keys 64*hf..64*hf+63 of every block
+    } else if (warp < 16) {
+        setmaxnreg_inc<104>();
+        const int hf = warp >> 2;  // keys 32*hf..32*hf+31 of every block
         const int r = (warp & 3) * 32 + lane;
         const int grow = qi * kBM + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tbase + C::TM_S + lane_off + hf * 64;
+        const uint32_t tS = tbase + C::TM_S + lane_off + hf * 32;
         const bool valid = grow < a.N;
         const size_t st_idx = (static_cast<size_t>(b) * a.Hq + h) * a.N + (valid ? grow : 0);
         const float nlse2 = valid ? -a.lse[st_idx] * kLog2e : 0.f;
@@ -307,23 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nj && ok; ++j) {
             if (!(ok = mbar_wait_warp(BAR_SDF, j & 1, a.watch, 26))) break;
             tc_fence_after();
-            const uint32_t tDP = tbase + C::TM_DP + (j & 1) * 128 + lane_off + hf * 64;
-            uint32_t sv[64], dp[64];
+            const uint32_t tDP = tbase + C::TM_DP + (j & 1) * 128 + lane_off + hf * 32;
+            uint32_t sv[32], dp[32];
             tmem_ld32(tS, sv);
-            tmem_ld32(tS + 32, sv + 32);
             tmem_ld32(tDP, dp);
-            tmem_ld32(tDP + 32, dp + 32);
             tmem_wait_ld();
-            reg_fence<64>(sv);
-            reg_fence<64>(dp);
+            reg_fence<32>(sv);
+            reg_fence<32>(dp);
             // both buffers are in registers: S(j+1) may now overwrite S(j)
             tc_fence_before();
             mbar_arrive(BAR_LD);
-            const int kbase = j * kBN + hf * 64;
-            const bool need_mask = kbase + 63 > lim;
-            uint32_t pk[32];
+            const int kbase = j * kBN + hf * 32;
+            const bool need_mask = kbase + 31 > lim;
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
                 // two columns per packed f32x2 FMA / ADD / MUL
                 float x0, x1;
                 f2_split(fma2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nlse2x2),
@@ -339,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f2_split(mul2(f2(p0, p1), t), d0, d1);
                 pk[c >> 1] = pack_op<F16>(d0, d1);
             }
-            tmem_st32(tDP, pk);  // dS over the first 32 of this half's dP columns
+            tmem_st16(tDP, pk);  // dS over the first 16 of this quarter's dP columns
             tmem_wait_st();
             tc_fence_before();
             // S(j), dP(j) were issued before the MMA thread waits for PF(j-1):
@@ -352,14 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool ok_e = ok && mbar_wait_warp(BAR_ACC, 0, a.watch, 27);
         if (ok_e) {
             tc_fence_after();
-            // dQ = scale * (dS K): each warpgroup stages half of the d columns into
-            // the Q tile's shared memory (no MMA reads Q any more)
-            stage_rows_bf16<C::CHUNK>(
-                tbase + C::TM_DQ + lane_off, sQ, r, hf * (D / 2), (hf + 1) * (D / 2),
-                a.scale * pow2f(-(eds + ek)));
+            // dQ = scale * (dS K): the warpgroups stage 32-column slices of it
+            // into the Q tile's shared memory (no MMA reads Q any more)
+            if (hf * 32 < D)
+                stage_rows_bf16<C::CHUNK>(tbase + C::TM_DQ + lane_off, sQ, r, hf * 32, hf * 32 + 32,
+                                          a.scale * pow2f(-(eds + ek)));
             fence_proxy_async_smem();
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(1, kDqCompute);
         if (ok_e && warp == 0 && lane == 0) {
             for (int c = 0; c < C::NCH; ++c)
                 tma_store_4d(&tmDQ, sQ + c * C::CHUNK, c * 64, h, qi * kBM, b);
@@ -370,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kDqWarpMma) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -386,7 +403,7 @@ cudaError_t launch_dq(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const long long nblk = static_cast<long long>((a.N + kBM - 1) / kBM) * a.B * a.Hq;
     if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<static_cast<unsigned>(nblk), kThreads, smem, st>>>(F16 ? m.q16 : m.q, F16 ? m.k16 : m.k,
+    kern<<<static_cast<unsigned>(nblk), kDqThreads, smem, st>>>(F16 ? m.q16 : m.q, F16 ? m.k16 : m.k,
                                                             m.v, m.dout, m.dq, a);
     return cudaGetLastError();
 }

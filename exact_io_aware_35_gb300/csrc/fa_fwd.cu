@@ -767,9 +767,10 @@ cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
     const long long items = static_cast<long long>(a.n_qblk) * a.B * a.Hq;
     if (items <= 0 || items > 0x7fffffffLL || a.num_ctas <= 0) return cudaErrorInvalidConfiguration;
     // Dense: persistent, one CTA per SM (shared memory and registers allow no
-    // more), items dealt out longest first.  Block-sparse items differ in
-    // length with the mask, which a fixed deal would leave unbalanced: one CTA
-    // per item, balanced by the hardware's block scheduler.
+    // more), items dealt out round robin, longest query blocks first.
+    // Block-sparse: one CTA per item, balanced by the hardware's block
+    // scheduler (measured faster than the fixed deal on the synthetic masks,
+    // whose items differ in length with the mask).
     const long long ctas = SPARSE ? items : (items < a.num_ctas ? items : a.num_ctas);
     const unsigned grid = static_cast<unsigned>(ctas);
     kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, a);

@@ -218,8 +218,9 @@ def ring_bars(nslot):
 # ---------------------------------------------------------------- dQ kernel
 def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuers=False,
              single_dqd=False, skip_dqd=False):
-    """Eight compute warps (w, q): key half w (64 columns of S, dP) and TMEM
-    lanes 32q.. (query rows); each arrives on its own.  The MMA thread
+    """Sixteen compute warps (w, q): key quarter w (32 columns of S, dP, its
+    dS written into the first 16) and TMEM lanes 32q.. (query rows); each
+    arrives on its own.  The MMA thread
     arrives on PFS once it has seen dS(j) complete; a warp waits for that
     before its dS(j+1) arrival, so PF is never a phase ahead of its waiter.
     two_issuers (a variant that was tried and measured slower, not the
@@ -229,10 +230,10 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
     thread waits for it (phase j // 2) before dP(j+2); the dQ thread, which
     waits for PF, is the one that arrives on PFS.  single_dqd (one DQD
     barrier for both buffers) and skip_dqd are planted mistakes."""
-    warps = [(w, q) for w in (0, 1) for q in range(4)]
+    warps = [(w, q) for w in range(4) for q in range(4)]
 
     def model(rnd):
-        bars = {"QDO": 1, "SDF": 1, "LD": 257, "PF": 257 if first_gate_design else 256, "ACC": 1,
+        bars = {"QDO": 1, "SDF": 1, "LD": 513, "PF": 513 if first_gate_design else 512, "ACC": 1,
                 "PFS": 1, "DQD0": 1, "DQD1": 1, "DONE": 1}
         for nm, ns in (("K", KS), ("V", VS)):
             for s in range(ns):
