@@ -50,11 +50,14 @@ struct FwdCfg {
     static constexpr int CHUNK = kBM * 128;          // one 64-column chunk of a 128-row tile
     static constexpr int NCH = D / 64;               // chunks per tile
     static constexpr int TILE = NCH * CHUNK;         // bytes of a 128 x D bf16 tile
-    static constexpr int NSLOT = (D == 128) ? 4 : 8;  // K/V ring slots
+    // K/V ring slots: the block-sparse kernel streams each tile's K and V on
+    // its own (four ring entries per step) and takes one slot more at D = 128
+    static constexpr int NSLOT = (D == 128) ? (SPARSE ? 5 : 4) : 8;
     static constexpr int SMEM_Q = 2 * TILE;
     static constexpr int SMEM_KV = NSLOT * TILE;
-    // the epilogue's per-warp transpose buffers: 32 rows x 64 bytes per softmax warp
-    static constexpr int SMEM_STAGE = 8 * 2048;
+    // the epilogue's per-warp transpose buffers, 32 rows x 64 bytes per softmax
+    // warp; block-sparse CTAs run one item each and use their tile's Q buffer
+    static constexpr int SMEM_STAGE = SPARSE ? 0 : 8 * 2048;
     // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
     // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done
     static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1;
@@ -698,7 +701,9 @@ __global__ void __launch_bounds__(384, 1)
             // each store instruction writes whole pieces of eight rows (the
             // 16-byte quarters of row R at R * 64 + 16 * (q ^ ((R >> 1) & 3)),
             // which keeps both sides free of bank conflicts).
-            const uint32_t stg = sStage + warp * 2048;
+            // (block-sparse: one item per CTA, and Q_t is idle once o_final(t)
+            // says the tile's last product is done)
+            const uint32_t stg = SPARSE ? sQ + t * C::TILE + wq * 2048 : sStage + warp * 2048;
             const int wrow0 = I.row0 + t * kBM + wq * 32;  // the warp's first query
             auto store_chunk = [&](uint16_t* dstT, const uint32_t (&wv)[16], int cb) {
 #pragma unroll
