@@ -797,7 +797,7 @@ def run_sparse(args):
             "peak_source": peaks["source"] + " burst bf16",
             "dense_causal_ms": dense_ms, "speedup_vs_dense": dense_ms / ms,
             "gpu_launches": K,
-            "roofline": {"kernel": "fa_decode_split_kernel (block-mask walk)", "bound": "tensor",
+            "roofline": {"kernel": "fa_fwd_kernel (block-mask walk)", "bound": "tensor",
                          "achieved": tf / ws, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / ws / peak, "peak_source": peaks["source"] + " burst",
                          "launch_ms": ms, "algorithmic_work_per_launch": flops / ws,

@@ -510,8 +510,6 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
     a.n_qt = pl.n_qt;
     a.splits = pl.splits;
     a.blocks_per_split = pl.blocks_per_split;
-    a.block_mask = nullptr;
-    a.nkb = 0;
     a.watch = make_watch(di->status);
     const cudaError_t e = launch_decode(maps, a, d, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_splitkv launch");

@@ -27,10 +27,6 @@
 //   * with one split the kernel writes bf16 O and lse itself; with several,
 //     fp32 (O_s, lse_s) per split go to the caller's workspace and
 //     fa_decode_combine_kernel merges them.
-// The same kernel serves the block-sparse forward ("FlashAttention Kernel":
-// block-sparse FlashAttention skips the blocks a sparsity mask zeroes): one
-// head's 128 queries per tile, one split, and every role walks only the key
-// blocks the tile's mask row selects.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -51,25 +47,13 @@ struct DecCfg {
     static constexpr int THREADS = 192;               // softmax warps 0-3, MMA warp 4, TMA warp 5
 };
 
-// The key blocks a CTA visits: every block of [lo, hi), or, under a block
-// mask, those of [lo, hi) whose mask byte is nonzero.  Every role walks the
-// same sequence.
+// The key blocks a CTA visits: every block of [lo, hi).  Every role walks
+// the same sequence.
 struct KeyBlocks {
-    const uint8_t* row;
     int lo, hi;
-    __device__ int next(int kb) const {
-        ++kb;
-        if (row)
-            while (kb < hi && row[kb] == 0) ++kb;
-        return kb;
-    }
-    __device__ int first() const { return next(lo - 1); }
-    __device__ int count() const {
-        if (!row) return hi > lo ? hi - lo : 0;
-        int n = 0;
-        for (int x = lo; x < hi; ++x) n += row[x] != 0;
-        return n;
-    }
+    __device__ int next(int kb) const { return kb + 1; }
+    __device__ int first() const { return lo; }
+    __device__ int count() const { return hi > lo ? hi - lo : 0; }
 };
 
 constexpr int kDecWarpMma = 4;
@@ -118,8 +102,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     const int jb0 = split * a.blocks_per_split;
     int jb1 = min(jb0 + a.blocks_per_split, nkv_all);
     if (a.causal) jb1 = min(jb1, (q0 + nq_tile - 1 + a.Nk - a.Nq) / kBN + 1);
-    KeyBlocks blocks{nullptr, jb0, jb1};
-    if (a.block_mask) blocks.row = a.block_mask + (static_cast<size_t>(h0) * a.n_qt + qt) * a.nkb;
+    const KeyBlocks blocks{jb0, jb1};
     const int nkv = blocks.count();
 
     if (warp == 0 && lane == 0) {

@@ -121,7 +121,7 @@ struct BwdArgs {
 
 // Split-KV forward (fa_decode.cu): Nq queries of gp heads sharing a KV head
 // per 128-row tile (qpt queries x gp heads), the key blocks cut into `splits`
-// ranges of blocks_per_split blocks, or picked by a block mask.
+// ranges of blocks_per_split blocks.
 struct DecodeArgs {
     uint16_t* o;        // [B, Nq, Hq, d] bf16
     float* lse;         // [B, Hq, Nq]
@@ -130,13 +130,9 @@ struct DecodeArgs {
     int B, Hq, Hkv, Nq, Nk, g;
     int causal;         // query i sees keys j <= i + Nk - Nq
     float scale_log2;
-    int gp;             // query heads per tile (g for decoding, 1 for block-sparse)
+    int gp;             // query heads per tile
     int qpt, n_qt;      // queries per tile (128 / gp), query tiles
     int splits, blocks_per_split;
-    // block-sparse: [Hq, n_qt, nkb] bytes, nonzero = the 128 x 128 block is
-    // computed (then gp == 1, qpt == 128 and splits == 1); null: every block
-    const uint8_t* block_mask;
-    int nkb;
     Watch watch;         // status words, time limit and id of the launch
 };
 
