@@ -466,13 +466,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             tc_fence_before();
             mbar_arrive(BAR_PF(t));
         }
-        // ---- epilogue: O * sv / l -> bf16, plain stores (one 256-byte row per
-        // thread); lse
+        // ---- epilogue: O * sv / l -> bf16; lse.  Rows reach global memory
+        // through a per-warp transpose in the tile's Q buffer (idle once
+        // o_final(t) says the tile's last product is done): a thread writes its
+        // row's 64-byte piece of a 32-column chunk, then each store instruction
+        // writes whole pieces of eight rows (16-byte quarters of row R at
+        // R * 64 + 16 * (q ^ ((R >> 1) & 3)), free of bank conflicts).
         const bool ok_e = ok && mbar_wait_warp(BAR_OF(t), 0, a.watch, 57);
         if (ok_e) {  // every lane takes part in the (warp-collective) TMEM loads
             tc_fence_after();
             const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;
-            uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.N + grow) * a.Hq + h) * 128;
+            const uint32_t stg = sQ + t * kF8Tile + wq * 2048;
+            const int wrow0 = qt * 128 + wq * 32;  // the warp's first query
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
                 uint32_t o[32];
@@ -483,11 +488,22 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
-                if (grow < a.N)
 #pragma unroll
-                    for (int p4 = 0; p4 < 4; ++p4)
-                        reinterpret_cast<uint4*>(dst + cb)[p4] =
-                            make_uint4(w[4 * p4], w[4 * p4 + 1], w[4 * p4 + 2], w[4 * p4 + 3]);
+                for (int q4 = 0; q4 < 4; ++q4)
+                    st_shared_v4(stg + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4), w[4 * q4],
+                                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int s8 = 0; s8 < 4; ++s8) {
+                    const int R = 8 * s8 + (lane >> 2), q4 = lane & 3;
+                    uint32_t v[4];
+                    ld_shared_v4(stg + R * 64 + ((q4 ^ ((R >> 1) & 3)) << 4), v);
+                    if (wrow0 + R < a.N)
+                        *reinterpret_cast<uint4*>(
+                            a.o + ((static_cast<size_t>(b) * a.N + wrow0 + R) * a.Hq + h) * 128 + cb +
+                            q4 * 8) = make_uint4(v[0], v[1], v[2], v[3]);
+                }
+                __syncwarp();
             }
             if (grow < a.N)
                 a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
