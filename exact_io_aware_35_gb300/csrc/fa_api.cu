@@ -673,6 +673,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float
     a.rotate = (flags & FA_FP8_ROTATE) ? 1 : 0;
     a.quantize = (flags & FA_FP8_ATTEND_ONLY) ? 0 : 1;
     a.attend = (flags & FA_FP8_QUANTIZE_ONLY) ? 0 : 1;
+    a.num_ctas = di->num_sms;
     a.scale_log2 = scale * 1.4426950408889634f * (a.rotate ? 1.f / 128.f : 1.f);
     a.watch = make_watch(di->status);
     const cudaError_t e = launch_fp8(maps, a, static_cast<cudaStream_t>(stream));

@@ -31,12 +31,16 @@ namespace {
 
 constexpr int kF8Tile = 128 * 128;  // bytes of a 128 x 128 e4m3 tile
 constexpr int kF8Slots = 8;         // K / V^T ring slots (four key blocks)
-constexpr int kF8Threads = 352;     // softmax warps 0-7 (two tiles), MMA 8, TMA 9, gate 10
+// softmax warps 0-7 (two tiles), MMA 8, TMA 9, gate 10, warp 11 idle (a whole
+// issue warpgroup for setmaxnreg)
+constexpr int kF8Threads = 384;
 constexpr int kF8WarpMma = 8;
 constexpr int kF8WarpLoad = 9;
 constexpr int kF8WarpGate = 10;
-// barriers: Q, K/V full[slots], empty[slots], s_full[2], p_full[2], o_final[2], done
-constexpr int kF8Bars = 1 + 2 * kF8Slots + 2 + 2 + 2 + 1;
+// barriers: Q, K/V full[slots], empty[slots], s_full[2], p_full[2], o_final[2], done,
+// q_empty
+constexpr int kF8Bars = 1 + 2 * kF8Slots + 2 + 2 + 2 + 1 + 1;
+constexpr int kF8Stage = 8 * 2048;  // the epilogue's per-warp transpose buffers
 constexpr float kE4m3Max = 448.f;
 
 // The fixed sign of column c in the rotation diag(s) H: the top bit of
@@ -191,16 +195,21 @@ __global__ void __launch_bounds__(128) fp8_vt_kernel(const uint16_t* __restrict_
     }
 }
 
-// The forward.  One CTA per (batch, head, 256-query block): two 128-row
-// query tiles in shared memory, K_j and V^T_j streamed through one ring, and
-// the matmul/softmax interleave of the bf16 forward -- the tensor core runs
-// one tile's products while the other tile's softmax runs -- with every
-// product a kind::f8f6f4 MMA (K = 32 per instruction).  TMEM: S0 | S1 | O0 |
-// O1, 128 columns each; P (e4m3, four per 32-bit column) goes over the first
-// 32 columns of its S and feeds P V from TMEM.  Warps 0-3 do the softmax of
-// tile 0, 4-7 of tile 1 (one query row per thread), warp 8 issues MMAs, warp
-// 9 loads, warp 10 is the gate: it folds "V_j and K_{j+1} landed" into the
-// p_full barriers, so the MMA thread waits on two barriers per key block.
+// The forward: persistent CTAs, one per SM, walking (batch, head, 256-query
+// block) work items longest first, as the bf16 forward does; the K/V^T ring,
+// the barrier phases and TMEM run on from one item to the next, and the
+// producer loads an item's Q tiles once the previous item's score products
+// are done with them (q_empty).  Per item: two 128-row query tiles, K_j and
+// V^T_j streamed through one ring, and the matmul/softmax interleave of the
+// bf16 forward -- the tensor core runs one tile's products while the other
+// tile's softmax runs -- with every product a kind::f8f6f4 MMA (K = 32 per
+// instruction).  TMEM: S0 | S1 | O0 | O1, 128 columns each; P (e4m3, four per
+// 32-bit column) goes over the first 32 columns of its S and feeds P V from
+// TMEM.  Warps 0-3 do the softmax of tile 0, 4-7 of tile 1 (one query row
+// per thread, 208 registers by setmaxnreg), warp 8 issues MMAs, warp 9
+// loads, warp 10 is the gate: it folds "V_j and K_{j+1} landed" into the
+// p_full barriers, so the MMA thread waits on two barriers per key block;
+// warp 11 only completes the issue warpgroup (80 registers each).
 __global__ void __launch_bounds__(kF8Threads, 1)
     fa_fp8_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmVt, const Fp8Args a) {
@@ -209,7 +218,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sQ = smem_u32(smem);  // Q0, Q1
     const uint32_t sKV = sQ + 2 * kF8Tile;  // slot s at s * kF8Tile
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kF8Tile + kF8Slots * kF8Tile);
+    const uint32_t sStage = sKV + kF8Slots * kF8Tile;  // the epilogue's per-warp buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kF8Tile + kF8Slots * kF8Tile + kF8Stage);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kF8Bars);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t BAR_Q = bar0;
@@ -219,19 +229,28 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     auto BAR_PF = [&](int t) { return bar0 + 8u * (3 + 2 * kF8Slots + t); };  // P_t(j) written
     auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * kF8Slots + t); };  // O_t final
     const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * kF8Slots);
+    const uint32_t BAR_QE = bar0 + 8u * (8 + 2 * kF8Slots);  // the item's Q tiles no longer read
 
     const int warp = warp_id();
     const int lane = lane_id();
     const int per = a.B * a.Hq;
     const int n_qblk = (a.nb + 1) / 2;
-    const int qb = n_qblk - 1 - static_cast<int>(blockIdx.x) / per;  // longest blocks first
-    const int bh = static_cast<int>(blockIdx.x) % per;
-    const int b = bh / a.Hq;
-    const int h = bh % a.Hq;
-    const int hk = h / a.g;
-    // key blocks tile t = 0, 1 (query blocks 2qb, 2qb + 1) multiplies
-    const int nkv0 = a.causal ? min(2 * qb + 1, a.nb) : a.nb;
-    const int nkv = a.causal ? min(2 * qb + 2, a.nb) : a.nb;
+    const int n_items = n_qblk * per;
+    // work item w: longest query blocks first, heads of one KV group adjacent
+    struct Item {
+        int qb, b, h, hk, nkv0, nkv;  // key blocks tile t = 0, 1 (query blocks 2qb, 2qb + 1) multiplies
+    };
+    auto item = [&](int w) {
+        Item I;
+        I.qb = n_qblk - 1 - w / per;
+        const int bh = w % per;
+        I.b = bh / a.Hq;
+        I.h = bh % a.Hq;
+        I.hk = I.h / a.g;
+        I.nkv0 = a.causal ? min(2 * I.qb + 1, a.nb) : a.nb;
+        I.nkv = a.causal ? min(2 * I.qb + 2, a.nb) : a.nb;
+        return I;
+    };
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_Q, 1);
@@ -245,6 +264,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(BAR_OF(t), 1);
         }
         mbar_init(BAR_DONE, 1);
+        mbar_init(BAR_QE, 1);
         fence_barrier_init();
     }
     if (warp == kF8WarpMma) {
@@ -255,35 +275,46 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
+    // Registers: 384 threads launch with 168 each (64,512); each role first
+    // moves its warpgroup's share: 208 for the softmax warpgroups, 80 for the
+    // issue warpgroup (2 x 128 x 208 + 128 x 80 = 63,488).
 
     if (warp == kF8WarpLoad) {
-        // ================= TMA producer: Q0, Q1, then K_j, V^T_j alternately =================
+        // ================= TMA producer: per item Q0, Q1, then K_j, V^T_j alternately ======
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmVt);
             const uint64_t pol = l2_policy_evict_last();  // re-read by every query block
-            mbar_arrive_expect_tx(BAR_Q, 2 * kF8Tile);  // rows past N read as zero
-            for (int t = 0; t < 2; ++t)
-                tma_load_4d(sQ + t * kF8Tile, &tmQ, BAR_Q, 0, h, (2 * qb + t) * 128, b);
             int last_idx[kF8Slots];
             for (int s = 0; s < kF8Slots; ++s) last_idx[s] = -1;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j)
-                for (int w = 0; w < 2 && ok; ++w) {
-                    const int idx = 2 * j + w, slot = idx % kF8Slots;
-                    if (!(ok = mbar_wait(BAR_KVE(slot), ((idx / kF8Slots) & 1) ^ 1u, a.watch, 50)))
-                        break;
-                    mbar_arrive_expect_tx(BAR_KVF(slot), kF8Tile);
-                    if (w == 0)
-                        tma_load_4d_hint(sKV + slot * kF8Tile, &tmK, BAR_KVF(slot), 0, hk, j * 128,
-                                         b, pol);
-                    else
-                        tma_load_4d_hint(sKV + slot * kF8Tile, &tmVt, BAR_KVF(slot), j * 128, 0,
-                                         hk, b, pol);
-                    last_idx[slot] = idx;
-                }
-            mbar_drain(BAR_Q, 0, a.watch, 51);
+            int e = 0, it = 0;  // ring entry and items started, running over the items
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+                const Item I = item(w);
+                // the previous item's score products are done with Q
+                if (it > 0 && !(ok = mbar_wait(BAR_QE, (it - 1) & 1, a.watch, 64))) break;
+                mbar_arrive_expect_tx(BAR_Q, 2 * kF8Tile);  // rows past N read as zero
+                for (int t = 0; t < 2; ++t)
+                    tma_load_4d(sQ + t * kF8Tile, &tmQ, BAR_Q, 0, I.h, (2 * I.qb + t) * 128, I.b);
+                for (int j = 0; j < I.nkv && ok; ++j)
+                    for (int wv = 0; wv < 2 && ok; ++wv, ++e) {
+                        const int slot = e % kF8Slots;
+                        if (!(ok = mbar_wait(BAR_KVE(slot), ((e / kF8Slots) & 1) ^ 1u, a.watch, 50)))
+                            break;
+                        mbar_arrive_expect_tx(BAR_KVF(slot), kF8Tile);
+                        if (wv == 0)
+                            tma_load_4d_hint(sKV + slot * kF8Tile, &tmK, BAR_KVF(slot), 0, I.hk,
+                                             j * 128, I.b, pol);
+                        else
+                            tma_load_4d_hint(sKV + slot * kF8Tile, &tmVt, BAR_KVF(slot), j * 128, 0,
+                                             I.hk, I.b, pol);
+                        last_idx[slot] = e;
+                    }
+            }
+            // no copies in flight at exit: the last Q, the last load into each slot
+            if (it > 0) mbar_drain(BAR_Q, (it - 1) & 1, a.watch, 51);
             for (int s = 0; s < kF8Slots; ++s)
                 if (last_idx[s] >= 0)
                     mbar_drain(BAR_KVF(s), (last_idx[s] / kF8Slots) & 1, a.watch, 51);
@@ -293,190 +324,220 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // ================= gate: V_j and K_{j+1} landed -> p_full(t) =================
         // one arrival per tile that multiplies block j, made only after that
         // barrier's previous phase is over, so it can never count in the wrong one
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             bool ok = true;
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-                ok = mbar_wait(BAR_KVF(vidx % kF8Slots), (vidx / kF8Slots) & 1, a.watch, 58);
-                if (ok && j + 1 < nkv)
-                    ok = mbar_wait(BAR_KVF(kidx % kF8Slots), (kidx / kF8Slots) & 1, a.watch, 58);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (t == 0 && j >= nkv0) continue;
-                    if (j > 0) ok = mbar_wait(BAR_PF(t), (j - 1) & 1, a.watch, 59);
-                    if (ok) mbar_arrive(BAR_PF(t));
+            int e = 0, cnt[2] = {0, 0};
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+                const Item I = item(w);
+                for (int j = 0; j < I.nkv && ok; ++j) {
+                    const int vidx = e + 2 * j + 1, kidx = e + 2 * j + 2;
+                    ok = mbar_wait(BAR_KVF(vidx % kF8Slots), (vidx / kF8Slots) & 1, a.watch, 58);
+                    if (ok && j + 1 < I.nkv)
+                        ok = mbar_wait(BAR_KVF(kidx % kF8Slots), (kidx / kF8Slots) & 1, a.watch, 58);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (t == 0 && j >= I.nkv0) continue;
+                        if (cnt[t] > 0) ok = mbar_wait(BAR_PF(t), (cnt[t] - 1) & 1, a.watch, 59);
+                        if (ok) mbar_arrive(BAR_PF(t));
+                        ++cnt[t];
+                    }
                 }
+                e += 2 * I.nkv;
             }
         }
         __syncwarp();
     } else if (warp == kF8WarpMma) {
         // ================= MMA issuer: PV0(j), S0(j+1), PV1(j), S1(j+1) =================
         // S_t and P_t share TMEM columns: S_t(j+1) is issued after PV_t(j),
-        // which reads P_t(j), and the tensor core runs one thread's MMAs in order
+        // which reads P_t(j), and the tensor core runs one thread's MMAs in
+        // order; an item's first S_t follows the previous item's last PV_t
+        // the same way
+        setmaxnreg_dec<80>();
         if (lane == 0) {
             constexpr uint32_t ID = idesc_e4m3(128, 128);
             constexpr uint32_t HI = sdesc_hi(1024);
             const uint32_t q_lo = sdesc_lo(sQ, 16);
-            auto issue_s = [&](int t, int j) {
-                const uint32_t k_lo = sdesc_lo(sKV + ((2 * j) % kF8Slots) * kF8Tile, 16);
+            auto issue_s = [&](int t, int slot) {
+                const uint32_t k_lo = sdesc_lo(sKV + slot * kF8Tile, 16);
                 const uint32_t a_lo = q_lo + ((t * kF8Tile) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)  // 32 e4m3 = 32 bytes of the 128-byte rows
                     mma_f8_ss(tbase + t * 128, sdesc_at(a_lo, HI, ks * 32), sdesc_at(k_lo, HI, ks * 32),
                               ID, ks > 0);
             };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t v_lo = sdesc_lo(sKV + ((2 * j + 1) % kF8Slots) * kF8Tile, 16);
+            auto issue_pv = [&](int t, int slot, bool acc) {
+                const uint32_t v_lo = sdesc_lo(sKV + slot * kF8Tile, 16);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)  // 32 keys = 8 TMEM columns of P
                     mma_f8_ts(tbase + 256 + t * 128, tbase + t * 128 + ks * 8,
-                              sdesc_at(v_lo, HI, ks * 32), ID, (j > 0 || ks > 0) ? 1u : 0u);
+                              sdesc_at(v_lo, HI, ks * 32), ID, (acc || ks > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(BAR_Q, 0, a.watch, 53);
-            if (ok && (ok = mbar_wait(BAR_KVF(0), 0, a.watch, 53))) {
+            bool ok = true;
+            int e = 0, it = 0, cnt[2] = {0, 0};
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+                const Item I = item(w);
+                if (!(ok = mbar_wait(BAR_Q, it & 1, a.watch, 53))) break;
+                if (!(ok = mbar_wait(BAR_KVF(e % kF8Slots), (e / kF8Slots) & 1, a.watch, 53))) break;
                 tc_fence_after();
-                issue_s(0, 0);
+                issue_s(0, e % kF8Slots);
                 mma_commit(BAR_SF(0));
-                issue_s(1, 0);
+                issue_s(1, e % kF8Slots);
                 mma_commit(BAR_SF(1));
-                mma_commit(BAR_KVE(0));
-            }
-            // p_full(t) for block j also means V_j and K_{j+1} have landed
-            for (int j = 0; j < nkv && ok; ++j) {
-                const int vslot = (2 * j + 1) % kF8Slots, kslot = (2 * j + 2) % kF8Slots;
-                if (j < nkv0) {
-                    if (!(ok = mbar_wait(BAR_PF(0), j & 1, a.watch, 54))) break;
+                mma_commit(BAR_KVE(e % kF8Slots));
+                // p_full(t) for block j also means V_j and K_{j+1} have landed
+                for (int j = 0; j < I.nkv && ok; ++j) {
+                    const int vslot = (e + 2 * j + 1) % kF8Slots, kslot = (e + 2 * j + 2) % kF8Slots;
+                    if (j < I.nkv0) {
+                        if (!(ok = mbar_wait(BAR_PF(0), cnt[0] & 1, a.watch, 54))) break;
+                        ++cnt[0];
+                        tc_fence_after();
+                        issue_pv(0, vslot, j > 0);
+                        if (j == I.nkv0 - 1) mma_commit(BAR_OF(0));
+                    }
+                    if (j + 1 < I.nkv0) {
+                        issue_s(0, kslot);
+                        mma_commit(BAR_SF(0));
+                    }
+                    if (!(ok = mbar_wait(BAR_PF(1), cnt[1] & 1, a.watch, 54))) break;
+                    ++cnt[1];
                     tc_fence_after();
-                    issue_pv(0, j);
-                    if (j == nkv0 - 1) mma_commit(BAR_OF(0));
+                    issue_pv(1, vslot, j > 0);
+                    mma_commit(BAR_KVE(vslot));
+                    if (j == I.nkv - 1) mma_commit(BAR_OF(1));
+                    if (j + 1 < I.nkv) {
+                        issue_s(1, kslot);
+                        mma_commit(BAR_SF(1));
+                        mma_commit(BAR_KVE(kslot));
+                    }
                 }
-                if (j + 1 < nkv0) {
-                    issue_s(0, j + 1);
-                    mma_commit(BAR_SF(0));
-                }
-                if (!(ok = mbar_wait(BAR_PF(1), j & 1, a.watch, 54))) break;
-                tc_fence_after();
-                issue_pv(1, j);
-                mma_commit(BAR_KVE(vslot));
-                if (j == nkv - 1) mma_commit(BAR_OF(1));
-                if (j + 1 < nkv) {
-                    issue_s(1, j + 1);
-                    mma_commit(BAR_SF(1));
-                    mma_commit(BAR_KVE(kslot));
-                }
+                if (!ok) break;
+                e += 2 * I.nkv;
+                mma_commit(BAR_QE);  // the item's score products have read Q
             }
             mma_commit(BAR_DONE);
             mbar_drain(BAR_DONE, 0, a.watch, 55);
         }
         __syncwarp();
+    } else if (warp == kF8WarpMma + 3) {
+        setmaxnreg_dec<80>();  // idle: completes the issue warpgroup
     } else {
         // ================= softmax: one query row per thread =================
+        setmaxnreg_inc<208>();
         const int t = warp >> 2;   // query tile
         const int wq = warp & 3;   // TMEM lanes 32 wq ..
         const int r = wq * 32 + lane;
-        const int qt = 2 * qb + t;  // 128-row query block of the tile
-        const int grow = qt * 128 + r;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tbase + t * 128 + lane_off, tO = tbase + 256 + t * 128 + lane_off;
-        const float sq = qt < a.nb ? a.sq[(static_cast<size_t>(b) * a.Hq + h) * a.nb + qt] : 0.f;
-        const float* skrow = a.sk + (static_cast<size_t>(b) * a.Hkv + hk) * a.nb;
-        const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
-        const int nkv_mine = t ? nkv : nkv0;
-        float m_ref = -INFINITY, l = 0.f;
+        const uint32_t stg = sStage + warp * 2048;
         bool ok = true;
-        for (int j = 0; j < nkv_mine; ++j) {
-            if (!(ok = mbar_wait_warp(BAR_SF(t), j & 1, a.watch, 56))) break;
-            tc_fence_after();
-            // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
-            // and every exponent is one FMA, two columns per packed f32x2 op
-            const float sl2 = a.scale_log2 * sq * skrow[j];
-            uint32_t s[128];
-            tmem_ld32(tS + 0, s);
-            tmem_ld32(tS + 32, s + 32);
-            tmem_ld32(tS + 64, s + 64);
-            tmem_ld32(tS + 96, s + 96);
-            tmem_wait_ld();
-            reg_fence<128>(s);
-            const int kbase = j * 128;
-            if (kbase + 127 > lim) {
+        int nsf = 0, nof = 0;  // phases of s_full and o_final so far
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+            const Item I = item(w);
+            const int qt = 2 * I.qb + t;  // 128-row query block of the tile
+            const int grow = qt * 128 + r;
+            const float sq =
+                qt < a.nb ? a.sq[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.nb + qt] : 0.f;
+            const float* skrow = a.sk + (static_cast<size_t>(I.b) * a.Hkv + I.hk) * a.nb;
+            const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
+            const int nkv_mine = t ? I.nkv : I.nkv0;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < nkv_mine; ++j) {
+                if (!(ok = mbar_wait_warp(BAR_SF(t), nsf & 1, a.watch, 56))) break;
+                ++nsf;
+                tc_fence_after();
+                // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
+                // and every exponent is one FMA, two columns per packed f32x2 op
+                const float sl2 = a.scale_log2 * sq * skrow[j];
+                uint32_t s[128];
+                tmem_ld32(tS + 0, s);
+                tmem_ld32(tS + 32, s + 32);
+                tmem_ld32(tS + 64, s + 64);
+                tmem_ld32(tS + 96, s + 96);
+                tmem_wait_ld();
+                reg_fence<128>(s);
+                const int kbase = j * 128;
+                if (kbase + 127 > lim) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    s[c] = (kbase + c > lim) ? __float_as_uint(-INFINITY) : s[c];
-            }
-            float mk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
-#pragma unroll
-            for (int c = 16; c < 128; c += 16)
+                    for (int c = 0; c < 128; ++c)
+                        s[c] = (kbase + c > lim) ? __float_as_uint(-INFINITY) : s[c];
+                }
+                float mk[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    mk[i] = fmax3(mk[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
-            const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
-                                   fmaxf(mk[6], mk[7])) * sl2;
-            const float m_new = fmaxf(m_ref, mx);
-            const bool need = m_new > m_ref + 8.f;  // lazy rescale: P stays <= 2^8 < 448
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2(m_ref - m_new);
-                l *= alpha;
-                m_ref = m_new;
-            }
-            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
-            uint64_t ls2[2] = {0, 0};
-            uint32_t pk[32];
+                    mk[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                float e0, e1, e2, e3;
-                f2_split(fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, negx2),
-                         e0, e1);
-                f2_split(fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2,
-                              negx2), e2, e3);
-                const float p0 = ex2(e0), p1 = ex2(e1), p2 = ex2(e2), p3 = ex2(e3);
-                ls2[0] = add2(ls2[0], f2(p0, p1));
-                ls2[1] = add2(ls2[1], f2(p2, p3));
-                pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
-            }
-            {
-                float a0, a1;
-                f2_split(add2(ls2[0], ls2[1]), a0, a1);
-                l += a0 + a1;
-            }
-            tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S_t
-            // O_t was last written by PV_t(j-1), which finished before S_t(j)
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                for (int c = 16; c < 128; c += 16)
 #pragma unroll
-                for (int cb = 0; cb < 128; cb += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + cb, o);
-                    tmem_wait_ld();
-                    reg_fence<32>(o);
-                    const uint64_t ax2 = f2(alpha, alpha);
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float u0, u1;
-                        f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2),
-                                 u0, u1);
-                        o[i] = __float_as_uint(u0);
-                        o[i + 1] = __float_as_uint(u1);
-                    }
-                    tmem_st32(tO + cb, o);
+                    for (int i = 0; i < 8; ++i)
+                        mk[i] = fmax3(mk[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
+                const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                                       fmaxf(mk[6], mk[7])) * sl2;
+                const float m_new = fmaxf(m_ref, mx);
+                const bool need = m_new > m_ref + 8.f;  // lazy rescale: P stays <= 2^8 < 448
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
                 }
+                const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+                uint64_t ls2[2] = {0, 0};
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    float e0, e1, e2, e3;
+                    f2_split(fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, negx2),
+                             e0, e1);
+                    f2_split(fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2,
+                                  negx2), e2, e3);
+                    const float p0 = ex2(e0), p1 = ex2(e1), p2 = ex2(e2), p3 = ex2(e3);
+                    ls2[0] = add2(ls2[0], f2(p0, p1));
+                    ls2[1] = add2(ls2[1], f2(p2, p3));
+                    pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+                }
+                {
+                    float a0, a1;
+                    f2_split(add2(ls2[0], ls2[1]), a0, a1);
+                    l += a0 + a1;
+                }
+                tmem_st32(tS, pk);  // P (e4m3) over the first 32 columns of S_t
+                // O_t was last written by PV_t(j-1), which finished before S_t(j)
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int cb = 0; cb < 128; cb += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cb, o);
+                        tmem_wait_ld();
+                        reg_fence<32>(o);
+                        const uint64_t ax2 = f2(alpha, alpha);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float u0, u1;
+                            f2_split(mul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), ax2),
+                                     u0, u1);
+                            o[i] = __float_as_uint(u0);
+                            o[i + 1] = __float_as_uint(u1);
+                        }
+                        tmem_st32(tO + cb, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR_PF(t));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR_PF(t));
-        }
-        // ---- epilogue: O * sv / l -> bf16; lse.  Rows reach global memory
-        // through a per-warp transpose in the tile's Q buffer (idle once
-        // o_final(t) says the tile's last product is done): a thread writes its
-        // row's 64-byte piece of a 32-column chunk, then each store instruction
-        // writes whole pieces of eight rows (16-byte quarters of row R at
-        // R * 64 + 16 * (q ^ ((R >> 1) & 3)), free of bank conflicts).
-        const bool ok_e = ok && mbar_wait_warp(BAR_OF(t), 0, a.watch, 57);
-        if (ok_e) {  // every lane takes part in the (warp-collective) TMEM loads
+            if (!ok) break;
+            // ---- epilogue: O * sv / l -> bf16; lse.  Rows reach global memory
+            // through this warp's transpose buffer: a thread writes its row's
+            // 64-byte piece of a 32-column chunk, then each store instruction
+            // writes whole pieces of eight rows (16-byte quarters of row R at
+            // R * 64 + 16 * (q ^ ((R >> 1) & 3)), free of bank conflicts).  The
+            // next item's first P V product overwrites O_t only after this
+            // tile's next p_full arrival, which follows the loads below.
+            if (!(ok = mbar_wait_warp(BAR_OF(t), nof & 1, a.watch, 57))) break;
+            ++nof;
             tc_fence_after();
-            const float f = (l > 0.f) ? a.sv[static_cast<size_t>(b) * a.Hkv + hk] / l : 0.f;
-            const uint32_t stg = sQ + t * kF8Tile + wq * 2048;
+            const float f = (l > 0.f) ? a.sv[static_cast<size_t>(I.b) * a.Hkv + I.hk] / l : 0.f;
             const int wrow0 = qt * 128 + wq * 32;  // the warp's first query
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
@@ -484,14 +545,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 tmem_ld32(tO + cb, o);
                 tmem_wait_ld();
                 reg_fence<32>(o);
-                uint32_t w[16];
+                uint32_t wv[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+                    wv[i] = pack_bf16(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    st_shared_v4(stg + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4), w[4 * q4],
-                                 w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+                    st_shared_v4(stg + lane * 64 + ((q4 ^ ((lane >> 1) & 3)) << 4), wv[4 * q4],
+                                 wv[4 * q4 + 1], wv[4 * q4 + 2], wv[4 * q4 + 3]);
                 __syncwarp();
 #pragma unroll
                 for (int s8 = 0; s8 < 4; ++s8) {
@@ -500,13 +561,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     ld_shared_v4(stg + R * 64 + ((q4 ^ ((R >> 1) & 3)) << 4), v);
                     if (wrow0 + R < a.N)
                         *reinterpret_cast<uint4*>(
-                            a.o + ((static_cast<size_t>(b) * a.N + wrow0 + R) * a.Hq + h) * 128 + cb +
-                            q4 * 8) = make_uint4(v[0], v[1], v[2], v[3]);
+                            a.o + ((static_cast<size_t>(I.b) * a.N + wrow0 + R) * a.Hq + I.h) * 128 +
+                            cb + q4 * 8) = make_uint4(v[0], v[1], v[2], v[3]);
                 }
                 __syncwarp();
             }
             if (grow < a.N)
-                a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.N + grow] =
+                a.lse[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.N + grow] =
                     (m_ref + log2f(l)) * 0.6931471805599453f;
         }
     }
@@ -519,7 +580,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
 }
 
-constexpr int kF8Smem = 1024 + 2 * kF8Tile + kF8Slots * kF8Tile + kF8Bars * 8 + 16;
+constexpr int kF8Smem = 1024 + 2 * kF8Tile + kF8Slots * kF8Tile + kF8Stage + kF8Bars * 8 + 16;
 
 }  // namespace
 
@@ -544,10 +605,11 @@ cudaError_t launch_fp8(const Fp8Maps& m, const Fp8Args& a, cudaStream_t st) {
     if ((e = cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kF8Smem)) != cudaSuccess)
         return e;
-    const long long nblk = static_cast<long long>((a.nb + 1) / 2) * a.B * a.Hq;
-    if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    fa_fp8_fwd_kernel<<<static_cast<unsigned>(nblk), kF8Threads, kF8Smem, st>>>(m.q8, m.k8, m.vt8,
-                                                                              a);
+    const long long items = static_cast<long long>((a.nb + 1) / 2) * a.B * a.Hq;
+    if (items <= 0 || items > 0x7fffffffLL || a.num_ctas <= 0) return cudaErrorInvalidConfiguration;
+    // persistent: one CTA per SM (shared memory and registers allow no more)
+    const unsigned grid = static_cast<unsigned>(items < a.num_ctas ? items : a.num_ctas);
+    fa_fp8_fwd_kernel<<<grid, kF8Threads, kF8Smem, st>>>(m.q8, m.k8, m.vt8, a);
     return cudaGetLastError();
 }
 

@@ -167,6 +167,7 @@ struct Fp8Args {
     int causal;
     int rotate;         // q, k rows multiplied by diag(signs) H_128 before quantising
     int quantize, attend;  // which of the two steps to run
+    int num_ctas;       // persistent CTAs to launch at most (the device's SM count)
     float scale_log2;   // scale * log2(e), / 128 when rotated (H_128 H_128^T = 128 I)
     Watch watch;         // status words, time limit and id of the launch
 };

@@ -556,8 +556,10 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
 
 
 def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
-    """One CTA per work item with two query tiles (the FP8 forward runs it
-    with no copy warp): tile 0 multiplies key blocks [0, nkv0), tile 1
+    """One CTA per work item with two query tiles, the epilogue staging O in
+    the Q buffers behind a bar.sync (the forward kernels' earlier one-item
+    form; both now run fwd_persistent_model's protocol, the FP8 forward as
+    its d = 128 dense case without a copy warp): tile 0 multiplies key blocks [0, nkv0), tile 1
     [0, nkv) (nkv0 < nkv on the causal diagonal); four softmax warps per
     tile, warp q owning rows 32q.. of S_t and O_t; the epilogue stages O in
     Q_t's buffer."""
@@ -696,8 +698,9 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
     landed, committed to pv_done(t).  Dense rings are then released by both
     issuers (kv_empty counts 2); tile 0's issuer releases the entries of the
     blocks past its causal limit with plain arrivals once the slot's previous
-    phase has completed.  Otherwise (d = 128) one issuer, P over S_t, and a
-    gate warp folding V(k), K(k+1) landed into p_full(t).
+    phase has completed.  Otherwise (d = 128, and the FP8 forward: dense,
+    copy_q=False) one issuer, P over S_t, and a gate warp folding V(k),
+    K(k+1) landed into p_full(t).
 
     timeouts: every wait is bounded (simulate_with_timeouts decides its
     outcome) and each role takes the kernel's failure path: it stops issuing,
@@ -1373,8 +1376,8 @@ def simulate_with_timeouts(model, seed, p_spurious=0.0, limit=400, max_steps=200
 
 
 def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
-    """The one-item two-tile forward's roles (the FP8 forward, copy_q=False)
-    with every bounded wait's two outcomes:
+    """The one-item two-tile forward's roles (the earlier form of both
+    forward kernels) with every bounded wait's two outcomes:
     producer, gate, copy warp, MMA thread and the eight softmax warps (four
     per query tile), the epilogue's bar.sync over a tile's four warps, and the
     teardown __syncthreads over every role.  drop = (t, j): the gate's
