@@ -78,6 +78,7 @@ CASES = [  # (B, N, Hq, Hkv, causal, rotate)
     (2, 128, 2, 1, True, False),
     (1, 1000, 8, 2, True, True),
     (1, 77, 2, 2, False, True),
+    (2, 600, 48, 8, True, True),  # 288 items: several per persistent CTA
 ]
 
 

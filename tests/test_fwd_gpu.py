@@ -45,6 +45,12 @@ SHAPES = [
     (2, 3, 3, 700, 64, False),
     (1, 4, 4, 1024, 128, True),
     (1, 16, 1, 640, 128, True),
+    # more (batch, head, 256-row block) items than the GB300 has SMs (152):
+    # every persistent CTA takes two to four items, longest first when causal
+    (2, 48, 8, 600, 128, True),
+    (1, 80, 10, 530, 128, False),
+    (2, 64, 8, 520, 64, True),
+    (1, 96, 96, 400, 64, False),
 ]
 
 
