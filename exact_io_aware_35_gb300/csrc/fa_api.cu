@@ -527,12 +527,14 @@ fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* 
         return FA_ERR_INVALID_ARG;
     const int nb = (N + kBM - 1) / kBM;
     if (static_cast<long long>(B) * H * nb > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    if (nb > kSparseMaxBlocks) return FA_ERR_UNSUPPORTED;
     DeviceInfo* di = nullptr;
     if ((st = device_ready(&di)) != FA_OK) return st;
     FwdMaps maps;
     if ((st = make_map(&maps.q, q, B, N, H, d)) != FA_OK) return st;
     if ((st = make_map(&maps.k, k, B, N, Hkv, d)) != FA_OK) return st;
     if ((st = make_map(&maps.v, v, B, N, Hkv, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.o, o, B, N, H, d)) != FA_OK) return st;
     // the forward kernel, each of its two query tiles walking its own mask row
     FwdArgs a;
     a.o = static_cast<uint16_t*>(o);

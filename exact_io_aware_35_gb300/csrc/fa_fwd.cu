@@ -45,6 +45,10 @@
 namespace fa {
 namespace {
 
+// Block-sparse: words of the per-tile mask bitmask in shared memory; rows of
+// up to 32 x 224 = 7,168 key blocks (N <= 917,504) fit beside the K/V ring.
+constexpr int kSparseMaskWords = kSparseMaxBlocks / 32;
+
 template <int D, bool SPARSE>
 struct FwdCfg {
     static constexpr int CHUNK = kBM * 128;          // one 64-column chunk of a 128-row tile
@@ -59,10 +63,14 @@ struct FwdCfg {
     // warp; block-sparse CTAs run one item each and use their tile's Q buffer
     static constexpr int SMEM_STAGE = SPARSE ? 0 : 8 * 2048;
     // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
-    // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done
-    static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1;
+    // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done, and for
+    // block-sparse epi[2] (a tile's O staged for its TMA store)
+    static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1 + (SPARSE ? 2 : 0);
+    // block-sparse: the item's two mask rows as bitmasks (one bit per key
+    // block), read from global memory once when the CTA starts
+    static constexpr int SMEM_MASK = SPARSE ? (8 + 2 * kSparseMaskWords) * 4 : 0;
     static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + SMEM_Q + SMEM_KV + SMEM_STAGE + NBAR * 8 + 16;
+        1024 /*align slack*/ + SMEM_Q + SMEM_KV + SMEM_STAGE + NBAR * 8 + 16 + SMEM_MASK;
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
     // and, at D = 64, P0 [384,448) P1 [448,512): P (fp16 or bf16 pairs) gets
     // columns of its own instead of overwriting S_t (SPLITP).
@@ -93,7 +101,10 @@ constexpr float kRescaleThreshold = 8.0f;
 
 // The key blocks an item's two query tiles multiply.  Tile t takes the
 // blocks below n[t] (the causal diagonal or the ragged end), and, with a block
-// mask (SPARSE), only those whose mask byte is set.
+// mask (SPARSE), only those whose mask byte is set: count[t] blocks, the
+// highest of them last[t].  Blocks are taken in increasing order, so only a
+// tile's last block can need the element mask (only block n[t] - 1 reaches
+// past the diagonal or the ragged end).
 //   Dense: the tiles share K_j, V_j; every role walks j = 0 .. n[1] - 1, block
 //   j in the item's ring entries 2j (K) and 2j + 1 (V), and tile 0 just stops
 //   one block early on the diagonal.
@@ -101,54 +112,125 @@ constexpr float kRescaleThreshold = 8.0f;
 //   rows differ, and a shared walk would idle one tile on every block only
 //   the other has).  The tiles advance by step k, the k-th block of each; the
 //   ring holds K_0(0), K_1(0), then per step, tile by tile, V_t(k) and
-//   K_t(k+1) of the tiles that still have blocks.
+//   K_t(k+1) of the tiles that still have blocks.  That order depends only on
+//   the counts, so the issuers, the gate and the softmax run counted loops;
+//   only the producer needs the block indices, which it takes from the rows'
+//   bitmasks in shared memory (BlockCursor).
 template <bool SPARSE>
 struct TileBlocks {
     int n[2];
-    const uint8_t* row[2];  // SPARSE: the tiles' mask rows (null: the tile has no block)
-    __device__ __forceinline__ bool has(int t, int u) const {
-        if (u >= n[t]) return false;
-        return SPARSE ? (row[t] != nullptr && row[t][u] != 0) : true;
-    }
-    __device__ __forceinline__ int next_of(int t, int u) const {  // tile t's next block, or -1
-        if constexpr (!SPARSE) {
-            return u + 1 < n[t] ? u + 1 : -1;
-        } else {
-            for (++u; u < n[t]; ++u)
-                if (has(t, u)) return u;
-            return -1;
+    int count[2];
+    int last[2];  // -1 for a tile with no block
+};
+
+// The set bits of a tile's bitmask in increasing order (bit u of word u / 32:
+// block u is selected and below n[t]); `base` is the bitmask's shared-memory
+// address (32-bit state throughout: the producer that walks it runs on few
+// registers).
+struct BlockCursor {
+    uint32_t base;
+    int wd, nw;
+    uint32_t cur;
+    __device__ __forceinline__ BlockCursor(uint32_t b, int n)
+        : base(b), wd(0), nw((n + 31) >> 5), cur(nw > 0 ? ld_shared_u32(b) : 0u) {}
+    __device__ __forceinline__ int next() {  // the next block, or -1
+        while (cur == 0u) {
+            if (++wd >= nw) return -1;
+            cur = ld_shared_u32(base + 4u * wd);
         }
-    }
-    __device__ __forceinline__ int first_of(int t) const {  // tile t's first block, or -1
-        return has(t, 0) ? 0 : next_of(t, 0);
+        const int u = wd * 32 + __ffs(static_cast<int>(cur)) - 1;
+        cur &= cur - 1u;
+        return u;
     }
 };
 
-// One work item: (batch, head, 256-query block), longest blocks first, the
-// heads of one KV group adjacent.
+// Block-sparse shared memory beside the ring: eight words of per-warp partial
+// counts (build_mask_bits), then each tile's bitmask.
+constexpr int kSparseMaskHead = 8;
+
+// One work item: (batch, head, 256-query block).  Dense: longest blocks
+// first over the whole launch, the heads of one KV group adjacent.  SPARSE:
+// the items of one (batch, KV head) adjacent (longest first within it), so
+// that the CTAs running at one time read the scattered K/V blocks of one or
+// two KV heads.
+// SPARSE: `mk` is the CTA's shared-memory copy of the item's mask rows
+// (build_mask_bits; a block-sparse CTA runs exactly one item), or null while
+// it is being built.
 template <bool SPARSE>
 struct Item {
-    int b, h, hk, row0;
+    int b, h, hk, row0, qb;
     TileBlocks<SPARSE> blk;
-    __device__ __forceinline__ Item(int w, const FwdArgs& a) {
-        const int per = a.B * a.Hq;
-        const int qb = a.n_qblk - 1 - w / per;
-        const int bh = w % per;
-        b = bh / a.Hq;
-        h = bh % a.Hq;
-        hk = h / a.g;
+    __device__ __forceinline__ Item(int w, const FwdArgs& a, const uint32_t* mk) {
+        if constexpr (SPARSE) {
+            const int per_kv = a.n_qblk * a.g;
+            const int bk = w / per_kv, r = w % per_kv;
+            b = bk / a.Hkv;
+            hk = bk % a.Hkv;
+            qb = a.n_qblk - 1 - r / a.g;
+            h = hk * a.g + r % a.g;
+        } else {
+            const int per = a.B * a.Hq;
+            qb = a.n_qblk - 1 - w / per;
+            const int bh = w % per;
+            b = bh / a.Hq;
+            h = bh % a.Hq;
+            hk = h / a.g;
+        }
         row0 = qb * 2 * kBM;
         const int nkv_all = (a.N + kBN - 1) / kBN;
         blk.n[0] = a.causal ? min(row0 / kBN + 1, nkv_all) : nkv_all;
         blk.n[1] = a.causal ? min((row0 + kBM) / kBN + 1, nkv_all) : nkv_all;
-        blk.row[0] = blk.row[1] = nullptr;
-        if (SPARSE)
-            for (int t = 0; t < 2; ++t)
-                if (2 * qb + t < nkv_all)
-                    blk.row[t] =
-                        a.block_mask + (static_cast<size_t>(h) * nkv_all + 2 * qb + t) * nkv_all;
+        for (int t = 0; t < 2; ++t) {
+            blk.count[t] = blk.n[t];
+            blk.last[t] = blk.n[t] - 1;
+        }
+        if (SPARSE && mk != nullptr)
+            for (int t = 0; t < 2; ++t) {
+                // warps t, t + 2, t + 4, t + 6 built tile t: (count << 16) | (last + 1)
+                int c = 0, l1 = 0;
+                for (int i = t; i < 8; i += 2) {
+                    const uint32_t p = mk[i];
+                    c += static_cast<int>(p >> 16);
+                    l1 = max(l1, static_cast<int>(p & 0xffffu));
+                }
+                blk.count[t] = c;
+                blk.last[t] = l1 - 1;
+            }
+    }
+    // tile t's row of the global block mask (null past the last query block)
+    __device__ __forceinline__ const uint8_t* mask_row(const FwdArgs& a, int t) const {
+        const int nkv_all = (a.N + kBN - 1) / kBN;
+        if (2 * qb + t >= nkv_all) return nullptr;
+        return a.block_mask + (static_cast<size_t>(h) * nkv_all + 2 * qb + t) * nkv_all;
+    }
+    // SPARSE: tile t's bitmask in the shared-memory copy at address mk
+    __device__ __forceinline__ BlockCursor cursor(uint32_t mk, int t) const {
+        return BlockCursor(mk + 4u * (kSparseMaskHead + t * kSparseMaskWords), blk.n[t]);
     }
 };
+
+// Block-sparse: warps 0-7 turn the item's two mask rows into bitmasks (warp
+// w takes tile w & 1 and every fourth word from w >> 1): 32 coalesced byte
+// loads and a ballot per word, bits at or past the tile's limit n[t] left
+// clear (a row past the last query block has none).  Each warp also leaves
+// its words' block count and highest block + 1 in its head word.
+template <bool SPARSE>
+__device__ __forceinline__ void build_mask_bits(const Item<SPARSE>& I, const FwdArgs& a,
+                                                uint32_t* mk, int warp, int lane) {
+    const int t = warp & 1;
+    const uint8_t* row = I.mask_row(a, t);
+    const int n = I.blk.n[t];
+    int c = 0, l1 = 0;
+    for (int wd = warp >> 1; wd * 32 < n; wd += 4) {
+        const int u = wd * 32 + lane;
+        const bool on = row != nullptr && u < n && row[u] != 0;
+        const uint32_t word = __ballot_sync(0xffffffffu, on);
+        if (lane == 0) mk[kSparseMaskHead + t * kSparseMaskWords + wd] = word;
+        c += __popc(word);
+        if (word != 0u) l1 = wd * 32 + 32 - __clz(static_cast<int>(word));
+    }
+    if (lane == 0) mk[warp] = (static_cast<uint32_t>(c) << 16) | static_cast<uint32_t>(l1);
+}
 
 // F16: P is rounded to fp16 (not bf16) and multiplies the fp16 copy of V,
 // scaled by 2^v (the training forward, whose O feeds the backward's D).
@@ -156,7 +238,8 @@ struct Item {
 template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdArgs a) {
     using C = FwdCfg<D, SPARSE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -166,6 +249,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sStage = sKV + C::SMEM_KV;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_Q + C::SMEM_KV + C::SMEM_STAGE);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+    uint32_t* mbits = tmem_slot + 4;  // block-sparse bitmasks (SMEM_MASK bytes)
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t BAR_Q = bar0;        // the item's Q tiles landed
     const uint32_t BAR_QE = bar0 + 8u;  // the item's Q tiles no longer read
@@ -178,6 +262,7 @@ __global__ void __launch_bounds__(384, 1)
     auto BAR_SE = [&](int t) { return bar0 + 8u * (8 + 2 * C::NSLOT + t); };
     auto BAR_PVD = [&](int t) { return bar0 + 8u * (10 + 2 * C::NSLOT + t); };
     const uint32_t BAR_DONE = bar0 + 8u * (12 + 2 * C::NSLOT);
+    auto BAR_EPI = [&](int t) { return bar0 + 8u * (13 + 2 * C::NSLOT + t); };
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -200,6 +285,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(BAR_OF(t), 1);
             mbar_init(BAR_SE(t), 4);  // one arrival per softmax warp of the tile
             mbar_init(BAR_PVD(t), 1);
+            if (SPARSE) mbar_init(BAR_EPI(t), 4);  // likewise
         }
         mbar_init(BAR_DONE, kIssuers);
         fence_barrier_init();
@@ -208,6 +294,8 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
         tmem_relinquish();
     }
+    if constexpr (SPARSE)
+        if (warp < 8) build_mask_bits(Item<SPARSE>(blockIdx.x, a, nullptr), a, mbits, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -215,7 +303,8 @@ __global__ void __launch_bounds__(384, 1)
     // Registers: the launch gives every thread 168 (384 x 168 = 64,512); each
     // role below starts by moving its warpgroup's share: the softmax
     // warpgroups, which hold a 128-column row each, take 208 and the issue /
-    // copy warpgroup keeps 80 (2 x 128 x 208 + 128 x 80 = 63,488).
+    // copy warpgroup keeps 88 (2 x 128 x 208 + 128 x 88 = 64,512, the whole
+    // launch pool).
 
     constexpr uint32_t IDESC_QK = idesc_bf16(kBM, kBN, false, false);
     constexpr uint32_t IDESC_PV = idesc_16(kBM, D, false, true, F16);
@@ -245,7 +334,7 @@ __global__ void __launch_bounds__(384, 1)
 
     if (warp == kWarpLoad) {
         // ================= TMA producer =================
-        setmaxnreg_dec<80>();
+        setmaxnreg_dec<88>();
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
@@ -258,7 +347,7 @@ __global__ void __launch_bounds__(384, 1)
             int e = 0;   // ring entry, running over the items
             int it = 0;  // items started
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
-                const Item<SPARSE> I(w, a);
+                const Item<SPARSE> I(w, a, mbits);
                 // the previous item's score products and q copy are done with Q
                 if (it > 0 && !(ok = mbar_wait(BAR_QE, (it - 1) & 1, a.watch, 22))) break;
                 mbar_arrive_expect_tx(BAR_Q, 2 * C::TILE);
@@ -277,14 +366,15 @@ __global__ void __launch_bounds__(384, 1)
                     last_idx[slot] = e++;
                 };
                 if constexpr (SPARSE) {
-                    int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                    BlockCursor cur[2] = {I.cursor(smem_u32(mbits), 0), I.cursor(smem_u32(mbits), 1)};
+                    int u[2] = {cur[0].next(), cur[1].next()};
                     for (int t = 0; t < 2 && ok; ++t)
                         if (u[t] >= 0) load(&tmK, u[t]);
                     while (ok && (u[0] >= 0 || u[1] >= 0)) {
                         for (int t = 0; t < 2 && ok; ++t) {
                             if (u[t] < 0) continue;
                             load(&tmV, u[t]);
-                            const int un = I.blk.next_of(t, u[t]);
+                            const int un = cur[t].next();
                             if (ok && un >= 0) load(&tmK, un);
                             u[t] = un;
                         }
@@ -312,7 +402,7 @@ __global__ void __launch_bounds__(384, 1)
         // P_t and rescales O_t only after it.  Each ring entry is released
         // right after the product that reads it (dense entries by both
         // issuers).
-        setmaxnreg_dec<80>();
+        setmaxnreg_dec<88>();
         const int t = (warp == kWarpMma) ? 0 : 1;
         const uint32_t leader = elect_one();
         bool ok = true;
@@ -339,33 +429,26 @@ __global__ void __launch_bounds__(384, 1)
             ++npv;
         };
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
-            const Item<SPARSE> I(w, a);
+            const Item<SPARSE> I(w, a, mbits);
             if (!(ok = mbar_wait_warp(BAR_Q, it & 1, a.watch, 3))) break;
             if constexpr (SPARSE) {
-                // walk both tiles' streams to find this tile's ring entries
-                int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
-                int ek0 = -1;
-                for (int tt = 0; tt < 2; ++tt)
-                    if (u[tt] >= 0) {
-                        if (tt == t) ek0 = e;
-                        ++e;
-                    }
-                if (ek0 >= 0) qk(ek0);
-                int k = 0;
-                while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                // count both tiles' streams to find this tile's ring entries
+                const int c0 = I.blk.count[0], c1 = I.blk.count[1];
+                const int ek0 = (t == 0 || c0 == 0) ? e : e + 1;
+                e += (c0 > 0) + (c1 > 0);
+                if (I.blk.count[t] > 0) qk(ek0);
+                for (int k = 0; k < max(c0, c1) && ok; ++k)
                     for (int tt = 0; tt < 2 && ok; ++tt) {
-                        if (u[tt] < 0) continue;
+                        const int c = tt == 0 ? c0 : c1;
+                        if (k >= c) continue;
                         const int ev = e++;
-                        const int un = I.blk.next_of(tt, u[tt]);
-                        const int ek = un >= 0 ? e++ : -1;
+                        const bool more = k + 1 < c;
+                        const int ek = more ? e++ : -1;
                         if (tt == t) {
-                            if (ek >= 0) qk(ek);
-                            if (ok) pv(ev, k > 0, un < 0);
-                            ++k;
+                            if (more) qk(ek);
+                            if (ok) pv(ev, k > 0, !more);
                         }
-                        u[tt] = un;
                     }
-                }
             } else {
                 const int n = I.blk.n[t], n1 = I.blk.n[1];
                 for (int k = 0; k <= n && ok; ++k) {
@@ -398,7 +481,7 @@ __global__ void __launch_bounds__(384, 1)
         // arrival to p_full(t), but only once that barrier's previous phase
         // has completed, so the arrival can never be counted in the wrong
         // phase.
-        setmaxnreg_dec<80>();
+        setmaxnreg_dec<88>();
         if (lane == 0) {
             bool ok = true;
             int e = 0;
@@ -412,20 +495,18 @@ __global__ void __launch_bounds__(384, 1)
                 if (ok) ok = mbar_wait(BAR_KVF(ee % C::NSLOT), (ee / C::NSLOT) & 1, a.watch, 5);
             };
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-                const Item<SPARSE> I(w, a);
+                const Item<SPARSE> I(w, a, mbits);
                 if constexpr (SPARSE) {
-                    int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
-                    e += (u[0] >= 0) + (u[1] >= 0);  // the K_t(0)
-                    while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                    const int c0 = I.blk.count[0], c1 = I.blk.count[1];
+                    e += (c0 > 0) + (c1 > 0);  // the K_t(0)
+                    for (int k = 0; k < max(c0, c1) && ok; ++k)
                         for (int t = 0; t < 2 && ok; ++t) {
-                            if (u[t] < 0) continue;
+                            const int c = t == 0 ? c0 : c1;
+                            if (k >= c) continue;
                             landed(e++);
-                            const int un = I.blk.next_of(t, u[t]);
-                            if (un >= 0) landed(e++);
+                            if (k + 1 < c) landed(e++);
                             arrive(t);
-                            u[t] = un;
                         }
-                    }
                 } else {
                     const int n1 = I.blk.n[1];
                     for (int u = 0; u < n1 && ok; ++u) {
@@ -443,13 +524,13 @@ __global__ void __launch_bounds__(384, 1)
         // ================= copy: Q tiles -> fp16(q * 2^s) =================
         // Only the training forward (F16 with q16 set); then q_empty also
         // waits for this warp.
-        setmaxnreg_dec<80>();
+        setmaxnreg_dec<88>();
         if (copy_q) {
             const float mul = pow2f(ld_once(&a.f16s->q));
             const size_t row_el = static_cast<size_t>(a.Hq) * D;  // elements per token
             int it = 0;
             for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++it) {
-                const Item<SPARSE> I(w, a);
+                const Item<SPARSE> I(w, a, mbits);
                 if (!mbar_wait_warp(BAR_Q, it & 1, a.watch, 15)) break;
                 for (int t = 0; t < 2; ++t)
                     warp_tile_to_f16<D>(
@@ -463,21 +544,21 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ================= d = 128 MMA issuer (the whole warp; the leader lane issues) ======
-        setmaxnreg_dec<80>();
+        setmaxnreg_dec<88>();
         const uint32_t leader = elect_one();
         bool ok = true;
         int e = 0, it = 0;
         int cnt[2] = {0, 0};  // p_full phases waited, per tile
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
-            const Item<SPARSE> I(w, a);
+            const Item<SPARSE> I(w, a, mbits);
             if (!(ok = mbar_wait_warp(BAR_Q, it & 1, a.watch, 3))) break;
             if constexpr (SPARSE) {
                 // Per step k, tile by tile: PV_t(k) on p_full(t) (V_t(k) and
                 // K_t(k+1) landed, the gate), then S_t(k+1).  Every ring entry is
                 // released right after the product that reads it.
-                int u[2] = {I.blk.first_of(0), I.blk.first_of(1)};
+                const int c0 = I.blk.count[0], c1 = I.blk.count[1];
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (u[t] < 0) continue;
+                    if ((t == 0 ? c0 : c1) == 0) continue;
                     const int ek = e++;
                     if (!(ok = mbar_wait_warp(BAR_KVF(ek % C::NSLOT), (ek / C::NSLOT) & 1, a.watch, 4)))
                         break;
@@ -486,28 +567,25 @@ __global__ void __launch_bounds__(384, 1)
                     mma_commit_w(leader, BAR_SF(t));
                     mma_commit_w(leader, BAR_KVE(ek % C::NSLOT));
                 }
-                int k = 0;
-                while (ok && (u[0] >= 0 || u[1] >= 0)) {
+                for (int k = 0; k < max(c0, c1) && ok; ++k)
                     for (int t = 0; t < 2 && ok; ++t) {
-                        if (u[t] < 0) continue;
+                        const int c = t == 0 ? c0 : c1;
+                        if (k >= c) continue;
                         const int ev = e++;
-                        const int un = I.blk.next_of(t, u[t]);
-                        const int ek = un >= 0 ? e++ : -1;
+                        const bool more = k + 1 < c;
+                        const int ek = more ? e++ : -1;
                         if (!(ok = mbar_wait_warp(BAR_PF(t), cnt[t] & 1, a.watch, 6 + 2 * t))) break;
                         tc_fence_after();
                         issue_pv(leader, t, ev % C::NSLOT, k > 0);
                         mma_commit_w(leader, BAR_KVE(ev % C::NSLOT));
                         ++cnt[t];
-                        if (un < 0) mma_commit_w(leader, BAR_OF(t));
-                        if (ek >= 0) {
+                        if (!more) mma_commit_w(leader, BAR_OF(t));
+                        if (more) {
                             issue_qk(leader, t, ek % C::NSLOT);
                             mma_commit_w(leader, BAR_SF(t));
                             mma_commit_w(leader, BAR_KVE(ek % C::NSLOT));
                         }
-                        u[t] = un;
                     }
-                    ++k;
-                }
             } else {
                 // Per key block u (item entries 2u, 2u + 1): PV0(u) and S0(u + 1)
                 // while tile 0 has them, PV1(u), S1(u + 1).  p_full(t) for u also
@@ -575,15 +653,20 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         int nsf = 0, npf = 0, nof = 0;  // phases of s_full, p_full, o_final so far
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-            const Item<SPARSE> I(w, a);
+            const Item<SPARSE> I(w, a, mbits);
             const int grow = I.row0 + t * kBM + r;  // query index
             // last key index this row may see
             const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
             float m_ref = -INFINITY;  // reference max of the exponentials (log2 units)
             float l = 0.f;            // running sum, relative to m_ref
-            const int u0 = I.blk.first_of(t);
-            int j = 0;  // blocks of this item done so far
-            for (int u = u0; u >= 0; u = I.blk.next_of(t, u), ++j) {
+            // per-item values, read once here: inside the loop every barrier
+            // wait would force a fresh read of the item from local memory
+            const int nblk = I.blk.count[t];
+            // only the tile's last block can reach past the diagonal or the
+            // ragged end
+            const int klast = I.blk.last[t] * kBN;
+            const bool mask_last = klast + kBN - 1 > lim;
+            for (int j = 0; j < nblk; ++j) {  // the tile's j-th block
                 if (!(ok = mbar_wait_warp(BAR_SF(t), nsf & 1, a.watch, 10 + t))) break;
                 ++nsf;
                 tc_fence_after();
@@ -602,10 +685,9 @@ __global__ void __launch_bounds__(384, 1)
                 float x[kBN];
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(s[c]);
-                const int kbase = u * kBN;
-                if (kbase + kBN - 1 > lim) {  // diagonal block or ragged tail: mask
+                if (mask_last && j == nblk - 1) {  // diagonal block or ragged tail: mask
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) x[c] = (kbase + c > lim) ? -INFINITY : x[c];
+                    for (int c = 0; c < kBN; ++c) x[c] = (klast + c > lim) ? -INFINITY : x[c];
                 }
                 // row max: eight running maxima, three-input max instructions
                 float mk[8];
@@ -683,12 +765,69 @@ __global__ void __launch_bounds__(384, 1)
                 ++npf;
             }
             if (!ok) break;
+            if constexpr (SPARSE) {
+                // ---- block-sparse epilogue: O / l -> bf16 rows in the tile's
+                // own Q buffer (the 128-byte swizzle of the TMA maps), then one
+                // TMA store, which also drops the rows past N.  One item per
+                // CTA: Q_t is idle once o_final(t) says the tile's last
+                // product, and so its last score product, is done; a tile with
+                // no key block (O = 0, lse = -inf) waits for its Q load, the
+                // buffer's only other writer, instead.
+                const bool any = nblk > 0;
+                if (!(ok = any ? mbar_wait_warp(BAR_OF(t), nof & 1, a.watch, 12 + t)
+                               : mbar_wait_warp(BAR_Q, 0, a.watch, 26)))
+                    break;
+                nof += any ? 1 : 0;
+                tc_fence_after();
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                const uint32_t stage = sQ + t * C::TILE;
+#pragma unroll
+                for (int ch = 0; ch < C::NCH; ++ch) {  // 64-column chunks: one TMEM wait each
+                    uint32_t o[64];
+                    if (any) {
+                        tmem_ld32(tO + ch * 64, o);
+                        tmem_ld32(tO + ch * 64 + 32, o + 32);
+                        tmem_wait_ld();
+                        reg_fence<64>(o);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) o[i] = 0u;
+                    }
+                    const uint32_t rowbase = stage + ch * C::CHUNK + r * 128;
+#pragma unroll
+                    for (int p8 = 0; p8 < 8; ++p8) {  // 16-byte pieces of the row's 128 bytes
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            wv[i] = pack_bf16(__uint_as_float(o[8 * p8 + 2 * i]) * inv_l,
+                                              __uint_as_float(o[8 * p8 + 2 * i + 1]) * inv_l);
+                        st_shared_v4(rowbase + ((p8 ^ (r & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                if (grow < a.N)
+                    a.lse[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.N + grow] =
+                        (m_ref + log2f(l)) * 0.6931471805599453f;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR_EPI(t));
+                if (wq == 0) {  // the tile's first warp waits for all four, one lane stores
+                    if (!(ok = mbar_wait_warp(BAR_EPI(t), 0, a.watch, 27))) break;
+                    if (lane == 0) {
+                        for (int c = 0; c < C::NCH; ++c)
+                            tma_store_4d(&tmO, stage + c * C::CHUNK, c * 64, I.h, I.row0 + t * kBM,
+                                         I.b);
+                        tma_store_commit();
+                        tma_store_wait_read_all();
+                    }
+                    __syncwarp();
+                }
+                continue;
+            }
             // ---- epilogue: O / l -> bf16, each row from its thread straight to
-            // global memory.  A tile with no key block (block-sparse only) writes
-            // O = 0 and lse = -inf.  The next item's first P V product overwrites
+            // global memory.  The next item's first P V product overwrites
             // O_t only after this tile's next p_full arrival, which follows the
             // loads below.
-            const bool any = u0 >= 0;
+            const bool any = nblk > 0;
             if (any) {
                 if (!(ok = mbar_wait_warp(BAR_OF(t), nof & 1, a.watch, 12 + t))) break;
                 ++nof;
@@ -701,9 +840,7 @@ __global__ void __launch_bounds__(384, 1)
             // each store instruction writes whole pieces of eight rows (the
             // 16-byte quarters of row R at R * 64 + 16 * (q ^ ((R >> 1) & 3)),
             // which keeps both sides free of bank conflicts).
-            // (block-sparse: one item per CTA, and Q_t is idle once o_final(t)
-            // says the tile's last product is done)
-            const uint32_t stg = SPARSE ? sQ + t * C::TILE + wq * 2048 : sStage + warp * 2048;
+            const uint32_t stg = sStage + warp * 2048;
             const int wrow0 = I.row0 + t * kBM + wq * 32;  // the warp's first query
             auto store_chunk = [&](uint16_t* dstT, const uint32_t (&wv)[16], int cb) {
 #pragma unroll
@@ -778,7 +915,8 @@ cudaError_t launch_fwd_d(const FwdMaps& m, const FwdArgs& a, cudaStream_t st) {
     // whose items differ in length with the mask).
     const long long ctas = SPARSE ? items : (items < a.num_ctas ? items : a.num_ctas);
     const unsigned grid = static_cast<unsigned>(ctas);
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, a);
+    // the O map is read by the block-sparse epilogue only
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(m.q, m.k, m.v, SPARSE ? m.o : m.q, a);
     return cudaGetLastError();
 }
 

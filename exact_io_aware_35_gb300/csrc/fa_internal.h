@@ -20,6 +20,10 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 
+// Block-sparse forward: the longest mask row a thread block keeps in shared
+// memory (bits), so N <= 7,168 x 128 = 917,504.
+constexpr int kSparseMaxBlocks = 7168;
+
 // fp16 operand path.  bf16 inputs are copied to fp16 after a power-of-two
 // scaling (f16_scales_from), exact for all but the tiniest elements (bf16
 // carries 8 significant bits, fp16 11); P, P^T (at most 2^8) and dS, dS^T
@@ -181,9 +185,10 @@ struct Fp8Maps {
 // memset), then the forward kernel.
 cudaError_t launch_fp8(const Fp8Maps& maps, const Fp8Args& args, cudaStream_t stream);
 
-// Tensor maps of one call (all 4-D: d, H, N, B; box 64 x 1 x 128 x 1).
+// Tensor maps of one call (all 4-D: d, H, N, B; box 64 x 1 x 128 x 1); o is
+// set for the block-sparse forward only (its epilogue stores through it).
 struct FwdMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 struct BwdMaps {

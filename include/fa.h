@@ -253,9 +253,11 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int 
  *        head h may see key j only when block_mask[h][i / 128][j / 128] != 0
  *        (and, with causal, j <= i).  Read only.
  * A query row with no visible key gets o = 0 and lse = -inf.  Each thread
- * block takes two 128-query tiles of one head (the pipeline of fa_fwd); each
- * tile streams the K and V blocks of its own mask row.  Errors as fa_fwd;
- * FA_ERR_INVALID_ARG also for a null block_mask.
+ * block takes two 128-query tiles of one head (the pipeline of fa_fwd), reads
+ * their two mask rows once into shared memory, and each tile streams the K
+ * and V blocks of its own row.  Errors as fa_fwd; FA_ERR_INVALID_ARG also for
+ * a null block_mask; FA_ERR_UNSUPPORTED for N > 917,504 (mask rows longer
+ * than 7,168 blocks).
  */
 fa_status fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
                              const uint8_t* block_mask, int B, int H, int Hkv, int N, int d,

@@ -182,6 +182,8 @@ def test_blocksparse_invalid_arguments_rejected_on_host(lib):
     assert call(H=6, Hkv=4) == fa.FA_ERR_INVALID_ARG
     assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    # mask rows longer than the 7,168 blocks a thread block keeps in shared memory
+    assert call(N=7168 * 128 + 1) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_fp8_workspace_and_invalid_arguments(lib):

@@ -682,7 +682,7 @@ def stream_entries(sets):
 
 
 def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=False,
-                         mistake=None, timeouts=False, drop=None):
+                         mistake=None, timeouts=False, drop=None, stage_q=False):
     """The persistent forward: one CTA walks `items`, each a pair (tile 0's key
     blocks, tile 1's key blocks).  Dense items (sparse=False) share K and V
     between the tiles, ring entries K(u), V(u) per block of tile 1's range;
@@ -709,17 +709,26 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
     owes (the gate's on p_full at d = 128, the softmax warps' on s_empty at
     d = 64) never happens.
 
+    stage_q (the block-sparse kernel: one item per CTA): each tile's epilogue
+    writes its O rows into the tile's own Q buffer, arrives on epi(t) (four
+    warps), and the tile's first warp waits for it and stores the buffer (a
+    TMA store, read here as a read of the four rows).  The buffer is free once
+    o_final(t) has completed; a tile with no block waits for the Q load
+    instead.
+
     mistake: "no_q_empty" (Q reloaded without q_empty), "early_arrive" (tile
     0's issuer arrives on kv_empty without the previous-phase wait),
     "no_k_wait" (a score product before its K tile has landed), "no_pvd_wait"
     (P_t written before the previous P V product has read it), "no_of_wait"
     (the epilogue reads O without o_final), "no_drain" (the producer exits
-    without waiting for its last loads).  (The s_empty wait before an item's
+    without waiting for its last loads), "no_q_wait_empty" (stage_q: a tile with
+    no block stages O without waiting for its Q load).  (The s_empty wait before an item's
     first score product is implied by q_empty: the issuer's commit to it
     follows its last P V product, which followed the softmax's p_full; the
     kernel keeps the wait anyway.)"""
     rows = range(4)
     items = [(sorted(set(a)), sorted(set(b))) for a, b in items]
+    assert not stage_q or (sparse and len(items) == 1)
     nissue = 2 if split_p else 1
     n_roles = 1 + nissue + (0 if split_p else 1) + 8 + (1 if copy_q else 0)
 
@@ -747,7 +756,7 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
         bars = {"Q": 1, "QE": nissue + (1 if copy_q else 0), "DONE": nissue}
         for t in (0, 1):
             bars.update({f"SF{t}": 1, f"PF{t}": 128 if split_p else 129, f"OF{t}": 1,
-                         f"SE{t}": 4, f"PVD{t}": 1})
+                         f"SE{t}": 4, f"PVD{t}": 1, f"EPI{t}": 4})
         for s in range(NSLOT):
             bars[f"F{s}"] = 1
             bars[f"E{s}"] = 2 if (split_p and not sparse) else 1
@@ -992,6 +1001,18 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
                             break
                     nof += 1
                     yield ("read", {f"O.{me}": f"O{t}({i},{len(bl) - 1})"})
+                elif stage_q and mistake != "no_q_wait_empty":
+                    ok = (yield W("Q", i)) is not False
+                    if not ok:
+                        break
+                if stage_q:
+                    yield ("write", {f"Q.{me}": f"Ostage{t}"})
+                    yield ("arrive", f"EPI{t}", 1, 0)
+                    if q == 0:
+                        ok = (yield W(f"EPI{t}", 0)) is not False
+                        if not ok:
+                            break
+                        yield ("read", {f"Q.{t}.{qq}": f"Ostage{t}" for qq in rows})
             yield from teardown()
 
         roles = {"prod": producer()}
@@ -1189,6 +1210,26 @@ def test_forward_persistent_dense_protocol(items, split_p, nslot, copy_q):
 def test_forward_persistent_sparse_protocol(items, split_p, nslot):
     each_seed(fwd_persistent_model(PERSISTENT_SPARSE[items], nslot, split_p=split_p, sparse=True),
               seeds=range(40))
+
+
+SPARSE_ONE_ITEM = [it for case in PERSISTENT_SPARSE for it in case]
+
+
+@pytest.mark.parametrize("item", range(len(SPARSE_ONE_ITEM)))
+@pytest.mark.parametrize("split_p,nslot", [(False, 5), (True, 8)])
+def test_forward_sparse_one_item_epilogue_in_q_buffer(item, split_p, nslot):
+    # the block-sparse kernel: one item per CTA, O staged in the tile's own Q
+    # buffer and stored from there
+    each_seed(fwd_persistent_model([SPARSE_ONE_ITEM[item]], nslot, split_p=split_p, sparse=True,
+                                   stage_q=True), seeds=range(60))
+
+
+@pytest.mark.parametrize("split_p,nslot", [(False, 5), (True, 8)])
+def test_forward_sparse_empty_tile_must_wait_for_its_q_load(split_p, nslot):
+    # a tile with no block stages O over a Q load that may still be landing
+    assert fails_on_some_seed(fwd_persistent_model([([], [0, 3])], nslot, split_p=split_p,
+                                                   sparse=True, stage_q=True,
+                                                   mistake="no_q_wait_empty"))
 
 
 def test_forward_persistent_random_masks():
@@ -1528,34 +1569,36 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
     return model
 
 
-PERSISTENT_TIMEOUT_CASES = [  # (items, ring slots, split_p, sparse, copy_q)
-    (PERSISTENT_DENSE[0], 4, False, False, True),
-    (PERSISTENT_DENSE[0], 8, True, False, True),
-    (PERSISTENT_DENSE[2], 4, False, False, False),
-    (PERSISTENT_SPARSE[0], 5, False, True, False),
-    (PERSISTENT_SPARSE[1], 8, True, True, False),
+PERSISTENT_TIMEOUT_CASES = [  # (items, ring slots, split_p, sparse, copy_q, stage_q)
+    (PERSISTENT_DENSE[0], 4, False, False, True, False),
+    (PERSISTENT_DENSE[0], 8, True, False, True, False),
+    (PERSISTENT_DENSE[2], 4, False, False, False, False),
+    (PERSISTENT_SPARSE[0], 5, False, True, False, False),
+    (PERSISTENT_SPARSE[1], 8, True, True, False, False),
+    ([([0, 2, 3], [1, 2])], 5, False, True, False, True),
+    ([([], [0, 3])], 8, True, True, False, True),
 ]
 
 
 @pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
 def test_persistent_forward_without_faults_never_times_out(case):
-    items, nslot, split_p, sparse, copy_q = PERSISTENT_TIMEOUT_CASES[case]
+    items, nslot, split_p, sparse, copy_q, stage_q = PERSISTENT_TIMEOUT_CASES[case]
     for seed in range(20):
         assert not simulate_with_timeouts(
-            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True), seed,
-            limit=10 ** 6)
+            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True,
+                                 stage_q=stage_q), seed, limit=10 ** 6)
 
 
 @pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
 def test_persistent_forward_any_wait_running_out_ends_the_block_cleanly(case):
     # waits run out at random; whichever do, every role reaches the teardown
     # and nothing is left in flight
-    items, nslot, split_p, sparse, copy_q = PERSISTENT_TIMEOUT_CASES[case]
+    items, nslot, split_p, sparse, copy_q, stage_q = PERSISTENT_TIMEOUT_CASES[case]
     n_failed = 0
     for seed in range(80):
         n_failed += simulate_with_timeouts(
-            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True), seed,
-            p_spurious=0.01, limit=300)
+            fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True,
+                                 stage_q=stage_q), seed, p_spurious=0.01, limit=300)
     assert n_failed > 40  # the fault path ran in most schedules
 
 
