@@ -801,7 +801,7 @@ def run_sparse(args):
                          "achieved": tf / ws, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / ws / peak, "peak_source": peaks["source"] + " burst",
                          "launch_ms": ms, "algorithmic_work_per_launch": flops / ws,
-                         "traffic": None},
+                         "traffic": measured_traffic("fa_fwd_kernel", args.workload)},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
     if clk is not None:
