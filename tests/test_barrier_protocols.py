@@ -364,7 +364,7 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
 
 # -------------------------------------------------------------- dK/dV kernel
 def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, skip_dvd=False,
-               p_before_str=False):
+               p_before_str=False, three_regions=False, early_dpt=False, skip_dsf_wait=False):
     """Sixteen compute warps (g, q): query columns 32g.. of the transposed
     tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  The kernel's
     protocol (ds_smem False): a warp forms P^T(it) as soon as S^T(it) is in
@@ -372,8 +372,17 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     then, once dP^T(it) is in TMEM (SDF), copies dP^T(it) to registers (LD)
     and writes dS^T(it) over the other half ('d').  The MMA thread: dV(it)
     after P^T, S^T(it+1) over dP^T(it) after LD, dK(it) after dS^T, then
-    dP^T(it+1) over P^T(it), dS^T(it).  p_before_str (P^T formed without
-    waiting for S^T) is a planted mistake.  A variant that was tried and
+    dP^T(it+1) over P^T(it), dS^T(it).  three_regions (a variant tried at
+    d = 64, where TMEM has a third 128-column region, and measured slower:
+    dK/dV 0.551 -> 0.583 ms on gpt2s): the regions rotate, S^T(it) in
+    R[it % 3] and dP^T(it) in R[(it + 1) % 3], so dP^T(it+1) goes into the
+    region P^T, dS^T(it-1) left and is issued right after S^T(it+1), before
+    dK(it).
+    A warp then arrives on DSF(it) only once DSF(it-1) has completed (a fast
+    warp could otherwise run a step ahead into the previous phase).
+    early_dpt (that early issue with only two regions, over P^T(it), dS^T(it)),
+    skip_dsf_wait (three regions without the DSF(it-1) wait) and p_before_str
+    (P^T formed without waiting for S^T) are planted mistakes.  A variant that was tried and
     measured slower (ds_smem True, with the earlier single-step compute):
     dS^T goes to shared memory instead -- over the stage's dO tile (ds_in_do,
     d = 128) or into a buffer of its own (d = 64) -- once the MMA thread's
@@ -389,9 +398,13 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
             bars[f"STE{s}"] = 1
 
         def reg_s(it):  # S^T(it), then P^T(it) (/ dS^T(it))
+            if three_regions:
+                return "R%d" % (it % 3)
             return "Y" if it & 1 else "X"
 
         def reg_d(it):  # dP^T(it)
+            if three_regions:
+                return "R%d" % ((it + 1) % 3)
             return "X" if it & 1 else "Y"
 
         def region(r, tag):
@@ -456,16 +469,20 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
                 more = it + 1 < n_it
                 yield ("wait", "PF", it)
                 yield dv_mma(it)
+                early = three_regions or early_dpt
                 if more:
                     yield ("wait", f"STF{s2}", (it + 1) // NST)
                     yield ("wait", "LD", it)
                     yield st_mma(it + 1)  # over dP^T(it)
                     yield ("commit", "STR", it + 1)
+                    if early:  # into the third region (P^T, dS^T(it-1) were read by dK(it-1))
+                        yield dpt_mma(it + 1)
+                        yield ("commit", "SDF", it + 1)
                 if not dk_before_dsf:
                     yield ("wait", "DSF", it)
                 yield dk_mma(it)
                 yield ("commit", f"STE{s}", it // NST)
-                if more:
+                if more and not early:
                     yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
                     yield ("commit", "SDF", it + 1)
             yield ("commit", "ACC", 0)
@@ -487,6 +504,11 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
                                 f"vec{s}": f"lse,D({it})"})
                 yield ("arrive", "LD", 32, it)
                 yield ("write", {ds_buf(it, g, q): f"dS^T({it})"})
+                # with dP^T(it) issued before dK(it-1), a fast warp can reach
+                # here while DSF(it-1) still waits for slow ones: it arrives only
+                # once that phase has completed
+                if three_regions and it > 0 and not skip_dsf_wait:
+                    yield ("wait", "DSF", it - 1)
                 yield ("arrive", "DSF", 32, it)
             yield ("wait", "ACC", 0)
             yield ("read", {"dV": f"dV({n_it - 1})", "dK": f"dK({n_it - 1})"})
@@ -1169,8 +1191,9 @@ def test_dq_protocol(nj, two_issuers):
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
-def test_dkdv_protocol(n_it):
-    each_seed(dkdv_model(n_it))
+@pytest.mark.parametrize("three_regions", [False, True])
+def test_dkdv_protocol(n_it, three_regions):
+    each_seed(dkdv_model(n_it, three_regions=three_regions))
 
 
 @pytest.mark.parametrize("n_it", [1, 3, 16])
@@ -1305,6 +1328,16 @@ def test_dkdv_dk_before_ds_is_caught():
 def test_dkdv_p_before_s_ready_is_caught():
     # P^T formed from the region before S^T has been written there
     assert fails_on_some_seed(dkdv_model(4, p_before_str=True))
+
+
+def test_dkdv_three_regions_without_dsf_handshake_is_caught():
+    assert fails_on_some_seed(dkdv_model(5, three_regions=True, skip_dsf_wait=True))
+
+
+def test_dkdv_early_dp_without_third_region_is_caught():
+    # dP^T(it+1) issued before dK(it) with only two regions: it overwrites
+    # P^T(it), dS^T(it) before dK(it) and the warps have used them
+    assert fails_on_some_seed(dkdv_model(4, early_dpt=True))
 
 
 @pytest.mark.parametrize("ds_in_do", [True, False])
