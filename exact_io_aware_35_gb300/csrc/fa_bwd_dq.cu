@@ -9,17 +9,20 @@
 //
 // Pipelining.  Every MMA is 128 wide.  dP is double-buffered in TMEM and S is
 // not: as soon as both warpgroups have copied S(j) and dP(j) into registers
-// (barrier LD), the tensor core computes S(j+1) into the S buffer and dP(j+1)
-// into the other dP buffer, while the warpgroups write dS(j) (bf16 or fp16)
-// over the dP(j) columns they read.  dQ += dS(j) K_j then reads it from there
-// (barrier PF).  The warpgroups go from block j to block j+1 without waiting
-// for the tensor core, which runs S(j+1), dP(j+1) and dQ(j) meanwhile.
+// (barrier LD), the tensor core computes S(j+1) into the S buffer, while the
+// warpgroups write dS(j) (bf16 or fp16) over the dP(j) columns they read.
+// dQ += dS(j) K_j then reads it from there (barrier PF), and dP(j+2) follows
+// dQ(j) at once into that buffer: it waits for nothing the warps do, so it is
+// done long before they reach block j+2.  The tensor core's order per block is
+// S(j+1), dQ(j), dP(j+2); the warpgroups find S and dP ready at every block.
 // Four compute warpgroups: warpgroup h takes keys 32h..32h+31 of every block
 // and writes their dS into the first 16 of its own 32 dP columns, which keeps
 // the chain of loads, exponentials and stores per block short.  K and V stream through
-// separate TMA rings; a gate warp adds one arrival to LD(j) once K_{j+1} and
-// V_{j+1} have landed, so the MMA thread waits on LD and PF only (every wait
-// in the issuing thread costs tensor-core time).  Only LD carries the gate:
+// separate TMA rings, loaded in the products' first-use order (K_0, V_0, V_1,
+// K_1, V_2, K_2, ...); a gate warp adds one arrival to LD(j) once K_{j+1} has
+// landed, so S(j+1) needs one wait in the issuing thread (every wait there
+// costs tensor-core time); V_{j+2}, loaded two blocks ahead, is checked by the
+// MMA thread itself before dP(j+2).  Only LD carries the gate:
 // the warpgroups reach LD(j+1) only after S(j+1), which waits for LD(j), so no
 // arrival can land in the wrong phase.  PF needs one more step, because S(j+1)
 // is committed before the MMA thread waits for PF(j): the MMA thread arrives
@@ -178,9 +181,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     last_k[slot] = jj;
                 return true;
             };
-            // first-use order of the MMAs: K_0, V_0, K_1, V_1, ...
-            bool ok = true;
-            for (int i = 0; i < nj && ok; ++i) ok = load(i, false) && load(i, true);
+            // first-use order of the MMAs: K_0, V_0, V_1, K_1, V_2, K_2, ...
+            bool ok = load(0, false) && load(0, true);
+            for (int i = 1; i < nj && ok; ++i) ok = load(i, true) && load(i, false);
             // no copies in flight at exit: wait (bounded) for the last load of each slot
             mbar_drain(BAR_QDO, 0, a.watch, 21);
             for (int s = 0; s < C::KS; ++s)
@@ -192,15 +195,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         __syncwarp();
     } else if (warp == kDqWarpGate) {
-        // ================= gate: K_{j+1}, V_{j+1} landed -> LD(j) =================
+        // ================= gate: K_{j+1} landed -> LD(j) =================
         // Its arrival on LD(j) comes only after LD's previous phase is over.
         setmaxnreg_dec<64>();
         if (lane == 0) {
             bool ok = true;
             for (int j = 0; j < nj && ok; ++j) {
                 if (j + 1 < nj)
-                    ok = mbar_wait(BAR_KF((j + 1) % C::KS), ((j + 1) / C::KS) & 1, a.watch, 28) &&
-                         mbar_wait(BAR_VF((j + 1) % C::VS), ((j + 1) / C::VS) & 1, a.watch, 28);
+                    ok = mbar_wait(BAR_KF((j + 1) % C::KS), ((j + 1) / C::KS) & 1, a.watch, 28);
                 if (ok && j > 0) ok = mbar_wait(BAR_LD, (j - 1) & 1, a.watch, 28);
                 if (ok) mbar_arrive(BAR_LD);
             }
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 tc_fence_after();
                 return r;
             };
-            auto v_ready = [&](int jj) {  // (prologue only; the gate covers the loop)
+            auto v_ready = [&](int jj) {
                 const bool r = mbar_wait_warp(BAR_VF(jj % C::VS), (jj / C::VS) & 1, a.watch, 23);
                 tc_fence_after();
                 return r;
@@ -276,22 +278,27 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 issue_dp(0);
                 mma_commit_w(leader, BAR_SDF);
             }
+            if (ok && nj > 1 && (ok = v_ready(1))) issue_dp(1);  // into the other dP buffer
             for (int j = 0; j < nj && ok; ++j) {
-                // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j);
-                // dP(j+1) into the other dP buffer, over dS(j-1), which dQ(j-1)
-                // (issued earlier by this thread) has read; K_{j+1} and V_{j+1}
-                // have landed (the gate's arrival on LD)
+                // S(j+1) into the S buffer once both warpgroups hold S(j), dP(j)
+                // and K_{j+1} has landed (the gate's arrival on LD); its commit
+                // also covers dP(j+1), issued a block earlier
                 if (j + 1 < nj) {
                     if (!(ok = mbar_wait_warp(BAR_LD, j & 1, a.watch, 24))) break;
                     tc_fence_after();
                     issue_t(tS, q_lo, sK + ((j + 1) % C::KS) * C::TILE, IDESC_S);
-                    issue_dp(j + 1);
                     mma_commit_w(leader, BAR_SDF);
                 }
                 if (!(ok = mbar_wait_warp(BAR_PF, j & 1, a.watch, 24))) break;
                 if (leader) mbar_arrive(BAR_PFS);  // the warps may now arrive on PF(j+1)
                 tc_fence_after();
                 issue_dq(j);
+                // dP(j+2) over dS(j), which dQ(j), issued just before by this
+                // thread, reads first
+                if (j + 2 < nj) {
+                    if (!(ok = v_ready(j + 2))) break;
+                    issue_dp(j + 2);
+                }
             }
             // every issued MMA has finished before TMEM is released
             mma_commit_w(leader, BAR_ACC);

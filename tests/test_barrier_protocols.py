@@ -217,7 +217,7 @@ def ring_bars(nslot):
 
 # ---------------------------------------------------------------- dQ kernel
 def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuers=False,
-             single_dqd=False, skip_dqd=False):
+             single_dqd=False, skip_dqd=False, early_dp=False, dp_before_dq=False):
     """Sixteen compute warps (w, q): key quarter w (32 columns of S, dP, its
     dS written into the first 16) and TMEM lanes 32q.. (query rows); each
     arrives on its own.  The MMA thread
@@ -229,7 +229,14 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
     overwrites, so the dQ thread commits DQD(j % 2) after dQ(j) and the S/dP
     thread waits for it (phase j // 2) before dP(j+2); the dQ thread, which
     waits for PF, is the one that arrives on PFS.  single_dqd (one DQD
-    barrier for both buffers) and skip_dqd are planted mistakes."""
+    barrier for both buffers) and skip_dqd are planted mistakes.
+
+    early_dp: dP(j+2) is issued right after dQ(j), into the buffer dQ(j) has
+    just read, instead of next to S(j+2) behind LD(j+1); only S(j+1) waits for
+    LD(j), whose gate then folds in K_{j+1} alone, and the MMA thread waits
+    for V_{j+2} itself.  The producer loads in the products' first-use order
+    (K_0, V_0, V_1, K_1, V_2, K_2, ...).  dp_before_dq (dP(j+2) issued before
+    dQ(j)) is a planted mistake."""
     warps = [(w, q) for w in range(4) for q in range(4)]
 
     def model(rnd):
@@ -246,7 +253,8 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
             yield ("load", "QDO", 0, dict(every("Q", "Q"), dO="dO"))
             last = {}
             for i in range(nj):
-                for nm, ns in (("K", KS), ("V", VS)):
+                order = (("V", VS), ("K", KS)) if early_dp and i > 0 else (("K", KS), ("V", VS))
+                for nm, ns in order:
                     s = i % ns
                     yield ("wait", f"{nm}E{s}", i // ns - 1)
                     yield ("load", f"{nm}F{s}", i // ns, {f"{nm}{s}": f"{nm}({i})"})
@@ -259,7 +267,8 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
             for j in range(nj):
                 if j + 1 < nj:
                     yield ("wait", f"KF{(j + 1) % KS}", (j + 1) // KS)
-                    yield ("wait", f"VF{(j + 1) % VS}", (j + 1) // VS)
+                    if not early_dp:
+                        yield ("wait", f"VF{(j + 1) % VS}", (j + 1) // VS)
                 if j > 0:
                     yield ("wait", "LD", j - 1)
                 yield ("arrive", "LD", 1, j)
@@ -291,7 +300,30 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
             yield dp_mma(0)
             yield ("commit", "VE0", 0)
             yield ("commit", "SDF", 0)
+            if early_dp and nj > 1:
+                yield ("wait", "VF1", 0)
+                yield dp_mma(1)
+                yield ("commit", f"VE{1 % VS}", 1 // VS)
             for j in range(nj):
+                if early_dp:
+                    if j + 1 < nj:
+                        yield ("wait", "LD", j)
+                        yield s_mma(j + 1)
+                        yield ("commit", "SDF", j + 1)
+
+                    def dp_next():
+                        yield ("wait", f"VF{(j + 2) % VS}", (j + 2) // VS)
+                        yield dp_mma(j + 2)  # over dS(j), which dQ(j) reads first
+                        yield ("commit", f"VE{(j + 2) % VS}", (j + 2) // VS)
+                    if dp_before_dq and j + 2 < nj:
+                        yield from dp_next()
+                    yield ("wait", "PF", j)
+                    yield ("arrive", "PFS", 1, j)
+                    yield dq_mma(j)
+                    yield ("commit", f"KE{j % KS}", j // KS)
+                    if not dp_before_dq and j + 2 < nj:
+                        yield from dp_next()
+                    continue
                 if j + 1 < nj:
                     yield ("wait", "LD", j)
                     yield s_mma(j + 1)
@@ -1185,9 +1217,14 @@ def single_s_model(nkv, NSLOT=4, skip_empty=False):
 
 # ------------------------------------------------------------------ the kernels
 @pytest.mark.parametrize("nj", [1, 2, 3, 4, 7, 20])
-@pytest.mark.parametrize("two_issuers", [False, True])
-def test_dq_protocol(nj, two_issuers):
-    each_seed(dq_model(nj, two_issuers=two_issuers))
+@pytest.mark.parametrize("two_issuers,early_dp", [(False, False), (True, False), (False, True)])
+def test_dq_protocol(nj, two_issuers, early_dp):
+    each_seed(dq_model(nj, two_issuers=two_issuers, early_dp=early_dp))
+
+
+def test_dq_early_dp_before_dq_is_caught():
+    # dP(j+2) issued before dQ(j): it overwrites dS(j) before dQ(j) reads it
+    assert fails_on_some_seed(dq_model(6, early_dp=True, dp_before_dq=True))
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
