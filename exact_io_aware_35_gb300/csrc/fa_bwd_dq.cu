@@ -49,8 +49,12 @@ constexpr int kDqThreads = 640;
 template <int D>
 struct DqCfg : Tiles<D> {
     using T = Tiles<D>;
-    static constexpr int KS = 3;  // K ring slots: K_j (dQ), K_{j+1} (S), one ahead
-    static constexpr int VS = 2;  // V ring slots: V_{j+1} (dP), one ahead
+    // K ring: K_j (dQ), K_{j+1} (S), loads ahead; V ring: V_{j+2} (dP), loads
+    // ahead.  A tile lands about a block's time after its load starts, and at
+    // d = 128 (32 KB tiles) shared memory holds only one slot ahead of each;
+    // at d = 64 (16 KB) each ring gets one more.
+    static constexpr int KS = (D == 64) ? 4 : 3;
+    static constexpr int VS = (D == 64) ? 3 : 2;
     static constexpr int OFF_K = 2 * T::TILE;  // after Q, dO
     static constexpr int OFF_V = OFF_K + KS * T::TILE;
     static constexpr int OFF_BAR = OFF_V + VS * T::TILE;

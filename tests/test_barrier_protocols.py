@@ -1222,6 +1222,12 @@ def test_dq_protocol(nj, two_issuers, early_dp):
     each_seed(dq_model(nj, two_issuers=two_issuers, early_dp=early_dp))
 
 
+@pytest.mark.parametrize("nj", [1, 2, 3, 5, 16])
+def test_dq_protocol_deep_rings(nj):
+    # d = 64: four K and three V ring slots
+    each_seed(dq_model(nj, KS=4, VS=3, early_dp=True))
+
+
 def test_dq_early_dp_before_dq_is_caught():
     # dP(j+2) issued before dQ(j): it overwrites dS(j) before dQ(j) reads it
     assert fails_on_some_seed(dq_model(6, early_dp=True, dp_before_dq=True))
