@@ -49,7 +49,9 @@ constexpr int kDkCompute = 512;  // compute threads
 template <int D>
 struct DkdvCfg : Tiles<D> {
     using T = Tiles<D>;
-    static constexpr int NST = 2;  // {Q_i, dO_i} ring stages
+    // {Q_i, dO_i} ring stages: a stage's next load starts when dK of its last
+    // step is done; at d = 64 (32 KB stages) shared memory has room for a third
+    static constexpr int NST = (D == 64) ? 3 : 2;
     // smem: K, V, then NST stages of {Q_i, dO_i}, then per-stage lse2 / D vectors
     static constexpr int OFF_STAGE = 2 * T::TILE;
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
@@ -146,7 +148,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             }
         }
         const uint64_t pol_q = l2_policy_evict_last();
-        int last_it[C::NST] = {-1, -1};
+        int last_it[C::NST];
+        for (int s = 0; s < C::NST; ++s) last_it[s] = -1;
         // fp16 path: D is staged times 2^ds, the scale of dP^T (V dO^T of the
         // copies carries exactly 2^ds: the copy of dO is scaled by ds - v)
         const float dsc = F16 ? pow2f(ld_once(&a.f16s->ds)) : 1.f;

@@ -1363,6 +1363,12 @@ def test_decode_rescale_without_pv_wait_is_caught():
     assert fails_on_some_seed(decode_model(12, skip_pvd_wait=True))
 
 
+@pytest.mark.parametrize("n_it", [1, 2, 4, 16])
+def test_dkdv_protocol_three_stages(n_it):
+    # d = 64: three {Q, dO} stages
+    each_seed(dkdv_model(n_it, NST=3))
+
+
 def test_dkdv_dk_before_ds_is_caught():
     # dK += dS^T Q issued before the warpgroups have written dS^T
     assert fails_on_some_seed(dkdv_model(4, dk_before_dsf=True))
