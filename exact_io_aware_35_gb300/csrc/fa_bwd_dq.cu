@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mma_commit_w(leader, BAR_VE(jj % C::VS));
             };
             // dQ += dS(jj) K_jj: dS (packed pairs) of keys 16ks.. at columns
-            // 32(ks/2) + (ks%2)*8 of dP buffer jj & 1; K rows 16ks.. read MN-major
+            // 32(ks/2) + (ks%2)*8 of dP buffer jj & 1; K rows 16ks.. read MN-major.
+            // The caller commits K_jj's slot free (after the next dP, so that
+            // the two batches go to the tensor core back to back).
             auto issue_dq = [&](int jj) {
                 const uint32_t k_lo = sdesc_lo(sK + (jj % C::KS) * C::TILE, C::CHUNK), aS = tDP(jj);
 #pragma unroll
@@ -274,7 +276,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     mma_bf16_ts_w(leader, tDQ, aS + (ks >> 1) * 32 + (ks & 1) * 8,
                                   sdesc_at(k_lo, HI, ks * 2048), IDESC_DQ,
                                   (jj == 0 && ks == 0) ? 0u : 1u);
-                mma_commit_w(leader, BAR_KE(jj % C::KS));
             };
             bool ok = mbar_wait_warp(BAR_QDO, 0, a.watch, 22) && k_ready(0);
             if (ok) issue_t(tS, q_lo, sK, IDESC_S);
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     if (!(ok = v_ready(j + 2))) break;
                     issue_dp(j + 2);
                 }
+                mma_commit_w(leader, BAR_KE(j % C::KS));  // dQ(j) was K_j's last reader
             }
             // every issued MMA has finished before TMEM is released
             mma_commit_w(leader, BAR_ACC);

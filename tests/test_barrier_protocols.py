@@ -217,7 +217,8 @@ def ring_bars(nslot):
 
 # ---------------------------------------------------------------- dQ kernel
 def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuers=False,
-             single_dqd=False, skip_dqd=False, early_dp=False, dp_before_dq=False):
+             single_dqd=False, skip_dqd=False, early_dp=False, dp_before_dq=False,
+             late_ke=False):
     """Sixteen compute warps (w, q): key quarter w (32 columns of S, dP, its
     dS written into the first 16) and TMEM lanes 32q.. (query rows); each
     arrives on its own.  The MMA thread
@@ -235,8 +236,9 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
     just read, instead of next to S(j+2) behind LD(j+1); only S(j+1) waits for
     LD(j), whose gate then folds in K_{j+1} alone, and the MMA thread waits
     for V_{j+2} itself.  The producer loads in the products' first-use order
-    (K_0, V_0, V_1, K_1, V_2, K_2, ...).  dp_before_dq (dP(j+2) issued before
-    dQ(j)) is a planted mistake."""
+    (K_0, V_0, V_1, K_1, V_2, K_2, ...).  late_ke: the commit that frees K_j's
+    slot follows dP(j+2), so dQ(j) and dP(j+2) are issued back to back.
+    dp_before_dq (dP(j+2) issued before dQ(j)) is a planted mistake."""
     warps = [(w, q) for w in range(4) for q in range(4)]
 
     def model(rnd):
@@ -320,9 +322,12 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
                     yield ("wait", "PF", j)
                     yield ("arrive", "PFS", 1, j)
                     yield dq_mma(j)
-                    yield ("commit", f"KE{j % KS}", j // KS)
+                    if not late_ke:
+                        yield ("commit", f"KE{j % KS}", j // KS)
                     if not dp_before_dq and j + 2 < nj:
                         yield from dp_next()
+                    if late_ke:
+                        yield ("commit", f"KE{j % KS}", j // KS)
                     continue
                 if j + 1 < nj:
                     yield ("wait", "LD", j)
@@ -1220,6 +1225,12 @@ def single_s_model(nkv, NSLOT=4, skip_empty=False):
 @pytest.mark.parametrize("two_issuers,early_dp", [(False, False), (True, False), (False, True)])
 def test_dq_protocol(nj, two_issuers, early_dp):
     each_seed(dq_model(nj, two_issuers=two_issuers, early_dp=early_dp))
+
+
+@pytest.mark.parametrize("nj", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("ks,vs", [(3, 2), (4, 3)])
+def test_dq_protocol_late_ke(nj, ks, vs):
+    each_seed(dq_model(nj, KS=ks, VS=vs, early_dp=True, late_ke=True))
 
 
 @pytest.mark.parametrize("nj", [1, 2, 3, 5, 16])
