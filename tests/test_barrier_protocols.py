@@ -401,7 +401,8 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
 
 # -------------------------------------------------------------- dK/dV kernel
 def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, skip_dvd=False,
-               p_before_str=False, three_regions=False, early_dpt=False, skip_dsf_wait=False):
+               p_before_str=False, three_regions=False, early_dpt=False, skip_dsf_wait=False,
+               late_ste=False):
     """Sixteen compute warps (g, q): query columns 32g.. of the transposed
     tiles (warpgroup g) and key rows 32q.. (TMEM lanes).  The kernel's
     protocol (ds_smem False): a warp forms P^T(it) as soon as S^T(it) is in
@@ -419,7 +420,11 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     warp could otherwise run a step ahead into the previous phase).
     early_dpt (that early issue with only two regions, over P^T(it), dS^T(it)),
     skip_dsf_wait (three regions without the DSF(it-1) wait) and p_before_str
-    (P^T formed without waiting for S^T) are planted mistakes.  A variant that was tried and
+    (P^T formed without waiting for S^T) are planted mistakes.  late_ste (a
+    variant tried and measured slower: gqa8k dK/dV 2.84 -> 3.06 ms, the
+    two-stage ring starved): the commit that frees the step's {Q, dO} stage
+    follows dP^T(it+1) and its SDF commit, so dK(it) and dP^T(it+1) go to the
+    tensor core back to back.  A variant that was tried and
     measured slower (ds_smem True, with the earlier single-step compute):
     dS^T goes to shared memory instead -- over the stage's dO tile (ds_in_do,
     d = 128) or into a buffer of its own (d = 64) -- once the MMA thread's
@@ -518,10 +523,13 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
                 if not dk_before_dsf:
                     yield ("wait", "DSF", it)
                 yield dk_mma(it)
-                yield ("commit", f"STE{s}", it // NST)
+                if not late_ste:
+                    yield ("commit", f"STE{s}", it // NST)
                 if more and not early:
                     yield dpt_mma(it + 1)  # over P^T(it), dS^T(it)
                     yield ("commit", "SDF", it + 1)
+                if late_ste:
+                    yield ("commit", f"STE{s}", it // NST)
             yield ("commit", "ACC", 0)
             yield ("wait", "ACC", 0)
 
@@ -1372,6 +1380,12 @@ def test_forward_early_score_product_is_caught():
 def test_decode_rescale_without_pv_wait_is_caught():
     # O rescaled while P(j-1) V_{j-1} may still be accumulating into it
     assert fails_on_some_seed(decode_model(12, skip_pvd_wait=True))
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("nst", [2, 3])
+def test_dkdv_protocol_late_ste(n_it, nst):
+    each_seed(dkdv_model(n_it, NST=nst, late_ste=True))
 
 
 @pytest.mark.parametrize("n_it", [1, 2, 4, 16])
