@@ -39,7 +39,7 @@ constexpr int kF8WarpLoad = 9;
 constexpr int kF8WarpGate = 10;
 // barriers: Q, K/V full[slots], empty[slots], s_full[2], p_full[2], o_final[2], done,
 // q_empty
-constexpr int kF8Bars = 1 + 2 * kF8Slots + 2 + 2 + 2 + 1 + 1;
+constexpr int kF8Bars = 1 + 2 * kF8Slots + 2 + 2 + 2 + 1 + 1 + 1;
 constexpr int kF8Stage = 8 * 2048;  // the epilogue's per-warp transpose buffers
 constexpr float kE4m3Max = 448.f;
 
@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     auto BAR_OF = [&](int t) { return bar0 + 8u * (5 + 2 * kF8Slots + t); };  // O_t final
     const uint32_t BAR_DONE = bar0 + 8u * (7 + 2 * kF8Slots);
     const uint32_t BAR_QE = bar0 + 8u * (8 + 2 * kF8Slots);  // the item's Q tiles no longer read
+    const uint32_t BAR_G1 = bar0 + 8u * (9 + 2 * kF8Slots);  // the gate has seen the item's K_0 land
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         mbar_init(BAR_DONE, 1);
         mbar_init(BAR_QE, 1);
+        mbar_init(BAR_G1, 1);
         fence_barrier_init();
     }
     if (warp == kF8WarpMma) {
@@ -323,13 +325,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     } else if (warp == kF8WarpGate) {
         // ================= gate: V_j and K_{j+1} landed -> p_full(t) =================
         // one arrival per tile that multiplies block j, made only after that
-        // barrier's previous phase is over, so it can never count in the wrong one
+        // barrier's previous phase is over, so it can never count in the wrong
+        // one.  It alone waits on the ring's kv_full barriers, every entry in
+        // order (each item's K_0 too, passed on to the MMA thread on g1), so
+        // that its parity waits always find their slot at the awaited phase
+        // or the one after.
         setmaxnreg_dec<80>();
         if (lane == 0) {
             bool ok = true;
             int e = 0, cnt[2] = {0, 0};
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
                 const Item I = item(w);
+                ok = mbar_wait(BAR_KVF(e % kF8Slots), (e / kF8Slots) & 1, a.watch, 58);  // K_0
+                if (ok) mbar_arrive(BAR_G1);
                 for (int j = 0; j < I.nkv && ok; ++j) {
                     const int vidx = e + 2 * j + 1, kidx = e + 2 * j + 2;
                     ok = mbar_wait(BAR_KVF(vidx % kF8Slots), (vidx / kF8Slots) & 1, a.watch, 58);
@@ -377,7 +385,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
                 const Item I = item(w);
                 if (!(ok = mbar_wait(BAR_Q, it & 1, a.watch, 53))) break;
-                if (!(ok = mbar_wait(BAR_KVF(e % kF8Slots), (e / kF8Slots) & 1, a.watch, 53))) break;
+                // K_0 has landed: the gate has seen it (g1)
+                if (!(ok = mbar_wait(BAR_G1, it & 1, a.watch, 53))) break;
                 tc_fence_after();
                 issue_s(0, e % kF8Slots);
                 mma_commit(BAR_SF(0));

@@ -63,14 +63,16 @@ struct FwdCfg {
     // warp; block-sparse CTAs run one item each and use their tile's Q buffer
     static constexpr int SMEM_STAGE = SPARSE ? 0 : 8 * 2048;
     // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
-    // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done, and for
-    // block-sparse epi[2] (a tile's O staged for its TMA store)
-    static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1 + (SPARSE ? 2 : 0);
+    // p_full[2], o_final[2], s_empty[2], pv_done[2], mma_done, for
+    // block-sparse epi[2] (a tile's O staged for its TMA store), and g1 (the
+    // gate has seen the item's first K entries land)
+    static constexpr int NBAR = 2 + 2 * NSLOT + 10 + 1 + (SPARSE ? 2 : 0) + 1;
     // block-sparse: the item's two mask rows as bitmasks (one bit per key
     // block), read from global memory once when the CTA starts
     static constexpr int SMEM_MASK = SPARSE ? (8 + 2 * kSparseMaskWords) * 4 : 0;
     static constexpr int SMEM_BYTES =
         1024 /*align slack*/ + SMEM_Q + SMEM_KV + SMEM_STAGE + NBAR * 8 + 16 + SMEM_MASK;
+    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB a block may use");
     // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D)
     // and, at D = 64, P0 [384,448) P1 [448,512): P (fp16 or bf16 pairs) gets
     // columns of its own instead of overwriting S_t (SPLITP).
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(384, 1)
     auto BAR_PVD = [&](int t) { return bar0 + 8u * (10 + 2 * C::NSLOT + t); };
     const uint32_t BAR_DONE = bar0 + 8u * (12 + 2 * C::NSLOT);
     auto BAR_EPI = [&](int t) { return bar0 + 8u * (13 + 2 * C::NSLOT + t); };
+    const uint32_t BAR_G1 = bar0 + 8u * (C::NBAR - 1);
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -288,6 +291,7 @@ __global__ void __launch_bounds__(384, 1)
             if (SPARSE) mbar_init(BAR_EPI(t), 4);  // likewise
         }
         mbar_init(BAR_DONE, kIssuers);
+        mbar_init(BAR_G1, 1);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -480,7 +484,12 @@ __global__ void __launch_bounds__(384, 1)
         // For block k of tile t it waits for V(k) and K(k+1), then adds one
         // arrival to p_full(t), but only once that barrier's previous phase
         // has completed, so the arrival can never be counted in the wrong
-        // phase.
+        // phase.  It is the only thread that waits on the ring's kv_full
+        // barriers, every entry in ring order: an item's first K entries too,
+        // which it passes on to the MMA thread on g1.  A slot's parity wait
+        // answers right only at the awaited phase or the one after it; seeing
+        // every phase of a slot, and letting no entry be used before it has
+        // seen it land, keeps every wait there.
         setmaxnreg_dec<88>();
         if (lane == 0) {
             bool ok = true;
@@ -498,7 +507,9 @@ __global__ void __launch_bounds__(384, 1)
                 const Item<SPARSE> I(w, a, mbits);
                 if constexpr (SPARSE) {
                     const int c0 = I.blk.count[0], c1 = I.blk.count[1];
-                    e += (c0 > 0) + (c1 > 0);  // the K_t(0)
+                    if (c0 > 0) landed(e++);  // the K_t(0)
+                    if (c1 > 0) landed(e++);
+                    if (ok && (c0 > 0 || c1 > 0)) mbar_arrive(BAR_G1);
                     for (int k = 0; k < max(c0, c1) && ok; ++k)
                         for (int t = 0; t < 2 && ok; ++t) {
                             const int c = t == 0 ? c0 : c1;
@@ -509,6 +520,8 @@ __global__ void __launch_bounds__(384, 1)
                         }
                 } else {
                     const int n1 = I.blk.n[1];
+                    landed(e);  // K(0)
+                    if (ok) mbar_arrive(BAR_G1);
                     for (int u = 0; u < n1 && ok; ++u) {
                         landed(e + 2 * u + 1);
                         if (u + 1 < n1) landed(e + 2 * u + 2);
@@ -547,7 +560,7 @@ __global__ void __launch_bounds__(384, 1)
         setmaxnreg_dec<88>();
         const uint32_t leader = elect_one();
         bool ok = true;
-        int e = 0, it = 0;
+        int e = 0, it = 0, ng1 = 0;
         int cnt[2] = {0, 0};  // p_full phases waited, per tile
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
             const Item<SPARSE> I(w, a, mbits);
@@ -557,11 +570,12 @@ __global__ void __launch_bounds__(384, 1)
                 // K_t(k+1) landed, the gate), then S_t(k+1).  Every ring entry is
                 // released right after the product that reads it.
                 const int c0 = I.blk.count[0], c1 = I.blk.count[1];
+                // the gate has seen the item's first K entries land (g1)
+                if ((c0 > 0 || c1 > 0) && !(ok = mbar_wait_warp(BAR_G1, ng1++ & 1, a.watch, 4)))
+                    break;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if ((t == 0 ? c0 : c1) == 0) continue;
                     const int ek = e++;
-                    if (!(ok = mbar_wait_warp(BAR_KVF(ek % C::NSLOT), (ek / C::NSLOT) & 1, a.watch, 4)))
-                        break;
                     tc_fence_after();
                     issue_qk(leader, t, ek % C::NSLOT);
                     mma_commit_w(leader, BAR_SF(t));
@@ -593,8 +607,8 @@ __global__ void __launch_bounds__(384, 1)
                 // follows PV_t(u), which read P_t over S_t.  The item's first
                 // S_t follows the previous item's last PV_t the same way.
                 const int n0 = I.blk.n[0], n1 = I.blk.n[1];
-                if (!(ok = mbar_wait_warp(BAR_KVF(e % C::NSLOT), (e / C::NSLOT) & 1, a.watch, 4)))
-                    break;
+                // K(0) has landed: the gate has seen it (g1)
+                if (!(ok = mbar_wait_warp(BAR_G1, ng1++ & 1, a.watch, 4))) break;
                 tc_fence_after();
                 for (int t = 0; t < 2; ++t) {
                     issue_qk(leader, t, e % C::NSLOT);

@@ -55,7 +55,10 @@ class Bar:
             self.pending = self.count
 
     def done(self, phase):
-        if self.phase > phase + 1:
+        # the hardware's parity wait answers correctly only at phase p (still
+        # open) or p + 1 (completed): two phases on, or one phase short (the
+        # completed phase p - 2 has p's parity), it answers wrongly
+        if self.phase > phase + 1 or self.phase < phase:
             raise ProtocolError(f"{self.name}: wait for phase {phase} at phase {self.phase}")
         return self.phase > phase
 
@@ -267,11 +270,16 @@ def dq_model(nj, KS=3, VS=2, handshake=True, first_gate_design=False, two_issuer
 
         def gate():
             for j in range(nj):
+                if not early_dp and j > 0:
+                    # V_{j+1}'s slot last held V_{j-1}: LD(j-1) says it landed, so
+                    # the parity wait below cannot be a phase short (waiting V
+                    # first, as an earlier form did, could be)
+                    yield ("wait", "LD", j - 1)
                 if j + 1 < nj:
                     yield ("wait", f"KF{(j + 1) % KS}", (j + 1) // KS)
                     if not early_dp:
                         yield ("wait", f"VF{(j + 1) % VS}", (j + 1) // VS)
-                if j > 0:
+                if early_dp and j > 0:
                     yield ("wait", "LD", j - 1)
                 yield ("arrive", "LD", 1, j)
                 if first_gate_design:
@@ -622,6 +630,161 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     return model
 
 
+def dq_persistent_model(items, KS=4, VS=3, copy_q=True, mistake=None):
+    """The persistent dQ kernel (d = 64): one CTA walks `items`, each the key
+    block count of one (batch, head, 128-query block).  Blocks carry global
+    indices g across items, so the K/V rings, the dP buffers (g % 2) and the
+    per-block barriers (SDF, LD, PF, PFS) run on from one item to the next.
+    Within an item the order is the one-item kernel's (dP two blocks ahead).
+    At an item's start the MMA thread waits for its Q, dO (QDO) and for LD of
+    the previous item's last block before the new S(g0): the data is implied
+    by PF, which it waited for, but without that wait its parity wait for
+    LD(g0) could find the barrier a phase short.  The item's first dQ, which
+    starts the accumulator afresh, follows PF(g0), and every warp arrives on
+    that only after it has read the previous item's dQ out of TMEM.  Q and
+    dO are free for the next item once its last S and dP are done and the
+    copy warp has read dO (QE: a commit after the item's last S, one arrival
+    from the copy warp).  The warps stage dQ in a buffer of its own, once the
+    previous item's store has read it (EPE), and a store thread takes it from
+    there (EPF).  mistake: "no_qe", "no_ld_cross", "no_epe" drop the matching
+    wait."""
+    warps = [(w, q) for w in range(4) for q in range(4)]
+    G = sum(items)
+    starts = [sum(items[:i]) for i in range(len(items))]
+
+    def model(rnd):
+        bars = {"QDO": 1, "QE": 1 + (1 if copy_q else 0), "SDF": 1, "LD": 513, "PF": 512,
+                "PFS": 1, "ACC": 1, "EPF": 512, "EPE": 1, "DONE": 1}
+        for nm, ns in (("K", KS), ("V", VS)):
+            for s_ in range(ns):
+                bars[f"{nm}F{s_}"] = bars[f"{nm}E{s_}"] = 1
+
+        def every(pre, tag):
+            return {f"{pre}.{w}.{q}": tag for w, q in warps}
+
+        def producer():
+            last = {}
+            for it, nj in enumerate(items):
+                if it > 0 and mistake != "no_qe":
+                    yield ("wait", "QE", it - 1)
+                yield ("load", "QDO", it, dict(every("Q", f"Q({it})"), dO=f"dO({it})"))
+                g0 = starts[it]
+                order = [("K", g0), ("V", g0)]
+                for i in range(1, nj):
+                    order += [("V", g0 + i), ("K", g0 + i)]
+                for nm, g in order:
+                    ns = KS if nm == "K" else VS
+                    sl = g % ns
+                    yield ("wait", f"{nm}E{sl}", g // ns - 1)
+                    yield ("load", f"{nm}F{sl}", g // ns, {f"{nm}{sl}": f"{nm}({g})"})
+                    last[f"{nm}F{sl}"] = g // ns
+            if items:
+                yield ("wait", "QDO", len(items) - 1)
+            for bar, ph in last.items():
+                yield ("wait", bar, ph)
+
+        def gate():
+            for g in range(G):
+                if g + 1 < G:
+                    yield ("wait", f"KF{(g + 1) % KS}", (g + 1) // KS)
+                if g > 0:
+                    yield ("wait", "LD", g - 1)
+                yield ("arrive", "LD", 1, g)
+
+        def copy():
+            for it in range(len(items)):
+                yield ("wait", "QDO", it)
+                yield ("read", {"dO": f"dO({it})"})
+                yield ("arrive", "QE", 1, it)
+
+        def s_mma(it, g):
+            return ("mma", f"S({g})", dict(every("Q", f"Q({it})"), **{f"K{g % KS}": f"K({g})"}),
+                    every("S", f"S({g})"))
+
+        def dp_mma(it, g):
+            return ("mma", f"dP({g})", {"dO": f"dO({it})", f"V{g % VS}": f"V({g})"},
+                    every(f"DP{g & 1}", f"dP({g})"))
+
+        def dq_mma(it, j, g):
+            reads = dict(every(f"DP{g & 1}", f"dS({g})"), **{f"K{g % KS}": f"K({g})"})
+            if j > 0:
+                reads["dQ"] = f"dQ({it},{j - 1})"
+            return ("mma", f"dQ({g})", reads, {"dQ": f"dQ({it},{j})"})
+
+        def mma():
+            for it, nj in enumerate(items):
+                g0 = starts[it]
+                yield ("wait", "QDO", it)
+                if it > 0 and mistake != "no_ld_cross":
+                    yield ("wait", "LD", g0 - 1)  # S of the previous item's last block is read
+                yield ("wait", f"KF{g0 % KS}", g0 // KS)
+                yield s_mma(it, g0)
+                yield ("wait", f"VF{g0 % VS}", g0 // VS)
+                yield dp_mma(it, g0)
+                yield ("commit", f"VE{g0 % VS}", g0 // VS)
+                yield ("commit", "SDF", g0)
+                if nj == 1:
+                    yield ("commit", "QE", it)
+                if nj > 1:
+                    yield ("wait", f"VF{(g0 + 1) % VS}", (g0 + 1) // VS)
+                    yield dp_mma(it, g0 + 1)
+                    yield ("commit", f"VE{(g0 + 1) % VS}", (g0 + 1) // VS)
+                for j in range(nj):
+                    g = g0 + j
+                    if j + 1 < nj:
+                        yield ("wait", "LD", g)
+                        yield ("wait", f"KF{(g + 1) % KS}", (g + 1) // KS)
+                        yield s_mma(it, g + 1)
+                        yield ("commit", "SDF", g + 1)
+                        if j + 1 == nj - 1:
+                            yield ("commit", "QE", it)  # the item's last S and dP are issued
+                    yield ("wait", "PF", g)
+                    yield ("arrive", "PFS", 1, g)
+                    yield dq_mma(it, j, g)
+                    if j + 2 < nj:
+                        yield ("wait", f"VF{(g + 2) % VS}", (g + 2) // VS)
+                        yield dp_mma(it, g + 2)
+                        yield ("commit", f"VE{(g + 2) % VS}", (g + 2) // VS)
+                    yield ("commit", f"KE{g % KS}", g // KS)
+                yield ("commit", "ACC", it)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def compute(w, q):
+            me = f"{w}.{q}"
+            for it, nj in enumerate(items):
+                for j in range(nj):
+                    g = starts[it] + j
+                    yield ("wait", "SDF", g)
+                    yield ("read", {f"S.{me}": f"S({g})", f"DP{g & 1}.{me}": f"dP({g})"})
+                    yield ("arrive", "LD", 32, g)
+                    yield ("write", {f"DP{g & 1}.{me}": f"dS({g})"})
+                    if g > 0:
+                        yield ("wait", "PFS", g - 1)
+                    yield ("arrive", "PF", 32, g)
+                yield ("wait", "ACC", it)
+                yield ("read", {"dQ": f"dQ({it},{nj - 1})"})
+                if it > 0 and mistake != "no_epe":
+                    yield ("wait", "EPE", it - 1)
+                yield ("write", {f"ST.{me}": f"out({it})"})
+                yield ("arrive", "EPF", 32, it)
+
+        def store():
+            for it in range(len(items)):
+                yield ("wait", "EPF", it)
+                yield ("read", every("ST", f"out({it})"))
+                yield ("arrive", "EPE", 1, it)
+
+        roles = {"prod": producer(), "gate": gate(), "mma": mma(), "store": store()}
+        if copy_q:
+            roles["copy"] = copy()
+        for w, q in warps:
+            roles[f"c{w}{q}"] = compute(w, q)
+        return bars, roles
+
+    return model
+
+
 def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
     """One CTA per work item with two query tiles, the epilogue staging O in
     the Q buffers behind a bar.sync (the forward kernels' earlier one-item
@@ -634,7 +797,7 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
 
     def model(rnd):
         bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
-                "DONE": 1, "QC": 1}
+                "DONE": 1, "QC": 1, "G1": 1}
         bars.update(ring_bars(NSLOT))
         n_of = (nkv0, nkv)
 
@@ -642,6 +805,13 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
             return {f"{pre}.{t}.{q}": tag for q in rows}
 
         def gate():
+            # the gate alone waits on the ring's full barriers, every entry in
+            # order (K_0 too, passed on to the MMA thread on G1): a slot's
+            # parity wait answers right only at the awaited phase or the one
+            # after, and no slot can move on before the gate has let its entry
+            # be used
+            yield ("wait", "F0", 0)
+            yield ("arrive", "G1", 1, 0)
             for j in range(nkv):
                 v, kn = 2 * j + 1, 2 * j + 2
                 yield ("wait", f"F{v % NSLOT}", v // NSLOT)
@@ -673,7 +843,7 @@ def fwd_model(nkv0, nkv, NSLOT=4, copy_q=True, early_qk=False):
 
         def mma():
             yield ("wait", "Q", 0)
-            yield ("wait", "F0", 0)
+            yield ("wait", "G1", 0)
             yield qk(0, 0)
             yield ("commit", "SF0", 0)
             yield qk(1, 0)
@@ -788,7 +958,10 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
     "no_k_wait" (a score product before its K tile has landed), "no_pvd_wait"
     (P_t written before the previous P V product has read it), "no_of_wait"
     (the epilogue reads O without o_final), "no_drain" (the producer exits
-    without waiting for its last loads), "no_q_wait_empty" (stage_q: a tile with
+    without waiting for its last loads), "mma_waits_first_k" (the issuer waits
+    the item's first K entries itself and the gate starts at V(0): the gate's
+    parity wait on a slot can then come a phase early or two late),
+    "no_q_wait_empty" (stage_q: a tile with
     no block stages O without waiting for its Q load).  (The s_empty wait before an item's
     first score product is implied by q_empty: the issuer's commit to it
     follows its last P V product, which followed the softmax's p_full; the
@@ -820,7 +993,7 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
         return ("twait", bar, phase, mode) if timeouts else ("wait", bar, phase)
 
     def model(rnd):
-        bars = {"Q": 1, "QE": nissue + (1 if copy_q else 0), "DONE": nissue}
+        bars = {"Q": 1, "QE": nissue + (1 if copy_q else 0), "DONE": nissue, "G1": 1}
         for t in (0, 1):
             bars.update({f"SF{t}": 1, f"PF{t}": 128 if split_p else 129, f"OF{t}": 1,
                          f"SE{t}": 4, f"PVD{t}": 1, f"EPI{t}": 4})
@@ -888,8 +1061,24 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
             return ("commit", f"E{s}", ph)
 
         def gate():  # d = 128: V(k), K(k+1) landed -> p_full(t)
-            pf, ok = [0, 0], True
+            pf, ok, ng1 = [0, 0], True, 0
             for i, it in enumerate(items):
+                # the item's first K entries too, so that the gate sees every
+                # ring phase in order (a slot's parity wait answers right only
+                # once the phase before it was seen done)
+                firsts = [(1, "K", 0)] if not sparse and it[1] else \
+                    [(t, "K", 0) for t in (0, 1) if sparse and it[t]]
+                if mistake == "mma_waits_first_k":
+                    firsts = []
+                for (tt, w, kk) in firsts:
+                    s, ph = slot(i, tt, w, kk)
+                    if ok:
+                        ok = (yield W(f"F{s}", ph)) is not False
+                if not ok:
+                    break
+                if firsts:  # the MMA thread's first score products wait on this
+                    yield ("arrive", "G1", 1, ng1)
+                    ng1 += 1
                 if not sparse:
                     steps = [(u, [t for t in (0, 1) if u < len(it[t])]) for u in range(len(it[1]))]
                 else:
@@ -976,18 +1165,22 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
 
         def issuer_single():
             npv, nof, nsf = [0, 0], [0, 0], [0, 0]
-            ok = True
+            ok, ng1 = True, 0
             for i, it in enumerate(items):
                 ok = (yield W("Q", i)) is not False
+                if ok and (it[0] or it[1]) and mistake != "mma_waits_first_k":
+                    # the gate has seen the item's first K entries
+                    ok = (yield W("G1", ng1)) is not False
+                    ng1 += 1
                 for t in (0, 1):
                     if not ok:
                         break
-                    if it[t]:
+                    if it[t] and mistake == "mma_waits_first_k" and (sparse or t == 0):
                         s, ph = slot(i, t, "K", 0)
-                        if sparse or t == 0:
-                            ok = (yield W(f"F{s}", ph)) is not False
-                            if not ok:
-                                break
+                        ok = (yield W(f"F{s}", ph)) is not False
+                        if not ok:
+                            break
+                    if it[t]:
                         yield qk(i, t, 0)
                         yield ("commit", f"SF{t}", nsf[t])
                         nsf[t] += 1
@@ -1247,6 +1440,22 @@ def test_dq_protocol_deep_rings(nj):
     each_seed(dq_model(nj, KS=4, VS=3, early_dp=True))
 
 
+DQ_PERSISTENT_ITEMS = [[1], [2], [3], [16, 16], [1, 1, 1], [2, 3, 1, 4], [5, 1, 2], [3] * 6]
+
+
+@pytest.mark.parametrize("items", range(len(DQ_PERSISTENT_ITEMS)))
+@pytest.mark.parametrize("copy_q", [False, True])
+def test_dq_persistent_protocol(items, copy_q):
+    each_seed(dq_persistent_model(DQ_PERSISTENT_ITEMS[items], copy_q=copy_q), seeds=range(40))
+
+
+@pytest.mark.parametrize("mistake,items", [("no_qe", [3, 2, 4]), ("no_ld_cross", [3, 2, 4]),
+                                           ("no_epe", [1] * 6)])
+def test_dq_persistent_planted_mistakes_are_caught(mistake, items):
+    # (a store thread a whole item late needs short items to show)
+    assert fails_on_some_seed(dq_persistent_model(items, mistake=mistake), seeds=range(200))
+
+
 def test_dq_early_dp_before_dq_is_caught():
     # dP(j+2) issued before dQ(j): it overwrites dS(j) before dQ(j) reads it
     assert fails_on_some_seed(dq_model(6, early_dp=True, dp_before_dq=True))
@@ -1315,6 +1524,13 @@ def test_forward_sparse_empty_tile_must_wait_for_its_q_load(split_p, nslot):
     assert fails_on_some_seed(fwd_persistent_model([([], [0, 3])], nslot, split_p=split_p,
                                                    sparse=True, stage_q=True,
                                                    mistake="no_q_wait_empty"))
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_forward_gate_that_skips_first_k_is_caught(sparse):
+    items = PERSISTENT_SPARSE[0] if sparse else PERSISTENT_DENSE[0]
+    assert fails_on_some_seed(fwd_persistent_model(items, 5 if sparse else 4, sparse=sparse,
+                                                   mistake="mma_waits_first_k"))
 
 
 def test_forward_persistent_random_masks():
@@ -1533,7 +1749,7 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
     rows = range(4)
 
     def model(rnd):
-        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1,
+        bars = {"Q": 1, "SF0": 1, "SF1": 1, "PF0": 129, "PF1": 129, "OF0": 1, "OF1": 1, "G1": 1,
                 "DONE": 1, "QC": 1}
         bars.update(ring_bars(NSLOT))
         n_of = (nkv0, nkv)
@@ -1566,8 +1782,12 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
             yield from teardown()
 
         def gate():
-            ok = True
+            ok = yield ("twait", "F0", 0, "abort")  # K_0 too (every entry in order)
+            if ok:
+                yield ("arrive", "G1", 1, 0)
             for j in range(nkv):
+                if not ok:
+                    break
                 v, kn = 2 * j + 1, 2 * j + 2
                 ok = yield ("twait", f"F{v % NSLOT}", v // NSLOT, "abort")
                 if ok and j + 1 < nkv:
@@ -1607,7 +1827,7 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
         def mma():
             ok = yield ("twait", "Q", 0, "abort")
             if ok:
-                ok = yield ("twait", "F0", 0, "abort")
+                ok = yield ("twait", "G1", 0, "abort")
                 if ok:
                     yield qk(0, 0)
                     yield ("commit", "SF0", 0)
