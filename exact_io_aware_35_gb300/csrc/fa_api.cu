@@ -378,6 +378,7 @@ fa_status bwd_run(int stages, const void* q, const void* k, const void* v, const
     a.causal = causal ? 1 : 0;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_ctas = di->num_sms;
     a.watch = make_watch(di->status);
     if ((stages & 7) == 0) return FA_OK;
     cudaError_t e = launch_bwd(maps, a, stages & 7, cs);

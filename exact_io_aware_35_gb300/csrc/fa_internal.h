@@ -120,6 +120,7 @@ struct BwdArgs {
     int causal;
     float scale;         // softmax scale
     float scale_log2;    // scale * log2(e)
+    int num_ctas;        // persistent CTAs to launch at most (the device's SM count)
     Watch watch;         // status words, time limit and id of the launch
 };
 

@@ -645,8 +645,8 @@ def dq_persistent_model(items, KS=4, VS=3, copy_q=True, mistake=None):
     dO are free for the next item once its last S and dP are done and the
     copy warp has read dO (QE: a commit after the item's last S, one arrival
     from the copy warp).  The warps stage dQ in a buffer of its own, once the
-    previous item's store has read it (EPE), and a store thread takes it from
-    there (EPF).  mistake: "no_qe", "no_ld_cross", "no_epe" drop the matching
+    previous item's store has read it (EPE), and the copy warp, after the
+    item's dO copy, stores it from there (EPF).  mistake: "no_qe", "no_ld_cross", "no_epe" drop the matching
     wait."""
     warps = [(w, q) for w in range(4) for q in range(4)]
     G = sum(items)
@@ -691,11 +691,15 @@ def dq_persistent_model(items, KS=4, VS=3, copy_q=True, mistake=None):
                     yield ("wait", "LD", g - 1)
                 yield ("arrive", "LD", 1, g)
 
-        def copy():
+        def copy_and_store():  # one warp: the item's dO copy, then its dQ store
             for it in range(len(items)):
-                yield ("wait", "QDO", it)
-                yield ("read", {"dO": f"dO({it})"})
-                yield ("arrive", "QE", 1, it)
+                if copy_q:
+                    yield ("wait", "QDO", it)
+                    yield ("read", {"dO": f"dO({it})"})
+                    yield ("arrive", "QE", 1, it)
+                yield ("wait", "EPF", it)
+                yield ("read", every("ST", f"out({it})"))
+                yield ("arrive", "EPE", 1, it)
 
         def s_mma(it, g):
             return ("mma", f"S({g})", dict(every("Q", f"Q({it})"), **{f"K{g % KS}": f"K({g})"}),
@@ -769,15 +773,7 @@ def dq_persistent_model(items, KS=4, VS=3, copy_q=True, mistake=None):
                 yield ("write", {f"ST.{me}": f"out({it})"})
                 yield ("arrive", "EPF", 32, it)
 
-        def store():
-            for it in range(len(items)):
-                yield ("wait", "EPF", it)
-                yield ("read", every("ST", f"out({it})"))
-                yield ("arrive", "EPE", 1, it)
-
-        roles = {"prod": producer(), "gate": gate(), "mma": mma(), "store": store()}
-        if copy_q:
-            roles["copy"] = copy()
+        roles = {"prod": producer(), "gate": gate(), "mma": mma(), "copy": copy_and_store()}
         for w, q in warps:
             roles[f"c{w}{q}"] = compute(w, q)
         return bars, roles
