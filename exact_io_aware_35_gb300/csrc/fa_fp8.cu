@@ -49,70 +49,77 @@ __device__ __forceinline__ float rot_sign(int c) {
     return ((static_cast<uint32_t>(c) * 2654435761u) >> 31) ? -1.f : 1.f;
 }
 
-// x[i] = element 4 * lane + i of a 128-element row held by one warp.  In
-// place: y[k] = sum_c (-1)^popcount(k & c) x[c] (the Walsh-Hadamard transform
-// in natural order), butterflies over strides 1, 2 inside the lane and 4..64
-// across lanes.
-__device__ __forceinline__ void hadamard128(float (&x)[4], int lane) {
-    float a = x[0] + x[1], b = x[0] - x[1];
-    x[0] = a;
-    x[1] = b;
-    a = x[2] + x[3];
-    b = x[2] - x[3];
-    x[2] = a;
-    x[3] = b;
-    a = x[0] + x[2];
-    b = x[0] - x[2];
-    x[0] = a;
-    x[2] = b;
-    a = x[1] + x[3];
-    b = x[1] - x[3];
-    x[1] = a;
-    x[3] = b;
+// x[i] = element 32 * q + i of a 128-element row spread over the four lanes
+// of a lane quad (q = lane & 3).  In place: y[k] = sum_c (-1)^popcount(k & c)
+// x[c] (the Walsh-Hadamard transform in natural order): butterflies over
+// element strides 1..16 inside the lane, 32 and 64 across the quad.  (A
+// whole warp on one row, four elements a lane, needed five shuffle stages,
+// and the shuffles set the pace of the quantisation.)
+__device__ __forceinline__ void hadamard128_quad(float (&x)[32], int q) {
 #pragma unroll
     for (int s = 1; s < 32; s <<= 1)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 32; ++i)
+            if ((i & s) == 0) {
+                const float a = x[i], b = x[i + s];
+                x[i] = a + b;
+                x[i + s] = a - b;
+            }
+#pragma unroll
+    for (int s = 1; s < 4; s <<= 1)  // lane strides 1, 2: element strides 32, 64
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
             const float y = __shfl_xor_sync(0xffffffffu, x[i], s);
-            x[i] = (lane & s) ? (y - x[i]) : (x[i] + y);
+            x[i] = (q & s) ? (y - x[i]) : (x[i] + y);
         }
 }
 
-// One 128-row block of one head of q or k, in one pass: 8 warps of 16 rows
-// each hold their (rotated) rows in registers -- all 16 loads in flight at
-// once -- while the block's max |x| is reduced, then write the bytes.
+// One 128-row block of one head of q or k, in one pass: each warp holds 16
+// rows in registers, 8 at a time across its lane quads (lane 4r + q holds
+// elements 32q..32q+31 of row r), all of a lane's 16-byte loads in flight at
+// once, while the block's max |x| is reduced; then it writes the bytes.
 __global__ void __launch_bounds__(256) fp8_rows_kernel(const uint16_t* __restrict__ x,
                                                        uint8_t* __restrict__ x8,
                                                        float* __restrict__ sx, int N, int H,
                                                        int nb, int rotate) {
-    constexpr int RPW = 16;  // rows per warp
+    constexpr int PASSES = 2;  // 8 rows a warp per pass
     __shared__ float red[8];
     const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = blk * 128 + warp * RPW;
-    float v[RPW][4];
+    const int q = lane & 3, rq = lane >> 2;
+    float v[PASSES][32];
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const int n = r0 + rr;
-        uint2 u = make_uint2(0u, 0u);
-        if (n < N)
-            u = *reinterpret_cast<const uint2*>(x + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
-                                                4 * lane);
-        v[rr][0] = __uint_as_float(u.x << 16);
-        v[rr][1] = __uint_as_float(u.x & 0xffff0000u);
-        v[rr][2] = __uint_as_float(u.y << 16);
-        v[rr][3] = __uint_as_float(u.y & 0xffff0000u);
+    for (int p = 0; p < PASSES; ++p) {
+        const int n = blk * 128 + warp * 16 + p * 8 + rq;
+        uint4 u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                x + ((static_cast<size_t>(b) * N + n) * H + h) * 128 + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[i] = src[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w4[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[p][8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
+                v[p][8 * i + 2 * j + 1] = __uint_as_float(w4[j] & 0xffff0000u);
+            }
+        }
     }
     float m = 0.f;
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
+    for (int p = 0; p < PASSES; ++p) {
         if (rotate) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[rr][i] *= rot_sign(4 * lane + i);
-            hadamard128(v[rr], lane);
+            for (int i = 0; i < 32; ++i) v[p][i] *= rot_sign(32 * q + i);
+            hadamard128_quad(v[p], q);
         }
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[rr][0]), fabsf(v[rr][1])),
-                           fmaxf(fabsf(v[rr][2]), fabsf(v[rr][3]))));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[p][i]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -125,12 +132,19 @@ __global__ void __launch_bounds__(256) fp8_rows_kernel(const uint16_t* __restric
     if (threadIdx.x == 0)
         sx[(static_cast<size_t>(b) * H + h) * nb + blk] = m > 0.f ? m / kE4m3Max : 1.f;
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const int n = r0 + rr;
-        if (n < N)
-            *reinterpret_cast<uint32_t*>(x8 + ((static_cast<size_t>(b) * N + n) * H + h) * 128 +
-                                         4 * lane) =
-                pack_e4m3x4(v[rr][0] * inv, v[rr][1] * inv, v[rr][2] * inv, v[rr][3] * inv);
+    for (int p = 0; p < PASSES; ++p) {
+        const int n = blk * 128 + warp * 16 + p * 8 + rq;
+        if (n < N) {
+            uint32_t w8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w8[i] = pack_e4m3x4(v[p][4 * i] * inv, v[p][4 * i + 1] * inv, v[p][4 * i + 2] * inv,
+                                    v[p][4 * i + 3] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(
+                x8 + ((static_cast<size_t>(b) * N + n) * H + h) * 128 + 32 * q);
+            dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        }
     }
 }
 
@@ -141,12 +155,19 @@ __global__ void __launch_bounds__(128) fp8_vmax_kernel(const uint16_t* __restric
                                                        int Hkv) {
     const int blk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     uint32_t m = 0;
-    for (int i = threadIdx.x; i < 128 * 16; i += 128) {  // 16-byte pieces of the block
+    // the block's 16-byte pieces, all of a thread's sixteen loads in flight at once
+    uint4 u[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int i = threadIdx.x + 128 * k;
         const int n = blk * 128 + i / 16;
-        if (n >= N) break;
-        const uint4 u = *reinterpret_cast<const uint4*>(
-            v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + (i % 16) * 8);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        u[k] = (n < N) ? *reinterpret_cast<const uint4*>(
+                             v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + (i % 16) * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             m = max(m, (w[j] & 0x7fffu) << 16);
@@ -169,13 +190,21 @@ __global__ void __launch_bounds__(128) fp8_vt_kernel(const uint16_t* __restrict_
     const float m = __uint_as_float(vmax[static_cast<size_t>(b) * Hkv + hk]);
     const float inv = m > 0.f ? kE4m3Max / m : 1.f;
     if (blk == 0 && threadIdx.x == 0) sv[static_cast<size_t>(b) * Hkv + hk] = m > 0.f ? m / kE4m3Max : 1.f;
-    for (int i = threadIdx.x; i < 128 * 16; i += 128) {
-        const int kk = i / 16, c8 = (i % 16) * 8;
-        const int n = blk * 128 + kk;
-        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (n < N)
-            u = *reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + c8);
-        *reinterpret_cast<uint4*>(&tile[kk][c8]) = u;
+    {
+        uint4 u[16];  // all of a thread's sixteen loads in flight at once
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = threadIdx.x + 128 * k;
+            const int n = blk * 128 + i / 16;
+            u[k] = (n < N) ? *reinterpret_cast<const uint4*>(
+                                 v + ((static_cast<size_t>(b) * N + n) * Hkv + hk) * 128 + (i % 16) * 8)
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = threadIdx.x + 128 * k;
+            *reinterpret_cast<uint4*>(&tile[i / 16][(i % 16) * 8]) = u[k];
+        }
     }
     __syncthreads();
     const int c = threadIdx.x;  // head-dimension column = output row
