@@ -40,10 +40,11 @@ using namespace bwd;
 // Warp roles: warps 0-15 are four compute warpgroups (warpgroup w takes
 // queries 32w..32w+31 of every block: four warps per SM sub-partition keep the
 // exp2 and FMA pipes busy through each other's latencies), warp 16 issues the
-// MMAs, warp 17 loads.
+// MMAs, warp 17 loads, warp 18 stores each item's dV and dK.
 constexpr int kDkWarpMma = 16;
 constexpr int kDkWarpLoad = 17;
-constexpr int kDkThreads = 18 * 32;
+constexpr int kDkWarpStore = 18;
+constexpr int kDkThreads = 19 * 32;
 constexpr int kDkCompute = 512;  // compute threads
 
 template <int D>
@@ -52,16 +53,32 @@ struct DkdvCfg : Tiles<D> {
     // {Q_i, dO_i} ring stages: a stage's next load starts when dK of its last
     // step is done; at d = 64 (32 KB stages) shared memory has room for a third
     static constexpr int NST = (D == 64) ? 3 : 2;
-    // smem: K, V, then NST stages of {Q_i, dO_i}, then per-stage lse2 / D vectors
+    // d = 64: persistent CTAs, one per SM, dealt items longest first; dV and
+    // dK are staged for their TMA stores in a buffer of their own, so the next
+    // item's first stages can land meanwhile.  d = 128 has no room for that
+    // buffer: one item per CTA, dV and dK staged in stage 0's tiles.
+    static constexpr bool PERSIST = (D == 64);
+    // smem: K, V, then NST stages of {Q_i, dO_i}, then per-stage lse2 / D
+    // vectors, then (d = 64) the dV, dK staging tiles
     static constexpr int OFF_STAGE = 2 * T::TILE;
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
-    static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
-    // barriers: K/V, stage full[NST], stage empty[NST], dP^T ready, dP^T
-    // copied to registers, P^T written, dS^T written, all MMAs done, S^T ready
-    static constexpr int NBAR = 1 + 2 * NST + 1 + 1 + 1 + 1 + 1 + 1;
+    static constexpr int OFF_ST = OFF_VEC + NST * VEC_BYTES;  // a multiple of 1024
+    static constexpr int OFF_BAR = OFF_ST + (PERSIST ? 2 * T::TILE : 0);
+    // barriers: K/V full, stage full[NST], stage empty[NST], dP^T ready, dP^T
+    // copied to registers, P^T written, dS^T written, an item's MMAs done, S^T
+    // ready, K/V free, dV/dK staged, staging free, all MMAs done
+    static constexpr int NBAR = 1 + 2 * NST + 6 + 4;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
+    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB a block may use");
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
+};
+
+// One work item: (batch, kv head, 128-key block), low key blocks (the most
+// query blocks under the causal mask) first; its steps are (query head of the
+// group, query block) pairs.
+struct DkItem {
+    int b, hk, jb, qi0, nqi, n_it;
 };
 
 // F16: every operand tile is the fp16 copy (Q, K, V, dO scaled by 2^q, 2^k,
@@ -83,6 +100,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t sK = smem_u32(smem);
     const uint32_t sV = sK + C::TILE;
     const uint32_t sStage = sK + C::OFF_STAGE;  // stage s: Q at +2s*TILE, dO after it
+    // where dV (which = 0) and dK (which = 1) are staged for their stores
+    const uint32_t sST = C::PERSIST ? sK + C::OFF_ST : sStage;
     float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // stage s: lse2 at s*256, D at +128
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
@@ -90,24 +109,36 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t BAR_KV = bar0;
     auto BAR_STF = [&](int s) { return bar0 + 8u * (1 + s); };
     auto BAR_STE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
-    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // block's dP^T ready
+    const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // step's dP^T ready
     const uint32_t BAR_LD = BAR_SDF + 8u;                   // dP^T copied to registers
     const uint32_t BAR_PF = BAR_SDF + 16u;                  // P^T written
     const uint32_t BAR_DSF = BAR_SDF + 24u;                 // dS^T written
-    const uint32_t BAR_ACC = BAR_SDF + 32u;
-    const uint32_t BAR_STR = BAR_SDF + 40u;                 // block's S^T ready
+    const uint32_t BAR_ACC = BAR_SDF + 32u;                 // the item's dV, dK complete
+    const uint32_t BAR_STR = BAR_SDF + 40u;                 // step's S^T ready
+    const uint32_t BAR_KVE = BAR_SDF + 48u;                 // the item's K, V no longer read
+    const uint32_t BAR_EPF = BAR_SDF + 56u;                 // the item's dV, dK staged
+    const uint32_t BAR_EPE = BAR_SDF + 64u;                 // the staging stored (free again)
+    const uint32_t BAR_DONE = BAR_SDF + 72u;
 
     const int warp = warp_id();
     const int lane = lane_id();
     const int nqb = (a.N + kBM - 1) / kBM;
     const int per = a.B * a.Hkv;
-    const int jb = static_cast<int>(blockIdx.x) / per;  // causal: low key blocks have most work
-    const int bh = static_cast<int>(blockIdx.x) % per;
-    const int b = bh / a.Hkv;
-    const int hk = bh % a.Hkv;
-    const int qi0 = a.causal ? jb : 0;  // first query block that sees this key block
-    const int nqi = nqb - qi0;
-    const int n_it = a.g * nqi;         // (query head of the group, query block) pairs
+    const int n_items = nqb * per;
+    // Steps carry global indices g across a CTA's items, so the stage ring,
+    // the TMEM regions (X/Y by g's parity) and the per-step barriers run on
+    // from one item to the next.
+    auto item = [&](int w) {
+        DkItem I;
+        I.jb = w / per;  // causal: low key blocks have most work
+        const int bh = w % per;
+        I.b = bh / a.Hkv;
+        I.hk = bh % a.Hkv;
+        I.qi0 = a.causal ? I.jb : 0;  // first query block that sees this key block
+        I.nqi = nqb - I.qi0;
+        I.n_it = a.g * I.nqi;         // (query head of the group, query block) pairs
+        return I;
+    };
 
     if (warp == 0 && lane == 0) {
         mbar_init(BAR_KV, 1);
@@ -121,6 +152,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_init(BAR_DSF, kDkCompute);
         mbar_init(BAR_ACC, 1);
         mbar_init(BAR_STR, 1);
+        mbar_init(BAR_KVE, 1);
+        mbar_init(BAR_EPF, kDkCompute);
+        mbar_init(BAR_EPE, 1);
+        mbar_init(BAR_DONE, 1);
         fence_barrier_init();
     }
     if (warp == kDkWarpMma) {
@@ -131,6 +166,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // region of S^T(g) (then P^T, dS^T), and of dP^T(g)
+    auto reg_s = [&](int g) { return tbase + ((g & 1) ? C::TM_Y : C::TM_X); };
+    auto reg_d = [&](int g) { return tbase + ((g & 1) ? C::TM_X : C::TM_Y); };
 
     if (warp == kDkWarpLoad) {
         // TMA for tiles (lane 0); all 32 lanes fill the per-query lse2 / D vectors
@@ -141,11 +179,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             tma_prefetch_desc(&tmDO);
             tma_prefetch_desc(&tmDK);
             tma_prefetch_desc(&tmDV);
-            mbar_arrive_expect_tx(BAR_KV, 2 * C::TILE);
-            for (int c = 0; c < C::NCH; ++c) {
-                tma_load_4d(sK + c * C::CHUNK, &tmK, BAR_KV, c * 64, hk, jb * kBN, b);
-                tma_load_4d(sV + c * C::CHUNK, &tmV, BAR_KV, c * 64, hk, jb * kBN, b);
-            }
         }
         const uint64_t pol_q = l2_policy_evict_last();
         int last_it[C::NST];
@@ -153,64 +186,97 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         // fp16 path: D is staged times 2^ds, the scale of dP^T (V dO^T of the
         // copies carries exactly 2^ds: the copy of dO is scaled by ds - v)
         const float dsc = F16 ? pow2f(ld_once(&a.f16s->ds)) : 1.f;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % C::NST;
-            const int hq = hk * a.g + it / nqi;
-            const int qi = qi0 + it % nqi;
-            // this block's lse2 / D, read from global memory before waiting for
-            // the stage so that their latency overlaps the wait
-            const size_t base = (static_cast<size_t>(b) * a.Hq + hq) * a.N;
-            float lv[4], dv4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = qi * kBM + lane * 4 + u;
-                // a query row past N contributes nothing: P = exp2(-inf) = 0
-                lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
-                dv4[u] = (q < a.N) ? a.dsum[base + q] * dsc : 0.f;
-            }
-            // L2 prefetch of the Q, dO tiles two steps ahead (no slot needed)
-            if (lane == 0 && it + 2 < n_it) {
-                const int it2 = it + 2;
-                const int hq2 = hk * a.g + it2 / nqi, q2 = (qi0 + it2 % nqi) * kBM;
-                for (int c = 0; c < C::NCH; ++c) {
-                    tma_prefetch_4d(&tmQ, c * 64, hq2, q2, b, pol_q);
-                    tma_prefetch_4d(&tmDO, c * 64, hq2, q2, b, pol_q);
-                }
-            }
-            if (!mbar_wait_warp(BAR_STE(s), ((it / C::NST) & 1) ^ 1u, a.watch, 30)) break;
+        bool ok = true;
+        int g0 = 0, it = 0;
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+            const DkItem I = item(w);
+            // the previous item's last S^T and dP^T are done with K, V
+            if (it > 0 && !(ok = mbar_wait_warp(BAR_KVE, (it - 1) & 1, a.watch, 44))) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
-                const uint32_t dst = sStage + 2 * s * C::TILE;
+                mbar_arrive_expect_tx(BAR_KV, 2 * C::TILE);
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d_hint(dst + c * C::CHUNK, &tmQ, BAR_STF(s), c * 64, hq, qi * kBM, b,
-                                     pol_q);
-                    tma_load_4d_hint(dst + C::TILE + c * C::CHUNK, &tmDO, BAR_STF(s), c * 64, hq,
-                                     qi * kBM, b, pol_q);
+                    tma_load_4d(sK + c * C::CHUNK, &tmK, BAR_KV, c * 64, I.hk, I.jb * kBN, I.b);
+                    tma_load_4d(sV + c * C::CHUNK, &tmV, BAR_KV, c * 64, I.hk, I.jb * kBN, I.b);
                 }
             }
-            float* lse2 = vec + s * 2 * kBM;
-            *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
-            *reinterpret_cast<float4*>(lse2 + kBM + lane * 4) =
-                make_float4(dv4[0], dv4[1], dv4[2], dv4[3]);
-            mbar_arrive(BAR_STF(s));
-            last_it[s] = it;
+            for (int j = 0; j < I.n_it; ++j) {
+                const int g = g0 + j;
+                const int s = g % C::NST;
+                const int hq = I.hk * a.g + j / I.nqi;
+                const int qi = I.qi0 + j % I.nqi;
+                // this step's lse2 / D, read from global memory before waiting for
+                // the stage so that their latency overlaps the wait
+                const size_t base = (static_cast<size_t>(I.b) * a.Hq + hq) * a.N;
+                float lv[4], dv4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int q = qi * kBM + lane * 4 + u;
+                    // a query row past N contributes nothing: P = exp2(-inf) = 0
+                    lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
+                    dv4[u] = (q < a.N) ? a.dsum[base + q] * dsc : 0.f;
+                }
+                // L2 prefetch of the Q, dO tiles two steps ahead (no slot needed)
+                if (lane == 0 && j + 2 < I.n_it) {
+                    const int j2 = j + 2;
+                    const int hq2 = I.hk * a.g + j2 / I.nqi, q2 = (I.qi0 + j2 % I.nqi) * kBM;
+                    for (int c = 0; c < C::NCH; ++c) {
+                        tma_prefetch_4d(&tmQ, c * 64, hq2, q2, I.b, pol_q);
+                        tma_prefetch_4d(&tmDO, c * 64, hq2, q2, I.b, pol_q);
+                    }
+                }
+                if (!(ok = mbar_wait_warp(BAR_STE(s), ((g / C::NST) & 1) ^ 1u, a.watch, 30))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
+                    const uint32_t dst = sStage + 2 * s * C::TILE;
+                    for (int c = 0; c < C::NCH; ++c) {
+                        tma_load_4d_hint(dst + c * C::CHUNK, &tmQ, BAR_STF(s), c * 64, hq, qi * kBM,
+                                         I.b, pol_q);
+                        tma_load_4d_hint(dst + C::TILE + c * C::CHUNK, &tmDO, BAR_STF(s), c * 64, hq,
+                                         qi * kBM, I.b, pol_q);
+                    }
+                }
+                float* lse2 = vec + s * 2 * kBM;
+                *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+                *reinterpret_cast<float4*>(lse2 + kBM + lane * 4) =
+                    make_float4(dv4[0], dv4[1], dv4[2], dv4[3]);
+                mbar_arrive(BAR_STF(s));
+                last_it[s] = g;
+            }
+            g0 += I.n_it;
         }
         if (lane == 0) {  // no copies in flight at exit
-            mbar_drain(BAR_KV, 0, a.watch, 31);
+            if (it > 0) mbar_drain(BAR_KV, (it - 1) & 1, a.watch, 31);
             for (int s = 0; s < C::NST; ++s)
                 if (last_it[s] >= 0)
                     mbar_drain(BAR_STF(s), (last_it[s] / C::NST) & 1, a.watch, 31);
         }
         __syncwarp();
+    } else if (warp == kDkWarpStore) {
+        // ================= store: each item's staged dV and dK -> global memory =================
+        bool ok = true;
+        int it = 0;
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+            const DkItem I = item(w);
+            if (!(ok = mbar_wait_warp(BAR_EPF, it & 1, a.watch, 45))) break;
+            if (lane == 0) {
+                for (int which = 0; which < 2; ++which) {
+                    const CUtensorMap* tm = which ? &tmDK : &tmDV;
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_store_4d(tm, sST + which * C::TILE + c * C::CHUNK, c * 64, I.hk,
+                                     I.jb * kBN, I.b);
+                }
+                tma_store_commit();
+                tma_store_wait_read_all();
+                mbar_arrive(BAR_EPE);  // the staging may be written again
+            }
+            __syncwarp();
+        }
     } else if (warp == kDkWarpMma) {
         {
             const uint32_t leader = elect_one();
             constexpr uint32_t IDESC_S = idesc_16(kBN, kBM, false, false, F16);  // S^T, dP^T
             constexpr uint32_t IDESC_ACC = idesc_16(kBN, D, false, true, F16);  // dV, dK
             const uint32_t tDV = tbase + C::TM_ACC, tDK = tbase + C::TM_ACC + D;
-            // region of S^T(it) (then P^T, dS^T), and of dP^T(it)
-            auto reg_s = [&](int it) { return tbase + ((it & 1) ? C::TM_Y : C::TM_X); };
-            auto reg_d = [&](int it) { return tbase + ((it & 1) ? C::TM_X : C::TM_Y); };
             auto stage_q = [&](int s) { return sStage + 2 * s * C::TILE; };
             // descriptors built once per tile; each MMA only moves the start address
             constexpr uint32_t HI = sdesc_hi(1024);
@@ -224,59 +290,74 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     mma_bf16_ss_w(leader, dst, sdesc_at(a_lo, HI, off), sdesc_at(b_lo, HI, off), IDESC_S, ks > 0);
                 }
             };
-            // dV += P^T dO (dk = false) or dK += dS^T Q (dk = true): for queries
-            // 16ks.., P^T / dS^T (16-bit pairs) sit in columns 32w + (ks%2)*8 /
-            // 32w + 16 + (ks%2)*8 of S^T's region (w = ks/2); dO, Q rows 16ks.. are
-            // read MN-major
-            auto issue_acc = [&](int it, int s, bool dk) {
+            // dV += P^T dO (dk = false) or dK += dS^T Q (dk = true), starting afresh
+            // at an item's first step: for queries 16ks.., P^T / dS^T (16-bit
+            // pairs) sit in columns 32w + (ks%2)*8 / 32w + 16 + (ks%2)*8 of S^T's
+            // region (w = ks/2); dO, Q rows 16ks.. are read MN-major
+            auto issue_acc = [&](int g, int s, bool dk, bool first) {
                 const uint32_t b_lo = sdesc_lo(stage_q(s) + (dk ? 0 : C::TILE), C::CHUNK);
-                const uint32_t rs = reg_s(it) + (dk ? 16 : 0);
+                const uint32_t rs = reg_s(g) + (dk ? 16 : 0);
 #pragma unroll
                 for (int ks = 0; ks < kBM / 16; ++ks)
                     mma_bf16_ts_w(leader, dk ? tDK : tDV, rs + (ks >> 1) * 32 + (ks & 1) * 8,
-                                sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (it == 0 && ks == 0) ? 0u : 1u);
+                                sdesc_at(b_lo, HI, ks * 2048), IDESC_ACC, (first && ks == 0) ? 0u : 1u);
             };
-            bool ok = mbar_wait_warp(BAR_KV, 0, a.watch, 32) &&
-                      mbar_wait_warp(BAR_STF(0), 0, a.watch, 33);
-            if (ok) {
+            // per step: dV(g) once P^T(g) is written; S^T(g+1) over dP^T(g)
+            // once every warp holds dP^T(g); dK(g) once dS^T(g) is written;
+            // dP^T(g+1) over P^T(g), dS^T(g), which the two products above
+            // read first.  The warps form P^T(g+1) from S^T(g+1) while the
+            // tensor core runs dK(g) and dP^T(g+1).
+            bool ok = true;
+            int g0 = 0, it = 0;
+            for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+                const DkItem I = item(w);
+                const int n = I.n_it;
+                if (!(ok = mbar_wait_warp(BAR_KV, it & 1, a.watch, 32) &&
+                           mbar_wait_warp(BAR_STF(g0 % C::NST), (g0 / C::NST) & 1, a.watch, 33)))
+                    break;
+                // S^T(g0) goes over dP^T of the previous item's last step, which
+                // every warp holds (implied by its DSF, waited below; kept so that
+                // the parity waits on LD stay in order)
+                if (it > 0 && !(ok = mbar_wait_warp(BAR_LD, (g0 - 1) & 1, a.watch, 34))) break;
                 tc_fence_after();
-                issue_t(reg_s(0), k_lo, stage_q(0));
+                issue_t(reg_s(g0), k_lo, stage_q(g0 % C::NST));
                 mma_commit_w(leader, BAR_STR);
-                issue_t(reg_d(0), v_lo, stage_q(0) + C::TILE);
+                issue_t(reg_d(g0), v_lo, stage_q(g0 % C::NST) + C::TILE);
                 mma_commit_w(leader, BAR_SDF);
-            }
-            // per block: dV(it) once P^T(it) is written; S^T(it+1) over dP^T(it)
-            // once every warp holds dP^T(it); dK(it) once dS^T(it) is written;
-            // dP^T(it+1) over P^T(it), dS^T(it), which the two products above
-            // read first.  The warps form P^T(it+1) from S^T(it+1) while the
-            // tensor core runs dK(it) and dP^T(it+1).
-            for (int it = 0; it < n_it && ok; ++it) {
-                const int s = it % C::NST;
-                const int s2 = (it + 1) % C::NST;
-                const bool more = it + 1 < n_it;
-                if (!(ok = mbar_wait_warp(BAR_PF, it & 1, a.watch, 34))) break;
-                tc_fence_after();
-                issue_acc(it, s, false);
-                if (more) {
-                    if (!(ok = mbar_wait_warp(BAR_STF(s2), ((it + 1) / C::NST) & 1, a.watch, 33)))
-                        break;
-                    if (!(ok = mbar_wait_warp(BAR_LD, it & 1, a.watch, 34))) break;
+                if (n == 1) mma_commit_w(leader, BAR_KVE);  // the item's last S^T and dP^T
+                for (int j = 0; j < n && ok; ++j) {
+                    const int g = g0 + j;
+                    const int s = g % C::NST;
+                    const int s2 = (g + 1) % C::NST;
+                    const bool more = j + 1 < n;
+                    if (!(ok = mbar_wait_warp(BAR_PF, g & 1, a.watch, 34))) break;
                     tc_fence_after();
-                    issue_t(reg_d(it), k_lo, stage_q(s2));
-                    mma_commit_w(leader, BAR_STR);
+                    issue_acc(g, s, false, j == 0);
+                    if (more) {
+                        if (!(ok = mbar_wait_warp(BAR_STF(s2), ((g + 1) / C::NST) & 1, a.watch, 33)))
+                            break;
+                        if (!(ok = mbar_wait_warp(BAR_LD, g & 1, a.watch, 34))) break;
+                        tc_fence_after();
+                        issue_t(reg_s(g + 1), k_lo, stage_q(s2));  // over dP^T(g)
+                        mma_commit_w(leader, BAR_STR);
+                    }
+                    if (!(ok = mbar_wait_warp(BAR_DSF, g & 1, a.watch, 38))) break;
+                    tc_fence_after();
+                    issue_acc(g, s, true, j == 0);
+                    mma_commit_w(leader, BAR_STE(s));
+                    if (more) {
+                        issue_t(reg_d(g + 1), v_lo, stage_q(s2) + C::TILE);  // over P^T(g), dS^T(g)
+                        mma_commit_w(leader, BAR_SDF);
+                        if (j + 2 == n) mma_commit_w(leader, BAR_KVE);  // the item's last S^T, dP^T
+                    }
                 }
-                if (!(ok = mbar_wait_warp(BAR_DSF, it & 1, a.watch, 38))) break;
-                tc_fence_after();
-                issue_acc(it, s, true);
-                mma_commit_w(leader, BAR_STE(s));
-                if (more) {
-                    issue_t(reg_s(it), v_lo, stage_q(s2) + C::TILE);
-                    mma_commit_w(leader, BAR_SDF);
-                }
+                if (!ok) break;
+                mma_commit_w(leader, BAR_ACC);  // the item's dV and dK are complete
+                g0 += n;
             }
             // every issued MMA has finished before TMEM is released
-            mma_commit_w(leader, BAR_ACC);
-            mbar_drain(BAR_ACC, 0, a.watch, 35);
+            mma_commit_w(leader, BAR_DONE);
+            mbar_drain(BAR_DONE, 0, a.watch, 35);
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -284,11 +365,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const int r = (warp & 3) * 32 + lane;
         const int t4 = lane & 3;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        // In the 16x256b TMEM shape a thread holds, of each 16-lane block of its
-        // warp's 32 lanes, rows lane/4 and lane/4 + 8 and the 8 columns
-        // 8j + 2(lane%4) + {0,1} of the warpgroup's 32: so it needs only 8
-        // entries of the query-indexed vectors lse2 and D.
-        const int key0 = jb * kBN + (warp & 3) * 32 + (lane >> 2);
         // fp16 path: undo 2^(q+k) on S^T; dP^T and the staged D both carry
         // 2^ds, so dS^T = P^T (dP^T - D) does too
         int eq = 0, ek = 0, ev = 0, edo = 0;
@@ -301,114 +377,121 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const float mul_e = which ? a.scale * pow2f(-(eds + eq)) : pow2f(-edo);
         const uint64_t sl2x2 = f2(sl2, sl2);
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % C::NST;
-            const int qi = qi0 + it % nqi;
-            const uint32_t rs = tbase + ((it & 1) ? C::TM_Y : C::TM_X) + wg * 32 + lane_off;
-            const uint32_t rd = tbase + ((it & 1) ? C::TM_X : C::TM_Y) + wg * 32 + lane_off;
-            const float* lse2 = vec + s * 2 * kBM + wg * 32;
-            const float* dvec = vec + s * 2 * kBM + kBM + wg * 32;
-            const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
-            // ---- P^T = exp2(S^T scale log2 e - lse2), as soon as S^T is in TMEM
-            if (!(ok = mbar_wait_warp(BAR_STR, it & 1, a.watch, 36))) break;
-            tc_fence_after();
-            uint64_t nl[4];  // -lse2 of the thread's column pairs
+        int g0 = 0, it = 0;
+        for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
+            const DkItem I = item(w);
+            // In the 16x256b TMEM shape a thread holds, of each 16-lane block of
+            // its warp's 32 lanes, rows lane/4 and lane/4 + 8 and the 8 columns
+            // 8j + 2(lane%4) + {0,1} of the warpgroup's 32: so it needs only 8
+            // entries of the query-indexed vectors lse2 and D.
+            const int key0 = I.jb * kBN + (warp & 3) * 32 + (lane >> 2);
+            for (int j = 0; j < I.n_it; ++j) {
+                const int g = g0 + j;
+                const int s = g % C::NST;
+                const int qi = I.qi0 + j % I.nqi;
+                const uint32_t rs = reg_s(g) + wg * 32 + lane_off;
+                const uint32_t rd = reg_d(g) + wg * 32 + lane_off;
+                const float* lse2 = vec + s * 2 * kBM + wg * 32;
+                const float* dvec = vec + s * 2 * kBM + kBM + wg * 32;
+                const int qbase = qi * kBM + wg * 32 + 2 * t4;  // query of the thread's column 0
+                // ---- P^T = exp2(S^T scale log2 e - lse2), as soon as S^T is in TMEM
+                if (!(ok = mbar_wait_warp(BAR_STR, g & 1, a.watch, 36))) break;
+                tc_fence_after();
+                uint64_t nl[4];  // -lse2 of the thread's column pairs
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * j + 2 * t4);
-                nl[j] = f2(-l2.x, -l2.y);
-            }
-            uint32_t pk[2][8];  // P^T (16-bit pairs), kept for dS^T
-#pragma unroll
-            for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
-                const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
-                uint32_t sv[16];
-                tmem_ld16x256_x4(rs + lo, sv);
-                tmem_wait_ld();
-                reg_fence<16>(sv);
-                const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
-                // causal: key k is hidden from query q when k > q
-                const bool need_mask = a.causal && key + 8 > qbase;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                    for (int rsel = 0; rsel < 2; ++rsel) {
-                        const int i = 4 * j + 2 * rsel;
-                        float x0, x1;
-                        f2_split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2,
-                                      nl[j]), x0, x1);
-                        float p0 = ex2(x0), p1 = ex2(x1);
-                        if (need_mask) {
-                            const int q = qbase + 8 * j, k = key + 8 * rsel;
-                            p0 = (k > q) ? 0.f : p0;
-                            p1 = (k > q + 1) ? 0.f : p1;
-                        }
-                        pk[lb][2 * j + rsel] = pack_op<F16>(p0, p1);
-                    }
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float2 l2 = *reinterpret_cast<const float2*>(lse2 + 8 * jj + 2 * t4);
+                    nl[jj] = f2(-l2.x, -l2.y);
                 }
-                tmem_st16x128_x4(rs + lo, pk[lb]);  // P^T over the first 16 S^T columns read
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR_PF);
-            // ---- dS^T = P^T (dP^T - D), once dP^T is in TMEM (from the rounded P^T)
-            if (!(ok = mbar_wait_warp(BAR_SDF, it & 1, a.watch, 40))) break;
-            tc_fence_after();
-            uint32_t dp[2][16];
-            tmem_ld16x256_x4(rd, dp[0]);
-            tmem_ld16x256_x4(rd + (16u << 16), dp[1]);
-            uint64_t nd[4];  // -D of the thread's column pairs
+                uint32_t pk[2][8];  // P^T (16-bit pairs), kept for dS^T
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * j + 2 * t4);
-                nd[j] = f2(-d2.x, -d2.y);
-            }
-            tmem_wait_ld();
-            reg_fence<16>(dp[0]);
-            reg_fence<16>(dp[1]);
-            // every warp holds dP^T: S^T(it+1) may overwrite it
-            tc_fence_before();
-            mbar_arrive(BAR_LD);
-            uint32_t dk[2][8];
+                for (int lb = 0; lb < 2; ++lb) {  // TMEM lanes 16*lb.. of the warp's 32
+                    const uint32_t lo = static_cast<uint32_t>(lb * 16) << 16;
+                    uint32_t sv[16];
+                    tmem_ld16x256_x4(rs + lo, sv);
+                    tmem_wait_ld();
+                    reg_fence<16>(sv);
+                    const int key = key0 + 16 * lb;  // key of the thread's first row (+8: second)
+                    // causal: key k is hidden from query q when k > q
+                    const bool need_mask = a.causal && key + 8 > qbase;
 #pragma unroll
-            for (int lb = 0; lb < 2; ++lb)
+                    for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int rsel = 0; rsel < 2; ++rsel) {
-                        const int i = 4 * j + 2 * rsel;
-                        float p0, p1, e0, e1;
-                        unpack_op<F16>(pk[lb][2 * j + rsel], p0, p1);
-                        f2_split(mul2(f2(p0, p1),
-                                      add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
-                                           nd[j])), e0, e1);
-                        dk[lb][2 * j + rsel] = pack_op<F16>(e0, e1);
+                        for (int rsel = 0; rsel < 2; ++rsel) {
+                            const int i = 4 * jj + 2 * rsel;
+                            float x0, x1;
+                            f2_split(fma2(f2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2x2,
+                                          nl[jj]), x0, x1);
+                            float p0 = ex2(x0), p1 = ex2(x1);
+                            if (need_mask) {
+                                const int q = qbase + 8 * jj, k = key + 8 * rsel;
+                                p0 = (k > q) ? 0.f : p0;
+                                p1 = (k > q + 1) ? 0.f : p1;
+                            }
+                            pk[lb][2 * jj + rsel] = pack_op<F16>(p0, p1);
+                        }
                     }
-            tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
-            tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(BAR_DSF);
-        }
-        const bool ok_e = ok && mbar_wait_warp(BAR_ACC, 0, a.watch, 37);
-        // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 those
-        // of dK = scale * (dS^T Q); staging reuses stage 0's Q (dV) and dO (dK)
-        // buffers, idle once all MMAs are done
-        const uint32_t stage = sStage + which * C::TILE;
-        if (ok_e) {
+                    tmem_st16x128_x4(rs + lo, pk[lb]);  // P^T over the first 16 S^T columns read
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR_PF);
+                // ---- dS^T = P^T (dP^T - D), once dP^T is in TMEM (from the rounded P^T)
+                if (!(ok = mbar_wait_warp(BAR_SDF, g & 1, a.watch, 40))) break;
+                tc_fence_after();
+                uint32_t dp[2][16];
+                tmem_ld16x256_x4(rd, dp[0]);
+                tmem_ld16x256_x4(rd + (16u << 16), dp[1]);
+                uint64_t nd[4];  // -D of the thread's column pairs
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float2 d2 = *reinterpret_cast<const float2*>(dvec + 8 * jj + 2 * t4);
+                    nd[jj] = f2(-d2.x, -d2.y);
+                }
+                tmem_wait_ld();
+                reg_fence<16>(dp[0]);
+                reg_fence<16>(dp[1]);
+                // every warp holds dP^T: S^T(g+1) may overwrite it
+                tc_fence_before();
+                mbar_arrive(BAR_LD);
+                uint32_t dk[2][8];
+#pragma unroll
+                for (int lb = 0; lb < 2; ++lb)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int rsel = 0; rsel < 2; ++rsel) {
+                            const int i = 4 * jj + 2 * rsel;
+                            float p0, p1, e0, e1;
+                            unpack_op<F16>(pk[lb][2 * jj + rsel], p0, p1);
+                            f2_split(mul2(f2(p0, p1),
+                                          add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
+                                               nd[jj])), e0, e1);
+                            dk[lb][2 * jj + rsel] = pack_op<F16>(e0, e1);
+                        }
+                tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
+                tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(BAR_DSF);
+            }
+            if (!ok) break;
+            g0 += I.n_it;
+            // ---- epilogue: warpgroups 0, 1 write the two column halves of dV,
+            // warpgroups 2, 3 those of dK = scale * (dS^T Q), into the staging
+            // for the store warp.  The next item's dV, dK products start the
+            // accumulators afresh only after PF / DSF of its first step, which
+            // every warp arrives on after these TMEM loads.
+            if (!(ok = mbar_wait_warp(BAR_ACC, it & 1, a.watch, 37))) break;
             tc_fence_after();
+            // the staging is free once the previous item's stores have read it
+            if (C::PERSIST && it > 0 && !(ok = mbar_wait_warp(BAR_EPE, (it - 1) & 1, a.watch, 46)))
+                break;
             // dV carries 2^dout, dK 2^(ds+q) on the fp16 path
-            stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + which * D + lane_off, stage, r,
-                                      half * (D / 2), (half + 1) * (D / 2), mul_e);
+            stage_rows_bf16<C::CHUNK>(tbase + C::TM_ACC + which * D + lane_off, sST + which * C::TILE,
+                                      r, half * (D / 2), (half + 1) * (D / 2), mul_e);
             fence_proxy_async_smem();
-        }
-        named_bar_sync(1 + which, 256);
-        if (ok_e && half == 0 && r == 0) {
-            const CUtensorMap* tm = which ? &tmDK : &tmDV;
-            for (int c = 0; c < C::NCH; ++c)
-                tma_store_4d(tm, stage + c * C::CHUNK, c * 64, hk, jb * kBN, b);
-            tma_store_commit();
-            tma_store_wait_read_all();
+            mbar_arrive(BAR_EPF);
         }
     }
 
@@ -428,14 +511,15 @@ cudaError_t launch_dkdv(const BwdMaps& m, const BwdArgs& a, cudaStream_t st) {
     constexpr int smem = DkdvCfg<D>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long nblk = static_cast<long long>((a.N + kBN - 1) / kBN) * a.B * a.Hkv;
-    if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const long long items = static_cast<long long>((a.N + kBN - 1) / kBN) * a.B * a.Hkv;
+    if (items <= 0 || items > 0x7fffffffLL || a.num_ctas <= 0) return cudaErrorInvalidConfiguration;
+    // d = 64: persistent, one CTA per SM; d = 128: one CTA per item
+    const long long ctas = DkdvCfg<D>::PERSIST ? (items < a.num_ctas ? items : a.num_ctas) : items;
+    const unsigned grid = static_cast<unsigned>(ctas);
     if (F16)
-        kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q16, m.k16, m.v16, m.dout16,
-                                                                  m.dk, m.dv, a);
+        kern<<<grid, kDkThreads, smem, st>>>(m.q16, m.k16, m.v16, m.dout16, m.dk, m.dv, a);
     else
-        kern<<<static_cast<unsigned>(nblk), kDkThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk,
-                                                                  m.dv, a);
+        kern<<<grid, kDkThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, a);
     return cudaGetLastError();
 }
 

@@ -630,6 +630,163 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     return model
 
 
+def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
+    """The persistent dK/dV kernel (d = 64): one CTA walks `items`, each the
+    query-step count of one (batch, kv head, 128-key block).  Steps carry
+    global indices g across items, so the {Q, dO} stage ring, the TMEM
+    regions (X/Y by g's parity) and the per-step barriers run on.  Within an
+    item the order is the one-item kernel's two-step order.  K and V are
+    reloaded once the item's last S^T and dP^T have read them (KVE: a commit
+    after the item's last dP^T).  An item's first S^T goes over dP^T of the
+    previous item's last step, so it waits for LD of that step.  dV and dK of
+    the next item start afresh only after PF / DSF of its first step, which
+    the warps arrive on after their epilogue's TMEM loads.  The warps stage
+    dV and dK in a buffer of their own once the store warp has read the
+    previous item's (EPE), and the store warp stores them (EPF).  (The
+    cross-item LD wait is implied here: the MMA thread waited for DSF of that
+    step, which every warp arrives on after LD; the kernel keeps it anyway.)
+    lagging_store makes the store warp read an item's staging only after the
+    next item's accumulators are done, the lag EPE exists for.  mistake:
+    "no_kve", "no_epe" drop the matching wait."""
+    warps = [(g, q) for g in range(4) for q in range(4)]
+    starts = [sum(items[:i]) for i in range(len(items))]
+
+    def model(rnd):
+        bars = {"KV": 1, "KVE": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1,
+                "STR": 1, "EPF": 512, "EPE": 1, "DONE": 1}
+        for s_ in range(NST):
+            bars[f"STF{s_}"] = 1 + 32
+            bars[f"STE{s_}"] = 1
+
+        def reg_s(g):
+            return "Y" if g & 1 else "X"
+
+        def reg_d(g):
+            return "X" if g & 1 else "Y"
+
+        def region(r, tag):
+            return {f"{r}.{w}.{q}.{c}": tag for w, q in warps for c in "pd"}
+
+        def producer():
+            last = {}
+            for it, n in enumerate(items):
+                if it > 0 and mistake != "no_kve":
+                    yield ("wait", "KVE", it - 1)
+                yield ("load", "KV", it, {"K": f"K({it})", "V": f"V({it})"})
+                for j in range(n):
+                    g = starts[it] + j
+                    sl = g % NST
+                    yield ("wait", f"STE{sl}", g // NST - 1)
+                    tags = {f"Q{sl}": f"Q({g})"}
+                    tags.update({f"dO{sl}.{w}.{q}": f"dO({g})" for w, q in warps})
+                    yield ("load", f"STF{sl}", g // NST, tags)
+                    yield ("write", {f"vec{sl}": f"lse,D({g})"})
+                    yield ("arrive", f"STF{sl}", 32, g // NST)
+                    last[sl] = g // NST
+            if items:
+                yield ("wait", "KV", len(items) - 1)
+            for sl, ph in last.items():
+                yield ("wait", f"STF{sl}", ph)
+
+        def st_mma(it, g):
+            return ("mma", f"S^T({g})", {"K": f"K({it})", f"Q{g % NST}": f"Q({g})"},
+                    region(reg_s(g), f"S^T({g})"))
+
+        def dpt_mma(it, g):
+            reads = {"V": f"V({it})"}
+            reads.update({f"dO{g % NST}.{w}.{q}": f"dO({g})" for w, q in warps})
+            return ("mma", f"dP^T({g})", reads, region(reg_d(g), f"dP^T({g})"))
+
+        def dv_mma(it, j, g):
+            reads = {f"{reg_s(g)}.{w}.{q}.p": f"P^T({g})" for w, q in warps}
+            reads.update({f"dO{g % NST}.{w}.{q}": f"dO({g})" for w, q in warps})
+            if j > 0:
+                reads["dV"] = f"dV({it},{j - 1})"
+            return ("mma", f"dV({g})", reads, {"dV": f"dV({it},{j})"})
+
+        def dk_mma(it, j, g):
+            reads = {f"{reg_s(g)}.{w}.{q}.d": f"dS^T({g})" for w, q in warps}
+            reads[f"Q{g % NST}"] = f"Q({g})"
+            if j > 0:
+                reads["dK"] = f"dK({it},{j - 1})"
+            return ("mma", f"dK({g})", reads, {"dK": f"dK({it},{j})"})
+
+        def mma():
+            for it, n in enumerate(items):
+                g0 = starts[it]
+                yield ("wait", "KV", it)
+                yield ("wait", f"STF{g0 % NST}", g0 // NST)
+                if it > 0 and mistake != "no_ld_cross":
+                    yield ("wait", "LD", g0 - 1)  # S^T(g0) goes over dP^T(g0 - 1)
+                yield st_mma(it, g0)
+                yield ("commit", "STR", g0)
+                yield dpt_mma(it, g0)
+                yield ("commit", "SDF", g0)
+                if n == 1:
+                    yield ("commit", "KVE", it)
+                for j in range(n):
+                    g = g0 + j
+                    more = j + 1 < n
+                    yield ("wait", "PF", g)
+                    yield dv_mma(it, j, g)
+                    if more:
+                        yield ("wait", f"STF{(g + 1) % NST}", (g + 1) // NST)
+                        yield ("wait", "LD", g)
+                        yield st_mma(it, g + 1)
+                        yield ("commit", "STR", g + 1)
+                    yield ("wait", "DSF", g)
+                    yield dk_mma(it, j, g)
+                    yield ("commit", f"STE{g % NST}", g // NST)
+                    if more:
+                        yield dpt_mma(it, g + 1)
+                        yield ("commit", "SDF", g + 1)
+                        if j + 2 == n:
+                            yield ("commit", "KVE", it)  # the item's last S^T and dP^T
+                yield ("commit", "ACC", it)
+            yield ("commit", "DONE", 0)
+            yield ("wait", "DONE", 0)
+
+        def compute(w, q):
+            me = f"{w}.{q}"
+            for it, n in enumerate(items):
+                for j in range(n):
+                    g = starts[it] + j
+                    sl = g % NST
+                    rs, rd = reg_s(g), reg_d(g)
+                    yield ("wait", "STR", g)
+                    yield ("read", {f"{rs}.{me}.p": f"S^T({g})", f"{rs}.{me}.d": f"S^T({g})",
+                                    f"vec{sl}": f"lse,D({g})"})
+                    yield ("write", {f"{rs}.{me}.p": f"P^T({g})"})
+                    yield ("arrive", "PF", 32, g)
+                    yield ("wait", "SDF", g)
+                    yield ("read", {f"{rd}.{me}.p": f"dP^T({g})", f"{rd}.{me}.d": f"dP^T({g})",
+                                    f"vec{sl}": f"lse,D({g})"})
+                    yield ("arrive", "LD", 32, g)
+                    yield ("write", {f"{rs}.{me}.d": f"dS^T({g})"})
+                    yield ("arrive", "DSF", 32, g)
+                yield ("wait", "ACC", it)
+                yield ("read", {"dV": f"dV({it},{n - 1})", "dK": f"dK({it},{n - 1})"})
+                if it > 0 and mistake != "no_epe":
+                    yield ("wait", "EPE", it - 1)
+                yield ("write", {f"ST.{me}": f"out({it})"})
+                yield ("arrive", "EPF", 32, it)
+
+        def store():
+            for it in range(len(items)):
+                yield ("wait", "EPF", it)
+                if lagging_store and it + 1 < len(items):
+                    yield ("wait", "ACC", it + 1)
+                yield ("read", {f"ST.{w}.{q}": f"out({it})" for w, q in warps})
+                yield ("arrive", "EPE", 1, it)
+
+        roles = {"prod": producer(), "mma": mma(), "store": store()}
+        for w, q in warps:
+            roles[f"c{w}{q}"] = compute(w, q)
+        return bars, roles
+
+    return model
+
+
 def dq_persistent_model(items, KS=4, VS=3, copy_q=True, mistake=None):
     """The persistent dQ kernel (d = 64): one CTA walks `items`, each the key
     block count of one (batch, head, 128-query block).  Blocks carry global
@@ -1434,6 +1591,23 @@ def test_dq_protocol_late_ke(nj, ks, vs):
 def test_dq_protocol_deep_rings(nj):
     # d = 64: four K and three V ring slots
     each_seed(dq_model(nj, KS=4, VS=3, early_dp=True))
+
+
+DKDV_PERSISTENT_ITEMS = [[1], [2], [3], [16, 16], [1, 1, 1], [2, 3, 1, 4], [5, 1, 2], [3] * 6]
+
+
+@pytest.mark.parametrize("items", range(len(DKDV_PERSISTENT_ITEMS)))
+@pytest.mark.parametrize("lagging_store", [False, True])
+def test_dkdv_persistent_protocol(items, lagging_store):
+    each_seed(dkdv_persistent_model(DKDV_PERSISTENT_ITEMS[items], lagging_store=lagging_store),
+              seeds=range(40))
+
+
+@pytest.mark.parametrize("mistake,items,lag", [("no_kve", [3, 2, 4], False),
+                                               ("no_epe", [2, 1, 3], True)])
+def test_dkdv_persistent_planted_mistakes_are_caught(mistake, items, lag):
+    assert fails_on_some_seed(dkdv_persistent_model(items, mistake=mistake, lagging_store=lag),
+                              seeds=range(200))
 
 
 DQ_PERSISTENT_ITEMS = [[1], [2], [3], [16, 16], [1, 1, 1], [2, 3, 1, 4], [5, 1, 2], [3] * 6]
