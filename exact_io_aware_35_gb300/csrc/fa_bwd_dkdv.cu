@@ -462,12 +462,21 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 #pragma unroll
                         for (int rsel = 0; rsel < 2; ++rsel) {
                             const int i = 4 * jj + 2 * rsel;
-                            float p0, p1, e0, e1;
-                            unpack_op<F16>(pk[lb][2 * jj + rsel], p0, p1);
-                            f2_split(mul2(f2(p0, p1),
-                                          add2(f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])),
-                                               nd[jj])), e0, e1);
-                            dk[lb][2 * jj + rsel] = pack_op<F16>(e0, e1);
+                            const uint64_t t = add2(
+                                f2(__uint_as_float(dp[lb][i]), __uint_as_float(dp[lb][i + 1])), nd[jj]);
+                            if constexpr (F16) {
+                                // fp16 path: dP^T - D rounded to fp16, then one packed
+                                // fp16 product with the rounded P^T (two roundings of
+                                // 2^-11 each, three instructions a pair)
+                                float t0, t1;
+                                f2_split(t, t0, t1);
+                                dk[lb][2 * jj + rsel] = mul_f16x2(pk[lb][2 * jj + rsel], pack_f16(t0, t1));
+                            } else {
+                                float p0, p1, e0, e1;
+                                unpack_op<F16>(pk[lb][2 * jj + rsel], p0, p1);
+                                f2_split(mul2(f2(p0, p1), t), e0, e1);
+                                dk[lb][2 * jj + rsel] = pack_op<F16>(e0, e1);
+                            }
                         }
                 tmem_st16x128_x4(rs + 16, dk[0]);  // dS^T over the other 16
                 tmem_st16x128_x4(rs + (16u << 16) + 16, dk[1]);
