@@ -35,6 +35,14 @@
 namespace fa {
 namespace {
 
+// Elementwise product of two fp16 pairs, rounded once to fp16 (nearest even).
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+
 using namespace bwd;
 
 // Warp roles: warps 0-15 are four compute warpgroups (warpgroup w takes

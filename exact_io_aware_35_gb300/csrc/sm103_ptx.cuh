@@ -562,13 +562,6 @@ __device__ __forceinline__ uint32_t pack_op(float lo, float hi) {
     return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
 
-// Elementwise product of two fp16 pairs, rounded once to fp16 (nearest even).
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // The two values of a pack_op pair, exactly.
 template <bool F16>
 __device__ __forceinline__ void unpack_op(uint32_t w, float& lo, float& hi) {
