@@ -194,8 +194,27 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         // fp16 path: D is staged times 2^ds, the scale of dP^T (V dO^T of the
         // copies carries exactly 2^ds: the copy of dO is scaled by ds - v)
         const float dsc = F16 ? pow2f(ld_once(&a.f16s->ds)) : 1.f;
+        // A step's lse and D values (4 queries a lane) are read from global
+        // memory one step before the step that stages them and are first used
+        // there, so their latency never holds up the producer: two register sets,
+        // picked by the parity of the global step index (no copy between them,
+        // which would wait for the loads).  Rows past N read row N - 1 and are
+        // replaced when staged.
+        auto raw_vals = [&](const DkItem& It, int j, float (&r)[8]) {
+            const int hq = It.hk * a.g + j / It.nqi;
+            const int qi = It.qi0 + j % It.nqi;
+            const size_t base = (static_cast<size_t>(It.b) * a.Hq + hq) * a.N;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = min(qi * kBM + lane * 4 + u, a.N - 1);
+                r[u] = a.lse[base + q];
+                r[4 + u] = a.dsum[base + q];
+            }
+        };
+        float ra[8], rb[8];
         bool ok = true;
         int g0 = 0, it = 0;
+        if (static_cast<int>(blockIdx.x) < n_items) raw_vals(item(blockIdx.x), 0, ra);
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
             const DkItem I = item(w);
             // the previous item's last S^T and dP^T are done with K, V
@@ -212,42 +231,48 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 const int s = g % C::NST;
                 const int hq = I.hk * a.g + j / I.nqi;
                 const int qi = I.qi0 + j % I.nqi;
-                // this step's lse2 / D, read from global memory before waiting for
-                // the stage so that their latency overlaps the wait
-                const size_t base = (static_cast<size_t>(I.b) * a.Hq + hq) * a.N;
-                float lv[4], dv4[4];
+                auto step = [&](const float (&cur)[8], float (&nxt)[8]) -> bool {
+                    // the next step's values (the next item's first step after the last)
+                    if (j + 1 < I.n_it)
+                        raw_vals(I, j + 1, nxt);
+                    else if (w + static_cast<int>(gridDim.x) < n_items)
+                        raw_vals(item(w + gridDim.x), 0, nxt);
+                    // L2 prefetch of the Q, dO tiles two steps ahead (no slot needed)
+                    if (lane == 0 && j + 2 < I.n_it) {
+                        const int j2 = j + 2;
+                        const int hq2 = I.hk * a.g + j2 / I.nqi, q2 = (I.qi0 + j2 % I.nqi) * kBM;
+                        for (int c = 0; c < C::NCH; ++c) {
+                            tma_prefetch_4d(&tmQ, c * 64, hq2, q2, I.b, pol_q);
+                            tma_prefetch_4d(&tmDO, c * 64, hq2, q2, I.b, pol_q);
+                        }
+                    }
+                    if (!mbar_wait_warp(BAR_STE(s), ((g / C::NST) & 1) ^ 1u, a.watch, 30)) return false;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
+                        const uint32_t dst = sStage + 2 * s * C::TILE;
+                        for (int c = 0; c < C::NCH; ++c) {
+                            tma_load_4d_hint(dst + c * C::CHUNK, &tmQ, BAR_STF(s), c * 64, hq, qi * kBM,
+                                             I.b, pol_q);
+                            tma_load_4d_hint(dst + C::TILE + c * C::CHUNK, &tmDO, BAR_STF(s), c * 64, hq,
+                                             qi * kBM, I.b, pol_q);
+                        }
+                    }
+                    float lv[4], dv4[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int q = qi * kBM + lane * 4 + u;
-                    // a query row past N contributes nothing: P = exp2(-inf) = 0
-                    lv[u] = (q < a.N) ? a.lse[base + q] * kLog2e : INFINITY;
-                    dv4[u] = (q < a.N) ? a.dsum[base + q] * dsc : 0.f;
-                }
-                // L2 prefetch of the Q, dO tiles two steps ahead (no slot needed)
-                if (lane == 0 && j + 2 < I.n_it) {
-                    const int j2 = j + 2;
-                    const int hq2 = I.hk * a.g + j2 / I.nqi, q2 = (I.qi0 + j2 % I.nqi) * kBM;
-                    for (int c = 0; c < C::NCH; ++c) {
-                        tma_prefetch_4d(&tmQ, c * 64, hq2, q2, I.b, pol_q);
-                        tma_prefetch_4d(&tmDO, c * 64, hq2, q2, I.b, pol_q);
+                    for (int u = 0; u < 4; ++u) {
+                        // a query row past N contributes nothing: P = exp2(-inf) = 0
+                        const bool in = qi * kBM + lane * 4 + u < a.N;
+                        lv[u] = in ? cur[u] * kLog2e : INFINITY;
+                        dv4[u] = in ? cur[4 + u] * dsc : 0.f;
                     }
-                }
-                if (!(ok = mbar_wait_warp(BAR_STE(s), ((g / C::NST) & 1) ^ 1u, a.watch, 30))) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR_STF(s), 2 * C::TILE);
-                    const uint32_t dst = sStage + 2 * s * C::TILE;
-                    for (int c = 0; c < C::NCH; ++c) {
-                        tma_load_4d_hint(dst + c * C::CHUNK, &tmQ, BAR_STF(s), c * 64, hq, qi * kBM,
-                                         I.b, pol_q);
-                        tma_load_4d_hint(dst + C::TILE + c * C::CHUNK, &tmDO, BAR_STF(s), c * 64, hq,
-                                         qi * kBM, I.b, pol_q);
-                    }
-                }
-                float* lse2 = vec + s * 2 * kBM;
-                *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
-                *reinterpret_cast<float4*>(lse2 + kBM + lane * 4) =
-                    make_float4(dv4[0], dv4[1], dv4[2], dv4[3]);
-                mbar_arrive(BAR_STF(s));
+                    float* lse2 = vec + s * 2 * kBM;
+                    *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+                    *reinterpret_cast<float4*>(lse2 + kBM + lane * 4) =
+                        make_float4(dv4[0], dv4[1], dv4[2], dv4[3]);
+                    mbar_arrive(BAR_STF(s));
+                    return true;
+                };
+                if (!(ok = (g & 1) ? step(rb, ra) : step(ra, rb))) break;
                 last_it[s] = g;
             }
             g0 += I.n_it;
