@@ -66,17 +66,22 @@ struct DkdvCfg : Tiles<D> {
     // item's first stages can land meanwhile.  d = 128 has no room for that
     // buffer: one item per CTA, dV and dK staged in stage 0's tiles.
     static constexpr bool PERSIST = (D == 64);
+    // K/V buffers: at d = 64 item it's K, V go to buffer it % 2, loaded while
+    // item it - 1 runs (once item it - 2 is done with the buffer)
+    static constexpr int KVB = PERSIST ? 2 : 1;
     // smem: K, V, then NST stages of {Q_i, dO_i}, then per-stage lse2 / D
-    // vectors, then (d = 64) the dV, dK staging tiles
+    // vectors, then (d = 64) the dV, dK staging tiles and the second K, V
     static constexpr int OFF_STAGE = 2 * T::TILE;
     static constexpr int OFF_VEC = OFF_STAGE + NST * 2 * T::TILE;
     static constexpr int VEC_BYTES = 2 * kBM * 4;  // lse2[128], D[128]
     static constexpr int OFF_ST = OFF_VEC + NST * VEC_BYTES;  // a multiple of 1024
-    static constexpr int OFF_BAR = OFF_ST + (PERSIST ? 2 * T::TILE : 0);
+    static constexpr int OFF_KV2 = OFF_ST + (PERSIST ? 2 * T::TILE : 0);
+    static constexpr int OFF_BAR = OFF_KV2 + (KVB - 1) * 2 * T::TILE;
     // barriers: K/V full, stage full[NST], stage empty[NST], dP^T ready, dP^T
     // copied to registers, P^T written, dS^T written, an item's MMAs done, S^T
-    // ready, K/V free, dV/dK staged, staging free, all MMAs done
-    static constexpr int NBAR = 1 + 2 * NST + 6 + 4;
+    // ready, K/V free, dV/dK staged, staging free, all MMAs done, then K/V full
+    // and free of the second buffer
+    static constexpr int NBAR = 1 + 2 * NST + 6 + 4 + 2 * (KVB - 1);
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB a block may use");
     static constexpr uint32_t TM_X = 0, TM_Y = 128, TM_ACC = 256;
@@ -106,7 +111,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sK = smem_u32(smem);
-    const uint32_t sV = sK + C::TILE;
+    // K, V of buffer b (V follows K)
+    auto sK_of = [&](int b) { return b ? sK + C::OFF_KV2 : sK; };
     const uint32_t sStage = sK + C::OFF_STAGE;  // stage s: Q at +2s*TILE, dO after it
     // where dV (which = 0) and dK (which = 1) are staged for their stores
     const uint32_t sST = C::PERSIST ? sK + C::OFF_ST : sStage;
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
     const uint32_t bar0 = smem_u32(bars);
-    const uint32_t BAR_KV = bar0;
+    auto BAR_KV = [&](int b) { return b ? bar0 + 8u * (1 + 2 * C::NST + 10) : bar0; };
     auto BAR_STF = [&](int s) { return bar0 + 8u * (1 + s); };
     auto BAR_STE = [&](int s) { return bar0 + 8u * (1 + C::NST + s); };
     const uint32_t BAR_SDF = bar0 + 8u * (1 + 2 * C::NST);  // step's dP^T ready
@@ -123,7 +129,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t BAR_DSF = BAR_SDF + 24u;                 // dS^T written
     const uint32_t BAR_ACC = BAR_SDF + 32u;                 // the item's dV, dK complete
     const uint32_t BAR_STR = BAR_SDF + 40u;                 // step's S^T ready
-    const uint32_t BAR_KVE = BAR_SDF + 48u;                 // the item's K, V no longer read
+    auto BAR_KVE = [&](int b) {  // the item's K, V no longer read
+        return b ? BAR_SDF + 88u : BAR_SDF + 48u;
+    };
     const uint32_t BAR_EPF = BAR_SDF + 56u;                 // the item's dV, dK staged
     const uint32_t BAR_EPE = BAR_SDF + 64u;                 // the staging stored (free again)
     const uint32_t BAR_DONE = BAR_SDF + 72u;
@@ -149,7 +157,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     };
 
     if (warp == 0 && lane == 0) {
-        mbar_init(BAR_KV, 1);
+        for (int b = 0; b < C::KVB; ++b) {
+            mbar_init(BAR_KV(b), 1);
+            mbar_init(BAR_KVE(b), 1);
+        }
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(BAR_STF(s), 1 + 32);  // TMA transaction arrive + 32 lanes' vector writes
             mbar_init(BAR_STE(s), 1);
@@ -160,7 +171,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         mbar_init(BAR_DSF, kDkCompute);
         mbar_init(BAR_ACC, 1);
         mbar_init(BAR_STR, 1);
-        mbar_init(BAR_KVE, 1);
         mbar_init(BAR_EPF, kDkCompute);
         mbar_init(BAR_EPE, 1);
         mbar_init(BAR_DONE, 1);
@@ -217,13 +227,17 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         if (static_cast<int>(blockIdx.x) < n_items) raw_vals(item(blockIdx.x), 0, ra);
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
             const DkItem I = item(w);
-            // the previous item's last S^T and dP^T are done with K, V
-            if (it > 0 && !(ok = mbar_wait_warp(BAR_KVE, (it - 1) & 1, a.watch, 44))) break;
+            // the buffer's previous item's last S^T and dP^T are done with K, V
+            const int kb = it % C::KVB;
+            if (it >= C::KVB &&
+                !(ok = mbar_wait_warp(BAR_KVE(kb), ((it - C::KVB) / C::KVB) & 1, a.watch, 44)))
+                break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR_KV, 2 * C::TILE);
+                const uint32_t dK = sK_of(kb), dV = dK + C::TILE;
+                mbar_arrive_expect_tx(BAR_KV(kb), 2 * C::TILE);
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_4d(sK + c * C::CHUNK, &tmK, BAR_KV, c * 64, I.hk, I.jb * kBN, I.b);
-                    tma_load_4d(sV + c * C::CHUNK, &tmV, BAR_KV, c * 64, I.hk, I.jb * kBN, I.b);
+                    tma_load_4d(dK + c * C::CHUNK, &tmK, BAR_KV(kb), c * 64, I.hk, I.jb * kBN, I.b);
+                    tma_load_4d(dV + c * C::CHUNK, &tmV, BAR_KV(kb), c * 64, I.hk, I.jb * kBN, I.b);
                 }
             }
             for (int j = 0; j < I.n_it; ++j) {
@@ -278,7 +292,11 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             g0 += I.n_it;
         }
         if (lane == 0) {  // no copies in flight at exit
-            if (it > 0) mbar_drain(BAR_KV, (it - 1) & 1, a.watch, 31);
+            for (int b = 0; b < C::KVB; ++b)
+                if (it > b) {  // the buffer's last load
+                    const int last = b + ((it - 1 - b) / C::KVB) * C::KVB;
+                    mbar_drain(BAR_KV(b), (last / C::KVB) & 1, a.watch, 31);
+                }
             for (int s = 0; s < C::NST; ++s)
                 if (last_it[s] >= 0)
                     mbar_drain(BAR_STF(s), (last_it[s] / C::NST) & 1, a.watch, 31);
@@ -313,7 +331,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             auto stage_q = [&](int s) { return sStage + 2 * s * C::TILE; };
             // descriptors built once per tile; each MMA only moves the start address
             constexpr uint32_t HI = sdesc_hi(1024);
-            const uint32_t k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, 16);
             // dst = A B^T over the head dimension: S^T = K Q^T or dP^T = V dO^T
             auto issue_t = [&](uint32_t dst, uint32_t a_lo, uint32_t sB) {
                 const uint32_t b_lo = sdesc_lo(sB, 16);
@@ -345,7 +362,9 @@ __global__ void __launch_bounds__(kDkThreads, 1)
             for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++it) {
                 const DkItem I = item(w);
                 const int n = I.n_it;
-                if (!(ok = mbar_wait_warp(BAR_KV, it & 1, a.watch, 32) &&
+                const int kb = it % C::KVB;
+                const uint32_t k_lo = sdesc_lo(sK_of(kb), 16), v_lo = sdesc_lo(sK_of(kb) + C::TILE, 16);
+                if (!(ok = mbar_wait_warp(BAR_KV(kb), (it / C::KVB) & 1, a.watch, 32) &&
                            mbar_wait_warp(BAR_STF(g0 % C::NST), (g0 / C::NST) & 1, a.watch, 33)))
                     break;
                 // S^T(g0) goes over dP^T of the previous item's last step, which
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 mma_commit_w(leader, BAR_STR);
                 issue_t(reg_d(g0), v_lo, stage_q(g0 % C::NST) + C::TILE);
                 mma_commit_w(leader, BAR_SDF);
-                if (n == 1) mma_commit_w(leader, BAR_KVE);  // the item's last S^T and dP^T
+                if (n == 1) mma_commit_w(leader, BAR_KVE(kb));  // the item's last S^T and dP^T
                 for (int j = 0; j < n && ok; ++j) {
                     const int g = g0 + j;
                     const int s = g % C::NST;
@@ -381,7 +400,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                     if (more) {
                         issue_t(reg_d(g + 1), v_lo, stage_q(s2) + C::TILE);  // over P^T(g), dS^T(g)
                         mma_commit_w(leader, BAR_SDF);
-                        if (j + 2 == n) mma_commit_w(leader, BAR_KVE);  // the item's last S^T, dP^T
+                        if (j + 2 == n) mma_commit_w(leader, BAR_KVE(kb));  // the item's last S^T, dP^T
                     }
                 }
                 if (!ok) break;

@@ -630,7 +630,7 @@ def dkdv_model(n_it, NST=2, dk_before_dsf=False, ds_smem=False, ds_in_do=True, s
     return model
 
 
-def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
+def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False, kv_buffers=1):
     """The persistent dK/dV kernel (d = 64): one CTA walks `items`, each the
     query-step count of one (batch, kv head, 128-key block).  Steps carry
     global indices g across items, so the {Q, dO} stage ring, the TMEM
@@ -646,14 +646,21 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
     cross-item LD wait is implied here: the MMA thread waited for DSF of that
     step, which every warp arrives on after LD; the kernel keeps it anyway.)
     lagging_store makes the store warp read an item's staging only after the
-    next item's accumulators are done, the lag EPE exists for.  mistake:
-    "no_kve", "no_epe" drop the matching wait."""
+    next item's accumulators are done, the lag EPE exists for.  kv_buffers=2:
+    item it's K, V go to buffer it % 2 (barriers KV, KVE per buffer), loaded
+    once item it - 2 is done with that buffer, so the next item's tiles land
+    while the current item runs.  mistake: "no_kve", "no_epe" drop the
+    matching wait."""
+    KB = kv_buffers
     warps = [(g, q) for g in range(4) for q in range(4)]
     starts = [sum(items[:i]) for i in range(len(items))]
 
     def model(rnd):
-        bars = {"KV": 1, "KVE": 1, "SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1,
+        bars = {"SDF": 1, "LD": 512, "PF": 512, "DSF": 512, "ACC": 1,
                 "STR": 1, "EPF": 512, "EPE": 1, "DONE": 1}
+        for b_ in range(KB):
+            bars[f"KV{b_}"] = 1
+            bars[f"KVE{b_}"] = 1
         for s_ in range(NST):
             bars[f"STF{s_}"] = 1 + 32
             bars[f"STE{s_}"] = 1
@@ -670,9 +677,10 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
         def producer():
             last = {}
             for it, n in enumerate(items):
-                if it > 0 and mistake != "no_kve":
-                    yield ("wait", "KVE", it - 1)
-                yield ("load", "KV", it, {"K": f"K({it})", "V": f"V({it})"})
+                b = it % KB
+                if it >= KB and mistake != "no_kve":
+                    yield ("wait", f"KVE{b}", (it - KB) // KB)
+                yield ("load", f"KV{b}", it // KB, {f"K{b}": f"K({it})", f"V{b}": f"V({it})"})
                 for j in range(n):
                     g = starts[it] + j
                     sl = g % NST
@@ -683,17 +691,19 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
                     yield ("write", {f"vec{sl}": f"lse,D({g})"})
                     yield ("arrive", f"STF{sl}", 32, g // NST)
                     last[sl] = g // NST
-            if items:
-                yield ("wait", "KV", len(items) - 1)
+            for b in range(KB):
+                used = [i for i in range(len(items)) if i % KB == b]
+                if used:
+                    yield ("wait", f"KV{b}", used[-1] // KB)
             for sl, ph in last.items():
                 yield ("wait", f"STF{sl}", ph)
 
         def st_mma(it, g):
-            return ("mma", f"S^T({g})", {"K": f"K({it})", f"Q{g % NST}": f"Q({g})"},
+            return ("mma", f"S^T({g})", {f"K{it % KB}": f"K({it})", f"Q{g % NST}": f"Q({g})"},
                     region(reg_s(g), f"S^T({g})"))
 
         def dpt_mma(it, g):
-            reads = {"V": f"V({it})"}
+            reads = {f"V{it % KB}": f"V({it})"}
             reads.update({f"dO{g % NST}.{w}.{q}": f"dO({g})" for w, q in warps})
             return ("mma", f"dP^T({g})", reads, region(reg_d(g), f"dP^T({g})"))
 
@@ -714,7 +724,7 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
         def mma():
             for it, n in enumerate(items):
                 g0 = starts[it]
-                yield ("wait", "KV", it)
+                yield ("wait", f"KV{it % KB}", it // KB)
                 yield ("wait", f"STF{g0 % NST}", g0 // NST)
                 if it > 0 and mistake != "no_ld_cross":
                     yield ("wait", "LD", g0 - 1)  # S^T(g0) goes over dP^T(g0 - 1)
@@ -723,7 +733,7 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
                 yield dpt_mma(it, g0)
                 yield ("commit", "SDF", g0)
                 if n == 1:
-                    yield ("commit", "KVE", it)
+                    yield ("commit", f"KVE{it % KB}", it // KB)
                 for j in range(n):
                     g = g0 + j
                     more = j + 1 < n
@@ -741,7 +751,7 @@ def dkdv_persistent_model(items, NST=3, mistake=None, lagging_store=False):
                         yield dpt_mma(it, g + 1)
                         yield ("commit", "SDF", g + 1)
                         if j + 2 == n:
-                            yield ("commit", "KVE", it)  # the item's last S^T and dP^T
+                            yield ("commit", f"KVE{it % KB}", it // KB)  # the item's last S^T, dP^T
                 yield ("commit", "ACC", it)
             yield ("commit", "DONE", 0)
             yield ("wait", "DONE", 0)
@@ -1598,15 +1608,20 @@ DKDV_PERSISTENT_ITEMS = [[1], [2], [3], [16, 16], [1, 1, 1], [2, 3, 1, 4], [5, 1
 
 @pytest.mark.parametrize("items", range(len(DKDV_PERSISTENT_ITEMS)))
 @pytest.mark.parametrize("lagging_store", [False, True])
-def test_dkdv_persistent_protocol(items, lagging_store):
-    each_seed(dkdv_persistent_model(DKDV_PERSISTENT_ITEMS[items], lagging_store=lagging_store),
+@pytest.mark.parametrize("kvb", [1, 2])
+def test_dkdv_persistent_protocol(items, lagging_store, kvb):
+    each_seed(dkdv_persistent_model(DKDV_PERSISTENT_ITEMS[items], lagging_store=lagging_store,
+                                    kv_buffers=kvb),
               seeds=range(40))
 
 
-@pytest.mark.parametrize("mistake,items,lag", [("no_kve", [3, 2, 4], False),
-                                               ("no_epe", [2, 1, 3], True)])
-def test_dkdv_persistent_planted_mistakes_are_caught(mistake, items, lag):
-    assert fails_on_some_seed(dkdv_persistent_model(items, mistake=mistake, lagging_store=lag),
+@pytest.mark.parametrize("mistake,items,lag,kvb", [("no_kve", [3, 2, 4], False, 1),
+                                                   ("no_kve", [1, 1, 2, 1, 3], False, 2),
+                                                   ("no_epe", [2, 1, 3], True, 1),
+                                                   ("no_epe", [2, 1, 3], True, 2)])
+def test_dkdv_persistent_planted_mistakes_are_caught(mistake, items, lag, kvb):
+    assert fails_on_some_seed(dkdv_persistent_model(items, mistake=mistake, lagging_store=lag,
+                                                    kv_buffers=kvb),
                               seeds=range(200))
 
 
