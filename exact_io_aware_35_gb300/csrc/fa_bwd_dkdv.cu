@@ -1,12 +1,15 @@
 // fa_bwd_dkdv.cu -- dK and dV for exact attention, sm_103a.
 //
-// One CTA per (batch, kv head, 128-key block).  K and V stay in shared
-// memory; Q_i and dO_i of every query head of the GQA group and every query
-// block that sees the key block stream through a 2-stage TMA ring, with
-// lse * log2(e) and D for the block's queries staged by the TMA warp.  For
+// One work item per (batch, kv head, 128-key block): one CTA each at d = 128,
+// persistent CTAs walking several at d = 64.  An item's K and V stay in shared
+// memory (at d = 64 in one of two buffers, so that the next item's land while
+// the current one runs); Q_i and dO_i of every query head of the GQA group and
+// every query block that sees the key block stream through a TMA ring (2
+// stages, 3 at d = 64), with lse * log2(e) and D for the block's queries
+// staged by the TMA warp, which reads them a step ahead.  For
 // each, S^T = K Q_i^T and dP^T = V dO_i^T are recomputed into TMEM (keys on
 // the TMEM lanes), turned into P^T = exp2(S^T * scale * log2(e) - lse2) and
-// dS^T = P^T o (dP^T - D) in place (bf16), and dV += P^T dO_i,
+// dS^T = P^T o (dP^T - D) in place (16-bit pairs), and dV += P^T dO_i,
 // dK += dS^T Q_i take P^T / dS^T straight from TMEM as the A operand -- so no
 // transpose is ever materialised.  The group's query heads are summed inside
 // the CTA: no atomics.
@@ -41,7 +44,6 @@ __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
-
 
 using namespace bwd;
 
