@@ -1093,7 +1093,7 @@ def stream_entries(sets):
 
 
 def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=False,
-                         mistake=None, timeouts=False, drop=None, stage_q=False):
+                         mistake=None, timeouts=False, drop=None, stage_q=False, epi_tma=False):
     """The persistent forward: one CTA walks `items`, each a pair (tile 0's key
     blocks, tile 1's key blocks).  Dense items (sparse=False) share K and V
     between the tiles, ring entries K(u), V(u) per block of tile 1's range;
@@ -1127,11 +1127,19 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
     o_final(t) has completed; a tile with no block waits for the Q load
     instead.
 
+    epi_tma (a form of the dense kernel at d = 64 that was measured and not
+    kept): each tile's epilogue writes its O rows into a staging buffer of
+    the tile's own once the copy warp's stores of the previous item have read
+    it (epi_empty(t)), and arrives on epi(t) (128 threads); the copy warp,
+    after its Q copy, waits for epi(t), stores the buffer (a read of the four
+    warps' rows) and arrives on epi_empty(t).
+
     mistake: "no_q_empty" (Q reloaded without q_empty), "early_arrive" (tile
     0's issuer arrives on kv_empty without the previous-phase wait),
     "no_k_wait" (a score product before its K tile has landed), "no_pvd_wait"
     (P_t written before the previous P V product has read it), "no_of_wait"
-    (the epilogue reads O without o_final), "no_drain" (the producer exits
+    (the epilogue reads O without o_final), "no_epe" (epi_tma: the staging
+    rewritten without epi_empty), "no_drain" (the producer exits
     without waiting for its last loads), "mma_waits_first_k" (the issuer waits
     the item's first K entries itself and the gate starts at V(0): the gate's
     parity wait on a slot can then come a phase early or two late),
@@ -1144,7 +1152,7 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
     items = [(sorted(set(a)), sorted(set(b))) for a, b in items]
     assert not stage_q or (sparse and len(items) == 1)
     nissue = 2 if split_p else 1
-    n_roles = 1 + nissue + (0 if split_p else 1) + 8 + (1 if copy_q else 0)
+    n_roles = 1 + nissue + (0 if split_p else 1) + 8 + (1 if (copy_q or epi_tma) else 0)
 
     def entries(it):
         """the item's ring entries in order: (owner, kind, k) with owner a
@@ -1170,7 +1178,8 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
         bars = {"Q": 1, "QE": nissue + (1 if copy_q else 0), "DONE": nissue, "G1": 1}
         for t in (0, 1):
             bars.update({f"SF{t}": 1, f"PF{t}": 128 if split_p else 129, f"OF{t}": 1,
-                         f"SE{t}": 4, f"PVD{t}": 1, f"EPI{t}": 4})
+                         f"SE{t}": 4, f"PVD{t}": 1, f"EPI{t}": 128 if epi_tma else 4,
+                         f"EPE{t}": 1})
         for s in range(NSLOT):
             bars[f"F{s}"] = 1
             bars[f"E{s}"] = 2 if (split_p and not sparse) else 1
@@ -1391,12 +1400,23 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
             yield from teardown()
 
         def copy():
+            ok = True
             for i in range(len(items)):
-                ok = (yield W("Q", i)) is not False
-                if not ok:
-                    break
-                yield ("read", dict(tile("Q", 0, f"Q{i}"), **tile("Q", 1, f"Q{i}")))
-                yield ("arrive", "QE", 1, i)
+                if copy_q:
+                    ok = (yield W("Q", i)) is not False
+                    if not ok:
+                        break
+                    yield ("read", dict(tile("Q", 0, f"Q{i}"), **tile("Q", 1, f"Q{i}")))
+                    yield ("arrive", "QE", 1, i)
+                if epi_tma:
+                    for t in (0, 1):
+                        ok = (yield W(f"EPI{t}", i)) is not False
+                        if not ok:
+                            break
+                        yield ("read", {f"ST.{t}.{qq}": f"Ostage{t}({i})" for qq in rows})
+                        yield ("arrive", f"EPE{t}", 1, i)
+                    if not ok:
+                        break
             yield from teardown()
 
         def softmax(t, q):
@@ -1439,6 +1459,13 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
                     ok = (yield W("Q", i)) is not False
                     if not ok:
                         break
+                if epi_tma:
+                    if i > 0 and mistake != "no_epe":
+                        ok = (yield W(f"EPE{t}", i - 1)) is not False
+                        if not ok:
+                            break
+                    yield ("write", {f"ST.{me}": f"Ostage{t}({i})"})
+                    yield ("arrive", f"EPI{t}", 32, i)
                 if stage_q:
                     yield ("write", {f"Q.{me}": f"Ostage{t}"})
                     yield ("arrive", f"EPI{t}", 1, 0)
@@ -1457,7 +1484,7 @@ def fwd_persistent_model(items, NSLOT=4, split_p=False, sparse=False, copy_q=Fal
         for t in (0, 1):
             for q in rows:
                 roles[f"s{t}{q}"] = softmax(t, q)
-        if copy_q:
+        if copy_q or epi_tma:
             roles["copy"] = copy()
         return bars, roles
 
@@ -1702,6 +1729,23 @@ PERSISTENT_SPARSE = [
 def test_forward_persistent_dense_protocol(items, split_p, nslot, copy_q):
     each_seed(fwd_persistent_model(PERSISTENT_DENSE[items], nslot, split_p=split_p, copy_q=copy_q),
               seeds=range(40))
+
+
+@pytest.mark.parametrize("items", range(len(PERSISTENT_DENSE)))
+@pytest.mark.parametrize("copy_q", [False, True])
+def test_forward_persistent_dense_staged_epilogue_protocol(items, copy_q):
+    # d = 64 dense with O staged per tile for the copy warp's TMA stores (a
+    # measured form, not kept)
+    each_seed(fwd_persistent_model(PERSISTENT_DENSE[items], 8, split_p=True, copy_q=copy_q,
+                                   epi_tma=True), seeds=range(40))
+
+
+@pytest.mark.parametrize("copy_q", [False, True])
+def test_forward_staging_rewritten_before_its_store_is_caught(copy_q):
+    items = [([0], [0])] * 4  # short items, so a slow copy warp lags a whole item
+    assert fails_on_some_seed(fwd_persistent_model(items, 8, split_p=True, copy_q=copy_q,
+                                                   epi_tma=True, mistake="no_epe"),
+                              seeds=range(300))
 
 
 @pytest.mark.parametrize("items", range(len(PERSISTENT_SPARSE)))
@@ -2101,36 +2145,38 @@ def fwd_timeout_model(nkv0, nkv, NSLOT=4, copy_q=True, drop=None):
     return model
 
 
-PERSISTENT_TIMEOUT_CASES = [  # (items, ring slots, split_p, sparse, copy_q, stage_q)
-    (PERSISTENT_DENSE[0], 4, False, False, True, False),
-    (PERSISTENT_DENSE[0], 8, True, False, True, False),
-    (PERSISTENT_DENSE[2], 4, False, False, False, False),
-    (PERSISTENT_SPARSE[0], 5, False, True, False, False),
-    (PERSISTENT_SPARSE[1], 8, True, True, False, False),
-    ([([0, 2, 3], [1, 2])], 5, False, True, False, True),
-    ([([], [0, 3])], 8, True, True, False, True),
+PERSISTENT_TIMEOUT_CASES = [  # (items, ring slots, split_p, sparse, copy_q, stage_q, epi_tma)
+    (PERSISTENT_DENSE[0], 4, False, False, True, False, False),
+    (PERSISTENT_DENSE[0], 8, True, False, True, False, True),
+    (PERSISTENT_DENSE[1], 8, True, False, False, False, True),
+    (PERSISTENT_DENSE[2], 4, False, False, False, False, False),
+    (PERSISTENT_SPARSE[0], 5, False, True, False, False, False),
+    (PERSISTENT_SPARSE[1], 8, True, True, False, False, False),
+    ([([0, 2, 3], [1, 2])], 5, False, True, False, True, False),
+    ([([], [0, 3])], 8, True, True, False, True, False),
 ]
 
 
 @pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
 def test_persistent_forward_without_faults_never_times_out(case):
-    items, nslot, split_p, sparse, copy_q, stage_q = PERSISTENT_TIMEOUT_CASES[case]
+    items, nslot, split_p, sparse, copy_q, stage_q, epi_tma = PERSISTENT_TIMEOUT_CASES[case]
     for seed in range(20):
         assert not simulate_with_timeouts(
             fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True,
-                                 stage_q=stage_q), seed, limit=10 ** 6)
+                                 stage_q=stage_q, epi_tma=epi_tma), seed, limit=10 ** 6)
 
 
 @pytest.mark.parametrize("case", range(len(PERSISTENT_TIMEOUT_CASES)))
 def test_persistent_forward_any_wait_running_out_ends_the_block_cleanly(case):
     # waits run out at random; whichever do, every role reaches the teardown
     # and nothing is left in flight
-    items, nslot, split_p, sparse, copy_q, stage_q = PERSISTENT_TIMEOUT_CASES[case]
+    items, nslot, split_p, sparse, copy_q, stage_q, epi_tma = PERSISTENT_TIMEOUT_CASES[case]
     n_failed = 0
     for seed in range(80):
         n_failed += simulate_with_timeouts(
             fwd_persistent_model(items, nslot, split_p, sparse, copy_q, timeouts=True,
-                                 stage_q=stage_q), seed, p_spurious=0.01, limit=300)
+                                 stage_q=stage_q, epi_tma=epi_tma), seed, p_spurious=0.01,
+            limit=300)
     assert n_failed > 40  # the fault path ran in most schedules
 
 
