@@ -479,13 +479,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
             const int nkv_mine = t ? I.nkv : I.nkv0;
             float m_ref = -INFINITY, l = 0.f;
+            // key block j's scale, read a block ahead so that its load has a
+            // whole block to land before the maximum needs it
+            float sk_next = nkv_mine > 0 ? skrow[0] : 0.f;
             for (int j = 0; j < nkv_mine; ++j) {
+                const float sk_j = sk_next;
+                if (j + 1 < nkv_mine) sk_next = skrow[j + 1];
                 if (!(ok = mbar_wait_warp(BAR_SF(t), nsf & 1, a.watch, 56))) break;
                 ++nsf;
                 tc_fence_after();
                 // x = S * sl2 in log2 units; the maximum is taken on S itself (sl2 > 0)
                 // and every exponent is one FMA, two columns per packed f32x2 op
-                const float sl2 = a.scale_log2 * sq * skrow[j];
+                const float sl2 = a.scale_log2 * sq * sk_j;
                 uint32_t s[128];
                 tmem_ld32(tS + 0, s);
                 tmem_ld32(tS + 32, s + 32);
