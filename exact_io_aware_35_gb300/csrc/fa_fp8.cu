@@ -476,6 +476,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const float sq =
                 qt < a.nb ? a.sq[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.nb + qt] : 0.f;
             const float* skrow = a.sk + (static_cast<size_t>(I.b) * a.Hkv + I.hk) * a.nb;
+            // V's scale, read now and first used by the epilogue
+            const float sv = a.sv[static_cast<size_t>(I.b) * a.Hkv + I.hk];
             const int lim = a.causal ? min(grow, a.N - 1) : a.N - 1;
             const int nkv_mine = t ? I.nkv : I.nkv0;
             float m_ref = -INFINITY, l = 0.f;
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (!(ok = mbar_wait_warp(BAR_OF(t), nof & 1, a.watch, 57))) break;
             ++nof;
             tc_fence_after();
-            const float f = (l > 0.f) ? a.sv[static_cast<size_t>(I.b) * a.Hkv + I.hk] / l : 0.f;
+            const float f = (l > 0.f) ? sv / l : 0.f;
             const int wrow0 = qt * 128 + wq * 32;  // the warp's first query
 #pragma unroll
             for (int cb = 0; cb < 128; cb += 32) {
