@@ -469,12 +469,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const uint32_t stg = sStage + warp * 2048;
         bool ok = true;
         int nsf = 0, nof = 0;  // phases of s_full and o_final so far
+        // the tile's query-block scale, read one item ahead (and first used
+        // there, in the item's first block)
+        auto q_scale = [&](int w) {
+            const Item J = item(w);
+            const int qt = 2 * J.qb + t;
+            return qt < a.nb ? a.sq[(static_cast<size_t>(J.b) * a.Hq + J.h) * a.nb + qt] : 0.f;
+        };
+        float sq_next = static_cast<int>(blockIdx.x) < n_items ? q_scale(blockIdx.x) : 0.f;
         for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
             const Item I = item(w);
             const int qt = 2 * I.qb + t;  // 128-row query block of the tile
             const int grow = qt * 128 + r;
-            const float sq =
-                qt < a.nb ? a.sq[(static_cast<size_t>(I.b) * a.Hq + I.h) * a.nb + qt] : 0.f;
+            const float sq = sq_next;
+            if (w + static_cast<int>(gridDim.x) < n_items) sq_next = q_scale(w + gridDim.x);
             const float* skrow = a.sk + (static_cast<size_t>(I.b) * a.Hkv + I.hk) * a.nb;
             // V's scale, read now and first used by the epilogue
             const float sv = a.sv[static_cast<size_t>(I.b) * a.Hkv + I.hk];
